@@ -1,0 +1,183 @@
+// Device and host helpers shared by the libdsa kernels (sm_103a).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dsa.h"
+
+namespace dsa {
+
+constexpr int kBlockPositions = 256;  // raw positions per logical block, every cache kind
+constexpr double kTwoPi = 6.283185307179586476925286766559;
+
+// -------------------------------------------------------------------------------------
+// host side
+// -------------------------------------------------------------------------------------
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline int window_of(int kind) { return kind == DSA_C4A ? 8 : 128; }
+inline int stride_of(int kind) { return kind == DSA_C4A ? 4 : 128; }
+
+inline dsa_status_t launch_status() {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+inline int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
+
+inline bool pool_ok(const dsa_pool_t* p) {
+    if (!p || !p->data || p->num_blocks <= 0 || p->rows_per_block <= 0 || p->dim <= 0) return false;
+    if (p->dtype != DSA_BF16 && p->dtype != DSA_FP8_E4M3) return false;
+    if (p->dtype == DSA_FP8_E4M3 && (!p->scale || !aligned(p->scale, 16))) return false;
+    return aligned(p->data, 16);
+}
+
+inline bool table_ok(const dsa_block_table_t* t, int batch) {
+    return t && t->table && t->max_blocks > 0 && t->batch >= batch;
+}
+
+// -------------------------------------------------------------------------------------
+// device side
+// -------------------------------------------------------------------------------------
+// First error wins; later errors leave the recorded code in place.
+__device__ __forceinline__ void report(int32_t* status, int32_t code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+// Number of entries of a kind (window w, stride s) that T raw tokens form.
+__device__ __forceinline__ int entries_formed(long long T, int w, int s) {
+    return T < w ? 0 : (int)((T - w) / s + 1);
+}
+
+// Physical row of logical row `i` (rows_per_block `epb`) of request `r`, or -1 if the
+// block is unmapped, outside the pool or beyond the table.
+__device__ __forceinline__ long long physical_row(const dsa_block_table_t& bt, int r, long long i, int epb,
+                                                  int num_blocks) {
+    long long lb = i / epb;
+    if (i < 0 || lb >= bt.max_blocks) return -1;
+    int pb = __ldg(bt.table + (long long)r * bt.max_blocks + lb);
+    if (pb < 0 || pb >= num_blocks) return -1;
+    return (long long)pb * epb + (i - lb * epb);
+}
+
+// cos / sin of pos * theta^(-2j / rope_dim): the angle is formed and reduced modulo 2 pi in
+// double precision (positions reach 2^20, where a float angle has lost its fraction), then
+// evaluated in float.
+__device__ __forceinline__ void rope_cos_sin(long long pos, int j, int rope_dim, double theta, float* c, float* s) {
+    double f = pow(theta, -2.0 * (double)j / (double)rope_dim);
+    double a = (double)pos * f;
+    a -= kTwoPi * rint(a / kTwoPi);
+    sincosf((float)a, s, c);
+}
+
+__device__ __forceinline__ float bf16_to_float(uint16_t b) {
+    return __uint_as_float(((uint32_t)b) << 16);
+}
+
+__device__ __forceinline__ uint16_t float_to_bf16(float f) {
+    __nv_bfloat16 h = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// e4m3 encode (round to nearest even, saturate to +-448) and decode via CUDA's conversions.
+__device__ __forceinline__ uint8_t float_to_e4m3(float f) {
+    return (uint8_t)__nv_cvt_float_to_fp8(f, __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ float e4m3_to_float(uint8_t c) {
+    __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)c, __NV_E4M3);
+    return __half2float(*reinterpret_cast<__half*>(&h));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// ---- shared-memory addresses, mbarriers and bulk copies (PTX) ----------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: gives up after `limit_ns` nanoseconds of %globaltimer and returns false.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > limit_ns) return false;
+    }
+}
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate copy or MMA
+
+// 1-D bulk copy global -> shared (TMA engine), completing on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 2-D tiled tensor copy global -> shared with the tensor map's swizzle.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+}  // namespace dsa

@@ -1,0 +1,320 @@
+// dsa_compress: c4a / c128a compressor + RMSNorm + RoPE + paged insert, SWA insert and the
+// rolling residual, in one streaming pass.
+//
+// [P1] "DeepSeek DSA、DeepSeek V4与vLLM Hybrid KV Cache详解" §5.2 and [P2] "DeepSeek V4
+// 稀疏注意力完全解剖" 机制二: a compressed token is a weighted sum of w raw tokens taken at
+// stride s (c4a: 8 / 4, c128a: 128 / 128).  [P2] 融合点 1: the sum, RMSNorm, RoPE and the
+// cache insert are one kernel that reads each raw token once and writes each entry once.
+// [P2] 设计 2: the last w raw tokens are kept as a per-request rolling residual.
+//
+// Work split: one warp per emitted entry or per new token; a warp owns a whole row, each lane
+// DIM/32 consecutive elements, so every row load and store is one coalesced transaction set.
+// Raw tokens of an entry that are shared with its neighbour (c4a overlap) are re-read from L2.
+#include "common.cuh"
+
+namespace dsa {
+
+struct CompressArgs {
+    int w, s, batch, dim;
+    const int32_t* cu_new;
+    const int32_t* start_pos;
+    const uint16_t* x_new;
+    const float* logit_new;
+    uint16_t* state_x;
+    float* state_logit;
+    const int32_t* state_slot;
+    int num_slots;
+    const float* gamma;
+    float eps;
+    int rope_dim;
+    double theta;
+    dsa_pool_t out;
+    dsa_block_table_t out_bt;
+    dsa_pool_t swa;
+    dsa_block_table_t swa_bt;
+    int has_swa;
+    int entry_items;  // warps per request reserved for entries
+    int token_items;  // warps per request reserved for new tokens
+    int fuse_ring;    // token warps also update the rolling state (at most one new token per request)
+    int32_t* status;
+};
+
+template <int E>
+__device__ __forceinline__ void load_bf16(const uint16_t* row, int lane, float (&v)[E]) {
+    const uint16_t* p = row + lane * E;
+    if constexpr (E == 16) {
+        uint4 a = *reinterpret_cast<const uint4*>(p);
+        uint4 b = *reinterpret_cast<const uint4*>(p + 8);
+        uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            v[2 * k] = __uint_as_float(u[k] << 16);
+            v[2 * k + 1] = __uint_as_float(u[k] & 0xffff0000u);
+        }
+    } else if constexpr (E == 4) {
+        uint2 a = *reinterpret_cast<const uint2*>(p);
+        v[0] = __uint_as_float(a.x << 16);
+        v[1] = __uint_as_float(a.x & 0xffff0000u);
+        v[2] = __uint_as_float(a.y << 16);
+        v[3] = __uint_as_float(a.y & 0xffff0000u);
+    } else {
+        static_assert(E == 2, "row width");
+        uint32_t a = *reinterpret_cast<const uint32_t*>(p);
+        v[0] = __uint_as_float(a << 16);
+        v[1] = __uint_as_float(a & 0xffff0000u);
+    }
+}
+
+template <int E>
+__device__ __forceinline__ void copy_bf16(uint16_t* dst, const uint16_t* src, int lane) {
+    if constexpr (E == 16) {
+        reinterpret_cast<uint4*>(dst + lane * E)[0] = reinterpret_cast<const uint4*>(src + lane * E)[0];
+        reinterpret_cast<uint4*>(dst + lane * E)[1] = reinterpret_cast<const uint4*>(src + lane * E)[1];
+    } else if constexpr (E == 4) {
+        *reinterpret_cast<uint2*>(dst + lane * E) = *reinterpret_cast<const uint2*>(src + lane * E);
+    } else {
+        *reinterpret_cast<uint32_t*>(dst + lane * E) = *reinterpret_cast<const uint32_t*>(src + lane * E);
+    }
+}
+
+// Store one row (the warp's E values per lane) into a pool row: bf16, or e4m3 + amax/448 scale.
+template <int E>
+__device__ __forceinline__ void store_row(const dsa_pool_t& pool, long long prow, int lane, const float (&v)[E]) {
+    if (pool.dtype == DSA_BF16) {
+        uint16_t* dst = reinterpret_cast<uint16_t*>(pool.data) + prow * (E * 32) + lane * E;
+        uint32_t u[E / 2];
+#pragma unroll
+        for (int k = 0; k < E / 2; ++k)
+            u[k] = (uint32_t)float_to_bf16(v[2 * k]) | ((uint32_t)float_to_bf16(v[2 * k + 1]) << 16);
+        if constexpr (E == 16) {
+            reinterpret_cast<uint4*>(dst)[0] = make_uint4(u[0], u[1], u[2], u[3]);
+            reinterpret_cast<uint4*>(dst)[1] = make_uint4(u[4], u[5], u[6], u[7]);
+        } else if constexpr (E == 4) {
+            *reinterpret_cast<uint2*>(dst) = make_uint2(u[0], u[1]);
+        } else {
+            *reinterpret_cast<uint32_t*>(dst) = u[0];
+        }
+    } else {
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < E; ++k) amax = fmaxf(amax, fabsf(v[k]));
+        amax = warp_max(amax);
+        const float scale = amax > 0.f ? amax / 448.f : 1.f;
+        uint8_t* dst = reinterpret_cast<uint8_t*>(pool.data) + prow * (E * 32) + lane * E;
+        uint8_t c[E];
+#pragma unroll
+        for (int k = 0; k < E; ++k) c[k] = float_to_e4m3(v[k] / scale);
+        if constexpr (E == 16) {
+            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(c);
+        } else if constexpr (E == 4) {
+            *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(c);
+        } else {
+            *reinterpret_cast<uint16_t*>(dst) = *reinterpret_cast<const uint16_t*>(c);
+        }
+        if (lane == 0) pool.scale[prow] = scale;
+    }
+}
+
+// Rotate the lane's pairs that fall in the last rope_dim dims by R_pos.
+template <int E>
+__device__ __forceinline__ void rope_row(float (&v)[E], int lane, int dim, int rope_dim, double theta, long long pos) {
+    const int first = dim - rope_dim;
+#pragma unroll
+    for (int k = 0; k < E; k += 2) {
+        const int d = lane * E + k;
+        if (d >= first) {
+            float c, s;
+            rope_cos_sin(pos, (d - first) >> 1, rope_dim, theta, &c, &s);
+            const float x0 = v[k], x1 = v[k + 1];
+            v[k] = x0 * c - x1 * s;
+            v[k + 1] = x0 * s + x1 * c;
+        }
+    }
+}
+
+template <int DIM>
+__global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
+    constexpr int E = DIM / 32;
+    const int lane = threadIdx.x & 31;
+    const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int r = blockIdx.y;
+    const int cu0 = a.cu_new[r];
+    const int n = a.cu_new[r + 1] - cu0;
+    const long long start = a.start_pos[r];
+    const long long end = start + n;
+    const int slot = a.state_slot[r];
+    if (n < 0 || start < 0 || slot < 0 || slot >= a.num_slots) {
+        if (item == 0 && lane == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
+        return;
+    }
+    const int w = a.w, s = a.s;
+
+    if (item < a.entry_items) {
+        // entries whose last raw token s*i + w - 1 lies in [start, end)
+        const long long lo_num = start - w + 1;
+        const long long i_lo = lo_num <= 0 ? 0 : (lo_num + s - 1) / s;
+        const long long i_hi = end >= w ? (end - w) / s : -1;
+        const long long i = i_lo + item;
+        if (i > i_hi) return;
+        const long long base = (long long)s * i;
+        auto logit_at = [&](long long p) -> float {
+            return p < start ? a.state_logit[(long long)slot * w + (p % w)] : a.logit_new[cu0 + (p - start)];
+        };
+        auto row_at = [&](long long p) -> const uint16_t* {
+            return p < start ? a.state_x + ((long long)slot * w + (p % w)) * DIM
+                             : a.x_new + (long long)(cu0 + (p - start)) * DIM;
+        };
+        // gate g_j = softmax_j(z_{s i + j})
+        float mx = -INFINITY;
+        for (int j = lane; j < w; j += 32) mx = fmaxf(mx, logit_at(base + j));
+        mx = warp_max(mx);
+        float den = 0.f;
+        for (int j = lane; j < w; j += 32) den += expf(logit_at(base + j) - mx);
+        den = warp_sum(den);
+        const float inv_den = 1.f / den;
+        float acc[E];
+#pragma unroll
+        for (int k = 0; k < E; ++k) acc[k] = 0.f;
+        for (int j = 0; j < w; ++j) {
+            const long long p = base + j;
+            const float g = expf(logit_at(p) - mx) * inv_den;
+            float x[E];
+            load_bf16<E>(row_at(p), lane, x);
+#pragma unroll
+            for (int k = 0; k < E; ++k) acc[k] = fmaf(g, x[k], acc[k]);
+        }
+        // RMSNorm
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < E; ++k) ss = fmaf(acc[k], acc[k], ss);
+        ss = warp_sum(ss);
+        const float rs = rsqrtf(ss / (float)DIM + a.eps);
+#pragma unroll
+        for (int k = 0; k < E; ++k) acc[k] *= rs * (a.gamma ? a.gamma[lane * E + k] : 1.f);
+        // RoPE at the last covered position
+        rope_row<E>(acc, lane, DIM, a.rope_dim, a.theta, base + w - 1);
+        const long long prow = physical_row(a.out_bt, r, i, a.out.rows_per_block, a.out.num_blocks);
+        if (prow < 0) {
+            if (lane == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
+            return;
+        }
+        store_row<E>(a.out, prow, lane, acc);
+        return;
+    }
+
+    const int j = item - a.entry_items;
+    if (j >= n || j >= a.token_items) return;
+    const long long p = start + j;
+    const uint16_t* xrow = a.x_new + (long long)(cu0 + j) * DIM;
+    if (a.has_swa) {
+        float v[E];
+        load_bf16<E>(xrow, lane, v);
+        rope_row<E>(v, lane, DIM, a.rope_dim, a.theta, p);
+        const long long prow = physical_row(a.swa_bt, r, p, kBlockPositions, a.swa.num_blocks);
+        if (prow < 0) {
+            if (lane == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
+        } else {
+            store_row<E>(a.swa, prow, lane, v);
+        }
+    }
+    if (a.fuse_ring && j >= n - w) {
+        const long long ring = (long long)slot * w + (p % w);
+        copy_bf16<E>(a.state_x + ring * DIM, xrow, lane);
+        if (lane == 0) a.state_logit[ring] = a.logit_new[cu0 + j];
+    }
+}
+
+// Rolling-state update after a multi-token append: slot p % w <- token p for the last w new tokens.
+template <int DIM>
+__global__ void __launch_bounds__(256) ring_update_kernel(CompressArgs a) {
+    constexpr int E = DIM / 32;
+    const int lane = threadIdx.x & 31;
+    const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int r = blockIdx.y;
+    const int cu0 = a.cu_new[r];
+    const int n = a.cu_new[r + 1] - cu0;
+    const int slot = a.state_slot[r];
+    if (item >= a.w || n <= 0 || slot < 0 || slot >= a.num_slots) return;
+    const int j = n - a.w + item;  // new-token index
+    if (j < 0) return;
+    const long long p = (long long)a.start_pos[r] + j;
+    const long long ring = (long long)slot * a.w + (p % a.w);
+    copy_bf16<E>(a.state_x + ring * DIM, a.x_new + (long long)(cu0 + j) * DIM, lane);
+    if (lane == 0) a.state_logit[ring] = a.logit_new[cu0 + j];
+}
+
+template <int DIM>
+static dsa_status_t launch_compress(const CompressArgs& a, int max_new, cudaStream_t st) {
+    const int items = a.entry_items + a.token_items;
+    dim3 grid((items + 7) / 8, a.batch);
+    compress_kernel<DIM><<<grid, 256, 0, st>>>(a);
+    if (!a.fuse_ring && max_new > 0) {
+        dim3 g2((a.w + 7) / 8, a.batch);
+        ring_update_kernel<DIM><<<g2, 256, 0, st>>>(a);
+    }
+    return launch_status();
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" dsa_status_t dsa_compress(int32_t kind, int32_t batch, const int32_t* cu_new, const int32_t* start_pos,
+                                     int32_t max_new, const void* x_new, const float* logit_new, void* state_x,
+                                     float* state_logit, const int32_t* state_slot, int32_t num_slots,
+                                     const float* rms_gamma, float rms_eps, const dsa_rope_t* rope,
+                                     const dsa_pool_t* out, const dsa_block_table_t* out_bt, const dsa_pool_t* swa,
+                                     const dsa_block_table_t* swa_bt, int32_t* dev_status, void* stream) {
+    if (kind != DSA_C4A && kind != DSA_C128A) return DSA_ERR_INVALID_ARG;
+    if (batch < 0 || max_new < 0 || num_slots <= 0 || !(rms_eps > 0.f)) return DSA_ERR_INVALID_ARG;
+    if (batch == 0 || max_new == 0) return DSA_OK;
+    if (!cu_new || !start_pos || !x_new || !logit_new || !state_x || !state_logit || !state_slot || !rope)
+        return DSA_ERR_INVALID_ARG;
+    if (!pool_ok(out) || !table_ok(out_bt, batch)) return DSA_ERR_INVALID_ARG;
+    const int w = window_of(kind), s = stride_of(kind);
+    if (out->rows_per_block != kBlockPositions / s) return DSA_ERR_INVALID_ARG;
+    const int dim = out->dim;
+    if (dim != 64 && dim != 128 && dim != 512) return DSA_ERR_UNSUPPORTED;
+    if (rope->rope_dim < 0 || rope->rope_dim > dim || (rope->rope_dim & 1) || !(rope->theta > 0.0))
+        return DSA_ERR_INVALID_ARG;
+    if (swa) {
+        if (!pool_ok(swa) || !table_ok(swa_bt, batch)) return DSA_ERR_INVALID_ARG;
+        if (swa->rows_per_block != kBlockPositions || swa->dim != dim) return DSA_ERR_INVALID_ARG;
+    }
+    if (!aligned(x_new, 16) || !aligned(state_x, 16)) return DSA_ERR_INVALID_ARG;
+
+    CompressArgs a{};
+    a.w = w;
+    a.s = s;
+    a.batch = batch;
+    a.dim = dim;
+    a.cu_new = cu_new;
+    a.start_pos = start_pos;
+    a.x_new = static_cast<const uint16_t*>(x_new);
+    a.logit_new = logit_new;
+    a.state_x = static_cast<uint16_t*>(state_x);
+    a.state_logit = state_logit;
+    a.state_slot = state_slot;
+    a.num_slots = num_slots;
+    a.gamma = rms_gamma;
+    a.eps = rms_eps;
+    a.rope_dim = rope->rope_dim;
+    a.theta = rope->theta;
+    a.out = *out;
+    a.out_bt = *out_bt;
+    a.has_swa = swa != nullptr;
+    if (swa) {
+        a.swa = *swa;
+        a.swa_bt = *swa_bt;
+    }
+    a.entry_items = max_new / s + 1;
+    a.token_items = max_new;
+    a.fuse_ring = max_new <= 1;
+    a.status = dev_status;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (dim) {
+        case 64: return launch_compress<64>(a, max_new, st);
+        case 128: return launch_compress<128>(a, max_new, st);
+        default: return launch_compress<512>(a, max_new, st);
+    }
+}

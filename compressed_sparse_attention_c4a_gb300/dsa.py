@@ -1,0 +1,161 @@
+"""Python binding of libdsa.so (ctypes): argument marshalling only.
+
+Every function has the name of the C entry point it calls and takes torch tensors (device memory)
+plus Python ints/floats; all arithmetic runs in the library's CUDA kernels.  There is no fallback:
+if libdsa.so is not built, importing this module raises.
+"""
+import ctypes
+import os
+
+import torch
+
+_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdsa.so")
+if not os.path.exists(_PATH):
+    raise ImportError(f"{_PATH} is not built; run `python -m compressed_sparse_attention_c4a_gb300.build`")
+_lib = ctypes.CDLL(_PATH)
+
+DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_DEVICE_FAULT, DSA_ERR_TIMEOUT = range(6)
+DSA_BF16, DSA_FP8_E4M3 = 0, 1
+DSA_C4A, DSA_C128A = 0, 1
+KIND = {"c4a": DSA_C4A, "c128a": DSA_C128A}
+
+EXPORTS = ["dsa_status_string", "dsa_compress", "dsa_index_scores", "dsa_topk", "dsa_attn_workspace_size",
+           "dsa_sparse_attn_decode", "dsa_sparse_attn_prefill", "dsa_gather_rows"]
+
+
+class DsaPool(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("num_blocks", ctypes.c_int32),
+                ("rows_per_block", ctypes.c_int32), ("dim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class DsaBlockTable(ctypes.Structure):
+    _fields_ = [("table", ctypes.c_void_p), ("batch", ctypes.c_int32), ("max_blocks", ctypes.c_int32)]
+
+
+class DsaRope(ctypes.Structure):
+    _fields_ = [("rope_dim", ctypes.c_int32), ("theta", ctypes.c_double)]
+
+
+class DsaError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn}: {dsa_status_string(code)} ({code})")
+        self.code = code
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_lib.dsa_status_string.restype = ctypes.c_char_p
+_lib.dsa_status_string.argtypes = [_I]
+_lib.dsa_attn_workspace_size.restype = ctypes.c_size_t
+_lib.dsa_attn_workspace_size.argtypes = [_I, _I, _I]
+for _name, _args in {
+    "dsa_compress": [_I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P],
+    "dsa_index_scores": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P],
+    "dsa_topk": [_I, _P, _I, _P, _I, _P, _P, _P],
+    "dsa_sparse_attn_decode": [_I, _I, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, ctypes.c_float, _P, _P, _P, _P,
+                               ctypes.c_size_t, _P, _P],
+    "dsa_sparse_attn_prefill": [_I, _I, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, ctypes.c_float, _P, _P, _P,
+                                _P, ctypes.c_size_t, _P, _P],
+    "dsa_gather_rows": [_P, _P, _I, _P, _P, _P, _P, _P, _P],
+}.items():
+    getattr(_lib, _name).restype = _I
+    getattr(_lib, _name).argtypes = _args
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn, code):
+    if code != DSA_OK:
+        raise DsaError(fn, code)
+
+
+def dsa_status_string(code):
+    return _lib.dsa_status_string(code).decode()
+
+
+def pool(data, rows_per_block, scale=None):
+    """A DsaPool over a tensor viewed as [num_blocks * rows_per_block, dim] (bf16 or uint8 e4m3)."""
+    dim = data.shape[-1]
+    rows = data.numel() // dim
+    assert rows % rows_per_block == 0
+    dtype = DSA_BF16 if data.dtype == torch.bfloat16 else DSA_FP8_E4M3
+    return DsaPool(data.data_ptr(), None if scale is None else scale.data_ptr(), rows // rows_per_block,
+                   rows_per_block, dim, dtype)
+
+
+def block_table(table):
+    """A DsaBlockTable over an int32 [batch][max_blocks] tensor."""
+    return DsaBlockTable(table.data_ptr(), table.shape[0], table.shape[1])
+
+
+def rope(rope_dim=64, theta=10000.0):
+    return DsaRope(rope_dim, theta)
+
+
+def dsa_compress(kind, cu_new, start_pos, max_new, x_new, logit_new, state_x, state_logit, state_slot,
+                 rope_cfg, out, out_bt, swa=None, swa_bt=None, rms_gamma=None, rms_eps=1e-6, dev_status=None,
+                 stream=None):
+    code = _lib.dsa_compress(KIND.get(kind, kind), start_pos.numel(), _ptr(cu_new), _ptr(start_pos), int(max_new),
+                             _ptr(x_new), _ptr(logit_new), _ptr(state_x), _ptr(state_logit), _ptr(state_slot),
+                             state_x.shape[0], _ptr(rms_gamma), float(rms_eps), ctypes.byref(rope_cfg),
+                             ctypes.byref(out), ctypes.byref(out_bt),
+                             None if swa is None else ctypes.byref(swa),
+                             None if swa_bt is None else ctypes.byref(swa_bt), _ptr(dev_status), _stream(stream))
+    _check("dsa_compress", code)
+
+
+def dsa_index_scores(q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, n_visible=None, dev_status=None,
+                     stream=None):
+    nq, heads, dim = q8.shape
+    code = _lib.dsa_index_scores(nq, heads, dim, _ptr(q8), _ptr(q_scale), _ptr(w), _ptr(q_pos), _ptr(q_req),
+                                 int(q_group), ctypes.byref(keys), ctypes.byref(bt), _ptr(scores), scores.shape[1],
+                                 _ptr(n_visible), _ptr(dev_status), _stream(stream))
+    _check("dsa_index_scores", code)
+
+
+def dsa_topk(scores, n_valid, k, idx_out, dev_status=None, stream=None):
+    code = _lib.dsa_topk(scores.shape[0], _ptr(scores), scores.shape[1], _ptr(n_valid), int(k), _ptr(idx_out),
+                         _ptr(dev_status), _stream(stream))
+    _check("dsa_topk", code)
+
+
+def dsa_attn_workspace_size(nq, heads, max_keys):
+    return int(_lib.dsa_attn_workspace_size(int(nq), int(heads), int(max_keys)))
+
+
+def dsa_sparse_attn_decode(q, q_pos, kind, topk, k, main, main_bt, swa, swa_bt, window, sm_scale, rope_cfg, out,
+                           lse=None, workspace=None, dev_status=None, stream=None):
+    B, H, _ = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    code = _lib.dsa_sparse_attn_decode(B, H, _ptr(q), _ptr(q_pos), KIND.get(kind, kind), _ptr(topk), int(k),
+                                       ctypes.byref(main), ctypes.byref(main_bt), ctypes.byref(swa),
+                                       ctypes.byref(swa_bt), int(window), float(sm_scale), ctypes.byref(rope_cfg),
+                                       _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                                       _stream(stream))
+    _check("dsa_sparse_attn_decode", code)
+
+
+def dsa_sparse_attn_prefill(q, q_pos, q_req, kind, topk, k, main, main_bt, swa, swa_bt, window, sm_scale, rope_cfg,
+                            out, lse=None, workspace=None, dev_status=None, stream=None):
+    nq, H, _ = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    code = _lib.dsa_sparse_attn_prefill(nq, H, _ptr(q), _ptr(q_pos), _ptr(q_req), KIND.get(kind, kind), _ptr(topk),
+                                        int(k), ctypes.byref(main), ctypes.byref(main_bt), ctypes.byref(swa),
+                                        ctypes.byref(swa_bt), int(window), float(sm_scale), ctypes.byref(rope_cfg),
+                                        _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                                        _stream(stream))
+    _check("dsa_sparse_attn_prefill", code)
+
+
+def dsa_gather_rows(pool_, bt, req, ids, out, out_scale=None, dev_status=None, stream=None):
+    code = _lib.dsa_gather_rows(ctypes.byref(pool_), ctypes.byref(bt), ids.numel(), _ptr(req), _ptr(ids), _ptr(out),
+                                _ptr(out_scale), _ptr(dev_status), _stream(stream))
+    _check("dsa_gather_rows", code)

@@ -1,0 +1,99 @@
+"""One layer step over resident device caches: the C-ABI calls in the order the layer runs them.
+
+[P2] "DeepSeek V4 稀疏注意力完全解剖", 全景图 steps C-E: compress -> RMSNorm -> RoPE -> insert and SWA
+insertion; indexer scores -> top-K; main attention over top-K entries plus the window; inverse RoPE.
+This module owns output buffers and calls libdsa; it computes nothing itself.
+"""
+import math
+
+import torch
+
+from . import dsa
+
+SM_SCALE = 1.0 / math.sqrt(512.0)
+ROPE_THETA = 10000.0
+
+
+def _query_group(spec, idx_heads):
+    """Largest power of two <= 256/heads that divides every request's query count (1 for decode)."""
+    if spec.queries != "all":
+        return 1
+    g = max(1, 256 // idx_heads)
+    while g > 1 and any(n % g for n in spec.new):
+        g //= 2
+    return g
+
+
+class LayerStep:
+    """Device-resident state and buffers of one case (a dict from ``synth.make_case`` on cuda)."""
+
+    def __init__(self, case):
+        spec = case["spec"]
+        self.case, self.spec = case, spec
+        dev = case["q"].device
+        self.kind = spec.kind
+        epb = case["epb"]
+        self.main = dsa.pool(case["main_data"], epb, case["main_scale"])
+        self.main_bt = dsa.block_table(case["bt_main"])
+        self.swa = dsa.pool(case["swa_data"], 256, case["swa_scale"])
+        self.swa_bt = dsa.block_table(case["bt_swa"])
+        self.rope_main = dsa.rope(spec.rope_dim, ROPE_THETA)
+        self.has_index = spec.idx_heads > 0
+        nq = case["nq"]
+        if self.has_index:
+            self.idx = dsa.pool(case["idx_data"], 64, case["idx_scale"])
+            self.idx_bt = dsa.block_table(case["bt_idx"])
+            self.rope_idx = dsa.rope(min(spec.rope_dim, spec.idx_dim), ROPE_THETA)
+            self.ld = case["ld"]
+            self.scores = torch.empty((nq, self.ld), dtype=torch.float32, device=dev)
+            self.n_visible = torch.empty((nq,), dtype=torch.int32, device=dev)
+            self.topk = torch.empty((nq, spec.topk), dtype=torch.int32, device=dev)
+            self.q_group = _query_group(spec, spec.idx_heads)
+        self.out = torch.empty((nq, spec.heads, spec.dim), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((nq, spec.heads), dtype=torch.float32, device=dev)
+        max_keys = (spec.topk if self.has_index else case["bt_main"].shape[1] * epb) + spec.window
+        ws = dsa.dsa_attn_workspace_size(nq, spec.heads, max_keys)
+        self.workspace = torch.empty((max(ws, 256),), dtype=torch.uint8, device=dev) if ws else None
+        self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
+        self.max_new = max(spec.new) if spec.new else 0
+
+    # ---- stages ------------------------------------------------------------------------
+    def compress(self):
+        c = self.case
+        dsa.dsa_compress(self.kind, c["cu_new"], c["start_pos"], self.max_new, c["x_new"], c["z_new"], c["state_x"],
+                         c["state_z"], c["state_slot"], self.rope_main, self.main, self.main_bt, self.swa,
+                         self.swa_bt, dev_status=self.status)
+        if self.has_index and self.spec.index_compress:
+            dsa.dsa_compress(self.kind, c["cu_new"], c["start_pos"], self.max_new, c["xi_new"], c["zi_new"],
+                             c["state_xi"], c["state_zi"], c["state_slot"], self.rope_idx, self.idx, self.idx_bt,
+                             dev_status=self.status)
+
+    def index(self):
+        c = self.case
+        dsa.dsa_index_scores(c["q8"], c["q_scale"], c["w"], c["q_pos"], c["q_req"], self.q_group, self.idx,
+                             self.idx_bt, self.scores, self.n_visible, dev_status=self.status)
+
+    def select(self):
+        dsa.dsa_topk(self.scores, self.n_visible, self.spec.topk, self.topk, dev_status=self.status)
+
+    def attend(self, topk=None):
+        c, s = self.case, self.spec
+        tk = (self.topk if topk is None else topk) if self.has_index else None
+        k = s.topk if self.has_index else 0
+        if s.queries == "last":
+            dsa.dsa_sparse_attn_decode(c["q"], c["q_pos"], self.kind, tk, k, self.main, self.main_bt, self.swa,
+                                       self.swa_bt, s.window, SM_SCALE, self.rope_main, self.out, self.lse,
+                                       self.workspace, dev_status=self.status)
+        else:
+            dsa.dsa_sparse_attn_prefill(c["q"], c["q_pos"], c["q_req"], self.kind, tk, k, self.main, self.main_bt,
+                                        self.swa, self.swa_bt, s.window, SM_SCALE, self.rope_main, self.out,
+                                        self.lse, self.workspace, dev_status=self.status)
+
+    def run(self):
+        """The whole step: compress (+SWA insert), index, top-k, attention with inverse RoPE."""
+        self.compress()
+        if self.has_index:
+            self.index()
+            self.select()
+        self.attend()
+        return self.out

@@ -1,0 +1,235 @@
+/*
+ * dsa.h - C ABI of libdsa.so: one DeepSeek-V4-style compressed sparse attention layer
+ * step (c4a / c128a) on a GB300 (sm_103a).
+ *
+ * Sources, cited by page title and section:
+ *   [P1] "DeepSeek DSA、DeepSeek V4与vLLM Hybrid KV Cache详解" (gentlecold.top)
+ *   [P2] "DeepSeek V4 稀疏注意力完全解剖" (zoe.im)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Memory.  Every pointer argument is DEVICE memory owned by the caller unless the
+ *   comment says "host".  The library never allocates or frees memory and keeps no
+ *   mutable global state, so calls are reentrant and can be recorded in a CUDA graph.
+ * Streams.  `stream` is a cudaStream_t (NULL = legacy default stream).  Every call only
+ *   enqueues work on that stream and returns; none synchronises.
+ * Host-side errors.  A call returns DSA_OK or an error code; when the host-side checks
+ *   fail no kernel is launched and no memory is touched.
+ *     DSA_ERR_INVALID_ARG  null / misaligned pointer, inconsistent sizes
+ *     DSA_ERR_UNSUPPORTED  a size outside what the kernels implement (stated per call)
+ *     DSA_ERR_CUDA         the CUDA runtime refused a launch
+ * Device-side errors.  `dev_status` (optional, one int32 in device memory, may be NULL)
+ *   receives the first error that a kernel detects (first writer wins; a zero value is
+ *   never overwritten with zero, so the caller clears it):
+ *     DSA_ERR_DEVICE_FAULT a needed block is unmapped (-1) or outside the pool, a
+ *                          position lies beyond its block table, or an index is out of
+ *                          range; the affected row is written as zeros (scores: -inf)
+ *     DSA_ERR_TIMEOUT      a bounded wait on an asynchronous copy or MMA expired
+ *   Kernels never trap or assert.
+ * Paged caches ([P2] 设计 1; [P1] §2.2, §6.1).  A logical block always covers 256 raw
+ *   token positions: 64 c4a entries, 2 c128a entries or 256 SWA tokens.  Compressed
+ *   entry i (stride s) lives in logical block i / (256/s), row i % (256/s); raw token p
+ *   lives in SWA block p / 256, row p % 256.  A request's block table row maps logical
+ *   blocks to physical blocks of a pool; -1 marks an unmapped block.
+ * RoPE ([P2] 深潜：为什么必须做 Inverse RoPE).  Acts on the last rope_dim dims of a row
+ *   in interleaved pairs (dim - rope_dim + 2j, dim - rope_dim + 2j + 1), angle
+ *   pos * theta^(-2j / rope_dim); the angle is formed in double precision.
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t dsa_status_t;
+#define DSA_OK 0
+#define DSA_ERR_INVALID_ARG 1
+#define DSA_ERR_UNSUPPORTED 2
+#define DSA_ERR_CUDA 3
+#define DSA_ERR_DEVICE_FAULT 4
+#define DSA_ERR_TIMEOUT 5
+
+/* storage formats of a pool row */
+#define DSA_BF16 0
+#define DSA_FP8_E4M3 1 /* e4m3 bytes + one fp32 scale per row: value = scale * e4m3(code) */
+
+/* compressor kinds ([P1] §5.2, [P2] 机制二) */
+#define DSA_C4A 0   /* window 8 raw tokens, stride 4: 64 entries per block */
+#define DSA_C128A 1 /* window 128, stride 128: 2 entries per block */
+
+/* A paged pool.  data: [num_blocks][rows_per_block][dim] elements (bf16 or e4m3 bytes),
+ * row-major and contiguous, 16-byte aligned.  scale: [num_blocks][rows_per_block] fp32,
+ * required for DSA_FP8_E4M3 and ignored for DSA_BF16. */
+typedef struct dsa_pool {
+    void* data;
+    float* scale;
+    int32_t num_blocks;
+    int32_t rows_per_block;
+    int32_t dim;
+    int32_t dtype;
+} dsa_pool_t;
+
+/* Block tables: table[r * max_blocks + b] = physical block of request r's logical block b. */
+typedef struct dsa_block_table {
+    const int32_t* table;
+    int32_t batch;
+    int32_t max_blocks;
+} dsa_block_table_t;
+
+typedef struct dsa_rope {
+    int32_t rope_dim; /* even, <= dim; 64 for the main cache */
+    double theta;     /* 10000 */
+} dsa_rope_t;
+
+/* Human-readable name of a status code (static string; never NULL). */
+const char* dsa_status_string(dsa_status_t status);
+
+/*
+ * dsa_compress - compressor + RMSNorm + RoPE + paged insert, and SWA insert.
+ * [P1] §5.2 / [P2] 机制二 (c4a: weighted sum of 8 raw tokens at stride 4; c128a: 128 at
+ * stride 128), [P2] 融合点 1 (compress -> RMSNorm -> RoPE -> cache insert in one pass),
+ * [P2] 设计 2 (the rolling residual of the last w raw tokens), [P2] 融合点 3 (SWA keys:
+ * RoPE then insert).
+ *
+ * Request r appends raw tokens x_new[cu_new[r] .. cu_new[r+1]) at positions
+ * start_pos[r], start_pos[r] + 1, ...  Every entry i whose last covered token
+ * s*i + w - 1 is among them is formed as
+ *     g = softmax_j(z_{s*i+j}),  u = sum_j g_j x_{s*i+j},
+ *     v = gamma * u / sqrt(mean(u^2) + eps),  entry = R_{s*i+w-1} v
+ * and stored at logical row i of `out` through row r of `out_bt` (bf16, or e4m3 with
+ * scale = amax/448 when out->dtype is DSA_FP8_E4M3).  Window tokens older than
+ * start_pos[r] are read from the rolling state slot state_slot[r]:
+ * state_x[slot][p % w][dim] (bf16) and state_logit[slot][p % w] (fp32).  Afterwards the
+ * state holds the request's last w raw tokens (slot position p % w).  With `swa` non-NULL
+ * each new token p is also stored as R_p x_p at SWA logical row p through swa_bt.
+ *
+ * kind       DSA_C4A or DSA_C128A (w, s) = (8, 4) or (128, 128)
+ * batch      requests (host int, >= 0; 0 is a no-op)
+ * cu_new     [batch + 1] int32, cu_new[0] = 0, non-decreasing
+ * start_pos  [batch] int32 >= 0
+ * max_new    host int: an upper bound of cu_new[r+1] - cu_new[r] over r (grid sizing)
+ * x_new      [cu_new[batch]][dim] bf16;  logit_new [cu_new[batch]] fp32
+ * state_*    rolling state; num_slots host int = number of slots; state_slot [batch]
+ * rms_gamma  [dim] fp32 or NULL (= all ones);  rms_eps > 0
+ * out        bf16 or fp8 pool, rows_per_block = 256/s;  swa: rows_per_block = 256, or NULL
+ * Supported: dim in {64, 128, 512} (multiple of 64), rope_dim even and <= dim.
+ */
+dsa_status_t dsa_compress(int32_t kind, int32_t batch, const int32_t* cu_new, const int32_t* start_pos,
+                          int32_t max_new, const void* x_new, const float* logit_new, void* state_x,
+                          float* state_logit, const int32_t* state_slot, int32_t num_slots,
+                          const float* rms_gamma, float rms_eps, const dsa_rope_t* rope,
+                          const dsa_pool_t* out, const dsa_block_table_t* out_bt, const dsa_pool_t* swa,
+                          const dsa_block_table_t* swa_bt, int32_t* dev_status, void* stream);
+
+/*
+ * dsa_index_scores - lightning-indexer scores of each query against every visible
+ * c4a entry.  [P1] §4.1 (a few heads, FP8), [P2] 机制三.  With e4m3 query codes q8 and
+ * per-(query, head) scale sq, e4m3 key codes k8 with per-entry scale sk:
+ *     I(m, i) = sum_h w_h * max(0, sq_h * sk_i * <q8_h, k8_i>),  i < n_vis(m),
+ * n_vis(m) = number of c4a entries whose last covered token is <= m.
+ * Computed on the tensor cores (tcgen05, fp8 x fp8 -> fp32) from key tiles that TMA
+ * stages in shared memory.
+ *
+ * nq         queries (host);  heads in {4, 8, 16};  dim in {64, 128}
+ * q8         [nq][heads][dim] e4m3 bytes;  q_scale, w: [nq][heads] fp32
+ * q_pos      [nq] int32 position m of each query;  q_req [nq] int32 request of each query
+ * q_group    host int in 1 .. 256/heads: queries g*q_group .. g*q_group + q_group - 1 must
+ *            belong to one request (decode: 1; chunked prefill: up to 256/heads); a group
+ *            that mixes requests raises DSA_ERR_DEVICE_FAULT
+ * keys       fp8 pool, rows_per_block 64, dim = dim; bt: its block table
+ * scores     [nq][ld] fp32 out: I(m, i) for i < n_vis(m); -inf for n_vis(m) <= i < the end of
+ *            the 128-entry tile holding n_vis(m) - 1; the rest of the row is not written
+ * ld         host int, >= n_vis of every query, a multiple of 4
+ * n_visible  [nq] int32 out (n_vis per query), or NULL
+ */
+dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8, const float* q_scale,
+                              const float* w, const int32_t* q_pos, const int32_t* q_req, int32_t q_group,
+                              const dsa_pool_t* keys, const dsa_block_table_t* bt, float* scores, int32_t ld,
+                              int32_t* n_visible, int32_t* dev_status, void* stream);
+
+/*
+ * dsa_topk - per-query top-k of indexer scores.  [P1] §4.2: S_t = TopK(I_{t,:}, k).
+ * Row q selects the k largest of scores[q][0 .. n_valid[q]), ties broken toward the
+ * lower index, so the selected set is unique; idx_out[q] lists it in increasing index
+ * order, padded with -1 when n_valid[q] < k.  Exact (radix select on the fp32 bit
+ * patterns); NaN scores are not supported.
+ *
+ * nq, k      host ints; 1 <= k <= 2048
+ * scores     [nq][ld] fp32;  n_valid [nq] int32 in [0, ld]
+ * idx_out    [nq][k] int32 out
+ */
+dsa_status_t dsa_topk(int32_t nq, const float* scores, int32_t ld, const int32_t* n_valid, int32_t k,
+                      int32_t* idx_out, int32_t* dev_status, void* stream);
+
+/*
+ * Split-K workspace (bytes) that dsa_sparse_attn_decode / _prefill need for nq query
+ * rows of `heads` heads and at most `max_keys` keys per row (compressed + window) on the
+ * current device.  0 means the call needs none.
+ */
+size_t dsa_attn_workspace_size(int32_t nq, int32_t heads, int32_t max_keys);
+
+/*
+ * dsa_sparse_attn_decode - main attention of one decode query per request.
+ * [P1] §4.2-4.3 (attention over the top-k entries, MQA mode: every entry is shared by
+ * all heads), [P2] 机制一 (K = V: one stored row is both key and value), [P2] 机制四 /
+ * [P1] §5.3 (a 128-token sliding window of uncompressed tokens is seen together with the
+ * compressed entries), [P2] 深潜 (inverse RoPE on the output), [P2] 融合点 2 (fused into
+ * the output store).  For query row b at position m = q_pos[b], request b:
+ *     keys = {main row i : i in topk[b], i >= 0}  U  {swa row p : max(0, m-window+1) <= p <= m}
+ *     p_hj = softmax_j(<q_bh, key_j> * sm_scale),  o_bh = sum_j p_hj key_j
+ *     out_bh = o_bh with its last rope_dim dims rotated by R_m^-1.
+ * topk == NULL selects every visible entry i < n_vis(m) (the c128a layer).
+ *
+ * batch      rows (host);  heads in {16, 32, 64, 128}
+ * q          [batch][heads][512] bf16, already rotated at m;  q_pos [batch] int32
+ * kind       DSA_C4A or DSA_C128A (visibility and rows_per_block of `main`)
+ * topk       [batch][k] int32 logical entry ids (-1 = none) or NULL;  k host int <= 2048
+ * main, swa  pools with dim 512, bf16 or fp8 (per-row scale);  window: host int, 1..1024
+ * sm_scale   host float (1/sqrt(512) in the layer)
+ * out        [batch][heads][512] bf16;  lse [batch][heads] fp32 (natural log of the softmax
+ *            denominator) or NULL
+ * workspace  >= dsa_attn_workspace_size(batch, heads, max_keys) bytes, 256-byte aligned, or
+ *            NULL when that size is 0; max_keys = (topk ? k : main_bt->max_blocks *
+ *            main->rows_per_block) + window
+ * Supported: dim 512, rope_dim <= 64.
+ */
+dsa_status_t dsa_sparse_attn_decode(int32_t batch, int32_t heads, const void* q, const int32_t* q_pos,
+                                    int32_t kind, const int32_t* topk, int32_t k, const dsa_pool_t* main,
+                                    const dsa_block_table_t* main_bt, const dsa_pool_t* swa,
+                                    const dsa_block_table_t* swa_bt, int32_t window, float sm_scale,
+                                    const dsa_rope_t* rope, void* out, float* lse, void* workspace,
+                                    size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * dsa_sparse_attn_prefill - the same attention for nq query tokens of a chunk, each with
+ * its own position, request and top-k row (causal: a token sees only entries and window
+ * tokens at or before its position).  Arguments as dsa_sparse_attn_decode, plus
+ * q_req [nq] int32 mapping each query row to its request's table rows.
+ */
+dsa_status_t dsa_sparse_attn_prefill(int32_t nq, int32_t heads, const void* q, const int32_t* q_pos,
+                                     const int32_t* q_req, int32_t kind, const int32_t* topk, int32_t k,
+                                     const dsa_pool_t* main, const dsa_block_table_t* main_bt,
+                                     const dsa_pool_t* swa, const dsa_block_table_t* swa_bt, int32_t window,
+                                     float sm_scale, const dsa_rope_t* rope, void* out, float* lse,
+                                     void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                     void* stream);
+
+/*
+ * dsa_gather_rows - copy the stored bytes of n logical rows, exactly as the attention
+ * reads them, into a dense array (a checking hook for the block-table translation of
+ * [P1] §2.2 / [P2] 设计 1).  Row j is logical row ids[j] of request req[j].
+ * out: [n][dim * element_size] bytes;  out_scale: [n] fp32 (fp8 pools) or NULL.
+ * An unmapped or out-of-range row is written as zeros and raises DSA_ERR_DEVICE_FAULT.
+ */
+dsa_status_t dsa_gather_rows(const dsa_pool_t* pool, const dsa_block_table_t* bt, int32_t n, const int32_t* req,
+                             const int32_t* ids, void* out, float* out_scale, int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H */

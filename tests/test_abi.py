@@ -1,0 +1,68 @@
+"""The C-ABI library builds, loads and exports every entry point that include/dsa.h declares;
+host-side validation rejects bad arguments before anything reaches the GPU (no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from compressed_sparse_attention_c4a_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_binding_exposes_the_same_names(lib):
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    for n in _declared():
+        assert callable(getattr(dsa, n)), n
+
+
+def test_status_strings(lib):
+    lib.dsa_status_string.restype = ctypes.c_char_p
+    assert lib.dsa_status_string(0) == b"ok"
+    assert b"device" in lib.dsa_status_string(4)
+    assert lib.dsa_status_string(99) == b"unknown status"
+
+
+def test_host_validation_rejects_before_launch(lib):
+    P = ctypes.c_void_p
+    # top-k: k outside 1..2048, ld not a multiple of 4
+    lib.dsa_topk.argtypes = [ctypes.c_int32, P, ctypes.c_int32, P, ctypes.c_int32, P, P, P]
+    assert lib.dsa_topk(4, P(16), 64, P(16), 0, P(16), None, None) == 1
+    assert lib.dsa_topk(4, P(16), 66, P(16), 8, P(16), None, None) == 1
+    assert lib.dsa_topk(0, None, 64, None, 8, None, None, None) == 0          # empty: a no-op
+    # indexer: unsupported head count / dim
+    lib.dsa_index_scores.argtypes = [ctypes.c_int32] * 3 + [P] * 5 + [ctypes.c_int32, P, P, P, ctypes.c_int32, P, P,
+                                                                       P]
+    assert lib.dsa_index_scores(1, 5, 128, *[P(16)] * 5, 1, P(16), P(16), P(16), 64, None, None, None) == 2
+    assert lib.dsa_index_scores(1, 8, 96, *[P(16)] * 5, 1, P(16), P(16), P(16), 64, None, None, None) == 2
+    # compress: bad kind, null pointers
+    lib.dsa_compress.restype = ctypes.c_int32
+    args = [ctypes.c_int32(7), ctypes.c_int32(1)] + [None] * 18
+    assert lib.dsa_compress(*args) == 1
+    args = [ctypes.c_int32(0), ctypes.c_int32(1), None, None, ctypes.c_int32(1)] + [None] * 15
+    assert lib.dsa_compress(*args) == 1
+
+
+def test_workspace_size_is_zero_for_unsupported_heads(lib):
+    lib.dsa_attn_workspace_size.restype = ctypes.c_size_t
+    assert lib.dsa_attn_workspace_size(32, 48, 640) == 0
+    assert lib.dsa_attn_workspace_size(0, 64, 640) == 0

@@ -1,0 +1,209 @@
+"""GPU parity, stage by stage, on small seeded cases that span several tiles and ragged tails.
+
+Each stage of the CUDA path is compared with the oracle on byte-identical inputs: the oracle's
+indexer reads the GPU's compressed key pool, its top-k reads the GPU's scores, its attention reads
+the GPU's pools and top-k indices.  Tolerances are the ones stated in tests/_parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+from compressed_sparse_attention_c4a_gb300 import synth
+from compressed_sparse_attention_c4a_gb300.step import LayerStep, SM_SCALE
+from oracle import layer as OL, attention as OA
+from _parity import (ATTN_MAX_ABS, ATTN_REL_L2, ROW_REL_L2, np64, rel_l2, to_device, oracle_pool, rolling_states,
+                     new_tokens, pool_rows, topk_sets_match)
+
+pytestmark = pytest.mark.gpu
+S = synth.CaseSpec
+
+CASES = {
+    # decode, ragged contexts: one below k visible entries, one at a 256-position block boundary
+    "c4a_decode": S("c4a_decode", cached=[1000, 2999, 777, 4095], new=[1] * 4, seed=11),
+    # bulk compression from an empty cache (the tiny-layer shape at reduced length)
+    "c4a_bulk": S("c4a_bulk", cached=[0], new=[700], heads=16, idx_heads=4, idx_dim=64, index_compress=False,
+                  seed=12),
+    # chunked prefill whose first entry straddles the cached tokens (state ring) and the chunk
+    "c4a_chunk": S("c4a_chunk", cached=[1037], new=[300], queries="all", seed=13),
+    "c4a_multi_prefill": S("c4a_multi_prefill", cached=[300, 515], new=[64, 32], queries="all", heads=32, seed=14),
+    # c128a: dense over entries; context 128 sees exactly its first entry
+    "c128a_decode": S("c128a_decode", kind="c128a", cached=[5000, 1279, 127], new=[1] * 3, idx_heads=0, topk=0,
+                      seed=15),
+    "c128a_fp8": S("c128a_fp8", kind="c128a", cached=[3000, 640], new=[1] * 2, idx_heads=0, topk=0,
+                   main_dtype="fp8", swa_dtype="fp8", seed=16),
+    "c128a_chunk": S("c128a_chunk", kind="c128a", cached=[300], new=[200], queries="all", idx_heads=0, topk=0,
+                     seed=17),
+}
+INDEXED = [n for n, s in CASES.items() if s.idx_heads]
+
+
+def _setup(name):
+    cpu = synth.make_case(CASES[name], "cpu")
+    gpu = to_device(cpu)
+    return cpu, gpu, LayerStep(gpu)
+
+
+def _oracle_compress(cpu, which):
+    spec = cpu["spec"]
+    epb = cpu["epb"]
+    if which == "main":
+        pool = oracle_pool(cpu["main_data"], cpu["main_scale"], epb)
+        swa = oracle_pool(cpu["swa_data"], cpu["swa_scale"], 256)
+        bt, swa_bt = np64(cpu["bt_main"]), np64(cpu["bt_swa"])
+        rope_dim = spec.rope_dim
+    else:
+        pool = oracle_pool(cpu["idx_data"], cpu["idx_scale"], 64)
+        swa, bt, swa_bt = None, np64(cpu["bt_idx"]), None
+        rope_dim = min(spec.rope_dim, spec.idx_dim)
+    states = rolling_states(cpu, which)
+    xs, zs = new_tokens(cpu, which)
+    emitted = OL.compress(spec.kind, np64(cpu["start_pos"]), xs, zs, states, rope_dim, pool, bt, swa, swa_bt)
+    return pool, swa, states, emitted
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_compress_main_and_swa(name):
+    cpu, gpu, step = _setup(name)
+    step.compress()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    pool, swa, states, emitted = _oracle_compress(cpu, "main")
+    spec, epb = cpu["spec"], cpu["epb"]
+    bt = np64(cpu["bt_main"])
+    got, want = [], []
+    for r, ids in enumerate(emitted):
+        for i in ids:
+            prow = int(bt[r][i // epb]) * epb + i % epb
+            got.append(pool_rows(gpu["main_data"], gpu["main_scale"], [prow])[0])
+            want.append(pool.read(bt[r], [i])[0])
+    assert sum(len(e) for e in emitted) == len(got)
+    if got:
+        assert rel_l2(got, want) <= ROW_REL_L2
+    # SWA rows of every new token
+    sbt = np64(cpu["bt_swa"])
+    start, cu = np64(cpu["start_pos"]), np64(cpu["cu_new"])
+    g2, w2 = [], []
+    for r in range(spec.batch):
+        for j in range(cu[r + 1] - cu[r]):
+            p = int(start[r]) + j
+            prow = int(sbt[r][p // 256]) * 256 + p % 256
+            g2.append(pool_rows(gpu["swa_data"], gpu["swa_scale"], [prow])[0])
+            w2.append(swa.read(sbt[r], [p])[0])
+    assert rel_l2(g2, w2) <= ROW_REL_L2
+    # rolling state: a bit-exact copy of the last w raw tokens
+    gx, gz = np64(gpu["state_x"]), np64(gpu["state_z"])
+    for r in range(spec.batch):
+        slot = int(np64(cpu["state_slot"])[r])
+        assert np.array_equal(gx[slot], states[r].x) and np.array_equal(gz[slot], states[r].z)
+
+
+@pytest.mark.parametrize("name", [n for n in INDEXED if CASES[n].index_compress])
+def test_compress_indexer_fp8(name):
+    cpu, gpu, step = _setup(name)
+    step.compress()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    pool, _, states, emitted = _oracle_compress(cpu, "index")
+    bt = np64(cpu["bt_idx"])
+    got, want = [], []
+    for r, ids in enumerate(emitted):
+        for i in ids:
+            prow = int(bt[r][i // 64]) * 64 + i % 64
+            got.append(pool_rows(gpu["idx_data"], gpu["idx_scale"], [prow])[0])
+            want.append(pool.read(bt[r], [i])[0])
+    assert got and rel_l2(got, want) <= ROW_REL_L2
+    gx = np64(gpu["state_xi"])
+    for r in range(cpu["spec"].batch):
+        assert np.array_equal(gx[int(np64(cpu["state_slot"])[r])], states[r].x)
+
+
+def _oracle_scores_on_gpu_pool(cpu, gpu):
+    pool = oracle_pool(gpu["idx_data"], gpu["idx_scale"], 64)
+    return OL.index_scores(np64(cpu["q8"]), np64(cpu["q_scale"]), np64(cpu["w"]), np64(cpu["q_pos"]),
+                           np64(cpu["q_req"]), pool, np64(cpu["bt_idx"]))
+
+
+@pytest.mark.parametrize("name", INDEXED)
+def test_index_scores(name):
+    cpu, gpu, step = _setup(name)
+    step.compress()
+    step.index()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    want, nvis = _oracle_scores_on_gpu_pool(cpu, gpu)
+    got = np64(step.scores)
+    gn = np64(step.n_visible)
+    g_all, w_all = [], []
+    for q, n in nvis.items():
+        assert gn[q] == n
+        g_all.append(got[q, :n])
+        w_all.append(want[q][:n])
+        tile_end = min(step.ld, ((n + 127) // 128) * 128) if n else 0
+        assert np.all(np.isneginf(got[q, n:tile_end]))
+    assert rel_l2(np.concatenate(g_all), np.concatenate(w_all)) <= ROW_REL_L2
+
+
+@pytest.mark.parametrize("name", INDEXED)
+def test_topk(name):
+    cpu, gpu, step = _setup(name)
+    step.compress()
+    step.index()
+    step.select()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    k = cpu["spec"].topk
+    scores, gidx, nv = np64(step.scores), np64(step.topk), np64(step.n_visible)
+    for q in range(cpu["nq"]):
+        # same fp32 scores -> identical index list (increasing order, -1 padded)
+        assert list(gidx[q]) == list(OL.topk(scores[q], int(nv[q]), k))
+    want, nvis = _oracle_scores_on_gpu_pool(cpu, gpu)
+    for q, n in nvis.items():
+        ok, nd = topk_sets_match(gidx[q], want[q], n, k)
+        assert ok, (q, nd)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_attention(name):
+    cpu, gpu, step = _setup(name)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    spec, epb = cpu["spec"], cpu["epb"]
+    main = oracle_pool(gpu["main_data"], gpu["main_scale"], epb)
+    swa = oracle_pool(gpu["swa_data"], gpu["swa_scale"], 256)
+    topk = np64(step.topk) if step.has_index else None
+    want, lse = OL.sparse_attn(np64(cpu["q"]), np64(cpu["q_pos"]), np64(cpu["q_req"]), spec.kind, topk, main,
+                               np64(cpu["bt_main"]), swa, np64(cpu["bt_swa"]), spec.window, SM_SCALE, spec.rope_dim)
+    got, glse = np64(step.out), np64(step.lse)
+    W = np.stack([want[q] for q in range(cpu["nq"])])
+    assert np.max(np.abs(got - W)) <= ATTN_MAX_ABS
+    assert rel_l2(got, W) <= ATTN_REL_L2
+    assert np.max(np.abs(glse - np.stack([lse[q] for q in range(cpu["nq"])]))) <= 1e-3
+
+
+def test_gather_rows_bit_exact_and_unmapped_fault():
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    cpu, gpu, step = _setup("c4a_decode")
+    bt = np64(cpu["bt_main"])
+    rng = np.random.default_rng(0)
+    req = rng.integers(0, 4, 300).astype(np.int32)
+    ids = np.array([rng.integers(0, 64 * int((bt[r] >= 0).sum())) for r in req], dtype=np.int32)
+    out = torch.empty((300, 1024), dtype=torch.uint8, device="cuda")
+    dsa.dsa_gather_rows(step.main, step.main_bt, torch.from_numpy(req).cuda(), torch.from_numpy(ids).cuda(), out,
+                        dev_status=step.status)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    raw = cpu["main_data"].view(torch.uint8).view(-1, 1024).numpy()
+    want = raw[[int(bt[r][i // 64]) * 64 + i % 64 for r, i in zip(req, ids)]]
+    assert np.array_equal(out.cpu().numpy(), want)
+    # a row in an unmapped block: zeros and a device fault status, other rows intact
+    bad = torch.tensor([0, 0], dtype=torch.int32, device="cuda")
+    bad_ids = torch.tensor([5, 64 * bt.shape[1] - 1], dtype=torch.int32, device="cuda")
+    bt_holes = gpu["bt_main"].clone()
+    bt_holes[0, -1] = -1
+    out2 = torch.full((2, 1024), 7, dtype=torch.uint8, device="cuda")
+    dsa.dsa_gather_rows(step.main, dsa.block_table(bt_holes), bad, bad_ids, out2, dev_status=step.status)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == dsa.DSA_ERR_DEVICE_FAULT
+    assert np.array_equal(out2[0].cpu().numpy(), raw[int(bt[0][0]) * 64 + 5])
+    assert int(out2[1].sum().item()) == 0
