@@ -1,0 +1,471 @@
+"""Benchmark of one compressed-sparse-attention layer step on GB300.
+
+A step is one pass of the whole layer path over one batch: compress the new token(s) (main c4a /
+c128a cache, indexer cache, SWA insert), indexer scores, top-k, sparse attention with the fused
+inverse RoPE.  Default workload: the c4a decode batch (32 requests x 65,536-token context, 64
+heads, d = 512, indexer 8 x 128 fp8, top-k 512, SWA 128).  Metric: query tokens per second per
+layer (one query per request per step).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Timing: CUDA graphs of the step replayed over 4 resident cache copies (distinct layers), so that
+each step's working set was evicted from L2 by the three steps before it; CUDA events on the
+launching stream; max over ranks.  Multi-GPU: independent replicas (weak scaling), no collective
+on the data path.  ``--impl reference`` times the CPU oracle on a bounded sample of the same
+workload and prints the same JSON line with "impl": "reference".
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from compressed_sparse_attention_c4a_gb300 import synth  # noqa: E402
+
+METRIC = "c4a DSA decode query-tokens/s per layer"
+UNIT = "query-tokens/s"
+COPIES = 4
+KERNEL_SOURCES = {"index_kernel": "index_scores.cu", "attn_kernel": "attention.cu", "topk_kernel": "topk.cu",
+                  "compress_kernel": "compress.cu"}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--workload", default="c4a_decode_batch", choices=sorted(synth.case_specs()))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU work of the oracle sample")
+    return ap.parse_args()
+
+
+def rank_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+# ---------------------------------------------------------------------------------------------
+# algorithmic work of a step
+# ---------------------------------------------------------------------------------------------
+def n_entries(T, kind):
+    w, s = synth.WINDOW[kind]
+    return 0 if T < w else (T - w) // s + 1
+
+
+def algorithmic_bytes(spec):
+    """Bytes a step must move at minimum: indexer keys (+scale) of every visible entry, the gathered
+    top-k (or all visible) rows and the window rows of every query (bf16: 1024 B, fp8: 516 B)."""
+    row_main = 1024 if spec.main_dtype == "bf16" else 516
+    row_swa = 1024 if spec.swa_dtype == "bf16" else 516
+    idx_row = spec.idx_dim + 4
+    idx = att = 0
+    for r in range(spec.batch):
+        T = spec.cached[r] + spec.new[r]
+        ms = [T - 1] if spec.queries == "last" else list(range(spec.cached[r], T))
+        for m in ms:
+            nv = n_entries(m + 1, spec.kind)
+            if spec.idx_heads:
+                idx += nv * idx_row
+                att += min(spec.topk, nv) * row_main
+            else:
+                att += nv * row_main
+            att += min(spec.window, m + 1) * row_swa
+    return idx, att
+
+
+def attention_flops(spec):
+    """QK^T and PV flops over every key a query attends (2 * 2 * d per key and head)."""
+    f = 0
+    for r in range(spec.batch):
+        T = spec.cached[r] + spec.new[r]
+        ms = [T - 1] if spec.queries == "last" else list(range(spec.cached[r], T))
+        for m in ms:
+            nv = n_entries(m + 1, spec.kind)
+            keys = (min(spec.topk, nv) if spec.idx_heads else nv) + min(spec.window, m + 1)
+            f += 4 * spec.dim * spec.heads * keys
+    return f
+
+
+def queries_per_step(spec):
+    return spec.batch if spec.queries == "last" else sum(spec.new)
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            p = [x.strip() for x in l.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx = float(p[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        busy = [s for s in sm if mx and s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------------------------
+def peaks():
+    try:
+        p = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def ncu_traffic(kernel, workload):
+    """dram bytes per launch from the committed ncu summary, or None if absent or the kernel changed."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    src = os.path.join(ROOT, "compressed_sparse_attention_c4a_gb300", "csrc", KERNEL_SOURCES[kernel])
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    txt = open(path).read()
+    got_hash = got_bytes = None
+    for line in txt.splitlines():
+        if line.startswith("source_sha256_16:"):
+            got_hash = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_launch:"):
+            got_bytes = float(line.split(":", 1)[1].strip())
+    return got_bytes if got_hash == digest else None
+
+
+def run_gpu(args, rank, world, local_rank):
+    from compressed_sparse_attention_c4a_gb300 import build as _build
+    _build.build()
+    from compressed_sparse_attention_c4a_gb300.step import LayerStep
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    spec = synth.case_specs()[args.workload]
+    copies = []
+    for c in range(COPIES):
+        s = synth.CaseSpec(**{**spec.__dict__, "seed": spec.seed + 100 * c + 10000 * rank})
+        copies.append(LayerStep(synth.make_case(s, dev)))
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+    q_step = queries_per_step(spec)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # warm-up (eager; also loads the kernels) then graphs: S steps rotate over the copies
+    with torch.cuda.stream(stream):
+        for i in range(max(3, min(args.warmup, 50))):
+            copies[i % COPIES].run()
+    torch.cuda.synchronize()
+    per_graph = COPIES * max(1, min(25, args.steps // (COPIES * 4) or 1))
+    g_plain = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_plain, stream=stream):
+        for i in range(per_graph):
+            copies[i % COPIES].run()
+    # same steps with events around the indexer and attention launches (kernel durations)
+    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(per_graph)]
+          for n in ("index", "topk", "attend")}
+    g_timed = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_timed, stream=stream):
+        for i in range(per_graph):
+            st = copies[i % COPIES]
+            st.compress()
+            if st.has_index:
+                ev["index"][i][0].record(stream)
+                st.index()
+                ev["index"][i][1].record(stream)
+                ev["topk"][i][0].record(stream)
+                st.select()
+                ev["topk"][i][1].record(stream)
+            ev["attend"][i][0].record(stream)
+            st.attend()
+            ev["attend"][i][1].record(stream)
+    reps = max(1, math.ceil(args.steps / per_graph))
+    steps = reps * per_graph
+    warm_reps = max(1, math.ceil(max(3, args.warmup) / per_graph))
+    for _ in range(warm_reps):
+        g_plain.replay()
+    barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        t0.record(stream)
+        for _ in range(reps):
+            g_plain.replay()
+        t1.record(stream)
+        barrier()
+    ms_total = t0.elapsed_time(t1)
+    # kernel durations from the instrumented graph (its own timed region)
+    g_timed.replay()
+    torch.cuda.synchronize()
+    k_ms = {n: statistics.mean(a.elapsed_time(b) for a, b in pairs) for n, pairs in ev.items()
+            if copies[0].has_index or n == "attend"}
+    status = max(int(c.status.item()) for c in copies)
+
+    # e2e: host (pinned) inputs -> device, step, output -> host, all inside the timed region
+    e2e = run_e2e(copies, stream, spec, args, barrier)
+
+    ms_step = ms_total / steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_step, e2e["ms_step"]], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, e2e_ms = float(t[0]), float(t[1])
+    else:
+        e2e_ms = e2e["ms_step"]
+    value = q_step * world / (ms_step / 1e3)
+    idx_bytes, att_bytes = algorithmic_bytes(spec)
+    hbm, tfl, src = peaks()
+    kern = {}
+    if "index" in k_ms:
+        kern["index_kernel"] = {"ms": k_ms["index"], "bytes": idx_bytes, "gbs": idx_bytes / (k_ms["index"] * 1e6)}
+        kern["topk_kernel"] = {"ms": k_ms["topk"]}
+    kern["attn_kernel"] = {"ms": k_ms["attend"], "bytes": att_bytes, "gbs": att_bytes / (k_ms["attend"] * 1e6),
+                           "tflops": attention_flops(spec) / (k_ms["attend"] * 1e9)}
+    dominant = max((n for n in kern if "bytes" in kern[n]), key=lambda n: kern[n]["ms"])
+    if dominant == "index_kernel" or spec.queries == "last":
+        roof = {"kernel": dominant, "bound": "hbm", "achieved": round(kern[dominant]["gbs"], 1),
+                "peak": hbm, "unit": "GB/s", "frac": round(kern[dominant]["gbs"] / hbm, 4),
+                "traffic": ncu_traffic(dominant, args.workload), "peak_source": f"{src} hbm_gbs (burst copy)",
+                "bytes_per_launch": kern[dominant]["bytes"]}
+    else:
+        roof = {"kernel": dominant, "bound": "tensor", "achieved": round(kern[dominant]["tflops"], 1), "peak": tfl,
+                "unit": "TFLOP/s", "frac": round(kern[dominant]["tflops"] / tfl, 4),
+                "traffic": ncu_traffic(dominant, args.workload), "peak_source": f"{src} bf16_tflops (burst)"}
+    launches_per_step = copies[0].launches_per_step()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": warm_reps * per_graph, "ms_per_step": round(ms_step, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 attention + e4m3 indexer (fp32 accumulate)",
+        "data": "synthetic (seeded N(0,1) caches, queries and tokens; no weights)",
+        "config": {"workload": args.workload, "kind": spec.kind, "batch": spec.batch,
+                   "context": sorted(set(c + n for c, n in zip(spec.cached, spec.new)))[:4],
+                   "new_tokens_per_request": max(spec.new), "heads": spec.heads, "dim": spec.dim,
+                   "indexer": f"{spec.idx_heads}x{spec.idx_dim} e4m3" if spec.idx_heads else None,
+                   "topk": spec.topk or None, "window": spec.window, "kv": spec.main_dtype,
+                   "l2": f"inputs larger than L2: {COPIES} resident cache copies rotate, each step's working set is "
+                         f"evicted by the other copies", "parallelism": f"replicas x{world}"},
+        "step_bytes": idx_bytes + att_bytes, "step_gbs": round((idx_bytes + att_bytes) / (ms_step * 1e6), 1),
+        "kernels": {n: {k: round(v, 6) for k, v in d.items()} for n, d in kern.items()},
+        "roofline": roof, "gpu_launches": launches_per_step * steps, "device_status": status,
+        "e2e": {"value": round(q_step * world / (e2e_ms / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e_ms, 6)},
+        "clocks": clk.summary(),
+    }
+    return line, copies
+
+
+def run_e2e(copies, stream, spec, args, barrier):
+    """Per step: pinned host inputs -> device, the step, output -> pinned host (one CUDA graph per step)."""
+    names = ["x_new", "z_new", "q", "q_pos", "start_pos"]
+    if spec.idx_heads:
+        names += ["xi_new", "zi_new", "q8", "q_scale", "w"]
+    hosts = []
+    for st in copies:
+        hosts.append({n: st.case[n].cpu().pin_memory() for n in names})
+    outs = [torch.empty(st.out.shape, dtype=st.out.dtype, pin_memory=True) for st in copies]
+    h2d = sum(t.numel() * t.element_size() for t in hosts[0].values())
+    d2h = outs[0].numel() * outs[0].element_size()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i, st in enumerate(copies):
+            for n in names:
+                st.case[n].copy_(hosts[i][n], non_blocking=True)
+            st.run()
+            outs[i].copy_(st.out, non_blocking=True)
+    reps = max(1, min(200, args.steps // (4 * len(copies))))
+    for _ in range(3):
+        graph.replay()
+    barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    t1.record(stream)
+    barrier()
+    return {"ms_step": t0.elapsed_time(t1) / (reps * len(copies)), "h2d": h2d, "d2h": d2h}
+
+
+# ---------------------------------------------------------------------------------------------
+# the oracle (CPU) arm
+# ---------------------------------------------------------------------------------------------
+def oracle_sample(spec, case, n_requests, rows_per_request=None):
+    """Run the oracle's whole step for the first n_requests requests of a case; returns (seconds, queries)."""
+    import numpy as np
+    from oracle import layer as OL, compress as OC
+
+    def np64(t):
+        t = t.detach().cpu()
+        return t.to(torch.float64).numpy() if t.is_floating_point() else t.numpy()
+
+    epb = case["epb"]
+    t0 = time.perf_counter()
+    main = OL.Pool(epb, OL.BF16 if spec.main_dtype == "bf16" else OL.FP8,
+                   np64(case["main_data"]) if spec.main_dtype == "bf16" else case["main_data"].cpu().numpy().copy(),
+                   None if spec.main_dtype == "bf16" else np64(case["main_scale"]))
+    swa = OL.Pool(256, OL.BF16 if spec.swa_dtype == "bf16" else OL.FP8,
+                  np64(case["swa_data"]) if spec.swa_dtype == "bf16" else case["swa_data"].cpu().numpy().copy(),
+                  None if spec.swa_dtype == "bf16" else np64(case["swa_scale"]))
+    copy_s = time.perf_counter() - t0
+    cu, start = np64(case["cu_new"]), np64(case["start_pos"])
+    bt_main, bt_swa = np64(case["bt_main"]), np64(case["bt_swa"])
+    q_pos, q_req = np64(case["q_pos"]), np64(case["q_req"])
+    rows = [q for q in range(case["nq"]) if q_req[q] < n_requests]
+    if rows_per_request is not None:
+        keep = []
+        for r in range(n_requests):
+            rr = [q for q in rows if q_req[q] == r]
+            keep += rr[:rows_per_request]
+        rows = keep
+    xs = np64(case["x_new"])
+    zs = np64(case["z_new"])
+    sx, sz = np64(case["state_x"]), np64(case["state_z"])
+    t0 = time.perf_counter()
+    states = [OC.RollingState(spec.kind, spec.dim, sx[r], sz[r]) for r in range(n_requests)]
+    OL.compress(spec.kind, start[:n_requests], [xs[cu[r]:cu[r + 1]] for r in range(n_requests)],
+                [zs[cu[r]:cu[r + 1]] for r in range(n_requests)], states, spec.rope_dim, main, bt_main, swa, bt_swa)
+    topk = None
+    if spec.idx_heads:
+        idx = OL.Pool(64, OL.FP8, case["idx_data"].cpu().numpy().copy(), np64(case["idx_scale"]))
+        if spec.index_compress:
+            xi, zi = np64(case["xi_new"]), np64(case["zi_new"])
+            sxi, szi = np64(case["state_xi"]), np64(case["state_zi"])
+            st2 = [OC.RollingState(spec.kind, spec.idx_dim, sxi[r], szi[r]) for r in range(n_requests)]
+            OL.compress(spec.kind, start[:n_requests], [xi[cu[r]:cu[r + 1]] for r in range(n_requests)],
+                        [zi[cu[r]:cu[r + 1]] for r in range(n_requests)], st2, min(spec.rope_dim, spec.idx_dim), idx,
+                        np64(case["bt_idx"]))
+        scores, nvis = OL.index_scores(case["q8"].cpu().numpy(), np64(case["q_scale"]), np64(case["w"]), q_pos, q_req,
+                                       idx, np64(case["bt_idx"]), rows=rows)
+        topk = np.full((case["nq"], spec.topk), -1, dtype=np.int64)
+        for q in rows:
+            topk[q] = OL.topk(scores[q], nvis[q], spec.topk)
+    OL.sparse_attn(np64(case["q"]), q_pos, q_req, spec.kind, topk, main, bt_main, swa, bt_swa, spec.window,
+                   1.0 / math.sqrt(512.0), spec.rope_dim, rows=rows)
+    return time.perf_counter() - t0, len(rows), copy_s
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_baseline(spec, case, seconds):
+    """Time the oracle on a bounded sample (about `seconds` of CPU work) of the workload."""
+    per_req_rows = None if spec.queries == "last" else 2
+    t1, q1, _ = oracle_sample(spec, case, 1, per_req_rows)
+    n = max(1, min(spec.batch, int(seconds / max(t1, 1e-3))))
+    if n > 1:
+        t, q, _ = oracle_sample(spec, case, n, per_req_rows)
+    else:
+        t, q = t1, q1
+    what = (f"oracle step (compress, index, top-k, attention) for {n} of {spec.batch} requests"
+            if spec.queries == "last" else f"oracle step for {q} of {queries_per_step(spec)} query tokens")
+    return {"value": round(q / t, 3), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": what,
+            "seconds": round(t, 2)}
+
+
+def run_reference(args, rank):
+    spec = synth.case_specs()[args.workload]
+    if rank != 0:
+        return None
+    case = synth.make_case(spec, "cpu")
+    per_req_rows = None if spec.queries == "last" else 2
+    t1, q1, _ = oracle_sample(spec, case, 1, per_req_rows)
+    n = max(1, min(spec.batch, int(max(2.0, args.cpu_seconds / 4) / max(t1, 1e-3))))
+    times, qs = [], 0
+    for _ in range(max(1, args.warmup if args.warmup < 2 else 1)):
+        oracle_sample(spec, case, n, per_req_rows)
+    steps = max(1, min(args.steps, 3))
+    for _ in range(steps):
+        t, q, _ = oracle_sample(spec, case, n, per_req_rows)
+        times.append(t)
+        qs = q
+    ms = statistics.mean(times) * 1e3
+    value = qs / (ms / 1e3)
+    sample = f"each step: the oracle's whole layer step for {qs} of {queries_per_step(spec)} query tokens"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 0,
+            "steps": steps, "warmup": 1, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": args.workload, "batch": spec.batch, "heads": spec.heads},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local_rank = rank_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    line, copies = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(copies[0].spec, copies[0].case, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

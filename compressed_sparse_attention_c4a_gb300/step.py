@@ -89,6 +89,16 @@ class LayerStep:
                                         self.swa, self.swa_bt, s.window, SM_SCALE, self.rope_main, self.out,
                                         self.lse, self.workspace, dev_status=self.status)
 
+    def launches_per_step(self):
+        """Kernels one ``run()`` launches (compress: +1 ring kernel when a request appends > 1 token;
+        attention: +1 combine kernel when keys are split over CTAs)."""
+        per_compress = 1 + (1 if self.max_new > 1 else 0)
+        n = per_compress
+        if self.has_index:
+            n += (per_compress if self.spec.index_compress else 0) + 2
+        n += 1 + (1 if self.workspace is not None else 0)
+        return n
+
     def run(self):
         """The whole step: compress (+SWA insert), index, top-k, attention with inverse RoPE."""
         self.compress()
