@@ -29,6 +29,18 @@ def bf16_round(x):
     return np.ldexp(np.rint(m * 256.0), e - 8)
 
 
+def bf16_decode(bits):
+    """bfloat16 bit patterns (uint16) to float64: the bits are the high half of an IEEE binary32."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def bf16_encode(x):
+    """float64 values to bfloat16 bit patterns (uint16), rounding to nearest even first."""
+    r = bf16_round(x).astype(np.float32)          # exact: a bf16 value is a binary32 value
+    return (r.view(np.uint32) >> 16).astype(np.uint16)
+
+
 def e4m3_decode(codes):
     """Decode e4m3 bytes to float64: S EEEE MMM, bias 7.
 

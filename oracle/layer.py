@@ -23,13 +23,17 @@ FP8 = "fp8_e4m3"
 
 
 class Pool:
-    """A paged cache pool: ``data`` [num_blocks * epb, dim], ``scale`` [num_blocks * epb] for fp8."""
+    """A paged cache pool: ``data`` [num_blocks * epb, dim], ``scale`` [num_blocks * epb] for fp8.
+
+    bf16 pools hold either float64 values or the raw uint16 bit patterns (decoded on read).
+    """
 
     def __init__(self, epb, dtype, data, scale=None):
         self.epb = epb
         self.dtype = dtype
         self.data = data
         self.scale = scale
+        self.bits = dtype == BF16 and data.dtype == np.uint16
 
     @property
     def num_blocks(self):
@@ -39,6 +43,8 @@ class Pool:
         """Decoded float64 rows for logical ids."""
         rows = paging.physical_rows(table_row, ids, self.epb, self.num_blocks)
         if self.dtype == BF16:
+            if self.bits:
+                return codecs.bf16_decode(self.data[rows])
             return np.asarray(self.data[rows], dtype=np.float64)
         return codecs.fp8_dequantize_rows(self.data[rows], self.scale[rows])
 
@@ -52,7 +58,7 @@ class Pool:
         rows = paging.physical_rows(table_row, ids, self.epb, self.num_blocks)
         values = np.atleast_2d(np.asarray(values, dtype=np.float64))
         if self.dtype == BF16:
-            self.data[rows] = codecs.bf16_round(values)
+            self.data[rows] = codecs.bf16_encode(values) if self.bits else codecs.bf16_round(values)
         else:
             codes, scale = codecs.fp8_quantize_rows(values)
             self.data[rows] = codes

@@ -41,7 +41,7 @@ def to_device(case, device="cuda"):
 def oracle_pool(data, scale, epb):
     """An oracle Pool over (copies of) a case's pool tensors."""
     if data.dtype == torch.bfloat16:
-        return OL.Pool(epb, OL.BF16, np64(data).copy())
+        return OL.Pool(epb, OL.BF16, data.detach().cpu().view(torch.int16).numpy().view(np.uint16).copy())
     return OL.Pool(epb, OL.FP8, data.detach().cpu().numpy().copy(), np64(scale).copy())
 
 

@@ -1,0 +1,129 @@
+"""GPU parity at the full sizes of the five workloads, in the launch configuration bench.py times
+(``LayerStep.run()``: compress -> index -> top-k -> attention).
+
+Decode workloads are checked on every query row; the chunked prefill (8,192 query tokens) on a
+sample of rows the oracle computes one by one: the chunk's first rows (whose window and first
+entry straddle the cached context and the chunk), rows at 128-entry tile and 256-position block
+edges, the last row, and seeded random rows.  Compressor rows are checked for every emitted entry.
+"""
+import numpy as np
+import pytest
+import torch
+
+from compressed_sparse_attention_c4a_gb300 import synth
+from compressed_sparse_attention_c4a_gb300.step import LayerStep, SM_SCALE
+from oracle import layer as OL
+from _parity import (ATTN_MAX_ABS, ATTN_REL_L2, ROW_REL_L2, np64, rel_l2, to_device, oracle_pool, rolling_states,
+                     new_tokens, pool_rows, topk_sets_match)
+
+pytestmark = pytest.mark.gpu
+SPECS = synth.case_specs()
+
+
+def _rows(cpu):
+    nq = cpu["nq"]
+    if cpu["spec"].queries == "last":
+        return list(range(nq))
+    fixed = [0, 1, 2, 3, 4, 7, 127, 128, 255, 256, 1000, 4095, 4096, 8190, nq - 1]
+    rnd = np.random.default_rng(0).choice(nq, 9, replace=False).tolist()
+    return sorted(set(r for r in fixed + rnd if r < nq))
+
+
+def _compare_compress(cpu, gpu, which):
+    spec, epb = cpu["spec"], cpu["epb"]
+    if which == "main":
+        pool = oracle_pool(cpu["main_data"], cpu["main_scale"], epb)
+        swa = oracle_pool(cpu["swa_data"], cpu["swa_scale"], 256)
+        bt, sbt, rope_dim, rpb = np64(cpu["bt_main"]), np64(cpu["bt_swa"]), spec.rope_dim, epb
+        gdata, gscale = gpu["main_data"], gpu["main_scale"]
+    else:
+        pool = oracle_pool(cpu["idx_data"], cpu["idx_scale"], 64)
+        swa, sbt, bt, rope_dim, rpb = None, None, np64(cpu["bt_idx"]), min(spec.rope_dim, spec.idx_dim), 64
+        gdata, gscale = gpu["idx_data"], gpu["idx_scale"]
+    states = rolling_states(cpu, which)
+    xs, zs = new_tokens(cpu, which)
+    emitted = OL.compress(spec.kind, np64(cpu["start_pos"]), xs, zs, states, rope_dim, pool, bt, swa, sbt)
+    prows, want = [], []
+    for r, ids in enumerate(emitted):
+        for i in ids:
+            prows.append(int(bt[r][i // rpb]) * rpb + i % rpb)
+            want.append(pool.read(bt[r], [i])[0])
+    assert prows, "the step emits entries"
+    assert rel_l2(pool_rows(gdata, gscale, prows), np.stack(want)) <= ROW_REL_L2
+    key = "state_x" if which == "main" else "state_xi"
+    gx = np64(gpu[key])
+    slots = np64(cpu["state_slot"])
+    for r in range(spec.batch):
+        assert np.array_equal(gx[slots[r]], states[r].x)
+    if swa is not None:
+        start, cu = np64(cpu["start_pos"]), np64(cpu["cu_new"])
+        pr, wv = [], []
+        for r in range(spec.batch):
+            n = int(cu[r + 1] - cu[r])
+            for j in sorted(set([0, n - 1] + list(range(0, n, max(1, n // 64))))):
+                p = int(start[r]) + j
+                pr.append(int(sbt[r][p // 256]) * 256 + p % 256)
+                wv.append(swa.read(sbt[r], [p])[0])
+        assert rel_l2(pool_rows(gpu["swa_data"], gpu["swa_scale"], pr), np.stack(wv)) <= ROW_REL_L2
+
+
+@pytest.mark.parametrize("name", ["c4a_tiny_decode", "c4a_decode_batch", "c128a_decode", "c128a_decode_fp8",
+                                  "c4a_mixed_decode", "c4a_chunked_prefill"])
+def test_workload_parity(name):
+    spec = SPECS[name]
+    cpu = synth.make_case(spec, "cpu")
+    gpu = to_device(cpu)
+    step = LayerStep(gpu)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    rows = _rows(cpu)
+    rows_t = torch.tensor(rows, device="cuda")
+
+    _compare_compress(cpu, gpu, "main")
+    if spec.idx_heads and spec.index_compress:
+        _compare_compress(cpu, gpu, "index")
+
+    topk = None
+    if spec.idx_heads:
+        idx_pool = oracle_pool(gpu["idx_data"], gpu["idx_scale"], 64)
+        want, nvis = OL.index_scores(np64(cpu["q8"]), np64(cpu["q_scale"]), np64(cpu["w"]), np64(cpu["q_pos"]),
+                                     np64(cpu["q_req"]), idx_pool, np64(cpu["bt_idx"]), rows=rows)
+        got = np64(step.scores[rows_t])
+        gn = np64(step.n_visible)
+        gidx = np64(step.topk[rows_t])
+        g_all, w_all = [], []
+        for j, q in enumerate(rows):
+            n = nvis[q]
+            assert gn[q] == n
+            g_all.append(got[j, :n])
+            w_all.append(want[q][:n])
+            assert list(gidx[j]) == list(OL.topk(got[j], n, spec.topk))          # same scores: exact
+            ok, nd = topk_sets_match(gidx[j], want[q], n, spec.topk)           # oracle scores: near-ties only
+            assert ok, (q, nd)
+        assert rel_l2(np.concatenate(g_all), np.concatenate(w_all)) <= ROW_REL_L2
+        topk = np.full((cpu["nq"], spec.topk), -1, dtype=np.int64)
+        topk[rows] = gidx
+
+    main = oracle_pool(gpu["main_data"], gpu["main_scale"], cpu["epb"])
+    swa = oracle_pool(gpu["swa_data"], gpu["swa_scale"], 256)
+    want_o, want_l = OL.sparse_attn(_LazyRows(cpu["q"]), np64(cpu["q_pos"]), np64(cpu["q_req"]), spec.kind, topk,
+                                    main, np64(cpu["bt_main"]), swa, np64(cpu["bt_swa"]), spec.window, SM_SCALE,
+                                    spec.rope_dim, rows=rows)
+    got_o = np64(step.out[rows_t])
+    got_l = np64(step.lse[rows_t])
+    W = np.stack([want_o[q] for q in rows])
+    assert np.max(np.abs(got_o - W)) <= ATTN_MAX_ABS
+    assert rel_l2(got_o, W) <= ATTN_REL_L2
+    assert np.max(np.abs(got_l - np.stack([want_l[q] for q in rows]))) <= 1e-3
+
+
+class _LazyRows:
+    """Row access to a (large) bf16 query tensor, decoded to float64 one row at a time."""
+
+    def __init__(self, t):
+        self.t = t
+        self.shape = tuple(t.shape)
+
+    def __getitem__(self, i):
+        return np64(self.t[int(i)])

@@ -73,6 +73,14 @@ def test_bf16_round_matches_torch():
     assert codecs.bf16_round(np.array([1.0 + 3 * 2 ** -8]))[0] == 1.0 + 2 ** -6
 
 
+def test_bf16_bits_codec_matches_torch():
+    g = torch.Generator().manual_seed(8)
+    x = torch.randn(100000, generator=g, dtype=torch.float32) * 3.0
+    bits = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(codecs.bf16_decode(bits), x.to(torch.bfloat16).double().numpy())
+    assert np.array_equal(codecs.bf16_encode(x.double().numpy()), bits)
+
+
 def test_fp8_row_quantisation():
     v = np.array([[0.5, -3.0, 1.25, 0.0], [0.0, 0.0, 0.0, 0.0]])
     codes, scale = codecs.fp8_quantize_rows(v)
