@@ -245,11 +245,12 @@ def run_gpu(args, rank, world, local_rank):
     reps = max(1, math.ceil(args.steps / per_graph))
     steps = reps * per_graph
     warm_reps = max(1, math.ceil(max(3, args.warmup) / per_graph))
-    for _ in range(warm_reps):
-        g_plain.replay()
+    with torch.cuda.stream(stream):       # replay() launches on the current stream
+        for _ in range(warm_reps):
+            g_plain.replay()
     barrier()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local_rank) as clk:
+    with ClockSampler(local_rank) as clk, torch.cuda.stream(stream):
         t0.record(stream)
         for _ in range(reps):
             g_plain.replay()
@@ -263,7 +264,8 @@ def run_gpu(args, rank, world, local_rank):
     try:
         if g_timed is None:
             raise RuntimeError("no external events")
-        g_timed.replay()
+        with torch.cuda.stream(stream):
+            g_timed.replay()
         torch.cuda.synchronize()
         k_ms = {n: statistics.mean(a.elapsed_time(b) for a, b in ev[n]) for n in stages}
     except RuntimeError:
@@ -274,12 +276,13 @@ def run_gpu(args, rank, world, local_rank):
                 for i in range(per_graph):
                     st = copies[i % COPIES]
                     {"index": st.index, "topk": st.select, "attend": st.attend}[n]()
-            g.replay()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(4):
+            with torch.cuda.stream(stream):
                 g.replay()
-            b.record(stream)
+                a.record(stream)
+                for _ in range(4):
+                    g.replay()
+                b.record(stream)
             torch.cuda.synchronize()
             k_ms[n] = a.elapsed_time(b) / (4 * per_graph)
     status = max(int(c.status.item()) for c in copies)
@@ -356,14 +359,16 @@ def run_e2e(copies, stream, spec, args, barrier):
             st.run()
             outs[i].copy_(st.out, non_blocking=True)
     reps = max(1, min(200, args.steps // (4 * len(copies))))
-    for _ in range(3):
-        graph.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
     barrier()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(reps):
-        graph.replay()
-    t1.record(stream)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        t1.record(stream)
     barrier()
     return {"ms_step": t0.elapsed_time(t1) / (reps * len(copies)), "h2d": h2d, "d2h": d2h}
 

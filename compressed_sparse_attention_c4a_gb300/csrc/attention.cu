@@ -38,8 +38,7 @@ struct AttnArgs {
     dsa_block_table_t swa_bt;
     int window;
     float scale_log2;                         // sm_scale * log2(e)
-    int rope_dim;
-    double theta;
+    RopeTable rope;
     uint16_t* out;
     float* lse;
     float* ws_o;                              // [rows][nsplit][heads][512]
@@ -378,14 +377,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
         const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
         uint16_t* out0 = a.out + ((long long)row * a.heads + head0) * kD;
         uint16_t* out1 = a.out + ((long long)row * a.heads + head1) * kD;
-        const int first = kD - a.rope_dim;
+        const int first = kD - a.rope.rope_dim;
 #pragma unroll
         for (int nt = 0; nt < ON; ++nt) {
             const int col = wk * DW + nt * 8 + 2 * t4;
             float x0 = o[nt][0] * i0, x1 = o[nt][1] * i0, y0 = o[nt][2] * i1, y1 = o[nt][3] * i1;
             if (col >= first) {
                 float cs, sn;
-                rope_cos_sin(m, (col - first) >> 1, a.rope_dim, a.theta, &cs, &sn);
+                rope_cos_sin(m, a.rope.inv_freq[(col - first) >> 1], &cs, &sn);
                 // R_m^-1: rotation by -angle
                 const float u0 = x0 * cs + x1 * sn, u1 = -x0 * sn + x1 * cs;
                 const float v0 = y0 * cs + y1 * sn, v1 = -y0 * sn + y1 * cs;
@@ -441,14 +440,14 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
     const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[e] *= inv;
-    const int first = kD - a.rope_dim;
+    const int first = kD - a.rope.rope_dim;
     const int m = a.q_pos[row];
 #pragma unroll
     for (int e = 0; e < 4; e += 2) {
         const int col = tid * 4 + e;
         if (col >= first) {
             float cs, sn;
-            rope_cos_sin(m, (col - first) >> 1, a.rope_dim, a.theta, &cs, &sn);
+            rope_cos_sin(m, a.rope.inv_freq[(col - first) >> 1], &cs, &sn);
             const float x0 = acc[e], x1 = acc[e + 1];
             acc[e] = x0 * cs + x1 * sn;
             acc[e + 1] = -x0 * sn + x1 * cs;
@@ -541,8 +540,7 @@ static dsa_status_t sparse_attn(int32_t rows, int32_t heads, const void* q, cons
     a.swa_bt = *swa_bt;
     a.window = window;
     a.scale_log2 = sm_scale * kLog2e;
-    a.rope_dim = rope->rope_dim;
-    a.theta = rope->theta;
+    a.rope = make_rope_table(rope->rope_dim, rope->theta);
     a.out = static_cast<uint16_t*>(out);
     a.lse = lse;
     if (need > 0) {

@@ -5,6 +5,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "dsa.h"
@@ -69,14 +70,26 @@ __device__ __forceinline__ long long physical_row(const dsa_block_table_t& bt, i
     return (long long)pb * epb + (i - lb * epb);
 }
 
-// cos / sin of pos * theta^(-2j / rope_dim): the angle is formed and reduced modulo 2 pi in
-// double precision (positions reach 2^20, where a float angle has lost its fraction), then
-// evaluated in float.
-__device__ __forceinline__ void rope_cos_sin(long long pos, int j, int rope_dim, double theta, float* c, float* s) {
-    double f = pow(theta, -2.0 * (double)j / (double)rope_dim);
-    double a = (double)pos * f;
-    a -= kTwoPi * rint(a / kTwoPi);
-    sincosf((float)a, s, c);
+// RoPE frequencies theta^(-2j / rope_dim), j < rope_dim / 2, computed on the host in double precision and
+// passed by value in the kernel arguments (no device memory, no device-side pow).
+struct RopeTable {
+    double inv_freq[32];
+    int rope_dim;
+};
+
+inline RopeTable make_rope_table(int rope_dim, double theta) {
+    RopeTable t{};
+    t.rope_dim = rope_dim;
+    for (int j = 0; j < rope_dim / 2 && j < 32; ++j) t.inv_freq[j] = pow(theta, -2.0 * j / (double)rope_dim);
+    return t;
+}
+
+// cos / sin of pos * inv_freq: the angle is formed and reduced modulo 2 pi in double precision (at
+// positions near 2^20 a float angle has no fraction bits left), then evaluated in float.
+__device__ __forceinline__ void rope_cos_sin(long long pos, double inv_freq, float* c, float* s) {
+    const double a = (double)pos * inv_freq;
+    const double r = fma(-kTwoPi, rint(a * (1.0 / kTwoPi)), a);
+    sincosf((float)r, s, c);
 }
 
 __device__ __forceinline__ float bf16_to_float(uint16_t b) {
@@ -130,6 +143,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {

@@ -26,8 +26,7 @@ struct CompressArgs {
     int num_slots;
     const float* gamma;
     float eps;
-    int rope_dim;
-    double theta;
+    RopeTable rope;
     dsa_pool_t out;
     dsa_block_table_t out_bt;
     dsa_pool_t swa;
@@ -117,14 +116,14 @@ __device__ __forceinline__ void store_row(const dsa_pool_t& pool, long long prow
 
 // Rotate the lane's pairs that fall in the last rope_dim dims by R_pos.
 template <int E>
-__device__ __forceinline__ void rope_row(float (&v)[E], int lane, int dim, int rope_dim, double theta, long long pos) {
-    const int first = dim - rope_dim;
+__device__ __forceinline__ void rope_row(float (&v)[E], int lane, int dim, const RopeTable& rt, long long pos) {
+    const int first = dim - rt.rope_dim;
 #pragma unroll
     for (int k = 0; k < E; k += 2) {
         const int d = lane * E + k;
         if (d >= first) {
             float c, s;
-            rope_cos_sin(pos, (d - first) >> 1, rope_dim, theta, &c, &s);
+            rope_cos_sin(pos, rt.inv_freq[(d - first) >> 1], &c, &s);
             const float x0 = v[k], x1 = v[k + 1];
             v[k] = x0 * c - x1 * s;
             v[k + 1] = x0 * s + x1 * c;
@@ -192,7 +191,7 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
 #pragma unroll
         for (int k = 0; k < E; ++k) acc[k] *= rs * (a.gamma ? a.gamma[lane * E + k] : 1.f);
         // RoPE at the last covered position
-        rope_row<E>(acc, lane, DIM, a.rope_dim, a.theta, base + w - 1);
+        rope_row<E>(acc, lane, DIM, a.rope, base + w - 1);
         const long long prow = physical_row(a.out_bt, r, i, a.out.rows_per_block, a.out.num_blocks);
         if (prow < 0) {
             if (lane == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
@@ -209,7 +208,7 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
     if (a.has_swa) {
         float v[E];
         load_bf16<E>(xrow, lane, v);
-        rope_row<E>(v, lane, DIM, a.rope_dim, a.theta, p);
+        rope_row<E>(v, lane, DIM, a.rope, p);
         const long long prow = physical_row(a.swa_bt, r, p, kBlockPositions, a.swa.num_blocks);
         if (prow < 0) {
             if (lane == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
@@ -298,8 +297,7 @@ extern "C" dsa_status_t dsa_compress(int32_t kind, int32_t batch, const int32_t*
     a.num_slots = num_slots;
     a.gamma = rms_gamma;
     a.eps = rms_eps;
-    a.rope_dim = rope->rope_dim;
-    a.theta = rope->theta;
+    a.rope = make_rope_table(rope->rope_dim, rope->theta);
     a.out = *out;
     a.out_bt = *out_bt;
     a.has_swa = swa != nullptr;

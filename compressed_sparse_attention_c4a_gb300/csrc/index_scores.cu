@@ -13,16 +13,21 @@
 // weight and causal mask, writing coalesced score rows.  Every wait is bounded.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace dsa {
 
-constexpr int kIdxThreads = 128;
+constexpr int kIdxThreads = 192;  // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
 constexpr int kTileEntries = 128;
-constexpr int kPage = 64;  // c4a entries per 256-position block
+constexpr int kPage = 64;         // c4a entries per 256-position block
+constexpr int kChunkItems = 4;    // consecutive tiles of one group handled back to back by one CTA
 
 struct IdxArgs {
     int nq, heads, q_group, n_cols, tmem_cols, ld;
+    int n_groups, tiles, stages, stage_bytes;
+    long long total_items, n_chunks;
     const float* q_scale;
     const float* w;
     const int32_t* q_pos;
@@ -86,60 +91,99 @@ __device__ __forceinline__ uint32_t idesc_f8(int n) {
     return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTileEntries >> 4) << 24);
 }
 
+__device__ __forceinline__ int visible_of(const IdxArgs& a, int q) {
+    const int m = a.q_pos[q];
+    return m < 0 ? 0 : entries_formed((long long)m + 1, 8, 4);
+}
+
+// Group g = queries [g * q_group, ...) of one request: its request id (or -1 if the group mixes
+// requests or names a request beyond the table) and the largest visible-entry count.
+struct GroupInfo {
+    int g, r, max_vis;
+};
+
+__device__ __forceinline__ GroupInfo group_info(const IdxArgs& a, int g) {
+    const int q0 = g * a.q_group;
+    const int nqg = min(a.q_group, a.nq - q0);
+    GroupInfo gi{g, a.q_req[q0], 0};
+    for (int j = 0; j < nqg; ++j) {
+        gi.max_vis = max(gi.max_vis, visible_of(a, q0 + j));
+        if (a.q_req[q0 + j] != gi.r) gi.r = -1;
+    }
+    if (gi.r < 0 || gi.r >= a.bt.batch) gi.r = -1;
+    return gi;
+}
+
+// Every role walks the same sequence of valid items: chunks of kChunkItems consecutive tiles of the
+// rectangular (group x tile) space, chunk c going to CTA c mod gridDim.x; a tile is valid when it
+// holds at least one entry visible to some query of its group.
+template <typename F>
+__device__ __forceinline__ void for_each_item(const IdxArgs& a, volatile int* abort_flag, F&& fn) {
+    int n = 0;
+    GroupInfo gi{-1, -1, 0};
+    for (long long ch = blockIdx.x; ch < a.n_chunks; ch += gridDim.x) {
+        for (int u = 0; u < kChunkItems; ++u) {
+            const long long it = ch * kChunkItems + u;
+            if (it >= a.total_items) break;
+            if (*abort_flag) return;
+            const int g = (int)(it / a.tiles), t = (int)(it % a.tiles);
+            if (g != gi.g) {
+                gi = group_info(a, g);
+                if (gi.r < 0) report(a.status, DSA_ERR_DEVICE_FAULT);
+            }
+            if (gi.r < 0 || t * kTileEntries >= gi.max_vis) continue;
+            fn(n, gi, t);
+            ++n;
+        }
+    }
+}
+
+// Bounded wait that also gives up once another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              int32_t* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            report(status, DSA_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 template <int DIM>
 __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constant__ CUtensorMap kmap,
                                                             const __grid_constant__ CUtensorMap qmap, IdxArgs a) {
-    constexpr int kA = kTileEntries * DIM;  // bytes of the key tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sA = smem;
-    uint8_t* sB = smem + kA;                                  // n_cols rows x DIM (1024-aligned: kA is)
-    float* s_kscale = reinterpret_cast<float*>(sB + a.n_cols * DIM);
-    float* s_sq = s_kscale + kTileEntries;
-    float* s_w = s_sq + 256;
-    int* s_nvis = reinterpret_cast<int*>(s_w + 256);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s_nvis + 64);
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2);
-    int* s_page_ok = reinterpret_cast<int*>(s_tmem + 1);
+    const int S = a.stages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * a.stage_bytes);
+    uint64_t* empty = full + S;
+    uint64_t* tfull = empty + S;   // [2]
+    uint64_t* tempty = tfull + 2;  // [2]
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(s_tmem + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int grp = blockIdx.y, tile = blockIdx.x;
-    const int q0 = grp * a.q_group;
-    const int nqg = min(a.q_group, a.nq - q0);
-    const int r = a.q_req[q0];
 
-    // group visibility (every thread computes the same values)
-    int max_vis = 0;
-    bool mixed = false;
-    for (int j = 0; j < nqg; ++j) {
-        const int m = a.q_pos[q0 + j];
-        max_vis = max(max_vis, m < 0 ? 0 : entries_formed((long long)m + 1, 8, 4));
-        mixed |= a.q_req[q0 + j] != r;
-    }
-    if (mixed || r < 0 || r >= a.bt.batch) {
-        if (tid == 0 && tile == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
-        return;
-    }
-    if (tile == 0 && tid < nqg && a.n_visible) {
-        const int m = a.q_pos[q0 + tid];
-        a.n_visible[q0 + tid] = m < 0 ? 0 : entries_formed((long long)m + 1, 8, 4);
-    }
-    const int e0 = tile * kTileEntries;
-    if (e0 >= max_vis) return;
+    // visible-entry count of every query (grid-strided, independent of the tile loop)
+    if (a.n_visible)
+        for (int q = blockIdx.x * kIdxThreads + tid; q < a.nq; q += gridDim.x * kIdxThreads)
+            a.n_visible[q] = visible_of(a, q);
 
-    if (tid < nqg) {
-        const int m = a.q_pos[q0 + tid];
-        s_nvis[tid] = m < 0 ? 0 : entries_formed((long long)m + 1, 8, 4);
-    }
-    for (int c = tid; c < a.n_cols; c += kIdxThreads) {
-        const int j = c / a.heads;
-        const bool ok = j < nqg;
-        s_sq[c] = ok ? a.q_scale[(long long)q0 * a.heads + c] : 0.f;
-        s_w[c] = ok ? a.w[(long long)q0 * a.heads + c] : 0.f;
-    }
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4 * 32);
+        }
+        *abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(s_tmem, a.tmem_cols);
@@ -148,80 +192,98 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
-    bool ok = true;
-    if (tid == 0) {
-        uint32_t bytes = (uint32_t)a.n_cols * DIM;
-        int blk[2];
-        for (int pi = 0; pi < 2; ++pi) {
-            const int lp = 2 * tile + pi;  // logical block
-            blk[pi] = -1;
-            s_page_ok[pi] = 0;
-            if (lp * kPage >= max_vis) continue;
-            const int b = lp < a.bt.max_blocks ? a.bt.table[(long long)r * a.bt.max_blocks + lp] : -1;
-            if (b < 0 || b >= a.num_blocks) {
-                report(a.status, DSA_ERR_DEVICE_FAULT);
-                continue;
-            }
-            blk[pi] = b;
-            s_page_ok[pi] = 1;
-            bytes += kPage * DIM + kPage * 4;
-        }
-        mbar_arrive_expect_tx(&bars[0], bytes);
-        for (int pi = 0; pi < 2; ++pi) {
-            if (blk[pi] < 0) continue;
-            tma_load_2d(sA + pi * kPage * DIM, &kmap, 0, blk[pi] * kPage, &bars[0]);
-            bulk_g2s(s_kscale + pi * kPage, a.key_scale + (long long)blk[pi] * kPage, kPage * 4, &bars[0]);
-        }
-        tma_load_2d(sB, &qmap, 0, q0 * a.heads, &bars[0]);
-    }
-    __syncthreads();
-    ok = mbar_wait_bounded(&bars[0], 0, kWaitLimitNs);
-    ok = __syncthreads_and(ok);   // block-uniform: tcgen05.ld below is warp-collective
-    if (!ok && tid == 0) {
-        report(a.status, DSA_ERR_TIMEOUT);
-        mbar_wait_bounded(&bars[0], 0, kWaitLimitNs);  // give copies still in flight a last chance to land
-    }
-    if (ok && tid == 0) {
-        tc_fence_after();
-        const uint32_t a_addr = smem_u32(sA), b_addr = smem_u32(sB);
-        const uint32_t idesc = idesc_f8(a.n_cols);
-#pragma unroll
-        for (int ks = 0; ks < DIM / 32; ++ks)
-            mma_f8(tmem, smem_desc(a_addr + ks * 32, DIM), smem_desc(b_addr + ks * 32, DIM), idesc, ks > 0);
-        mma_commit(&bars[1]);
-    }
-    bool mma_ok = ok ? mbar_wait_bounded(&bars[1], 0, kWaitLimitNs) : false;
-    mma_ok = __syncthreads_and(mma_ok);
-    if (ok && !mma_ok && tid == 0) report(a.status, DSA_ERR_TIMEOUT);
-    ok = mma_ok;
-    tc_fence_after();
-
-    // epilogue: thread <-> TMEM lane <-> entry
-    const int row = warp * 32 + lane;
-    const int e = e0 + row;
-    const bool page_ok = s_page_ok[row / kPage] != 0;
-    const float sk = page_ok ? s_kscale[row] : 0.f;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    float acc_q = 0.f;
-    for (int c0 = 0; c0 < a.n_cols; c0 += 16) {
-        float v[16];
-        if (ok) tmem_ld16(lane_base + c0, v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int c = c0 + i;
-            if (ok) acc_q += s_w[c] * fmaxf(0.f, s_sq[c] * sk * v[i]);
-            if ((c + 1) % a.heads == 0) {
-                const int j = c / a.heads;
-                if (j < nqg && e < a.ld) {
-                    const bool vis = ok && page_ok && e < s_nvis[j];
-                    a.scores[(long long)(q0 + j) * a.ld + e] = vis ? acc_q : -INFINITY;
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---- producer: two key pages + the group's query tile per stage --------------------------
+            for_each_item(a, abort_flag, [&](int n, const GroupInfo& gi, int t) {
+                const int s = n % S;
+                if (!wait_or_abort(&empty[s], ((n / S) & 1) ^ 1, abort_flag, a.status)) return;
+                uint8_t* sa = smem + (size_t)s * a.stage_bytes;
+                int blk[2] = {-1, -1};
+                uint32_t bytes = (uint32_t)a.n_cols * DIM;
+                for (int pi = 0; pi < 2; ++pi) {
+                    const int lp = 2 * t + pi;
+                    if (lp * kPage >= gi.max_vis) continue;
+                    const int b = lp < a.bt.max_blocks ? a.bt.table[(long long)gi.r * a.bt.max_blocks + lp] : -1;
+                    if (b < 0 || b >= a.num_blocks) {
+                        report(a.status, DSA_ERR_DEVICE_FAULT);
+                        continue;
+                    }
+                    blk[pi] = b;
+                    bytes += kPage * DIM;
                 }
-                acc_q = 0.f;
-            }
+                mbar_arrive_expect_tx(&full[s], bytes);
+                for (int pi = 0; pi < 2; ++pi)
+                    if (blk[pi] >= 0) tma_load_2d(sa + pi * kPage * DIM, &kmap, 0, blk[pi] * kPage, &full[s]);
+                tma_load_2d(sa + kTileEntries * DIM, &qmap, 0, gi.g * a.q_group * a.heads, &full[s]);
+            });
         }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---- MMA issuer: D[entry][q*heads + h] = <k8_entry, q8_(q,h)>, accumulated over dim ------
+            const uint32_t idesc = idesc_f8(a.n_cols);
+            for_each_item(a, abort_flag, [&](int n, const GroupInfo&, int) {
+                const int s = n % S, b = n & 1;
+                if (!wait_or_abort(&full[s], (n / S) & 1, abort_flag, a.status)) return;
+                if (!wait_or_abort(&tempty[b], ((n >> 1) & 1) ^ 1, abort_flag, a.status)) return;
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(smem + (size_t)s * a.stage_bytes);
+                const uint32_t b_addr = a_addr + kTileEntries * DIM;
+#pragma unroll
+                for (int ks = 0; ks < DIM / 32; ++ks)
+                    mma_f8(tmem + b * a.n_cols, smem_desc(a_addr + ks * 32, DIM), smem_desc(b_addr + ks * 32, DIM),
+                           idesc, ks > 0);
+                mma_commit(&empty[s]);
+                mma_commit(&tfull[b]);
+            });
+        }
+    } else {
+        // ---- epilogue: TMEM lane <-> entry; ReLU, scales, head weights, causal mask -------------------
+        const int quad = warp & 3;  // TMEM lanes this warp may access
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        for_each_item(a, abort_flag, [&](int n, const GroupInfo& gi, int t) {
+            const int b = n & 1;
+            const bool ok = wait_or_abort(&tfull[b], (n >> 1) & 1, abort_flag, a.status);
+            if (!__all_sync(0xffffffffu, ok)) return;  // warp-uniform: tcgen05.ld is warp-collective
+            tc_fence_after();
+            const int e = t * kTileEntries + row;
+            const int lp = 2 * t + row / kPage;
+            int blk = -1;
+            if (lp * kPage < gi.max_vis && lp < a.bt.max_blocks) {
+                blk = a.bt.table[(long long)gi.r * a.bt.max_blocks + lp];
+                if (blk >= a.num_blocks) blk = -1;
+            }
+            const float sk = blk >= 0 ? a.key_scale[(long long)blk * kPage + (row % kPage)] : 0.f;
+            const int q0 = gi.g * a.q_group;
+            const int nqg = min(a.q_group, a.nq - q0);
+            float acc_q = 0.f;
+            for (int c0 = 0; c0 < a.n_cols; c0 += 16) {
+                float v[16];
+                tmem_ld16(lane_base + b * a.n_cols + c0, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int c = c0 + i;
+                    const int j = c / a.heads;
+                    if (j < nqg) {
+                        const long long qh = (long long)q0 * a.heads + c;
+                        acc_q += __ldg(a.w + qh) * fmaxf(0.f, __ldg(a.q_scale + qh) * sk * v[i]);
+                    }
+                    if ((c + 1) % a.heads == 0) {
+                        if (j < nqg && e < a.ld)
+                            a.scores[(long long)(q0 + j) * a.ld + e] =
+                                (blk >= 0 && e < visible_of(a, q0 + j)) ? acc_q : -INFINITY;
+                        acc_q = 0.f;
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[b]);
+        });
     }
     tc_fence_before();
     __syncthreads();
+    tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, a.tmem_cols);
 }
 
@@ -249,16 +311,17 @@ static bool make_map(CUtensorMap* map, const void* base, uint64_t rows, int dim,
 }
 
 template <int DIM>
-static dsa_status_t launch_index(const CUtensorMap& kmap, const CUtensorMap& qmap, const IdxArgs& a, int tiles,
-                                 int groups, cudaStream_t st) {
-    const int need = 1024 + kTileEntries * DIM + a.n_cols * DIM + (kTileEntries + 256 + 256 + 64) * 4 + 64;
-    // at most 512 / tmem_cols resident CTAs per SM, so that every tcgen05.alloc is satisfied at once
-    const int per_sm = 512 / a.tmem_cols;
-    const int cap = 232448 / per_sm - 1024;
-    const int smem = per_sm >= 16 ? need : (need > cap ? need : cap);
+static dsa_status_t launch_index(const CUtensorMap& kmap, const CUtensorMap& qmap, IdxArgs a, cudaStream_t st) {
+    // stage = 128 key rows + the query tile; ~96-192 KB of stages per SM keeps enough bytes in flight
+    a.stage_bytes = ((kTileEntries + a.n_cols) * DIM + 1023) / 1024 * 1024;
+    const int ctas_per_sm = a.stage_bytes <= 24 * 1024 ? 2 : 1;
+    const int budget = 227 * 1024 / ctas_per_sm - 1024 - 256;
+    a.stages = max(2, min(8, budget / a.stage_bytes));
+    const int smem = 1024 + a.stages * a.stage_bytes + 256;
     if (cudaFuncSetAttribute(index_kernel<DIM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return DSA_ERR_CUDA;
-    index_kernel<DIM><<<dim3(tiles, groups), kIdxThreads, smem, st>>>(kmap, qmap, a);
+    const long long grid = std::min<long long>(a.n_chunks, (long long)sm_count() * ctas_per_sm);
+    index_kernel<DIM><<<(unsigned)std::max<long long>(grid, 1), kIdxThreads, smem, st>>>(kmap, qmap, a);
     return launch_status();
 }
 
@@ -287,7 +350,7 @@ extern "C" dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim,
     a.heads = heads;
     a.q_group = q_group;
     a.n_cols = n_cols;
-    a.tmem_cols = n_cols <= 32 ? 32 : (n_cols <= 64 ? 64 : (n_cols <= 128 ? 128 : 256));
+    a.tmem_cols = 2 * n_cols <= 32 ? 32 : (2 * n_cols <= 64 ? 64 : (2 * n_cols <= 128 ? 128 : (2 * n_cols <= 256 ? 256 : 512)));
     a.ld = ld;
     a.q_scale = q_scale;
     a.w = w;
@@ -302,9 +365,10 @@ extern "C" dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim,
     CUtensorMap kmap, qmap;
     if (!make_map(&kmap, keys->data, (uint64_t)keys->num_blocks * kPage, dim, kPage)) return DSA_ERR_CUDA;
     if (!make_map(&qmap, q8, (uint64_t)nq * heads, dim, n_cols)) return DSA_ERR_CUDA;
-    const int tiles = (ld + kTileEntries - 1) / kTileEntries;
-    const int groups = (nq + q_group - 1) / q_group;
+    a.tiles = (ld + kTileEntries - 1) / kTileEntries;
+    a.n_groups = (nq + q_group - 1) / q_group;
+    a.total_items = (long long)a.tiles * a.n_groups;
+    a.n_chunks = (a.total_items + kChunkItems - 1) / kChunkItems;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return dim == 128 ? launch_index<128>(kmap, qmap, a, tiles, groups, st)
-                      : launch_index<64>(kmap, qmap, a, tiles, groups, st);
+    return dim == 128 ? launch_index<128>(kmap, qmap, a, st) : launch_index<64>(kmap, qmap, a, st);
 }

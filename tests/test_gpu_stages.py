@@ -207,3 +207,47 @@ def test_gather_rows_bit_exact_and_unmapped_fault():
     assert int(step.status.item()) == dsa.DSA_ERR_DEVICE_FAULT
     assert np.array_equal(out2[0].cpu().numpy(), raw[int(bt[0][0]) * 64 + 5])
     assert int(out2[1].sum().item()) == 0
+
+
+@pytest.mark.parametrize("ld", [1024, 16384, 65536])
+def test_topk_edge_cases_exact(ld):
+    """Ties, all-equal rows, n == k + 1, n < k, empty rows, -inf tails, negative scores; rows that fit
+    shared memory and rows that stream from L2 (ld > 40,960)."""
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    rng = np.random.default_rng(ld)
+    k = 512
+    rows, nv = [], []
+    n_full = ld - 3
+    for case in range(10):
+        r = rng.standard_normal(ld).astype(np.float32)
+        n = n_full
+        if case == 0:
+            r[:] = 1.5                                              # all equal: lowest indices win
+        elif case == 1:
+            r = rng.integers(0, 7, ld).astype(np.float32)           # heavy ties at the threshold
+        elif case == 2:
+            n = min(ld, k + 1)
+        elif case == 3:
+            n = k - 5
+        elif case == 4:
+            n = 0
+        elif case == 5:
+            r = -np.abs(r)                                          # negative scores
+        elif case == 6:
+            r[n_full // 2:] = -np.inf                               # many invisible-looking entries
+        elif case == 7:
+            r = (rng.integers(0, 3, ld) * 2.0 ** -20).astype(np.float32)   # ties among tiny values
+        elif case == 8:
+            r[::2] = 0.0                                            # half exact zeros (ReLU-like)
+        rows.append(r)
+        nv.append(n)
+    scores = torch.from_numpy(np.stack(rows)).cuda()
+    n_valid = torch.tensor(nv, dtype=torch.int32, device="cuda")
+    out = torch.empty((len(rows), k), dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dsa.dsa_topk(scores, n_valid, k, out, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = out.cpu().numpy()
+    for i, (r, n) in enumerate(zip(rows, nv)):
+        assert list(got[i]) == list(OL.topk(r.astype(np.float64), n, k)), i
