@@ -231,7 +231,8 @@ def run_gpu(args, rank, world, local_rank):
         with torch.cuda.graph(g_timed, stream=stream):
             for i in range(per_graph):
                 st = copies[i % COPIES]
-                st.compress()
+                st.compress_main()
+                st.compress_index()
                 if st.has_index:
                     ev["index"][i][0].record(stream)
                     st.index()

@@ -131,7 +131,7 @@ __device__ __forceinline__ void rope_row(float (&v)[E], int lane, int dim, const
     }
 }
 
-template <int DIM>
+template <int DIM, int W>
 __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
     constexpr int E = DIM / 32;
     const int lane = threadIdx.x & 31;
@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
         if (item == 0 && lane == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
         return;
     }
-    const int w = a.w, s = a.s;
+    constexpr int w = W;
+    const int s = a.s;
 
     if (item < a.entry_items) {
         // entries whose last raw token s*i + w - 1 lies in [start, end)
@@ -163,24 +164,42 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
             return p < start ? a.state_x + ((long long)slot * w + (p % w)) * DIM
                              : a.x_new + (long long)(cu0 + (p - start)) * DIM;
         };
-        // gate g_j = softmax_j(z_{s i + j})
+        // gate g_j = softmax_j(z_{s i + j}): lane l holds the logits of window tokens l, l + 32, ...
+        constexpr int LPL = (W + 31) / 32;  // logits per lane
+        float z[LPL];
         float mx = -INFINITY;
-        for (int j = lane; j < w; j += 32) mx = fmaxf(mx, logit_at(base + j));
+#pragma unroll
+        for (int u = 0; u < LPL; ++u) {
+            const int j = lane + 32 * u;
+            z[u] = j < W ? logit_at(base + j) : -INFINITY;
+            mx = fmaxf(mx, z[u]);
+        }
         mx = warp_max(mx);
         float den = 0.f;
-        for (int j = lane; j < w; j += 32) den += expf(logit_at(base + j) - mx);
+#pragma unroll
+        for (int u = 0; u < LPL; ++u) {
+            z[u] = (lane + 32 * u) < W ? expf(z[u] - mx) : 0.f;
+            den += z[u];
+        }
         den = warp_sum(den);
         const float inv_den = 1.f / den;
         float acc[E];
 #pragma unroll
         for (int k = 0; k < E; ++k) acc[k] = 0.f;
-        for (int j = 0; j < w; ++j) {
-            const long long p = base + j;
-            const float g = expf(logit_at(p) - mx) * inv_den;
-            float x[E];
-            load_bf16<E>(row_at(p), lane, x);
+        // weighted sum, 8 window rows in flight at a time
+        constexpr int RB = W < 8 ? W : 8;
+#pragma unroll 1
+        for (int j0 = 0; j0 < W; j0 += RB) {
+            float x[RB][E];
 #pragma unroll
-            for (int k = 0; k < E; ++k) acc[k] = fmaf(g, x[k], acc[k]);
+            for (int u = 0; u < RB; ++u) load_bf16<E>(row_at(base + j0 + u), lane, x[u]);
+#pragma unroll
+            for (int u = 0; u < RB; ++u) {
+                const int j = j0 + u;
+                const float g = __shfl_sync(0xffffffffu, z[j / 32 < LPL ? j / 32 : 0], j & 31) * inv_den;
+#pragma unroll
+                for (int k = 0; k < E; ++k) acc[k] = fmaf(g, x[u][k], acc[k]);
+            }
         }
         // RMSNorm
         float ss = 0.f;
@@ -246,7 +265,10 @@ template <int DIM>
 static dsa_status_t launch_compress(const CompressArgs& a, int max_new, cudaStream_t st) {
     const int items = a.entry_items + a.token_items;
     dim3 grid((items + 7) / 8, a.batch);
-    compress_kernel<DIM><<<grid, 256, 0, st>>>(a);
+    if (a.w == 8)
+        compress_kernel<DIM, 8><<<grid, 256, 0, st>>>(a);
+    else
+        compress_kernel<DIM, 128><<<grid, 256, 0, st>>>(a);
     if (!a.fuse_ring && max_new > 0) {
         dim3 g2((a.w + 7) / 8, a.batch);
         ring_update_kernel<DIM><<<g2, 256, 0, st>>>(a);

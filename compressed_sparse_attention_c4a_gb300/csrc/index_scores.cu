@@ -26,7 +26,7 @@ constexpr int kChunkItems = 4;    // consecutive tiles of one group handled back
 
 struct IdxArgs {
     int nq, heads, q_group, n_cols, tmem_cols, ld;
-    int n_groups, tiles, stages, stage_bytes;
+    int n_groups, tiles, stages, stage_bytes, n_acc;  // n_acc: TMEM accumulators (2 or 4)
     long long total_items, n_chunks;
     const float* q_scale;
     const float* w;
@@ -91,10 +91,10 @@ __device__ __forceinline__ uint32_t idesc_f8(int n) {
     return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTileEntries >> 4) << 24);
 }
 
-__device__ __forceinline__ int visible_of(const IdxArgs& a, int q) {
-    const int m = a.q_pos[q];
-    return m < 0 ? 0 : entries_formed((long long)m + 1, 8, 4);
-}
+// c4a entries visible to the query at position m: those whose last raw token 4i + 7 <= m.
+__device__ __forceinline__ int visible_at(int m) { return m < 7 ? 0 : ((m - 7) >> 2) + 1; }
+
+__device__ __forceinline__ int visible_of(const IdxArgs& a, int q) { return visible_at(a.q_pos[q]); }
 
 // Group g = queries [g * q_group, ...) of one request: its request id (or -1 if the group mixes
 // requests or names a request beyond the table) and the largest visible-entry count.
@@ -154,18 +154,34 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
     }
 }
 
-template <int DIM>
+// Per-stage layout (bytes from the stage start): key tile [128][DIM] (swizzled), query tile
+// [n_cols][DIM] (swizzled), then StageMeta, then fp32 entry scales [128], head weights [n_cols] and
+// query scales [n_cols] (bulk copies).  The stage is released by the epilogue, so everything the
+// epilogue reads stays in shared memory until it is done.
+struct StageMeta {
+    int blk[2];    // physical block of each 64-entry page, -1 if not loaded
+    int nq;        // queries in the group
+    int q0;        // first query of the group
+    int e0;        // first entry of the tile
+    int nvis[64];  // visible entries per query of the group
+};
+
+__host__ __device__ constexpr int meta_bytes() { return ((int)sizeof(StageMeta) + 15) / 16 * 16; }
+
+template <int DIM, int HEADS>
 __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constant__ CUtensorMap kmap,
                                                             const __grid_constant__ CUtensorMap qmap, IdxArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int S = a.stages;
+    const int S = a.stages, NA = a.n_acc;
+    const int tiles_bytes = (kTileEntries + a.n_cols) * DIM;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * a.stage_bytes);
     uint64_t* empty = full + S;
-    uint64_t* tfull = empty + S;   // [2]
-    uint64_t* tempty = tfull + 2;  // [2]
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + 2);
+    uint64_t* tfull = empty + S;   // [NA]
+    uint64_t* tempty = tfull + 4;  // [NA]
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(s_tmem + 1);
+    int* grp_nvis = reinterpret_cast<int*>(s_tmem + 2);  // producer-private cache [64]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -177,9 +193,9 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            mbar_init(&empty[i], 4 * 32);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NA; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], 4 * 32);
         }
@@ -194,28 +210,50 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---- producer: two key pages + the group's query tile per stage --------------------------
+            // ---- producer: two key pages, scales, the group's query tile, weights and scales --------
+            int cached_g = -1;
             for_each_item(a, abort_flag, [&](int n, const GroupInfo& gi, int t) {
                 const int s = n % S;
                 if (!wait_or_abort(&empty[s], ((n / S) & 1) ^ 1, abort_flag, a.status)) return;
-                uint8_t* sa = smem + (size_t)s * a.stage_bytes;
-                int blk[2] = {-1, -1};
-                uint32_t bytes = (uint32_t)a.n_cols * DIM;
+                uint8_t* st = smem + (size_t)s * a.stage_bytes;
+                StageMeta* meta = reinterpret_cast<StageMeta*>(st + tiles_bytes);
+                float* sscale = reinterpret_cast<float*>(st + tiles_bytes + meta_bytes());
+                float* sw = sscale + kTileEntries;
+                float* ssq = sw + a.n_cols;
+                const int q0 = gi.g * a.q_group;
+                const int nqg = min(a.q_group, a.nq - q0);
+                if (gi.g != cached_g) {
+                    for (int j = 0; j < nqg; ++j) grp_nvis[j] = visible_of(a, q0 + j);
+                    cached_g = gi.g;
+                }
+                uint32_t bytes = (uint32_t)a.n_cols * DIM + 2u * nqg * HEADS * 4u;
                 for (int pi = 0; pi < 2; ++pi) {
                     const int lp = 2 * t + pi;
-                    if (lp * kPage >= gi.max_vis) continue;
-                    const int b = lp < a.bt.max_blocks ? a.bt.table[(long long)gi.r * a.bt.max_blocks + lp] : -1;
-                    if (b < 0 || b >= a.num_blocks) {
-                        report(a.status, DSA_ERR_DEVICE_FAULT);
-                        continue;
+                    int b = -1;
+                    if (lp * kPage < gi.max_vis) {
+                        b = lp < a.bt.max_blocks ? a.bt.table[(long long)gi.r * a.bt.max_blocks + lp] : -1;
+                        if (b < 0 || b >= a.num_blocks) {
+                            report(a.status, DSA_ERR_DEVICE_FAULT);
+                            b = -1;
+                        }
                     }
-                    blk[pi] = b;
-                    bytes += kPage * DIM;
+                    meta->blk[pi] = b;
+                    if (b >= 0) bytes += kPage * DIM + kPage * 4;
                 }
-                mbar_arrive_expect_tx(&full[s], bytes);
-                for (int pi = 0; pi < 2; ++pi)
-                    if (blk[pi] >= 0) tma_load_2d(sa + pi * kPage * DIM, &kmap, 0, blk[pi] * kPage, &full[s]);
-                tma_load_2d(sa + kTileEntries * DIM, &qmap, 0, gi.g * a.q_group * a.heads, &full[s]);
+                meta->nq = nqg;
+                meta->q0 = q0;
+                meta->e0 = t * kTileEntries;
+                for (int j = 0; j < nqg; ++j) meta->nvis[j] = grp_nvis[j];
+                mbar_arrive_expect_tx(&full[s], bytes);  // release: the meta writes above are visible
+                for (int pi = 0; pi < 2; ++pi) {
+                    const int b = meta->blk[pi];
+                    if (b < 0) continue;
+                    tma_load_2d(st + pi * kPage * DIM, &kmap, 0, b * kPage, &full[s]);
+                    bulk_g2s(sscale + pi * kPage, a.key_scale + (long long)b * kPage, kPage * 4, &full[s]);
+                }
+                tma_load_2d(st + kTileEntries * DIM, &qmap, 0, q0 * HEADS, &full[s]);
+                bulk_g2s(sw, a.w + (long long)q0 * HEADS, nqg * HEADS * 4, &full[s]);
+                bulk_g2s(ssq, a.q_scale + (long long)q0 * HEADS, nqg * HEADS * 4, &full[s]);
             });
         }
     } else if (warp == 1) {
@@ -223,9 +261,9 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
             // ---- MMA issuer: D[entry][q*heads + h] = <k8_entry, q8_(q,h)>, accumulated over dim ------
             const uint32_t idesc = idesc_f8(a.n_cols);
             for_each_item(a, abort_flag, [&](int n, const GroupInfo&, int) {
-                const int s = n % S, b = n & 1;
+                const int s = n % S, b = n % NA;
                 if (!wait_or_abort(&full[s], (n / S) & 1, abort_flag, a.status)) return;
-                if (!wait_or_abort(&tempty[b], ((n >> 1) & 1) ^ 1, abort_flag, a.status)) return;
+                if (!wait_or_abort(&tempty[b], ((n / NA) & 1) ^ 1, abort_flag, a.status)) return;
                 tc_fence_after();
                 const uint32_t a_addr = smem_u32(smem + (size_t)s * a.stage_bytes);
                 const uint32_t b_addr = a_addr + kTileEntries * DIM;
@@ -233,7 +271,6 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
                 for (int ks = 0; ks < DIM / 32; ++ks)
                     mma_f8(tmem + b * a.n_cols, smem_desc(a_addr + ks * 32, DIM), smem_desc(b_addr + ks * 32, DIM),
                            idesc, ks > 0);
-                mma_commit(&empty[s]);
                 mma_commit(&tfull[b]);
             });
         }
@@ -242,43 +279,41 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
         const int quad = warp & 3;  // TMEM lanes this warp may access
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        for_each_item(a, abort_flag, [&](int n, const GroupInfo& gi, int t) {
-            const int b = n & 1;
-            const bool ok = wait_or_abort(&tfull[b], (n >> 1) & 1, abort_flag, a.status);
+        for_each_item(a, abort_flag, [&](int n, const GroupInfo&, int) {
+            const int s = n % S, b = n % NA;
+            const bool ok = wait_or_abort(&tfull[b], (n / NA) & 1, abort_flag, a.status);
             if (!__all_sync(0xffffffffu, ok)) return;  // warp-uniform: tcgen05.ld is warp-collective
             tc_fence_after();
-            const int e = t * kTileEntries + row;
-            const int lp = 2 * t + row / kPage;
-            int blk = -1;
-            if (lp * kPage < gi.max_vis && lp < a.bt.max_blocks) {
-                blk = a.bt.table[(long long)gi.r * a.bt.max_blocks + lp];
-                if (blk >= a.num_blocks) blk = -1;
-            }
-            const float sk = blk >= 0 ? a.key_scale[(long long)blk * kPage + (row % kPage)] : 0.f;
-            const int q0 = gi.g * a.q_group;
-            const int nqg = min(a.q_group, a.nq - q0);
-            float acc_q = 0.f;
+            const uint8_t* st = smem + (size_t)s * a.stage_bytes;
+            const StageMeta* meta = reinterpret_cast<const StageMeta*>(st + tiles_bytes);
+            const float* sscale = reinterpret_cast<const float*>(st + tiles_bytes + meta_bytes());
+            const float* sw = sscale + kTileEntries;
+            const float* ssq = sw + a.n_cols;
+            const bool page_ok = meta->blk[row / kPage] >= 0;
+            const float sk = page_ok ? sscale[row] : 0.f;
+            const int e = meta->e0 + row;
+            const int nqg = meta->nq, q0 = meta->q0;
             for (int c0 = 0; c0 < a.n_cols; c0 += 16) {
                 float v[16];
                 tmem_ld16(lane_base + b * a.n_cols + c0, v);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int c = c0 + i;
-                    const int j = c / a.heads;
+                for (int jj = 0; jj < 16 / HEADS; ++jj) {
+                    const int j = c0 / HEADS + jj;
                     if (j < nqg) {
-                        const long long qh = (long long)q0 * a.heads + c;
-                        acc_q += __ldg(a.w + qh) * fmaxf(0.f, __ldg(a.q_scale + qh) * sk * v[i]);
-                    }
-                    if ((c + 1) % a.heads == 0) {
-                        if (j < nqg && e < a.ld)
-                            a.scores[(long long)(q0 + j) * a.ld + e] =
-                                (blk >= 0 && e < visible_of(a, q0 + j)) ? acc_q : -INFINITY;
-                        acc_q = 0.f;
+                        float acc = 0.f;
+#pragma unroll
+                        for (int h = 0; h < HEADS; ++h) {
+                            const int c = c0 + jj * HEADS + h;
+                            acc += sw[c] * fmaxf(0.f, ssq[c] * sk * v[jj * HEADS + h]);
+                        }
+                        if (e < a.ld)
+                            a.scores[(long long)(q0 + j) * a.ld + e] = (page_ok && e < meta->nvis[j]) ? acc : -INFINITY;
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive(&tempty[b]);
+            mbar_arrive(&empty[s]);
         });
     }
     tc_fence_before();
@@ -310,19 +345,31 @@ static bool make_map(CUtensorMap* map, const void* base, uint64_t rows, int dim,
     return res == CUDA_SUCCESS;
 }
 
-template <int DIM>
+template <int DIM, int HEADS>
 static dsa_status_t launch_index(const CUtensorMap& kmap, const CUtensorMap& qmap, IdxArgs a, cudaStream_t st) {
-    // stage = 128 key rows + the query tile; ~96-192 KB of stages per SM keeps enough bytes in flight
-    a.stage_bytes = ((kTileEntries + a.n_cols) * DIM + 1023) / 1024 * 1024;
+    // stage = key tile + query tile + metadata + scales/weights; ~100-200 KB of stages per SM
+    const int payload = (kTileEntries + a.n_cols) * DIM + meta_bytes() + (kTileEntries + 2 * a.n_cols) * 4;
+    a.stage_bytes = (payload + 1023) / 1024 * 1024;
     const int ctas_per_sm = a.stage_bytes <= 24 * 1024 ? 2 : 1;
-    const int budget = 227 * 1024 / ctas_per_sm - 1024 - 256;
-    a.stages = max(2, min(8, budget / a.stage_bytes));
-    const int smem = 1024 + a.stages * a.stage_bytes + 256;
-    if (cudaFuncSetAttribute(index_kernel<DIM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    const int extra = 1024 + 512;  // alignment slack + barriers and the producer's cache
+    a.stages = max(2, min(8, (227 * 1024 / ctas_per_sm - extra) / a.stage_bytes));
+    const int smem = extra + a.stages * a.stage_bytes;
+    if (cudaFuncSetAttribute(index_kernel<DIM, HEADS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
         return DSA_ERR_CUDA;
     const long long grid = std::min<long long>(a.n_chunks, (long long)sm_count() * ctas_per_sm);
-    index_kernel<DIM><<<(unsigned)std::max<long long>(grid, 1), kIdxThreads, smem, st>>>(kmap, qmap, a);
+    index_kernel<DIM, HEADS><<<(unsigned)std::max<long long>(grid, 1), kIdxThreads, smem, st>>>(kmap, qmap, a);
     return launch_status();
+}
+
+template <int DIM>
+static dsa_status_t launch_index_heads(const CUtensorMap& kmap, const CUtensorMap& qmap, const IdxArgs& a,
+                                       cudaStream_t st) {
+    switch (a.heads) {
+        case 4: return launch_index<DIM, 4>(kmap, qmap, a, st);
+        case 8: return launch_index<DIM, 8>(kmap, qmap, a, st);
+        default: return launch_index<DIM, 16>(kmap, qmap, a, st);
+    }
 }
 
 }  // namespace dsa
@@ -343,14 +390,17 @@ extern "C" dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim,
         return DSA_ERR_INVALID_ARG;
     if (!pool_ok(keys) || keys->dtype != DSA_FP8_E4M3 || keys->dim != dim || keys->rows_per_block != kPage)
         return DSA_ERR_INVALID_ARG;
-    if (!aligned(q8, 16)) return DSA_ERR_INVALID_ARG;
+    if (!aligned(q8, 16) || !aligned(q_scale, 16) || !aligned(w, 16)) return DSA_ERR_INVALID_ARG;
+    if (q_group > 64) return DSA_ERR_INVALID_ARG;
     const int n_cols = ((q_group * heads + 15) / 16) * 16;  // M = 128 needs N % 16 == 0
     IdxArgs a{};
     a.nq = nq;
     a.heads = heads;
     a.q_group = q_group;
     a.n_cols = n_cols;
-    a.tmem_cols = 2 * n_cols <= 32 ? 32 : (2 * n_cols <= 64 ? 64 : (2 * n_cols <= 128 ? 128 : (2 * n_cols <= 256 ? 256 : 512)));
+    a.n_acc = n_cols <= 128 ? 4 : 2;  // TMEM accumulators in flight (at most 512 columns)
+    a.tmem_cols = 32;
+    while (a.tmem_cols < a.n_acc * n_cols) a.tmem_cols *= 2;
     a.ld = ld;
     a.q_scale = q_scale;
     a.w = w;
@@ -370,5 +420,5 @@ extern "C" dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim,
     a.total_items = (long long)a.tiles * a.n_groups;
     a.n_chunks = (a.total_items + kChunkItems - 1) / kChunkItems;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return dim == 128 ? launch_index<128>(kmap, qmap, a, st) : launch_index<64>(kmap, qmap, a, st);
+    return dim == 128 ? launch_index_heads<128>(kmap, qmap, a, st) : launch_index_heads<64>(kmap, qmap, a, st);
 }

@@ -67,6 +67,27 @@ __device__ __forceinline__ void block_scan2(uint32_t a, uint32_t b, uint32_t* ex
     __syncthreads();
 }
 
+// Histogram increment aggregated over the warp's lanes that hit the same bin (scores cluster in a
+// few exponent buckets, so plain shared-memory atomics would serialise).
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin) {
+    const unsigned active = __activemask();
+    const unsigned peers = __match_any_sync(active, bin);
+    if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+}
+
+// Append `key` to a shared list when `take`, one atomic per warp.
+__device__ __forceinline__ void list_append(uint32_t* list, uint32_t* count, bool take, uint32_t key) {
+    const unsigned active = __activemask();
+    const unsigned ballot = __ballot_sync(active, take);
+    if (!ballot) return;
+    const int lane = threadIdx.x & 31;
+    const int leader = __ffs(ballot) - 1;
+    uint32_t base = 0;
+    if (lane == leader) base = atomicAdd(count, (uint32_t)__popc(ballot));
+    base = __shfl_sync(active, base, leader);
+    if (take) list[base + __popc(ballot & ((1u << lane) - 1u))] = key;
+}
+
 struct SelectState {
     uint32_t prefix, mask, need;
 };
@@ -142,7 +163,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     __syncthreads();
 
     // digit 1: bits 31..21 over the whole row
-    for (int i = tid; i < n; i += kTopkThreads) atomicAdd(&hist[key_at(i) >> 21], 1u);
+    for (int i = tid; i < n; i += kTopkThreads) hist_add(hist, key_at(i) >> 21);
     __syncthreads();
     SelectState st{0u, 0u, (uint32_t)k};
     bool done = select_bucket(hist, 21, 0x7FFu, st, warp_tot, sel);
@@ -152,7 +173,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
         if (use_cand) {
             for (int i = tid; i < n; i += kTopkThreads) {
                 const uint32_t key = key_at(i);
-                if ((key & st.mask) == st.prefix) cand[atomicAdd(&n_cand, 1u)] = key;
+                list_append(cand, &n_cand, (key & st.mask) == st.prefix, key);
             }
         }
         for (int pass = 0; pass < 2 && !done; ++pass) {
@@ -170,7 +191,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
             } else {
                 for (int i = tid; i < n; i += kTopkThreads) {
                     const uint32_t key = key_at(i);
-                    if ((key & st.mask) == st.prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
+                    if ((key & st.mask) == st.prefix) hist_add(hist, (key >> sh) & dm);
                 }
             }
             __syncthreads();

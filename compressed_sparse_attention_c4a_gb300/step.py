@@ -56,17 +56,27 @@ class LayerStep:
         self.workspace = torch.empty((max(ws, 256),), dtype=torch.uint8, device=dev) if ws else None
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
         self.max_new = max(spec.new) if spec.new else 0
+        self.side = None
 
     # ---- stages ------------------------------------------------------------------------
-    def compress(self):
+    def compress_main(self):
+        """Main-cache compressor + SWA insert."""
         c = self.case
         dsa.dsa_compress(self.kind, c["cu_new"], c["start_pos"], self.max_new, c["x_new"], c["z_new"], c["state_x"],
                          c["state_z"], c["state_slot"], self.rope_main, self.main, self.main_bt, self.swa,
                          self.swa_bt, dev_status=self.status)
+
+    def compress_index(self):
+        """Indexer-cache compressor (fp8 keys + scale)."""
+        c = self.case
         if self.has_index and self.spec.index_compress:
             dsa.dsa_compress(self.kind, c["cu_new"], c["start_pos"], self.max_new, c["xi_new"], c["zi_new"],
                              c["state_xi"], c["state_zi"], c["state_slot"], self.rope_idx, self.idx, self.idx_bt,
                              dev_status=self.status)
+
+    def compress(self):
+        self.compress_main()
+        self.compress_index()
 
     def index(self):
         c = self.case
@@ -100,10 +110,25 @@ class LayerStep:
         return n
 
     def run(self):
-        """The whole step: compress (+SWA insert), index, top-k, attention with inverse RoPE."""
-        self.compress()
-        if self.has_index:
-            self.index()
-            self.select()
+        """The whole step: compress (+SWA insert), index, top-k, attention with inverse RoPE.
+
+        Two streams, as in the pages' multi-stream layout: the main-cache compressor and SWA insert
+        run on a side stream while the indexer chain (indexer compressor -> scores -> top-k) runs on
+        the current one; attention waits for both.  Captured into a CUDA graph this is a fork/join.
+        """
+        if not self.has_index:
+            self.compress_main()
+            self.attend()
+            return self.out
+        cur = torch.cuda.current_stream()
+        if self.side is None:
+            self.side = torch.cuda.Stream(device=cur.device)
+        self.side.wait_stream(cur)
+        with torch.cuda.stream(self.side):
+            self.compress_main()
+        self.compress_index()
+        self.index()
+        self.select()
+        cur.wait_stream(self.side)
         self.attend()
         return self.out
