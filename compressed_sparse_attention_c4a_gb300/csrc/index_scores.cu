@@ -22,7 +22,7 @@ namespace dsa {
 constexpr int kIdxThreads = 192;  // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
 constexpr int kTileEntries = 128;
 constexpr int kPage = 64;         // c4a entries per 256-position block
-constexpr int kChunkItems = 4;    // consecutive tiles of one group handled back to back by one CTA
+constexpr int kChunkItems = 8;    // consecutive tiles of one group handled back to back by one CTA
 
 struct IdxArgs {
     int nq, heads, q_group, n_cols, tmem_cols, ld;
@@ -96,46 +96,56 @@ __device__ __forceinline__ int visible_at(int m) { return m < 7 ? 0 : ((m - 7) >
 
 __device__ __forceinline__ int visible_of(const IdxArgs& a, int q) { return visible_at(a.q_pos[q]); }
 
-// Group g = queries [g * q_group, ...) of one request: its request id (or -1 if the group mixes
-// requests or names a request beyond the table) and the largest visible-entry count.
-struct GroupInfo {
-    int g, r, max_vis;
+// Item = one 128-entry tile of one query group.  Its request, visibility and the physical blocks of
+// its two 64-entry pages, resolved by one producer lane.
+struct ItemInfo {
+    int valid, g, t, r, max_vis, blk0, blk1;
 };
 
-__device__ __forceinline__ GroupInfo group_info(const IdxArgs& a, int g) {
-    const int q0 = g * a.q_group;
+__device__ __forceinline__ ItemInfo item_info(const IdxArgs& a, long long it) {
+    ItemInfo x{0, 0, 0, -1, 0, -1, -1};
+    if (it >= a.total_items) return x;
+    x.g = (int)(it / a.tiles);
+    x.t = (int)(it % a.tiles);
+    const int q0 = x.g * a.q_group;
     const int nqg = min(a.q_group, a.nq - q0);
-    GroupInfo gi{g, a.q_req[q0], 0};
+    x.r = a.q_req[q0];
     for (int j = 0; j < nqg; ++j) {
-        gi.max_vis = max(gi.max_vis, visible_of(a, q0 + j));
-        if (a.q_req[q0 + j] != gi.r) gi.r = -1;
+        x.max_vis = max(x.max_vis, visible_of(a, q0 + j));
+        if (a.q_req[q0 + j] != x.r) x.r = -1;
     }
-    if (gi.r < 0 || gi.r >= a.bt.batch) gi.r = -1;
-    return gi;
+    if (x.r < 0 || x.r >= a.bt.batch) {
+        report(a.status, DSA_ERR_DEVICE_FAULT);
+        return x;
+    }
+    if (x.t * kTileEntries >= x.max_vis) return x;
+    x.valid = 1;
+    int blk[2] = {-1, -1};
+    for (int pi = 0; pi < 2; ++pi) {
+        const int lp = 2 * x.t + pi;
+        if (lp * kPage >= x.max_vis) continue;
+        const int b = lp < a.bt.max_blocks ? a.bt.table[(long long)x.r * a.bt.max_blocks + lp] : -1;
+        if (b < 0 || b >= a.num_blocks) {
+            report(a.status, DSA_ERR_DEVICE_FAULT);
+            continue;
+        }
+        blk[pi] = b;
+    }
+    x.blk0 = blk[0];
+    x.blk1 = blk[1];
+    return x;
 }
 
-// Every role walks the same sequence of valid items: chunks of kChunkItems consecutive tiles of the
-// rectangular (group x tile) space, chunk c going to CTA c mod gridDim.x; a tile is valid when it
-// holds at least one entry visible to some query of its group.
-template <typename F>
-__device__ __forceinline__ void for_each_item(const IdxArgs& a, volatile int* abort_flag, F&& fn) {
-    int n = 0;
-    GroupInfo gi{-1, -1, 0};
-    for (long long ch = blockIdx.x; ch < a.n_chunks; ch += gridDim.x) {
-        for (int u = 0; u < kChunkItems; ++u) {
-            const long long it = ch * kChunkItems + u;
-            if (it >= a.total_items) break;
-            if (*abort_flag) return;
-            const int g = (int)(it / a.tiles), t = (int)(it % a.tiles);
-            if (g != gi.g) {
-                gi = group_info(a, g);
-                if (gi.r < 0) report(a.status, DSA_ERR_DEVICE_FAULT);
-            }
-            if (gi.r < 0 || t * kTileEntries >= gi.max_vis) continue;
-            fn(n, gi, t);
-            ++n;
-        }
-    }
+__device__ __forceinline__ ItemInfo shfl_item(const ItemInfo& x, int src) {
+    ItemInfo y;
+    y.valid = __shfl_sync(0xffffffffu, x.valid, src);
+    y.g = __shfl_sync(0xffffffffu, x.g, src);
+    y.t = __shfl_sync(0xffffffffu, x.t, src);
+    y.r = __shfl_sync(0xffffffffu, x.r, src);
+    y.max_vis = __shfl_sync(0xffffffffu, x.max_vis, src);
+    y.blk0 = __shfl_sync(0xffffffffu, x.blk0, src);
+    y.blk1 = __shfl_sync(0xffffffffu, x.blk1, src);
+    return y;
 }
 
 // Bounded wait that also gives up once another role has aborted.
@@ -155,10 +165,12 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 }
 
 // Per-stage layout (bytes from the stage start): key tile [128][DIM] (swizzled), query tile
-// [n_cols][DIM] (swizzled), then StageMeta, then fp32 entry scales [128], head weights [n_cols] and
-// query scales [n_cols] (bulk copies).  The stage is released by the epilogue, so everything the
-// epilogue reads stays in shared memory until it is done.
+// [n_cols][DIM] (swizzled), StageMeta, then fp32 entry scales [128], head weights [n_cols] and query
+// scales [n_cols] (bulk copies).  Only the producer walks the work list; it describes each item in its
+// stage (or posts a terminal stage), so the MMA and epilogue roles never touch global metadata.  The
+// epilogue releases the stage, so everything it reads stays in shared memory until it is done.
 struct StageMeta {
+    int terminal;  // 1: no more items for this CTA
     int blk[2];    // physical block of each 64-entry page, -1 if not loaded
     int nq;        // queries in the group
     int q0;        // first query of the group
@@ -181,9 +193,10 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
     uint64_t* tempty = tfull + 4;  // [NA]
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(s_tmem + 1);
-    int* grp_nvis = reinterpret_cast<int*>(s_tmem + 2);  // producer-private cache [64]
+    int* grp_nvis = reinterpret_cast<int*>(s_tmem + 2);  // producer warp's cache [64]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    auto stage_meta = [&](int s) { return reinterpret_cast<StageMeta*>(smem + (size_t)s * a.stage_bytes + tiles_bytes); };
 
     // visible-entry count of every query (grid-strided, independent of the tile loop)
     if (a.n_visible)
@@ -209,61 +222,87 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
     const uint32_t tmem = *s_tmem;
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ---- producer: two key pages, scales, the group's query tile, weights and scales --------
-            int cached_g = -1;
-            for_each_item(a, abort_flag, [&](int n, const GroupInfo& gi, int t) {
-                const int s = n % S;
-                if (!wait_or_abort(&empty[s], ((n / S) & 1) ^ 1, abort_flag, a.status)) return;
-                uint8_t* st = smem + (size_t)s * a.stage_bytes;
-                StageMeta* meta = reinterpret_cast<StageMeta*>(st + tiles_bytes);
-                float* sscale = reinterpret_cast<float*>(st + tiles_bytes + meta_bytes());
-                float* sw = sscale + kTileEntries;
-                float* ssq = sw + a.n_cols;
-                const int q0 = gi.g * a.q_group;
+        // ---- producer warp: lanes resolve a chunk's items (next chunk prefetched), lane 0 issues TMA ----
+        int n = 0, cached_g = -1;
+        long long ch = blockIdx.x;
+        ItemInfo cur = item_info(a, lane < kChunkItems && ch < a.n_chunks ? ch * kChunkItems + lane : a.total_items);
+        bool alive = true;
+        while (ch < a.n_chunks && alive) {
+            const long long nch = ch + gridDim.x;
+            const ItemInfo nxt =
+                item_info(a, lane < kChunkItems && nch < a.n_chunks ? nch * kChunkItems + lane : a.total_items);
+            for (int u = 0; u < kChunkItems; ++u) {
+                const ItemInfo it = shfl_item(cur, u);
+                if (!it.valid) continue;
+                const int q0 = it.g * a.q_group;
                 const int nqg = min(a.q_group, a.nq - q0);
-                if (gi.g != cached_g) {
-                    for (int j = 0; j < nqg; ++j) grp_nvis[j] = visible_of(a, q0 + j);
-                    cached_g = gi.g;
+                if (a.q_group > 1 && it.g != cached_g) {  // per-query visibility of a multi-query group
+                    for (int j = lane; j < nqg; j += 32) grp_nvis[j] = visible_of(a, q0 + j);
+                    __syncwarp();
+                    cached_g = it.g;
                 }
-                uint32_t bytes = (uint32_t)a.n_cols * DIM + 2u * nqg * HEADS * 4u;
-                for (int pi = 0; pi < 2; ++pi) {
-                    const int lp = 2 * t + pi;
-                    int b = -1;
-                    if (lp * kPage < gi.max_vis) {
-                        b = lp < a.bt.max_blocks ? a.bt.table[(long long)gi.r * a.bt.max_blocks + lp] : -1;
-                        if (b < 0 || b >= a.num_blocks) {
-                            report(a.status, DSA_ERR_DEVICE_FAULT);
-                            b = -1;
+                if (lane == 0) {
+                    const int s = n % S;
+                    if (!wait_or_abort(&empty[s], ((n / S) & 1) ^ 1, abort_flag, a.status)) {
+                        alive = false;
+                    } else {
+                        uint8_t* st = smem + (size_t)s * a.stage_bytes;
+                        StageMeta* meta = stage_meta(s);
+                        float* sscale = reinterpret_cast<float*>(st + tiles_bytes + meta_bytes());
+                        float* sw = sscale + kTileEntries;
+                        float* ssq = sw + a.n_cols;
+                        meta->terminal = 0;
+                        meta->blk[0] = it.blk0;
+                        meta->blk[1] = it.blk1;
+                        meta->nq = nqg;
+                        meta->q0 = q0;
+                        meta->e0 = it.t * kTileEntries;
+                        if (a.q_group == 1) meta->nvis[0] = it.max_vis;
+                        else
+                            for (int j = 0; j < nqg; ++j) meta->nvis[j] = grp_nvis[j];
+                        const uint32_t bytes = (uint32_t)a.n_cols * DIM + 2u * nqg * HEADS * 4u +
+                                               (it.blk0 >= 0 ? kPage * (DIM + 4) : 0) +
+                                               (it.blk1 >= 0 ? kPage * (DIM + 4) : 0);
+                        mbar_arrive_expect_tx(&full[s], bytes);  // release: the meta writes above are visible
+                        if (it.blk0 >= 0) {
+                            tma_load_2d(st, &kmap, 0, it.blk0 * kPage, &full[s]);
+                            bulk_g2s(sscale, a.key_scale + (long long)it.blk0 * kPage, kPage * 4, &full[s]);
                         }
+                        if (it.blk1 >= 0) {
+                            tma_load_2d(st + kPage * DIM, &kmap, 0, it.blk1 * kPage, &full[s]);
+                            bulk_g2s(sscale + kPage, a.key_scale + (long long)it.blk1 * kPage, kPage * 4, &full[s]);
+                        }
+                        tma_load_2d(st + kTileEntries * DIM, &qmap, 0, q0 * HEADS, &full[s]);
+                        bulk_g2s(sw, a.w + (long long)q0 * HEADS, nqg * HEADS * 4, &full[s]);
+                        bulk_g2s(ssq, a.q_scale + (long long)q0 * HEADS, nqg * HEADS * 4, &full[s]);
                     }
-                    meta->blk[pi] = b;
-                    if (b >= 0) bytes += kPage * DIM + kPage * 4;
                 }
-                meta->nq = nqg;
-                meta->q0 = q0;
-                meta->e0 = t * kTileEntries;
-                for (int j = 0; j < nqg; ++j) meta->nvis[j] = grp_nvis[j];
-                mbar_arrive_expect_tx(&full[s], bytes);  // release: the meta writes above are visible
-                for (int pi = 0; pi < 2; ++pi) {
-                    const int b = meta->blk[pi];
-                    if (b < 0) continue;
-                    tma_load_2d(st + pi * kPage * DIM, &kmap, 0, b * kPage, &full[s]);
-                    bulk_g2s(sscale + pi * kPage, a.key_scale + (long long)b * kPage, kPage * 4, &full[s]);
-                }
-                tma_load_2d(st + kTileEntries * DIM, &qmap, 0, q0 * HEADS, &full[s]);
-                bulk_g2s(sw, a.w + (long long)q0 * HEADS, nqg * HEADS * 4, &full[s]);
-                bulk_g2s(ssq, a.q_scale + (long long)q0 * HEADS, nqg * HEADS * 4, &full[s]);
-            });
+                alive = __shfl_sync(0xffffffffu, alive, 0);
+                if (!alive) break;
+                ++n;
+            }
+            cur = nxt;
+            ch = nch;
+        }
+        if (lane == 0 && alive) {  // terminal stage: consumers stop here
+            const int s = n % S;
+            if (wait_or_abort(&empty[s], ((n / S) & 1) ^ 1, abort_flag, a.status)) {
+                stage_meta(s)->terminal = 1;
+                mbar_arrive(&full[s]);
+            }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ---- MMA issuer: D[entry][q*heads + h] = <k8_entry, q8_(q,h)>, accumulated over dim ------
             const uint32_t idesc = idesc_f8(a.n_cols);
-            for_each_item(a, abort_flag, [&](int n, const GroupInfo&, int) {
+            for (int n = 0;; ++n) {
                 const int s = n % S, b = n % NA;
-                if (!wait_or_abort(&full[s], (n / S) & 1, abort_flag, a.status)) return;
-                if (!wait_or_abort(&tempty[b], ((n / NA) & 1) ^ 1, abort_flag, a.status)) return;
+                if (!wait_or_abort(&full[s], (n / S) & 1, abort_flag, a.status)) break;
+                if (!wait_or_abort(&tempty[b], ((n / NA) & 1) ^ 1, abort_flag, a.status)) break;
+                if (stage_meta(s)->terminal) {
+                    mbar_arrive(&tfull[b]);
+                    break;
+                }
                 tc_fence_after();
                 const uint32_t a_addr = smem_u32(smem + (size_t)s * a.stage_bytes);
                 const uint32_t b_addr = a_addr + kTileEntries * DIM;
@@ -272,20 +311,22 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
                     mma_f8(tmem + b * a.n_cols, smem_desc(a_addr + ks * 32, DIM), smem_desc(b_addr + ks * 32, DIM),
                            idesc, ks > 0);
                 mma_commit(&tfull[b]);
-            });
+            }
         }
     } else {
         // ---- epilogue: TMEM lane <-> entry; ReLU, scales, head weights, causal mask -------------------
         const int quad = warp & 3;  // TMEM lanes this warp may access
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        for_each_item(a, abort_flag, [&](int n, const GroupInfo&, int) {
+        for (int n = 0;; ++n) {
             const int s = n % S, b = n % NA;
-            const bool ok = wait_or_abort(&tfull[b], (n / NA) & 1, abort_flag, a.status);
-            if (!__all_sync(0xffffffffu, ok)) return;  // warp-uniform: tcgen05.ld is warp-collective
+            bool ok = wait_or_abort(&tfull[b], (n / NA) & 1, abort_flag, a.status);
+            ok = ok && wait_or_abort(&full[s], (n / S) & 1, abort_flag, a.status);  // completed: orders the meta
+            if (!__all_sync(0xffffffffu, ok)) break;  // warp-uniform: tcgen05.ld is warp-collective
+            const StageMeta* meta = stage_meta(s);
+            if (meta->terminal) break;
             tc_fence_after();
             const uint8_t* st = smem + (size_t)s * a.stage_bytes;
-            const StageMeta* meta = reinterpret_cast<const StageMeta*>(st + tiles_bytes);
             const float* sscale = reinterpret_cast<const float*>(st + tiles_bytes + meta_bytes());
             const float* sw = sscale + kTileEntries;
             const float* ssq = sw + a.n_cols;
@@ -314,7 +355,7 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
             tc_fence_before();
             mbar_arrive(&tempty[b]);
             mbar_arrive(&empty[s]);
-        });
+        }
     }
     tc_fence_before();
     __syncthreads();
