@@ -102,27 +102,31 @@ struct ItemInfo {
     int valid, g, t, r, max_vis, blk0, blk1;
 };
 
-__device__ __forceinline__ ItemInfo item_info(const IdxArgs& a, long long it) {
-    ItemInfo x{0, 0, 0, -1, 0, -1, -1};
-    if (it >= a.total_items) return x;
-    x.g = (int)(it / a.tiles);
-    x.t = (int)(it % a.tiles);
-    const int q0 = x.g * a.q_group;
+// Request and visible-entry bound of query group g (r = -1 if the group mixes requests or names a
+// request beyond the table).
+__device__ __forceinline__ void group_of(const IdxArgs& a, int g, int* r, int* max_vis) {
+    const int q0 = g * a.q_group;
     const int nqg = min(a.q_group, a.nq - q0);
-    x.r = a.q_req[q0];
+    int rr = a.q_req[q0], mv = 0;
     for (int j = 0; j < nqg; ++j) {
-        x.max_vis = max(x.max_vis, visible_of(a, q0 + j));
-        if (a.q_req[q0 + j] != x.r) x.r = -1;
+        mv = max(mv, visible_of(a, q0 + j));
+        if (a.q_req[q0 + j] != rr) rr = -1;
     }
-    if (x.r < 0 || x.r >= a.bt.batch) {
-        report(a.status, DSA_ERR_DEVICE_FAULT);
-        return x;
-    }
-    if (x.t * kTileEntries >= x.max_vis) return x;
+    if (rr >= a.bt.batch) rr = -1;
+    *r = rr;
+    *max_vis = mv;
+}
+
+// Item (g, t): tile t of group g; `valid` = 0 marks "no item".
+__device__ __forceinline__ ItemInfo item_info(const IdxArgs& a, int valid, int g, int t) {
+    ItemInfo x{0, g, t, -1, 0, -1, -1};
+    if (!valid) return x;
+    group_of(a, g, &x.r, &x.max_vis);
+    if (x.r < 0 || t * kTileEntries >= x.max_vis) return x;
     x.valid = 1;
     int blk[2] = {-1, -1};
     for (int pi = 0; pi < 2; ++pi) {
-        const int lp = 2 * x.t + pi;
+        const int lp = 2 * t + pi;
         if (lp * kPage >= x.max_vis) continue;
         const int b = lp < a.bt.max_blocks ? a.bt.table[(long long)x.r * a.bt.max_blocks + lp] : -1;
         if (b < 0 || b >= a.num_blocks) {
@@ -194,6 +198,7 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(s_tmem + 1);
     int* grp_nvis = reinterpret_cast<int*>(s_tmem + 2);  // producer warp's cache [64]
+    int* grp_prefix = grp_nvis + 64;                     // [n_groups + 1] valid tiles before each group
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     auto stage_meta = [&](int s) { return reinterpret_cast<StageMeta*>(smem + (size_t)s * a.stage_bytes + tiles_bytes); };
@@ -222,15 +227,57 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
     const uint32_t tmem = *s_tmem;
 
     if (warp == 0) {
-        // ---- producer warp: lanes resolve a chunk's items (next chunk prefetched), lane 0 issues TMA ----
+        // ---- producer warp ---------------------------------------------------------------------------
+        // Valid tiles per group -> prefix sums in shared memory; this CTA takes an equal contiguous
+        // share [lo, hi) of all valid (group, tile) items.  Lanes resolve items kChunkItems at a time
+        // (the next batch is prefetched while the current one is issued); lane 0 issues the copies.
+        int* pre = grp_prefix;
+        long long carry = 0;
+        for (int g0 = 0; g0 < a.n_groups; g0 += 32) {
+            const int g = g0 + lane;
+            int cnt = 0;
+            if (g < a.n_groups) {
+                int r, mv;
+                group_of(a, g, &r, &mv);
+                if (r < 0) report(a.status, DSA_ERR_DEVICE_FAULT);
+                else cnt = min((mv + kTileEntries - 1) / kTileEntries, a.tiles);
+            }
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (g < a.n_groups) pre[g] = (int)(carry + incl - cnt);
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) pre[a.n_groups] = (int)carry;
+        __syncwarp();
+        const long long V = carry;
+        const long long lo = V * blockIdx.x / gridDim.x, hi = V * (blockIdx.x + 1) / gridDim.x;
+        // item index -> (group, tile) by binary search over the prefix
+        auto locate = [&](long long idx, int* g, int* t) {
+            int l = 0, h = a.n_groups - 1;
+            while (l < h) {
+                const int mid = (l + h + 1) >> 1;
+                if (pre[mid] <= idx) l = mid;
+                else h = mid - 1;
+            }
+            *g = l;
+            *t = (int)(idx - pre[l]);
+        };
+        auto resolve = [&](long long base) {
+            const long long idx = base + lane;
+            int g = 0, t = 0;
+            const int valid = lane < kChunkItems && idx < hi;
+            if (valid) locate(idx, &g, &t);
+            return item_info(a, valid, g, t);
+        };
         int n = 0, cached_g = -1;
-        long long ch = blockIdx.x;
-        ItemInfo cur = item_info(a, lane < kChunkItems && ch < a.n_chunks ? ch * kChunkItems + lane : a.total_items);
         bool alive = true;
-        while (ch < a.n_chunks && alive) {
-            const long long nch = ch + gridDim.x;
-            const ItemInfo nxt =
-                item_info(a, lane < kChunkItems && nch < a.n_chunks ? nch * kChunkItems + lane : a.total_items);
+        ItemInfo cur = resolve(lo);
+        for (long long base = lo; base < hi && alive; base += kChunkItems) {
+            const ItemInfo nxt = resolve(base + kChunkItems);
             for (int u = 0; u < kChunkItems; ++u) {
                 const ItemInfo it = shfl_item(cur, u);
                 if (!it.valid) continue;
@@ -282,7 +329,6 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
                 ++n;
             }
             cur = nxt;
-            ch = nch;
         }
         if (lane == 0 && alive) {  // terminal stage: consumers stop here
             const int s = n % S;
@@ -392,13 +438,14 @@ static dsa_status_t launch_index(const CUtensorMap& kmap, const CUtensorMap& qma
     const int payload = (kTileEntries + a.n_cols) * DIM + meta_bytes() + (kTileEntries + 2 * a.n_cols) * 4;
     a.stage_bytes = (payload + 1023) / 1024 * 1024;
     const int ctas_per_sm = a.stage_bytes <= 24 * 1024 ? 2 : 1;
-    const int extra = 1024 + 512;  // alignment slack + barriers and the producer's cache
+    // alignment slack + barriers, the producer's caches and the per-group prefix of valid tiles
+    const int extra = 1024 + 512 + ((a.n_groups + 1) * 4 + 15) / 16 * 16;
     a.stages = max(2, min(8, (227 * 1024 / ctas_per_sm - extra) / a.stage_bytes));
     const int smem = extra + a.stages * a.stage_bytes;
     if (cudaFuncSetAttribute(index_kernel<DIM, HEADS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
         return DSA_ERR_CUDA;
-    const long long grid = std::min<long long>(a.n_chunks, (long long)sm_count() * ctas_per_sm);
+    const long long grid = std::min<long long>(a.total_items, (long long)sm_count() * ctas_per_sm);
     index_kernel<DIM, HEADS><<<(unsigned)std::max<long long>(grid, 1), kIdxThreads, smem, st>>>(kmap, qmap, a);
     return launch_status();
 }
@@ -433,6 +480,7 @@ extern "C" dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim,
         return DSA_ERR_INVALID_ARG;
     if (!aligned(q8, 16) || !aligned(q_scale, 16) || !aligned(w, 16)) return DSA_ERR_INVALID_ARG;
     if (q_group > 64) return DSA_ERR_INVALID_ARG;
+    if ((nq + q_group - 1) / q_group > 16384) return DSA_ERR_UNSUPPORTED;  // per-group prefix lives in smem
     const int n_cols = ((q_group * heads + 15) / 16) * 16;  // M = 128 needs N % 16 == 0
     IdxArgs a{};
     a.nq = nq;

@@ -3,24 +3,29 @@
 // [P1] "DeepSeek DSA、DeepSeek V4与vLLM Hybrid KV Cache详解" §4.2: S_t = TopK(I_{t,:}, k); the
 // main attention reads only S_t.  [P2] "DeepSeek V4 稀疏注意力完全解剖" 机制三: k = 512 for c4a.
 //
-// One CTA (1024 threads) per query row; scores become order-preserving uint32 keys.
-//   1. The row is read once (coalesced, 16-byte loads) into shared memory when it fits (rows up to
-//      40,960 entries; longer rows are re-read from L2 in each pass).
-//   2. Radix select of the k-th largest key: an 11-bit histogram over the row picks the bucket that
-//      holds it; the keys of that bucket (typically a few hundred) are gathered into a candidate
-//      list and the remaining 11 + 10 bits are resolved on the candidates only.  The select stops
-//      early as soon as a bucket holds exactly the elements still needed.
-//   3. One pass compacts the selection in increasing index order: thread t owns a contiguous run
-//      of indices (of odd length, so shared-memory reads are bank-conflict free), and one block
-//      scan both ranks tied keys by index (lowest indices win) and gives every selected index
-//      its output slot.
+// One CTA (1024 threads) per query row.
+//   1. The row is read once (coalesced 16-byte loads) into shared memory when it fits (rows up to
+//      40,960 entries; longer rows are re-read from L2 in each pass).  Its finite max M and min m are
+//      reduced.
+//   2. Bucket select: bin(v) = 2047 - floor((M - v) * 2046 / (M - m)) for finite v, bin(-inf) = 0.  The
+//      map is monotone (larger score -> same or larger bin; equal scores share a bin) and spreads
+//      scores evenly, so one shared-memory histogram pass has little atomic contention.  A suffix
+//      scan finds the bin b* holding the k-th largest score and `need`, the count still missing.
+//   3. Inside b*: when it holds at most 1024 scores, each candidate is ranked directly against the
+//      others (larger score first, lower index first among equals) and the `need` best are marked in
+//      a bitmap.  Otherwise (heavy ties) a radix select on the 32-bit order keys of the candidates
+//      finds the exact threshold key T and the number of entries equal to T still needed.
+//   4. One pass compacts the selection in increasing index order: thread t owns a contiguous run of
+//      indices (odd length: bank-conflict-free shared-memory reads) and a block scan gives every
+//      selected index its slot; the scan also ranks entries equal to T by index (lowest wins).
 #include "common.cuh"
 
 namespace dsa {
 
 constexpr int kTopkThreads = 1024;
 constexpr int kBins = 2048;
-constexpr int kCandMax = 8192;
+constexpr int kCandMax = 8192;   // candidate keys kept for the radix path
+constexpr int kRankMax = 1024;   // candidates ranked directly (one per thread)
 constexpr int kResidentMax = 40960;
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -67,71 +72,46 @@ __device__ __forceinline__ void block_scan2(uint32_t a, uint32_t b, uint32_t* ex
     __syncthreads();
 }
 
-// Histogram increment aggregated over the warp's lanes that hit the same bin (scores cluster in a
-// few exponent buckets, so plain shared-memory atomics would serialise).
-__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin) {
-    const unsigned active = __activemask();
-    const unsigned peers = __match_any_sync(active, bin);
-    if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
-}
-
-// Append `key` to a shared list when `take`, one atomic per warp.
-__device__ __forceinline__ void list_append(uint32_t* list, uint32_t* count, bool take, uint32_t key) {
-    const unsigned active = __activemask();
-    const unsigned ballot = __ballot_sync(active, take);
-    if (!ballot) return;
-    const int lane = threadIdx.x & 31;
-    const int leader = __ffs(ballot) - 1;
-    uint32_t base = 0;
-    if (lane == leader) base = atomicAdd(count, (uint32_t)__popc(ballot));
-    base = __shfl_sync(active, base, leader);
-    if (take) list[base + __popc(ballot & ((1u << lane) - 1u))] = key;
-}
-
-struct SelectState {
-    uint32_t prefix, mask, need;
-};
-
-// Given a filled histogram of one digit, find the bucket holding the need-th largest remaining key.
-// Returns true when that bucket holds exactly the keys still needed (select finished).
-__device__ __forceinline__ bool select_bucket(const uint32_t* hist, int shift, uint32_t dmask, SelectState& st,
-                                              uint32_t (*warp_tot)[2], uint32_t* sel) {
+// Given a filled histogram, find the bin (scanning from the top) that holds the need-th largest
+// remaining element; need is reduced by the count above it.  Returns the bin.
+__device__ __forceinline__ uint32_t select_bin(const uint32_t* hist, uint32_t& need, uint32_t (*warp_tot)[2],
+                                               uint32_t* sel) {
     const int tid = threadIdx.x;
     const int b_hi = kBins - 1 - 2 * tid, b_lo = b_hi - 1;  // bins in descending order, two per thread
     const uint32_t c_hi = hist[b_hi], c_lo = hist[b_lo];
     uint32_t ex, ex2, tot, tot2;
     block_scan2(c_hi + c_lo, 0u, &ex, &ex2, &tot, &tot2, warp_tot);
-    if (ex < st.need && st.need <= ex + c_hi) {
+    if (ex < need && need <= ex + c_hi) {
         sel[0] = (uint32_t)b_hi;
         sel[1] = ex;
-    } else if (ex + c_hi < st.need && st.need <= ex + c_hi + c_lo) {
+    } else if (ex + c_hi < need && need <= ex + c_hi + c_lo) {
         sel[0] = (uint32_t)b_lo;
         sel[1] = ex + c_hi;
     }
     __syncthreads();
     const uint32_t b = sel[0];
-    st.need -= sel[1];
-    st.prefix |= b << shift;
-    st.mask |= dmask << shift;
-    const bool done = hist[b] == st.need;
+    need -= sel[1];
     __syncthreads();
-    return done;
+    return b;
 }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ scores, int ld,
+__global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float* __restrict__ scores, int ld,
                                                             const int32_t* __restrict__ n_valid, int k,
                                                             int32_t* __restrict__ idx_out, int32_t* status,
                                                             int resident) {
     extern __shared__ uint32_t smem_topk[];
-    uint32_t* hist = smem_topk;              // [kBins]
-    uint32_t* cand = hist + kBins;           // [kCandMax] keys of the selected bucket
-    uint32_t* rowk = cand + kCandMax;        // [ld] order keys of the row (resident mode)
+    uint32_t* hist = smem_topk;                  // [kBins]
+    uint32_t* cand_key = hist + kBins;           // [kCandMax]
+    uint32_t* cand_idx = cand_key + kCandMax;    // [kRankMax]
+    uint32_t* marks = cand_idx + kRankMax;       // [ld / 32 + 1] bitmap of ranked winners
+    float* rowv = reinterpret_cast<float*>(marks + (ld >> 5) + 1);  // [ld] the row (resident mode)
     __shared__ uint32_t warp_tot[32][2];
     __shared__ uint32_t sel[2];
     __shared__ uint32_t n_cand;
+    __shared__ float red_max[32], red_min[32];
 
     const int row = blockIdx.x;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     int32_t* out = idx_out + (long long)row * k;
     const int n = n_valid[row];
     if (n < 0 || n > ld) {
@@ -144,86 +124,177 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
         return;
     }
     const float* s = scores + (long long)row * ld;
+    float mx = -INFINITY, mn = INFINITY;
     if (resident) {
         for (int i = tid * 4; i < n; i += kTopkThreads * 4) {
+            float v[4];
             if (i + 4 <= n) {
                 const float4 q = *reinterpret_cast<const float4*>(s + i);
-                rowk[i] = order_key(q.x);
-                rowk[i + 1] = order_key(q.y);
-                rowk[i + 2] = order_key(q.z);
-                rowk[i + 3] = order_key(q.w);
+                v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
             } else {
-                for (int u = i; u < n; ++u) rowk[u] = order_key(s[u]);
+                for (int u = 0; u < 4; ++u) v[u] = i + u < n ? s[i + u] : -INFINITY;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (i + u < n) rowv[i + u] = v[u];
+                if (v[u] != -INFINITY) {
+                    mx = fmaxf(mx, v[u]);
+                    mn = fminf(mn, v[u]);
+                }
+            }
+        }
+    } else {
+        for (int i = tid; i < n; i += kTopkThreads) {
+            const float v = __ldg(s + i);
+            if (v != -INFINITY) {
+                mx = fmaxf(mx, v);
+                mn = fminf(mn, v);
             }
         }
     }
-    auto key_at = [&](int i) -> uint32_t { return resident ? rowk[i] : order_key(__ldg(s + i)); };
     for (int b = tid; b < kBins; b += kTopkThreads) hist[b] = 0;
+    for (int w = tid; w <= (ld >> 5); w += kTopkThreads) marks[w] = 0;
     if (tid == 0) n_cand = 0;
+    mx = warp_max(mx);
+    mn = -warp_max(-mn);
+    if (lane == 0) {
+        red_max[wid] = mx;
+        red_min[wid] = mn;
+    }
     __syncthreads();
+    mx = -INFINITY;
+    mn = INFINITY;
+#pragma unroll 8
+    for (int w = 0; w < 32; ++w) {
+        mx = fmaxf(mx, red_max[w]);
+        mn = fminf(mn, red_min[w]);
+    }
+    const bool any_finite = mx != -INFINITY;
+    const float scale = (any_finite && mx > mn) ? 2046.f / (mx - mn) : 0.f;
+    auto val_at = [&](int i) -> float { return resident ? rowv[i] : __ldg(s + i); };
+    auto bin_of = [&](float v) -> uint32_t {
+        if (v == -INFINITY) return 0u;
+        return 2047u - (uint32_t)fminf(2046.f, (mx - v) * scale);
+    };
 
-    // digit 1: bits 31..21 over the whole row
-    for (int i = tid; i < n; i += kTopkThreads) hist_add(hist, key_at(i) >> 21);
+    // 2. value-bucket histogram and the bucket of the k-th largest score
+    for (int i = tid; i < n; i += kTopkThreads) atomicAdd(&hist[bin_of(val_at(i))], 1u);
     __syncthreads();
-    SelectState st{0u, 0u, (uint32_t)k};
-    bool done = select_bucket(hist, 21, 0x7FFu, st, warp_tot, sel);
-    if (!done) {
-        const uint32_t bucket = hist[st.prefix >> 21];
-        const bool use_cand = bucket <= (uint32_t)kCandMax;
-        if (use_cand) {
+    uint32_t need = (uint32_t)k;
+    const uint32_t bstar = select_bin(hist, need, warp_tot, sel);
+    const uint32_t in_bucket = hist[bstar];
+    const bool take_all = in_bucket == need;
+    const bool rank_mode = !take_all && in_bucket <= (uint32_t)kRankMax;
+    uint32_t T = 0u, need_T = 0u;  // radix path: threshold key and entries equal to it still needed
+
+    // 3. resolve the bucket
+    if (!take_all) {
+        const bool keep = in_bucket <= (uint32_t)kCandMax;
+        if (rank_mode || keep) {
             for (int i = tid; i < n; i += kTopkThreads) {
-                const uint32_t key = key_at(i);
-                list_append(cand, &n_cand, (key & st.mask) == st.prefix, key);
+                const float v = val_at(i);
+                const bool take = bin_of(v) == bstar;
+                const unsigned active = __activemask();
+                const unsigned ballot = __ballot_sync(active, take);
+                if (ballot) {
+                    const int leader = __ffs(ballot) - 1;
+                    uint32_t base = 0;
+                    if (lane == leader) base = atomicAdd(&n_cand, (uint32_t)__popc(ballot));
+                    base = __shfl_sync(active, base, leader);
+                    if (take) {
+                        const uint32_t slot = base + __popc(ballot & ((1u << lane) - 1u));
+                        cand_key[slot] = order_key(v);
+                        if (rank_mode) cand_idx[slot] = (uint32_t)i;
+                    }
+                }
             }
+            __syncthreads();
         }
-        for (int pass = 0; pass < 2 && !done; ++pass) {
-            const int sh = pass == 0 ? 10 : 0;
-            const uint32_t dm = pass == 0 ? 0x7FFu : 0x3FFu;
-            __syncthreads();
-            for (int b = tid; b < kBins; b += kTopkThreads) hist[b] = 0;
-            __syncthreads();
-            if (use_cand) {
-                const int nc = (int)n_cand;
-                for (int i = tid; i < nc; i += kTopkThreads) {
-                    const uint32_t key = cand[i];
-                    if ((key & st.mask) == st.prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
+        if (rank_mode) {
+            const int nc = (int)n_cand;
+            if (tid < nc) {
+                const uint32_t my_k = cand_key[tid], my_i = cand_idx[tid];
+                uint32_t better = 0;
+                for (int j = 0; j < nc; ++j) {
+                    const uint32_t kj = cand_key[j];
+                    better += (kj > my_k) || (kj == my_k && cand_idx[j] < my_i);
                 }
-            } else {
-                for (int i = tid; i < n; i += kTopkThreads) {
-                    const uint32_t key = key_at(i);
-                    if ((key & st.mask) == st.prefix) hist_add(hist, (key >> sh) & dm);
-                }
+                if (better < need) atomicOr(&marks[my_i >> 5], 1u << (my_i & 31));
             }
             __syncthreads();
-            done = select_bucket(hist, sh, dm, st, warp_tot, sel);
+        } else {
+            // radix select on the order keys of the bucket's entries: digits of 11, 11 and 10 bits
+            uint32_t prefix = 0u, mask = 0u;
+            need_T = need;
+            for (int pass = 0; pass < 3; ++pass) {
+                const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+                const uint32_t dm = pass == 2 ? 0x3FFu : 0x7FFu;
+                for (int b = tid; b < kBins; b += kTopkThreads) hist[b] = 0;
+                __syncthreads();
+                if (keep) {
+                    const int nc = (int)n_cand;
+                    for (int i = tid; i < nc; i += kTopkThreads) {
+                        const uint32_t key = cand_key[i];
+                        if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
+                    }
+                } else {
+                    for (int i = tid; i < n; i += kTopkThreads) {
+                        const float v = val_at(i);
+                        const uint32_t key = order_key(v);
+                        if (bin_of(v) == bstar && (key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
+                    }
+                }
+                __syncthreads();
+                const uint32_t d = select_bin(hist, need_T, warp_tot, sel);
+                prefix |= d << sh;
+                mask |= dm << sh;
+            }
+            T = prefix;
         }
     }
-    // keys above the final bucket are all taken; inside it, all of it (done) or the `need` lowest indices
-    const bool take_all = done;
-    const uint32_t bucket_hi = st.prefix | ~st.mask;
+
+    // 4. ordered compaction: definite winners, plus entries equal to T ranked by index (radix path)
     int run = (n + kTopkThreads - 1) / kTopkThreads;
-    run |= 1;  // odd run length: conflict-free strided shared-memory reads
+    run |= 1;
     const int lo = min(n, tid * run), hi = min(n, lo + run);
-    uint32_t gt = 0, eq = 0;
+    auto classify = [&](int i, bool* def, bool* tie) {
+        const float v = val_at(i);
+        const uint32_t b = bin_of(v);
+        *def = false;
+        *tie = false;
+        if (b > bstar) *def = true;
+        else if (b == bstar) {
+            if (take_all) *def = true;
+            else if (rank_mode) *def = (marks[i >> 5] >> (i & 31)) & 1u;
+            else {
+                const uint32_t key = order_key(v);
+                *def = key > T;
+                *tie = key == T;
+            }
+        }
+    };
+    uint32_t cd = 0, ct = 0;
     for (int i = lo; i < hi; ++i) {
-        const uint32_t key = key_at(i);
-        if (key > bucket_hi) ++gt;
-        else if ((key & st.mask) == st.prefix) ++eq;
+        bool d, t;
+        classify(i, &d, &t);
+        cd += d;
+        ct += t;
     }
-    uint32_t ex_gt, ex_eq, tot_gt, tot_eq;
-    block_scan2(gt, eq, &ex_gt, &ex_eq, &tot_gt, &tot_eq, warp_tot);
-    uint32_t eq_rank = ex_eq;
-    uint32_t pos = ex_gt + (take_all ? ex_eq : min(ex_eq, st.need));
+    uint32_t ex_d, ex_t, tot_d, tot_t;
+    block_scan2(cd, ct, &ex_d, &ex_t, &tot_d, &tot_t, warp_tot);
+    uint32_t tie_rank = ex_t;
+    uint32_t pos = ex_d + min(ex_t, need_T);
     for (int i = lo; i < hi; ++i) {
-        const uint32_t key = key_at(i);
-        if (key > bucket_hi) {
+        bool d, t;
+        classify(i, &d, &t);
+        if (d) {
             out[pos++] = i;
-        } else if ((key & st.mask) == st.prefix) {
-            if (take_all || eq_rank < st.need) out[pos++] = i;
-            ++eq_rank;
+        } else if (t) {
+            if (tie_rank < need_T) out[pos++] = i;
+            ++tie_rank;
         }
     }
-    const uint32_t total = tot_gt + (take_all ? tot_eq : min(tot_eq, st.need));
+    const uint32_t total = tot_d + min(tot_t, need_T);
     for (int i = (int)total + tid; i < k; i += kTopkThreads) out[i] = -1;
     if (tid == 0 && total != (uint32_t)k) report(status, DSA_ERR_DEVICE_FAULT);
 }
@@ -238,7 +309,9 @@ extern "C" dsa_status_t dsa_topk(int32_t nq, const float* scores, int32_t ld, co
     if (nq == 0) return DSA_OK;
     if (!scores || !n_valid || !idx_out || !aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
     const int resident = ld <= kResidentMax ? 1 : 0;
-    const size_t smem = (size_t)(kBins + kCandMax + (resident ? ld : 0)) * sizeof(uint32_t);
+    const size_t words = (size_t)kBins + kCandMax + kRankMax + (ld >> 5) + 1 + (resident ? ld : 0);
+    const size_t smem = words * sizeof(uint32_t);
+    if (smem > 227 * 1024) return DSA_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DSA_ERR_CUDA;
     topk_kernel<<<nq, kTopkThreads, smem, static_cast<cudaStream_t>(stream)>>>(scores, ld, n_valid, k, idx_out,
