@@ -170,7 +170,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float* __re
         mn = fminf(mn, red_min[w]);
     }
     const bool any_finite = mx != -INFINITY;
-    const float scale = (any_finite && mx > mn) ? 2046.f / (mx - mn) : 0.f;
+    float scale = (any_finite && mx > mn) ? 2046.f / (mx - mn) : 0.f;
+    if (!isfinite(scale)) scale = 0.f;  // degenerate range: one bucket, resolved by the radix path
     auto val_at = [&](int i) -> float { return resident ? rowv[i] : __ldg(s + i); };
     auto bin_of = [&](float v) -> uint32_t {
         if (v == -INFINITY) return 0u;
