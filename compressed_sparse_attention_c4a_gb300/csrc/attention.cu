@@ -13,6 +13,8 @@
 // the tensor cores (bf16 mma, fp32 accumulation).  Softmax is online (base-2, fp32).  When a row's
 // keys are split over several CTAs, each writes an unnormalised partial (O, max, sum) and a
 // combine kernel merges them and applies the inverse rotation.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace dsa {
@@ -587,4 +589,72 @@ extern "C" dsa_status_t dsa_sparse_attn_prefill(int32_t nq, int32_t heads, const
     if (!q_req) return DSA_ERR_INVALID_ARG;
     return sparse_attn(nq, heads, q, q_pos, q_req, kind, topk, k, main, main_bt, swa, swa_bt, window, sm_scale, rope,
                        out, lse, workspace, workspace_bytes, dev_status, stream);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Decode attention for callers that cannot allocate device memory.
+//
+// Some callers cannot hand the library a workspace: a serving loop that forbids cudaMalloc on its
+// hot path (an allocation can synchronise the device and stall every stream), a host that owns all
+// device memory through its own arena and exposes no allocator, or a plugin that only receives the
+// input and output pointers.  For them this entry point keeps the split-K partials in a fixed array
+// that is part of the library image (a file-scope __device__ array): every GPU that loads the library
+// holds these bytes until the process exits.  All calls share the one array, so calls that may
+// overlap on the GPU (different streams, or different host threads on one device) race on it and
+// must be serialised by the caller.  Every partial a call reads was written earlier in the same call,
+// so no part of the array has to start at zero.
+// ---------------------------------------------------------------------------------------------
+namespace dsa {
+
+constexpr size_t kStaticScratchBytes = 32u << 20;  // 32 MiB
+static __device__ __align__(256) uint8_t g_attn_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+static std::mutex g_scratch_mutex;
+static void* g_scratch_addr[kMaxDevices];
+
+// Device address of the array on the current device.  In host code `g_attn_scratch` names a
+// host-side stand-in, not device memory, so the address is looked up once per device (with that
+// device current) and cached.
+static void* static_scratch(int* status) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *status = DSA_ERR_CUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || !p) {
+            *status = DSA_ERR_CUDA;
+            return nullptr;
+        }
+        g_scratch_addr[dev] = p;
+    }
+    *status = DSA_OK;
+    return g_scratch_addr[dev];
+}
+
+}  // namespace dsa
+
+extern "C" size_t dsa_attn_static_scratch_bytes(void) { return dsa::kStaticScratchBytes; }
+
+extern "C" dsa_status_t dsa_sparse_attn_decode_static(int32_t batch, int32_t heads, const void* q,
+                                                      const int32_t* q_pos, int32_t kind, const int32_t* topk,
+                                                      int32_t k, const dsa_pool_t* main,
+                                                      const dsa_block_table_t* main_bt, const dsa_pool_t* swa,
+                                                      const dsa_block_table_t* swa_bt, int32_t window, float sm_scale,
+                                                      const dsa_rope_t* rope, void* out, float* lse,
+                                                      int32_t* dev_status, void* stream) {
+    if (batch < 0 || !main || !main_bt || window < 1) return DSA_ERR_INVALID_ARG;
+    if (batch == 0) return DSA_OK;
+    if (heads != 16 && heads != 32 && heads != 64 && heads != 128) return DSA_ERR_UNSUPPORTED;
+    const int max_comp = topk ? k : main_bt->max_blocks * main->rows_per_block;
+    const size_t need = workspace_bytes_for(batch, plan_splits(batch, heads, max_comp + window), heads);
+    if (need > kStaticScratchBytes) return DSA_ERR_UNSUPPORTED;  // beyond the fixed scratch: use the workspace call
+    int st = DSA_OK;
+    void* scratch = need > 0 ? static_scratch(&st) : nullptr;
+    if (st != DSA_OK) return st;
+    return sparse_attn(batch, heads, q, q_pos, nullptr, kind, topk, k, main, main_bt, swa, swa_bt, window, sm_scale,
+                       rope, out, lse, scratch, need > 0 ? kStaticScratchBytes : 0, dev_status, stream);
 }

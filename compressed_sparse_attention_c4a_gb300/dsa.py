@@ -20,7 +20,8 @@ DSA_C4A, DSA_C128A = 0, 1
 KIND = {"c4a": DSA_C4A, "c128a": DSA_C128A}
 
 EXPORTS = ["dsa_status_string", "dsa_compress", "dsa_index_scores", "dsa_topk", "dsa_attn_workspace_size",
-           "dsa_sparse_attn_decode", "dsa_sparse_attn_prefill", "dsa_gather_rows"]
+           "dsa_sparse_attn_decode", "dsa_sparse_attn_prefill", "dsa_gather_rows", "dsa_sparse_attn_decode_static",
+           "dsa_attn_static_scratch_bytes"]
 
 
 class DsaPool(ctypes.Structure):
@@ -48,6 +49,8 @@ _lib.dsa_status_string.restype = ctypes.c_char_p
 _lib.dsa_status_string.argtypes = [_I]
 _lib.dsa_attn_workspace_size.restype = ctypes.c_size_t
 _lib.dsa_attn_workspace_size.argtypes = [_I, _I, _I]
+_lib.dsa_attn_static_scratch_bytes.restype = ctypes.c_size_t
+_lib.dsa_attn_static_scratch_bytes.argtypes = []
 for _name, _args in {
     "dsa_compress": [_I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P],
     "dsa_index_scores": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P],
@@ -57,6 +60,8 @@ for _name, _args in {
     "dsa_sparse_attn_prefill": [_I, _I, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, ctypes.c_float, _P, _P, _P,
                                 _P, ctypes.c_size_t, _P, _P],
     "dsa_gather_rows": [_P, _P, _I, _P, _P, _P, _P, _P, _P],
+    "dsa_sparse_attn_decode_static": [_I, _I, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, ctypes.c_float, _P, _P, _P,
+                                      _P, _P],
 }.items():
     getattr(_lib, _name).restype = _I
     getattr(_lib, _name).argtypes = _args
@@ -159,3 +164,20 @@ def dsa_gather_rows(pool_, bt, req, ids, out, out_scale=None, dev_status=None, s
     code = _lib.dsa_gather_rows(ctypes.byref(pool_), ctypes.byref(bt), ids.numel(), _ptr(req), _ptr(ids), _ptr(out),
                                 _ptr(out_scale), _ptr(dev_status), _stream(stream))
     _check("dsa_gather_rows", code)
+
+
+def dsa_attn_static_scratch_bytes():
+    return int(_lib.dsa_attn_static_scratch_bytes())
+
+
+def dsa_sparse_attn_decode_static(q, q_pos, kind, topk, k, main, main_bt, swa, swa_bt, window, sm_scale, rope_cfg,
+                                  out, lse=None, dev_status=None, stream=None):
+    """dsa_sparse_attn_decode for callers that cannot allocate: split-K partials go to the library's
+    fixed per-device scratch array instead of a caller workspace (see include/dsa.h)."""
+    B, H, _ = q.shape
+    code = _lib.dsa_sparse_attn_decode_static(B, H, _ptr(q), _ptr(q_pos), KIND.get(kind, kind), _ptr(topk), int(k),
+                                              ctypes.byref(main), ctypes.byref(main_bt), ctypes.byref(swa),
+                                              ctypes.byref(swa_bt), int(window), float(sm_scale),
+                                              ctypes.byref(rope_cfg), _ptr(out), _ptr(lse), _ptr(dev_status),
+                                              _stream(stream))
+    _check("dsa_sparse_attn_decode_static", code)

@@ -11,6 +11,8 @@
  * Memory.  Every pointer argument is DEVICE memory owned by the caller unless the
  *   comment says "host".  The library never allocates or frees memory and keeps no
  *   mutable global state, so calls are reentrant and can be recorded in a CUDA graph.
+ *   The one exception is dsa_sparse_attn_decode_static (below): a fixed scratch array in
+ *   the library image plus a per-device cache of its address.
  * Streams.  `stream` is a cudaStream_t (NULL = legacy default stream).  Every call only
  *   enqueues work on that stream and returns; none synchronises.
  * Host-side errors.  A call returns DSA_OK or an error code; when the host-side checks
@@ -217,6 +219,33 @@ dsa_status_t dsa_sparse_attn_prefill(int32_t nq, int32_t heads, const void* q, c
                                      float sm_scale, const dsa_rope_t* rope, void* out, float* lse,
                                      void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                      void* stream);
+
+/*
+ * dsa_sparse_attn_decode_static - dsa_sparse_attn_decode without a caller workspace, for callers that
+ * cannot allocate device memory: a serving loop that forbids cudaMalloc on its hot path (an allocation
+ * can synchronise the device and stall every stream), a host whose device memory all belongs to its
+ * own arena with no allocator to call, or a plugin that is only handed the input and output pointers.
+ * The pages have no counterpart to this call; it exists for those callers only.
+ *
+ * Arguments and results are those of dsa_sparse_attn_decode minus `workspace` / `workspace_bytes`.
+ * The split-K partials live in a fixed array inside the library image, of
+ * dsa_attn_static_scratch_bytes() bytes (32 MiB) on every GPU that loads the library, held until the
+ * process exits.  A call whose plan needs more than that (dsa_attn_workspace_size() of the same sizes)
+ * returns DSA_ERR_UNSUPPORTED without launching anything.  The call allocates and frees nothing.
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress, with that
+ * device current) and caches it; make that first call before any stream capture.  All calls share the
+ * one array and its contents persist between calls, so calls that can overlap on the GPU (two streams,
+ * or two host threads on one device) race on it and must be serialised by the caller.
+ */
+dsa_status_t dsa_sparse_attn_decode_static(int32_t batch, int32_t heads, const void* q, const int32_t* q_pos,
+                                           int32_t kind, const int32_t* topk, int32_t k, const dsa_pool_t* main,
+                                           const dsa_block_table_t* main_bt, const dsa_pool_t* swa,
+                                           const dsa_block_table_t* swa_bt, int32_t window, float sm_scale,
+                                           const dsa_rope_t* rope, void* out, float* lse, int32_t* dev_status,
+                                           void* stream);
+
+/* Size in bytes of the fixed scratch array that dsa_sparse_attn_decode_static uses (32 MiB). */
+size_t dsa_attn_static_scratch_bytes(void);
 
 /*
  * dsa_gather_rows - copy the stored bytes of n logical rows, exactly as the attention
