@@ -126,20 +126,27 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float* __re
     const float* s = scores + (long long)row * ld;
     float mx = -INFINITY, mn = INFINITY;
     if (resident) {
-        for (int i = tid * 4; i < n; i += kTopkThreads * 4) {
-            float v[4];
-            if (i + 4 <= n) {
-                const float4 q = *reinterpret_cast<const float4*>(s + i);
-                v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
-            } else {
-                for (int u = 0; u < 4; ++u) v[u] = i + u < n ? s[i + u] : -INFINITY;
+        // up to 4 float4 loads per thread in flight before any is consumed
+        for (int i0 = tid * 4; i0 < n; i0 += kTopkThreads * 16) {
+            float4 q[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * kTopkThreads * 4;
+                q[u] = i + 4 <= n ? *reinterpret_cast<const float4*>(s + i) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                if (i + u < n) rowv[i + u] = v[u];
-                if (v[u] != -INFINITY) {
-                    mx = fmaxf(mx, v[u]);
-                    mn = fminf(mn, v[u]);
+                const int i = i0 + u * kTopkThreads * 4;
+                float v[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+                if (i + 4 > n)
+                    for (int e = 0; e < 4; ++e) v[e] = i + e < n ? s[i + e] : -INFINITY;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (i + e < n) rowv[i + e] = v[e];
+                    if (v[e] != -INFINITY) {
+                        mx = fmaxf(mx, v[e]);
+                        mn = fminf(mn, v[e]);
+                    }
                 }
             }
         }
@@ -162,13 +169,16 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float* __re
         red_min[wid] = mn;
     }
     __syncthreads();
-    mx = -INFINITY;
-    mn = INFINITY;
-#pragma unroll 8
-    for (int w = 0; w < 32; ++w) {
-        mx = fmaxf(mx, red_max[w]);
-        mn = fminf(mn, red_min[w]);
+    if (wid == 0) {
+        float a = warp_max(red_max[lane]), b = -warp_max(-red_min[lane]);
+        if (lane == 0) {
+            red_max[0] = a;
+            red_min[0] = b;
+        }
     }
+    __syncthreads();
+    mx = red_max[0];
+    mn = red_min[0];
     const bool any_finite = mx != -INFINITY;
     float scale = (any_finite && mx > mn) ? 2046.f / (mx - mn) : 0.f;
     if (!isfinite(scale)) scale = 0.f;  // degenerate range: one bucket, resolved by the radix path
@@ -255,8 +265,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float* __re
     }
 
     // 4. ordered compaction: definite winners, plus entries equal to T ranked by index (radix path)
-    int run = (n + kTopkThreads - 1) / kTopkThreads;
-    run |= 1;
+    int run = (n + kTopkThreads - 1) / kTopkThreads;  // <= 64 (ld <= 65,536)
+    if (resident) run |= 1;                              // odd: conflict-free strided smem reads (<= 41)
     const int lo = min(n, tid * run), hi = min(n, lo + run);
     auto classify = [&](int i, bool* def, bool* tie) {
         const float v = val_at(i);
@@ -274,24 +284,26 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float* __re
             }
         }
     };
-    uint32_t cd = 0, ct = 0;
+    // a thread's run is at most 64 entries (rows up to 65,535 scores), so its classification fits two
+    // 64-bit masks: computed once, used for the counts and again for the writes
+    unsigned long long mdef = 0ull, mtie = 0ull;
     for (int i = lo; i < hi; ++i) {
         bool d, t;
         classify(i, &d, &t);
-        cd += d;
-        ct += t;
+        mdef |= (unsigned long long)d << (i - lo);
+        mtie |= (unsigned long long)t << (i - lo);
     }
+    const uint32_t cd = __popcll(mdef), ct = __popcll(mtie);
     uint32_t ex_d, ex_t, tot_d, tot_t;
     block_scan2(cd, ct, &ex_d, &ex_t, &tot_d, &tot_t, warp_tot);
     uint32_t tie_rank = ex_t;
     uint32_t pos = ex_d + min(ex_t, need_T);
-    for (int i = lo; i < hi; ++i) {
-        bool d, t;
-        classify(i, &d, &t);
-        if (d) {
-            out[pos++] = i;
-        } else if (t) {
-            if (tie_rank < need_T) out[pos++] = i;
+    for (unsigned long long m = mdef | mtie; m; m &= m - 1) {
+        const int b = __ffsll((long long)m) - 1;
+        if ((mdef >> b) & 1ull) {
+            out[pos++] = lo + b;
+        } else {
+            if (tie_rank < need_T) out[pos++] = lo + b;
             ++tie_rank;
         }
     }
@@ -309,6 +321,7 @@ extern "C" dsa_status_t dsa_topk(int32_t nq, const float* scores, int32_t ld, co
     if (nq < 0 || k < 1 || k > 2048 || ld < 0 || (ld & 3)) return DSA_ERR_INVALID_ARG;
     if (nq == 0) return DSA_OK;
     if (!scores || !n_valid || !idx_out || !aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
+    if (ld > 64 * kTopkThreads) return DSA_ERR_UNSUPPORTED;  // a thread's run must fit a 64-bit mask
     const int resident = ld <= kResidentMax ? 1 : 0;
     const size_t words = (size_t)kBins + kCandMax + kRankMax + (ld >> 5) + 1 + (resident ? ld : 0);
     const size_t smem = words * sizeof(uint32_t);
