@@ -13,6 +13,7 @@
 // the tensor cores (bf16 mma, fp32 accumulation).  Softmax is online (base-2, fp32).  When a row's
 // keys are split over several CTAs, each writes an unnormalised partial (O, max, sum) and a
 // combine kernel merges them and applies the inverse rotation.
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -461,16 +462,315 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
         a.lse[(long long)row * a.heads + head] = Ls > 0.f ? (M + log2f(Ls)) / kLog2e : -INFINITY;
 }
 
+// ---------------------------------------------------------------------------------------------
+// bf16 rows on the 5th-generation tensor cores (tcgen05, TMEM accumulators).
+//
+// One CTA (4 warps) per (query row, group of NH heads, key split); a split is a run of 128-key
+// tiles.  For each tile the 128 key rows are gathered through the block tables into shared memory
+// in 128B-swizzled 8-row x 128-byte atoms, laid out [64-dim chunk][8-key group][8 keys][128 B].
+// That one copy serves both products (K = V):
+//   S^T = K Q^T   : A = K tile, K-major (M = 128 keys, K = 512 dims), B = Q (N = NH heads, K-major),
+//                   accumulated in TMEM columns [0, NH): lane = key, column = head;
+//   O^T += V^T P^T: A = the same tile read MN-major (M = 128 dims per MMA, K = 16 keys),
+//                   B = P^T (N = NH heads, K = keys, K-major), four 128-dim tiles in TMEM columns
+//                   [NH, 5 NH): lane = dim, column = head.
+// Softmax runs per head over TMEM lanes: each thread holds one key's NH logits; per-head max and sum
+// are warp shuffle reductions plus a 4-warp combine in shared memory (online across tiles, with O^T
+// rescaled in TMEM when a head's max grows).  The epilogue reads O^T (lane = dim), applies 1/l and
+// R_m^-1 (pairs of dims sit in neighbouring lanes) and stores bf16, or writes split-K partials.
+// ---------------------------------------------------------------------------------------------
+constexpr int kTcKeys = 128;
+constexpr int kTcThreads = 128;
+
+template <int NH>
+struct TcSmem {
+    static constexpr int kQ = NH * kD * 2;          // [8][NH][128 B]
+    static constexpr int kK = kTcKeys * kD * 2;     // [8][128][128 B]
+    static constexpr int kP = NH * kTcKeys * 2;     // [2][NH][128 B]
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + kQ;
+    static constexpr int kOffP = kOffK + kK;
+    static constexpr int kOffMeta = kOffP + kP;                  // long long [128]
+    static constexpr int kOffFlag = kOffMeta + kTcKeys * 8;      // int [128]
+    static constexpr int kOffRed = kOffFlag + kTcKeys * 4;       // float [4][NH] x 2
+    static constexpr int kOffStat = kOffRed + 2 * 4 * NH * 4;    // float m[NH], l[NH], mnew[NH], alpha[NH]
+    static constexpr int kOffBar = kOffStat + 4 * NH * 4;        // mbarrier, tmem address
+    static constexpr int kBytes = kOffBar + 64;
+    static constexpr int kAlloc = kBytes + 1024;                 // + alignment slack
+    static constexpr int kTmemCols = 5 * NH <= 128 ? 128 : (5 * NH <= 256 ? 256 : 512);
+};
+
+// Byte offset of element (row r, element e) in a tile of 128B-swizzled atoms whose rows are 128 bytes
+// (64 bf16) long: atoms of 8 rows are 1024 bytes apart, 64-element chunks `chunk_stride` apart.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int e, int chunk_stride) {
+    const int c = e >> 6, in = e & 63;
+    return (uint32_t)(c * chunk_stride + (r >> 3) * 1024 + (r & 7) * 128 + ((((in >> 3) ^ (r & 7))) << 4) +
+                      ((in & 7) << 1));
+}
+
+template <int NH>
+__global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnArgs a) {
+    using L = TcSmem<NH>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sQ = smem_u32(smem + L::kOffQ), sK = smem_u32(smem + L::kOffK), sP = smem_u32(smem + L::kOffP);
+    long long* meta_row = reinterpret_cast<long long*>(smem + L::kOffMeta);
+    int* meta_flag = reinterpret_cast<int*>(smem + L::kOffFlag);
+    float* red_a = reinterpret_cast<float*>(smem + L::kOffRed);
+    float* red_b = red_a + 4 * NH;
+    float* st_m = reinterpret_cast<float*>(smem + L::kOffStat);
+    float* st_l = st_m + NH;
+    float* st_mnew = st_l + NH;
+    float* st_alpha = st_mnew + NH;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar + 1);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int split = blockIdx.x % a.nsplit;
+    const int hg = (blockIdx.x / a.nsplit) % a.hg_count;
+    const int row = blockIdx.x / (a.nsplit * a.hg_count);
+    const int r = a.q_req ? a.q_req[row] : row;
+    const int m = a.q_pos[row];
+    const bool row_ok = r >= 0 && r < a.main_bt.batch && r < a.swa_bt.batch && m >= 0;
+    if (!row_ok && tid == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
+    const int n_vis = row_ok ? entries_formed((long long)m + 1, a.kind_w, a.kind_s) : 0;
+    const int n_comp = a.topk ? a.k : n_vis;
+    const int wlo = max(0, m - a.window + 1);
+    const int n_keys = row_ok ? n_comp + (m - wlo + 1) : 0;
+    const int key_lo = split * a.cps * kTcKeys;
+    const int key_hi = min(n_keys, key_lo + a.cps * kTcKeys);
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(s_tmem, L::kTmemCols);
+    for (int h = tid; h < NH; h += kTcThreads) {
+        st_m[h] = -INFINITY;
+        st_l[h] = 0.f;
+    }
+    // Q rows of this head group -> B operand layout
+    {
+        const uint16_t* qsrc = a.q + ((long long)row * a.heads + (long long)hg * NH) * kD;
+        for (int i = tid; i < NH * (kD / 8); i += kTcThreads) {
+            const int h = i / (kD / 8), e = (i % (kD / 8)) * 8;
+            cp_async16(sQ + sw128_offset(h, e, NH * 128), qsrc + (long long)h * kD + e, row_ok ? 16u : 0u);
+        }
+        cp_async_commit();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    const uint32_t tS = tmem, tO = tmem + NH;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t idesc_s = idesc_bf16(NH, 0), idesc_o = idesc_bf16(NH, 1);
+
+    uint32_t phase = 0;
+    bool ok = true, first = true;
+    for (int kt = key_lo; kt < key_hi && ok; kt += kTcKeys) {
+        // resolve the tile's keys (thread j <-> key kt + j), then gather rows warp by warp
+        {
+            const int j = kt + tid;
+            long long p = -1;
+            bool sw = false;
+            if (j < key_hi) p = resolve_key(a, row, r, m, n_vis, n_comp, wlo, j, &sw);
+            meta_row[tid] = p;
+            meta_flag[tid] = p < 0 ? 0 : (sw ? 2 : 1);
+        }
+        __syncthreads();
+        for (int kk = warp; kk < kTcKeys; kk += 4) {
+            const int flag = meta_flag[kk];
+            const uint8_t* base = flag == 2 ? static_cast<const uint8_t*>(a.swa.data)
+                                            : static_cast<const uint8_t*>(a.main.data);
+            const uint8_t* src = flag ? base + meta_row[kk] * (2 * kD) : base;
+            for (int piece = lane; piece < kD / 8; piece += 32)
+                cp_async16(sK + sw128_offset(kk, piece * 8, kTcKeys * 128), src + piece * 16, flag ? 16u : 0u);
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        fence_proxy_async_smem();  // cp.async writes -> visible to the tensor core (async proxy)
+        __syncthreads();
+
+        // S^T = K Q^T
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll 4
+            for (int ks = 0; ks < kD / 16; ++ks) {
+                const uint32_t koff = (ks >> 2) * (kTcKeys * 128) + (ks & 3) * 32;
+                const uint32_t qoff = (ks >> 2) * (NH * 128) + (ks & 3) * 32;
+                mma_bf16_ss(tS, sw128_desc(sK + koff, 16, 1024), sw128_desc(sQ + qoff, 16, 1024), idesc_s, ks > 0);
+            }
+            mma_commit(bar);
+        }
+        ok = mbar_wait_bounded(bar, phase, kWaitLimitNs);
+        phase ^= 1;
+        ok = __syncthreads_and(ok);
+        if (!ok) {
+            if (tid == 0) report(a.status, DSA_ERR_TIMEOUT);
+            break;
+        }
+        tc_fence_after();
+
+        // softmax over this tile's keys, per head (thread = key, NH logits in registers)
+        const int key = tid;
+        const bool valid = meta_flag[key] != 0;
+        float sv[NH];
+#pragma unroll
+        for (int c0 = 0; c0 < NH; c0 += 16) {
+            float v[16];
+            tmem_ld16(tS + lane_off + c0, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sv[c0 + i] = valid ? v[i] * a.scale_log2 : -INFINITY;
+        }
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+            const float w = warp_max(sv[h]);
+            if (lane == (h & 31)) red_a[warp * NH + h] = w;
+        }
+        __syncthreads();
+        for (int h = tid; h < NH; h += kTcThreads) {
+            const float mo = st_m[h];
+            const float mt = fmaxf(fmaxf(red_a[h], red_a[NH + h]), fmaxf(red_a[2 * NH + h], red_a[3 * NH + h]));
+            const float mn = fmaxf(mo, mt);
+            st_mnew[h] = mn;
+            st_alpha[h] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
+        }
+        __syncthreads();
+        // P^T (bf16) for the PV product, per-head partial sums
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+            const float mn = st_mnew[h];
+            const float p = mn == -INFINITY ? 0.f : exp2f(sv[h] - mn);
+            sv[h] = p;
+            const uint32_t off = sw128_offset(h, key, NH * 128);
+            *reinterpret_cast<uint16_t*>(smem + L::kOffP + off) = float_to_bf16(p);
+        }
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+            const float w = warp_sum(sv[h]);
+            if (lane == (h & 31)) red_b[warp * NH + h] = w;
+        }
+        __syncthreads();
+        bool grew = false;
+        for (int h = tid; h < NH; h += kTcThreads) {
+            const float sum = red_b[h] + red_b[NH + h] + red_b[2 * NH + h] + red_b[3 * NH + h];
+            st_l[h] = st_l[h] * st_alpha[h] + sum;
+            grew |= st_alpha[h] != 1.f;
+            st_m[h] = st_mnew[h];
+        }
+        grew = __syncthreads_or(grew);
+        // rescale the running O^T where a head's max grew (lane = dim, column = head)
+        if (!first && grew) {
+#pragma unroll 1
+            for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+                for (int c0 = 0; c0 < NH; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(tO + mt * NH + lane_off + c0, v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] *= st_alpha[c0 + i];
+                    tmem_st16(tO + mt * NH + lane_off + c0, v);
+                }
+            }
+            tmem_wait_st();
+        }
+        fence_proxy_async_smem();  // P^T stores -> async proxy
+        tc_fence_before();
+        __syncthreads();
+
+        // O^T += V^T P^T
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+                for (int ks = 0; ks < kTcKeys / 16; ++ks) {
+                    const uint32_t voff = (2 * mt) * (kTcKeys * 128) + (2 * ks) * 1024;
+                    const uint32_t poff = (ks >> 2) * (NH * 128) + (ks & 3) * 32;
+                    mma_bf16_ss(tO + mt * NH, sw128_desc(sK + voff, kTcKeys * 128, 1024),
+                                sw128_desc(sP + poff, 16, 1024), idesc_o, (first && ks == 0) ? 0u : 1u);
+                }
+            }
+            mma_commit(bar);
+        }
+        ok = mbar_wait_bounded(bar, phase, kWaitLimitNs);
+        phase ^= 1;
+        ok = __syncthreads_and(ok);
+        if (!ok && tid == 0) report(a.status, DSA_ERR_TIMEOUT);
+        tc_fence_after();
+        first = false;
+    }
+
+    // ---- epilogue: thread = dim within each 128-dim tile of O^T ----------------------------------
+    __syncthreads();
+    const bool have = !first && ok;
+    if (a.nsplit == 1) {
+        const int rd = a.rope.rope_dim, firstd = kD - rd;
+#pragma unroll 1
+        for (int mt = 0; mt < 4; ++mt) {
+            const int d = mt * 128 + warp * 32 + lane;
+            float cs = 1.f, sn = 0.f;
+            if (d >= firstd) rope_cos_sin(m, a.rope.inv_freq[(d - firstd) >> 1], &cs, &sn);
+#pragma unroll
+            for (int c0 = 0; c0 < NH; c0 += 16) {
+                float v[16];
+                if (have) tmem_ld16(tO + mt * NH + lane_off + c0, v);
+                else
+                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int h = c0 + i;
+                    const float l = st_l[h];
+                    const float x = l > 0.f ? v[i] / l : 0.f;
+                    const float y = __shfl_xor_sync(0xffffffffu, x, 1);  // the pair partner's value
+                    float o = x;
+                    if (d >= firstd) o = (d & 1) ? (-y * sn + x * cs) : (x * cs + y * sn);  // R_m^-1
+                    a.out[((long long)row * a.heads + hg * NH + h) * kD + d] = float_to_bf16(o);
+                }
+            }
+        }
+        if (a.lse)
+            for (int h = tid; h < NH; h += kTcThreads) {
+                const float l = st_l[h];
+                a.lse[(long long)row * a.heads + hg * NH + h] = l > 0.f ? (st_m[h] + log2f(l)) / kLog2e : -INFINITY;
+            }
+    } else {
+        const long long base0 = ((long long)row * a.nsplit + split) * a.heads + hg * NH;
+#pragma unroll 1
+        for (int mt = 0; mt < 4; ++mt) {
+            const int d = mt * 128 + warp * 32 + lane;
+#pragma unroll
+            for (int c0 = 0; c0 < NH; c0 += 16) {
+                float v[16];
+                if (have) tmem_ld16(tO + mt * NH + lane_off + c0, v);
+                else
+                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) a.ws_o[(base0 + c0 + i) * kD + d] = v[i];
+            }
+        }
+        for (int h = tid; h < NH; h += kTcThreads) {
+            a.ws_ml[(base0 + h) * 2 + 0] = st_m[h];
+            a.ws_ml[(base0 + h) * 2 + 1] = st_l[h];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, L::kTmemCols);
+}
+
 // Split plan shared by the workspace query and the launch.
 struct SplitPlan {
     int hg, hg_count, nsplit, cps;
 };
 
-static SplitPlan plan_splits(int rows, int heads, int max_keys) {
+static SplitPlan plan_splits(int rows, int heads, int max_keys, int chunk) {
     SplitPlan p;
     p.hg = heads >= 64 ? 64 : heads;
     p.hg_count = heads / p.hg;
-    const int n_chunks = max(1, (max_keys + kChunk - 1) / kChunk);
+    const int n_chunks = max(1, (max_keys + chunk - 1) / chunk);
     const long long units = (long long)rows * p.hg_count;
     const int sms = sm_count();
     int ns = units >= sms ? 1 : (int)(sms / units);
@@ -483,6 +783,27 @@ static SplitPlan plan_splits(int rows, int heads, int max_keys) {
 static size_t workspace_bytes_for(int rows, const SplitPlan& p, int heads) {
     if (p.nsplit <= 1) return 0;
     return (size_t)rows * p.nsplit * heads * (kD + 2) * sizeof(float);
+}
+
+// Keys per split unit: 128-key tiles on the tensor-core path (bf16 rows), 64-key chunks for e4m3 rows.
+static int chunk_for(int dtype) { return dtype == DSA_BF16 ? kTcKeys : kChunk; }
+
+// Workspace that covers either row format (the size query does not know the pool's format).
+static size_t workspace_bytes_any(int rows, int heads, int max_keys) {
+    return std::max(workspace_bytes_for(rows, plan_splits(rows, heads, max_keys, kTcKeys), heads),
+                    workspace_bytes_for(rows, plan_splits(rows, heads, max_keys, kChunk), heads));
+}
+
+template <int NH>
+static dsa_status_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
+    using L = TcSmem<NH>;
+    if (cudaFuncSetAttribute(attn_tc_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
+        cudaSuccess)
+        return DSA_ERR_CUDA;
+    const long long grid = (long long)a.rows * a.hg_count * a.nsplit;
+    attn_tc_kernel<NH><<<(unsigned)grid, kTcThreads, L::kAlloc, st>>>(a);
+    if (a.nsplit > 1) attn_combine_kernel<<<a.rows * a.heads, 128, 0, st>>>(a);
+    return launch_status();
 }
 
 template <int HG, bool FP8>
@@ -519,7 +840,7 @@ static dsa_status_t sparse_attn(int32_t rows, int32_t heads, const void* q, cons
         return DSA_ERR_INVALID_ARG;
     const int max_comp = topk ? k : main_bt->max_blocks * main->rows_per_block;
     const int max_keys = max_comp + window;
-    const SplitPlan p = plan_splits(rows, heads, max_keys);
+    const SplitPlan p = plan_splits(rows, heads, max_keys, chunk_for(main->dtype));
     const size_t need = workspace_bytes_for(rows, p, heads);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256))) return DSA_ERR_INVALID_ARG;
 
@@ -552,6 +873,13 @@ static dsa_status_t sparse_attn(int32_t rows, int32_t heads, const void* q, cons
     a.status = dev_status;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool fp8 = main->dtype == DSA_FP8_E4M3;
+    if (!fp8) {
+        switch (p.hg) {
+            case 16: return launch_attn_tc<16>(a, st);
+            case 32: return launch_attn_tc<32>(a, st);
+            default: return launch_attn_tc<64>(a, st);
+        }
+    }
     switch (p.hg) {
         case 16: return fp8 ? launch_attn<16, true>(a, st) : launch_attn<16, false>(a, st);
         case 32: return fp8 ? launch_attn<32, true>(a, st) : launch_attn<32, false>(a, st);
@@ -566,7 +894,7 @@ using namespace dsa;
 extern "C" size_t dsa_attn_workspace_size(int32_t nq, int32_t heads, int32_t max_keys) {
     if (nq <= 0 || heads <= 0 || max_keys <= 0) return 0;
     if (heads != 16 && heads != 32 && heads != 64 && heads != 128) return 0;
-    return workspace_bytes_for(nq, plan_splits(nq, heads, max_keys), heads);
+    return workspace_bytes_any(nq, heads, max_keys);
 }
 
 extern "C" dsa_status_t dsa_sparse_attn_decode(int32_t batch, int32_t heads, const void* q, const int32_t* q_pos,
@@ -650,7 +978,7 @@ extern "C" dsa_status_t dsa_sparse_attn_decode_static(int32_t batch, int32_t hea
     if (batch == 0) return DSA_OK;
     if (heads != 16 && heads != 32 && heads != 64 && heads != 128) return DSA_ERR_UNSUPPORTED;
     const int max_comp = topk ? k : main_bt->max_blocks * main->rows_per_block;
-    const size_t need = workspace_bytes_for(batch, plan_splits(batch, heads, max_comp + window), heads);
+    const size_t need = workspace_bytes_any(batch, heads, max_comp + window);
     if (need > kStaticScratchBytes) return DSA_ERR_UNSUPPORTED;  // beyond the fixed scratch: use the workspace call
     int st = DSA_OK;
     void* scratch = need > 0 ? static_scratch(&st) : nullptr;
