@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
 // R_m^-1 (pairs of dims sit in neighbouring lanes) and stores bf16, or writes split-K partials.
 // ---------------------------------------------------------------------------------------------
 constexpr int kTcKeys = 128;
-constexpr int kTcThreads = 128;
+constexpr int kTcThreads = 256;  // 8 warps: two per TMEM lane quadrant
 
 template <int NH>
 struct TcSmem {
@@ -508,9 +508,37 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int e, int chunk_stride)
                       ((in & 7) << 1));
 }
 
+// Reduce N values per lane across the 32 lanes of a warp, transposed: after log2(32) exchange steps
+// lane l holds the reduction (over all lanes) of value index l * N / 32 (N <= 32), using N - 1
+// shuffles instead of 5 N.  `op` is max or add.
+template <int N, typename Op>
+__device__ __forceinline__ float transpose_reduce(float (&v)[N], Op op) {
+    const int lane = threadIdx.x & 31;
+    int n = N;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        if (n > 1) {
+            const bool upper = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < N / 2; ++i) {
+                if (i < n / 2) {
+                    const float send = upper ? v[i] : v[i + n / 2];
+                    const float keep = upper ? v[i + n / 2] : v[i];
+                    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, o));
+                }
+            }
+            n >>= 1;
+        } else {
+            v[0] = op(v[0], __shfl_xor_sync(0xffffffffu, v[0], o));
+        }
+    }
+    return v[0];
+}
+
 template <int NH>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnArgs a) {
     using L = TcSmem<NH>;
+    constexpr int HH = NH / 2;  // heads per warp in the softmax (the two warps of a quadrant split them)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sQ = smem_u32(smem + L::kOffQ), sK = smem_u32(smem + L::kOffK), sP = smem_u32(smem + L::kOffP);
@@ -526,6 +554,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnArgs a) {
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar + 1);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int quad = warp & 3, half = warp >> 2;  // TMEM lanes 32 quad .. ; heads / dim tiles of this half
     const int split = blockIdx.x % a.nsplit;
     const int hg = (blockIdx.x / a.nsplit) % a.hg_count;
     const int row = blockIdx.x / (a.nsplit * a.hg_count);
@@ -563,14 +592,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnArgs a) {
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t tS = tmem, tO = tmem + NH;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t idesc_s = idesc_bf16(NH, 0), idesc_o = idesc_bf16(NH, 1);
+    const int h0 = half * HH;  // this warp's heads in the softmax: [h0, h0 + HH)
+    auto fmax_op = [](float x, float y) { return fmaxf(x, y); };
+    auto add_op = [](float x, float y) { return x + y; };
 
     uint32_t phase = 0;
     bool ok = true, first = true;
     for (int kt = key_lo; kt < key_hi && ok; kt += kTcKeys) {
         // resolve the tile's keys (thread j <-> key kt + j), then gather rows warp by warp
-        {
+        if (tid < kTcKeys) {
             const int j = kt + tid;
             long long p = -1;
             bool sw = false;
@@ -579,7 +611,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnArgs a) {
             meta_flag[tid] = p < 0 ? 0 : (sw ? 2 : 1);
         }
         __syncthreads();
-        for (int kk = warp; kk < kTcKeys; kk += 4) {
+        for (int kk = warp; kk < kTcKeys; kk += kTcThreads / 32) {
             const int flag = meta_flag[kk];
             const uint8_t* base = flag == 2 ? static_cast<const uint8_t*>(a.swa.data)
                                             : static_cast<const uint8_t*>(a.main.data);
@@ -612,21 +644,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnArgs a) {
         }
         tc_fence_after();
 
-        // softmax over this tile's keys, per head (thread = key, NH logits in registers)
-        const int key = tid;
+        // softmax over this tile's keys, per head: thread = key (quadrant lane), HH heads of this half
+        const int key = quad * 32 + lane;
         const bool valid = meta_flag[key] != 0;
-        float sv[NH];
+        float sv[HH], tmp[HH];
 #pragma unroll
-        for (int c0 = 0; c0 < NH; c0 += 16) {
+        for (int c0 = 0; c0 < HH; c0 += 16) {
             float v[16];
-            tmem_ld16(tS + lane_off + c0, v);
+            tmem_ld16(tS + lane_off + h0 + c0, v);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) sv[c0 + i] = valid ? v[i] * a.scale_log2 : -INFINITY;
+            for (int i = 0; i < 16; ++i)
+                if (c0 + i < HH) sv[c0 + i] = valid ? v[i] * a.scale_log2 : -INFINITY;
         }
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-            const float w = warp_max(sv[h]);
-            if (lane == (h & 31)) red_a[warp * NH + h] = w;
+        for (int i = 0; i < HH; ++i) tmp[i] = sv[i];
+        {
+            const float w = transpose_reduce<HH>(tmp, fmax_op);  // head h0 + lane * HH / 32
+            if ((lane & (32 / HH - 1)) == 0) red_a[quad * NH + h0 + lane * HH / 32] = w;
         }
         __syncthreads();
         for (int h = tid; h < NH; h += kTcThreads) {
@@ -639,17 +673,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnArgs a) {
         __syncthreads();
         // P^T (bf16) for the PV product, per-head partial sums
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
+        for (int i = 0; i < HH; ++i) {
+            const int h = h0 + i;
             const float mn = st_mnew[h];
-            const float p = mn == -INFINITY ? 0.f : exp2f(sv[h] - mn);
-            sv[h] = p;
-            const uint32_t off = sw128_offset(h, key, NH * 128);
-            *reinterpret_cast<uint16_t*>(smem + L::kOffP + off) = float_to_bf16(p);
+            const float p = mn == -INFINITY ? 0.f : exp2f(sv[i] - mn);
+            sv[i] = p;
+            *reinterpret_cast<uint16_t*>(smem + L::kOffP + sw128_offset(h, key, NH * 128)) = float_to_bf16(p);
         }
-#pragma unroll
-        for (int h = 0; h < NH; ++h) {
-            const float w = warp_sum(sv[h]);
-            if (lane == (h & 31)) red_b[warp * NH + h] = w;
+        {
+            const float w = transpose_reduce<HH>(sv, add_op);
+            if ((lane & (32 / HH - 1)) == 0) red_b[quad * NH + h0 + lane * HH / 32] = w;
         }
         __syncthreads();
         bool grew = false;
@@ -660,10 +693,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnArgs a) {
             st_m[h] = st_mnew[h];
         }
         grew = __syncthreads_or(grew);
-        // rescale the running O^T where a head's max grew (lane = dim, column = head)
+        // rescale the running O^T where a head's max grew (lane = dim, column = head); each half of
+        // the warps owns two of the four 128-dim tiles
         if (!first && grew) {
 #pragma unroll 1
-            for (int mt = 0; mt < 4; ++mt) {
+            for (int mt = 2 * half; mt < 2 * half + 2; ++mt) {
 #pragma unroll
                 for (int c0 = 0; c0 < NH; c0 += 16) {
                     float v[16];
@@ -702,14 +736,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnArgs a) {
         first = false;
     }
 
-    // ---- epilogue: thread = dim within each 128-dim tile of O^T ----------------------------------
+    // ---- epilogue: thread = dim of a 128-dim tile of O^T; each half of the warps owns two tiles -----
     __syncthreads();
     const bool have = !first && ok;
     if (a.nsplit == 1) {
         const int rd = a.rope.rope_dim, firstd = kD - rd;
 #pragma unroll 1
-        for (int mt = 0; mt < 4; ++mt) {
-            const int d = mt * 128 + warp * 32 + lane;
+        for (int mt = 2 * half; mt < 2 * half + 2; ++mt) {
+            const int d = mt * 128 + quad * 32 + lane;
             float cs = 1.f, sn = 0.f;
             if (d >= firstd) rope_cos_sin(m, a.rope.inv_freq[(d - firstd) >> 1], &cs, &sn);
 #pragma unroll
@@ -726,7 +760,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnArgs a) {
                     const float y = __shfl_xor_sync(0xffffffffu, x, 1);  // the pair partner's value
                     float o = x;
                     if (d >= firstd) o = (d & 1) ? (-y * sn + x * cs) : (x * cs + y * sn);  // R_m^-1
-                    a.out[((long long)row * a.heads + hg * NH + h) * kD + d] = float_to_bf16(o);
+                    const float o_hi = __shfl_xor_sync(0xffffffffu, o, 1);
+                    if ((d & 1) == 0)  // even lane stores the (d, d + 1) pair
+                        *reinterpret_cast<uint32_t*>(a.out + ((long long)row * a.heads + hg * NH + h) * kD + d) =
+                            (uint32_t)float_to_bf16(o) | ((uint32_t)float_to_bf16(o_hi) << 16);
                 }
             }
         }
@@ -738,8 +775,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnArgs a) {
     } else {
         const long long base0 = ((long long)row * a.nsplit + split) * a.heads + hg * NH;
 #pragma unroll 1
-        for (int mt = 0; mt < 4; ++mt) {
-            const int d = mt * 128 + warp * 32 + lane;
+        for (int mt = 2 * half; mt < 2 * half + 2; ++mt) {
+            const int d = mt * 128 + quad * 32 + lane;
 #pragma unroll
             for (int c0 = 0; c0 < NH; c0 += 16) {
                 float v[16];
