@@ -24,6 +24,8 @@ namespace dsa {
 __global__ void __launch_bounds__(256) gather_rows_kernel(dsa_pool_t pool, dsa_block_table_t bt, int n,
                                                           const int32_t* req, const int32_t* ids, uint8_t* out,
                                                           float* out_scale, int row_bytes, int32_t* status) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int j = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (j >= n) return;
@@ -58,7 +60,8 @@ extern "C" dsa_status_t dsa_gather_rows(const dsa_pool_t* pool, const dsa_block_
         return DSA_ERR_INVALID_ARG;
     const int row_bytes = pool->dim * (pool->dtype == DSA_BF16 ? 2 : 1);
     if (row_bytes % 16 || !aligned(out, 16)) return DSA_ERR_INVALID_ARG;
-    gather_rows_kernel<<<(n + 7) / 8, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        *pool, *bt, n, req, ids, static_cast<uint8_t*>(out), out_scale, row_bytes, dev_status);
+    if (launch_pdl(gather_rows_kernel, dim3((n + 7) / 8), dim3(256), 0, static_cast<cudaStream_t>(stream), *pool, *bt,
+                   n, req, ids, static_cast<uint8_t*>(out), out_scale, row_bytes, dev_status) != cudaSuccess)
+        return DSA_ERR_CUDA;
     return launch_status();
 }

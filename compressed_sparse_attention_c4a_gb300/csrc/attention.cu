@@ -125,6 +125,8 @@ struct AttnSmem {
 
 template <int HG, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
     using L = AttnSmem<HG, FP8>;
     constexpr int MT = HG / 16;        // 16-head m-tiles
     constexpr int WPM = 8 / MT;        // warps per m-tile
@@ -421,6 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
 
 // Merge split partials of one (row, head): 128 threads x 4 dims; inverse RoPE; bf16 store.
 __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int row = blockIdx.x / a.heads, head = blockIdx.x % a.heads;
     const int tid = threadIdx.x;
     float M = -INFINITY;
@@ -558,6 +562,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnArgs a) {
     const int split = blockIdx.x % a.nsplit;
     const int hg = (blockIdx.x / a.nsplit) % a.hg_count;
     const int row = blockIdx.x / (a.nsplit * a.hg_count);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(s_tmem, L::kTmemCols);
+    for (int h = tid; h < NH; h += kTcThreads) {
+        st_m[h] = -INFINITY;
+        st_l[h] = 0.f;
+    }
+    pdl_wait();  // on-chip set-up above; global memory only below
+    pdl_launch_dependents();
     const int r = a.q_req ? a.q_req[row] : row;
     const int m = a.q_pos[row];
     const bool row_ok = r >= 0 && r < a.main_bt.batch && r < a.swa_bt.batch && m >= 0;
@@ -568,16 +583,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnArgs a) {
     const int n_keys = row_ok ? n_comp + (m - wlo + 1) : 0;
     const int key_lo = split * a.cps * kTcKeys;
     const int key_hi = min(n_keys, key_lo + a.cps * kTcKeys);
-
-    if (tid == 0) {
-        mbar_init(bar, 1);
-        fence_barrier_init();
-    }
-    if (warp == 0) tmem_alloc(s_tmem, L::kTmemCols);
-    for (int h = tid; h < NH; h += kTcThreads) {
-        st_m[h] = -INFINITY;
-        st_l[h] = 0.f;
-    }
     // Q rows of this head group -> B operand layout
     {
         const uint16_t* qsrc = a.q + ((long long)row * a.heads + (long long)hg * NH) * kD;
@@ -598,17 +603,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnArgs a) {
     auto fmax_op = [](float x, float y) { return fmaxf(x, y); };
     auto add_op = [](float x, float y) { return x + y; };
 
-    uint32_t phase = 0;
-    bool ok = true, first = true;
-    for (int kt = key_lo; kt < key_hi && ok; kt += kTcKeys) {
-        // resolve the tile's keys (thread j <-> key kt + j), then gather rows warp by warp
+    // key resolution (top-k index -> block table -> physical row) of the next tile runs one tile
+    // ahead, so its dependent global loads overlap the current tile's copies, MMAs and softmax
+    long long nxt_row = -1;
+    int nxt_flag = 0;
+    auto resolve_tile = [&](int kt) {
         if (tid < kTcKeys) {
             const int j = kt + tid;
             long long p = -1;
             bool sw = false;
             if (j < key_hi) p = resolve_key(a, row, r, m, n_vis, n_comp, wlo, j, &sw);
-            meta_row[tid] = p;
-            meta_flag[tid] = p < 0 ? 0 : (sw ? 2 : 1);
+            nxt_row = p;
+            nxt_flag = p < 0 ? 0 : (sw ? 2 : 1);
+        }
+    };
+    resolve_tile(key_lo);
+
+    uint32_t phase = 0;
+    bool ok = true, first = true;
+    for (int kt = key_lo; kt < key_hi && ok; kt += kTcKeys) {
+        // publish the tile's resolved keys (thread j <-> key kt + j), then gather rows warp by warp
+        if (tid < kTcKeys) {
+            meta_row[tid] = nxt_row;
+            meta_flag[tid] = nxt_flag;
         }
         __syncthreads();
         for (int kk = warp; kk < kTcKeys; kk += kTcThreads / 32) {
@@ -620,6 +637,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnArgs a) {
                 cp_async16(sK + sw128_offset(kk, piece * 8, kTcKeys * 128), src + piece * 16, flag ? 16u : 0u);
         }
         cp_async_commit();
+        if (kt + kTcKeys < key_hi) resolve_tile(kt + kTcKeys);
         cp_async_wait_all();
         fence_proxy_async_smem();  // cp.async writes -> visible to the tensor core (async proxy)
         __syncthreads();
@@ -838,8 +856,10 @@ static dsa_status_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
         cudaSuccess)
         return DSA_ERR_CUDA;
     const long long grid = (long long)a.rows * a.hg_count * a.nsplit;
-    attn_tc_kernel<NH><<<(unsigned)grid, kTcThreads, L::kAlloc, st>>>(a);
-    if (a.nsplit > 1) attn_combine_kernel<<<a.rows * a.heads, 128, 0, st>>>(a);
+    cudaError_t e = launch_pdl(attn_tc_kernel<NH>, dim3((unsigned)grid), dim3(kTcThreads), L::kAlloc, st, a);
+    if (e == cudaSuccess && a.nsplit > 1)
+        e = launch_pdl(attn_combine_kernel, dim3(a.rows * a.heads), dim3(128), 0, st, a);
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
     return launch_status();
 }
 
@@ -849,8 +869,10 @@ static dsa_status_t launch_attn(const AttnArgs& a, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(attn_kernel<HG, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return DSA_ERR_CUDA;
     const long long grid = (long long)a.rows * a.hg_count * a.nsplit;
-    attn_kernel<HG, FP8><<<(unsigned)grid, kThreads, L::kBytes, st>>>(a);
-    if (a.nsplit > 1) attn_combine_kernel<<<a.rows * a.heads, 128, 0, st>>>(a);
+    e = launch_pdl(attn_kernel<HG, FP8>, dim3((unsigned)grid), dim3(kThreads), L::kBytes, st, a);
+    if (e == cudaSuccess && a.nsplit > 1)
+        e = launch_pdl(attn_combine_kernel, dim3(a.rows * a.heads), dim3(128), 0, st, a);
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
     return launch_status();
 }
 

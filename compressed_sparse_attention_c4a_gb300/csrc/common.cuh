@@ -8,6 +8,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "dsa.h"
 
 namespace dsa {
@@ -26,6 +28,22 @@ inline int stride_of(int kind) { return kind == DSA_C4A ? 4 : 128; }
 inline dsa_status_t launch_status() {
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+template <typename... Exp, typename... Act>
+inline cudaError_t launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Act&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...);
 }
 
 inline int sm_count() {
@@ -49,6 +67,15 @@ inline bool table_ok(const dsa_block_table_t* t, int batch) {
 // -------------------------------------------------------------------------------------
 // device side
 // -------------------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library is launched with programmatic stream
+// serialisation, so it may be scheduled while its predecessor on the stream is still running.  Each
+// kernel does only on-chip set-up (barriers, TMEM allocation, shared memory) before pdl_wait(), which
+// returns once the predecessor grid has completed and its writes are visible; it then lets its own
+// dependent start its set-up (pdl_launch_dependents).  So at most one kernel runs ahead, and only
+// through work that touches no global memory.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // First error wins; later errors leave the recorded code in place.
 __device__ __forceinline__ void report(int32_t* status, int32_t code) {
     if (status) atomicCAS(status, 0, code);

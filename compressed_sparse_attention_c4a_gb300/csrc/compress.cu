@@ -133,6 +133,8 @@ __device__ __forceinline__ void rope_row(float (&v)[E], int lane, int dim, const
 
 template <int DIM, int W>
 __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
     constexpr int E = DIM / 32;
     const int lane = threadIdx.x & 31;
     const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -245,6 +247,8 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
 // Rolling-state update after a multi-token append: slot p % w <- token p for the last w new tokens.
 template <int DIM>
 __global__ void __launch_bounds__(256) ring_update_kernel(CompressArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
     constexpr int E = DIM / 32;
     const int lane = threadIdx.x & 31;
     const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -265,14 +269,11 @@ template <int DIM>
 static dsa_status_t launch_compress(const CompressArgs& a, int max_new, cudaStream_t st) {
     const int items = a.entry_items + a.token_items;
     dim3 grid((items + 7) / 8, a.batch);
-    if (a.w == 8)
-        compress_kernel<DIM, 8><<<grid, 256, 0, st>>>(a);
-    else
-        compress_kernel<DIM, 128><<<grid, 256, 0, st>>>(a);
-    if (!a.fuse_ring && max_new > 0) {
-        dim3 g2((a.w + 7) / 8, a.batch);
-        ring_update_kernel<DIM><<<g2, 256, 0, st>>>(a);
-    }
+    cudaError_t e = a.w == 8 ? launch_pdl(compress_kernel<DIM, 8>, grid, dim3(256), 0, st, a)
+                             : launch_pdl(compress_kernel<DIM, 128>, grid, dim3(256), 0, st, a);
+    if (e == cudaSuccess && !a.fuse_ring && max_new > 0)
+        e = launch_pdl(ring_update_kernel<DIM>, dim3((a.w + 7) / 8, a.batch), dim3(256), 0, st, a);
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
     return launch_status();
 }
 

@@ -165,11 +165,6 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     auto stage_meta = [&](int s) { return reinterpret_cast<StageMeta*>(smem + (size_t)s * a.stage_bytes + tiles_bytes); };
 
-    // visible-entry count of every query (grid-strided, independent of the tile loop)
-    if (a.n_visible)
-        for (int q = blockIdx.x * kIdxThreads + tid; q < a.nq; q += gridDim.x * kIdxThreads)
-            a.n_visible[q] = visible_of(a, q);
-
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
@@ -187,6 +182,13 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
+    pdl_wait();  // on-chip set-up above; global memory only below
+    pdl_launch_dependents();
+
+    // visible-entry count of every query (grid-strided, independent of the tile loop)
+    if (a.n_visible)
+        for (int q = blockIdx.x * kIdxThreads + tid; q < a.nq; q += gridDim.x * kIdxThreads)
+            a.n_visible[q] = visible_of(a, q);
 
     if (warp == 0) {
         // ---- producer warp ---------------------------------------------------------------------------
@@ -408,7 +410,9 @@ static dsa_status_t launch_index(const CUtensorMap& kmap, const CUtensorMap& qma
         cudaSuccess)
         return DSA_ERR_CUDA;
     const long long grid = std::min<long long>(a.total_items, (long long)sm_count() * ctas_per_sm);
-    index_kernel<DIM, HEADS><<<(unsigned)std::max<long long>(grid, 1), kIdxThreads, smem, st>>>(kmap, qmap, a);
+    if (launch_pdl(index_kernel<DIM, HEADS>, dim3((unsigned)std::max<long long>(grid, 1)), dim3(kIdxThreads), smem,
+                   st, kmap, qmap, a) != cudaSuccess)
+        return DSA_ERR_CUDA;
     return launch_status();
 }
 

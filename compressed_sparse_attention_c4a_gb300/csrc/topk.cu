@@ -99,6 +99,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float* __re
                                                             const int32_t* __restrict__ n_valid, int k,
                                                             int32_t* __restrict__ idx_out, int32_t* status,
                                                             int resident) {
+    pdl_wait();
+    pdl_launch_dependents();
     extern __shared__ uint32_t smem_topk[];
     uint32_t* hist = smem_topk;                  // [kBins]
     uint32_t* cand_key = hist + kBins;           // [kCandMax]
@@ -328,7 +330,8 @@ extern "C" dsa_status_t dsa_topk(int32_t nq, const float* scores, int32_t ld, co
     if (smem > 227 * 1024) return DSA_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DSA_ERR_CUDA;
-    topk_kernel<<<nq, kTopkThreads, smem, static_cast<cudaStream_t>(stream)>>>(scores, ld, n_valid, k, idx_out,
-                                                                                 dev_status, resident);
+    if (launch_pdl(topk_kernel, dim3(nq), dim3(kTopkThreads), smem, static_cast<cudaStream_t>(stream), scores, ld,
+                   n_valid, k, idx_out, dev_status, resident) != cudaSuccess)
+        return DSA_ERR_CUDA;
     return launch_status();
 }
