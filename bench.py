@@ -291,14 +291,7 @@ def run_gpu(args, rank, world, local_rank):
     # e2e: host (pinned) inputs -> device, step, output -> host, all inside the timed region
     e2e = run_e2e(copies, stream, spec, args, barrier)
 
-    ms_step = ms_total / steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_step, e2e["ms_step"]], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, e2e_ms = float(t[0]), float(t[1])
-    else:
-        e2e_ms = e2e["ms_step"]
+    ms_step, e2e_ms = max_over_ranks([ms_total / steps, e2e["ms_step"]], dev)
     value = q_step * world / (ms_step / 1e3)
     idx_bytes, att_bytes = algorithmic_bytes(spec)
     hbm, tfl, src = peaks()
@@ -324,13 +317,7 @@ def run_gpu(args, rank, world, local_rank):
         "warmup": warm_reps * per_graph, "ms_per_step": round(ms_step, 6), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 attention + e4m3 indexer (fp32 accumulate)",
         "data": "synthetic (seeded N(0,1) caches, queries and tokens; no weights)",
-        "config": {"workload": args.workload, "kind": spec.kind, "batch": spec.batch,
-                   "context": sorted(set(c + n for c, n in zip(spec.cached, spec.new)))[:4],
-                   "new_tokens_per_request": max(spec.new), "heads": spec.heads, "dim": spec.dim,
-                   "indexer": f"{spec.idx_heads}x{spec.idx_dim} e4m3" if spec.idx_heads else None,
-                   "topk": spec.topk or None, "window": spec.window, "kv": spec.main_dtype,
-                   "l2": f"inputs larger than L2: {COPIES} resident cache copies rotate, each step's working set is "
-                         f"evicted by the other copies", "parallelism": f"replicas x{world}"},
+        "config": workload_config(args.workload, spec, world),
         "step_bytes": idx_bytes + att_bytes, "step_gbs": round((idx_bytes + att_bytes) / (ms_step * 1e6), 1),
         "kernels": {n: {k: round(v, 6) for k, v in d.items()} for n, d in kern.items()}, "kernel_timing": timing,
         "roofline": roof, "gpu_launches": launches_per_step * steps, "device_status": status,
@@ -339,6 +326,27 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clk.summary(),
     }
     return line, copies
+
+
+def workload_config(name, spec, world):
+    """The `config` object of both arms' JSON lines."""
+    return {"workload": name, "kind": spec.kind, "batch": spec.batch,
+            "context": sorted(set(c + n for c, n in zip(spec.cached, spec.new)))[:4],
+            "new_tokens_per_request": max(spec.new), "heads": spec.heads, "dim": spec.dim,
+            "indexer": f"{spec.idx_heads}x{spec.idx_dim} e4m3" if spec.idx_heads else None,
+            "topk": spec.topk or None, "window": spec.window, "kv": spec.main_dtype,
+            "l2": f"inputs larger than L2: {COPIES} resident cache copies rotate, each step's working set is "
+                  f"evicted by the other copies", "parallelism": f"replicas x{world}"}
+
+
+def max_over_ranks(values, device):
+    """Element-wise max of per-rank floats over the default process group (identity on one rank)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
 
 
 def run_e2e(copies, stream, spec, args, barrier):
@@ -457,7 +465,7 @@ def cpu_baseline(spec, case, seconds):
             "seconds": round(t, 2)}
 
 
-def run_reference(args, rank):
+def run_reference(args, rank, world):
     spec = synth.case_specs()[args.workload]
     if rank != 0:
         return None
@@ -476,10 +484,10 @@ def run_reference(args, rank):
     ms = statistics.mean(times) * 1e3
     value = qs / (ms / 1e3)
     sample = f"each step: the oracle's whole layer step for {qs} of {queries_per_step(spec)} query tokens"
-    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 0,
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
             "steps": steps, "warmup": 1, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": args.workload, "batch": spec.batch, "heads": spec.heads},
+            "config": workload_config(args.workload, spec, world),
             "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -489,7 +497,7 @@ def main():
     args = parse()
     rank, world, local_rank = rank_env()
     if args.impl == "reference":
-        line = run_reference(args, rank)
+        line = run_reference(args, rank, world)
         if line is not None:
             print(json.dumps(line), flush=True)
         return
