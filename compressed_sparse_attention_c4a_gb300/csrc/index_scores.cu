@@ -79,11 +79,14 @@ __device__ __forceinline__ void group_of(const IdxArgs& a, int g, int* r, int* m
     *max_vis = mv;
 }
 
-// Item (g, t): tile t of group g; `valid` = 0 marks "no item".
-__device__ __forceinline__ ItemInfo item_info(const IdxArgs& a, int valid, int g, int t) {
+// Item (g, t): tile t of group g; `valid` = 0 marks "no item".  The group's request and visible-entry
+// bound come from the producer's shared-memory table (filled once per CTA).
+__device__ __forceinline__ ItemInfo item_info(const IdxArgs& a, int valid, int g, int t, const int* grp_r,
+                                              const int* grp_mv) {
     ItemInfo x{0, g, t, -1, 0, -1, -1};
     if (!valid) return x;
-    group_of(a, g, &x.r, &x.max_vis);
+    x.r = grp_r[g];
+    x.max_vis = grp_mv[g];
     if (x.r < 0 || t * kTileEntries >= x.max_vis) return x;
     x.valid = 1;
     int blk[2] = {-1, -1};
@@ -161,6 +164,8 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
     volatile int* abort_flag = reinterpret_cast<volatile int*>(s_tmem + 1);
     int* grp_nvis = reinterpret_cast<int*>(s_tmem + 2);  // producer warp's cache [64]
     int* grp_prefix = grp_nvis + 64;                     // [n_groups + 1] valid tiles before each group
+    int* grp_r = grp_prefix + a.n_groups + 1;            // [n_groups] request of each group (-1: invalid)
+    int* grp_mv = grp_r + a.n_groups;                    // [n_groups] visible-entry bound of each group
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     auto stage_meta = [&](int s) { return reinterpret_cast<StageMeta*>(smem + (size_t)s * a.stage_bytes + tiles_bytes); };
@@ -203,6 +208,8 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
             if (g < a.n_groups) {
                 int r, mv;
                 group_of(a, g, &r, &mv);
+                grp_r[g] = r;
+                grp_mv[g] = mv;
                 if (r < 0) report(a.status, DSA_ERR_DEVICE_FAULT);
                 else cnt = min((mv + kTileEntries - 1) / kTileEntries, a.tiles);
             }
@@ -235,7 +242,7 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
             int g = 0, t = 0;
             const int valid = lane < kChunkItems && idx < hi;
             if (valid) locate(idx, &g, &t);
-            return item_info(a, valid, g, t);
+            return item_info(a, valid, g, t, grp_r, grp_mv);
         };
         int n = 0, cached_g = -1;
         bool alive = true;
@@ -403,7 +410,7 @@ static dsa_status_t launch_index(const CUtensorMap& kmap, const CUtensorMap& qma
     a.stage_bytes = (payload + 1023) / 1024 * 1024;
     const int ctas_per_sm = a.stage_bytes <= 24 * 1024 ? 2 : 1;
     // alignment slack + barriers, the producer's caches and the per-group prefix of valid tiles
-    const int extra = 1024 + 512 + ((a.n_groups + 1) * 4 + 15) / 16 * 16;
+    const int extra = 1024 + 512 + ((3 * a.n_groups + 1) * 4 + 15) / 16 * 16;
     a.stages = max(2, min(8, (227 * 1024 / ctas_per_sm - extra) / a.stage_bytes));
     const int smem = extra + a.stages * a.stage_bytes;
     if (cudaFuncSetAttribute(index_kernel<DIM, HEADS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
@@ -446,7 +453,7 @@ extern "C" dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim,
         return DSA_ERR_INVALID_ARG;
     if (!aligned(q8, 16) || !aligned(q_scale, 16) || !aligned(w, 16)) return DSA_ERR_INVALID_ARG;
     if (q_group > 64) return DSA_ERR_INVALID_ARG;
-    if ((nq + q_group - 1) / q_group > 16384) return DSA_ERR_UNSUPPORTED;  // per-group prefix lives in smem
+    if ((nq + q_group - 1) / q_group > 4096) return DSA_ERR_UNSUPPORTED;  // per-group tables live in smem
     const int n_cols = ((q_group * heads + 15) / 16) * 16;  // M = 128 needs N % 16 == 0
     IdxArgs a{};
     a.nq = nq;

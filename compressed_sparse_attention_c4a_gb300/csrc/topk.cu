@@ -3,30 +3,36 @@
 // [P1] "DeepSeek DSA、DeepSeek V4与vLLM Hybrid KV Cache详解" §4.2: S_t = TopK(I_{t,:}, k); the
 // main attention reads only S_t.  [P2] "DeepSeek V4 稀疏注意力完全解剖" 机制三: k = 512 for c4a.
 //
-// One CTA (1024 threads) per query row.
-//   1. The row is read once (coalesced 16-byte loads) into shared memory when it fits (rows up to
-//      40,960 entries; longer rows are re-read from L2 in each pass).  Its finite max M and min m are
-//      reduced.
-//   2. Bucket select: bin(v) = 2047 - floor((M - v) * 2046 / (M - m)) for finite v, bin(-inf) = 0.  The
-//      map is monotone (larger score -> same or larger bin; equal scores share a bin) and spreads
-//      scores evenly, so one shared-memory histogram pass has little atomic contention.  A suffix
-//      scan finds the bin b* holding the k-th largest score and `need`, the count still missing.
-//   3. Inside b*: when it holds at most 1024 scores, each candidate is ranked directly against the
-//      others (larger score first, lower index first among equals) and the `need` best are marked in
-//      a bitmap.  Otherwise (heavy ties) a radix select on the 32-bit order keys of the candidates
-//      finds the exact threshold key T and the number of entries equal to T still needed.
-//   4. One pass compacts the selection in increasing index order: thread t owns a contiguous run of
-//      indices (odd length: bank-conflict-free shared-memory reads) and a block scan gives every
-//      selected index its slot; the scan also ranks entries equal to T by index (lowest wins).
+// One thread-block cluster of 4 CTAs (1024 threads each) per query row; CTA q holds the q-th quarter
+// of the row in shared memory.  Partial results are combined through distributed shared memory
+// (each CTA reads the other three CTAs' copies), so every CTA takes the same decisions:
+//   1. max M and min m of the finite scores;
+//   2. bucket select: bin(v) = 2047 - floor((M - v) * 2046 / (M - m)) for finite v, bin(-inf) = 0 --
+//      monotone (larger score -> same or larger bin; equal scores share a bin) and even, so the
+//      shared-memory histogram has little atomic contention; the summed histogram gives the bin b*
+//      holding the k-th largest score and `need`, the count still missing;
+//   3. unless b* holds exactly `need` scores: when it holds at most 256, every CTA publishes its
+//      members of b* and each member counts the better ones (larger score, or equal score and lower
+//      index) across the cluster -- the `need` best are marked; otherwise (heavy ties) a radix
+//      select over the 32-bit order keys of b*'s scores (digits of 11, 11, 10 bits, histograms summed
+//      across the cluster) gives the exact threshold key T and how many entries equal to T are still
+//      needed;
+//   4. ordered compaction: thread t of CTA q owns a contiguous run of indices; a block scan plus the
+//      totals of the lower CTAs give every selected index its slot in increasing index order, and
+//      rank entries equal to T by index (the lowest indices win).
+#include <cooperative_groups.h>
+
 #include "common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace dsa {
 
 constexpr int kTopkThreads = 1024;
+constexpr int kTopkCluster = 4;
 constexpr int kBins = 2048;
-constexpr int kCandMax = 8192;   // candidate keys kept for the radix path
-constexpr int kRankMax = 1024;   // candidates ranked directly (one per thread)
-constexpr int kResidentMax = 40960;
+constexpr int kQuarterMax = 40960;  // scores per CTA kept in shared memory (rows up to 163,840)
+constexpr int kRankMax = 256;       // bucket sizes (cluster-wide) resolved by direct ranking
 
 __device__ __forceinline__ uint32_t order_key(float f) {
     uint32_t u = __float_as_uint(f);
@@ -72,8 +78,8 @@ __device__ __forceinline__ void block_scan2(uint32_t a, uint32_t b, uint32_t* ex
     __syncthreads();
 }
 
-// Given a filled histogram, find the bin (scanning from the top) that holds the need-th largest
-// remaining element; need is reduced by the count above it.  Returns the bin.
+// Given the cluster-wide histogram, find the bin (scanning from the top) that holds the need-th
+// largest remaining element; need is reduced by the count above it.  Returns the bin.
 __device__ __forceinline__ uint32_t select_bin(const uint32_t* hist, uint32_t& need, uint32_t (*warp_tot)[2],
                                                uint32_t* sel) {
     const int tid = threadIdx.x;
@@ -95,223 +101,252 @@ __device__ __forceinline__ uint32_t select_bin(const uint32_t* hist, uint32_t& n
     return b;
 }
 
-__global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const float* __restrict__ scores, int ld,
-                                                            const int32_t* __restrict__ n_valid, int k,
-                                                            int32_t* __restrict__ idx_out, int32_t* status,
-                                                            int resident) {
+// hsum[b] = sum over the cluster's CTAs of their local hist[b]; ends with a block barrier.
+__device__ __forceinline__ void cluster_hist_sum(cg::cluster_group& cluster, uint32_t* hist, uint32_t* hsum) {
+    cluster.sync();  // every CTA's local histogram is complete
+    uint32_t* remote[kTopkCluster];
+#pragma unroll
+    for (int c = 0; c < kTopkCluster; ++c) remote[c] = cluster.map_shared_rank(hist, c);
+    for (int b = threadIdx.x; b < kBins; b += kTopkThreads) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int c = 0; c < kTopkCluster; ++c) v += remote[c][b];
+        hsum[b] = v;
+    }
+    __syncthreads();
+}
+
+__global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads, 1)
+    topk_kernel(const float* __restrict__ scores, int ld, const int32_t* __restrict__ n_valid, int k,
+                int32_t* __restrict__ idx_out, int32_t* status) {
     pdl_wait();
     pdl_launch_dependents();
+    cg::cluster_group cluster = cg::this_cluster();
     extern __shared__ uint32_t smem_topk[];
-    uint32_t* hist = smem_topk;                  // [kBins]
-    uint32_t* cand_key = hist + kBins;           // [kCandMax]
-    uint32_t* cand_idx = cand_key + kCandMax;    // [kRankMax]
-    uint32_t* marks = cand_idx + kRankMax;       // [ld / 32 + 1] bitmap of ranked winners
-    float* rowv = reinterpret_cast<float*>(marks + (ld >> 5) + 1);  // [ld] the row (resident mode)
+    uint32_t* hist = smem_topk;                             // [kBins] this CTA's histogram
+    uint32_t* hsum = hist + kBins;                          // [kBins] cluster-wide histogram
+    uint32_t* cand_key = hsum + kBins;                      // [kRankMax] this CTA's members of b*
+    uint32_t* cand_idx = cand_key + kRankMax;               // [kRankMax] their row indices
+    uint32_t* marks = cand_idx + kRankMax;                  // [chunk / 32 + 1] ranked winners (local index)
+    float* rowv = reinterpret_cast<float*>(marks + kQuarterMax / 32 + 1);  // this CTA's quarter of the row
+    __shared__ uint32_t n_cand;
     __shared__ uint32_t warp_tot[32][2];
     __shared__ uint32_t sel[2];
-    __shared__ uint32_t n_cand;
-    __shared__ float red_max[32], red_min[32];
+    __shared__ float red[2];
+    __shared__ uint32_t totals[2];
 
-    const int row = blockIdx.x;
+    const int row = blockIdx.x / kTopkCluster;
+    const int qr = (int)cluster.block_rank();
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     int32_t* out = idx_out + (long long)row * k;
-    const int n = n_valid[row];
+    const int n = n_valid[row];  // the same for the whole cluster: every branch below is cluster-uniform
     if (n < 0 || n > ld) {
-        if (tid == 0) report(status, DSA_ERR_DEVICE_FAULT);
-        for (int i = tid; i < k; i += kTopkThreads) out[i] = -1;
+        if (qr == 0) {
+            if (tid == 0) report(status, DSA_ERR_DEVICE_FAULT);
+            for (int i = tid; i < k; i += kTopkThreads) out[i] = -1;
+        }
         return;
     }
     if (n <= k) {
-        for (int i = tid; i < k; i += kTopkThreads) out[i] = i < n ? i : -1;
+        if (qr == 0)
+            for (int i = tid; i < k; i += kTopkThreads) out[i] = i < n ? i : -1;
         return;
     }
     const float* s = scores + (long long)row * ld;
+    const int chunk = ((n + kTopkCluster - 1) / kTopkCluster + 3) & ~3;  // multiple of 4: aligned float4 loads
+    const int base = qr * chunk;
+    const int mq = max(0, min(n, base + chunk) - base);  // scores in this CTA's quarter
+
+    // 1. quarter -> shared memory, local max / min, then the cluster's
     float mx = -INFINITY, mn = INFINITY;
-    if (resident) {
-        // up to 4 float4 loads per thread in flight before any is consumed
-        for (int i0 = tid * 4; i0 < n; i0 += kTopkThreads * 16) {
-            float4 q[4];
+    for (int i0 = tid * 4; i0 < mq; i0 += kTopkThreads * 16) {
+        float4 q[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = i0 + u * kTopkThreads * 4;
-                q[u] = i + 4 <= n ? *reinterpret_cast<const float4*>(s + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = i0 + u * kTopkThreads * 4;
-                float v[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-                if (i + 4 > n)
-                    for (int e = 0; e < 4; ++e) v[e] = i + e < n ? s[i + e] : -INFINITY;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if (i + e < n) rowv[i + e] = v[e];
-                    if (v[e] != -INFINITY) {
-                        mx = fmaxf(mx, v[e]);
-                        mn = fminf(mn, v[e]);
-                    }
-                }
-            }
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * kTopkThreads * 4;
+            q[u] = i + 4 <= mq ? *reinterpret_cast<const float4*>(s + base + i) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-    } else {
-        for (int i = tid; i < n; i += kTopkThreads) {
-            const float v = __ldg(s + i);
-            if (v != -INFINITY) {
-                mx = fmaxf(mx, v);
-                mn = fminf(mn, v);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * kTopkThreads * 4;
+            float v[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+            if (i + 4 > mq)
+                for (int e = 0; e < 4; ++e) v[e] = i + e < mq ? s[base + i + e] : -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (i + e < mq) rowv[i + e] = v[e];
+                if (v[e] != -INFINITY) {
+                    mx = fmaxf(mx, v[e]);
+                    mn = fminf(mn, v[e]);
+                }
             }
         }
     }
     for (int b = tid; b < kBins; b += kTopkThreads) hist[b] = 0;
-    for (int w = tid; w <= (ld >> 5); w += kTopkThreads) marks[w] = 0;
+    for (int w = tid; w <= (mq >> 5); w += kTopkThreads) marks[w] = 0;
     if (tid == 0) n_cand = 0;
     mx = warp_max(mx);
     mn = -warp_max(-mn);
     if (lane == 0) {
-        red_max[wid] = mx;
-        red_min[wid] = mn;
+        warp_tot[wid][0] = __float_as_uint(mx);
+        warp_tot[wid][1] = __float_as_uint(mn);
     }
     __syncthreads();
     if (wid == 0) {
-        float a = warp_max(red_max[lane]), b = -warp_max(-red_min[lane]);
+        const float a = warp_max(__uint_as_float(warp_tot[lane][0]));
+        const float b = -warp_max(-__uint_as_float(warp_tot[lane][1]));
         if (lane == 0) {
-            red_max[0] = a;
-            red_min[0] = b;
+            red[0] = a;
+            red[1] = b;
         }
     }
-    __syncthreads();
-    mx = red_max[0];
-    mn = red_min[0];
+    cluster.sync();
+    mx = -INFINITY;
+    mn = INFINITY;
+#pragma unroll
+    for (int c = 0; c < kTopkCluster; ++c) {
+        const float* rr = cluster.map_shared_rank(red, c);
+        mx = fmaxf(mx, rr[0]);
+        mn = fminf(mn, rr[1]);
+    }
     const bool any_finite = mx != -INFINITY;
     float scale = (any_finite && mx > mn) ? 2046.f / (mx - mn) : 0.f;
-    if (!isfinite(scale)) scale = 0.f;  // degenerate range: one bucket, resolved by the radix path
-    auto val_at = [&](int i) -> float { return resident ? rowv[i] : __ldg(s + i); };
+    if (!isfinite(scale)) scale = 0.f;  // degenerate range: one bucket, resolved by the radix passes
     auto bin_of = [&](float v) -> uint32_t {
         if (v == -INFINITY) return 0u;
         return 2047u - (uint32_t)fminf(2046.f, (mx - v) * scale);
     };
 
-    // 2. value-bucket histogram and the bucket of the k-th largest score
-    for (int i = tid; i < n; i += kTopkThreads) atomicAdd(&hist[bin_of(val_at(i))], 1u);
-    __syncthreads();
+    // 2. value buckets: local histogram, cluster-wide sum, the bucket of the k-th largest score
+    for (int i = tid; i < mq; i += kTopkThreads) atomicAdd(&hist[bin_of(rowv[i])], 1u);
+    cluster_hist_sum(cluster, hist, hsum);
     uint32_t need = (uint32_t)k;
-    const uint32_t bstar = select_bin(hist, need, warp_tot, sel);
-    const uint32_t in_bucket = hist[bstar];
+    const uint32_t bstar = select_bin(hsum, need, warp_tot, sel);
+    const uint32_t in_bucket = hsum[bstar];
     const bool take_all = in_bucket == need;
     const bool rank_mode = !take_all && in_bucket <= (uint32_t)kRankMax;
-    uint32_t T = 0u, need_T = 0u;  // radix path: threshold key and entries equal to it still needed
 
-    // 3. resolve the bucket
-    if (!take_all) {
-        const bool keep = in_bucket <= (uint32_t)kCandMax;
-        if (rank_mode || keep) {
-            for (int i = tid; i < n; i += kTopkThreads) {
-                const float v = val_at(i);
-                const bool take = bin_of(v) == bstar;
-                const unsigned active = __activemask();
-                const unsigned ballot = __ballot_sync(active, take);
-                if (ballot) {
-                    const int leader = __ffs(ballot) - 1;
-                    uint32_t base = 0;
-                    if (lane == leader) base = atomicAdd(&n_cand, (uint32_t)__popc(ballot));
-                    base = __shfl_sync(active, base, leader);
-                    if (take) {
-                        const uint32_t slot = base + __popc(ballot & ((1u << lane) - 1u));
-                        cand_key[slot] = order_key(v);
-                        if (rank_mode) cand_idx[slot] = (uint32_t)i;
-                    }
+    // 3a. small bucket: rank its members directly across the cluster
+    if (rank_mode) {
+        for (int i = tid; i < mq; i += kTopkThreads) {
+            const float v = rowv[i];
+            const bool take = bin_of(v) == bstar;
+            const unsigned active = __activemask();
+            const unsigned ballot = __ballot_sync(active, take);
+            if (ballot) {
+                const int leader = __ffs(ballot) - 1;
+                uint32_t slot0 = 0;
+                if (lane == leader) slot0 = atomicAdd(&n_cand, (uint32_t)__popc(ballot));
+                slot0 = __shfl_sync(active, slot0, leader);
+                if (take) {
+                    const uint32_t slot = slot0 + __popc(ballot & ((1u << lane) - 1u));
+                    cand_key[slot] = order_key(v);
+                    cand_idx[slot] = (uint32_t)(base + i);
                 }
             }
-            __syncthreads();
         }
-        if (rank_mode) {
-            const int nc = (int)n_cand;
-            if (tid < nc) {
-                const uint32_t my_k = cand_key[tid], my_i = cand_idx[tid];
-                uint32_t better = 0;
+        cluster.sync();  // every CTA's member list is complete
+        if (tid < (int)n_cand) {
+            const uint32_t my_k = cand_key[tid], my_i = cand_idx[tid];
+            uint32_t better = 0;
+#pragma unroll 1
+            for (int c = 0; c < kTopkCluster; ++c) {
+                const uint32_t* rk = cluster.map_shared_rank(cand_key, c);
+                const uint32_t* ri = cluster.map_shared_rank(cand_idx, c);
+                const int nc = (int)*cluster.map_shared_rank(&n_cand, c);
                 for (int j = 0; j < nc; ++j) {
-                    const uint32_t kj = cand_key[j];
-                    better += (kj > my_k) || (kj == my_k && cand_idx[j] < my_i);
+                    const uint32_t kj = rk[j];
+                    better += (kj > my_k) || (kj == my_k && ri[j] < my_i);
                 }
-                if (better < need) atomicOr(&marks[my_i >> 5], 1u << (my_i & 31));
             }
-            __syncthreads();
-        } else {
-            // radix select on the order keys of the bucket's entries: digits of 11, 11 and 10 bits
-            uint32_t prefix = 0u, mask = 0u;
-            need_T = need;
-            for (int pass = 0; pass < 3; ++pass) {
-                const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-                const uint32_t dm = pass == 2 ? 0x3FFu : 0x7FFu;
-                for (int b = tid; b < kBins; b += kTopkThreads) hist[b] = 0;
-                __syncthreads();
-                if (keep) {
-                    const int nc = (int)n_cand;
-                    for (int i = tid; i < nc; i += kTopkThreads) {
-                        const uint32_t key = cand_key[i];
-                        if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
-                    }
-                } else {
-                    for (int i = tid; i < n; i += kTopkThreads) {
-                        const float v = val_at(i);
-                        const uint32_t key = order_key(v);
-                        if (bin_of(v) == bstar && (key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
-                    }
-                }
-                __syncthreads();
-                const uint32_t d = select_bin(hist, need_T, warp_tot, sel);
-                prefix |= d << sh;
-                mask |= dm << sh;
+            if (better < need) {
+                const uint32_t li = my_i - (uint32_t)base;
+                atomicOr(&marks[li >> 5], 1u << (li & 31));
             }
-            T = prefix;
         }
+        __syncthreads();
     }
 
-    // 4. ordered compaction: definite winners, plus entries equal to T ranked by index (radix path)
-    int run = (n + kTopkThreads - 1) / kTopkThreads;  // <= 64 (ld <= 65,536)
-    if (resident) run |= 1;                              // odd: conflict-free strided smem reads (<= 41)
-    const int lo = min(n, tid * run), hi = min(n, lo + run);
-    auto classify = [&](int i, bool* def, bool* tie) {
-        const float v = val_at(i);
-        const uint32_t b = bin_of(v);
-        *def = false;
-        *tie = false;
-        if (b > bstar) *def = true;
-        else if (b == bstar) {
-            if (take_all) *def = true;
-            else if (rank_mode) *def = (marks[i >> 5] >> (i & 31)) & 1u;
-            else {
+    // 3b. heavy ties: radix select inside b* for the threshold key T and the entries equal to T still needed
+    uint32_t T = 0u, need_T = 0u, prefix = 0u, mask = 0u;
+    if (!take_all && !rank_mode) {
+        need_T = need;
+        for (int pass = 0; pass < 3; ++pass) {
+            const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+            const uint32_t dm = pass == 2 ? 0x3FFu : 0x7FFu;
+            cluster.sync();  // the other CTAs are done reading this CTA's previous histogram
+            for (int b = tid; b < kBins; b += kTopkThreads) hist[b] = 0;
+            __syncthreads();
+            for (int i = tid; i < mq; i += kTopkThreads) {
+                const float v = rowv[i];
                 const uint32_t key = order_key(v);
-                *def = key > T;
-                *tie = key == T;
+                if (bin_of(v) == bstar && (key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
             }
+            cluster_hist_sum(cluster, hist, hsum);
+            const uint32_t d = select_bin(hsum, need_T, warp_tot, sel);
+            prefix |= d << sh;
+            mask |= dm << sh;
         }
-    };
-    // a thread's run is at most 64 entries (rows up to 65,535 scores), so its classification fits two
-    // 64-bit masks: computed once, used for the counts and again for the writes
+        T = prefix;
+    }
+
+    // 4. ordered compaction over the quarter
+    int run = (mq + kTopkThreads - 1) / kTopkThreads;  // <= 40
+    run |= 1;                                          // odd: conflict-free strided shared-memory reads
+    const int lo = min(mq, tid * run), hi = min(mq, lo + run);
     unsigned long long mdef = 0ull, mtie = 0ull;
     for (int i = lo; i < hi; ++i) {
-        bool d, t;
-        classify(i, &d, &t);
+        const float v = rowv[i];
+        const uint32_t b = bin_of(v);
+        bool d = b > bstar, t = false;
+        if (b == bstar) {
+            if (take_all) d = true;
+            else if (rank_mode) d = (marks[i >> 5] >> (i & 31)) & 1u;
+            else {
+                const uint32_t key = order_key(v);
+                d = key > T;
+                t = key == T;
+            }
+        }
         mdef |= (unsigned long long)d << (i - lo);
         mtie |= (unsigned long long)t << (i - lo);
     }
-    const uint32_t cd = __popcll(mdef), ct = __popcll(mtie);
     uint32_t ex_d, ex_t, tot_d, tot_t;
-    block_scan2(cd, ct, &ex_d, &ex_t, &tot_d, &tot_t, warp_tot);
-    uint32_t tie_rank = ex_t;
-    uint32_t pos = ex_d + min(ex_t, need_T);
-    for (unsigned long long m = mdef | mtie; m; m &= m - 1) {
-        const int b = __ffsll((long long)m) - 1;
+    block_scan2((uint32_t)__popcll(mdef), (uint32_t)__popcll(mtie), &ex_d, &ex_t, &tot_d, &tot_t, warp_tot);
+    if (tid == 0) {
+        totals[0] = tot_d;
+        totals[1] = tot_t;
+    }
+    cluster.sync();
+    uint32_t base_d = 0, base_t = 0, all_d = 0, all_t = 0;
+#pragma unroll
+    for (int c = 0; c < kTopkCluster; ++c) {
+        const uint32_t* tt = cluster.map_shared_rank(totals, c);
+        const uint32_t a = tt[0], b = tt[1];
+        if (c < qr) {
+            base_d += a;
+            base_t += b;
+        }
+        all_d += a;
+        all_t += b;
+    }
+    uint32_t tie_rank = base_t + ex_t;
+    uint32_t pos = base_d + ex_d + min(tie_rank, need_T);
+    for (unsigned long long mm = mdef | mtie; mm; mm &= mm - 1) {
+        const int b = __ffsll((long long)mm) - 1;
         if ((mdef >> b) & 1ull) {
-            out[pos++] = lo + b;
+            out[pos++] = base + lo + b;
         } else {
-            if (tie_rank < need_T) out[pos++] = lo + b;
+            if (tie_rank < need_T) out[pos++] = base + lo + b;
             ++tie_rank;
         }
     }
-    const uint32_t total = tot_d + min(tot_t, need_T);
-    for (int i = (int)total + tid; i < k; i += kTopkThreads) out[i] = -1;
-    if (tid == 0 && total != (uint32_t)k) report(status, DSA_ERR_DEVICE_FAULT);
+    const uint32_t total = all_d + min(all_t, need_T);
+    if (qr == kTopkCluster - 1) {
+        for (int i = (int)total + tid; i < k; i += kTopkThreads) out[i] = -1;
+        if (tid == 0 && total != (uint32_t)k) report(status, DSA_ERR_DEVICE_FAULT);
+    }
+    cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 }  // namespace dsa
@@ -323,15 +358,14 @@ extern "C" dsa_status_t dsa_topk(int32_t nq, const float* scores, int32_t ld, co
     if (nq < 0 || k < 1 || k > 2048 || ld < 0 || (ld & 3)) return DSA_ERR_INVALID_ARG;
     if (nq == 0) return DSA_OK;
     if (!scores || !n_valid || !idx_out || !aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
-    if (ld > 64 * kTopkThreads) return DSA_ERR_UNSUPPORTED;  // a thread's run must fit a 64-bit mask
-    const int resident = ld <= kResidentMax ? 1 : 0;
-    const size_t words = (size_t)kBins + kCandMax + kRankMax + (ld >> 5) + 1 + (resident ? ld : 0);
-    const size_t smem = words * sizeof(uint32_t);
-    if (smem > 227 * 1024) return DSA_ERR_UNSUPPORTED;
+    const int chunk = ((ld + kTopkCluster - 1) / kTopkCluster + 3) & ~3;
+    if (chunk > kQuarterMax) return DSA_ERR_UNSUPPORTED;
+    const size_t smem = (size_t)(2 * kBins + 2 * kRankMax + kQuarterMax / 32 + 1) * sizeof(uint32_t) +
+                        (size_t)chunk * sizeof(float);
     if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DSA_ERR_CUDA;
-    if (launch_pdl(topk_kernel, dim3(nq), dim3(kTopkThreads), smem, static_cast<cudaStream_t>(stream), scores, ld,
-                   n_valid, k, idx_out, dev_status, resident) != cudaSuccess)
+    if (launch_pdl(topk_kernel, dim3(nq * kTopkCluster), dim3(kTopkThreads), smem, static_cast<cudaStream_t>(stream),
+                   scores, ld, n_valid, k, idx_out, dev_status) != cudaSuccess)
         return DSA_ERR_CUDA;
     return launch_status();
 }

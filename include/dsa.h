@@ -140,8 +140,9 @@ dsa_status_t dsa_compress(int32_t kind, int32_t batch, const int32_t* cu_new, co
  * q8         [nq][heads][dim] e4m3 bytes;  q_scale, w: [nq][heads] fp32
  * q_pos      [nq] int32 position m of each query;  q_req [nq] int32 request of each query
  * q_group    host int in 1 .. 256/heads: queries g*q_group .. g*q_group + q_group - 1 must
- *            belong to one request (decode: 1; chunked prefill: up to 256/heads); a group
- *            that mixes requests raises DSA_ERR_DEVICE_FAULT
+ *            belong to one request (decode: 1; chunked prefill: up to 256/heads, at most 64); a
+ *            group that mixes requests raises DSA_ERR_DEVICE_FAULT; at most 4096 groups
+ *            (ceil(nq / q_group)), else DSA_ERR_UNSUPPORTED
  * keys       fp8 pool, rows_per_block 64, dim = dim; bt: its block table
  * scores     [nq][ld] fp32 out: I(m, i) for i < n_vis(m); -inf for n_vis(m) <= i < the end of
  *            the 128-entry tile holding n_vis(m) - 1; the rest of the row is not written
@@ -160,7 +161,7 @@ dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim, const uint
  * order, padded with -1 when n_valid[q] < k.  Exact (radix select on the fp32 bit
  * patterns); NaN scores are not supported.
  *
- * nq, k      host ints; 1 <= k <= 2048
+ * nq, k      host ints; 1 <= k <= 2048; ld <= 163,840 (else DSA_ERR_UNSUPPORTED)
  * scores     [nq][ld] fp32;  n_valid [nq] int32 in [0, ld]
  * idx_out    [nq][k] int32 out
  */
