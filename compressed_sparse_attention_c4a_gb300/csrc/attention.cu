@@ -469,39 +469,65 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
 // ---------------------------------------------------------------------------------------------
 // bf16 rows on the 5th-generation tensor cores (tcgen05, TMEM accumulators).
 //
-// One CTA (4 warps) per (query row, group of NH heads, key split); a split is a run of 128-key
-// tiles.  For each tile the 128 key rows are gathered through the block tables into shared memory
-// in 128B-swizzled 8-row x 128-byte atoms, laid out [64-dim chunk][8-key group][8 keys][128 B].
-// That one copy serves both products (K = V):
-//   S^T = K Q^T   : A = K tile, K-major (M = 128 keys, K = 512 dims), B = Q (N = NH heads, K-major),
-//                   accumulated in TMEM columns [0, NH): lane = key, column = head;
-//   O^T += V^T P^T: A = the same tile read MN-major (M = 128 dims per MMA, K = 16 keys),
-//                   B = P^T (N = NH heads, K = keys, K-major), four 128-dim tiles in TMEM columns
-//                   [NH, 5 NH): lane = dim, column = head.
-// Softmax runs per head over TMEM lanes: each thread holds one key's NH logits; per-head max and sum
-// are warp shuffle reductions plus a 4-warp combine in shared memory (online across tiles, with O^T
-// rescaled in TMEM when a head's max grows).  The epilogue reads O^T (lane = dim), applies 1/l and
-// R_m^-1 (pairs of dims sit in neighbouring lanes) and stores bf16, or writes split-K partials.
+// Work split.  A row's keys (top-k entries, then window positions) form 64-key sub-tiles.  One
+// cluster of CL CTAs (CL = 1, 2 or 4, chosen at launch) serves one (query row, group of NH <= 64 heads,
+// key split); CTA c of the cluster takes the split's sub-tiles c, c + CL, c + 2 CL, ...  Each CTA keeps
+// its partial softmax state on chip, and the cluster merges the CL partials through distributed
+// shared memory, so a split-K workspace in global memory is needed only when one cluster per row is
+// not enough to fill the GPU (several splits per row, merged by attn_combine_kernel).
+//
+// Inside a CTA (288 threads), warp-specialised and pipelined over two 64 KB key stages:
+//   warps 4-7  gather: resolve the sub-tile's keys (top-k index -> block table -> physical row, one
+//              sub-tile ahead) and copy the rows into a stage with cp.async, 128B-swizzled,
+//              laid out [64-dim chunk][8-key group][8 keys][128 B] (the query rows are copied with
+//              the first sub-tile into the same layout, padded with zero rows to 64);
+//   warp 8     issues the MMAs (one thread):
+//              S   = Q K^T   : M = 64 (heads), N = 64 keys, K = 512; TMEM lanes = heads, columns = keys;
+//              O^T += V^T P^T: M = 128 dims per MMA (the stage read MN-major, K = V), N = NH heads,
+//                              K = 64 keys; four 128-dim accumulators, lanes = dims, columns = heads;
+//              S of sub-tile i + 1 is issued before O^T of sub-tile i, so it overlaps the softmax;
+//   warps 0-3  softmax, one thread per head (lanes 0-15 of each quadrant hold the M = 64 rows): the
+//              64 logits of a sub-tile are a row of TMEM, so max and sum are thread-local; P is
+//              written as the head's 128-byte row of the P^T operand.  The running maximum is
+//              lazy: it moves (and O^T is rescaled in TMEM) only when a sub-tile's maximum exceeds it
+//              by more than 2^8, so exp2(s - m) <= 2^8 stays exact in fp32 and rescales are rare.
+// Merge: each CTA sends (m, l) per head to every CTA of the cluster, then scales its O^T by
+// 2^(m - M) (M the cluster maximum) and sends each 128-dim tile to the CTA that owns it (tile t
+// belongs to CTA t mod CL), into that CTA's now idle key stages.  The owner sums the CL tiles,
+// divides by L and applies R_m^-1 (pairs of dims sit in neighbouring lanes) before the bf16 store,
+// or writes an fp32 partial with (M, L) when the row has several splits.
 // ---------------------------------------------------------------------------------------------
-constexpr int kTcKeys = 128;
-constexpr int kTcThreads = 256;  // 8 warps: two per TMEM lane quadrant
+constexpr int kClKeys = 64;                 // keys per sub-tile
+constexpr int kClGatherWarps = 11;          // warps 5 .. 15
+constexpr int kClThreads = 32 * (5 + kClGatherWarps);
+constexpr int kClGatherThreads = 32 * kClGatherWarps;
+constexpr int kClRound = kClGatherThreads / kClKeys;   // sub-tiles resolved per round (5)
+constexpr int kClRing = 2 * kClRound;                  // resolved sub-tiles kept (a ring of 10)
+constexpr int kClStage = kClKeys * kD * 2;
+constexpr float kLazyLog2 = 8.f;            // the running maximum moves when exceeded by more than this
 
 template <int NH>
-struct TcSmem {
-    static constexpr int kQ = NH * kD * 2;          // [8][NH][128 B]
-    static constexpr int kK = kTcKeys * kD * 2;     // [8][128][128 B]
-    static constexpr int kP = NH * kTcKeys * 2;     // [2][NH][128 B]
+struct ClSmem {
+    static constexpr int kQ = 64 * kD * 2;                          // [8][64 rows][128 B]
+    static constexpr int kP = NH * kClKeys * 2;                     // [NH rows][128 B]
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kQ;
-    static constexpr int kOffP = kOffK + kK;
-    static constexpr int kOffMeta = kOffP + kP;                  // long long [128]
-    static constexpr int kOffFlag = kOffMeta + kTcKeys * 8;      // int [128]
-    static constexpr int kOffRed = kOffFlag + kTcKeys * 4;       // float [4][NH] x 2
-    static constexpr int kOffStat = kOffRed + 2 * 4 * NH * 4;    // float m[NH], l[NH], mnew[NH], alpha[NH]
-    static constexpr int kOffBar = kOffStat + 4 * NH * 4;        // mbarrier, tmem address
-    static constexpr int kBytes = kOffBar + 64;
-    static constexpr int kAlloc = kBytes + 1024;                 // + alignment slack
-    static constexpr int kTmemCols = 5 * NH <= 128 ? 128 : (5 * NH <= 256 ? 256 : 512);
+    static constexpr int kOffK = kOffQ + kQ;                        // two stages; exchanged tiles at the end
+    static constexpr int kOffP = kOffK + 2 * kClStage;              // two P^T buffers; output staging at the end
+    static constexpr int kOffRow = kOffP + 2 * kP;                  // int [ring][64]: physical rows (-1 masked)
+    static constexpr int kOffPool = kOffRow + kClRing * kClKeys * 4;  // uint8 [ring][64]: 1 main, 2 window
+    static constexpr int kOffMask = kOffPool + kClRing * kClKeys;   // uint32 [2][2]: valid keys of a stage
+    static constexpr int kOffAlpha = kOffMask + 16;                 // float [2][NH]
+    static constexpr int kOffVote = kOffAlpha + 2 * NH * 4;         // int [2][4]
+    static constexpr int kOffOwn = kOffVote + 32;                   // float m[NH], l[NH] of this CTA
+    static constexpr int kOffStat = kOffOwn + 2 * NH * 4;           // float [4 ranks][NH][2]: (m, l) of each CTA
+    static constexpr int kOffFac = kOffStat + 4 * NH * 8;           // float f[NH], L[NH], M[NH], 1/L[NH]
+    static constexpr int kOffBar = kOffFac + 4 * NH * 4;            // 10 mbarriers, TMEM address
+    static constexpr int kBytes = kOffBar + 10 * 8 + 16;
+    static constexpr int kAlloc = kBytes + 1024;                    // + alignment slack
+    static constexpr int kTile = 128 * NH * 4;                      // one 128-dim O tile, fp32 [NH / 4][128] float4
+    static_assert(6 * kTile <= kQ + 2 * kClStage, "sent and received tiles must fit in the query rows and stages");
+    static_assert(NH * 128 * 2 <= 2 * kP, "an output tile must fit in the P^T buffers");
+    static constexpr int kTmemCols = 128 + 4 * NH <= 256 ? 256 : 512;
 };
 
 // Byte offset of element (row r, element e) in a tile of 128B-swizzled atoms whose rows are 128 bytes
@@ -512,319 +538,490 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int e, int chunk_stride)
                       ((in & 7) << 1));
 }
 
-// Reduce N values per lane across the 32 lanes of a warp, transposed: after log2(32) exchange steps
-// lane l holds the reduction (over all lanes) of value index l * N / 32 (N <= 32), using N - 1
-// shuffles instead of 5 N.  `op` is max or add.
-template <int N, typename Op>
-__device__ __forceinline__ float transpose_reduce(float (&v)[N], Op op) {
-    const int lane = threadIdx.x & 31;
-    int n = N;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        if (n > 1) {
-            const bool upper = (lane & o) != 0;
-#pragma unroll
-            for (int i = 0; i < N / 2; ++i) {
-                if (i < n / 2) {
-                    const float send = upper ? v[i] : v[i + n / 2];
-                    const float keep = upper ? v[i + n / 2] : v[i];
-                    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, o));
-                }
-            }
-            n >>= 1;
-        } else {
-            v[0] = op(v[0], __shfl_xor_sync(0xffffffffu, v[0], o));
+// Key j of a row for the tensor-core kernel.  Keys [0, n_comp) are compressed slots, [n_comp, ncp) padding
+// up to a multiple of 4, [ncp, ncp + window count) window positions.  Returns the physical row (pool in
+// *pool: 1 main, 2 window) or -1 for a masked key; reports faults.
+__device__ __forceinline__ int resolve_key4(const AttnArgs& a, int row, int r, int n_vis, int n_comp, int ncp,
+                                            int wlo, int j, int* pool) {
+    if (j < ncp) {
+        *pool = 1;
+        if (j >= n_comp) return -1;
+        const int id = a.topk ? __ldg(a.topk + (long long)row * a.k + j) : j;
+        if (id < 0) return -1;
+        if (id >= n_vis) {
+            report(a.status, DSA_ERR_DEVICE_FAULT);
+            return -1;
         }
+        const long long p = physical_row(a.main_bt, r, id, a.main.rows_per_block, a.main.num_blocks);
+        if (p < 0) report(a.status, DSA_ERR_DEVICE_FAULT);
+        return (int)p;
     }
-    return v[0];
+    *pool = 2;
+    const long long p = physical_row(a.swa_bt, r, (long long)wlo + (j - ncp), kBlockPositions, a.swa.num_blocks);
+    if (p < 0) report(a.status, DSA_ERR_DEVICE_FAULT);
+    return (int)p;
 }
 
 template <int NH>
-__global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnArgs a) {
-    using L = TcSmem<NH>;
-    constexpr int HH = NH / 2;  // heads per warp in the softmax (the two warps of a quadrant split them)
+__global__ void __launch_bounds__(kClThreads, 1)
+    attn_cl_kernel(const __grid_constant__ CUtensorMap qmap, AttnArgs a) {
+    using L = ClSmem<NH>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sQ = smem_u32(smem + L::kOffQ), sK = smem_u32(smem + L::kOffK), sP = smem_u32(smem + L::kOffP);
-    long long* meta_row = reinterpret_cast<long long*>(smem + L::kOffMeta);
-    int* meta_flag = reinterpret_cast<int*>(smem + L::kOffFlag);
-    float* red_a = reinterpret_cast<float*>(smem + L::kOffRed);
-    float* red_b = red_a + 4 * NH;
-    float* st_m = reinterpret_cast<float*>(smem + L::kOffStat);
-    float* st_l = st_m + NH;
-    float* st_mnew = st_l + NH;
-    float* st_alpha = st_mnew + NH;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar + 1);
+    int* s_row = reinterpret_cast<int*>(smem + L::kOffRow);
+    uint8_t* s_pool = smem + L::kOffPool;
+    uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + L::kOffMask);
+    float* s_alpha = reinterpret_cast<float*>(smem + L::kOffAlpha);
+    int* s_vote = reinterpret_cast<int*>(smem + L::kOffVote);
+    float* s_own = reinterpret_cast<float*>(smem + L::kOffOwn);
+    float* s_stat = reinterpret_cast<float*>(smem + L::kOffStat);
+    float* s_fac = reinterpret_cast<float*>(smem + L::kOffFac);
+    float* s_L = s_fac + NH;
+    float* s_M = s_L + NH;
+    float* s_inv = s_M + NH;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // stage gathered (gather threads)
+    uint64_t* sfull = full + 2;                                         // S in TMEM (MMA commit)
+    uint64_t* pfull = full + 4;                                         // P^T written (4 warps)
+    uint64_t* pvdone = full + 6;                                        // O^T += V^T P^T done (commit)
+    uint64_t* qfull = full + 8;                                         // query rows loaded
+    uint64_t* xfull = full + 9;                                         // exchanged tiles loaded
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(full + 10);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int quad = warp & 3, half = warp >> 2;  // TMEM lanes 32 quad .. ; heads / dim tiles of this half
-    const int split = blockIdx.x % a.nsplit;
-    const int hg = (blockIdx.x / a.nsplit) % a.hg_count;
-    const int row = blockIdx.x / (a.nsplit * a.hg_count);
+    const int crank = (int)cluster_ctarank(), csize = (int)cluster_nctarank();
+    const int cid = blockIdx.x / csize;
+    const int split = cid % a.nsplit;
+    const int hg = (cid / a.nsplit) % a.hg_count;
+    const int row = cid / (a.nsplit * a.hg_count);
     if (tid == 0) {
-        mbar_init(bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&full[b], kClGatherThreads);
+            mbar_init(&sfull[b], 1);
+            mbar_init(&pfull[b], 4);
+            mbar_init(&pvdone[b], 1);
+        }
+        mbar_init(qfull, 1);
+        mbar_init(xfull, 1);
         fence_barrier_init();
     }
-    if (warp == 0) tmem_alloc(s_tmem, L::kTmemCols);
-    for (int h = tid; h < NH; h += kTcThreads) {
-        st_m[h] = -INFINITY;
-        st_l[h] = 0.f;
-    }
-    pdl_wait();  // on-chip set-up above; global memory only below
-    pdl_launch_dependents();
-    const int r = a.q_req ? a.q_req[row] : row;
-    const int m = a.q_pos[row];
-    const bool row_ok = r >= 0 && r < a.main_bt.batch && r < a.swa_bt.batch && m >= 0;
-    if (!row_ok && tid == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
-    const int n_vis = row_ok ? entries_formed((long long)m + 1, a.kind_w, a.kind_s) : 0;
-    const int n_comp = a.topk ? a.k : n_vis;
-    const int wlo = max(0, m - a.window + 1);
-    const int n_keys = row_ok ? n_comp + (m - wlo + 1) : 0;
-    const int key_lo = split * a.cps * kTcKeys;
-    const int key_hi = min(n_keys, key_lo + a.cps * kTcKeys);
-    // Q rows of this head group -> B operand layout
-    {
-        const uint16_t* qsrc = a.q + ((long long)row * a.heads + (long long)hg * NH) * kD;
-        for (int i = tid; i < NH * (kD / 8); i += kTcThreads) {
-            const int h = i / (kD / 8), e = (i % (kD / 8)) * 8;
-            cp_async16(sQ + sw128_offset(h, e, NH * 128), qsrc + (long long)h * kD + e, row_ok ? 16u : 0u);
+    if constexpr (NH < 64)  // the S product reads 64 query rows: rows NH.. are zero
+        for (int i = tid; i < 8 * (64 - NH) * 8; i += kClThreads) {
+            const int c = i / ((64 - NH) * 8), rr = NH + (i / 8) % (64 - NH), u = i % 8;
+            *reinterpret_cast<uint4*>(smem + L::kOffQ + c * 8192 + rr * 128 + u * 16) = make_uint4(0, 0, 0, 0);
         }
-        cp_async_commit();
-    }
+    fence_proxy_async_smem();
+    if (warp == 0) tmem_alloc(s_tmem, L::kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t tS = tmem, tO = tmem + NH;
-    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t idesc_s = idesc_bf16(NH, 0), idesc_o = idesc_bf16(NH, 1);
-    const int h0 = half * HH;  // this warp's heads in the softmax: [h0, h0 + HH)
-    auto fmax_op = [](float x, float y) { return fmaxf(x, y); };
-    auto add_op = [](float x, float y) { return x + y; };
+    const uint32_t tS = tmem, tO = tmem + 128;
+    cluster_arrive_relaxed();  // phase 0: this CTA has started (waited on before distributed shared memory use)
+    pdl_wait();                // on-chip set-up above; global memory only below
+    pdl_launch_dependents();
 
-    // key resolution (top-k index -> block table -> physical row) of the next tile runs one tile
-    // ahead, so its dependent global loads overlap the current tile's copies, MMAs and softmax
-    long long nxt_row = -1;
-    int nxt_flag = 0;
-    auto resolve_tile = [&](int kt) {
-        if (tid < kTcKeys) {
-            const int j = kt + tid;
-            long long p = -1;
-            bool sw = false;
-            if (j < key_hi) p = resolve_key(a, row, r, m, n_vis, n_comp, wlo, j, &sw);
-            nxt_row = p;
-            nxt_flag = p < 0 ? 0 : (sw ? 2 : 1);
-        }
-    };
-    resolve_tile(key_lo);
+    const int r = a.q_req ? a.q_req[row] : row;
+    const int m = a.q_pos[row];
+    const bool row_ok = r >= 0 && r < a.main_bt.batch && r < a.swa_bt.batch && m >= 0;
+    if (!row_ok && tid == 0 && crank == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
+    const int n_vis = row_ok ? entries_formed((long long)m + 1, a.kind_w, a.kind_s) : 0;
+    const int n_comp = a.topk ? a.k : n_vis;
+    const int ncp = (n_comp + 3) & ~3;
+    const int wlo = max(0, m - a.window + 1);
+    const int n_keys = row_ok ? ncp + (m - wlo + 1) : 0;
+    const int n_sub = (n_keys + kClKeys - 1) / kClKeys;
+    const int g_lo = split * a.cps, g_hi = min(n_sub, g_lo + a.cps);
+    const int n_mine = g_hi > g_lo + crank ? (g_hi - g_lo - crank + csize - 1) / csize : 0;
+    bool ok = true;
 
-    uint32_t phase = 0;
-    bool ok = true, first = true;
-    for (int kt = key_lo; kt < key_hi && ok; kt += kTcKeys) {
-        // publish the tile's resolved keys (thread j <-> key kt + j), then gather rows warp by warp
-        if (tid < kTcKeys) {
-            meta_row[tid] = nxt_row;
-            meta_flag[tid] = nxt_flag;
+    if (warp >= 5) {
+        // ---- gather warps: resolve keys a round ahead, prefetch rows into L2, copy with cp.async -----
+        const int gt = tid - 160, gw = warp - 5;
+        if (gt == 0) {
+            if (n_mine > 0) {
+                mbar_expect_tx(qfull, NH * kD * 2);
+                for (int c = 0; c < kD / 64; ++c)
+                    tma_load_2d(smem + L::kOffQ + c * 8192, &qmap, c * 64, row * a.heads + hg * NH, qfull);
+            }
+            mbar_arrive(qfull);
         }
-        __syncthreads();
-        for (int kk = warp; kk < kTcKeys; kk += kTcThreads / 32) {
-            const int flag = meta_flag[kk];
-            const uint8_t* base = flag == 2 ? static_cast<const uint8_t*>(a.swa.data)
-                                            : static_cast<const uint8_t*>(a.main.data);
-            const uint8_t* src = flag ? base + meta_row[kk] * (2 * kD) : base;
-            for (int piece = lane; piece < kD / 8; piece += 32)
-                cp_async16(sK + sw128_offset(kk, piece * 8, kTcKeys * 128), src + piece * 16, flag ? 16u : 0u);
+        // sub-tiles [R * kClRound, (R + 1) * kClRound): thread -> sub-tile R * kClRound + gt / 64, key gt % 64
+        auto resolve_round = [&](int R) {
+            const int i = R * kClRound + (gt >> 6);
+            if (gt >= kClRound * kClKeys || i >= n_mine) return;
+            const int j = (g_lo + crank + csize * i) * kClKeys + (gt & 63);
+            int v = -1, pool = 1;
+            if (j < n_keys) {
+                v = resolve_key4(a, row, r, n_vis, n_comp, ncp, wlo, j, &pool);
+                if (v >= 0) {
+                    const uint8_t* base = pool == 2 ? static_cast<const uint8_t*>(a.swa.data)
+                                                    : static_cast<const uint8_t*>(a.main.data);
+                    prefetch_l2(base + (long long)v * (2 * kD), 2 * kD);
+                }
+            }
+            s_row[(i % kClRing) * kClKeys + (gt & 63)] = v;
+            s_pool[(i % kClRing) * kClKeys + (gt & 63)] = (uint8_t)pool;
+        };
+        if (n_mine > 0) resolve_round(0);
+        for (int i = 0; i < n_mine; ++i) {
+            const int s = i & 1;
+            if (i >= 2) ok = ok && mbar_wait_bounded(&pvdone[s], ((i - 2) >> 1) & 1, kWaitLimitNs);
+            named_bar_sync(1, kClGatherThreads);  // sub-tile i's rows are visible; earlier gathers are done
+            const int* rows = s_row + (i % kClRing) * kClKeys;
+            const uint8_t* pools = s_pool + (i % kClRing) * kClKeys;
+            if (gt < kClKeys) {  // warps 5 and 6: the stage's key mask for the softmax
+                const uint32_t bits = __ballot_sync(0xffffffffu, rows[gt] >= 0);
+                if (lane == 0) s_mask[s * 2 + gw] = bits;
+            }
+            if (ok) {
+                const uint32_t stage = sK + s * kClStage;
+#pragma unroll 1
+                for (int kk = gw; kk < kClKeys; kk += kClGatherWarps) {
+                    const int rr = rows[kk];
+                    const uint8_t* base = pools[kk] == 2 ? static_cast<const uint8_t*>(a.swa.data)
+                                                         : static_cast<const uint8_t*>(a.main.data);
+                    const uint8_t* src = rr >= 0 ? base + (long long)rr * (2 * kD) : base;
+#pragma unroll
+                    for (int piece = lane; piece < kD / 8; piece += 32)
+                        cp_async16(stage + sw128_offset(kk, piece * 8, kClKeys * 128), src + piece * 16,
+                                   rr >= 0 ? 16u : 0u);
+                }
+            }
+            cp_async_commit();
+            // the next round of keys once this one's second sub-tile is under way: its rows reach L2 while
+            // the sub-tiles in between are processed (ring slots of sub-tiles < i are free by now)
+            if (i % kClRound == 2) resolve_round(i / kClRound + 1);
+            cp_async_wait_all();
+            fence_proxy_async_smem();  // cp.async writes -> visible to the tensor core (async proxy)
+            mbar_arrive(&full[s]);
         }
-        cp_async_commit();
-        if (kt + kTcKeys < key_hi) resolve_tile(kt + kTcKeys);
-        cp_async_wait_all();
-        fence_proxy_async_smem();  // cp.async writes -> visible to the tensor core (async proxy)
-        __syncthreads();
-
-        // S^T = K Q^T
-        if (tid == 0) {
+        if (!ok) report(a.status, DSA_ERR_TIMEOUT);
+    } else if (warp == 4) {
+        // ---- MMA issue: the whole warp waits, one elected lane issues ----------------------------
+        // S of sub-tile i + 1 goes first when its keys are in (it overlaps the softmax of sub-tile i), but
+        // the product of sub-tile i never waits behind a gather that has not arrived.
+        const uint32_t idesc_s = idesc_bf16(kClKeys, 0, 64), idesc_o = idesc_bf16(NH, 1, 128);
+        const uint64_t dq = sw128_desc(sQ, 16, 1024);
+        if (n_mine > 0) ok = mbar_wait_bounded(qfull, 0, kWaitLimitNs);
+        auto issue_s = [&](int i) {
+            const int s = i & 1;
             tc_fence_after();
-#pragma unroll 4
+            const uint64_t dk = sw128_desc(sK + s * kClStage, 16, 1024);
+#pragma unroll
             for (int ks = 0; ks < kD / 16; ++ks) {
-                const uint32_t koff = (ks >> 2) * (kTcKeys * 128) + (ks & 3) * 32;
-                const uint32_t qoff = (ks >> 2) * (NH * 128) + (ks & 3) * 32;
-                mma_bf16_ss(tS, sw128_desc(sK + koff, 16, 1024), sw128_desc(sQ + qoff, 16, 1024), idesc_s, ks > 0);
+                const uint64_t off = (uint64_t)((((ks >> 2) * (64 * 128)) + (ks & 3) * 32) >> 4);
+                mma_bf16_ss_elect(tS + s * kClKeys, dq + off, dk + off, idesc_s, ks > 0 ? 1u : 0u);
             }
-            mma_commit(bar);
-        }
-        ok = mbar_wait_bounded(bar, phase, kWaitLimitNs);
-        phase ^= 1;
-        ok = __syncthreads_and(ok);
-        if (!ok) {
-            if (tid == 0) report(a.status, DSA_ERR_TIMEOUT);
-            break;
-        }
-        tc_fence_after();
-
-        // softmax over this tile's keys, per head: thread = key (quadrant lane), HH heads of this half
-        const int key = quad * 32 + lane;
-        const bool valid = meta_flag[key] != 0;
-        float sv[HH], tmp[HH];
-#pragma unroll
-        for (int c0 = 0; c0 < HH; c0 += 16) {
-            float v[16];
-            tmem_ld16(tS + lane_off + h0 + c0, v);
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (c0 + i < HH) sv[c0 + i] = valid ? v[i] * a.scale_log2 : -INFINITY;
-        }
-#pragma unroll
-        for (int i = 0; i < HH; ++i) tmp[i] = sv[i];
-        {
-            const float w = transpose_reduce<HH>(tmp, fmax_op);  // head h0 + lane * HH / 32
-            if ((lane & (32 / HH - 1)) == 0) red_a[quad * NH + h0 + lane * HH / 32] = w;
-        }
-        __syncthreads();
-        for (int h = tid; h < NH; h += kTcThreads) {
-            const float mo = st_m[h];
-            const float mt = fmaxf(fmaxf(red_a[h], red_a[NH + h]), fmaxf(red_a[2 * NH + h], red_a[3 * NH + h]));
-            const float mn = fmaxf(mo, mt);
-            st_mnew[h] = mn;
-            st_alpha[h] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
-        }
-        __syncthreads();
-        // P^T (bf16) for the PV product, per-head partial sums
-#pragma unroll
-        for (int i = 0; i < HH; ++i) {
-            const int h = h0 + i;
-            const float mn = st_mnew[h];
-            const float p = mn == -INFINITY ? 0.f : exp2f(sv[i] - mn);
-            sv[i] = p;
-            *reinterpret_cast<uint16_t*>(smem + L::kOffP + sw128_offset(h, key, NH * 128)) = float_to_bf16(p);
-        }
-        {
-            const float w = transpose_reduce<HH>(sv, add_op);
-            if ((lane & (32 / HH - 1)) == 0) red_b[quad * NH + h0 + lane * HH / 32] = w;
-        }
-        __syncthreads();
-        bool grew = false;
-        for (int h = tid; h < NH; h += kTcThreads) {
-            const float sum = red_b[h] + red_b[NH + h] + red_b[2 * NH + h] + red_b[3 * NH + h];
-            st_l[h] = st_l[h] * st_alpha[h] + sum;
-            grew |= st_alpha[h] != 1.f;
-            st_m[h] = st_mnew[h];
-        }
-        grew = __syncthreads_or(grew);
-        // rescale the running O^T where a head's max grew (lane = dim, column = head); each half of
-        // the warps owns two of the four 128-dim tiles
-        if (!first && grew) {
-#pragma unroll 1
-            for (int mt = 2 * half; mt < 2 * half + 2; ++mt) {
-#pragma unroll
-                for (int c0 = 0; c0 < NH; c0 += 16) {
-                    float v[16];
-                    tmem_ld16(tO + mt * NH + lane_off + c0, v);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] *= st_alpha[c0 + i];
-                    tmem_st16(tO + mt * NH + lane_off + c0, v);
-                }
-            }
-            tmem_wait_st();
-        }
-        fence_proxy_async_smem();  // P^T stores -> async proxy
-        tc_fence_before();
-        __syncthreads();
-
-        // O^T += V^T P^T
-        if (tid == 0) {
+            mma_commit_elect(&sfull[s]);
+        };
+        auto issue_pv = [&](int i) {
+            const int s = i & 1;
             tc_fence_after();
-#pragma unroll 1
-            for (int mt = 0; mt < 4; ++mt) {
+            const uint64_t dv = sw128_desc(sK + s * kClStage, kClKeys * 128, 1024);
+            const uint64_t dp = sw128_desc(sP + s * L::kP, 16, 1024);
 #pragma unroll
-                for (int ks = 0; ks < kTcKeys / 16; ++ks) {
-                    const uint32_t voff = (2 * mt) * (kTcKeys * 128) + (2 * ks) * 1024;
-                    const uint32_t poff = (ks >> 2) * (NH * 128) + (ks & 3) * 32;
-                    mma_bf16_ss(tO + mt * NH, sw128_desc(sK + voff, kTcKeys * 128, 1024),
-                                sw128_desc(sP + poff, 16, 1024), idesc_o, (first && ks == 0) ? 0u : 1u);
+            for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+                for (int ks = 0; ks < kClKeys / 16; ++ks)
+                    mma_bf16_ss_elect(tO + mt * NH,
+                                      dv + (uint64_t)(((2 * mt) * (kClKeys * 128) + (2 * ks) * 1024) >> 4),
+                                      dp + (uint64_t)((ks * 32) >> 4), idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
+            mma_commit_elect(&pvdone[s]);
+        };
+        int next_s = 0;  // next sub-tile whose S is to be issued
+        ok = __all_sync(0xffffffffu, ok);
+        for (int i = 0; i < n_mine && ok; ++i) {
+            // S for every sub-tile <= i whose keys are in; then P V of sub-tile i, issuing the next S
+            // meanwhile if its keys arrive first
+            const uint64_t t0 = global_ns();
+            bool pv_done = false;
+            while (ok && !pv_done) {
+                if (next_s < n_mine && next_s <= i + 1 &&
+                    __all_sync(0xffffffffu, mbar_try_wait(&full[next_s & 1], (next_s >> 1) & 1))) {
+                    issue_s(next_s);
+                    ++next_s;
+                    continue;
+                }
+                if (next_s > i && __all_sync(0xffffffffu, mbar_try_wait(&pfull[i & 1], (i >> 1) & 1))) {
+                    issue_pv(i);
+                    pv_done = true;
+                    continue;
+                }
+                if (global_ns() - t0 > kWaitLimitNs) ok = false;
+                ok = __all_sync(0xffffffffu, ok);
+            }
+        }
+        if (!ok && lane == 0) report(a.status, DSA_ERR_TIMEOUT);
+    } else {
+        // ---- softmax warps: thread = head (lanes 0-15 of the quadrant) --------------------------
+        const int h = warp * 16 + lane;
+        const bool hthread = lane < 16 && h < NH;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        float m_run = -INFINITY, l_run = 0.f;
+        for (int i = 0; i < n_mine; ++i) {
+            const int s = i & 1;
+            ok = ok && mbar_wait_bounded(&full[s], (i >> 1) & 1, kWaitLimitNs);  // the stage's key mask
+            ok = ok && mbar_wait_bounded(&sfull[s], (i >> 1) & 1, kWaitLimitNs);
+            if (i >= 2) ok = ok && mbar_wait_bounded(&pvdone[s], ((i - 2) >> 1) & 1, kWaitLimitNs);  // P^T buffer free
+            ok = __all_sync(0xffffffffu, ok);
+            float sv[kClKeys];
+            float alpha = 1.f;
+            bool resc = false;
+            if (ok) {
+                tc_fence_after();
+                tmem_ld64(tS + s * kClKeys + lane_off, sv);
+                const uint64_t vm = ((uint64_t)s_mask[s * 2 + 1] << 32) | s_mask[s * 2];
+                float mx = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < kClKeys; ++j) {
+                    sv[j] = ((vm >> j) & 1) ? sv[j] * a.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, sv[j]);
+                }
+                if (mx > m_run + kLazyLog2) {  // also the first finite maximum (m_run = -inf)
+                    alpha = exp2f(m_run - mx);
+                    resc = i > 0;
+                    m_run = mx;
+                }
+                const float mr = m_run == -INFINITY ? 0.f : m_run;  // all keys so far masked: p = 0
+                const uint32_t prow = sP + s * L::kP + (h >> 3) * 1024 + (h & 7) * 128;
+                float sum = 0.f;
+#pragma unroll
+                for (int c = 0; c < kClKeys / 8; ++c) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint16_t b0 = float_to_bf16(exp2f(sv[8 * c + 2 * e] - mr));
+                        const uint16_t b1 = float_to_bf16(exp2f(sv[8 * c + 2 * e + 1] - mr));
+                        sum += bf16_to_float(b0) + bf16_to_float(b1);
+                        w[e] = (uint32_t)b0 | ((uint32_t)b1 << 16);
+                    }
+                    if (hthread)
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((c ^ (h & 7)) << 4)),
+                                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                                     : "memory");
+                }
+                l_run = l_run * alpha + sum;
+            }
+            if (hthread) s_alpha[s * NH + h] = alpha;
+            const bool any = __any_sync(0xffffffffu, resc && hthread);
+            if (lane == 0) s_vote[s * 4 + warp] = any ? 1 : 0;
+            named_bar_sync(2, 128);
+            if (s_vote[s * 4] | s_vote[s * 4 + 1] | s_vote[s * 4 + 2] | s_vote[s * 4 + 3]) {
+                // a head's maximum moved: O^T (after the previous sub-tile's product) times alpha per head
+                ok = ok && mbar_wait_bounded(&pvdone[(i - 1) & 1], ((i - 1) >> 1) & 1, kWaitLimitNs);
+                ok = __all_sync(0xffffffffu, ok);
+                if (ok) {
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+                        for (int c0 = 0; c0 < NH; c0 += 16) {
+                            float v[16];
+                            tmem_ld16(tO + mt * NH + lane_off + c0, v);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v[e] *= s_alpha[s * NH + c0 + e];
+                            tmem_st16(tO + mt * NH + lane_off + c0, v);
+                        }
+                    }
+                    tmem_wait_st();
                 }
             }
-            mma_commit(bar);
+            fence_proxy_async_smem();  // P^T stores -> async proxy
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pfull[s]);
         }
-        ok = mbar_wait_bounded(bar, phase, kWaitLimitNs);
-        phase ^= 1;
-        ok = __syncthreads_and(ok);
-        if (!ok && tid == 0) report(a.status, DSA_ERR_TIMEOUT);
-        tc_fence_after();
-        first = false;
+        if (n_mine > 0) {  // the last product must be complete before O^T is read
+            ok = ok && mbar_wait_bounded(&pvdone[(n_mine - 1) & 1], ((n_mine - 1) >> 1) & 1, kWaitLimitNs);
+            tc_fence_after();
+        }
+        if (hthread) {
+            s_own[h] = m_run;
+            s_own[NH + h] = l_run;
+        }
+        if (!ok) report(a.status, DSA_ERR_TIMEOUT);
     }
 
-    // ---- epilogue: thread = dim of a 128-dim tile of O^T; each half of the warps owns two tiles -----
+    // ---- merge across the cluster ---------------------------------------------------------------
+    // Every CTA sends (m, l) per head to every CTA of the cluster (distributed shared memory), so all of
+    // them know the cluster maximum M and denominator L; each scales its O^T by 2^(m - M) and pushes
+    // the tiles that other CTAs own straight into their shared memory (bulk copies); each owner adds its
+    // own tile from TMEM, applies 1 / L and R_m^-1 and stores bf16 (or an fp32 split partial).
+    tc_fence_before();
+    const bool all_ok = __syncthreads_and(ok);  // O^T complete (the softmax warps waited for it); s_own set
+    tc_fence_after();
+    const bool have = n_mine > 0 && all_ok;
+    constexpr int G = NH / 4;                    // heads per finishing thread (a TMEM load of G columns)
+    const int quad = warp & 3, quarter = warp >> 2;
+    const int d = quad * 32 + lane, h0 = quarter * G;  // thread: dim d of a 128-dim tile, heads h0 .. h0 + G
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const int tiles_per = 4 / csize;
+    auto tmem_cols = [&](int t, float (&v)[G]) {
+        if constexpr (G == 16) tmem_ld16(tO + t * NH + lane_off + h0, v);
+        else if constexpr (G == 8) tmem_ld8(tO + t * NH + lane_off + h0, v);
+        else tmem_ld4(tO + t * NH + lane_off + h0, v);
+    };
+    auto tmem_cols_nowait = [&](int t, float (&v)[G]) { tmem_ld_nowait<G>(tO + t * NH + lane_off + h0, v); };
+    cluster_wait();  // phase 0: every CTA of the cluster has started
+    if (csize > 1 && tid == 0)  // before any peer can push (pushes follow phase 1)
+        mbar_arrive_expect_tx(xfull, (uint32_t)((csize - 1) * tiles_per * L::kTile));
+    for (int h = tid; h < NH; h += kClThreads) {
+        const uint32_t dst = smem_u32(s_stat + (crank * NH + h) * 2);
+        const float mo = have ? s_own[h] : -INFINITY, lo = have ? s_own[NH + h] : 0.f;
+        for (int q = 0; q < csize; ++q) st_cluster_v2(mapa_shared(dst, (uint32_t)q), mo, lo);
+    }
+    cluster_arrive();  // phase 1: statistics delivered; every CTA's products are complete
+    cluster_wait();
+    for (int h = tid; h < NH; h += kClThreads) {
+        float M = -INFINITY;
+        for (int q = 0; q < csize; ++q) M = fmaxf(M, s_stat[(q * NH + h) * 2]);
+        float Ls = 0.f;
+        for (int q = 0; q < csize; ++q) {
+            const float mq = s_stat[(q * NH + h) * 2];
+            if (mq != -INFINITY) Ls += s_stat[(q * NH + h) * 2 + 1] * exp2f(mq - M);
+        }
+        const float mo = s_stat[(crank * NH + h) * 2];
+        s_fac[h] = mo == -INFINITY ? 0.f : exp2f(mo - M);
+        s_L[h] = Ls;
+        s_M[h] = M;
+        s_inv[h] = Ls > 0.f ? 1.f / Ls : 0.f;
+    }
     __syncthreads();
-    const bool have = !first && ok;
-    if (a.nsplit == 1) {
-        const int rd = a.rope.rope_dim, firstd = kD - rd;
+    float f[G], inv[G];
+#pragma unroll
+    for (int e = 0; e < G; e += 4) {
+        const float4 a4 = *reinterpret_cast<const float4*>(s_fac + h0 + e);
+        const float4 b4 = *reinterpret_cast<const float4*>(s_inv + h0 + e);
+        f[e] = a4.x, f[e + 1] = a4.y, f[e + 2] = a4.z, f[e + 3] = a4.w;
+        inv[e] = b4.x, inv[e + 1] = b4.y, inv[e + 2] = b4.z, inv[e + 3] = b4.w;
+    }
+    // tiles this CTA sends sit at [0, 3 tiles) of shared memory, the tiles it receives at [3, 6 tiles)
+    // (query rows and key stages, idle now); each as [NH / 4 head quads][128 dims] float4
+    uint8_t* xout = smem + L::kOffQ;
+    uint8_t* xin = smem + L::kOffQ + 3 * L::kTile;
+    if (csize > 1) {
+        float v[4][G];  // all four tiles' columns in flight together, then the three (or two) sent ones staged
+        if (have) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) tmem_cols_nowait(t, v[t]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int t = 0; t < 4; ++t) tmem_regs_after_wait<G>(v[t]);
+        }
+        int sl = 0;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            if (t % csize == crank) continue;
+#pragma unroll
+            for (int q4 = 0; q4 < G / 4; ++q4)
+                *reinterpret_cast<float4*>(xout + sl * L::kTile + ((h0 / 4 + q4) * 128 + d) * 16) =
+                    have ? make_float4(v[t][4 * q4] * f[4 * q4], v[t][4 * q4 + 1] * f[4 * q4 + 1],
+                                       v[t][4 * q4 + 2] * f[4 * q4 + 2], v[t][4 * q4 + 3] * f[4 * q4 + 3])
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+            ++sl;
+        }
+        fence_proxy_async_smem();  // staged tiles -> async proxy (the bulk copies)
+        __syncthreads();
+        if (tid == 0) {
+            int sl2 = 0;
+            for (int t = 0; t < 4; ++t) {
+                const int o = t % csize;
+                if (o == crank) continue;
+                const int slot = (crank - (crank > o ? 1 : 0)) * tiles_per + t / csize;  // in the owner's xin
+                bulk_s2cluster(mapa_shared(smem_u32(xin + slot * L::kTile), (uint32_t)o),
+                               smem_u32(xout + sl2 * L::kTile), L::kTile, mapa_shared(smem_u32(xfull), (uint32_t)o));
+                ++sl2;
+            }
+        }
+        ok = mbar_wait_bounded(xfull, 0, kWaitLimitNs);
+        if (!ok && tid == 0) report(a.status, DSA_ERR_TIMEOUT);
+        cluster_arrive_relaxed();  // phase 2: this CTA's incoming tiles are complete (waited on before exit)
+    }
+    // ---- owner: finish each owned tile; bf16 output staged as [NH][128] in the P^T buffers and stored
+    // with 16-byte writes, or fp32 split partials ------------------------------------------------------
+    uint8_t* ostage = smem + L::kOffP;
+    const int rd = a.rope.rope_dim, firstd = kD - rd;
 #pragma unroll 1
-        for (int mt = 2 * half; mt < 2 * half + 2; ++mt) {
-            const int d = mt * 128 + quad * 32 + lane;
-            float cs = 1.f, sn = 0.f;
-            if (d >= firstd) rope_cos_sin(m, a.rope.inv_freq[(d - firstd) >> 1], &cs, &sn);
+    for (int j = 0; j < tiles_per; ++j) {
+        const int t = crank + csize * j;
+        const int D = t * 128 + d;
+        float cs = 1.f, sn = 0.f;
+        if (a.nsplit == 1 && D >= firstd) rope_cos_sin(m, a.rope.inv_freq[(D - firstd) >> 1], &cs, &sn);
+        float v[G];
+        if (have) tmem_cols(t, v);
 #pragma unroll
-            for (int c0 = 0; c0 < NH; c0 += 16) {
-                float v[16];
-                if (have) tmem_ld16(tO + mt * NH + lane_off + c0, v);
-                else
-                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        for (int e = 0; e < G; ++e) v[e] = have ? v[e] * f[e] : 0.f;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int h = c0 + i;
-                    const float l = st_l[h];
-                    const float x = l > 0.f ? v[i] / l : 0.f;
-                    const float y = __shfl_xor_sync(0xffffffffu, x, 1);  // the pair partner's value
-                    float o = x;
-                    if (d >= firstd) o = (d & 1) ? (-y * sn + x * cs) : (x * cs + y * sn);  // R_m^-1
-                    const float o_hi = __shfl_xor_sync(0xffffffffu, o, 1);
-                    if ((d & 1) == 0)  // even lane stores the (d, d + 1) pair
-                        *reinterpret_cast<uint32_t*>(a.out + ((long long)row * a.heads + hg * NH + h) * kD + d) =
-                            (uint32_t)float_to_bf16(o) | ((uint32_t)float_to_bf16(o_hi) << 16);
+        for (int si = 0; si < 3; ++si) {
+            if (si < csize - 1) {
+                const uint8_t* src = xin + (si * tiles_per + j) * L::kTile;
+#pragma unroll
+                for (int q4 = 0; q4 < G / 4; ++q4) {
+                    const float4 w = *reinterpret_cast<const float4*>(src + ((h0 / 4 + q4) * 128 + d) * 16);
+                    v[4 * q4] += w.x;
+                    v[4 * q4 + 1] += w.y;
+                    v[4 * q4 + 2] += w.z;
+                    v[4 * q4 + 3] += w.w;
                 }
             }
         }
-        if (a.lse)
-            for (int h = tid; h < NH; h += kTcThreads) {
-                const float l = st_l[h];
-                a.lse[(long long)row * a.heads + hg * NH + h] = l > 0.f ? (st_m[h] + log2f(l)) / kLog2e : -INFINITY;
-            }
-    } else {
-        const long long base0 = ((long long)row * a.nsplit + split) * a.heads + hg * NH;
-#pragma unroll 1
-        for (int mt = 2 * half; mt < 2 * half + 2; ++mt) {
-            const int d = mt * 128 + quad * 32 + lane;
+        if (a.nsplit == 1) {
 #pragma unroll
-            for (int c0 = 0; c0 < NH; c0 += 16) {
-                float v[16];
-                if (have) tmem_ld16(tO + mt * NH + lane_off + c0, v);
-                else
-                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) a.ws_o[(base0 + c0 + i) * kD + d] = v[i];
+            for (int e = 0; e < G; ++e) {
+                const float x = v[e] * inv[e];
+                const float y = __shfl_xor_sync(0xffffffffu, x, 1);  // the pair partner's value
+                float o = x;
+                if (D >= firstd) o = (D & 1) ? (-y * sn + x * cs) : (x * cs + y * sn);  // R_m^-1
+                reinterpret_cast<uint16_t*>(ostage)[(h0 + e) * 128 + d] = float_to_bf16(o);
             }
-        }
-        for (int h = tid; h < NH; h += kTcThreads) {
-            a.ws_ml[(base0 + h) * 2 + 0] = st_m[h];
-            a.ws_ml[(base0 + h) * 2 + 1] = st_l[h];
+            __syncthreads();
+            // NH rows of 256 bytes -> out[row][hg * NH + h][t * 128 .. + 128]
+            for (int i = tid; i < NH * 16; i += kClThreads) {
+                const int h = i >> 4, u = i & 15;
+                *reinterpret_cast<uint4*>(a.out + ((long long)row * a.heads + hg * NH + h) * kD + t * 128 + u * 8) =
+                    *reinterpret_cast<const uint4*>(ostage + h * 256 + u * 16);
+            }
+            __syncthreads();
+        } else {
+            const long long base0 = ((long long)row * a.nsplit + split) * a.heads + hg * NH + h0;
+#pragma unroll
+            for (int e = 0; e < G; ++e) a.ws_o[(base0 + e) * kD + D] = v[e];
         }
     }
+    if (crank == 0) {
+        for (int h = tid; h < NH; h += kClThreads) {
+            const float Ls = s_L[h], M = s_M[h];
+            if (a.nsplit == 1) {
+                if (a.lse) a.lse[(long long)row * a.heads + hg * NH + h] = Ls > 0.f ? (M + log2f(Ls)) / kLog2e : -INFINITY;
+            } else {
+                const long long b = ((long long)row * a.nsplit + split) * a.heads + hg * NH + h;
+                a.ws_ml[b * 2 + 0] = Ls > 0.f ? M : -INFINITY;
+                a.ws_ml[b * 2 + 1] = Ls;
+            }
+        }
+    }
+    if (csize > 1) cluster_wait();  // phase 2: no copy out of this CTA's shared memory is still running
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, L::kTmemCols);
 }
 
-// Split plan shared by the workspace query and the launch.
+// Split plans, shared by the workspace query and the launch.
+//   e4m3 rows (mma.sync kernel): one CTA per (row, head group, split) over 64-key chunks;
+//   bf16 rows (tcgen05 kernel): one cluster of `cl` CTAs per (row, head group, split) over 64-key
+//   sub-tiles: clusters of 4 while four CTAs per row still fit on the GPU at once, then 2, then 1;
+//   a row splits further only when its clusters leave SMs idle, and never below two sub-tiles per CTA.
 struct SplitPlan {
-    int hg, hg_count, nsplit, cps;
+    int hg, hg_count, nsplit, cps, cl;
 };
 
 static SplitPlan plan_splits(int rows, int heads, int max_keys, int chunk) {
     SplitPlan p;
     p.hg = heads >= 64 ? 64 : heads;
     p.hg_count = heads / p.hg;
+    p.cl = 1;
     const int n_chunks = max(1, (max_keys + chunk - 1) / chunk);
     const long long units = (long long)rows * p.hg_count;
     const int sms = sm_count();
@@ -835,28 +1032,64 @@ static SplitPlan plan_splits(int rows, int heads, int max_keys, int chunk) {
     return p;
 }
 
+static SplitPlan plan_cluster(int rows, int heads, int max_keys) {
+    SplitPlan p;
+    p.hg = heads >= 64 ? 64 : heads;
+    p.hg_count = heads / p.hg;
+    const int n_sub = max(1, (max_keys + kClKeys - 1) / kClKeys);
+    const long long units = (long long)rows * p.hg_count;
+    const long long sms = sm_count();
+    int cl = units * 4 <= sms ? 4 : (units * 2 <= sms ? 2 : 1);
+    while (cl > 1 && cl > n_sub) cl >>= 1;
+    long long ns = units * cl >= sms ? 1 : sms / (units * cl);
+    ns = std::max(1ll, std::min(ns, (long long)((n_sub + 2 * cl - 1) / (2 * cl))));
+    p.cl = cl;
+    p.cps = (int)((n_sub + ns - 1) / ns);
+    p.nsplit = (n_sub + p.cps - 1) / p.cps;
+    return p;
+}
+
+static SplitPlan plan_for(int rows, int heads, int max_keys, int dtype) {
+    return dtype == DSA_BF16 ? plan_cluster(rows, heads, max_keys) : plan_splits(rows, heads, max_keys, kChunk);
+}
+
+// Workspace: split partials [rows][nsplit][heads][512] + (m, l) [rows][nsplit][heads][2] when a row's keys
+// are split over several clusters (the CTAs of one cluster merge on chip).
 static size_t workspace_bytes_for(int rows, const SplitPlan& p, int heads) {
     if (p.nsplit <= 1) return 0;
     return (size_t)rows * p.nsplit * heads * (kD + 2) * sizeof(float);
 }
 
-// Keys per split unit: 128-key tiles on the tensor-core path (bf16 rows), 64-key chunks for e4m3 rows.
-static int chunk_for(int dtype) { return dtype == DSA_BF16 ? kTcKeys : kChunk; }
-
 // Workspace that covers either row format (the size query does not know the pool's format).
 static size_t workspace_bytes_any(int rows, int heads, int max_keys) {
-    return std::max(workspace_bytes_for(rows, plan_splits(rows, heads, max_keys, kTcKeys), heads),
-                    workspace_bytes_for(rows, plan_splits(rows, heads, max_keys, kChunk), heads));
+    return std::max(workspace_bytes_for(rows, plan_for(rows, heads, max_keys, DSA_BF16), heads),
+                    workspace_bytes_for(rows, plan_for(rows, heads, max_keys, DSA_FP8_E4M3), heads));
+}
+
+// Tensor map of a [rows][512] bf16 matrix with boxes of 64 columns x box_rows rows, 128B-swizzled.
+static bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t rows, int box_rows) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    cuuint64_t gdim[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)kD * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    cuuint32_t estride[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, estride,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int NH>
-static dsa_status_t launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
-    using L = TcSmem<NH>;
-    if (cudaFuncSetAttribute(attn_tc_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
+static dsa_status_t launch_attn_cl(const AttnArgs& a, int cl, cudaStream_t st) {
+    using L = ClSmem<NH>;
+    CUtensorMap qmap;
+    if (!make_bf16_map(&qmap, a.q, (uint64_t)a.rows * a.heads, NH)) return DSA_ERR_CUDA;
+    if (cudaFuncSetAttribute(attn_cl_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
         cudaSuccess)
         return DSA_ERR_CUDA;
-    const long long grid = (long long)a.rows * a.hg_count * a.nsplit;
-    cudaError_t e = launch_pdl(attn_tc_kernel<NH>, dim3((unsigned)grid), dim3(kTcThreads), L::kAlloc, st, a);
+    const long long grid = (long long)a.rows * a.hg_count * a.nsplit * cl;
+    cudaError_t e = launch_pdl_cluster(attn_cl_kernel<NH>, dim3((unsigned)grid), dim3(kClThreads), L::kAlloc, st, cl,
+                                       qmap, a);
     if (e == cudaSuccess && a.nsplit > 1)
         e = launch_pdl(attn_combine_kernel, dim3(a.rows * a.heads), dim3(128), 0, st, a);
     if (e != cudaSuccess) return DSA_ERR_CUDA;
@@ -893,13 +1126,16 @@ static dsa_status_t sparse_attn(int32_t rows, int32_t heads, const void* q, cons
         return DSA_ERR_INVALID_ARG;
     if (main->dim != kD || swa->dim != kD) return DSA_ERR_UNSUPPORTED;
     if (main->dtype != swa->dtype) return DSA_ERR_UNSUPPORTED;
+    if ((long long)main->num_blocks * main->rows_per_block > 0x7fffffffll ||
+        (long long)swa->num_blocks * swa->rows_per_block > 0x7fffffffll)
+        return DSA_ERR_UNSUPPORTED;  // rows are addressed with 32-bit indices
     if (main->rows_per_block != kBlockPositions / stride_of(kind) || swa->rows_per_block != kBlockPositions)
         return DSA_ERR_INVALID_ARG;
     if (rope->rope_dim < 0 || rope->rope_dim > 64 || (rope->rope_dim & 1) || !(rope->theta > 0.0))
         return DSA_ERR_INVALID_ARG;
     const int max_comp = topk ? k : main_bt->max_blocks * main->rows_per_block;
     const int max_keys = max_comp + window;
-    const SplitPlan p = plan_splits(rows, heads, max_keys, chunk_for(main->dtype));
+    const SplitPlan p = plan_for(rows, heads, max_keys, main->dtype);
     const size_t need = workspace_bytes_for(rows, p, heads);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256))) return DSA_ERR_INVALID_ARG;
 
@@ -925,18 +1161,19 @@ static dsa_status_t sparse_attn(int32_t rows, int32_t heads, const void* q, cons
     a.rope = make_rope_table(rope->rope_dim, rope->theta);
     a.out = static_cast<uint16_t*>(out);
     a.lse = lse;
-    if (need > 0) {
+    if (p.nsplit > 1) {
         a.ws_o = static_cast<float*>(workspace);
         a.ws_ml = a.ws_o + (size_t)rows * p.nsplit * heads * kD;
     }
+
     a.status = dev_status;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool fp8 = main->dtype == DSA_FP8_E4M3;
     if (!fp8) {
         switch (p.hg) {
-            case 16: return launch_attn_tc<16>(a, st);
-            case 32: return launch_attn_tc<32>(a, st);
-            default: return launch_attn_tc<64>(a, st);
+            case 16: return launch_attn_cl<16>(a, p.cl, st);
+            case 32: return launch_attn_cl<32>(a, p.cl, st);
+            default: return launch_attn_cl<64>(a, p.cl, st);
         }
     }
     switch (p.hg) {
@@ -954,6 +1191,18 @@ extern "C" size_t dsa_attn_workspace_size(int32_t nq, int32_t heads, int32_t max
     if (nq <= 0 || heads <= 0 || max_keys <= 0) return 0;
     if (heads != 16 && heads != 32 && heads != 64 && heads != 128) return 0;
     return workspace_bytes_any(nq, heads, max_keys);
+}
+
+extern "C" dsa_status_t dsa_attn_plan(int32_t nq, int32_t heads, int32_t max_keys, int32_t dtype, int32_t* plan) {
+    if (!plan || nq <= 0 || max_keys <= 0) return DSA_ERR_INVALID_ARG;
+    if (dtype != DSA_BF16 && dtype != DSA_FP8_E4M3) return DSA_ERR_INVALID_ARG;
+    if (heads != 16 && heads != 32 && heads != 64 && heads != 128) return DSA_ERR_UNSUPPORTED;
+    const SplitPlan p = plan_for(nq, heads, max_keys, dtype);
+    plan[0] = p.hg;
+    plan[1] = p.cl;
+    plan[2] = p.nsplit;
+    plan[3] = p.nsplit > 1 ? 2 : 1;
+    return DSA_OK;
 }
 
 extern "C" dsa_status_t dsa_sparse_attn_decode(int32_t batch, int32_t heads, const void* q, const int32_t* q_pos,

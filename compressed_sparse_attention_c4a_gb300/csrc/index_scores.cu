@@ -380,17 +380,8 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
     if (warp == 0) tmem_dealloc(tmem, a.tmem_cols);
 }
 
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-        return nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-}
-
 static bool make_map(CUtensorMap* map, const void* base, uint64_t rows, int dim, int box_rows) {
-    auto fn = encode_fn();
+    auto fn = tensor_map_encoder();
     if (!fn) return false;
     cuuint64_t gdim[2] = {(cuuint64_t)dim, (cuuint64_t)rows};
     cuuint64_t gstride[1] = {(cuuint64_t)dim};

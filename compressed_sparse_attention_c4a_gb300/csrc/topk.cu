@@ -3,9 +3,10 @@
 // [P1] "DeepSeek DSA、DeepSeek V4与vLLM Hybrid KV Cache详解" §4.2: S_t = TopK(I_{t,:}, k); the
 // main attention reads only S_t.  [P2] "DeepSeek V4 稀疏注意力完全解剖" 机制三: k = 512 for c4a.
 //
-// One thread-block cluster of 4 CTAs (1024 threads each) per query row; CTA q holds the q-th quarter
-// of the row in shared memory.  Partial results are combined through distributed shared memory
-// (each CTA reads the other three CTAs' copies), so every CTA takes the same decisions:
+// One thread-block cluster of C CTAs (1024 threads each) per query row, C = 1 when the row fits one CTA's
+// shared memory (up to 40,960 scores) and 4 for longer rows; CTA q holds the q-th of C parts of the row
+// in shared memory.  Partial results are combined through distributed shared memory (each CTA reads
+// the other CTAs' copies), so every CTA takes the same decisions:
 //   1. max M and min m of the finite scores;
 //   2. bucket select: bin(v) = 2047 - floor((M - v) * 2046 / (M - m)) for finite v, bin(-inf) = 0 --
 //      monotone (larger score -> same or larger bin; equal scores share a bin) and even, so the
@@ -29,9 +30,9 @@ namespace cg = cooperative_groups;
 namespace dsa {
 
 constexpr int kTopkThreads = 1024;
-constexpr int kTopkCluster = 4;
+constexpr int kTopkClusterMax = 4;
 constexpr int kBins = 2048;
-constexpr int kQuarterMax = 40960;  // scores per CTA kept in shared memory (rows up to 163,840)
+constexpr int kQuarterMax = 40960;  // scores per CTA kept in shared memory (rows up to 163,840 with C = 4)
 constexpr int kRankMax = 256;       // bucket sizes (cluster-wide) resolved by direct ranking
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -102,21 +103,27 @@ __device__ __forceinline__ uint32_t select_bin(const uint32_t* hist, uint32_t& n
 }
 
 // hsum[b] = sum over the cluster's CTAs of their local hist[b]; ends with a block barrier.
-__device__ __forceinline__ void cluster_hist_sum(cg::cluster_group& cluster, uint32_t* hist, uint32_t* hsum) {
+__device__ __forceinline__ void cluster_hist_sum(cg::cluster_group& cluster, int csz, uint32_t* hist,
+                                                 uint32_t* hsum) {
     cluster.sync();  // every CTA's local histogram is complete
-    uint32_t* remote[kTopkCluster];
+    if (csz == 1) {
+        for (int b = threadIdx.x; b < kBins; b += kTopkThreads) hsum[b] = hist[b];
+    } else {
+        uint32_t* remote[kTopkClusterMax];
 #pragma unroll
-    for (int c = 0; c < kTopkCluster; ++c) remote[c] = cluster.map_shared_rank(hist, c);
-    for (int b = threadIdx.x; b < kBins; b += kTopkThreads) {
-        uint32_t v = 0;
+        for (int c = 0; c < kTopkClusterMax; ++c) remote[c] = cluster.map_shared_rank(hist, c < csz ? c : 0);
+        for (int b = threadIdx.x; b < kBins; b += kTopkThreads) {
+            uint32_t v = 0;
 #pragma unroll
-        for (int c = 0; c < kTopkCluster; ++c) v += remote[c][b];
-        hsum[b] = v;
+            for (int c = 0; c < kTopkClusterMax; ++c)
+                if (c < csz) v += remote[c][b];
+            hsum[b] = v;
+        }
     }
     __syncthreads();
 }
 
-__global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads, 1)
+__global__ void __launch_bounds__(kTopkThreads, 1)
     topk_kernel(const float* __restrict__ scores, int ld, const int32_t* __restrict__ n_valid, int k,
                 int32_t* __restrict__ idx_out, int32_t* status) {
     pdl_wait();
@@ -135,7 +142,8 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
     __shared__ float red[2];
     __shared__ uint32_t totals[2];
 
-    const int row = blockIdx.x / kTopkCluster;
+    const int csz = (int)cluster.num_blocks();
+    const int row = blockIdx.x / csz;
     const int qr = (int)cluster.block_rank();
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     int32_t* out = idx_out + (long long)row * k;
@@ -153,7 +161,7 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
         return;
     }
     const float* s = scores + (long long)row * ld;
-    const int chunk = ((n + kTopkCluster - 1) / kTopkCluster + 3) & ~3;  // multiple of 4: aligned float4 loads
+    const int chunk = ((n + csz - 1) / csz + 3) & ~3;  // multiple of 4: aligned float4 loads
     const int base = qr * chunk;
     const int mq = max(0, min(n, base + chunk) - base);  // scores in this CTA's quarter
 
@@ -203,8 +211,7 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
     cluster.sync();
     mx = -INFINITY;
     mn = INFINITY;
-#pragma unroll
-    for (int c = 0; c < kTopkCluster; ++c) {
+    for (int c = 0; c < csz; ++c) {
         const float* rr = cluster.map_shared_rank(red, c);
         mx = fmaxf(mx, rr[0]);
         mn = fminf(mn, rr[1]);
@@ -219,7 +226,7 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
 
     // 2. value buckets: local histogram, cluster-wide sum, the bucket of the k-th largest score
     for (int i = tid; i < mq; i += kTopkThreads) atomicAdd(&hist[bin_of(rowv[i])], 1u);
-    cluster_hist_sum(cluster, hist, hsum);
+    cluster_hist_sum(cluster, csz, hist, hsum);
     uint32_t need = (uint32_t)k;
     const uint32_t bstar = select_bin(hsum, need, warp_tot, sel);
     const uint32_t in_bucket = hsum[bstar];
@@ -250,7 +257,7 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
             const uint32_t my_k = cand_key[tid], my_i = cand_idx[tid];
             uint32_t better = 0;
 #pragma unroll 1
-            for (int c = 0; c < kTopkCluster; ++c) {
+            for (int c = 0; c < csz; ++c) {
                 const uint32_t* rk = cluster.map_shared_rank(cand_key, c);
                 const uint32_t* ri = cluster.map_shared_rank(cand_idx, c);
                 const int nc = (int)*cluster.map_shared_rank(&n_cand, c);
@@ -282,7 +289,7 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
                 const uint32_t key = order_key(v);
                 if (bin_of(v) == bstar && (key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
             }
-            cluster_hist_sum(cluster, hist, hsum);
+            cluster_hist_sum(cluster, csz, hist, hsum);
             const uint32_t d = select_bin(hsum, need_T, warp_tot, sel);
             prefix |= d << sh;
             mask |= dm << sh;
@@ -319,8 +326,7 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
     }
     cluster.sync();
     uint32_t base_d = 0, base_t = 0, all_d = 0, all_t = 0;
-#pragma unroll
-    for (int c = 0; c < kTopkCluster; ++c) {
+    for (int c = 0; c < csz; ++c) {
         const uint32_t* tt = cluster.map_shared_rank(totals, c);
         const uint32_t a = tt[0], b = tt[1];
         if (c < qr) {
@@ -342,11 +348,279 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
         }
     }
     const uint32_t total = all_d + min(all_t, need_T);
-    if (qr == kTopkCluster - 1) {
+    if (qr == csz - 1) {
         for (int i = (int)total + tid; i < k; i += kTopkThreads) out[i] = -1;
         if (tid == 0 && total != (uint32_t)k) report(status, DSA_ERR_DEVICE_FAULT);
     }
     cluster.sync();  // no CTA leaves while another may still read its shared memory
+}
+
+// ---------------------------------------------------------------------------------------------
+// Rows of up to 16,384 scores: one CTA per row, the row in registers.  Thread t holds the VPT
+// consecutive scores [t VPT, t VPT + VPT), so the ordered compaction is one block scan of per-thread
+// counts.  Same decisions as above (max / min, value buckets, direct ranking of a small bucket or a
+// radix select inside a crowded one), without distributed shared memory or a staged copy of the row.
+// ---------------------------------------------------------------------------------------------
+template <int THREADS>
+struct RegScan {
+    static constexpr int kWarps = THREADS / 32;
+    // Exclusive block scan of two counters; also the totals.  Ends with a barrier.
+    static __device__ __forceinline__ void scan2(uint32_t a, uint32_t b, uint32_t* ex_a, uint32_t* ex_b,
+                                                 uint32_t* tot_a, uint32_t* tot_b, uint32_t (*wt)[2]) {
+        const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+        uint32_t ia = a, ib = b;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t ta = __shfl_up_sync(0xffffffffu, ia, o), tb = __shfl_up_sync(0xffffffffu, ib, o);
+            if (lane >= o) {
+                ia += ta;
+                ib += tb;
+            }
+        }
+        if (lane == 31) {
+            wt[wid][0] = ia;
+            wt[wid][1] = ib;
+        }
+        __syncthreads();
+        if (wid == 0) {
+            uint32_t wa = lane < kWarps ? wt[lane][0] : 0u, wb = lane < kWarps ? wt[lane][1] : 0u;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t ta = __shfl_up_sync(0xffffffffu, wa, o), tb = __shfl_up_sync(0xffffffffu, wb, o);
+                if (lane >= o) {
+                    wa += ta;
+                    wb += tb;
+                }
+            }
+            if (lane < kWarps) {
+                wt[lane][0] = wa;
+                wt[lane][1] = wb;
+            }
+        }
+        __syncthreads();
+        *ex_a = (wid ? wt[wid - 1][0] : 0u) + ia - a;
+        *ex_b = (wid ? wt[wid - 1][1] : 0u) + ib - b;
+        *tot_a = wt[kWarps - 1][0];
+        *tot_b = wt[kWarps - 1][1];
+        __syncthreads();
+    }
+    // The bin (from the top) holding the need-th largest counted element; need drops by the count above.
+    static __device__ __forceinline__ uint32_t select(const uint32_t* hist, uint32_t& need, uint32_t (*wt)[2],
+                                                      uint32_t* sel) {
+        constexpr int BPT = kBins / THREADS;  // bins per thread, in descending order
+        const int tid = threadIdx.x;
+        uint32_t c[BPT], sum = 0;
+#pragma unroll
+        for (int e = 0; e < BPT; ++e) {
+            c[e] = hist[kBins - 1 - BPT * tid - e];
+            sum += c[e];
+        }
+        uint32_t ex, ex2, tot, tot2;
+        scan2(sum, 0u, &ex, &ex2, &tot, &tot2, wt);
+#pragma unroll
+        for (int e = 0; e < BPT; ++e) {
+            if (ex < need && need <= ex + c[e]) {
+                sel[0] = (uint32_t)(kBins - 1 - BPT * tid - e);
+                sel[1] = ex;
+            }
+            ex += c[e];
+        }
+        __syncthreads();
+        const uint32_t b = sel[0];
+        need -= sel[1];
+        __syncthreads();
+        return b;
+    }
+};
+
+template <int THREADS, int VPT>
+__global__ void __launch_bounds__(THREADS, 1)
+    topk_reg_kernel(const float* __restrict__ scores, int ld, const int32_t* __restrict__ n_valid, int k,
+                    int32_t* __restrict__ idx_out, int32_t* status) {
+    static_assert(VPT % 4 == 0 && VPT <= 32, "a thread's run is a multiple of 4 and fits one 32-bit mask");
+    using SC = RegScan<THREADS>;
+    __shared__ uint32_t hist[kBins];
+    __shared__ uint32_t cand_key[kRankMax], cand_idx[kRankMax];
+    __shared__ uint32_t marks[THREADS * VPT / 32];  // ranked winners of a small bucket, by row index
+    __shared__ uint32_t wt[32][2];
+    __shared__ uint32_t sel[2];
+    __shared__ uint32_t n_cand;
+    __shared__ float red[2][32];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    int32_t* out = idx_out + (long long)row * k;
+    const int n = n_valid[row];
+    if (n < 0 || n > ld) {
+        if (tid == 0) report(status, DSA_ERR_DEVICE_FAULT);
+        for (int i = tid; i < k; i += THREADS) out[i] = -1;
+        return;
+    }
+    if (n <= k) {
+        for (int i = tid; i < k; i += THREADS) out[i] = i < n ? i : -1;
+        return;
+    }
+    // 1. this thread's run of scores; max / min of the finite ones over the row
+    const float* s = scores + (long long)row * ld;
+    const int i0 = tid * VPT;
+    const int nv = max(0, min(VPT, n - i0));  // valid scores in the run
+    float v[VPT];
+#pragma unroll
+    for (int u = 0; u < VPT; u += 4) {
+        if (u + 4 <= nv) {
+            const float4 q = *reinterpret_cast<const float4*>(s + i0 + u);
+            v[u] = q.x, v[u + 1] = q.y, v[u + 2] = q.z, v[u + 3] = q.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[u + e] = u + e < nv ? s[i0 + u + e] : -INFINITY;
+        }
+    }
+    for (int b = tid; b < kBins; b += THREADS) hist[b] = 0;
+    for (int w = tid; w < THREADS * VPT / 32; w += THREADS) marks[w] = 0;
+    if (tid == 0) n_cand = 0;
+    float mx = -INFINITY, mn = INFINITY;
+#pragma unroll
+    for (int u = 0; u < VPT; ++u)
+        if (v[u] != -INFINITY) {
+            mx = fmaxf(mx, v[u]);
+            mn = fminf(mn, v[u]);
+        }
+    mx = warp_max(mx);
+    mn = -warp_max(-mn);
+    if (lane == 0) {
+        red[0][wid] = mx;
+        red[1][wid] = mn;
+    }
+    __syncthreads();
+    mx = -INFINITY;
+    mn = INFINITY;
+#pragma unroll
+    for (int w = 0; w < SC::kWarps; ++w) {
+        mx = fmaxf(mx, red[0][w]);
+        mn = fminf(mn, red[1][w]);
+    }
+    float scale = (mx != -INFINITY && mx > mn) ? 2046.f / (mx - mn) : 0.f;
+    if (!isfinite(scale)) scale = 0.f;  // degenerate range: one bucket, resolved by the radix passes
+    // 2. value buckets, computed once per score and kept packed (two 16-bit bins per register):
+    // bin(v) = 2047 - round((mx - v) * scale) for finite v (the rounding by adding 2^23 keeps it monotone:
+    // a larger score never lands in a lower bin, equal scores share one), bin(-inf) = 0
+    uint32_t bins[VPT / 2];
+#pragma unroll
+    for (int u = 0; u < VPT; u += 2) {
+        uint32_t b2[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float t = fminf(2046.f, (mx - v[u + e]) * scale);
+            b2[e] = v[u + e] == -INFINITY ? 0u : 2047u - (__float_as_uint(t + 8388608.f) - 0x4B000000u);
+        }
+        bins[u / 2] = b2[0] | (b2[1] << 16);
+    }
+    auto bin_at = [&](int u) -> uint32_t { return (bins[u / 2] >> (16 * (u & 1))) & 0xFFFFu; };
+#pragma unroll
+    for (int u = 0; u < VPT; ++u)
+        if (u < nv) atomicAdd(&hist[bin_at(u)], 1u);
+    __syncthreads();
+    uint32_t need = (uint32_t)k;
+    const uint32_t bstar = SC::select(hist, need, wt, sel);
+    const uint32_t in_bucket = hist[bstar];
+    const bool take_all = in_bucket == need;
+    const bool rank_mode = !take_all && in_bucket <= (uint32_t)kRankMax;
+    // this thread's scores above b* (always taken) and in b*
+    uint32_t above = 0u, inb = 0u;
+#pragma unroll
+    for (int u = 0; u < VPT; ++u) {
+        const uint32_t b = bin_at(u);
+        if (u < nv && b > bstar) above |= 1u << u;
+        if (u < nv && b == bstar) inb |= 1u << u;
+    }
+    // 3a. small bucket: its members ranked directly (larger score, or equal score and lower index)
+    if (rank_mode) {
+        const uint32_t cnt = (uint32_t)__popc(inb);
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        uint32_t wbase = 0;
+        if (lane == 31 && incl) wbase = atomicAdd(&n_cand, incl);
+        wbase = __shfl_sync(0xffffffffu, wbase, 31);
+        uint32_t slot = wbase + incl - cnt;
+#pragma unroll
+        for (int u = 0; u < VPT; ++u)  // static indices keep v[] in registers
+            if ((inb >> u) & 1u) {
+                cand_key[slot] = order_key(v[u]);
+                cand_idx[slot] = (uint32_t)(i0 + u);
+                ++slot;
+            }
+        __syncthreads();
+        const int nc = (int)n_cand;
+        for (int c = tid; c < nc; c += THREADS) {
+            const uint32_t my_k = cand_key[c], my_i = cand_idx[c];
+            uint32_t better = 0;
+            for (int j = 0; j < nc; ++j) {
+                const uint32_t kj = cand_key[j];
+                better += (kj > my_k) || (kj == my_k && cand_idx[j] < my_i);
+            }
+            if (better < need) atomicOr(&marks[my_i >> 5], 1u << (my_i & 31));
+        }
+        __syncthreads();
+    }
+    // 3b. crowded bucket: radix select on the 32-bit order keys inside b* for the threshold key T and
+    // the number of entries equal to T still needed
+    uint32_t T = 0u, need_T = 0u;
+    if (!take_all && !rank_mode) {
+        need_T = need;
+        uint32_t prefix = 0u, mask = 0u;
+#pragma unroll 1
+        for (int pass = 0; pass < 3; ++pass) {
+            const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+            const uint32_t dm = pass == 2 ? 0x3FFu : 0x7FFu;
+            for (int b = tid; b < kBins; b += THREADS) hist[b] = 0;
+            __syncthreads();
+#pragma unroll
+            for (int u = 0; u < VPT; ++u) {
+                const uint32_t key = order_key(v[u]);
+                if (((inb >> u) & 1u) && (key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
+            }
+            __syncthreads();
+            const uint32_t dg = SC::select(hist, need_T, wt, sel);
+            prefix |= dg << sh;
+            mask |= dm << sh;
+        }
+        T = prefix;
+    }
+    // 4. ordered compaction: definite members and (lowest-index first) entries equal to T
+    uint32_t dmask = above, tmask = 0u;
+    if (take_all) dmask |= inb;
+    else if (rank_mode) {
+        for (uint32_t m = inb; m; m &= m - 1) {
+            const int u = __ffs(m) - 1;
+            if ((marks[(i0 + u) >> 5] >> ((i0 + u) & 31)) & 1u) dmask |= 1u << u;
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < VPT; ++u) {
+            const uint32_t key = order_key(v[u]);
+            if (((inb >> u) & 1u) && key > T) dmask |= 1u << u;
+            if (((inb >> u) & 1u) && key == T) tmask |= 1u << u;
+        }
+    }
+    uint32_t ex_d, ex_t, tot_d, tot_t;
+    SC::scan2((uint32_t)__popc(dmask), (uint32_t)__popc(tmask), &ex_d, &ex_t, &tot_d, &tot_t, wt);
+    uint32_t tie_rank = ex_t;
+    uint32_t pos = ex_d + min(tie_rank, need_T);
+    for (uint32_t m = dmask | tmask; m; m &= m - 1) {
+        const int u = __ffs(m) - 1;
+        if ((dmask >> u) & 1u) out[pos++] = i0 + u;
+        else {
+            if (tie_rank < need_T) out[pos++] = i0 + u;
+            ++tie_rank;
+        }
+    }
+    const uint32_t total = tot_d + min(tot_t, need_T);
+    for (int i = (int)total + tid; i < k; i += THREADS) out[i] = -1;
+    if (tid == 0 && total != (uint32_t)k) report(status, DSA_ERR_DEVICE_FAULT);
 }
 
 }  // namespace dsa
@@ -358,14 +632,21 @@ extern "C" dsa_status_t dsa_topk(int32_t nq, const float* scores, int32_t ld, co
     if (nq < 0 || k < 1 || k > 2048 || ld < 0 || (ld & 3)) return DSA_ERR_INVALID_ARG;
     if (nq == 0) return DSA_OK;
     if (!scores || !n_valid || !idx_out || !aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
-    const int chunk = ((ld + kTopkCluster - 1) / kTopkCluster + 3) & ~3;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (ld <= 16 * 1024) {  // one CTA per row, the row in registers
+        const cudaError_t e = launch_pdl(topk_reg_kernel<1024, 16>, dim3(nq), dim3(1024), 0, st, scores, ld, n_valid,
+                                         k, idx_out, dev_status);
+        return e == cudaSuccess ? launch_status() : DSA_ERR_CUDA;
+    }
+    const int csz = ld <= kQuarterMax ? 1 : kTopkClusterMax;
+    const int chunk = ((ld + csz - 1) / csz + 3) & ~3;
     if (chunk > kQuarterMax) return DSA_ERR_UNSUPPORTED;
     const size_t smem = (size_t)(2 * kBins + 2 * kRankMax + kQuarterMax / 32 + 1) * sizeof(uint32_t) +
                         (size_t)chunk * sizeof(float);
     if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DSA_ERR_CUDA;
-    if (launch_pdl(topk_kernel, dim3(nq * kTopkCluster), dim3(kTopkThreads), smem, static_cast<cudaStream_t>(stream),
-                   scores, ld, n_valid, k, idx_out, dev_status) != cudaSuccess)
+    if (launch_pdl_cluster(topk_kernel, dim3(nq * csz), dim3(kTopkThreads), smem, st, csz, scores, ld, n_valid, k,
+                           idx_out, dev_status) != cudaSuccess)
         return DSA_ERR_CUDA;
     return launch_status();
 }

@@ -21,7 +21,7 @@ KIND = {"c4a": DSA_C4A, "c128a": DSA_C128A}
 
 EXPORTS = ["dsa_status_string", "dsa_compress", "dsa_index_scores", "dsa_topk", "dsa_attn_workspace_size",
            "dsa_sparse_attn_decode", "dsa_sparse_attn_prefill", "dsa_gather_rows", "dsa_sparse_attn_decode_static",
-           "dsa_attn_static_scratch_bytes"]
+           "dsa_attn_static_scratch_bytes", "dsa_attn_plan"]
 
 
 class DsaPool(ctypes.Structure):
@@ -51,6 +51,8 @@ _lib.dsa_attn_workspace_size.restype = ctypes.c_size_t
 _lib.dsa_attn_workspace_size.argtypes = [_I, _I, _I]
 _lib.dsa_attn_static_scratch_bytes.restype = ctypes.c_size_t
 _lib.dsa_attn_static_scratch_bytes.argtypes = []
+_lib.dsa_attn_plan.restype = ctypes.c_int32
+_lib.dsa_attn_plan.argtypes = [_I, _I, _I, _I, _P]
 for _name, _args in {
     "dsa_compress": [_I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P],
     "dsa_index_scores": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P],
@@ -134,6 +136,15 @@ def dsa_topk(scores, n_valid, k, idx_out, dev_status=None, stream=None):
 
 def dsa_attn_workspace_size(nq, heads, max_keys):
     return int(_lib.dsa_attn_workspace_size(int(nq), int(heads), int(max_keys)))
+
+
+def dsa_attn_plan(nq, heads, max_keys, dtype="bf16"):
+    """(heads per CTA, CTAs per cluster, key splits per row, kernels per call) of the attention call."""
+    plan = (ctypes.c_int32 * 4)()
+    code = _lib.dsa_attn_plan(int(nq), int(heads), int(max_keys), {"bf16": DSA_BF16, "fp8": DSA_FP8_E4M3}.get(dtype, dtype),
+                              plan)
+    _check("dsa_attn_plan", code)
+    return tuple(int(x) for x in plan)
 
 
 def dsa_sparse_attn_decode(q, q_pos, kind, topk, k, main, main_bt, swa, swa_bt, window, sm_scale, rope_cfg, out,

@@ -53,6 +53,7 @@ class LayerStep:
         self.lse = torch.empty((nq, spec.heads), dtype=torch.float32, device=dev)
         max_keys = (spec.topk if self.has_index else case["bt_main"].shape[1] * epb) + spec.window
         ws = dsa.dsa_attn_workspace_size(nq, spec.heads, max_keys)
+        self.attn_plan = dsa.dsa_attn_plan(nq, spec.heads, max_keys, spec.main_dtype)
         self.workspace = torch.empty((max(ws, 256),), dtype=torch.uint8, device=dev) if ws else None
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
         self.max_new = max(spec.new) if spec.new else 0
@@ -101,12 +102,12 @@ class LayerStep:
 
     def launches_per_step(self):
         """Kernels one ``run()`` launches (compress: +1 ring kernel when a request appends > 1 token;
-        attention: +1 combine kernel when keys are split over CTAs)."""
+        attention: +1 merge kernel when a row's keys are split over several clusters)."""
         per_compress = 1 + (1 if self.max_new > 1 else 0)
         n = per_compress
         if self.has_index:
             n += (per_compress if self.spec.index_compress else 0) + 2
-        n += 1 + (1 if self.workspace is not None else 0)
+        n += self.attn_plan[3]
         return n
 
     def run(self):

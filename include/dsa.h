@@ -169,11 +169,22 @@ dsa_status_t dsa_topk(int32_t nq, const float* scores, int32_t ld, const int32_t
                       int32_t* idx_out, int32_t* dev_status, void* stream);
 
 /*
- * Split-K workspace (bytes) that dsa_sparse_attn_decode / _prefill need for nq query
- * rows of `heads` heads and at most `max_keys` keys per row (compressed + window) on the
- * current device.  0 means the call needs none.
+ * Workspace (bytes) that dsa_sparse_attn_decode / _prefill need for nq query rows of
+ * `heads` heads and at most `max_keys` keys per row (compressed + window) on the current
+ * device, for either pool format: the fp32 partial outputs and (max, sum) pairs of rows whose
+ * keys are split over several groups of CTAs.  0 means the call needs none.
  */
 size_t dsa_attn_workspace_size(int32_t nq, int32_t heads, int32_t max_keys);
+
+/*
+ * dsa_attn_plan - how dsa_sparse_attn_decode / _prefill split the work for these sizes on
+ * the current device and pool format (dtype DSA_BF16 or DSA_FP8_E4M3); host only, launches
+ * nothing.  plan[0] = heads per CTA, plan[1] = CTAs per cluster (one query row's keys shared
+ * among them), plan[2] = key splits per row, plan[3] = kernels one call launches (1, or 2 with
+ * the split merge).  Returns DSA_ERR_INVALID_ARG / DSA_ERR_UNSUPPORTED as the attention call
+ * would for these sizes.
+ */
+dsa_status_t dsa_attn_plan(int32_t nq, int32_t heads, int32_t max_keys, int32_t dtype, int32_t* plan);
 
 /*
  * dsa_sparse_attn_decode - main attention of one decode query per request.

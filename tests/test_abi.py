@@ -66,3 +66,19 @@ def test_workspace_size_is_zero_for_unsupported_heads(lib):
     lib.dsa_attn_workspace_size.restype = ctypes.c_size_t
     assert lib.dsa_attn_workspace_size(32, 48, 640) == 0
     assert lib.dsa_attn_workspace_size(0, 64, 640) == 0
+
+
+def test_attention_plan_host_only(lib):
+    """The split plan is host arithmetic: valid without a GPU (the SM count falls back to a default)."""
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    hg, cl, ns, launches = dsa.dsa_attn_plan(32, 64, 640, "bf16")
+    assert hg == 64 and cl in (1, 2, 4) and ns >= 1 and launches == (2 if ns > 1 else 1)
+    hg, cl, ns, launches = dsa.dsa_attn_plan(4, 128, 8320, "bf16")
+    assert hg == 64 and cl == 4 and ns > 1 and launches == 2
+    assert dsa.dsa_attn_plan(8192, 64, 640, "bf16")[1:3] == (1, 1)        # many rows: one CTA per row
+    P = ctypes.c_void_p
+    lib.dsa_attn_plan.argtypes = [ctypes.c_int32] * 4 + [P]
+    plan = (ctypes.c_int32 * 4)()
+    assert lib.dsa_attn_plan(0, 64, 640, 0, plan) == 1
+    assert lib.dsa_attn_plan(4, 48, 640, 0, plan) == 2
+    assert lib.dsa_attn_plan(4, 64, 640, 7, plan) == 1

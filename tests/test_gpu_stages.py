@@ -181,6 +181,42 @@ def test_attention(name):
     assert np.max(np.abs(glse - np.stack([lse[q] for q in range(cpu["nq"])]))) <= 1e-3
 
 
+SHARP = {
+    # 4 rows: clusters of 4 CTAs and two key splits per row (split partials merged by the combine kernel)
+    "c4a_decode": CASES["c4a_decode"],
+    # 48 rows: clusters of 2 CTAs
+    "c4a_decode_48": S("c4a_decode_48", cached=[int(x) for x in np.random.default_rng(18).integers(600, 3000, 48)],
+                       new=[1] * 48, seed=18),
+    # dense over c128a entries, a long key list per CTA
+    "c128a_decode": CASES["c128a_decode"],
+}
+
+
+@pytest.mark.parametrize("name", list(SHARP))
+def test_attention_sharp_scores(name):
+    """Queries scaled by 40: logits spread over hundreds of log2 units, so a CTA's running maximum
+    keeps moving between sub-tiles (the rescale path) and the softmax is nearly one-hot."""
+    cpu = synth.make_case(SHARP[name], "cpu")
+    gpu = to_device(cpu)
+    gpu["q"].mul_(40.0)
+    step = LayerStep(gpu)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    spec, epb = cpu["spec"], cpu["epb"]
+    main = oracle_pool(gpu["main_data"], gpu["main_scale"], epb)
+    swa = oracle_pool(gpu["swa_data"], gpu["swa_scale"], 256)
+    topk = np64(step.topk) if step.has_index else None
+    want, lse = OL.sparse_attn(np64(gpu["q"]), np64(cpu["q_pos"]), np64(cpu["q_req"]), spec.kind, topk, main,
+                               np64(cpu["bt_main"]), swa, np64(cpu["bt_swa"]), spec.window, SM_SCALE, spec.rope_dim)
+    got, glse = np64(step.out), np64(step.lse)
+    W = np.stack([want[q] for q in range(cpu["nq"])])
+    assert np.max(np.abs(got - W)) <= ATTN_MAX_ABS
+    assert rel_l2(got, W) <= ATTN_REL_L2
+    L = np.stack([lse[q] for q in range(cpu["nq"])])
+    assert np.max(np.abs(glse - L) / np.maximum(1.0, np.abs(L))) <= 1e-4
+
+
 def test_gather_rows_bit_exact_and_unmapped_fault():
     from compressed_sparse_attention_c4a_gb300 import dsa
     cpu, gpu, step = _setup("c4a_decode")
