@@ -7,10 +7,12 @@
 //
 // Tile: 128 consecutive entries of one request (two 64-entry pages of the paged fp8 key pool) x
 // N = (queries of the group) * heads columns.  TMA copies each page (a 64 x dim box, 128B or 64B
-// swizzle) and the group's query codes into shared memory; one thread issues
-// tcgen05.mma.kind::f8f6f4 (M = 128, N, K = 32 per instruction, fp32 accumulation in TMEM); four
-// warps read their 32 TMEM lanes (one entry each) and apply the per-entry scale, ReLU, per-head
-// weight and causal mask, writing coalesced score rows.  Every wait is bounded.
+// swizzle) into a stage; the group's query codes, head weights and query scales go into one of two
+// group buffers only when the group changes (a CTA's items are consecutive tiles of few groups).  One
+// thread issues tcgen05.mma.kind::f8f6f4 (M = 128, N, K = 32 per instruction, fp32 accumulation in
+// TMEM); four warps read their 32 TMEM lanes (one entry each), load the entry's key scale and apply
+// it, ReLU, the per-head weights and the causal mask, writing coalesced score rows.  Every wait is
+// bounded.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -22,12 +24,13 @@ namespace dsa {
 constexpr int kIdxThreads = 192;  // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
 constexpr int kTileEntries = 128;
 constexpr int kPage = 64;         // c4a entries per 256-position block
-constexpr int kChunkItems = 8;    // consecutive tiles of one group handled back to back by one CTA
+constexpr int kChunkItems = 32;   // items resolved together (one per producer lane)
 
 struct IdxArgs {
     int nq, heads, q_group, n_cols, tmem_cols, ld;
-    int n_groups, tiles, stages, stage_bytes, n_acc;  // n_acc: TMEM accumulators (2 or 4)
-    long long total_items, n_chunks;
+    int n_groups, items, stages, stage_bytes, n_acc;  // items per group; n_acc: TMEM accumulators (2 or 4)
+    int gbuf_bytes;                                   // one group buffer: query codes, head weights, query scales
+    long long total_items;
     const float* q_scale;
     const float* w;
     const int32_t* q_pos;
@@ -58,10 +61,11 @@ __device__ __forceinline__ int visible_at(int m) { return m < 7 ? 0 : ((m - 7) >
 
 __device__ __forceinline__ int visible_of(const IdxArgs& a, int q) { return visible_at(a.q_pos[q]); }
 
-// Item = one 128-entry tile of one query group.  Its request, visibility and the physical blocks of
-// its two 64-entry pages, resolved by one producer lane.
+// Item = `tpi` consecutive 128-entry tiles of one query group (tpi = 1 or 2).  Its request, visibility
+// and the physical blocks of its 64-entry pages, resolved by one producer lane.
 struct ItemInfo {
-    int valid, g, t, r, max_vis, blk0, blk1;
+    int valid, g, t, r, max_vis, want;  // want: bit p set when page p holds visible entries
+    int blk[4];
 };
 
 // Request and visible-entry bound of query group g (r = -1 if the group mixes requests or names a
@@ -81,27 +85,24 @@ __device__ __forceinline__ void group_of(const IdxArgs& a, int g, int* r, int* m
 
 // Item (g, t): tile t of group g; `valid` = 0 marks "no item".  The group's request and visible-entry
 // bound come from the producer's shared-memory table (filled once per CTA).
+template <int TPI>
 __device__ __forceinline__ ItemInfo item_info(const IdxArgs& a, int valid, int g, int t, const int* grp_r,
                                               const int* grp_mv) {
-    ItemInfo x{0, g, t, -1, 0, -1, -1};
+    ItemInfo x{0, g, t, -1, 0, 0, {-1, -1, -1, -1}};
     if (!valid) return x;
     x.r = grp_r[g];
     x.max_vis = grp_mv[g];
-    if (x.r < 0 || t * kTileEntries >= x.max_vis) return x;
+    if (x.r < 0 || t * TPI * kTileEntries >= x.max_vis) return x;
     x.valid = 1;
-    int blk[2] = {-1, -1};
-    for (int pi = 0; pi < 2; ++pi) {
-        const int lp = 2 * t + pi;
-        if (lp * kPage >= x.max_vis) continue;
-        const int b = lp < a.bt.max_blocks ? a.bt.table[(long long)x.r * a.bt.max_blocks + lp] : -1;
-        if (b < 0 || b >= a.num_blocks) {
-            report(a.status, DSA_ERR_DEVICE_FAULT);
-            continue;
-        }
-        blk[pi] = b;
+    // no branch on the loaded table entries: the loads stay in flight until the item is used
+#pragma unroll
+    for (int pi = 0; pi < 2 * TPI; ++pi) {
+        const int lp = 2 * TPI * t + pi;
+        const bool want = lp * kPage < x.max_vis;
+        const bool in_table = want && lp < a.bt.max_blocks;
+        x.blk[pi] = in_table ? a.bt.table[(long long)x.r * a.bt.max_blocks + lp] : -1;
+        x.want |= want ? (1 << pi) : 0;
     }
-    x.blk0 = blk[0];
-    x.blk1 = blk[1];
     return x;
 }
 
@@ -112,8 +113,9 @@ __device__ __forceinline__ ItemInfo shfl_item(const ItemInfo& x, int src) {
     y.t = __shfl_sync(0xffffffffu, x.t, src);
     y.r = __shfl_sync(0xffffffffu, x.r, src);
     y.max_vis = __shfl_sync(0xffffffffu, x.max_vis, src);
-    y.blk0 = __shfl_sync(0xffffffffu, x.blk0, src);
-    y.blk1 = __shfl_sync(0xffffffffu, x.blk1, src);
+    y.want = __shfl_sync(0xffffffffu, x.want, src);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) y.blk[p] = __shfl_sync(0xffffffffu, x.blk[p], src);
     return y;
 }
 
@@ -133,14 +135,16 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
     }
 }
 
-// Per-stage layout (bytes from the stage start): key tile [128][DIM] (swizzled), query tile
-// [n_cols][DIM] (swizzled), StageMeta, then fp32 entry scales [128], head weights [n_cols] and query
-// scales [n_cols] (bulk copies).  Only the producer walks the work list; it describes each item in its
+// Per-stage layout (bytes from the stage start): key tiles [TPI][128][DIM] (swizzled), StageMeta, fp32
+// entry scales [TPI * 128] (cp.async, 16 bytes per producer lane and tile, completing on the stage's
+// barrier).  Group
+// buffer: query tile [n_cols][DIM] (swizzled), head weights [n_cols], query scales [n_cols].  Only the producer walks the work list; it describes each item in its
 // stage (or posts a terminal stage), so the MMA and epilogue roles never touch global metadata.  The
 // epilogue releases the stage, so everything it reads stays in shared memory until it is done.
 struct StageMeta {
     int terminal;  // 1: no more items for this CTA
-    int blk[2];    // physical block of each 64-entry page, -1 if not loaded
+    int gb;        // group buffer holding the item's query codes, weights and query scales
+    int blk[4];    // physical block of each 64-entry page, -1 if not loaded
     int nq;        // queries in the group
     int q0;        // first query of the group
     int e0;        // first entry of the tile
@@ -149,18 +153,23 @@ struct StageMeta {
 
 __host__ __device__ constexpr int meta_bytes() { return ((int)sizeof(StageMeta) + 15) / 16 * 16; }
 
-template <int DIM, int HEADS>
+template <int DIM, int HEADS, int TPI>
 __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constant__ CUtensorMap kmap,
                                                             const __grid_constant__ CUtensorMap qmap, IdxArgs a) {
+    constexpr int kItem = TPI * kTileEntries;  // entries per item
+    constexpr int kPages = 2 * TPI;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = a.stages, NA = a.n_acc;
-    const int tiles_bytes = (kTileEntries + a.n_cols) * DIM;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * a.stage_bytes);
+    const int tiles_bytes = kItem * DIM;
+    uint8_t* gbase = smem + (size_t)S * a.stage_bytes;  // two group buffers
+    uint64_t* full = reinterpret_cast<uint64_t*>(gbase + 2 * a.gbuf_bytes);
     uint64_t* empty = full + S;
     uint64_t* tfull = empty + S;   // [NA]
     uint64_t* tempty = tfull + 4;  // [NA]
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + 4);
+    uint64_t* gfull = tempty + 4;  // [2] group buffer loaded
+    uint64_t* gempty = gfull + 2;  // [2] group buffer released by the epilogue warps
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(gempty + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(s_tmem + 1);
     int* grp_nvis = reinterpret_cast<int*>(s_tmem + 2);  // producer warp's cache [64]
     int* grp_prefix = grp_nvis + 64;                     // [n_groups + 1] valid tiles before each group
@@ -172,12 +181,16 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
 
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
-            mbar_init(&full[i], 1);
+            mbar_init(&full[i], 1 + 32);  // the producer's lane 0 (with the TMA bytes) + 32 scale copies
             mbar_init(&empty[i], 4 * 32);
         }
         for (int b = 0; b < NA; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], 4 * 32);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&gfull[b], 1);
+            mbar_init(&gempty[b], 4);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -211,7 +224,7 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
                 grp_r[g] = r;
                 grp_mv[g] = mv;
                 if (r < 0) report(a.status, DSA_ERR_DEVICE_FAULT);
-                else cnt = min((mv + kTileEntries - 1) / kTileEntries, a.tiles);
+                else cnt = min((mv + kItem - 1) / kItem, a.items);
             }
             int incl = cnt;
 #pragma unroll
@@ -242,16 +255,27 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
             int g = 0, t = 0;
             const int valid = lane < kChunkItems && idx < hi;
             if (valid) locate(idx, &g, &t);
-            return item_info(a, valid, g, t, grp_r, grp_mv);
+            return item_info<TPI>(a, valid, g, t, grp_r, grp_mv);
         };
-        int n = 0, cached_g = -1;
+        int n = 0, cached_g = -1, ps = 0, pphase = 0;  // items issued; stage index and its phase parity
+        int cur_g = -1, gb = 1, guse[2] = {0, 0};  // group in the current buffer, buffer index, loads per buffer
         bool alive = true;
         ItemInfo cur = resolve(lo);
         for (long long base = lo; base < hi && alive; base += kChunkItems) {
             const ItemInfo nxt = resolve(base + kChunkItems);
             for (int u = 0; u < kChunkItems; ++u) {
-                const ItemInfo it = shfl_item(cur, u);
+                ItemInfo it = shfl_item(cur, u);
                 if (!it.valid) continue;
+                // a visible page whose table entry is unmapped or outside the pool: a device fault, not loaded
+                bool bad = false;
+#pragma unroll
+                for (int p = 0; p < kPages; ++p) {
+                    const bool w = (it.want >> p) & 1;
+                    const bool b = w && (it.blk[p] < 0 || it.blk[p] >= a.num_blocks);
+                    bad |= b;
+                    if (b || !w) it.blk[p] = -1;
+                }
+                if (bad && lane == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
                 const int q0 = it.g * a.q_group;
                 const int nqg = min(a.q_group, a.nq - q0);
                 if (a.q_group > 1 && it.g != cached_g) {  // per-query visibility of a multi-query group
@@ -259,75 +283,129 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
                     __syncwarp();
                     cached_g = it.g;
                 }
-                if (lane == 0) {
-                    const int s = n % S;
-                    if (!wait_or_abort(&empty[s], ((n / S) & 1) ^ 1, abort_flag, a.status)) {
+                if (lane == 0 && it.g != cur_g) {
+                    // a new group: its query codes, weights and query scales into the other buffer, once the
+                    // epilogue has let go of that buffer's previous group
+                    gb ^= 1;
+                    if (guse[gb] > 0 && !wait_or_abort(&gempty[gb], (guse[gb] - 1) & 1, abort_flag, a.status)) {
                         alive = false;
                     } else {
-                        uint8_t* st = smem + (size_t)s * a.stage_bytes;
-                        StageMeta* meta = stage_meta(s);
-                        float* sscale = reinterpret_cast<float*>(st + tiles_bytes + meta_bytes());
-                        float* sw = sscale + kTileEntries;
-                        float* ssq = sw + a.n_cols;
-                        meta->terminal = 0;
-                        meta->blk[0] = it.blk0;
-                        meta->blk[1] = it.blk1;
-                        meta->nq = nqg;
-                        meta->q0 = q0;
-                        meta->e0 = it.t * kTileEntries;
-                        if (a.q_group == 1) meta->nvis[0] = it.max_vis;
-                        else
-                            for (int j = 0; j < nqg; ++j) meta->nvis[j] = grp_nvis[j];
-                        const uint32_t bytes = (uint32_t)a.n_cols * DIM + 2u * nqg * HEADS * 4u +
-                                               (it.blk0 >= 0 ? kPage * (DIM + 4) : 0) +
-                                               (it.blk1 >= 0 ? kPage * (DIM + 4) : 0);
-                        mbar_arrive_expect_tx(&full[s], bytes);  // release: the meta writes above are visible
-                        if (it.blk0 >= 0) {
-                            tma_load_2d(st, &kmap, 0, it.blk0 * kPage, &full[s]);
-                            bulk_g2s(sscale, a.key_scale + (long long)it.blk0 * kPage, kPage * 4, &full[s]);
-                        }
-                        if (it.blk1 >= 0) {
-                            tma_load_2d(st + kPage * DIM, &kmap, 0, it.blk1 * kPage, &full[s]);
-                            bulk_g2s(sscale + kPage, a.key_scale + (long long)it.blk1 * kPage, kPage * 4, &full[s]);
-                        }
-                        tma_load_2d(st + kTileEntries * DIM, &qmap, 0, q0 * HEADS, &full[s]);
-                        bulk_g2s(sw, a.w + (long long)q0 * HEADS, nqg * HEADS * 4, &full[s]);
-                        bulk_g2s(ssq, a.q_scale + (long long)q0 * HEADS, nqg * HEADS * 4, &full[s]);
+                        uint8_t* gp = gbase + (size_t)gb * a.gbuf_bytes;
+                        mbar_arrive_expect_tx(&gfull[gb], (uint32_t)a.n_cols * DIM + 2u * nqg * HEADS * 4u);
+                        tma_load_2d(gp, &qmap, 0, q0 * HEADS, &gfull[gb]);
+                        bulk_g2s(gp + a.n_cols * DIM, a.w + (long long)q0 * HEADS, nqg * HEADS * 4, &gfull[gb]);
+                        bulk_g2s(gp + a.n_cols * DIM + a.n_cols * 4, a.q_scale + (long long)q0 * HEADS, nqg * HEADS * 4,
+                                 &gfull[gb]);
+                        ++guse[gb];
+                        cur_g = it.g;
                     }
+                }
+                const int s = ps;
+                bool go = false;
+                if (lane == 0 && alive) {
+                    go = wait_or_abort(&empty[s], pphase ^ 1, abort_flag, a.status);
+                    alive = go;
+                }
+                go = __shfl_sync(0xffffffffu, go, 0);
+                uint8_t* st = smem + (size_t)s * a.stage_bytes;
+                if (go) {  // the entry scales: 16 lanes per page, zero-filled where a page is absent
+#pragma unroll
+                    for (int i = 0; i < TPI; ++i) {
+                        const int pg = 2 * i + (lane >> 4);
+                        const int bp = (lane >> 4) ? it.blk[2 * i + 1] : it.blk[2 * i];
+                        const float* src = bp >= 0 ? a.key_scale + (long long)bp * kPage + (lane & 15) * 4 : a.key_scale;
+                        cp_async16_nc(smem_u32(st + tiles_bytes + meta_bytes() + (pg * kPage + (lane & 15) * 4) * 4), src,
+                                      bp >= 0 ? 16u : 0u);
+                    }
+                    cp_async_arrive_noinc(&full[s]);
+                }
+                if (lane == 0 && go) {
+                    StageMeta* meta = stage_meta(s);
+                    meta->terminal = 0;
+                    meta->gb = gb;
+                    uint32_t bytes = 0;
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        meta->blk[p] = p < kPages ? it.blk[p] : -1;
+                        if (p < kPages && it.blk[p] >= 0) bytes += kPage * DIM;
+                    }
+                    meta->nq = nqg;
+                    meta->q0 = q0;
+                    meta->e0 = it.t * kItem;
+                    if (a.q_group == 1) meta->nvis[0] = it.max_vis;
+                    else
+                        for (int j = 0; j < nqg; ++j) meta->nvis[j] = grp_nvis[j];
+                    mbar_arrive_expect_tx(&full[s], bytes);  // release: the meta writes above are visible
+                }
+                __syncwarp();
+                if (go && lane < kPages) {  // one page per lane
+                    int bp = it.blk[0];
+#pragma unroll
+                    for (int p = 1; p < kPages; ++p)
+                        if (lane == p) bp = it.blk[p];
+                    if (bp >= 0) tma_load_2d(st + lane * kPage * DIM, &kmap, 0, bp * kPage, &full[s]);
                 }
                 alive = __shfl_sync(0xffffffffu, alive, 0);
                 if (!alive) break;
                 ++n;
+                if (++ps == S) {
+                    ps = 0;
+                    pphase ^= 1;
+                }
             }
             cur = nxt;
         }
-        if (lane == 0 && alive) {  // terminal stage: consumers stop here
-            const int s = n % S;
-            if (wait_or_abort(&empty[s], ((n / S) & 1) ^ 1, abort_flag, a.status)) {
-                stage_meta(s)->terminal = 1;
+        {  // terminal stage: consumers stop here (33 arrivals, no bytes)
+            const int s = ps;
+            bool go = false;
+            if (lane == 0 && alive) {
+                go = wait_or_abort(&empty[s], pphase ^ 1, abort_flag, a.status);
+                if (go) stage_meta(s)->terminal = 1;
+            }
+            go = __shfl_sync(0xffffffffu, go, 0);
+            if (go) {
                 mbar_arrive(&full[s]);
+                if (lane == 0) mbar_arrive(&full[s]);
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---- MMA issuer: D[entry][q*heads + h] = <k8_entry, q8_(q,h)>, accumulated over dim ------
-            const uint32_t idesc = idesc_f8(a.n_cols);
-            for (int n = 0;; ++n) {
-                const int s = n % S, b = n % NA;
-                if (!wait_or_abort(&full[s], (n / S) & 1, abort_flag, a.status)) break;
-                if (!wait_or_abort(&tempty[b], ((n / NA) & 1) ^ 1, abort_flag, a.status)) break;
-                if (stage_meta(s)->terminal) {
-                    mbar_arrive(&tfull[b]);
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t a_addr = smem_u32(smem + (size_t)s * a.stage_bytes);
-                const uint32_t b_addr = a_addr + kTileEntries * DIM;
+        // ---- MMA issuer: D[entry][q*heads + h] = <k8_entry, q8_(q,h)>, accumulated over dim; the warp
+        // waits, one elected lane issues --------------------------------------------------------------
+        const uint32_t idesc = idesc_f8(a.n_cols);
+        int prev_gb = -1, muse[2] = {0, 0};
+        int s = 0, sph = 0, b = 0, bph = 0;  // stage / accumulator index and phase parity
+        for (int n = 0;; ++n) {
+            bool ok = wait_or_abort(&full[s], sph, abort_flag, a.status);
+            ok = ok && wait_or_abort(&tempty[b], bph ^ 1, abort_flag, a.status);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            if (stage_meta(s)->terminal) {
+                if (lane == 0) mbar_arrive(&tfull[b]);
+                break;
+            }
+            const int gbi = stage_meta(s)->gb;
+            if (gbi != prev_gb) {  // the first item of a group: its buffer's load
+                prev_gb = gbi;
+                ++muse[gbi];
+                ok = wait_or_abort(&gfull[gbi], (muse[gbi] - 1) & 1, abort_flag, a.status);
+                if (!__all_sync(0xffffffffu, ok)) break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(smem + (size_t)s * a.stage_bytes);
+            const uint32_t b_addr = smem_u32(gbase + (size_t)gbi * a.gbuf_bytes);
+#pragma unroll
+            for (int tt = 0; tt < TPI; ++tt)
 #pragma unroll
                 for (int ks = 0; ks < DIM / 32; ++ks)
-                    mma_f8(tmem + b * a.n_cols, smem_desc(a_addr + ks * 32, DIM), smem_desc(b_addr + ks * 32, DIM),
-                           idesc, ks > 0);
-                mma_commit(&tfull[b]);
+                    mma_f8_elect(tmem + (b * TPI + tt) * a.n_cols, smem_desc(a_addr + tt * kTileEntries * DIM + ks * 32, DIM),
+                                 smem_desc(b_addr + ks * 32, DIM), idesc, ks > 0 ? 1u : 0u);
+            mma_commit_elect(&tfull[b]);
+            if (++s == S) {
+                s = 0;
+                sph ^= 1;
+            }
+            if (++b == NA) {
+                b = 0;
+                bph ^= 1;
             }
         }
     } else {
@@ -335,43 +413,66 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
         const int quad = warp & 3;  // TMEM lanes this warp may access
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        int prev_gb = -1, euse[2] = {0, 0};
+        int s = 0, sph = 0, b = 0, bph = 0;  // stage / accumulator index and phase parity
         for (int n = 0;; ++n) {
-            const int s = n % S, b = n % NA;
-            bool ok = wait_or_abort(&tfull[b], (n / NA) & 1, abort_flag, a.status);
-            ok = ok && wait_or_abort(&full[s], (n / S) & 1, abort_flag, a.status);  // completed: orders the meta
-            if (!__all_sync(0xffffffffu, ok)) break;  // warp-uniform: tcgen05.ld is warp-collective
+            bool ok = wait_or_abort(&full[s], sph, abort_flag, a.status);  // completed: orders the meta
+            if (!__all_sync(0xffffffffu, ok)) break;
             const StageMeta* meta = stage_meta(s);
             if (meta->terminal) break;
+
+            const int gbi = meta->gb;
+            if (gbi != prev_gb) {  // this warp is done with the previous group's buffer
+                if (prev_gb >= 0 && lane == 0) mbar_arrive(&gempty[prev_gb]);
+                prev_gb = gbi;
+                ++euse[gbi];
+                ok = wait_or_abort(&gfull[gbi], (euse[gbi] - 1) & 1, abort_flag, a.status);
+            }
+            ok = ok && wait_or_abort(&tfull[b], bph, abort_flag, a.status);
+            if (!__all_sync(0xffffffffu, ok)) break;  // warp-uniform: tcgen05.ld is warp-collective
             tc_fence_after();
-            const uint8_t* st = smem + (size_t)s * a.stage_bytes;
-            const float* sscale = reinterpret_cast<const float*>(st + tiles_bytes + meta_bytes());
-            const float* sw = sscale + kTileEntries;
+            const float* sw = reinterpret_cast<const float*>(gbase + (size_t)gbi * a.gbuf_bytes + a.n_cols * DIM);
             const float* ssq = sw + a.n_cols;
-            const bool page_ok = meta->blk[row / kPage] >= 0;
-            const float sk = page_ok ? sscale[row] : 0.f;
-            const int e = meta->e0 + row;
             const int nqg = meta->nq, q0 = meta->q0;
-            for (int c0 = 0; c0 < a.n_cols; c0 += 16) {
-                float v[16];
-                tmem_ld16(lane_base + b * a.n_cols + c0, v);
+            const float* sscale = reinterpret_cast<const float*>(smem + (size_t)s * a.stage_bytes + tiles_bytes +
+                                                                 meta_bytes());
 #pragma unroll
-                for (int jj = 0; jj < 16 / HEADS; ++jj) {
-                    const int j = c0 / HEADS + jj;
-                    if (j < nqg) {
-                        float acc = 0.f;
+            for (int tt = 0; tt < TPI; ++tt) {
+                const int er = tt * kTileEntries + row;  // entry of the item
+                const bool page_ok = meta->blk[er / kPage] >= 0;
+                const float sk = page_ok ? sscale[er] : 0.f;
+                const int e = meta->e0 + er;
+                for (int c0 = 0; c0 < a.n_cols; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(lane_base + (b * TPI + tt) * a.n_cols + c0, v);
 #pragma unroll
-                        for (int h = 0; h < HEADS; ++h) {
-                            const int c = c0 + jj * HEADS + h;
-                            acc += sw[c] * fmaxf(0.f, ssq[c] * sk * v[jj * HEADS + h]);
+                    for (int jj = 0; jj < 16 / HEADS; ++jj) {
+                        const int j = c0 / HEADS + jj;
+                        if (j < nqg) {
+                            float acc = 0.f;
+#pragma unroll
+                            for (int h = 0; h < HEADS; ++h) {
+                                const int c = c0 + jj * HEADS + h;
+                                acc += sw[c] * fmaxf(0.f, ssq[c] * sk * v[jj * HEADS + h]);
+                            }
+                            if (e < a.ld)
+                                a.scores[(long long)(q0 + j) * a.ld + e] =
+                                    (page_ok && e < meta->nvis[j]) ? acc : -INFINITY;
                         }
-                        if (e < a.ld)
-                            a.scores[(long long)(q0 + j) * a.ld + e] = (page_ok && e < meta->nvis[j]) ? acc : -INFINITY;
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive(&tempty[b]);
             mbar_arrive(&empty[s]);
+            if (++s == S) {
+                s = 0;
+                sph ^= 1;
+            }
+            if (++b == NA) {
+                b = 0;
+                bph ^= 1;
+            }
         }
     }
     tc_fence_before();
@@ -394,33 +495,41 @@ static bool make_map(CUtensorMap* map, const void* base, uint64_t rows, int dim,
     return res == CUDA_SUCCESS;
 }
 
-template <int DIM, int HEADS>
+template <int DIM, int HEADS, int TPI>
 static dsa_status_t launch_index(const CUtensorMap& kmap, const CUtensorMap& qmap, IdxArgs a, cudaStream_t st) {
-    // stage = key tile + query tile + metadata + scales/weights; ~100-200 KB of stages per SM
-    const int payload = (kTileEntries + a.n_cols) * DIM + meta_bytes() + (kTileEntries + 2 * a.n_cols) * 4;
-    a.stage_bytes = (payload + 1023) / 1024 * 1024;
-    const int ctas_per_sm = a.stage_bytes <= 24 * 1024 ? 2 : 1;
-    // alignment slack + barriers, the producer's caches and the per-group prefix of valid tiles
-    const int extra = 1024 + 512 + ((3 * a.n_groups + 1) * 4 + 15) / 16 * 16;
+    // stage = TPI key tiles + metadata + entry scales; two group buffers of query codes + weights + query scales
+    a.stage_bytes = (TPI * kTileEntries * DIM + meta_bytes() + TPI * kTileEntries * 4 + 1023) / 1024 * 1024;
+    a.gbuf_bytes = (a.n_cols * DIM + 2 * a.n_cols * 4 + 1023) / 1024 * 1024;
+    a.items = (a.items + TPI - 1) / TPI;  // tiles -> items per group
+    // alignment slack + group buffers + barriers, the producer's caches and the per-group prefix of valid items
+    const int extra = 1024 + 2 * a.gbuf_bytes + 640 + ((3 * a.n_groups + 1) * 4 + 15) / 16 * 16;
+    const int ctas_per_sm = 2 * (extra + 3 * a.stage_bytes) <= 227 * 1024 && 2 * a.tmem_cols <= 512 ? 2 : 1;
     a.stages = max(2, min(8, (227 * 1024 / ctas_per_sm - extra) / a.stage_bytes));
     const int smem = extra + a.stages * a.stage_bytes;
-    if (cudaFuncSetAttribute(index_kernel<DIM, HEADS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    if (cudaFuncSetAttribute(index_kernel<DIM, HEADS, TPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
         return DSA_ERR_CUDA;
+    a.total_items = (long long)a.items * a.n_groups;
     const long long grid = std::min<long long>(a.total_items, (long long)sm_count() * ctas_per_sm);
-    if (launch_pdl(index_kernel<DIM, HEADS>, dim3((unsigned)std::max<long long>(grid, 1)), dim3(kIdxThreads), smem,
+    if (launch_pdl(index_kernel<DIM, HEADS, TPI>, dim3((unsigned)std::max<long long>(grid, 1)), dim3(kIdxThreads), smem,
                    st, kmap, qmap, a) != cudaSuccess)
         return DSA_ERR_CUDA;
     return launch_status();
+}
+
+template <int DIM, int HEADS>
+static dsa_status_t launch_index_tpi(const CUtensorMap& kmap, const CUtensorMap& qmap, const IdxArgs& a,
+                                     cudaStream_t st) {
+    return a.n_cols <= 128 ? launch_index<DIM, HEADS, 2>(kmap, qmap, a, st) : launch_index<DIM, HEADS, 1>(kmap, qmap, a, st);
 }
 
 template <int DIM>
 static dsa_status_t launch_index_heads(const CUtensorMap& kmap, const CUtensorMap& qmap, const IdxArgs& a,
                                        cudaStream_t st) {
     switch (a.heads) {
-        case 4: return launch_index<DIM, 4>(kmap, qmap, a, st);
-        case 8: return launch_index<DIM, 8>(kmap, qmap, a, st);
-        default: return launch_index<DIM, 16>(kmap, qmap, a, st);
+        case 4: return launch_index_tpi<DIM, 4>(kmap, qmap, a, st);
+        case 8: return launch_index_tpi<DIM, 8>(kmap, qmap, a, st);
+        default: return launch_index_tpi<DIM, 16>(kmap, qmap, a, st);
     }
 }
 
@@ -451,9 +560,10 @@ extern "C" dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim,
     a.heads = heads;
     a.q_group = q_group;
     a.n_cols = n_cols;
-    a.n_acc = n_cols <= 128 ? 4 : 2;  // TMEM accumulators in flight (at most 512 columns)
+    const int tpi = n_cols <= 128 ? 2 : 1;  // 128-entry tiles per item (a stage)
+    a.n_acc = tpi * n_cols <= 128 ? 4 : 2;  // TMEM accumulators in flight (at most 512 columns)
     a.tmem_cols = 32;
-    while (a.tmem_cols < a.n_acc * n_cols) a.tmem_cols *= 2;
+    while (a.tmem_cols < a.n_acc * tpi * n_cols) a.tmem_cols *= 2;
     a.ld = ld;
     a.q_scale = q_scale;
     a.w = w;
@@ -468,10 +578,8 @@ extern "C" dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim,
     CUtensorMap kmap, qmap;
     if (!make_map(&kmap, keys->data, (uint64_t)keys->num_blocks * kPage, dim, kPage)) return DSA_ERR_CUDA;
     if (!make_map(&qmap, q8, (uint64_t)nq * heads, dim, n_cols)) return DSA_ERR_CUDA;
-    a.tiles = (ld + kTileEntries - 1) / kTileEntries;
+    a.items = (ld + kTileEntries - 1) / kTileEntries;  // tiles per group; items once the launch picks TPI
     a.n_groups = (nq + q_group - 1) / q_group;
-    a.total_items = (long long)a.tiles * a.n_groups;
-    a.n_chunks = (a.total_items + kChunkItems - 1) / kChunkItems;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return dim == 128 ? launch_index_heads<128>(kmap, qmap, a, st) : launch_index_heads<64>(kmap, qmap, a, st);
 }
