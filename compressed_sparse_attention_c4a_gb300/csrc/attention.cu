@@ -505,6 +505,7 @@ constexpr int kClRound = kClGatherThreads / kClKeys;   // sub-tiles resolved per
 constexpr int kClRing = 2 * kClRound;                  // resolved sub-tiles kept (a ring of 10)
 constexpr int kClStage = kClKeys * kD * 2;
 constexpr float kLazyLog2 = 8.f;            // the running maximum moves when exceeded by more than this
+constexpr int kBtCache = 1024;              // main block tables up to this many blocks are cached in shared memory
 
 template <int NH>
 struct ClSmem {
@@ -521,7 +522,9 @@ struct ClSmem {
     static constexpr int kOffOwn = kOffVote + 32;                   // float m[NH], l[NH] of this CTA
     static constexpr int kOffStat = kOffOwn + 2 * NH * 4;           // float [4 ranks][NH][2]: (m, l) of each CTA
     static constexpr int kOffFac = kOffStat + 4 * NH * 8;           // float f[NH], L[NH], M[NH], 1/L[NH]
-    static constexpr int kOffBar = kOffFac + 4 * NH * 4;            // 10 mbarriers, TMEM address
+    static constexpr int kOffBt = kOffFac + 4 * NH * 4;             // int [kBtCache]: the request's main block table
+    static constexpr int kOffSwb = kOffBt + kBtCache * 4;           // int [8]: window-pool blocks from that of wlo
+    static constexpr int kOffBar = kOffSwb + 32;                    // 10 mbarriers, TMEM address
     static constexpr int kBytes = kOffBar + 10 * 8 + 16;
     static constexpr int kAlloc = kBytes + 1024;                    // + alignment slack
     static constexpr int kTile = 128 * NH * 4;                      // one 128-dim O tile, fp32 [NH / 4][128] float4
@@ -538,29 +541,8 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int e, int chunk_stride)
                       ((in & 7) << 1));
 }
 
-// Key j of a row for the tensor-core kernel.  Keys [0, n_comp) are compressed slots, [n_comp, ncp) padding
-// up to a multiple of 4, [ncp, ncp + window count) window positions.  Returns the physical row (pool in
-// *pool: 1 main, 2 window) or -1 for a masked key; reports faults.
-__device__ __forceinline__ int resolve_key4(const AttnArgs& a, int row, int r, int n_vis, int n_comp, int ncp,
-                                            int wlo, int j, int* pool) {
-    if (j < ncp) {
-        *pool = 1;
-        if (j >= n_comp) return -1;
-        const int id = a.topk ? __ldg(a.topk + (long long)row * a.k + j) : j;
-        if (id < 0) return -1;
-        if (id >= n_vis) {
-            report(a.status, DSA_ERR_DEVICE_FAULT);
-            return -1;
-        }
-        const long long p = physical_row(a.main_bt, r, id, a.main.rows_per_block, a.main.num_blocks);
-        if (p < 0) report(a.status, DSA_ERR_DEVICE_FAULT);
-        return (int)p;
-    }
-    *pool = 2;
-    const long long p = physical_row(a.swa_bt, r, (long long)wlo + (j - ncp), kBlockPositions, a.swa.num_blocks);
-    if (p < 0) report(a.status, DSA_ERR_DEVICE_FAULT);
-    return (int)p;
-}
+// Keys of a row for the tensor-core kernel: [0, n_comp) compressed slots, [n_comp, ncp) padding up to a
+// multiple of 4, [ncp, ncp + window count) window positions.
 
 template <int NH>
 __global__ void __launch_bounds__(kClThreads, 1)
@@ -638,32 +620,77 @@ __global__ void __launch_bounds__(kClThreads, 1)
     if (warp >= 5) {
         // ---- gather warps: resolve keys a round ahead, prefetch rows into L2, copy with cp.async -----
         const int gt = tid - 160, gw = warp - 5;
-        if (gt == 0) {
-            if (n_mine > 0) {
-                mbar_expect_tx(qfull, NH * kD * 2);
-                for (int c = 0; c < kD / 64; ++c)
-                    tma_load_2d(smem + L::kOffQ + c * 8192, &qmap, c * 64, row * a.heads + hg * NH, qfull);
-            }
-            mbar_arrive(qfull);
-        }
-        // sub-tiles [R * kClRound, (R + 1) * kClRound): thread -> sub-tile R * kClRound + gt / 64, key gt % 64
-        auto resolve_round = [&](int R) {
+        // The request's main block table (when it has at most kBtCache blocks) and the window pool's blocks
+        // of positions wlo .. m are cached in shared memory, loaded in the same round trip as the first
+        // round's top-k indices; a key then resolves with one global load (its top-k index) at most.
+        const bool bt_cached = a.main_bt.max_blocks <= kBtCache;
+        int* s_bt = reinterpret_cast<int*>(smem + L::kOffBt);
+        int* s_swb = reinterpret_cast<int*>(smem + L::kOffSwb);
+        // sub-tiles [R * kClRound, (R + 1) * kClRound): thread -> sub-tile R * kClRound + gt / 64, key gt % 64.
+        // Step 1: the key's top-k index (or entry / window position), no dependent load.
+        auto key_id = [&](int R, int* id) -> int {  // returns j (the key's index in the row), -1 if none
             const int i = R * kClRound + (gt >> 6);
-            if (gt >= kClRound * kClKeys || i >= n_mine) return;
+            if (gt >= kClRound * kClKeys || i >= n_mine) return -1;
             const int j = (g_lo + crank + csize * i) * kClKeys + (gt & 63);
+            *id = -1;
+            if (j < n_keys && j < n_comp) *id = a.topk ? __ldg(a.topk + (long long)row * a.k + j) : j;
+            return j;
+        };
+        // Step 2: index -> physical row through the cached tables (or global memory), L2 prefetch, ring slot.
+        auto finish_key = [&](int R, int j, int id) {
+            const int i = R * kClRound + (gt >> 6);
+            if (j < 0) return;
             int v = -1, pool = 1;
-            if (j < n_keys) {
-                v = resolve_key4(a, row, r, n_vis, n_comp, ncp, wlo, j, &pool);
-                if (v >= 0) {
-                    const uint8_t* base = pool == 2 ? static_cast<const uint8_t*>(a.swa.data)
-                                                    : static_cast<const uint8_t*>(a.main.data);
-                    prefetch_l2(base + (long long)v * (2 * kD), 2 * kD);
+            if (j < ncp) {
+                if (j < n_comp && id >= 0) {
+                    if (id >= n_vis) {
+                        report(a.status, DSA_ERR_DEVICE_FAULT);
+                    } else {
+                        const int epb = a.main.rows_per_block;
+                        const int lb = id / epb;
+                        const int pb = lb < a.main_bt.max_blocks
+                                           ? (bt_cached ? s_bt[lb] : __ldg(a.main_bt.table + (long long)r * a.main_bt.max_blocks + lb))
+                                           : -1;
+                        if (pb < 0 || pb >= a.main.num_blocks) report(a.status, DSA_ERR_DEVICE_FAULT);
+                        else v = pb * epb + (id - lb * epb);
+                    }
                 }
+            } else if (j < n_keys) {
+                pool = 2;
+                const int pos = wlo + (j - ncp);
+                const int lb = pos / kBlockPositions;
+                const int pb = s_swb[lb - wlo / kBlockPositions];  // the window (<= 1024 positions) spans <= 5 blocks
+                if (pb < 0 || pb >= a.swa.num_blocks) report(a.status, DSA_ERR_DEVICE_FAULT);
+                else v = pb * kBlockPositions + (pos - lb * kBlockPositions);
+            }
+            if (v >= 0 && R > 0) {  // rows of later rounds start moving into L2 (the first round is gathered at once)
+                const uint8_t* base = pool == 2 ? static_cast<const uint8_t*>(a.swa.data)
+                                                : static_cast<const uint8_t*>(a.main.data);
+                prefetch_l2(base + (long long)v * (2 * kD), 2 * kD);
             }
             s_row[(i % kClRing) * kClKeys + (gt & 63)] = v;
             s_pool[(i % kClRing) * kClKeys + (gt & 63)] = (uint8_t)pool;
         };
-        if (n_mine > 0) resolve_round(0);
+        auto resolve_round = [&](int R) {
+            int id = -1;
+            const int j = key_id(R, &id);
+            finish_key(R, j, id);
+        };
+        if (n_mine > 0) {
+            int id0 = -1;
+            const int j0 = key_id(0, &id0);
+            if (bt_cached)
+                for (int b = gt; b < a.main_bt.max_blocks; b += kClGatherThreads)
+                    s_bt[b] = __ldg(a.main_bt.table + (long long)r * a.main_bt.max_blocks + b);
+            if (gt < 8) {
+                const int lb = wlo / kBlockPositions + gt;
+                s_swb[gt] = (row_ok && lb <= m / kBlockPositions && lb < a.swa_bt.max_blocks)
+                                ? __ldg(a.swa_bt.table + (long long)r * a.swa_bt.max_blocks + lb)
+                                : -1;
+            }
+            named_bar_sync(1, kClGatherThreads);  // cached tables visible
+            finish_key(0, j0, id0);
+        }
         for (int i = 0; i < n_mine; ++i) {
             const int s = i & 1;
             if (i >= 2) ok = ok && mbar_wait_bounded(&pvdone[s], ((i - 2) >> 1) & 1, kWaitLimitNs);
@@ -703,7 +730,17 @@ __global__ void __launch_bounds__(kClThreads, 1)
         // the product of sub-tile i never waits behind a gather that has not arrived.
         const uint32_t idesc_s = idesc_bf16(kClKeys, 0, 64), idesc_o = idesc_bf16(NH, 1, 128);
         const uint64_t dq = sw128_desc(sQ, 16, 1024);
-        if (n_mine > 0) ok = mbar_wait_bounded(qfull, 0, kWaitLimitNs);
+        if (n_mine > 0) {
+            // the query rows, one 64-dim box per lane (off the gather warps: a single thread issues one box
+            // per several hundred cycles)
+            if (lane == 0) mbar_expect_tx(qfull, NH * kD * 2);
+            __syncwarp();
+            if (lane < kD / 64)
+                tma_load_2d(smem + L::kOffQ + lane * 8192, &qmap, lane * 64, row * a.heads + hg * NH, qfull);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qfull);
+            ok = mbar_wait_bounded(qfull, 0, kWaitLimitNs);
+        }
         auto issue_s = [&](int i) {
             const int s = i & 1;
             tc_fence_after();
