@@ -7,12 +7,10 @@
 // K and V are one stored row; [P2] 深潜 (Inverse RoPE): out = R_m^-1 sum_j p_j k_j; [P2] 融合点 2:
 // the inverse rotation is fused with the output store.
 //
-// Work split.  One CTA per (query row, group of HG heads, key split).  Keys are processed in chunks
-// of 64 rows gathered through the block tables into shared memory (double buffered, cp.async);
-// each chunk is used twice from the same tile: as K for S = Q K^T and as V for O += P V, both on
-// the tensor cores (bf16 mma, fp32 accumulation).  Softmax is online (base-2, fp32).  When a row's
-// keys are split over several CTAs, each writes an unnormalised partial (O, max, sum) and a
-// combine kernel merges them and applies the inverse rotation.
+// Work split: see attn_cl_kernel below (a cluster of CTAs per query row, 64-key sub-tiles, tcgen05 MMAs
+// with TMEM accumulators, on-chip merge).  When one cluster per row cannot fill the GPU, a row's keys are
+// split over several clusters; each writes an unnormalised partial (O, max, sum) and attn_combine_kernel
+// merges them and applies the inverse rotation.
 #include <algorithm>
 #include <mutex>
 
@@ -21,14 +19,10 @@
 namespace dsa {
 
 constexpr int kD = 512;
-constexpr int kChunk = 64;                    // keys per chunk
-constexpr int kRowStride = kD * 2 + 16;       // bf16 row + 16 B pad: conflict-free ldmatrix
-constexpr int kPStride = kChunk * 2 + 16;     // P tile row stride (bytes)
-constexpr int kThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct AttnArgs {
-    int rows, heads, hg_count, nsplit, cps;   // cps = chunks per split
+    int rows, heads, hg_count, nsplit, cps;   // cps = 64-key sub-tiles per split
     const uint16_t* q;
     const int32_t* q_pos;
     const int32_t* q_req;                     // NULL: row r belongs to request r
@@ -55,370 +49,8 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return (uint32_t)float_to_bf16(lo) | ((uint32_t)float_to_bf16(hi) << 16);
-}
-
-// Key j of a row: compressed slot j < n_comp, else window position.  Returns the physical row
-// (in the pool chosen by *use_swa), or -1 for a masked key; reports faults.
-__device__ __forceinline__ long long resolve_key(const AttnArgs& a, int row, int r, int m, int n_vis, int n_comp,
-                                                 int wlo, int j, bool* use_swa) {
-    if (j < n_comp) {
-        *use_swa = false;
-        int id = a.topk ? __ldg(a.topk + (long long)row * a.k + j) : j;
-        if (id < 0) return -1;
-        if (id >= n_vis) {
-            report(a.status, DSA_ERR_DEVICE_FAULT);
-            return -1;
-        }
-        long long p = physical_row(a.main_bt, r, id, a.main.rows_per_block, a.main.num_blocks);
-        if (p < 0) report(a.status, DSA_ERR_DEVICE_FAULT);
-        return p;
-    }
-    *use_swa = true;
-    const long long pos = (long long)wlo + (j - n_comp);
-    long long p = physical_row(a.swa_bt, r, pos, kBlockPositions, a.swa.num_blocks);
-    if (p < 0) report(a.status, DSA_ERR_DEVICE_FAULT);
-    return p;
-}
-
-template <int HG, bool FP8>
-struct AttnSmem {
-    static constexpr int kQ = HG * kRowStride;
-    static constexpr int kK = kChunk * kRowStride;              // one bf16 tile
-    static constexpr int kNumK = FP8 ? 1 : 2;                   // bf16 tiles
-    static constexpr int kK8 = FP8 ? kChunk * kD : 0;           // fp8 staging tile
-    static constexpr int kP = HG * kPStride;
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kQ;
-    static constexpr int kOffK8 = kOffK + kNumK * kK;
-    static constexpr int kOffP = kOffK8 + 2 * kK8;
-    static constexpr int kOffMeta = kOffP + kP;                 // long long rows[3][64]
-    static constexpr int kOffFlags = kOffMeta + 3 * kChunk * 8; // int8: 0 masked, 1 main, 2 swa
-    static constexpr int kOffScale = kOffFlags + 3 * kChunk;    // float[2][64]
-    static constexpr int kOffStats = kOffScale + 2 * kChunk * 4;// float rowmax[HG][8], rowsum[HG][8]
-    static constexpr int kOffML = kOffStats + 2 * HG * 8 * 4;   // float m[HG], l[HG]
-    static constexpr int kBytes = kOffML + 2 * HG * 4;
-};
-
-template <int HG, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
-    pdl_wait();
-    pdl_launch_dependents();
-    using L = AttnSmem<HG, FP8>;
-    constexpr int MT = HG / 16;        // 16-head m-tiles
-    constexpr int WPM = 8 / MT;        // warps per m-tile
-    constexpr int KW = kChunk / WPM;   // keys per warp in S = Q K^T
-    constexpr int NT = KW / 8;         // n-tiles per warp in S
-    constexpr int DW = kD / WPM;       // output dims per warp in O += P V
-    constexpr int ON = DW / 8;         // n-tiles per warp in O
-
-    extern __shared__ __align__(128) uint8_t smem[];
-    const uint32_t sbase = smem_u32(smem);
-    long long* meta_row = reinterpret_cast<long long*>(smem + L::kOffMeta);
-    int8_t* meta_flag = reinterpret_cast<int8_t*>(smem + L::kOffFlags);
-    float* key_scale = reinterpret_cast<float*>(smem + L::kOffScale);
-    float* row_max = reinterpret_cast<float*>(smem + L::kOffStats);
-    float* row_sum = row_max + HG * 8;
-    float* sm_m = reinterpret_cast<float*>(smem + L::kOffML);
-    float* sm_l = sm_m + HG;
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, t4 = lane & 3;
-    const int mt = warp / WPM, wk = warp % WPM;
-
-    const int split = blockIdx.x % a.nsplit;
-    const int hg = (blockIdx.x / a.nsplit) % a.hg_count;
-    const int row = blockIdx.x / (a.nsplit * a.hg_count);
-    const int r = a.q_req ? a.q_req[row] : row;
-    const int m = a.q_pos[row];
-    const bool row_ok = r >= 0 && r < a.main_bt.batch && r < a.swa_bt.batch && m >= 0;
-    if (!row_ok && tid == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
-    const int n_vis = row_ok ? entries_formed((long long)m + 1, a.kind_w, a.kind_s) : 0;
-    const int n_comp = a.topk ? a.k : n_vis;
-    const int wlo = max(0, m - a.window + 1);
-    const int n_keys = row_ok ? n_comp + (m - wlo + 1) : 0;
-    const int key_lo = split * a.cps * kChunk;
-    const int key_hi = min(n_keys, key_lo + a.cps * kChunk);
-    const int n_chunks = key_hi > key_lo ? (key_hi - key_lo + kChunk - 1) / kChunk : 0;
-
-    for (int i = tid; i < HG; i += kThreads) {
-        sm_m[i] = -INFINITY;
-        sm_l[i] = 0.f;
-    }
-    // key metadata of chunks 0 and 1
-    auto resolve_chunk = [&](int c, int jj) {
-        const int j = key_lo + c * kChunk + jj;
-        long long p = -1;
-        bool sw = false;
-        if (j < key_hi) p = resolve_key(a, row, r, m, n_vis, n_comp, wlo, j, &sw);
-        meta_row[(c % 3) * kChunk + jj] = p;
-        meta_flag[(c % 3) * kChunk + jj] = p < 0 ? 0 : (sw ? 2 : 1);
-    };
-    if (tid < kChunk) {
-        if (n_chunks > 0) resolve_chunk(0, tid);
-    } else if (tid < 2 * kChunk) {
-        if (n_chunks > 1) resolve_chunk(1, tid - kChunk);
-    }
-    __syncthreads();
-
-    const int row_bytes = FP8 ? kD : 2 * kD;
-    auto issue_chunk = [&](int c) {
-        // warp w gathers keys 8w .. 8w+7 of the chunk; each key row is one contiguous copy
-        const int mb = (c % 3) * kChunk;
-        const int buf = c & 1;
-        const uint32_t dst0 = FP8 ? sbase + L::kOffK8 + buf * L::kK8 : sbase + L::kOffK + buf * L::kK;
-        const int dst_stride = FP8 ? kD : kRowStride;
-        for (int kk = warp * 8; kk < warp * 8 + 8; ++kk) {
-            const int flag = meta_flag[mb + kk];
-            const long long prow = meta_row[mb + kk];
-            const uint8_t* base = flag == 2 ? static_cast<const uint8_t*>(a.swa.data)
-                                            : static_cast<const uint8_t*>(a.main.data);
-            const uint8_t* src = flag ? base + prow * row_bytes : base;
-            for (int piece = lane; piece < row_bytes / 16; piece += 32)
-                cp_async16(dst0 + kk * dst_stride + piece * 16, src + piece * 16, flag ? 16u : 0u);
-            if (FP8 && lane == 0)
-                key_scale[buf * kChunk + kk] =
-                    flag == 2 ? a.swa.scale[prow] : (flag == 1 ? a.main.scale[prow] : 0.f);
-        }
-    };
-    // Q rows of this head group
-    {
-        const uint16_t* qsrc = a.q + ((long long)row * a.heads + (long long)hg * HG) * kD;
-        for (int i = tid; i < HG * (kD / 8); i += kThreads) {
-            const int h = i / (kD / 8), piece = i % (kD / 8);
-            cp_async16(sbase + L::kOffQ + h * kRowStride + piece * 16, qsrc + (long long)h * kD + piece * 8,
-                       row_ok ? 16u : 0u);
-        }
-    }
-    if (n_chunks > 0) issue_chunk(0);
-    cp_async_commit();
-
-    float o[ON][4];
-#pragma unroll
-    for (int i = 0; i < ON; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-
-    const uint32_t sQ = sbase + L::kOffQ;
-    const uint32_t sP = sbase + L::kOffP;
-    for (int c = 0; c < n_chunks; ++c) {
-        cp_async_wait_all();
-        __syncthreads();
-        if (c + 1 < n_chunks) issue_chunk(c + 1);
-        cp_async_commit();
-        if (c + 2 < n_chunks && tid < kChunk) resolve_chunk(c + 2, tid);
-        const int buf = c & 1;
-        uint32_t sK;
-        if constexpr (FP8) {
-            // exact e4m3 -> bf16 conversion of the staged codes into the single bf16 tile
-            const uint8_t* src = smem + L::kOffK8 + buf * L::kK8;
-            uint8_t* dst = smem + L::kOffK;
-            for (int i = tid; i < kChunk * kD / 4; i += kThreads) {
-                const int kk = i / (kD / 4), e4 = (i % (kD / 4)) * 4;
-                const uint32_t cw = *reinterpret_cast<const uint32_t*>(src + kk * kD + e4);
-                uint2 v;
-                v.x = pack_bf16(e4m3_to_float(cw & 0xff), e4m3_to_float((cw >> 8) & 0xff));
-                v.y = pack_bf16(e4m3_to_float((cw >> 16) & 0xff), e4m3_to_float(cw >> 24));
-                *reinterpret_cast<uint2*>(dst + kk * kRowStride + e4 * 2) = v;
-            }
-            __syncthreads();
-            sK = sbase + L::kOffK;
-        } else {
-            sK = sbase + L::kOffK + buf * L::kK;
-        }
-        const int mb = (c % 3) * kChunk;
-
-        // ---- S = Q K^T for heads [16 mt, 16 mt + 16) x keys [KW wk, KW wk + KW) ----------
-        float s[NT][4];
-#pragma unroll
-        for (int i = 0; i < NT; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-        const uint32_t qa = sQ + (mt * 16 + (lane & 15)) * kRowStride + (lane >> 4) * 16;
-#pragma unroll 4
-        for (int ks = 0; ks < kD / 16; ++ks) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(qa + ks * 32, a0, a1, a2, a3);
-            if constexpr (NT == 1) {
-                uint32_t b0, b1;
-                const uint32_t kb = sK + (wk * KW + (lane & 7)) * kRowStride + ((lane >> 3) & 1) * 16 + ks * 32;
-                ldsm_x2(kb, b0, b1);
-                mma_bf16(s[0], a0, a1, a2, a3, b0, b1);
-            } else {
-#pragma unroll
-                for (int np = 0; np < NT / 2; ++np) {
-                    uint32_t b0, b1, b2, b3;
-                    const int key = wk * KW + np * 16 + (lane & 7) + ((lane >> 4) << 3);
-                    ldsm_x4(sK + key * kRowStride + ((lane >> 3) & 1) * 16 + ks * 32, b0, b1, b2, b3);
-                    mma_bf16(s[2 * np], a0, a1, a2, a3, b0, b1);
-                    mma_bf16(s[2 * np + 1], a0, a1, a2, a3, b2, b3);
-                }
-            }
-        }
-        // ---- scale, mask, chunk row max ----------------------------------------------------
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int key = wk * KW + nt * 8 + 2 * t4 + e;
-                float f = a.scale_log2;
-                if constexpr (FP8) f *= key_scale[buf * kChunk + key];
-                const bool valid = meta_flag[mb + key] != 0;
-                s[nt][e] = valid ? s[nt][e] * f : -INFINITY;
-                s[nt][2 + e] = valid ? s[nt][2 + e] * f : -INFINITY;
-                mx0 = fmaxf(mx0, s[nt][e]);
-                mx1 = fmaxf(mx1, s[nt][2 + e]);
-            }
-        }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const int h0 = mt * 16 + g, h1 = h0 + 8;
-        if (t4 == 0) {
-            row_max[h0 * 8 + wk] = mx0;
-            row_max[h1 * 8 + wk] = mx1;
-        }
-        __syncthreads();
-        float cm0 = -INFINITY, cm1 = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < WPM; ++i) {
-            cm0 = fmaxf(cm0, row_max[h0 * 8 + i]);
-            cm1 = fmaxf(cm1, row_max[h1 * 8 + i]);
-        }
-        const float mo0 = sm_m[h0], mo1 = sm_m[h1];
-        const float mn0 = fmaxf(mo0, cm0), mn1 = fmaxf(mo1, cm1);
-        // ---- P = exp2(S - m_new), row sums, P (times the fp8 row scale) to shared memory ----
-        float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int key = wk * KW + nt * 8 + 2 * t4;
-            float p0 = mn0 == -INFINITY ? 0.f : exp2f(s[nt][0] - mn0);
-            float p1 = mn0 == -INFINITY ? 0.f : exp2f(s[nt][1] - mn0);
-            float p2 = mn1 == -INFINITY ? 0.f : exp2f(s[nt][2] - mn1);
-            float p3 = mn1 == -INFINITY ? 0.f : exp2f(s[nt][3] - mn1);
-            ps0 += p0 + p1;
-            ps1 += p2 + p3;
-            if constexpr (FP8) {
-                const float k0 = key_scale[buf * kChunk + key], k1 = key_scale[buf * kChunk + key + 1];
-                p0 *= k0; p1 *= k1; p2 *= k0; p3 *= k1;
-            }
-            *reinterpret_cast<uint32_t*>(smem + L::kOffP + h0 * kPStride + key * 2) = pack_bf16(p0, p1);
-            *reinterpret_cast<uint32_t*>(smem + L::kOffP + h1 * kPStride + key * 2) = pack_bf16(p2, p3);
-        }
-        ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
-        ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
-        ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
-        ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
-        if (t4 == 0) {
-            row_sum[h0 * 8 + wk] = ps0;
-            row_sum[h1 * 8 + wk] = ps1;
-        }
-        __syncthreads();
-        float cs0 = 0.f, cs1 = 0.f;
-#pragma unroll
-        for (int i = 0; i < WPM; ++i) {
-            cs0 += row_sum[h0 * 8 + i];
-            cs1 += row_sum[h1 * 8 + i];
-        }
-        const float al0 = mo0 == -INFINITY ? 0.f : exp2f(mo0 - mn0);
-        const float al1 = mo1 == -INFINITY ? 0.f : exp2f(mo1 - mn1);
-        if (wk == 0 && t4 == 0) {
-            sm_m[h0] = mn0;
-            sm_m[h1] = mn1;
-            sm_l[h0] = sm_l[h0] * al0 + cs0;
-            sm_l[h1] = sm_l[h1] * al1 + cs1;
-        }
-#pragma unroll
-        for (int i = 0; i < ON; ++i) {
-            o[i][0] *= al0;
-            o[i][1] *= al0;
-            o[i][2] *= al1;
-            o[i][3] *= al1;
-        }
-        // ---- O += P V, dims [DW wk, DW wk + DW) -------------------------------------------
-        const uint32_t pa = sP + (mt * 16 + (lane & 15)) * kPStride + (lane >> 4) * 16;
-#pragma unroll
-        for (int ks = 0; ks < kChunk / 16; ++ks) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(pa + ks * 32, a0, a1, a2, a3);
-            const uint32_t vb = sK + (ks * 16 + (lane & 15)) * kRowStride + (lane >> 4) * 16 + wk * DW * 2;
-#pragma unroll
-            for (int np = 0; np < ON / 2; ++np) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vb + np * 32, b0, b1, b2, b3);
-                mma_bf16(o[2 * np], a0, a1, a2, a3, b0, b1);
-                mma_bf16(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
-            }
-        }
-    }
-    __syncthreads();
-
-    // ---- epilogue ----------------------------------------------------------------------------
-    const int h0 = mt * 16 + g, h1 = h0 + 8;
-    const float m0 = sm_m[h0], m1 = sm_m[h1], l0 = sm_l[h0], l1 = sm_l[h1];
-    const int head0 = hg * HG + h0, head1 = hg * HG + h1;
-    if (a.nsplit == 1) {
-        const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
-        uint16_t* out0 = a.out + ((long long)row * a.heads + head0) * kD;
-        uint16_t* out1 = a.out + ((long long)row * a.heads + head1) * kD;
-        const int first = kD - a.rope.rope_dim;
-#pragma unroll
-        for (int nt = 0; nt < ON; ++nt) {
-            const int col = wk * DW + nt * 8 + 2 * t4;
-            float x0 = o[nt][0] * i0, x1 = o[nt][1] * i0, y0 = o[nt][2] * i1, y1 = o[nt][3] * i1;
-            if (col >= first) {
-                float cs, sn;
-                rope_cos_sin(m, a.rope.inv_freq[(col - first) >> 1], &cs, &sn);
-                // R_m^-1: rotation by -angle
-                const float u0 = x0 * cs + x1 * sn, u1 = -x0 * sn + x1 * cs;
-                const float v0 = y0 * cs + y1 * sn, v1 = -y0 * sn + y1 * cs;
-                x0 = u0; x1 = u1; y0 = v0; y1 = v1;
-            }
-            *reinterpret_cast<uint32_t*>(out0 + col) = pack_bf16(x0, x1);
-            *reinterpret_cast<uint32_t*>(out1 + col) = pack_bf16(y0, y1);
-        }
-        if (a.lse && wk == 0 && t4 == 0) {
-            a.lse[(long long)row * a.heads + head0] = l0 > 0.f ? (m0 + log2f(l0)) / kLog2e : -INFINITY;
-            a.lse[(long long)row * a.heads + head1] = l1 > 0.f ? (m1 + log2f(l1)) / kLog2e : -INFINITY;
-        }
-    } else {
-        const long long base0 = ((long long)row * a.nsplit + split) * a.heads;
-        float* wo0 = a.ws_o + (base0 + head0) * kD;
-        float* wo1 = a.ws_o + (base0 + head1) * kD;
-#pragma unroll
-        for (int nt = 0; nt < ON; ++nt) {
-            const int col = wk * DW + nt * 8 + 2 * t4;
-            *reinterpret_cast<float2*>(wo0 + col) = make_float2(o[nt][0], o[nt][1]);
-            *reinterpret_cast<float2*>(wo1 + col) = make_float2(o[nt][2], o[nt][3]);
-        }
-        if (wk == 0 && t4 == 0) {
-            a.ws_ml[(base0 + head0) * 2 + 0] = m0;
-            a.ws_ml[(base0 + head0) * 2 + 1] = l0;
-            a.ws_ml[(base0 + head1) * 2 + 0] = m1;
-            a.ws_ml[(base0 + head1) * 2 + 1] = l1;
-        }
-    }
 }
 
 // Merge split partials of one (row, head): 128 threads x 4 dims; inverse RoPE; bf16 store.
@@ -516,7 +148,8 @@ struct ClSmem {
     static constexpr int kOffP = kOffK + 2 * kClStage;              // two P^T buffers; output staging at the end
     static constexpr int kOffRow = kOffP + 2 * kP;                  // int [ring][64]: physical rows (-1 masked)
     static constexpr int kOffPool = kOffRow + kClRing * kClKeys * 4;  // uint8 [ring][64]: 1 main, 2 window
-    static constexpr int kOffMask = kOffPool + kClRing * kClKeys;   // uint32 [2][2]: valid keys of a stage
+    static constexpr int kOffKsc = kOffPool + kClRing * kClKeys;    // float [2][64]: e4m3 row scales of a stage
+    static constexpr int kOffMask = kOffKsc + 2 * kClKeys * 4;      // uint32 [2][2]: valid keys of a stage
     static constexpr int kOffAlpha = kOffMask + 16;                 // float [2][NH]
     static constexpr int kOffVote = kOffAlpha + 2 * NH * 4;         // int [2][4]
     static constexpr int kOffOwn = kOffVote + 32;                   // float m[NH], l[NH] of this CTA
@@ -527,6 +160,7 @@ struct ClSmem {
     static constexpr int kOffBar = kOffSwb + 32;                    // 10 mbarriers, TMEM address
     static constexpr int kBytes = kOffBar + 10 * 8 + 16;
     static constexpr int kAlloc = kBytes + 1024;                    // + alignment slack
+    static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
     static constexpr int kTile = 128 * NH * 4;                      // one 128-dim O tile, fp32 [NH / 4][128] float4
     static_assert(6 * kTile <= kQ + 2 * kClStage, "sent and received tiles must fit in the query rows and stages");
     static_assert(NH * 128 * 2 <= 2 * kP, "an output tile must fit in the P^T buffers");
@@ -544,7 +178,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int e, int chunk_stride)
 // Keys of a row for the tensor-core kernel: [0, n_comp) compressed slots, [n_comp, ncp) padding up to a
 // multiple of 4, [ncp, ncp + window count) window positions.
 
-template <int NH>
+template <int NH, bool FP8>
 __global__ void __launch_bounds__(kClThreads, 1)
     attn_cl_kernel(const __grid_constant__ CUtensorMap qmap, AttnArgs a) {
     using L = ClSmem<NH>;
@@ -553,6 +187,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const uint32_t sQ = smem_u32(smem + L::kOffQ), sK = smem_u32(smem + L::kOffK), sP = smem_u32(smem + L::kOffP);
     int* s_row = reinterpret_cast<int*>(smem + L::kOffRow);
     uint8_t* s_pool = smem + L::kOffPool;
+    float* s_ksc = reinterpret_cast<float*>(smem + L::kOffKsc);
     uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + L::kOffMask);
     float* s_alpha = reinterpret_cast<float*>(smem + L::kOffAlpha);
     int* s_vote = reinterpret_cast<int*>(smem + L::kOffVote);
@@ -664,9 +299,10 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 else v = pb * kBlockPositions + (pos - lb * kBlockPositions);
             }
             if (v >= 0 && R > 0) {  // rows of later rounds start moving into L2 (the first round is gathered at once)
+                constexpr int kRowBytes = FP8 ? kD : 2 * kD;
                 const uint8_t* base = pool == 2 ? static_cast<const uint8_t*>(a.swa.data)
                                                 : static_cast<const uint8_t*>(a.main.data);
-                prefetch_l2(base + (long long)v * (2 * kD), 2 * kD);
+                prefetch_l2(base + (long long)v * kRowBytes, kRowBytes);
             }
             s_row[(i % kClRing) * kClKeys + (gt & 63)] = v;
             s_pool[(i % kClRing) * kClKeys + (gt & 63)] = (uint8_t)pool;
@@ -701,7 +337,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 const uint32_t bits = __ballot_sync(0xffffffffu, rows[gt] >= 0);
                 if (lane == 0) s_mask[s * 2 + gw] = bits;
             }
-            if (ok) {
+            if (ok && !FP8) {
                 const uint32_t stage = sK + s * kClStage;
 #pragma unroll 1
                 for (int kk = gw; kk < kClKeys; kk += kClGatherWarps) {
@@ -715,7 +351,70 @@ __global__ void __launch_bounds__(kClThreads, 1)
                                    rr >= 0 ? 16u : 0u);
                 }
             }
+            if (ok && FP8) {
+                // e4m3 rows: lane l holds codes of dims 16 l .. 16 l + 15 (one 16-byte load per row); every
+                // row of this warp is loaded first, then the codes become bf16 (exactly: e4m3 -> fp16 -> fp32 ->
+                // bf16 loses nothing) in the swizzled stage; the row scale goes beside the stage
+                constexpr int kRowsPerWarp = (kClKeys + kClGatherWarps - 1) / kClGatherWarps;
+                const uint32_t stage = sK + s * kClStage;
+                uint4 code[kRowsPerWarp];
+                float ksc = 0.f;
+#pragma unroll
+                for (int u = 0; u < kRowsPerWarp; ++u) {
+                    const int kk = gw + u * kClGatherWarps;
+                    code[u] = make_uint4(0, 0, 0, 0);
+                    if (kk < kClKeys) {
+                        const int rr = rows[kk];
+                        const dsa_pool_t& pl = pools[kk] == 2 ? a.swa : a.main;
+                        if (rr >= 0) {
+                            code[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(pl.data) +
+                                                                           (long long)rr * kD) + lane);
+                            if (lane == u) ksc = __ldg(pl.scale + rr);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kRowsPerWarp; ++u) {
+                    const int kk = gw + u * kClGatherWarps;
+                    if (kk < kClKeys) {
+                        const uint32_t w4[4] = {code[u].x, code[u].y, code[u].z, code[u].w};
+                        uint32_t bf[8];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                            for (int hlf = 0; hlf < 2; ++hlf) {
+                                const __half2_raw h2 =
+                                    __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[q] >> (16 * hlf)), __NV_E4M3);
+                                const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+                                bf[2 * q + hlf] = pack_bf16(f2.x, f2.y);
+                            }
+                        }
+                        const int d0 = 16 * lane;
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + sw128_offset(kk, d0, kClKeys * 128)),
+                                     "r"(bf[0]), "r"(bf[1]), "r"(bf[2]), "r"(bf[3])
+                                     : "memory");
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + sw128_offset(kk, d0 + 8, kClKeys * 128)),
+                                     "r"(bf[4]), "r"(bf[5]), "r"(bf[6]), "r"(bf[7])
+                                     : "memory");
+                        if (lane == u) s_ksc[s * kClKeys + kk] = rows[kk] >= 0 ? ksc : 0.f;
+                    }
+                }
+            }
             cp_async_commit();
+            if (i == 0) {  // the first round's later sub-tiles start moving into L2 once sub-tile 0 is under way
+                constexpr int kRowBytes = FP8 ? kD : 2 * kD;
+                for (int t = kClKeys + gt; t < kClRound * kClKeys; t += kClGatherThreads) {
+                    const int ii = t / kClKeys;
+                    if (ii >= n_mine) break;
+                    const int rr = s_row[(ii % kClRing) * kClKeys + (t % kClKeys)];
+                    if (rr >= 0) {
+                        const uint8_t* base = s_pool[(ii % kClRing) * kClKeys + (t % kClKeys)] == 2
+                                                  ? static_cast<const uint8_t*>(a.swa.data)
+                                                  : static_cast<const uint8_t*>(a.main.data);
+                        prefetch_l2(base + (long long)rr * kRowBytes, kRowBytes);
+                    }
+                }
+            }
             // the next round of keys once this one's second sub-tile is under way: its rows reach L2 while
             // the sub-tiles in between are processed (ring slots of sub-tiles < i are free by now)
             if (i % kClRound == 2) resolve_round(i / kClRound + 1);
@@ -812,7 +511,8 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 float mx = -INFINITY;
 #pragma unroll
                 for (int j = 0; j < kClKeys; ++j) {
-                    sv[j] = ((vm >> j) & 1) ? sv[j] * a.scale_log2 : -INFINITY;
+                    const float ls = FP8 ? a.scale_log2 * s_ksc[s * kClKeys + j] : a.scale_log2;  // e4m3: times the row scale
+                    sv[j] = ((vm >> j) & 1) ? sv[j] * ls : -INFINITY;
                     mx = fmaxf(mx, sv[j]);
                 }
                 if (mx > m_run + kLazyLog2) {  // also the first finite maximum (m_run = -inf)
@@ -828,10 +528,16 @@ __global__ void __launch_bounds__(kClThreads, 1)
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const uint16_t b0 = float_to_bf16(exp2f(sv[8 * c + 2 * e] - mr));
-                        const uint16_t b1 = float_to_bf16(exp2f(sv[8 * c + 2 * e + 1] - mr));
-                        sum += bf16_to_float(b0) + bf16_to_float(b1);
-                        w[e] = (uint32_t)b0 | ((uint32_t)b1 << 16);
+                        if constexpr (FP8) {  // the probability that multiplies the codes carries the row scale
+                            const float p0 = exp2f(sv[8 * c + 2 * e] - mr), p1 = exp2f(sv[8 * c + 2 * e + 1] - mr);
+                            sum += p0 + p1;
+                            w[e] = pack_bf16(p0 * s_ksc[s * kClKeys + 8 * c + 2 * e], p1 * s_ksc[s * kClKeys + 8 * c + 2 * e + 1]);
+                        } else {
+                            const uint16_t b0 = float_to_bf16(exp2f(sv[8 * c + 2 * e] - mr));
+                            const uint16_t b1 = float_to_bf16(exp2f(sv[8 * c + 2 * e + 1] - mr));
+                            sum += bf16_to_float(b0) + bf16_to_float(b1);
+                            w[e] = (uint32_t)b0 | ((uint32_t)b1 << 16);
+                        }
                     }
                     if (hthread)
                         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((c ^ (h & 7)) << 4)),
@@ -1054,21 +760,6 @@ struct SplitPlan {
     int hg, hg_count, nsplit, cps, cl;
 };
 
-static SplitPlan plan_splits(int rows, int heads, int max_keys, int chunk) {
-    SplitPlan p;
-    p.hg = heads >= 64 ? 64 : heads;
-    p.hg_count = heads / p.hg;
-    p.cl = 1;
-    const int n_chunks = max(1, (max_keys + chunk - 1) / chunk);
-    const long long units = (long long)rows * p.hg_count;
-    const int sms = sm_count();
-    int ns = units >= sms ? 1 : (int)(sms / units);
-    ns = max(1, min(ns, n_chunks));
-    p.cps = (n_chunks + ns - 1) / ns;
-    p.nsplit = (n_chunks + p.cps - 1) / p.cps;
-    return p;
-}
-
 static SplitPlan plan_cluster(int rows, int heads, int max_keys) {
     SplitPlan p;
     p.hg = heads >= 64 ? 64 : heads;
@@ -1087,7 +778,8 @@ static SplitPlan plan_cluster(int rows, int heads, int max_keys) {
 }
 
 static SplitPlan plan_for(int rows, int heads, int max_keys, int dtype) {
-    return dtype == DSA_BF16 ? plan_cluster(rows, heads, max_keys) : plan_splits(rows, heads, max_keys, kChunk);
+    (void)dtype;  // both row formats run on the cluster kernel
+    return plan_cluster(rows, heads, max_keys);
 }
 
 // Workspace: split partials [rows][nsplit][heads][512] + (m, l) [rows][nsplit][heads][2] when a row's keys
@@ -1116,30 +808,17 @@ static bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t rows, int
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NH>
+template <int NH, bool FP8>
 static dsa_status_t launch_attn_cl(const AttnArgs& a, int cl, cudaStream_t st) {
     using L = ClSmem<NH>;
     CUtensorMap qmap;
     if (!make_bf16_map(&qmap, a.q, (uint64_t)a.rows * a.heads, NH)) return DSA_ERR_CUDA;
-    if (cudaFuncSetAttribute(attn_cl_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
+    if (cudaFuncSetAttribute(attn_cl_kernel<NH, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
         cudaSuccess)
         return DSA_ERR_CUDA;
     const long long grid = (long long)a.rows * a.hg_count * a.nsplit * cl;
-    cudaError_t e = launch_pdl_cluster(attn_cl_kernel<NH>, dim3((unsigned)grid), dim3(kClThreads), L::kAlloc, st, cl,
+    cudaError_t e = launch_pdl_cluster(attn_cl_kernel<NH, FP8>, dim3((unsigned)grid), dim3(kClThreads), L::kAlloc, st, cl,
                                        qmap, a);
-    if (e == cudaSuccess && a.nsplit > 1)
-        e = launch_pdl(attn_combine_kernel, dim3(a.rows * a.heads), dim3(128), 0, st, a);
-    if (e != cudaSuccess) return DSA_ERR_CUDA;
-    return launch_status();
-}
-
-template <int HG, bool FP8>
-static dsa_status_t launch_attn(const AttnArgs& a, cudaStream_t st) {
-    using L = AttnSmem<HG, FP8>;
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HG, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
-    if (e != cudaSuccess) return DSA_ERR_CUDA;
-    const long long grid = (long long)a.rows * a.hg_count * a.nsplit;
-    e = launch_pdl(attn_kernel<HG, FP8>, dim3((unsigned)grid), dim3(kThreads), L::kBytes, st, a);
     if (e == cudaSuccess && a.nsplit > 1)
         e = launch_pdl(attn_combine_kernel, dim3(a.rows * a.heads), dim3(128), 0, st, a);
     if (e != cudaSuccess) return DSA_ERR_CUDA;
@@ -1208,15 +887,15 @@ static dsa_status_t sparse_attn(int32_t rows, int32_t heads, const void* q, cons
     const bool fp8 = main->dtype == DSA_FP8_E4M3;
     if (!fp8) {
         switch (p.hg) {
-            case 16: return launch_attn_cl<16>(a, p.cl, st);
-            case 32: return launch_attn_cl<32>(a, p.cl, st);
-            default: return launch_attn_cl<64>(a, p.cl, st);
+            case 16: return launch_attn_cl<16, false>(a, p.cl, st);
+            case 32: return launch_attn_cl<32, false>(a, p.cl, st);
+            default: return launch_attn_cl<64, false>(a, p.cl, st);
         }
     }
     switch (p.hg) {
-        case 16: return fp8 ? launch_attn<16, true>(a, st) : launch_attn<16, false>(a, st);
-        case 32: return fp8 ? launch_attn<32, true>(a, st) : launch_attn<32, false>(a, st);
-        default: return fp8 ? launch_attn<64, true>(a, st) : launch_attn<64, false>(a, st);
+        case 16: return launch_attn_cl<16, true>(a, p.cl, st);
+        case 32: return launch_attn_cl<32, true>(a, p.cl, st);
+        default: return launch_attn_cl<64, true>(a, p.cl, st);
     }
 }
 
