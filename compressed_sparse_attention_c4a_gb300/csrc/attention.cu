@@ -161,7 +161,7 @@ struct ClSmem {
     static constexpr int kBytes = kOffBar + 10 * 8 + 16;
     static constexpr int kAlloc = kBytes + 1024;                    // + alignment slack
     static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
-    static constexpr int kTile = 128 * NH * 4;                      // one 128-dim O tile, fp32 [NH / 4][128] float4
+    static constexpr int kTile = 128 * NH * 2;                      // one exchanged 128-dim O tile: [NH / 4][128] x 4 bf16
     static_assert(6 * kTile <= kQ + 2 * kClStage, "sent and received tiles must fit in the query rows and stages");
     static_assert(NH * 128 * 2 <= 2 * kP, "an output tile must fit in the P^T buffers");
     static constexpr int kTmemCols = 128 + 4 * NH <= 256 ? 256 : 512;
@@ -640,7 +640,8 @@ __global__ void __launch_bounds__(kClThreads, 1)
         inv[e] = b4.x, inv[e + 1] = b4.y, inv[e + 2] = b4.z, inv[e + 3] = b4.w;
     }
     // tiles this CTA sends sit at [0, 3 tiles) of shared memory, the tiles it receives at [3, 6 tiles)
-    // (query rows and key stages, idle now); each as [NH / 4 head quads][128 dims] float4
+    // (query rows and key stages, idle now); each as [NH / 4 head quads][128 dims] x 4 bf16, already scaled
+    // to the cluster maximum (the owner's own tile stays fp32 in TMEM)
     uint8_t* xout = smem + L::kOffQ;
     uint8_t* xin = smem + L::kOffQ + 3 * L::kTile;
     if (csize > 1) {
@@ -658,24 +659,24 @@ __global__ void __launch_bounds__(kClThreads, 1)
             if (t % csize == crank) continue;
 #pragma unroll
             for (int q4 = 0; q4 < G / 4; ++q4)
-                *reinterpret_cast<float4*>(xout + sl * L::kTile + ((h0 / 4 + q4) * 128 + d) * 16) =
-                    have ? make_float4(v[t][4 * q4] * f[4 * q4], v[t][4 * q4 + 1] * f[4 * q4 + 1],
-                                       v[t][4 * q4 + 2] * f[4 * q4 + 2], v[t][4 * q4 + 3] * f[4 * q4 + 3])
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<uint2*>(xout + sl * L::kTile + ((h0 / 4 + q4) * 128 + d) * 8) =
+                    have ? make_uint2(pack_bf16(v[t][4 * q4] * f[4 * q4], v[t][4 * q4 + 1] * f[4 * q4 + 1]),
+                                      pack_bf16(v[t][4 * q4 + 2] * f[4 * q4 + 2], v[t][4 * q4 + 3] * f[4 * q4 + 3]))
+                         : make_uint2(0u, 0u);
             ++sl;
         }
         fence_proxy_async_smem();  // staged tiles -> async proxy (the bulk copies)
         __syncthreads();
-        if (tid == 0) {
-            int sl2 = 0;
-            for (int t = 0; t < 4; ++t) {
-                const int o = t % csize;
-                if (o == crank) continue;
-                const int slot = (crank - (crank > o ? 1 : 0)) * tiles_per + t / csize;  // in the owner's xin
-                bulk_s2cluster(mapa_shared(smem_u32(xin + slot * L::kTile), (uint32_t)o),
-                               smem_u32(xout + sl2 * L::kTile), L::kTile, mapa_shared(smem_u32(xfull), (uint32_t)o));
-                ++sl2;
-            }
+        // one push per sent tile, each from lane 0 of a different warp (one thread issues a bulk copy only
+        // every several hundred cycles)
+        if (lane == 0 && warp < 4 - tiles_per) {
+            int t = 0, seen = -1;
+            for (; t < 4; ++t)
+                if (t % csize != crank && ++seen == warp) break;
+            const int o = t % csize;
+            const int slot = (crank - (crank > o ? 1 : 0)) * tiles_per + t / csize;  // in the owner's xin
+            bulk_s2cluster(mapa_shared(smem_u32(xin + slot * L::kTile), (uint32_t)o),
+                           smem_u32(xout + warp * L::kTile), L::kTile, mapa_shared(smem_u32(xfull), (uint32_t)o));
         }
         ok = mbar_wait_bounded(xfull, 0, kWaitLimitNs);
         if (!ok && tid == 0) report(a.status, DSA_ERR_TIMEOUT);
@@ -701,11 +702,11 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 const uint8_t* src = xin + (si * tiles_per + j) * L::kTile;
 #pragma unroll
                 for (int q4 = 0; q4 < G / 4; ++q4) {
-                    const float4 w = *reinterpret_cast<const float4*>(src + ((h0 / 4 + q4) * 128 + d) * 16);
-                    v[4 * q4] += w.x;
-                    v[4 * q4 + 1] += w.y;
-                    v[4 * q4 + 2] += w.z;
-                    v[4 * q4 + 3] += w.w;
+                    const uint2 w = *reinterpret_cast<const uint2*>(src + ((h0 / 4 + q4) * 128 + d) * 8);
+                    v[4 * q4] += bf16_to_float((uint16_t)(w.x & 0xFFFFu));
+                    v[4 * q4 + 1] += bf16_to_float((uint16_t)(w.x >> 16));
+                    v[4 * q4 + 2] += bf16_to_float((uint16_t)(w.y & 0xFFFFu));
+                    v[4 * q4 + 3] += bf16_to_float((uint16_t)(w.y >> 16));
                 }
             }
         }

@@ -159,6 +159,8 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
         const long long i = i_lo + item;
         if (i > i_hi) return;
         const long long base = (long long)s * i;
+        // the destination row first: its block-table load is in flight with the logits and rows below
+        const long long prow = physical_row(a.out_bt, r, i, a.out.rows_per_block, a.out.num_blocks);
         auto logit_at = [&](long long p) -> float {
             return p < start ? a.state_logit[(long long)slot * w + (p % w)] : a.logit_new[cu0 + (p - start)];
         };
@@ -213,7 +215,6 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
         for (int k = 0; k < E; ++k) acc[k] *= rs * (a.gamma ? a.gamma[lane * E + k] : 1.f);
         // RoPE at the last covered position
         rope_row<E>(acc, lane, DIM, a.rope, base + w - 1);
-        const long long prow = physical_row(a.out_bt, r, i, a.out.rows_per_block, a.out.num_blocks);
         if (prow < 0) {
             if (lane == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
             return;
@@ -227,10 +228,10 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
     const long long p = start + j;
     const uint16_t* xrow = a.x_new + (long long)(cu0 + j) * DIM;
     if (a.has_swa) {
+        const long long prow = physical_row(a.swa_bt, r, p, kBlockPositions, a.swa.num_blocks);  // with the row load
         float v[E];
         load_bf16<E>(xrow, lane, v);
         rope_row<E>(v, lane, DIM, a.rope, p);
-        const long long prow = physical_row(a.swa_bt, r, p, kBlockPositions, a.swa.num_blocks);
         if (prow < 0) {
             if (lane == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
         } else {
