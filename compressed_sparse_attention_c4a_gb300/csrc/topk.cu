@@ -35,8 +35,10 @@ constexpr int kBins = 2048;
 constexpr int kQuarterMax = 40960;  // scores per CTA kept in shared memory (rows up to 163,840 with C = 4)
 constexpr int kRankMax = 256;       // bucket sizes (cluster-wide) resolved by direct ranking
 
+// Monotone 32-bit key of a score; -0 and +0 compare equal as floats, so they share one key.
 __device__ __forceinline__ uint32_t order_key(float f) {
     uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u) u = 0u;
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 

@@ -287,3 +287,23 @@ def test_topk_edge_cases_exact(ld):
     got = out.cpu().numpy()
     for i, (r, n) in enumerate(zip(rows, nv)):
         assert list(got[i]) == list(OL.topk(r.astype(np.float64), n, k)), i
+
+
+def test_topk_many_rows_exact():
+    """Many rows of random length: random scores, and rows of heavy ties that mix -0 and +0 (equal
+    scores: the lower index wins), against the oracle's top-k index for index."""
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    rng = np.random.default_rng(77)
+    nq, ld, k = 700, 4096, 512
+    scores = rng.standard_normal((nq, ld)).astype(np.float32)
+    scores[::7] = np.round(scores[::7] * 2)                      # heavy ties on every 7th row
+    nv = rng.integers(0, ld + 1, nq).astype(np.int32)
+    nv[::5] = ld
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty((nq, k), dtype=torch.int32, device="cuda")
+    dsa.dsa_topk(torch.from_numpy(scores).cuda(), torch.from_numpy(nv).cuda(), k, out, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = out.cpu().numpy()
+    for i in range(nq):
+        assert list(got[i]) == list(OL.topk(scores[i].astype(np.float64), int(nv[i]), k)), i
