@@ -189,6 +189,8 @@ SHARP = {
                        new=[1] * 48, seed=18),
     # dense over c128a entries, a long key list per CTA
     "c128a_decode": CASES["c128a_decode"],
+    # 128 query heads: two 64-head groups per row, each its own cluster
+    "c4a_decode_128h": S("c4a_decode_128h", cached=[1500, 3071], new=[1, 1], heads=128, seed=19),
 }
 
 
