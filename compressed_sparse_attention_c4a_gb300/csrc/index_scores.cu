@@ -10,9 +10,9 @@
 // swizzle) into a stage; the group's query codes, head weights and query scales go into one of two
 // group buffers only when the group changes (a CTA's items are consecutive tiles of few groups).  One
 // thread issues tcgen05.mma.kind::f8f6f4 (M = 128, N, K = 32 per instruction, fp32 accumulation in
-// TMEM); four warps read their 32 TMEM lanes (one entry each), load the entry's key scale and apply
-// it, ReLU, the per-head weights and the causal mask, writing coalesced score rows.  Every wait is
-// bounded.
+// TMEM); the epilogue warps read their 32 TMEM lanes (one entry each) over a slice of the columns, apply
+// the entry's key scale, ReLU, the per-head weights (folded with the query scales once per group) and
+// the causal mask, writing coalesced score rows.  Every wait is bounded.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -21,7 +21,18 @@
 
 namespace dsa {
 
-constexpr int kIdxThreads = 192;  // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
+// warp 0: TMA producer, warp 1: MMA issuer, then EW epilogue warps: 4 for narrow groups (N <= 128, two
+// tiles per item, two CTAs per SM), 12 for wide ones (N up to 256, one tile per item, one CTA per SM), so
+// that the epilogue keeps pace with the tensor cores.  Epilogue warp w reads TMEM lanes 32 * (w % 4) ..
+// + 31 (the quadrant its warp id allows) and column slice (w - 2) / 4 of EW / 4 slices.  Registers: a
+// sub-partition holds 16K of them and at most 3 (narrow, two CTAs) or 4 (wide) of the CTA's warps.
+template <int TPI>
+__host__ __device__ constexpr int epi_warps() { return TPI == 2 ? 4 : 12; }
+template <int TPI>
+__host__ __device__ constexpr int idx_threads() { return 64 + 32 * epi_warps<TPI>(); }
+// columns of one epilogue slice, at most: 16-column chunks of N split over EW / 4 slices
+template <int TPI>
+__host__ __device__ constexpr int slice_cols() { return TPI == 2 ? 128 : 96; }
 constexpr int kTileEntries = 128;
 constexpr int kPage = 64;         // c4a entries per 256-position block
 constexpr int kChunkItems = 32;   // items resolved together (one per producer lane)
@@ -137,8 +148,9 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 
 // Per-stage layout (bytes from the stage start): key tiles [TPI][128][DIM] (swizzled), StageMeta, fp32
 // entry scales [TPI * 128] (cp.async, 16 bytes per producer lane and tile, completing on the stage's
-// barrier).  Group
-// buffer: query tile [n_cols][DIM] (swizzled), head weights [n_cols], query scales [n_cols].  Only the producer walks the work list; it describes each item in its
+// barrier).  Group buffer: query tile [n_cols][DIM] (swizzled), head weights [n_cols], query scales
+// [n_cols], visible entries of each query of the group [64] (written by the producer lanes before the
+// buffer's barrier is armed).  Only the producer walks the work list; it describes each item in its
 // stage (or posts a terminal stage), so the MMA and epilogue roles never touch global metadata.  The
 // epilogue releases the stage, so everything it reads stays in shared memory until it is done.
 struct StageMeta {
@@ -148,22 +160,32 @@ struct StageMeta {
     int nq;        // queries in the group
     int q0;        // first query of the group
     int e0;        // first entry of the tile
-    int nvis[64];  // visible entries per query of the group
 };
 
 __host__ __device__ constexpr int meta_bytes() { return ((int)sizeof(StageMeta) + 15) / 16 * 16; }
 
+template <bool B>
+struct BoolTag {
+    static constexpr bool value = B;
+};
+
+__host__ __device__ constexpr int gbuf_nvis_offset(int n_cols, int dim) { return n_cols * dim + 2 * n_cols * 4; }
+
 template <int DIM, int HEADS, int TPI>
-__global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constant__ CUtensorMap kmap,
+__global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_constant__ CUtensorMap kmap,
                                                             const __grid_constant__ CUtensorMap qmap, IdxArgs a) {
     constexpr int kItem = TPI * kTileEntries;  // entries per item
     constexpr int kPages = 2 * TPI;
+    constexpr int EW = epi_warps<TPI>(), NSL = EW / 4, kSlice = slice_cols<TPI>();
+    constexpr int kThreads = idx_threads<TPI>();
+    constexpr int kBatch = TPI == 2 ? 4 : 2;  // 16-column TMEM loads in flight per wait (register budget)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = a.stages, NA = a.n_acc;
     const int tiles_bytes = kItem * DIM;
     uint8_t* gbase = smem + (size_t)S * a.stage_bytes;  // two group buffers
-    uint64_t* full = reinterpret_cast<uint64_t*>(gbase + 2 * a.gbuf_bytes);
+    float* s_fold = reinterpret_cast<float*>(gbase + 2 * a.gbuf_bytes);  // [EW][kSlice]: each epilogue warp's w_h * sq_h
+    uint64_t* full = reinterpret_cast<uint64_t*>(s_fold + EW * kSlice);
     uint64_t* empty = full + S;
     uint64_t* tfull = empty + S;   // [NA]
     uint64_t* tempty = tfull + 4;  // [NA]
@@ -171,8 +193,7 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
     uint64_t* gempty = gfull + 2;  // [2] group buffer released by the epilogue warps
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(gempty + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(s_tmem + 1);
-    int* grp_nvis = reinterpret_cast<int*>(s_tmem + 2);  // producer warp's cache [64]
-    int* grp_prefix = grp_nvis + 64;                     // [n_groups + 1] valid tiles before each group
+    int* grp_prefix = reinterpret_cast<int*>(s_tmem + 2);  // [n_groups + 1] valid tiles before each group
     int* grp_r = grp_prefix + a.n_groups + 1;            // [n_groups] request of each group (-1: invalid)
     int* grp_mv = grp_r + a.n_groups;                    // [n_groups] visible-entry bound of each group
 
@@ -182,15 +203,15 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1 + 32);  // the producer's lane 0 (with the TMA bytes) + 32 scale copies
-            mbar_init(&empty[i], 4 * 32);
+            mbar_init(&empty[i], EW * 32);
         }
         for (int b = 0; b < NA; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4 * 32);
+            mbar_init(&tempty[b], EW * 32);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&gfull[b], 1);
-            mbar_init(&gempty[b], 4);
+            mbar_init(&gempty[b], EW);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -205,7 +226,7 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
 
     // visible-entry count of every query (grid-strided, independent of the tile loop)
     if (a.n_visible)
-        for (int q = blockIdx.x * kIdxThreads + tid; q < a.nq; q += gridDim.x * kIdxThreads)
+        for (int q = blockIdx.x * kThreads + tid; q < a.nq; q += gridDim.x * kThreads)
             a.n_visible[q] = visible_of(a, q);
 
     if (warp == 0) {
@@ -257,7 +278,7 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
             if (valid) locate(idx, &g, &t);
             return item_info<TPI>(a, valid, g, t, grp_r, grp_mv);
         };
-        int n = 0, cached_g = -1, ps = 0, pphase = 0;  // items issued; stage index and its phase parity
+        int n = 0, ps = 0, pphase = 0;  // items issued; stage index and its phase parity
         int cur_g = -1, gb = 1, guse[2] = {0, 0};  // group in the current buffer, buffer index, loads per buffer
         bool alive = true;
         ItemInfo cur = resolve(lo);
@@ -278,24 +299,26 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
                 if (bad && lane == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
                 const int q0 = it.g * a.q_group;
                 const int nqg = min(a.q_group, a.nq - q0);
-                if (a.q_group > 1 && it.g != cached_g) {  // per-query visibility of a multi-query group
-                    for (int j = lane; j < nqg; j += 32) grp_nvis[j] = visible_of(a, q0 + j);
-                    __syncwarp();
-                    cached_g = it.g;
-                }
-                if (lane == 0 && it.g != cur_g) {
-                    // a new group: its query codes, weights and query scales into the other buffer, once the
-                    // epilogue has let go of that buffer's previous group
+                if (it.g != cur_g) {  // warp-uniform
+                    // a new group: its query codes, weights, query scales and per-query visible entries into
+                    // the other buffer, once the epilogue has let go of that buffer's previous group
                     gb ^= 1;
-                    if (guse[gb] > 0 && !wait_or_abort(&gempty[gb], (guse[gb] - 1) & 1, abort_flag, a.status)) {
+                    bool ok = true;
+                    if (lane == 0 && guse[gb] > 0) ok = wait_or_abort(&gempty[gb], (guse[gb] - 1) & 1, abort_flag, a.status);
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) {
                         alive = false;
                     } else {
                         uint8_t* gp = gbase + (size_t)gb * a.gbuf_bytes;
-                        mbar_arrive_expect_tx(&gfull[gb], (uint32_t)a.n_cols * DIM + 2u * nqg * HEADS * 4u);
-                        tma_load_2d(gp, &qmap, 0, q0 * HEADS, &gfull[gb]);
-                        bulk_g2s(gp + a.n_cols * DIM, a.w + (long long)q0 * HEADS, nqg * HEADS * 4, &gfull[gb]);
-                        bulk_g2s(gp + a.n_cols * DIM + a.n_cols * 4, a.q_scale + (long long)q0 * HEADS, nqg * HEADS * 4,
-                                 &gfull[gb]);
+                        int* gnv = reinterpret_cast<int*>(gp + gbuf_nvis_offset(a.n_cols, DIM));
+                        for (int j = lane; j < nqg; j += 32) gnv[j] = a.q_group == 1 ? it.max_vis : visible_of(a, q0 + j);
+                        __syncwarp();
+                        if (lane == 0) {  // release: the lanes' writes above are ordered before the arrival
+                            mbar_arrive_expect_tx(&gfull[gb], (uint32_t)a.n_cols * DIM + 2u * nqg * HEADS * 4u);
+                            tma_load_2d(gp, &qmap, 0, q0 * HEADS, &gfull[gb]);
+                            bulk_g2s(gp + a.n_cols * DIM, a.w + (long long)q0 * HEADS, nqg * HEADS * 4, &gfull[gb]);
+                            bulk_g2s(gp + a.n_cols * DIM + a.n_cols * 4, a.q_scale + (long long)q0 * HEADS,
+                                     nqg * HEADS * 4, &gfull[gb]);
+                        }
                         ++guse[gb];
                         cur_g = it.g;
                     }
@@ -332,9 +355,6 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
                     meta->nq = nqg;
                     meta->q0 = q0;
                     meta->e0 = it.t * kItem;
-                    if (a.q_group == 1) meta->nvis[0] = it.max_vis;
-                    else
-                        for (int j = 0; j < nqg; ++j) meta->nvis[j] = grp_nvis[j];
                     mbar_arrive_expect_tx(&full[s], bytes);  // release: the meta writes above are visible
                 }
                 __syncwarp();
@@ -409,10 +429,17 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
             }
         }
     } else {
-        // ---- epilogue: TMEM lane <-> entry; ReLU, scales, head weights, causal mask -------------------
+        // ---- epilogue: TMEM lane <-> entry, one column slice per warp ----------------------------------
+        // Per group the warp folds its columns' head weight and query scale, u_c = w_c * sq_c.  With
+        // every sq_c >= 0:  w_c * max(0, sq_c * sk * x) = sk * u_c * (sk >= 0 ? max(x, 0) : min(x, 0)),
+        // two instructions a column; a group with a negative query scale takes the literal formula.
         const int quad = warp & 3;  // TMEM lanes this warp may access
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        const int nch = a.n_cols / 16, sl = (warp - 2) >> 2;
+        const int ch_lo = sl * nch / NSL, ch_hi = (sl + 1) * nch / NSL;  // this warp's 16-column chunks
+        float* fold = s_fold + (warp - 2) * kSlice;
+        bool q_neg = false;
         int prev_gb = -1, euse[2] = {0, 0};
         int s = 0, sph = 0, b = 0, bph = 0;  // stage / accumulator index and phase parity
         for (int n = 0;; ++n) {
@@ -421,8 +448,9 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
             const StageMeta* meta = stage_meta(s);
             if (meta->terminal) break;
 
-            const int gbi = meta->gb;
-            if (gbi != prev_gb) {  // this warp is done with the previous group's buffer
+            const int gbi = meta->gb, nqg = meta->nq, q0 = meta->q0;
+            const bool new_group = gbi != prev_gb;
+            if (new_group) {  // this warp is done with the previous group's buffer
                 if (prev_gb >= 0 && lane == 0) mbar_arrive(&gempty[prev_gb]);
                 prev_gb = gbi;
                 ++euse[gbi];
@@ -431,9 +459,20 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
             ok = ok && wait_or_abort(&tfull[b], bph, abort_flag, a.status);
             if (!__all_sync(0xffffffffu, ok)) break;  // warp-uniform: tcgen05.ld is warp-collective
             tc_fence_after();
-            const float* sw = reinterpret_cast<const float*>(gbase + (size_t)gbi * a.gbuf_bytes + a.n_cols * DIM);
+            const uint8_t* gp = gbase + (size_t)gbi * a.gbuf_bytes;
+            const float* sw = reinterpret_cast<const float*>(gp + a.n_cols * DIM);
             const float* ssq = sw + a.n_cols;
-            const int nqg = meta->nq, q0 = meta->q0;
+            const int* gnv = reinterpret_cast<const int*>(gp + gbuf_nvis_offset(a.n_cols, DIM));
+            if (new_group) {
+                bool neg = false;
+                for (int c = ch_lo * 16 + lane; c < ch_hi * 16; c += 32) {
+                    const bool live = c < nqg * HEADS;  // columns past the group's queries hold stale values
+                    fold[c - ch_lo * 16] = live ? sw[c] * ssq[c] : 0.f;
+                    neg |= live && ssq[c] < 0.f;
+                }
+                q_neg = __any_sync(0xffffffffu, neg);
+                __syncwarp();
+            }
             const float* sscale = reinterpret_cast<const float*>(smem + (size_t)s * a.stage_bytes + tiles_bytes +
                                                                  meta_bytes());
 #pragma unroll
@@ -442,24 +481,67 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const __grid_constan
                 const bool page_ok = meta->blk[er / kPage] >= 0;
                 const float sk = page_ok ? sscale[er] : 0.f;
                 const int e = meta->e0 + er;
-                for (int c0 = 0; c0 < a.n_cols; c0 += 16) {
-                    float v[16];
-                    tmem_ld16(lane_base + (b * TPI + tt) * a.n_cols + c0, v);
+                const bool e_ok = e < a.ld;
+                float* out = a.scores + (long long)q0 * a.ld + e;
+                const uint32_t tbase = lane_base + (b * TPI + tt) * a.n_cols;
+                for (int cb = ch_lo; cb < ch_hi; cb += kBatch) {  // kBatch chunks per TMEM wait
+                    // the loads and the wait are warp-collective: warp-uniform control flow only
+                    float v[kBatch][16];
 #pragma unroll
-                    for (int jj = 0; jj < 16 / HEADS; ++jj) {
-                        const int j = c0 / HEADS + jj;
-                        if (j < nqg) {
-                            float acc = 0.f;
+                    for (int k = 0; k < kBatch; ++k)
+                        if (cb + k < ch_hi) tmem_ld_nowait<16>(tbase + (cb + k) * 16, v[k]);
+                    tmem_wait_ld();
 #pragma unroll
-                            for (int h = 0; h < HEADS; ++h) {
-                                const int c = c0 + jj * HEADS + h;
-                                acc += sw[c] * fmaxf(0.f, ssq[c] * sk * v[jj * HEADS + h]);
+                    for (int k = 0; k < kBatch; ++k) tmem_regs_after_wait<16>(v[k]);
+                    // register arithmetic and stores only (lanes may take different sides of the branches):
+                    // kNeg: the entry's key scale is negative, so min(x, 0) survives the ReLU; kLit: the group
+                    // holds a negative query scale and takes the literal formula.  Each query's head sum runs
+                    // as two independent chains and no branch separates the queries of a chunk; only the
+                    // stores are predicated.
+                    auto emit = [&](auto neg_tag, auto lit_tag) {
+                        constexpr bool kNeg = decltype(neg_tag)::value, kLit = decltype(lit_tag)::value;
+#pragma unroll
+                        for (int k = 0; k < kBatch; ++k) {
+                            if (cb + k >= ch_hi) break;  // warp-uniform
+                            float acc[16 / HEADS];
+#pragma unroll
+                            for (int jj = 0; jj < 16 / HEADS; ++jj) {
+                                const float* x = v[k] + jj * HEADS;
+                                const int c0 = (cb + k) * 16 + jj * HEADS;  // first column of query jj
+                                float a0 = 0.f, a1 = 0.f;
+                                if constexpr (!kLit) {
+                                    const float4* u4 = reinterpret_cast<const float4*>(fold + c0 - ch_lo * 16);
+#pragma unroll
+                                    for (int h4 = 0; h4 < HEADS / 4; ++h4) {
+                                        const float4 u = u4[h4];
+                                        const float* xh = x + 4 * h4;
+                                        a0 = fmaf(u.x, kNeg ? fminf(xh[0], 0.f) : fmaxf(xh[0], 0.f), a0);
+                                        a1 = fmaf(u.y, kNeg ? fminf(xh[1], 0.f) : fmaxf(xh[1], 0.f), a1);
+                                        a0 = fmaf(u.z, kNeg ? fminf(xh[2], 0.f) : fmaxf(xh[2], 0.f), a0);
+                                        a1 = fmaf(u.w, kNeg ? fminf(xh[3], 0.f) : fmaxf(xh[3], 0.f), a1);
+                                    }
+                                    acc[jj] = (a0 + a1) * sk;
+                                } else {
+#pragma unroll
+                                    for (int h = 0; h < HEADS; h += 2) {
+                                        a0 = fmaf(sw[c0 + h], fmaxf(0.f, ssq[c0 + h] * sk * x[h]), a0);
+                                        a1 = fmaf(sw[c0 + h + 1], fmaxf(0.f, ssq[c0 + h + 1] * sk * x[h + 1]), a1);
+                                    }
+                                    acc[jj] = a0 + a1;
+                                }
                             }
-                            if (e < a.ld)
-                                a.scores[(long long)(q0 + j) * a.ld + e] =
-                                    (page_ok && e < meta->nvis[j]) ? acc : -INFINITY;
+#pragma unroll
+                            for (int jj = 0; jj < 16 / HEADS; ++jj) {
+                                const int j = (cb + k) * (16 / HEADS) + jj;  // query of the group
+                                if (e_ok && j < nqg)
+                                    out[(long long)j * a.ld] = (page_ok && e < gnv[j]) ? acc[jj] : -INFINITY;
+                            }
                         }
-                    }
+                    };
+                    if (q_neg) emit(BoolTag<false>{}, BoolTag<true>{});
+                    else if (sk < 0.f) emit(BoolTag<true>{}, BoolTag<false>{});
+                    else emit(BoolTag<false>{}, BoolTag<false>{});
+                    __syncwarp();  // reconverge before the next collective load
                 }
             }
             tc_fence_before();
@@ -497,12 +579,15 @@ static bool make_map(CUtensorMap* map, const void* base, uint64_t rows, int dim,
 
 template <int DIM, int HEADS, int TPI>
 static dsa_status_t launch_index(const CUtensorMap& kmap, const CUtensorMap& qmap, IdxArgs a, cudaStream_t st) {
-    // stage = TPI key tiles + metadata + entry scales; two group buffers of query codes + weights + query scales
+    // stage = TPI key tiles + metadata + entry scales; two group buffers of query codes + weights + query
+    // scales + per-query visible entries
     a.stage_bytes = (TPI * kTileEntries * DIM + meta_bytes() + TPI * kTileEntries * 4 + 1023) / 1024 * 1024;
-    a.gbuf_bytes = (a.n_cols * DIM + 2 * a.n_cols * 4 + 1023) / 1024 * 1024;
+    a.gbuf_bytes = (gbuf_nvis_offset(a.n_cols, DIM) + 64 * 4 + 1023) / 1024 * 1024;
     a.items = (a.items + TPI - 1) / TPI;  // tiles -> items per group
-    // alignment slack + group buffers + barriers, the producer's caches and the per-group prefix of valid items
-    const int extra = 1024 + 2 * a.gbuf_bytes + 640 + ((3 * a.n_groups + 1) * 4 + 15) / 16 * 16;
+    // alignment slack + group buffers + the epilogue warps' folded weights + barriers and flags + the
+    // per-group prefix of valid items, requests and visible-entry bounds
+    const int extra = 1024 + 2 * a.gbuf_bytes + epi_warps<TPI>() * slice_cols<TPI>() * 4 + 256 +
+                      ((3 * a.n_groups + 1) * 4 + 15) / 16 * 16;
     const int ctas_per_sm = 2 * (extra + 3 * a.stage_bytes) <= 227 * 1024 && 2 * a.tmem_cols <= 512 ? 2 : 1;
     a.stages = max(2, min(8, (227 * 1024 / ctas_per_sm - extra) / a.stage_bytes));
     const int smem = extra + a.stages * a.stage_bytes;
@@ -511,7 +596,7 @@ static dsa_status_t launch_index(const CUtensorMap& kmap, const CUtensorMap& qma
         return DSA_ERR_CUDA;
     a.total_items = (long long)a.items * a.n_groups;
     const long long grid = std::min<long long>(a.total_items, (long long)sm_count() * ctas_per_sm);
-    if (launch_pdl(index_kernel<DIM, HEADS, TPI>, dim3((unsigned)std::max<long long>(grid, 1)), dim3(kIdxThreads), smem,
+    if (launch_pdl(index_kernel<DIM, HEADS, TPI>, dim3((unsigned)std::max<long long>(grid, 1)), dim3(idx_threads<TPI>()), smem,
                    st, kmap, qmap, a) != cudaSuccess)
         return DSA_ERR_CUDA;
     return launch_status();

@@ -143,6 +143,36 @@ def test_index_scores(name):
     assert rel_l2(np.concatenate(g_all), np.concatenate(w_all)) <= ROW_REL_L2
 
 
+@pytest.mark.parametrize("name", ["c4a_decode", "c4a_chunk", "c4a_multi_prefill"])
+def test_index_scores_signed_scales(name):
+    """Negative query scales in some query groups and negative key scales on some entries: the ReLU
+    then keeps the other sign of <q8, k8>, so both the folded-weight path (with its sign branch per
+    entry) and the literal formula of groups holding a negative query scale are exercised.  Groups are
+    1 (decode), 4 and 32 queries wide."""
+    cpu, gpu, step = _setup(name)
+    step.compress()
+    torch.cuda.synchronize()
+    nq, heads = cpu["q_scale"].shape
+    qs = cpu["q_scale"].clone()
+    flip = torch.zeros_like(qs, dtype=torch.bool)
+    flip[: nq // 2 : 3, 1] = True  # a negative head scale in early queries only: later groups stay non-negative
+    qs[flip] = -qs[flip]
+    gpu["q_scale"].copy_(qs.to(gpu["q_scale"].device))
+    ks = gpu["idx_scale"]
+    ks[::5] = -ks[::5]  # every fifth physical key row
+    step.index()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    pool = oracle_pool(gpu["idx_data"], gpu["idx_scale"], 64)
+    want, nvis = OL.index_scores(np64(cpu["q8"]), np64(qs), np64(cpu["w"]), np64(cpu["q_pos"]),
+                                 np64(cpu["q_req"]), pool, np64(cpu["bt_idx"]))
+    got = np64(step.scores)
+    g_all = np.concatenate([got[q, :n] for q, n in nvis.items()])
+    w_all = np.concatenate([want[q][:n] for q, n in nvis.items()])
+    assert rel_l2(g_all, w_all) <= ROW_REL_L2
+    assert np.any(w_all > 0)
+
+
 @pytest.mark.parametrize("name", INDEXED)
 def test_topk(name):
     cpu, gpu, step = _setup(name)
