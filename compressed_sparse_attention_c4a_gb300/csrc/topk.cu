@@ -34,6 +34,7 @@ constexpr int kTopkClusterMax = 4;
 constexpr int kBins = 2048;
 constexpr int kQuarterMax = 40960;  // scores per CTA kept in shared memory (rows up to 163,840 with C = 4)
 constexpr int kRankMax = 256;       // bucket sizes (cluster-wide) resolved by direct ranking
+constexpr int kMarkWords = (kQuarterMax / 32 + 1 + 3) & ~3;  // winner bitmap, padded to 16 bytes
 
 // Monotone 32-bit key of a score; -0 and +0 compare equal as floats, so they share one key.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -104,25 +105,27 @@ __device__ __forceinline__ uint32_t select_bin(const uint32_t* hist, uint32_t& n
     return b;
 }
 
-// hsum[b] = sum over the cluster's CTAs of their local hist[b]; ends with a block barrier.
-__device__ __forceinline__ void cluster_hist_sum(cg::cluster_group& cluster, int csz, uint32_t* hist,
-                                                 uint32_t* hsum) {
-    cluster.sync();  // every CTA's local histogram is complete
+// The cluster-wide histogram: hist itself when the cluster is one CTA, else hsum[b] = the sum of the
+// CTAs' hist[b].  Starts and ends with a barrier.
+__device__ __forceinline__ const uint32_t* cluster_hist_sum(cg::cluster_group& cluster, int csz, uint32_t* hist,
+                                                            uint32_t* hsum) {
     if (csz == 1) {
-        for (int b = threadIdx.x; b < kBins; b += kTopkThreads) hsum[b] = hist[b];
-    } else {
-        uint32_t* remote[kTopkClusterMax];
+        __syncthreads();
+        return hist;
+    }
+    cluster.sync();  // every CTA's local histogram is complete
+    uint32_t* remote[kTopkClusterMax];
 #pragma unroll
-        for (int c = 0; c < kTopkClusterMax; ++c) remote[c] = cluster.map_shared_rank(hist, c < csz ? c : 0);
-        for (int b = threadIdx.x; b < kBins; b += kTopkThreads) {
-            uint32_t v = 0;
+    for (int c = 0; c < kTopkClusterMax; ++c) remote[c] = cluster.map_shared_rank(hist, c < csz ? c : 0);
+    for (int b = threadIdx.x; b < kBins; b += kTopkThreads) {
+        uint32_t v = 0;
 #pragma unroll
-            for (int c = 0; c < kTopkClusterMax; ++c)
-                if (c < csz) v += remote[c][b];
-            hsum[b] = v;
-        }
+        for (int c = 0; c < kTopkClusterMax; ++c)
+            if (c < csz) v += remote[c][b];
+        hsum[b] = v;
     }
     __syncthreads();
+    return hsum;
 }
 
 __global__ void __launch_bounds__(kTopkThreads, 1)
@@ -131,13 +134,13 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
     pdl_wait();
     pdl_launch_dependents();
     cg::cluster_group cluster = cg::this_cluster();
-    extern __shared__ uint32_t smem_topk[];
-    uint32_t* hist = smem_topk;                             // [kBins] this CTA's histogram
-    uint32_t* hsum = hist + kBins;                          // [kBins] cluster-wide histogram
-    uint32_t* cand_key = hsum + kBins;                      // [kRankMax] this CTA's members of b*
-    uint32_t* cand_idx = cand_key + kRankMax;               // [kRankMax] their row indices
-    uint32_t* marks = cand_idx + kRankMax;                  // [chunk / 32 + 1] ranked winners (local index)
-    float* rowv = reinterpret_cast<float*>(marks + kQuarterMax / 32 + 1);  // this CTA's quarter of the row
+    extern __shared__ __align__(16) uint32_t smem_topk[];
+    uint32_t* hist = smem_topk;                                     // [kBins] this CTA's histogram
+    uint32_t* hsum = hist + kBins;                                  // [kBins] cluster-wide histogram (C > 1)
+    uint32_t* cand_key = hsum + kBins;                              // [kRankMax] this CTA's members of b*
+    uint32_t* cand_idx = cand_key + kRankMax;                       // [kRankMax] their row indices
+    uint32_t* marks = cand_idx + kRankMax;                          // [kMarkWords] ranked winners (local index)
+    float* rowv = reinterpret_cast<float*>(marks + kMarkWords);     // this CTA's part of the row (16-byte aligned)
     __shared__ uint32_t n_cand;
     __shared__ uint32_t warp_tot[32][2];
     __shared__ uint32_t sel[2];
@@ -145,6 +148,11 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
     __shared__ uint32_t totals[2];
 
     const int csz = (int)cluster.num_blocks();
+    // barrier over the cluster, or over the block when the cluster is one CTA
+    auto csync = [&]() {
+        if (csz > 1) cluster.sync();
+        else __syncthreads();
+    };
     const int row = blockIdx.x / csz;
     const int qr = (int)cluster.block_rank();
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -165,30 +173,34 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
     const float* s = scores + (long long)row * ld;
     const int chunk = ((n + csz - 1) / csz + 3) & ~3;  // multiple of 4: aligned float4 loads
     const int base = qr * chunk;
-    const int mq = max(0, min(n, base + chunk) - base);  // scores in this CTA's quarter
+    const int mq = max(0, min(n, base + chunk) - base);  // scores in this CTA's part
 
-    // 1. quarter -> shared memory, local max / min, then the cluster's
+    // 1. part -> shared memory (float4 stores; the tail of the last vector is -inf), local max / min
+    // of the finite scores, then the cluster's
     float mx = -INFINITY, mn = INFINITY;
     for (int i0 = tid * 4; i0 < mq; i0 += kTopkThreads * 16) {
         float4 q[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int i = i0 + u * kTopkThreads * 4;
-            q[u] = i + 4 <= mq ? *reinterpret_cast<const float4*>(s + base + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i + 4 <= mq) {
+                q[u] = *reinterpret_cast<const float4*>(s + base + i);
+            } else {
+                q[u].x = i < mq ? s[base + i] : -INFINITY;
+                q[u].y = i + 1 < mq ? s[base + i + 1] : -INFINITY;
+                q[u].z = i + 2 < mq ? s[base + i + 2] : -INFINITY;
+                q[u].w = -INFINITY;  // i + 3 >= mq here
+            }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int i = i0 + u * kTopkThreads * 4;
-            float v[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-            if (i + 4 > mq)
-                for (int e = 0; e < 4; ++e) v[e] = i + e < mq ? s[base + i + e] : -INFINITY;
+            if (i < mq) *reinterpret_cast<float4*>(rowv + i) = q[u];
+            const float v[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                if (i + e < mq) rowv[i + e] = v[e];
-                if (v[e] != -INFINITY) {
-                    mx = fmaxf(mx, v[e]);
-                    mn = fminf(mn, v[e]);
-                }
+                mx = fmaxf(mx, v[e]);  // -inf never raises the maximum
+                mn = fminf(mn, v[e] == -INFINITY ? INFINITY : v[e]);
             }
         }
     }
@@ -210,59 +222,120 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
             red[1] = b;
         }
     }
-    cluster.sync();
-    mx = -INFINITY;
-    mn = INFINITY;
-    for (int c = 0; c < csz; ++c) {
-        const float* rr = cluster.map_shared_rank(red, c);
-        mx = fmaxf(mx, rr[0]);
-        mn = fminf(mn, rr[1]);
+    csync();
+    if (csz > 1) {
+        mx = -INFINITY;
+        mn = INFINITY;
+        for (int c = 0; c < csz; ++c) {
+            const float* rr = cluster.map_shared_rank(red, c);
+            mx = fmaxf(mx, rr[0]);
+            mn = fminf(mn, rr[1]);
+        }
+    } else {
+        mx = red[0];
+        mn = red[1];
     }
     const bool any_finite = mx != -INFINITY;
     float scale = (any_finite && mx > mn) ? 2046.f / (mx - mn) : 0.f;
     if (!isfinite(scale)) scale = 0.f;  // degenerate range: one bucket, resolved by the radix passes
+    // bin(v) = 2047 - round(min(2046, (mx - v) * scale)), rounded by adding 2^23 (full-rate arithmetic):
+    // monotone (a larger score never lands in a lower bin, equal scores share one); -inf (and NaN
+    // products) land in bin 1, the lowest bin of finite scores, where the exact keys order them last
     auto bin_of = [&](float v) -> uint32_t {
-        if (v == -INFINITY) return 0u;
-        return 2047u - (uint32_t)fminf(2046.f, (mx - v) * scale);
+        const float t = fminf(2046.f, (mx - v) * scale);
+        return (2047u + 0x4B000000u) - __float_as_uint(t + 8388608.f);
     };
 
     // 2. value buckets: local histogram, cluster-wide sum, the bucket of the k-th largest score
-    for (int i = tid; i < mq; i += kTopkThreads) atomicAdd(&hist[bin_of(rowv[i])], 1u);
-    cluster_hist_sum(cluster, csz, hist, hsum);
+    for (int i = tid * 4; i < mq; i += kTopkThreads * 4) {
+        const float4 q = *reinterpret_cast<const float4*>(rowv + i);
+        atomicAdd(&hist[bin_of(q.x)], 1u);
+        if (i + 1 < mq) atomicAdd(&hist[bin_of(q.y)], 1u);
+        if (i + 2 < mq) atomicAdd(&hist[bin_of(q.z)], 1u);
+        if (i + 3 < mq) atomicAdd(&hist[bin_of(q.w)], 1u);
+    }
+    const uint32_t* hs = cluster_hist_sum(cluster, csz, hist, hsum);
     uint32_t need = (uint32_t)k;
-    const uint32_t bstar = select_bin(hsum, need, warp_tot, sel);
-    const uint32_t in_bucket = hsum[bstar];
+    const uint32_t bstar = select_bin(hs, need, warp_tot, sel);
+    const uint32_t in_bucket = hs[bstar];
     const bool take_all = in_bucket == need;
     const bool rank_mode = !take_all && in_bucket <= (uint32_t)kRankMax;
 
-    // 3a. small bucket: rank its members directly across the cluster
-    if (rank_mode) {
-        for (int i = tid; i < mq; i += kTopkThreads) {
-            const float v = rowv[i];
-            const bool take = bin_of(v) == bstar;
-            const unsigned active = __activemask();
-            const unsigned ballot = __ballot_sync(active, take);
-            if (ballot) {
-                const int leader = __ffs(ballot) - 1;
-                uint32_t slot0 = 0;
-                if (lane == leader) slot0 = atomicAdd(&n_cand, (uint32_t)__popc(ballot));
-                slot0 = __shfl_sync(active, slot0, leader);
-                if (take) {
-                    const uint32_t slot = slot0 + __popc(ballot & ((1u << lane) - 1u));
-                    cand_key[slot] = order_key(v);
-                    cand_idx[slot] = (uint32_t)(base + i);
-                }
+    // 3. heavy ties: radix select inside b* for the threshold key T and the entries equal to T still needed
+    uint32_t T = 0u, need_T = 0u, prefix = 0u, mask = 0u;
+    if (!take_all && !rank_mode) {
+        need_T = need;
+        for (int pass = 0; pass < 3; ++pass) {
+            const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+            const uint32_t dm = pass == 2 ? 0x3FFu : 0x7FFu;
+            csync();  // the other CTAs (and select_bin) are done reading this CTA's previous histogram
+            for (int b = tid; b < kBins; b += kTopkThreads) hist[b] = 0;
+            __syncthreads();
+            for (int i = tid; i < mq; i += kTopkThreads) {
+                const float v = rowv[i];
+                const uint32_t key = order_key(v);
+                if (bin_of(v) == bstar && (key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
+            }
+            const uint32_t* hp = cluster_hist_sum(cluster, csz, hist, hsum);
+            const uint32_t d = select_bin(hp, need_T, warp_tot, sel);
+            prefix |= d << sh;
+            mask |= dm << sh;
+        }
+        T = prefix;
+    }
+
+    // 4. one pass over this thread's contiguous run: scores above b* (taken), members of b* (taken
+    // whole, ranked, or split at T)
+    int run = (mq + kTopkThreads - 1) / kTopkThreads;  // <= 41
+    run |= 1;                                          // odd: conflict-free strided shared-memory reads
+    const int lo = min(mq, tid * run), hi = min(mq, lo + run);
+    unsigned long long mdef = 0ull, mtie = 0ull, mcand = 0ull;
+    for (int i = lo; i < hi; ++i) {
+        const float v = rowv[i];
+        const uint32_t b = bin_of(v);
+        bool d = b > bstar, t = false, c = false;
+        if (b == bstar) {
+            if (take_all) d = true;
+            else if (rank_mode) c = true;
+            else {
+                const uint32_t key = order_key(v);
+                d = key > T;
+                t = key == T;
             }
         }
-        cluster.sync();  // every CTA's member list is complete
+        mdef |= (unsigned long long)d << (i - lo);
+        mtie |= (unsigned long long)t << (i - lo);
+        mcand |= (unsigned long long)c << (i - lo);
+    }
+    // 5. small bucket: its members (at most kRankMax over the cluster) listed, then each counts the
+    // better ones (larger score, or equal score and lower index) across the cluster; the `need` best win
+    if (rank_mode) {
+        const uint32_t cnt = (uint32_t)__popcll(mcand);
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        uint32_t wbase = 0;
+        if (lane == 31 && incl) wbase = atomicAdd(&n_cand, incl);
+        wbase = __shfl_sync(0xffffffffu, wbase, 31);
+        uint32_t slot = wbase + incl - cnt;
+        for (unsigned long long m = mcand; m; m &= m - 1) {
+            const int u = __ffsll((long long)m) - 1;
+            cand_key[slot] = order_key(rowv[lo + u]);
+            cand_idx[slot] = (uint32_t)(base + lo + u);
+            ++slot;
+        }
+        csync();  // every CTA's member list is complete
         if (tid < (int)n_cand) {
             const uint32_t my_k = cand_key[tid], my_i = cand_idx[tid];
             uint32_t better = 0;
 #pragma unroll 1
             for (int c = 0; c < csz; ++c) {
-                const uint32_t* rk = cluster.map_shared_rank(cand_key, c);
-                const uint32_t* ri = cluster.map_shared_rank(cand_idx, c);
-                const int nc = (int)*cluster.map_shared_rank(&n_cand, c);
+                const uint32_t* rk = csz > 1 ? cluster.map_shared_rank(cand_key, c) : cand_key;
+                const uint32_t* ri = csz > 1 ? cluster.map_shared_rank(cand_idx, c) : cand_idx;
+                const int nc = csz > 1 ? (int)*cluster.map_shared_rank(&n_cand, c) : (int)n_cand;
                 for (int j = 0; j < nc; ++j) {
                     const uint32_t kj = rk[j];
                     better += (kj > my_k) || (kj == my_k && ri[j] < my_i);
@@ -273,70 +346,36 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
                 atomicOr(&marks[li >> 5], 1u << (li & 31));
             }
         }
-        __syncthreads();
+        __syncthreads();  // marks are local: each CTA ranks its own members
+        for (unsigned long long m = mcand; m; m &= m - 1) {
+            const int u = __ffsll((long long)m) - 1;
+            const int li = lo + u;
+            if ((marks[li >> 5] >> (li & 31)) & 1u) mdef |= 1ull << u;
+        }
     }
 
-    // 3b. heavy ties: radix select inside b* for the threshold key T and the entries equal to T still needed
-    uint32_t T = 0u, need_T = 0u, prefix = 0u, mask = 0u;
-    if (!take_all && !rank_mode) {
-        need_T = need;
-        for (int pass = 0; pass < 3; ++pass) {
-            const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-            const uint32_t dm = pass == 2 ? 0x3FFu : 0x7FFu;
-            cluster.sync();  // the other CTAs are done reading this CTA's previous histogram
-            for (int b = tid; b < kBins; b += kTopkThreads) hist[b] = 0;
-            __syncthreads();
-            for (int i = tid; i < mq; i += kTopkThreads) {
-                const float v = rowv[i];
-                const uint32_t key = order_key(v);
-                if (bin_of(v) == bstar && (key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
-            }
-            cluster_hist_sum(cluster, csz, hist, hsum);
-            const uint32_t d = select_bin(hsum, need_T, warp_tot, sel);
-            prefix |= d << sh;
-            mask |= dm << sh;
-        }
-        T = prefix;
-    }
-
-    // 4. ordered compaction over the quarter
-    int run = (mq + kTopkThreads - 1) / kTopkThreads;  // <= 40
-    run |= 1;                                          // odd: conflict-free strided shared-memory reads
-    const int lo = min(mq, tid * run), hi = min(mq, lo + run);
-    unsigned long long mdef = 0ull, mtie = 0ull;
-    for (int i = lo; i < hi; ++i) {
-        const float v = rowv[i];
-        const uint32_t b = bin_of(v);
-        bool d = b > bstar, t = false;
-        if (b == bstar) {
-            if (take_all) d = true;
-            else if (rank_mode) d = (marks[i >> 5] >> (i & 31)) & 1u;
-            else {
-                const uint32_t key = order_key(v);
-                d = key > T;
-                t = key == T;
-            }
-        }
-        mdef |= (unsigned long long)d << (i - lo);
-        mtie |= (unsigned long long)t << (i - lo);
-    }
+    // 6. ordered compaction: a block scan plus the totals of the lower CTAs give every selected index
+    // its slot in increasing index order; entries equal to T are ranked by index (the lowest win)
     uint32_t ex_d, ex_t, tot_d, tot_t;
     block_scan2((uint32_t)__popcll(mdef), (uint32_t)__popcll(mtie), &ex_d, &ex_t, &tot_d, &tot_t, warp_tot);
-    if (tid == 0) {
-        totals[0] = tot_d;
-        totals[1] = tot_t;
-    }
-    cluster.sync();
-    uint32_t base_d = 0, base_t = 0, all_d = 0, all_t = 0;
-    for (int c = 0; c < csz; ++c) {
-        const uint32_t* tt = cluster.map_shared_rank(totals, c);
-        const uint32_t a = tt[0], b = tt[1];
-        if (c < qr) {
-            base_d += a;
-            base_t += b;
+    uint32_t base_d = 0, base_t = 0, all_d = tot_d, all_t = tot_t;
+    if (csz > 1) {
+        if (tid == 0) {
+            totals[0] = tot_d;
+            totals[1] = tot_t;
         }
-        all_d += a;
-        all_t += b;
+        cluster.sync();
+        all_d = all_t = 0;
+        for (int c = 0; c < csz; ++c) {
+            const uint32_t* tt = cluster.map_shared_rank(totals, c);
+            const uint32_t a = tt[0], b = tt[1];
+            if (c < qr) {
+                base_d += a;
+                base_t += b;
+            }
+            all_d += a;
+            all_t += b;
+        }
     }
     uint32_t tie_rank = base_t + ex_t;
     uint32_t pos = base_d + ex_d + min(tie_rank, need_T);
@@ -354,7 +393,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
         for (int i = (int)total + tid; i < k; i += kTopkThreads) out[i] = -1;
         if (tid == 0 && total != (uint32_t)k) report(status, DSA_ERR_DEVICE_FAULT);
     }
-    cluster.sync();  // no CTA leaves while another may still read its shared memory
+    if (csz > 1) cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -643,7 +682,7 @@ extern "C" dsa_status_t dsa_topk(int32_t nq, const float* scores, int32_t ld, co
     const int csz = ld <= kQuarterMax ? 1 : kTopkClusterMax;
     const int chunk = ((ld + csz - 1) / csz + 3) & ~3;
     if (chunk > kQuarterMax) return DSA_ERR_UNSUPPORTED;
-    const size_t smem = (size_t)(2 * kBins + 2 * kRankMax + kQuarterMax / 32 + 1) * sizeof(uint32_t) +
+    const size_t smem = (size_t)(2 * kBins + 2 * kRankMax + kMarkWords) * sizeof(uint32_t) +
                         (size_t)chunk * sizeof(float);
     if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DSA_ERR_CUDA;

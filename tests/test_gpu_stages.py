@@ -277,10 +277,11 @@ def test_gather_rows_bit_exact_and_unmapped_fault():
     assert int(out2[1].sum().item()) == 0
 
 
-@pytest.mark.parametrize("ld", [1024, 16384, 65536])
+@pytest.mark.parametrize("ld", [1024, 16384, 20004, 34816, 65536])
 def test_topk_edge_cases_exact(ld):
-    """Ties, all-equal rows, n == k + 1, n < k, empty rows, -inf tails, negative scores; rows that fit
-    shared memory and rows that stream from L2 (ld > 40,960)."""
+    """Ties, all-equal rows, n == k + 1, n < k, empty rows, -inf tails, negative scores, rows whose
+    k-th entry is -inf; rows held in registers (ld <= 16,384), in one CTA's shared memory (up to
+    40,960) and split over a cluster (ld > 40,960)."""
     from compressed_sparse_attention_c4a_gb300 import dsa
     rng = np.random.default_rng(ld)
     k = 512
@@ -307,6 +308,10 @@ def test_topk_edge_cases_exact(ld):
             r = (rng.integers(0, 3, ld) * 2.0 ** -20).astype(np.float32)   # ties among tiny values
         elif case == 8:
             r[::2] = 0.0                                            # half exact zeros (ReLU-like)
+        elif case == 9:
+            fin = rng.choice(n_full, 100, replace=False)            # 100 finite scores: the other k - 100
+            r[:] = -np.inf                                          # winners are -inf, lowest index first
+            r[fin] = rng.standard_normal(100).astype(np.float32)
         rows.append(r)
         nv.append(n)
     scores = torch.from_numpy(np.stack(rows)).cuda()
