@@ -3,21 +3,23 @@
 // [P1] "DeepSeek DSA、DeepSeek V4与vLLM Hybrid KV Cache详解" §4.2: S_t = TopK(I_{t,:}, k); the
 // main attention reads only S_t.  [P2] "DeepSeek V4 稀疏注意力完全解剖" 机制三: k = 512 for c4a.
 //
-// One thread-block cluster of C CTAs (1024 threads each) per query row, C = 1 when the row fits one CTA's
-// shared memory (up to 40,960 scores) and 4 for longer rows; CTA q holds the q-th of C parts of the row
-// in shared memory.  Partial results are combined through distributed shared memory (each CTA reads
-// the other CTAs' copies), so every CTA takes the same decisions:
-//   1. max M and min m of the finite scores;
-//   2. bucket select: bin(v) = 2047 - floor((M - v) * 2046 / (M - m)) for finite v, bin(-inf) = 0 --
-//      monotone (larger score -> same or larger bin; equal scores share a bin) and even, so the
-//      shared-memory histogram has little atomic contention; the summed histogram gives the bin b*
-//      holding the k-th largest score and `need`, the count still missing;
-//   3. unless b* holds exactly `need` scores: when it holds at most 256, every CTA publishes its
-//      members of b* and each member counts the better ones (larger score, or equal score and lower
-//      index) across the cluster -- the `need` best are marked; otherwise (heavy ties) a radix
-//      select over the 32-bit order keys of b*'s scores (digits of 11, 11, 10 bits, histograms summed
-//      across the cluster) gives the exact threshold key T and how many entries equal to T are still
-//      needed;
+// Rows of up to 16,384 scores: one CTA per row with the row in registers (topk_reg_kernel).  Longer
+// rows: one thread-block cluster of C CTAs (512 threads, two CTAs per SM) per row, C = 1 up to 40,960
+// scores, else 2 or 4; CTA q handles the q-th of C parts.  Only a 16-bit value bucket per score is kept in
+// shared memory, so two rows share an SM and one row's loads overlap the other's arithmetic; exact scores
+// are read again (from L2) only where a bucket has to be split.  Partial results are combined through
+// distributed shared memory, so every CTA takes the same decisions:
+//   1. max M and min m of the finite scores (first read of the part);
+//   2. bucket select: bin(v) = 2047 - round(min(2046, (M - v) * 2046 / (M - m))) -- monotone (larger
+//      score -> same or larger bin; equal scores share a bin) and even, so the shared-memory histogram
+//      has little atomic contention; bins are stored while the histogram is built (second read); the
+//      summed histogram gives the bin b* holding the k-th largest score and `need`, the count still
+//      missing;
+//   3. unless b* holds exactly `need` scores: when it holds at most 256, its members are listed and each
+//      counts the better ones (larger score, or equal score and lower index) across the cluster -- the
+//      `need` best are marked; otherwise (heavy ties) a radix select over the 32-bit order keys of b*'s
+//      scores (digits of 11, 11, 10 bits, histograms summed across the cluster) gives the exact
+//      threshold key T and how many entries equal to T are still needed;
 //   4. ordered compaction: thread t of CTA q owns a contiguous run of indices; a block scan plus the
 //      totals of the lower CTAs give every selected index its slot in increasing index order, and
 //      rank entries equal to T by index (the lowest indices win).
@@ -29,12 +31,13 @@ namespace cg = cooperative_groups;
 
 namespace dsa {
 
-constexpr int kTopkThreads = 1024;
+constexpr int kTopkThreads = 512;
+constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkClusterMax = 4;
 constexpr int kBins = 2048;
-constexpr int kQuarterMax = 40960;  // scores per CTA kept in shared memory (rows up to 163,840 with C = 4)
-constexpr int kRankMax = 256;       // bucket sizes (cluster-wide) resolved by direct ranking
-constexpr int kMarkWords = (kQuarterMax / 32 + 1 + 3) & ~3;  // winner bitmap, padded to 16 bytes
+constexpr int kPartMax = 40960;  // scores per CTA (rows up to 163,840 with C = 4)
+constexpr int kRankMax = 256;    // bucket sizes (cluster-wide) resolved by direct ranking
+constexpr int kMarkWords = (kPartMax / 32 + 1 + 3) & ~3;  // winner bitmap, padded to 16 bytes
 
 // Monotone 32-bit key of a score; -0 and +0 compare equal as floats, so they share one key.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -43,365 +46,7 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive block scan of two counters; also returns the totals.
-__device__ __forceinline__ void block_scan2(uint32_t a, uint32_t b, uint32_t* ex_a, uint32_t* ex_b,
-                                            uint32_t* tot_a, uint32_t* tot_b, uint32_t (*warp_tot)[2]) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    uint32_t ia = a, ib = b;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        uint32_t ta = __shfl_up_sync(0xffffffffu, ia, o), tb = __shfl_up_sync(0xffffffffu, ib, o);
-        if (lane >= o) {
-            ia += ta;
-            ib += tb;
-        }
-    }
-    if (lane == 31) {
-        warp_tot[wid][0] = ia;
-        warp_tot[wid][1] = ib;
-    }
-    __syncthreads();
-    if (wid == 0) {
-        uint32_t wa = warp_tot[lane][0], wb = warp_tot[lane][1];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            uint32_t ta = __shfl_up_sync(0xffffffffu, wa, o), tb = __shfl_up_sync(0xffffffffu, wb, o);
-            if (lane >= o) {
-                wa += ta;
-                wb += tb;
-            }
-        }
-        warp_tot[lane][0] = wa;
-        warp_tot[lane][1] = wb;
-    }
-    __syncthreads();
-    *ex_a = (wid ? warp_tot[wid - 1][0] : 0u) + ia - a;
-    *ex_b = (wid ? warp_tot[wid - 1][1] : 0u) + ib - b;
-    *tot_a = warp_tot[31][0];
-    *tot_b = warp_tot[31][1];
-    __syncthreads();
-}
-
-// Given the cluster-wide histogram, find the bin (scanning from the top) that holds the need-th
-// largest remaining element; need is reduced by the count above it.  Returns the bin.
-__device__ __forceinline__ uint32_t select_bin(const uint32_t* hist, uint32_t& need, uint32_t (*warp_tot)[2],
-                                               uint32_t* sel) {
-    const int tid = threadIdx.x;
-    const int b_hi = kBins - 1 - 2 * tid, b_lo = b_hi - 1;  // bins in descending order, two per thread
-    const uint32_t c_hi = hist[b_hi], c_lo = hist[b_lo];
-    uint32_t ex, ex2, tot, tot2;
-    block_scan2(c_hi + c_lo, 0u, &ex, &ex2, &tot, &tot2, warp_tot);
-    if (ex < need && need <= ex + c_hi) {
-        sel[0] = (uint32_t)b_hi;
-        sel[1] = ex;
-    } else if (ex + c_hi < need && need <= ex + c_hi + c_lo) {
-        sel[0] = (uint32_t)b_lo;
-        sel[1] = ex + c_hi;
-    }
-    __syncthreads();
-    const uint32_t b = sel[0];
-    need -= sel[1];
-    __syncthreads();
-    return b;
-}
-
-// The cluster-wide histogram: hist itself when the cluster is one CTA, else hsum[b] = the sum of the
-// CTAs' hist[b].  Starts and ends with a barrier.
-__device__ __forceinline__ const uint32_t* cluster_hist_sum(cg::cluster_group& cluster, int csz, uint32_t* hist,
-                                                            uint32_t* hsum) {
-    if (csz == 1) {
-        __syncthreads();
-        return hist;
-    }
-    cluster.sync();  // every CTA's local histogram is complete
-    uint32_t* remote[kTopkClusterMax];
-#pragma unroll
-    for (int c = 0; c < kTopkClusterMax; ++c) remote[c] = cluster.map_shared_rank(hist, c < csz ? c : 0);
-    for (int b = threadIdx.x; b < kBins; b += kTopkThreads) {
-        uint32_t v = 0;
-#pragma unroll
-        for (int c = 0; c < kTopkClusterMax; ++c)
-            if (c < csz) v += remote[c][b];
-        hsum[b] = v;
-    }
-    __syncthreads();
-    return hsum;
-}
-
-__global__ void __launch_bounds__(kTopkThreads, 1)
-    topk_kernel(const float* __restrict__ scores, int ld, const int32_t* __restrict__ n_valid, int k,
-                int32_t* __restrict__ idx_out, int32_t* status) {
-    pdl_wait();
-    pdl_launch_dependents();
-    cg::cluster_group cluster = cg::this_cluster();
-    extern __shared__ __align__(16) uint32_t smem_topk[];
-    uint32_t* hist = smem_topk;                                     // [kBins] this CTA's histogram
-    uint32_t* hsum = hist + kBins;                                  // [kBins] cluster-wide histogram (C > 1)
-    uint32_t* cand_key = hsum + kBins;                              // [kRankMax] this CTA's members of b*
-    uint32_t* cand_idx = cand_key + kRankMax;                       // [kRankMax] their row indices
-    uint32_t* marks = cand_idx + kRankMax;                          // [kMarkWords] ranked winners (local index)
-    float* rowv = reinterpret_cast<float*>(marks + kMarkWords);     // this CTA's part of the row (16-byte aligned)
-    __shared__ uint32_t n_cand;
-    __shared__ uint32_t warp_tot[32][2];
-    __shared__ uint32_t sel[2];
-    __shared__ float red[2];
-    __shared__ uint32_t totals[2];
-
-    const int csz = (int)cluster.num_blocks();
-    // barrier over the cluster, or over the block when the cluster is one CTA
-    auto csync = [&]() {
-        if (csz > 1) cluster.sync();
-        else __syncthreads();
-    };
-    const int row = blockIdx.x / csz;
-    const int qr = (int)cluster.block_rank();
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    int32_t* out = idx_out + (long long)row * k;
-    const int n = n_valid[row];  // the same for the whole cluster: every branch below is cluster-uniform
-    if (n < 0 || n > ld) {
-        if (qr == 0) {
-            if (tid == 0) report(status, DSA_ERR_DEVICE_FAULT);
-            for (int i = tid; i < k; i += kTopkThreads) out[i] = -1;
-        }
-        return;
-    }
-    if (n <= k) {
-        if (qr == 0)
-            for (int i = tid; i < k; i += kTopkThreads) out[i] = i < n ? i : -1;
-        return;
-    }
-    const float* s = scores + (long long)row * ld;
-    const int chunk = ((n + csz - 1) / csz + 3) & ~3;  // multiple of 4: aligned float4 loads
-    const int base = qr * chunk;
-    const int mq = max(0, min(n, base + chunk) - base);  // scores in this CTA's part
-
-    // 1. part -> shared memory (float4 stores; the tail of the last vector is -inf), local max / min
-    // of the finite scores, then the cluster's
-    float mx = -INFINITY, mn = INFINITY;
-    for (int i0 = tid * 4; i0 < mq; i0 += kTopkThreads * 16) {
-        float4 q[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = i0 + u * kTopkThreads * 4;
-            if (i + 4 <= mq) {
-                q[u] = *reinterpret_cast<const float4*>(s + base + i);
-            } else {
-                q[u].x = i < mq ? s[base + i] : -INFINITY;
-                q[u].y = i + 1 < mq ? s[base + i + 1] : -INFINITY;
-                q[u].z = i + 2 < mq ? s[base + i + 2] : -INFINITY;
-                q[u].w = -INFINITY;  // i + 3 >= mq here
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = i0 + u * kTopkThreads * 4;
-            if (i < mq) *reinterpret_cast<float4*>(rowv + i) = q[u];
-            const float v[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                mx = fmaxf(mx, v[e]);  // -inf never raises the maximum
-                mn = fminf(mn, v[e] == -INFINITY ? INFINITY : v[e]);
-            }
-        }
-    }
-    for (int b = tid; b < kBins; b += kTopkThreads) hist[b] = 0;
-    for (int w = tid; w <= (mq >> 5); w += kTopkThreads) marks[w] = 0;
-    if (tid == 0) n_cand = 0;
-    mx = warp_max(mx);
-    mn = -warp_max(-mn);
-    if (lane == 0) {
-        warp_tot[wid][0] = __float_as_uint(mx);
-        warp_tot[wid][1] = __float_as_uint(mn);
-    }
-    __syncthreads();
-    if (wid == 0) {
-        const float a = warp_max(__uint_as_float(warp_tot[lane][0]));
-        const float b = -warp_max(-__uint_as_float(warp_tot[lane][1]));
-        if (lane == 0) {
-            red[0] = a;
-            red[1] = b;
-        }
-    }
-    csync();
-    if (csz > 1) {
-        mx = -INFINITY;
-        mn = INFINITY;
-        for (int c = 0; c < csz; ++c) {
-            const float* rr = cluster.map_shared_rank(red, c);
-            mx = fmaxf(mx, rr[0]);
-            mn = fminf(mn, rr[1]);
-        }
-    } else {
-        mx = red[0];
-        mn = red[1];
-    }
-    const bool any_finite = mx != -INFINITY;
-    float scale = (any_finite && mx > mn) ? 2046.f / (mx - mn) : 0.f;
-    if (!isfinite(scale)) scale = 0.f;  // degenerate range: one bucket, resolved by the radix passes
-    // bin(v) = 2047 - round(min(2046, (mx - v) * scale)), rounded by adding 2^23 (full-rate arithmetic):
-    // monotone (a larger score never lands in a lower bin, equal scores share one); -inf (and NaN
-    // products) land in bin 1, the lowest bin of finite scores, where the exact keys order them last
-    auto bin_of = [&](float v) -> uint32_t {
-        const float t = fminf(2046.f, (mx - v) * scale);
-        return (2047u + 0x4B000000u) - __float_as_uint(t + 8388608.f);
-    };
-
-    // 2. value buckets: local histogram, cluster-wide sum, the bucket of the k-th largest score
-    for (int i = tid * 4; i < mq; i += kTopkThreads * 4) {
-        const float4 q = *reinterpret_cast<const float4*>(rowv + i);
-        atomicAdd(&hist[bin_of(q.x)], 1u);
-        if (i + 1 < mq) atomicAdd(&hist[bin_of(q.y)], 1u);
-        if (i + 2 < mq) atomicAdd(&hist[bin_of(q.z)], 1u);
-        if (i + 3 < mq) atomicAdd(&hist[bin_of(q.w)], 1u);
-    }
-    const uint32_t* hs = cluster_hist_sum(cluster, csz, hist, hsum);
-    uint32_t need = (uint32_t)k;
-    const uint32_t bstar = select_bin(hs, need, warp_tot, sel);
-    const uint32_t in_bucket = hs[bstar];
-    const bool take_all = in_bucket == need;
-    const bool rank_mode = !take_all && in_bucket <= (uint32_t)kRankMax;
-
-    // 3. heavy ties: radix select inside b* for the threshold key T and the entries equal to T still needed
-    uint32_t T = 0u, need_T = 0u, prefix = 0u, mask = 0u;
-    if (!take_all && !rank_mode) {
-        need_T = need;
-        for (int pass = 0; pass < 3; ++pass) {
-            const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-            const uint32_t dm = pass == 2 ? 0x3FFu : 0x7FFu;
-            csync();  // the other CTAs (and select_bin) are done reading this CTA's previous histogram
-            for (int b = tid; b < kBins; b += kTopkThreads) hist[b] = 0;
-            __syncthreads();
-            for (int i = tid; i < mq; i += kTopkThreads) {
-                const float v = rowv[i];
-                const uint32_t key = order_key(v);
-                if (bin_of(v) == bstar && (key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
-            }
-            const uint32_t* hp = cluster_hist_sum(cluster, csz, hist, hsum);
-            const uint32_t d = select_bin(hp, need_T, warp_tot, sel);
-            prefix |= d << sh;
-            mask |= dm << sh;
-        }
-        T = prefix;
-    }
-
-    // 4. one pass over this thread's contiguous run: scores above b* (taken), members of b* (taken
-    // whole, ranked, or split at T)
-    int run = (mq + kTopkThreads - 1) / kTopkThreads;  // <= 41
-    run |= 1;                                          // odd: conflict-free strided shared-memory reads
-    const int lo = min(mq, tid * run), hi = min(mq, lo + run);
-    unsigned long long mdef = 0ull, mtie = 0ull, mcand = 0ull;
-    for (int i = lo; i < hi; ++i) {
-        const float v = rowv[i];
-        const uint32_t b = bin_of(v);
-        bool d = b > bstar, t = false, c = false;
-        if (b == bstar) {
-            if (take_all) d = true;
-            else if (rank_mode) c = true;
-            else {
-                const uint32_t key = order_key(v);
-                d = key > T;
-                t = key == T;
-            }
-        }
-        mdef |= (unsigned long long)d << (i - lo);
-        mtie |= (unsigned long long)t << (i - lo);
-        mcand |= (unsigned long long)c << (i - lo);
-    }
-    // 5. small bucket: its members (at most kRankMax over the cluster) listed, then each counts the
-    // better ones (larger score, or equal score and lower index) across the cluster; the `need` best win
-    if (rank_mode) {
-        const uint32_t cnt = (uint32_t)__popcll(mcand);
-        uint32_t incl = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += t;
-        }
-        uint32_t wbase = 0;
-        if (lane == 31 && incl) wbase = atomicAdd(&n_cand, incl);
-        wbase = __shfl_sync(0xffffffffu, wbase, 31);
-        uint32_t slot = wbase + incl - cnt;
-        for (unsigned long long m = mcand; m; m &= m - 1) {
-            const int u = __ffsll((long long)m) - 1;
-            cand_key[slot] = order_key(rowv[lo + u]);
-            cand_idx[slot] = (uint32_t)(base + lo + u);
-            ++slot;
-        }
-        csync();  // every CTA's member list is complete
-        if (tid < (int)n_cand) {
-            const uint32_t my_k = cand_key[tid], my_i = cand_idx[tid];
-            uint32_t better = 0;
-#pragma unroll 1
-            for (int c = 0; c < csz; ++c) {
-                const uint32_t* rk = csz > 1 ? cluster.map_shared_rank(cand_key, c) : cand_key;
-                const uint32_t* ri = csz > 1 ? cluster.map_shared_rank(cand_idx, c) : cand_idx;
-                const int nc = csz > 1 ? (int)*cluster.map_shared_rank(&n_cand, c) : (int)n_cand;
-                for (int j = 0; j < nc; ++j) {
-                    const uint32_t kj = rk[j];
-                    better += (kj > my_k) || (kj == my_k && ri[j] < my_i);
-                }
-            }
-            if (better < need) {
-                const uint32_t li = my_i - (uint32_t)base;
-                atomicOr(&marks[li >> 5], 1u << (li & 31));
-            }
-        }
-        __syncthreads();  // marks are local: each CTA ranks its own members
-        for (unsigned long long m = mcand; m; m &= m - 1) {
-            const int u = __ffsll((long long)m) - 1;
-            const int li = lo + u;
-            if ((marks[li >> 5] >> (li & 31)) & 1u) mdef |= 1ull << u;
-        }
-    }
-
-    // 6. ordered compaction: a block scan plus the totals of the lower CTAs give every selected index
-    // its slot in increasing index order; entries equal to T are ranked by index (the lowest win)
-    uint32_t ex_d, ex_t, tot_d, tot_t;
-    block_scan2((uint32_t)__popcll(mdef), (uint32_t)__popcll(mtie), &ex_d, &ex_t, &tot_d, &tot_t, warp_tot);
-    uint32_t base_d = 0, base_t = 0, all_d = tot_d, all_t = tot_t;
-    if (csz > 1) {
-        if (tid == 0) {
-            totals[0] = tot_d;
-            totals[1] = tot_t;
-        }
-        cluster.sync();
-        all_d = all_t = 0;
-        for (int c = 0; c < csz; ++c) {
-            const uint32_t* tt = cluster.map_shared_rank(totals, c);
-            const uint32_t a = tt[0], b = tt[1];
-            if (c < qr) {
-                base_d += a;
-                base_t += b;
-            }
-            all_d += a;
-            all_t += b;
-        }
-    }
-    uint32_t tie_rank = base_t + ex_t;
-    uint32_t pos = base_d + ex_d + min(tie_rank, need_T);
-    for (unsigned long long mm = mdef | mtie; mm; mm &= mm - 1) {
-        const int b = __ffsll((long long)mm) - 1;
-        if ((mdef >> b) & 1ull) {
-            out[pos++] = base + lo + b;
-        } else {
-            if (tie_rank < need_T) out[pos++] = base + lo + b;
-            ++tie_rank;
-        }
-    }
-    const uint32_t total = all_d + min(all_t, need_T);
-    if (qr == csz - 1) {
-        for (int i = (int)total + tid; i < k; i += kTopkThreads) out[i] = -1;
-        if (tid == 0 && total != (uint32_t)k) report(status, DSA_ERR_DEVICE_FAULT);
-    }
-    if (csz > 1) cluster.sync();  // no CTA leaves while another may still read its shared memory
-}
-
-// ---------------------------------------------------------------------------------------------
-// Rows of up to 16,384 scores: one CTA per row, the row in registers.  Thread t holds the VPT
-// consecutive scores [t VPT, t VPT + VPT), so the ordered compaction is one block scan of per-thread
-// counts.  Same decisions as above (max / min, value buckets, direct ranking of a small bucket or a
-// radix select inside a crowded one), without distributed shared memory or a staged copy of the row.
-// ---------------------------------------------------------------------------------------------
+// Block-wide scan and bin selection for a block of THREADS threads (kBins / THREADS bins each).
 template <int THREADS>
 struct RegScan {
     static constexpr int kWarps = THREADS / 32;
@@ -474,6 +119,354 @@ struct RegScan {
     }
 };
 
+// The cluster-wide histogram: hist itself when the cluster is one CTA, else hsum[b] = the sum of the
+// CTAs' hist[b].  Starts and ends with a barrier.
+__device__ __forceinline__ const uint32_t* cluster_hist_sum(cg::cluster_group& cluster, int csz, uint32_t* hist,
+                                                            uint32_t* hsum) {
+    if (csz == 1) {
+        __syncthreads();
+        return hist;
+    }
+    cluster.sync();  // every CTA's local histogram is complete
+    uint32_t* remote[kTopkClusterMax];
+#pragma unroll
+    for (int c = 0; c < kTopkClusterMax; ++c) remote[c] = cluster.map_shared_rank(hist, c < csz ? c : 0);
+    for (int b = threadIdx.x; b < kBins; b += kTopkThreads) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int c = 0; c < kTopkClusterMax; ++c)
+            if (c < csz) v += remote[c][b];
+        hsum[b] = v;
+    }
+    __syncthreads();
+    return hsum;
+}
+
+// Scores [i, i + 4) of a part as a float4; entries at or past `mq` read as -inf (no access).
+__device__ __forceinline__ float4 load_part4(const float* p, int i, int mq) {
+    if (i + 4 <= mq) return *reinterpret_cast<const float4*>(p + i);
+    float4 q;
+    q.x = i < mq ? p[i] : -INFINITY;
+    q.y = i + 1 < mq ? p[i + 1] : -INFINITY;
+    q.z = i + 2 < mq ? p[i + 2] : -INFINITY;
+    q.w = -INFINITY;  // i + 3 >= mq here
+    return q;
+}
+
+__global__ void __launch_bounds__(kTopkThreads, 2)
+    topk_kernel(const float* __restrict__ scores, int ld, const int32_t* __restrict__ n_valid, int k,
+                int32_t* __restrict__ idx_out, int32_t* status, int nq, int ahead) {
+    using SC = RegScan<kTopkThreads>;
+    pdl_wait();
+    pdl_launch_dependents();
+    cg::cluster_group cluster = cg::this_cluster();
+    extern __shared__ __align__(16) uint32_t smem_topk[];
+    uint32_t* hist = smem_topk;                                      // [kBins] this CTA's histogram
+    uint32_t* hsum = hist + kBins;                                   // [kBins] cluster-wide histogram (C > 1)
+    uint32_t* cand_key = hsum + kBins;                               // [kRankMax] this CTA's members of b*
+    uint32_t* cand_idx = cand_key + kRankMax;                        // [kRankMax] their row indices
+    uint32_t* marks = cand_idx + kRankMax;                           // [kMarkWords] ranked winners (local index)
+    uint16_t* bins = reinterpret_cast<uint16_t*>(marks + kMarkWords);  // [part] bucket of each score
+    __shared__ uint32_t n_cand;
+    __shared__ uint32_t wt[32][2];
+    __shared__ uint32_t sel[2];
+    __shared__ float red[2][kTopkThreads / 32];
+    __shared__ float red_c[2];
+    __shared__ uint32_t totals[2];
+    __shared__ uint32_t wcnt[kTopkWarps][2];
+
+    const int csz = (int)cluster.num_blocks();
+    // barrier over the cluster, or over the block when the cluster is one CTA
+    auto csync = [&]() {
+        if (csz > 1) cluster.sync();
+        else __syncthreads();
+    };
+    const int row = blockIdx.x / csz;
+    const int qr = (int)cluster.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    int32_t* out = idx_out + (long long)row * k;
+    const int n = n_valid[row];  // the same for the whole cluster: every branch below is cluster-uniform
+    if (n < 0 || n > ld) {
+        if (qr == 0) {
+            if (tid == 0) report(status, DSA_ERR_DEVICE_FAULT);
+            for (int i = tid; i < k; i += kTopkThreads) out[i] = -1;
+        }
+        return;
+    }
+    if (n <= k) {
+        if (qr == 0)
+            for (int i = tid; i < k; i += kTopkThreads) out[i] = i < n ? i : -1;
+        return;
+    }
+    const int chunk = ((n + csz - 1) / csz + 3) & ~3;  // multiple of 4: aligned float4 loads
+    const int base = qr * chunk;
+    const int mq = max(0, min(n, base + chunk) - base);  // scores in this CTA's part
+    const float* s = scores + (long long)row * ld + base;
+    // the row `ahead` rows on (likely the next one this SM slot takes) into L2, in 16 KB pieces
+    if (wid == 0 && row + ahead < nq) {
+        const int pc = ((ld + csz - 1) / csz + 3) & ~3;  // its part, bounded by the row's width
+        const int pb = min(ld, qr * pc), pe = min(ld, pb + pc);
+        const char* src = reinterpret_cast<const char*>(scores + (long long)(row + ahead) * ld + pb);
+        const int bytes = (pe - pb) * 4;
+        for (int off = lane * 16384; off < bytes; off += 32 * 16384)
+            prefetch_l2(src + off, (uint32_t)min(16384, bytes - off));
+    }
+
+    // 1. max / min of the finite scores of the part (eight float4 loads in flight per thread), then the
+    // block's and the cluster's
+    float mx = -INFINITY, mn = INFINITY;
+    for (int i0 = tid * 4; i0 < mq; i0 += kTopkThreads * 32) {
+        float4 q[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) q[u] = load_part4(s, i0 + u * kTopkThreads * 4, mq);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float v[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                mx = fmaxf(mx, v[e]);  // -inf never raises the maximum
+                mn = fminf(mn, v[e] == -INFINITY ? INFINITY : v[e]);
+            }
+        }
+    }
+    for (int b = tid; b < kBins; b += kTopkThreads) hist[b] = 0;
+    for (int w = tid; w <= (mq >> 5); w += kTopkThreads) marks[w] = 0;
+    if (tid == 0) n_cand = 0;
+    mx = warp_max(mx);
+    mn = -warp_max(-mn);
+    if (lane == 0) {
+        red[0][wid] = mx;
+        red[1][wid] = mn;
+    }
+    __syncthreads();
+    mx = -INFINITY;
+    mn = INFINITY;
+#pragma unroll
+    for (int w = 0; w < kTopkThreads / 32; ++w) {
+        mx = fmaxf(mx, red[0][w]);
+        mn = fminf(mn, red[1][w]);
+    }
+    if (csz > 1) {
+        if (tid == 0) {
+            red_c[0] = mx;
+            red_c[1] = mn;
+        }
+        cluster.sync();
+        mx = -INFINITY;
+        mn = INFINITY;
+        for (int c = 0; c < csz; ++c) {
+            const float* rr = cluster.map_shared_rank(red_c, c);
+            mx = fmaxf(mx, rr[0]);
+            mn = fminf(mn, rr[1]);
+        }
+    }
+    const bool any_finite = mx != -INFINITY;
+    float scale = (any_finite && mx > mn) ? 2046.f / (mx - mn) : 0.f;
+    if (!isfinite(scale)) scale = 0.f;  // degenerate range: one bucket, resolved by the radix passes
+    // bin(v) = 2047 - round(min(2046, (mx - v) * scale)), rounded by adding 2^23 (full-rate arithmetic):
+    // monotone (a larger score never lands in a lower bin, equal scores share one); -inf (and NaN
+    // products) land in bin 1, the lowest bin of finite scores, where the exact keys order them last.
+    // Bin 0 marks the padding past the part.
+    auto bin_of = [&](float v) -> uint32_t {
+        const float t = fminf(2046.f, (mx - v) * scale);
+        return (2047u + 0x4B000000u) - __float_as_uint(t + 8388608.f);
+    };
+
+    // 2. second read of the part (from L2): 16-bit bins into shared memory, local histogram, the
+    // cluster-wide sum and the bucket of the k-th largest score
+    for (int i0 = tid * 4; i0 < mq; i0 += kTopkThreads * 32) {
+        float4 q[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) q[u] = load_part4(s, i0 + u * kTopkThreads * 4, mq);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * kTopkThreads * 4;
+            if (i >= mq) break;
+            uint32_t b0 = bin_of(q[u].x), b1 = bin_of(q[u].y), b2 = bin_of(q[u].z), b3 = bin_of(q[u].w);
+            if (i + 4 <= mq) {
+                atomicAdd(&hist[b0], 1u);
+                atomicAdd(&hist[b1], 1u);
+                atomicAdd(&hist[b2], 1u);
+                atomicAdd(&hist[b3], 1u);
+            } else {  // the part's last, partial vector
+                b1 = i + 1 < mq ? b1 : 0u;
+                b2 = i + 2 < mq ? b2 : 0u;
+                b3 = 0u;
+                atomicAdd(&hist[b0], 1u);
+                if (b1) atomicAdd(&hist[b1], 1u);
+                if (b2) atomicAdd(&hist[b2], 1u);
+            }
+            *reinterpret_cast<uint2*>(bins + i) = make_uint2(b0 | (b1 << 16), b2 | (b3 << 16));
+        }
+    }
+    const uint32_t* hs = cluster_hist_sum(cluster, csz, hist, hsum);
+    uint32_t need = (uint32_t)k;
+    const uint32_t bstar = SC::select(hs, need, wt, sel);
+    const uint32_t in_bucket = hs[bstar];
+    const bool take_all = in_bucket == need;
+    const bool rank_mode = !take_all && in_bucket <= (uint32_t)kRankMax;
+
+    // 3. heavy ties: radix select inside b* (exact scores read again) for the threshold key T and the
+    // entries equal to T still needed
+    uint32_t T = 0u, need_T = 0u;
+    if (!take_all && !rank_mode) {
+        need_T = need;
+        uint32_t prefix = 0u, mask = 0u;
+        for (int pass = 0; pass < 3; ++pass) {
+            const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+            const uint32_t dm = pass == 2 ? 0x3FFu : 0x7FFu;
+            csync();  // the other CTAs (and the selection) are done reading this CTA's previous histogram
+            for (int b = tid; b < kBins; b += kTopkThreads) hist[b] = 0;
+            __syncthreads();
+            for (int i = tid; i < mq; i += kTopkThreads)
+                if (bins[i] == bstar) {
+                    const uint32_t key = order_key(s[i]);
+                    if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
+                }
+            const uint32_t* hp = cluster_hist_sum(cluster, csz, hist, hsum);
+            const uint32_t d = SC::select(hp, need_T, wt, sel);
+            prefix |= d << sh;
+            mask |= dm << sh;
+        }
+        T = prefix;
+    }
+
+    // 4. warp w owns the contiguous segment [w seg, (w + 1) seg) of the part, lane l its indices
+    // l, l + 32, ...; pass one counts what the warp takes (scores above b*, members of b* taken whole,
+    // ranked later, or split at T) and lists the members of a small b*
+    const int seg = ((mq + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
+    const int w0 = min(mq, wid * seg), w1 = min(mq, w0 + seg);
+    uint32_t cnt_d = 0, cnt_t = 0;
+    for (int i = w0 + lane; i < w1; i += 32) {
+        const uint32_t b = bins[i];
+        cnt_d += b > bstar;
+        if (b == bstar) {  // rare
+            if (take_all) {
+                ++cnt_d;
+            } else if (rank_mode) {
+                const uint32_t slot = atomicAdd(&n_cand, 1u);  // at most kRankMax over the cluster
+                cand_key[slot] = order_key(s[i]);
+                cand_idx[slot] = (uint32_t)(base + i);
+            } else {
+                const uint32_t key = order_key(s[i]);
+                cnt_d += key > T;
+                cnt_t += key == T;
+            }
+        }
+    }
+    cnt_d = __reduce_add_sync(0xffffffffu, cnt_d);
+    cnt_t = __reduce_add_sync(0xffffffffu, cnt_t);
+    if (lane == 0) {
+        wcnt[wid][0] = cnt_d;
+        wcnt[wid][1] = cnt_t;
+    }
+    // 5. small bucket: each listed member counts the better ones (larger score, or equal score and
+    // lower index) across the cluster; the `need` best are marked and counted in their warp
+    if (rank_mode) {
+        csync();  // every CTA's member list is complete
+        if (tid < (int)n_cand) {
+            const uint32_t my_k = cand_key[tid], my_i = cand_idx[tid];
+            uint32_t better = 0;
+#pragma unroll 1
+            for (int c = 0; c < csz; ++c) {
+                const uint32_t* rk = csz > 1 ? cluster.map_shared_rank(cand_key, c) : cand_key;
+                const uint32_t* ri = csz > 1 ? cluster.map_shared_rank(cand_idx, c) : cand_idx;
+                const int nc = csz > 1 ? (int)*cluster.map_shared_rank(&n_cand, c) : (int)n_cand;
+                for (int j = 0; j < nc; ++j) {
+                    const uint32_t kj = rk[j];
+                    better += (kj > my_k) || (kj == my_k && ri[j] < my_i);
+                }
+            }
+            if (better < need) {
+                const uint32_t li = my_i - (uint32_t)base;
+                atomicOr(&marks[li >> 5], 1u << (li & 31));
+                atomicAdd(&wcnt[li / seg][0], 1u);
+            }
+        }
+    }
+    __syncthreads();
+    // 6. ordered output: warp totals scanned (then the lower CTAs' totals added) give each warp its first
+    // slot; pass two walks the segment again in index order, a ballot placing each taken index.
+    // Entries equal to T are ranked by index: the lowest `need_T` win.
+    if (wid == 0) {
+        uint32_t d = lane < kTopkWarps ? wcnt[lane][0] : 0u, t = lane < kTopkWarps ? wcnt[lane][1] : 0u;
+        uint32_t id = d, it = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t a = __shfl_up_sync(0xffffffffu, id, o), b = __shfl_up_sync(0xffffffffu, it, o);
+            if (lane >= o) {
+                id += a;
+                it += b;
+            }
+        }
+        if (lane < kTopkWarps) {
+            wcnt[lane][0] = id - d;  // exclusive
+            wcnt[lane][1] = it - t;
+        }
+        if (lane == 31) {
+            totals[0] = id;
+            totals[1] = it;
+        }
+    }
+    __syncthreads();
+    uint32_t base_d = 0, base_t = 0, all_d = totals[0], all_t = totals[1];
+    if (csz > 1) {
+        cluster.sync();
+        all_d = all_t = 0;
+        for (int c = 0; c < csz; ++c) {
+            const uint32_t* tt = cluster.map_shared_rank(totals, c);
+            const uint32_t a = tt[0], b = tt[1];
+            if (c < qr) {
+                base_d += a;
+                base_t += b;
+            }
+            all_d += a;
+            all_t += b;
+        }
+    }
+    uint32_t run_d = base_d + wcnt[wid][0], run_t = base_t + wcnt[wid][1];  // taken before this iteration
+    const uint32_t lt = (1u << lane) - 1u;
+    const bool split = !take_all && !rank_mode;
+    for (int i0 = w0; i0 < w1; i0 += 32) {  // warp-uniform trip count
+        const int i = i0 + lane;
+        bool d = false, t = false;
+        if (i < w1) {
+            const uint32_t b = bins[i];
+            d = b > bstar;
+            if (b == bstar) {  // rare
+                if (take_all) d = true;
+                else if (rank_mode) d = (marks[i >> 5] >> (i & 31)) & 1u;
+                else {
+                    const uint32_t key = order_key(s[i]);
+                    d = key > T;
+                    t = key == T;
+                }
+            }
+        }
+        const uint32_t bd = __ballot_sync(0xffffffffu, d);
+        const uint32_t bt = split ? __ballot_sync(0xffffffffu, t) : 0u;
+        if (d | t) {
+            const uint32_t nd = run_d + __popc(bd & lt), nt = run_t + __popc(bt & lt);
+            if (d) out[nd + min(nt, need_T)] = base + i;
+            else if (nt < need_T) out[nd + nt] = base + i;
+        }
+        run_d += __popc(bd);
+        run_t += __popc(bt);
+    }
+    const uint32_t total = all_d + min(all_t, need_T);
+    if (qr == csz - 1) {
+        for (int i = (int)total + tid; i < k; i += kTopkThreads) out[i] = -1;
+        if (tid == 0 && total != (uint32_t)k) report(status, DSA_ERR_DEVICE_FAULT);
+    }
+    if (csz > 1) cluster.sync();  // no CTA leaves while another may still read its shared memory
+}
+
+// ---------------------------------------------------------------------------------------------
+// Rows of up to 16,384 scores: one CTA per row, the row in registers.  Thread t holds the VPT
+// consecutive scores [t VPT, t VPT + VPT), so the ordered compaction is one block scan of per-thread
+// counts.  Same decisions as above (max / min, value buckets, direct ranking of a small bucket or a
+// radix select inside a crowded one), without distributed shared memory or a staged copy of the row.
+// ---------------------------------------------------------------------------------------------
 template <int THREADS, int VPT>
 __global__ void __launch_bounds__(THREADS, 1)
     topk_reg_kernel(const float* __restrict__ scores, int ld, const int32_t* __restrict__ n_valid, int k,
@@ -679,15 +672,16 @@ extern "C" dsa_status_t dsa_topk(int32_t nq, const float* scores, int32_t ld, co
                                          k, idx_out, dev_status);
         return e == cudaSuccess ? launch_status() : DSA_ERR_CUDA;
     }
-    const int csz = ld <= kQuarterMax ? 1 : kTopkClusterMax;
+    const int csz = ld <= kPartMax ? 1 : (ld <= 2 * kPartMax ? 2 : kTopkClusterMax);
     const int chunk = ((ld + csz - 1) / csz + 3) & ~3;
-    if (chunk > kQuarterMax) return DSA_ERR_UNSUPPORTED;
+    if (chunk > kPartMax) return DSA_ERR_UNSUPPORTED;
     const size_t smem = (size_t)(2 * kBins + 2 * kRankMax + kMarkWords) * sizeof(uint32_t) +
-                        (size_t)chunk * sizeof(float);
+                        ((size_t)chunk * sizeof(uint16_t) + 15) / 16 * 16;
     if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DSA_ERR_CUDA;
+    const int ahead = std::max(1, 2 * sm_count() / csz);  // clusters resident at once (two CTAs per SM)
     if (launch_pdl_cluster(topk_kernel, dim3(nq * csz), dim3(kTopkThreads), smem, st, csz, scores, ld, n_valid, k,
-                           idx_out, dev_status) != cudaSuccess)
+                           idx_out, dev_status, nq, ahead) != cudaSuccess)
         return DSA_ERR_CUDA;
     return launch_status();
 }
