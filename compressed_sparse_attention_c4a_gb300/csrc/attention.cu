@@ -39,7 +39,7 @@ struct AttnArgs {
     uint16_t* out;
     float* lse;
     float* ws_o;                              // [rows][nsplit][heads][512]
-    float* ws_ml;                             // [rows][nsplit][heads][2]
+    float* ws_ml;                             // [rows][nsplit][heads][4]: M, L (bf16 P), E (fp32 P), 0
     int32_t* status;
 };
 
@@ -49,6 +49,7 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_but_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return (uint32_t)float_to_bf16(lo) | ((uint32_t)float_to_bf16(hi) << 16);
 }
@@ -61,15 +62,16 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
     const int tid = threadIdx.x;
     float M = -INFINITY;
     for (int sp = 0; sp < a.nsplit; ++sp)
-        M = fmaxf(M, a.ws_ml[(((long long)row * a.nsplit + sp) * a.heads + head) * 2]);
+        M = fmaxf(M, a.ws_ml[(((long long)row * a.nsplit + sp) * a.heads + head) * 4]);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float Ls = 0.f;
+    float Ls = 0.f, Es = 0.f;
     for (int sp = 0; sp < a.nsplit; ++sp) {
         const long long b = ((long long)row * a.nsplit + sp) * a.heads + head;
-        const float ms = a.ws_ml[b * 2], ls = a.ws_ml[b * 2 + 1];
+        const float ms = a.ws_ml[b * 4], ls = a.ws_ml[b * 4 + 1], es = a.ws_ml[b * 4 + 2];
         if (ms == -INFINITY) continue;
         const float f = exp2f(ms - M);
         Ls += f * ls;
+        Es += f * es;
         const float4 v = *reinterpret_cast<const float4*>(a.ws_o + b * kD + tid * 4);
         acc[0] += f * v.x;
         acc[1] += f * v.y;
@@ -95,32 +97,33 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
     uint16_t* dst = a.out + ((long long)row * a.heads + head) * kD + tid * 4;
     *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
     if (a.lse && tid == 0)
-        a.lse[(long long)row * a.heads + head] = Ls > 0.f ? (M + log2f(Ls)) / kLog2e : -INFINITY;
+        a.lse[(long long)row * a.heads + head] = Es > 0.f ? (M + log2f(Es)) / kLog2e : -INFINITY;
 }
 
 // ---------------------------------------------------------------------------------------------
 // bf16 rows on the 5th-generation tensor cores (tcgen05, TMEM accumulators).
 //
-// Work split.  A row's keys (top-k entries, then window positions) form 64-key sub-tiles.  One
+// Work split.  A row's keys (top-k entries, then window positions) form 32-key sub-tiles.  One
 // cluster of CL CTAs (CL = 1, 2 or 4, chosen at launch) serves one (query row, group of NH <= 64 heads,
 // key split); CTA c of the cluster takes the split's sub-tiles c, c + CL, c + 2 CL, ...  Each CTA keeps
 // its partial softmax state on chip, and the cluster merges the CL partials through distributed
 // shared memory, so a split-K workspace in global memory is needed only when one cluster per row is
 // not enough to fill the GPU (several splits per row, merged by attn_combine_kernel).
 //
-// Inside a CTA (288 threads), warp-specialised and pipelined over two 64 KB key stages:
-//   warps 4-7  gather: resolve the sub-tile's keys (top-k index -> block table -> physical row, one
-//              sub-tile ahead) and copy the rows into a stage with cp.async, 128B-swizzled,
-//              laid out [64-dim chunk][8-key group][8 keys][128 B] (the query rows are copied with
-//              the first sub-tile into the same layout, padded with zero rows to 64);
-//   warp 8     issues the MMAs (one thread):
-//              S   = Q K^T   : M = 64 (heads), N = 64 keys, K = 512; TMEM lanes = heads, columns = keys;
+// Inside a CTA (512 threads), warp-specialised and pipelined over four 32 KB key stages (a stage is
+// gathered again as soon as its sub-tile's P V is done, so up to three gathers run ahead of the math):
+//   warps 5-15 gather: resolve keys a round (11 sub-tiles) ahead (top-k index -> block table ->
+//              physical row, tables cached in shared memory), prefetch later rounds into L2, and copy
+//              the rows into a stage with cp.async, 128B-swizzled, laid out [64-dim chunk][32 keys]
+//              [128 B]; e4m3 rows are converted to bf16 on the way, their scales kept beside the stage;
+//   warp 4     loads the query rows (TMA, one 64-dim box per lane) and issues the MMAs (one elected lane):
+//              S   = Q K^T   : M = 64 (heads), N = 32 keys, K = 512; TMEM lanes = heads, columns = keys;
 //              O^T += V^T P^T: M = 128 dims per MMA (the stage read MN-major, K = V), N = NH heads,
-//                              K = 64 keys; four 128-dim accumulators, lanes = dims, columns = heads;
+//                              K = 32 keys; four 128-dim accumulators, lanes = dims, columns = heads;
 //              S of sub-tile i + 1 is issued before O^T of sub-tile i, so it overlaps the softmax;
 //   warps 0-3  softmax, one thread per head (lanes 0-15 of each quadrant hold the M = 64 rows): the
-//              64 logits of a sub-tile are a row of TMEM, so max and sum are thread-local; P is
-//              written as the head's 128-byte row of the P^T operand.  The running maximum is
+//              32 logits of a sub-tile are a row of TMEM, so max and sum are thread-local; P is
+//              written as the head's row of the P^T operand (two buffers).  The running maximum is
 //              lazy: it moves (and O^T is rescaled in TMEM) only when a sub-tile's maximum exceeds it
 //              by more than 2^8, so exp2(s - m) <= 2^8 stays exact in fp32 and rescales are rare.
 // Merge: each CTA sends (m, l) per head to every CTA of the cluster, then scales its O^T by
@@ -129,40 +132,43 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
 // divides by L and applies R_m^-1 (pairs of dims sit in neighbouring lanes) before the bf16 store,
 // or writes an fp32 partial with (M, L) when the row has several splits.
 // ---------------------------------------------------------------------------------------------
-constexpr int kClKeys = 64;                 // keys per sub-tile
+constexpr int kClKeys = 32;                 // keys per sub-tile
+constexpr int kClStages = 4;                // key stages in flight (a stage is free again after its P V)
 constexpr int kClGatherWarps = 11;          // warps 5 .. 15
 constexpr int kClThreads = 32 * (5 + kClGatherWarps);
 constexpr int kClGatherThreads = 32 * kClGatherWarps;
-constexpr int kClRound = kClGatherThreads / kClKeys;   // sub-tiles resolved per round (5)
-constexpr int kClRing = 2 * kClRound;                  // resolved sub-tiles kept (a ring of 10)
+constexpr int kClRound = kClGatherThreads / kClKeys;   // sub-tiles resolved per round (11)
+constexpr int kClRing = 2 * kClRound;                  // resolved sub-tiles kept (a ring of 22)
 constexpr int kClStage = kClKeys * kD * 2;
+static_assert(kClKeys == 32, "one 32-bit key mask and 32 S columns per sub-tile");
 constexpr float kLazyLog2 = 8.f;            // the running maximum moves when exceeded by more than this
 constexpr int kBtCache = 1024;              // main block tables up to this many blocks are cached in shared memory
 
 template <int NH>
 struct ClSmem {
     static constexpr int kQ = 64 * kD * 2;                          // [8][64 rows][128 B]
-    static constexpr int kP = NH * kClKeys * 2;                     // [NH rows][128 B]
+    static constexpr int kP = NH * 64 * 2;                          // [NH rows][128 B]: keys 0 .. 31 of 64 used
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kQ;                        // two stages; exchanged tiles at the end
-    static constexpr int kOffP = kOffK + 2 * kClStage;              // two P^T buffers; output staging at the end
-    static constexpr int kOffRow = kOffP + 2 * kP;                  // int [ring][64]: physical rows (-1 masked)
-    static constexpr int kOffPool = kOffRow + kClRing * kClKeys * 4;  // uint8 [ring][64]: 1 main, 2 window
-    static constexpr int kOffKsc = kOffPool + kClRing * kClKeys;    // float [2][64]: e4m3 row scales of a stage
-    static constexpr int kOffMask = kOffKsc + 2 * kClKeys * 4;      // uint32 [2][2]: valid keys of a stage
-    static constexpr int kOffAlpha = kOffMask + 16;                 // float [2][NH]
+    static constexpr int kOffK = kOffQ + kQ;                        // key stages; exchanged tiles at the end
+    static constexpr int kOffP = kOffK + kClStages * kClStage;      // two P^T buffers; output staging at the end
+    static constexpr int kOffRow = kOffP + 2 * kP;                  // int [ring][32]: physical rows (-1 masked)
+    static constexpr int kOffPool = kOffRow + kClRing * kClKeys * 4;  // uint8 [ring][32]: 1 main, 2 window
+    static constexpr int kOffKsc = kOffPool + kClRing * kClKeys;    // float [stages][32]: e4m3 row scales
+    static constexpr int kOffMask = kOffKsc + kClStages * kClKeys * 4;  // uint32 [stages]: valid keys of a stage
+    static constexpr int kOffAlpha = kOffMask + kClStages * 4;      // float [2][NH]
     static constexpr int kOffVote = kOffAlpha + 2 * NH * 4;         // int [2][4]
-    static constexpr int kOffOwn = kOffVote + 32;                   // float m[NH], l[NH] of this CTA
-    static constexpr int kOffStat = kOffOwn + 2 * NH * 4;           // float [4 ranks][NH][2]: (m, l) of each CTA
-    static constexpr int kOffFac = kOffStat + 4 * NH * 8;           // float f[NH], L[NH], M[NH], 1/L[NH]
-    static constexpr int kOffBt = kOffFac + 4 * NH * 4;             // int [kBtCache]: the request's main block table
+    static constexpr int kOffOwn = kOffVote + 32;                   // float m[NH], l[NH], e[NH] of this CTA
+    static constexpr int kOffStat = kOffOwn + 3 * NH * 4;           // float [4 ranks][NH][4]: (m, l, e, 0) of each CTA
+    static constexpr int kOffFac = kOffStat + 4 * NH * 16;          // float f[NH], L[NH], M[NH], 1/L[NH], E[NH]
+    static constexpr int kOffBt = kOffFac + 5 * NH * 4;             // int [kBtCache]: the request's main block table
     static constexpr int kOffSwb = kOffBt + kBtCache * 4;           // int [8]: window-pool blocks from that of wlo
-    static constexpr int kOffBar = kOffSwb + 32;                    // 10 mbarriers, TMEM address
-    static constexpr int kBytes = kOffBar + 10 * 8 + 16;
+    static constexpr int kBars = 2 * kClStages + 6;
+    static constexpr int kOffBar = kOffSwb + 32;                    // kBars mbarriers, TMEM address
+    static constexpr int kBytes = kOffBar + kBars * 8 + 16;
     static constexpr int kAlloc = kBytes + 1024;                    // + alignment slack
     static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
     static constexpr int kTile = 128 * NH * 2;                      // one exchanged 128-dim O tile: [NH / 4][128] x 4 bf16
-    static_assert(6 * kTile <= kQ + 2 * kClStage, "sent and received tiles must fit in the query rows and stages");
+    static_assert(6 * kTile <= kQ + kClStages * kClStage, "sent and received tiles must fit in the query rows and stages");
     static_assert(NH * 128 * 2 <= 2 * kP, "an output tile must fit in the P^T buffers");
     static constexpr int kTmemCols = 128 + 4 * NH <= 256 ? 256 : 512;
 };
@@ -197,13 +203,15 @@ __global__ void __launch_bounds__(kClThreads, 1)
     float* s_L = s_fac + NH;
     float* s_M = s_L + NH;
     float* s_inv = s_M + NH;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // stage gathered (gather threads)
-    uint64_t* sfull = full + 2;                                         // S in TMEM (MMA commit)
-    uint64_t* pfull = full + 4;                                         // P^T written (4 warps)
-    uint64_t* pvdone = full + 6;                                        // O^T += V^T P^T done (commit)
-    uint64_t* qfull = full + 8;                                         // query rows loaded
-    uint64_t* xfull = full + 9;                                         // exchanged tiles loaded
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(full + 10);
+    float* s_E = s_inv + NH;
+    // sub-tile i: key stage i % kClStages; S columns, P^T buffer and softmax scratch i & 1
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // [stages] stage gathered (gather threads)
+    uint64_t* sfull = full + kClStages;                                 // [2] S in TMEM (MMA commit)
+    uint64_t* pfull = sfull + 2;                                        // [2] P^T written (4 warps)
+    uint64_t* pvdone = pfull + 2;                                       // [stages] O^T += V^T P^T done (commit)
+    uint64_t* qfull = pvdone + kClStages;                               // query rows loaded
+    uint64_t* xfull = qfull + 1;                                        // exchanged tiles loaded
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(xfull + 1);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int crank = (int)cluster_ctarank(), csize = (int)cluster_nctarank();
@@ -212,11 +220,13 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const int hg = (cid / a.nsplit) % a.hg_count;
     const int row = cid / (a.nsplit * a.hg_count);
     if (tid == 0) {
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kClStages; ++b) {
             mbar_init(&full[b], kClGatherThreads);
+            mbar_init(&pvdone[b], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
             mbar_init(&sfull[b], 1);
             mbar_init(&pfull[b], 4);
-            mbar_init(&pvdone[b], 1);
         }
         mbar_init(qfull, 1);
         mbar_init(xfull, 1);
@@ -261,19 +271,19 @@ __global__ void __launch_bounds__(kClThreads, 1)
         const bool bt_cached = a.main_bt.max_blocks <= kBtCache;
         int* s_bt = reinterpret_cast<int*>(smem + L::kOffBt);
         int* s_swb = reinterpret_cast<int*>(smem + L::kOffSwb);
-        // sub-tiles [R * kClRound, (R + 1) * kClRound): thread -> sub-tile R * kClRound + gt / 64, key gt % 64.
+        // sub-tiles [R * kClRound, (R + 1) * kClRound): thread -> sub-tile R * kClRound + gt / 32, key gt % 32.
         // Step 1: the key's top-k index (or entry / window position), no dependent load.
         auto key_id = [&](int R, int* id) -> int {  // returns j (the key's index in the row), -1 if none
-            const int i = R * kClRound + (gt >> 6);
+            const int i = R * kClRound + gt / kClKeys;
             if (gt >= kClRound * kClKeys || i >= n_mine) return -1;
-            const int j = (g_lo + crank + csize * i) * kClKeys + (gt & 63);
+            const int j = (g_lo + crank + csize * i) * kClKeys + gt % kClKeys;
             *id = -1;
             if (j < n_keys && j < n_comp) *id = a.topk ? __ldg(a.topk + (long long)row * a.k + j) : j;
             return j;
         };
         // Step 2: index -> physical row through the cached tables (or global memory), L2 prefetch, ring slot.
         auto finish_key = [&](int R, int j, int id) {
-            const int i = R * kClRound + (gt >> 6);
+            const int i = R * kClRound + gt / kClKeys;
             if (j < 0) return;
             int v = -1, pool = 1;
             if (j < ncp) {
@@ -304,8 +314,8 @@ __global__ void __launch_bounds__(kClThreads, 1)
                                                 : static_cast<const uint8_t*>(a.main.data);
                 prefetch_l2(base + (long long)v * kRowBytes, kRowBytes);
             }
-            s_row[(i % kClRing) * kClKeys + (gt & 63)] = v;
-            s_pool[(i % kClRing) * kClKeys + (gt & 63)] = (uint8_t)pool;
+            s_row[(i % kClRing) * kClKeys + gt % kClKeys] = v;
+            s_pool[(i % kClRing) * kClKeys + gt % kClKeys] = (uint8_t)pool;
         };
         auto resolve_round = [&](int R) {
             int id = -1;
@@ -328,14 +338,15 @@ __global__ void __launch_bounds__(kClThreads, 1)
             finish_key(0, j0, id0);
         }
         for (int i = 0; i < n_mine; ++i) {
-            const int s = i & 1;
-            if (i >= 2) ok = ok && mbar_wait_bounded(&pvdone[s], ((i - 2) >> 1) & 1, kWaitLimitNs);
+            const int s = i % kClStages;
+            if (i >= kClStages)  // the stage's previous sub-tile has been multiplied into O^T
+                ok = ok && mbar_wait_bounded(&pvdone[s], ((i - kClStages) / kClStages) & 1, kWaitLimitNs);
             named_bar_sync(1, kClGatherThreads);  // sub-tile i's rows are visible; earlier gathers are done
             const int* rows = s_row + (i % kClRing) * kClKeys;
             const uint8_t* pools = s_pool + (i % kClRing) * kClKeys;
-            if (gt < kClKeys) {  // warps 5 and 6: the stage's key mask for the softmax
+            if (gt < kClKeys) {  // warp 5: the stage's key mask for the softmax
                 const uint32_t bits = __ballot_sync(0xffffffffu, rows[gt] >= 0);
-                if (lane == 0) s_mask[s * 2 + gw] = bits;
+                if (lane == 0) s_mask[s] = bits;
             }
             if (ok && !FP8) {
                 const uint32_t stage = sK + s * kClStage;
@@ -418,9 +429,21 @@ __global__ void __launch_bounds__(kClThreads, 1)
             // the next round of keys once this one's second sub-tile is under way: its rows reach L2 while
             // the sub-tiles in between are processed (ring slots of sub-tiles < i are free by now)
             if (i % kClRound == 2) resolve_round(i / kClRound + 1);
+            // a thread keeps two sub-tiles of copies in flight: sub-tile i - 1 is reported once its group
+            // (the one before sub-tile i's) has landed.  Its stage's consumers never wait on sub-tile i.
+            if constexpr (FP8) {  // this thread's converted rows are in the stage
+                fence_proxy_async_smem();
+                mbar_arrive(&full[s]);
+            } else if (i > 0) {
+                cp_async_wait_but_one();
+                fence_proxy_async_smem();  // cp.async writes -> visible to the tensor core (async proxy)
+                mbar_arrive(&full[(i - 1) % kClStages]);
+            }
+        }
+        if (!FP8 && n_mine > 0) {  // the last sub-tile
             cp_async_wait_all();
-            fence_proxy_async_smem();  // cp.async writes -> visible to the tensor core (async proxy)
-            mbar_arrive(&full[s]);
+            fence_proxy_async_smem();
+            mbar_arrive(&full[(n_mine - 1) % kClStages]);
         }
         if (!ok) report(a.status, DSA_ERR_TIMEOUT);
     } else if (warp == 4) {
@@ -441,21 +464,22 @@ __global__ void __launch_bounds__(kClThreads, 1)
             ok = mbar_wait_bounded(qfull, 0, kWaitLimitNs);
         }
         auto issue_s = [&](int i) {
-            const int s = i & 1;
+            const int s = i % kClStages;
             tc_fence_after();
             const uint64_t dk = sw128_desc(sK + s * kClStage, 16, 1024);
 #pragma unroll
-            for (int ks = 0; ks < kD / 16; ++ks) {
-                const uint64_t off = (uint64_t)((((ks >> 2) * (64 * 128)) + (ks & 3) * 32) >> 4);
-                mma_bf16_ss_elect(tS + s * kClKeys, dq + off, dk + off, idesc_s, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < kD / 16; ++ks) {  // 64-dim chunks are 64 query rows / 32 key rows apart
+                const uint64_t oq = (uint64_t)((((ks >> 2) * (64 * 128)) + (ks & 3) * 32) >> 4);
+                const uint64_t ok_ = (uint64_t)((((ks >> 2) * (kClKeys * 128)) + (ks & 3) * 32) >> 4);
+                mma_bf16_ss_elect(tS + (i & 1) * kClKeys, dq + oq, dk + ok_, idesc_s, ks > 0 ? 1u : 0u);
             }
-            mma_commit_elect(&sfull[s]);
+            mma_commit_elect(&sfull[i & 1]);
         };
         auto issue_pv = [&](int i) {
-            const int s = i & 1;
+            const int s = i % kClStages;
             tc_fence_after();
             const uint64_t dv = sw128_desc(sK + s * kClStage, kClKeys * 128, 1024);
-            const uint64_t dp = sw128_desc(sP + s * L::kP, 16, 1024);
+            const uint64_t dp = sw128_desc(sP + (i & 1) * L::kP, 16, 1024);
 #pragma unroll
             for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
@@ -474,7 +498,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             bool pv_done = false;
             while (ok && !pv_done) {
                 if (next_s < n_mine && next_s <= i + 1 &&
-                    __all_sync(0xffffffffu, mbar_try_wait(&full[next_s & 1], (next_s >> 1) & 1))) {
+                    __all_sync(0xffffffffu, mbar_try_wait(&full[next_s % kClStages], (next_s / kClStages) & 1))) {
                     issue_s(next_s);
                     ++next_s;
                     continue;
@@ -494,24 +518,31 @@ __global__ void __launch_bounds__(kClThreads, 1)
         const int h = warp * 16 + lane;
         const bool hthread = lane < 16 && h < NH;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        float m_run = -INFINITY, l_run = 0.f;
+        // l: sum of the probabilities as rounded into P^T (the output's normaliser, so a one-hot row stays
+        // exact); e: sum of the fp32 probabilities (the log-sum-exp)
+        float m_run = -INFINITY, l_run = 0.f, e_run = 0.f;
         for (int i = 0; i < n_mine; ++i) {
-            const int s = i & 1;
-            ok = ok && mbar_wait_bounded(&full[s], (i >> 1) & 1, kWaitLimitNs);  // the stage's key mask
+            const int st = i % kClStages, s = i & 1;  // key stage; S columns, P^T buffer and scratch
+            ok = ok && mbar_wait_bounded(&full[st], (i / kClStages) & 1, kWaitLimitNs);  // the stage's key mask
             ok = ok && mbar_wait_bounded(&sfull[s], (i >> 1) & 1, kWaitLimitNs);
-            if (i >= 2) ok = ok && mbar_wait_bounded(&pvdone[s], ((i - 2) >> 1) & 1, kWaitLimitNs);  // P^T buffer free
+            if (i >= 2)  // P^T buffer free: the product of sub-tile i - 2 is done
+                ok = ok && mbar_wait_bounded(&pvdone[(i - 2) % kClStages], ((i - 2) / kClStages) & 1, kWaitLimitNs);
             ok = __all_sync(0xffffffffu, ok);
             float sv[kClKeys];
             float alpha = 1.f;
             bool resc = false;
             if (ok) {
                 tc_fence_after();
-                tmem_ld64(tS + s * kClKeys + lane_off, sv);
-                const uint64_t vm = ((uint64_t)s_mask[s * 2 + 1] << 32) | s_mask[s * 2];
+                tmem_ld_nowait<16>(tS + s * kClKeys + lane_off, *reinterpret_cast<float(*)[16]>(sv));
+                tmem_ld_nowait<16>(tS + s * kClKeys + lane_off + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
+                tmem_wait_ld();
+                tmem_regs_after_wait<16>(*reinterpret_cast<float(*)[16]>(sv));
+                tmem_regs_after_wait<16>(*reinterpret_cast<float(*)[16]>(sv + 16));
+                const uint32_t vm = s_mask[st];
                 float mx = -INFINITY;
 #pragma unroll
                 for (int j = 0; j < kClKeys; ++j) {
-                    const float ls = FP8 ? a.scale_log2 * s_ksc[s * kClKeys + j] : a.scale_log2;  // e4m3: times the row scale
+                    const float ls = FP8 ? a.scale_log2 * s_ksc[st * kClKeys + j] : a.scale_log2;  // e4m3: times the row scale
                     sv[j] = ((vm >> j) & 1) ? sv[j] * ls : -INFINITY;
                     mx = fmaxf(mx, sv[j]);
                 }
@@ -522,7 +553,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 }
                 const float mr = m_run == -INFINITY ? 0.f : m_run;  // all keys so far masked: p = 0
                 const uint32_t prow = sP + s * L::kP + (h >> 3) * 1024 + (h & 7) * 128;
-                float sum = 0.f;
+                float sum = 0.f, esum = 0.f;
 #pragma unroll
                 for (int c = 0; c < kClKeys / 8; ++c) {
                     uint32_t w[4];
@@ -531,11 +562,13 @@ __global__ void __launch_bounds__(kClThreads, 1)
                         if constexpr (FP8) {  // the probability that multiplies the codes carries the row scale
                             const float p0 = exp2f(sv[8 * c + 2 * e] - mr), p1 = exp2f(sv[8 * c + 2 * e + 1] - mr);
                             sum += p0 + p1;
-                            w[e] = pack_bf16(p0 * s_ksc[s * kClKeys + 8 * c + 2 * e], p1 * s_ksc[s * kClKeys + 8 * c + 2 * e + 1]);
+                            esum += p0 + p1;
+                            w[e] = pack_bf16(p0 * s_ksc[st * kClKeys + 8 * c + 2 * e], p1 * s_ksc[st * kClKeys + 8 * c + 2 * e + 1]);
                         } else {
-                            const uint16_t b0 = float_to_bf16(exp2f(sv[8 * c + 2 * e] - mr));
-                            const uint16_t b1 = float_to_bf16(exp2f(sv[8 * c + 2 * e + 1] - mr));
+                            const float p0 = exp2f(sv[8 * c + 2 * e] - mr), p1 = exp2f(sv[8 * c + 2 * e + 1] - mr);
+                            const uint16_t b0 = float_to_bf16(p0), b1 = float_to_bf16(p1);
                             sum += bf16_to_float(b0) + bf16_to_float(b1);
+                            esum += p0 + p1;
                             w[e] = (uint32_t)b0 | ((uint32_t)b1 << 16);
                         }
                     }
@@ -545,6 +578,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
                                      : "memory");
                 }
                 l_run = l_run * alpha + sum;
+                e_run = e_run * alpha + esum;
             }
             if (hthread) s_alpha[s * NH + h] = alpha;
             const bool any = __any_sync(0xffffffffu, resc && hthread);
@@ -552,7 +586,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             named_bar_sync(2, 128);
             if (s_vote[s * 4] | s_vote[s * 4 + 1] | s_vote[s * 4 + 2] | s_vote[s * 4 + 3]) {
                 // a head's maximum moved: O^T (after the previous sub-tile's product) times alpha per head
-                ok = ok && mbar_wait_bounded(&pvdone[(i - 1) & 1], ((i - 1) >> 1) & 1, kWaitLimitNs);
+                ok = ok && mbar_wait_bounded(&pvdone[(i - 1) % kClStages], ((i - 1) / kClStages) & 1, kWaitLimitNs);
                 ok = __all_sync(0xffffffffu, ok);
                 if (ok) {
                     tc_fence_after();
@@ -576,12 +610,13 @@ __global__ void __launch_bounds__(kClThreads, 1)
             if (lane == 0) mbar_arrive(&pfull[s]);
         }
         if (n_mine > 0) {  // the last product must be complete before O^T is read
-            ok = ok && mbar_wait_bounded(&pvdone[(n_mine - 1) & 1], ((n_mine - 1) >> 1) & 1, kWaitLimitNs);
+            ok = ok && mbar_wait_bounded(&pvdone[(n_mine - 1) % kClStages], ((n_mine - 1) / kClStages) & 1, kWaitLimitNs);
             tc_fence_after();
         }
         if (hthread) {
             s_own[h] = m_run;
             s_own[NH + h] = l_run;
+            s_own[2 * NH + h] = e_run;
         }
         if (!ok) report(a.status, DSA_ERR_TIMEOUT);
     }
@@ -610,25 +645,32 @@ __global__ void __launch_bounds__(kClThreads, 1)
     if (csize > 1 && tid == 0)  // before any peer can push (pushes follow phase 1)
         mbar_arrive_expect_tx(xfull, (uint32_t)((csize - 1) * tiles_per * L::kTile));
     for (int h = tid; h < NH; h += kClThreads) {
-        const uint32_t dst = smem_u32(s_stat + (crank * NH + h) * 2);
-        const float mo = have ? s_own[h] : -INFINITY, lo = have ? s_own[NH + h] : 0.f;
-        for (int q = 0; q < csize; ++q) st_cluster_v2(mapa_shared(dst, (uint32_t)q), mo, lo);
+        const uint32_t dst = smem_u32(s_stat + (crank * NH + h) * 4);
+        const float mo = have ? s_own[h] : -INFINITY, lo = have ? s_own[NH + h] : 0.f,
+                    eo = have ? s_own[2 * NH + h] : 0.f;
+        for (int q = 0; q < csize; ++q)
+            st_cluster_v4(mapa_shared(dst, (uint32_t)q), mo, lo, eo, 0.f);
     }
     cluster_arrive();  // phase 1: statistics delivered; every CTA's products are complete
     cluster_wait();
     for (int h = tid; h < NH; h += kClThreads) {
         float M = -INFINITY;
-        for (int q = 0; q < csize; ++q) M = fmaxf(M, s_stat[(q * NH + h) * 2]);
-        float Ls = 0.f;
+        for (int q = 0; q < csize; ++q) M = fmaxf(M, s_stat[(q * NH + h) * 4]);
+        float Ls = 0.f, Es = 0.f;
         for (int q = 0; q < csize; ++q) {
-            const float mq = s_stat[(q * NH + h) * 2];
-            if (mq != -INFINITY) Ls += s_stat[(q * NH + h) * 2 + 1] * exp2f(mq - M);
+            const float mq = s_stat[(q * NH + h) * 4];
+            if (mq != -INFINITY) {
+                const float fq = exp2f(mq - M);
+                Ls += s_stat[(q * NH + h) * 4 + 1] * fq;
+                Es += s_stat[(q * NH + h) * 4 + 2] * fq;
+            }
         }
-        const float mo = s_stat[(crank * NH + h) * 2];
+        const float mo = s_stat[(crank * NH + h) * 4];
         s_fac[h] = mo == -INFINITY ? 0.f : exp2f(mo - M);
         s_L[h] = Ls;
         s_M[h] = M;
         s_inv[h] = Ls > 0.f ? 1.f / Ls : 0.f;
+        s_E[h] = Es;
     }
     __syncthreads();
     float f[G], inv[G];
@@ -735,13 +777,15 @@ __global__ void __launch_bounds__(kClThreads, 1)
     }
     if (crank == 0) {
         for (int h = tid; h < NH; h += kClThreads) {
-            const float Ls = s_L[h], M = s_M[h];
+            const float Ls = s_L[h], M = s_M[h], Es = s_E[h];
             if (a.nsplit == 1) {
-                if (a.lse) a.lse[(long long)row * a.heads + hg * NH + h] = Ls > 0.f ? (M + log2f(Ls)) / kLog2e : -INFINITY;
+                if (a.lse) a.lse[(long long)row * a.heads + hg * NH + h] = Es > 0.f ? (M + log2f(Es)) / kLog2e : -INFINITY;
             } else {
                 const long long b = ((long long)row * a.nsplit + split) * a.heads + hg * NH + h;
-                a.ws_ml[b * 2 + 0] = Ls > 0.f ? M : -INFINITY;
-                a.ws_ml[b * 2 + 1] = Ls;
+                a.ws_ml[b * 4 + 0] = Ls > 0.f ? M : -INFINITY;
+                a.ws_ml[b * 4 + 1] = Ls;
+                a.ws_ml[b * 4 + 2] = Es;
+                a.ws_ml[b * 4 + 3] = 0.f;
             }
         }
     }
@@ -754,7 +798,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
 
 // Split plans, shared by the workspace query and the launch.
 //   e4m3 rows (mma.sync kernel): one CTA per (row, head group, split) over 64-key chunks;
-//   bf16 rows (tcgen05 kernel): one cluster of `cl` CTAs per (row, head group, split) over 64-key
+//   bf16 rows (tcgen05 kernel): one cluster of `cl` CTAs per (row, head group, split) over 32-key
 //   sub-tiles: clusters of 4 while four CTAs per row still fit on the GPU at once, then 2, then 1;
 //   a row splits further only when its clusters leave SMs idle, and never below two sub-tiles per CTA.
 struct SplitPlan {
@@ -787,7 +831,7 @@ static SplitPlan plan_for(int rows, int heads, int max_keys, int dtype) {
 // are split over several clusters (the CTAs of one cluster merge on chip).
 static size_t workspace_bytes_for(int rows, const SplitPlan& p, int heads) {
     if (p.nsplit <= 1) return 0;
-    return (size_t)rows * p.nsplit * heads * (kD + 2) * sizeof(float);
+    return (size_t)rows * p.nsplit * heads * (kD + 4) * sizeof(float);
 }
 
 // Workspace that covers either row format (the size query does not know the pool's format).

@@ -171,8 +171,8 @@ dsa_status_t dsa_topk(int32_t nq, const float* scores, int32_t ld, const int32_t
 /*
  * Workspace (bytes) that dsa_sparse_attn_decode / _prefill need for nq query rows of
  * `heads` heads and at most `max_keys` keys per row (compressed + window) on the current
- * device, for either pool format: the fp32 partial outputs and (max, sum) pairs of rows whose
- * keys are split over several groups of CTAs.  0 means the call needs none.
+ * device, for either pool format: the fp32 partial outputs and (max, sums) of rows whose keys
+ * are split over several groups of CTAs.  0 means the call needs none.
  */
 size_t dsa_attn_workspace_size(int32_t nq, int32_t heads, int32_t max_keys);
 
