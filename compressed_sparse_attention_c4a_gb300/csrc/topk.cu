@@ -667,12 +667,15 @@ extern "C" dsa_status_t dsa_topk(int32_t nq, const float* scores, int32_t ld, co
     if (nq == 0) return DSA_OK;
     if (!scores || !n_valid || !idx_out || !aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (ld <= 16 * 1024) {  // one CTA per row, the row in registers
+    const long long slots = 2LL * sm_count();  // CTAs of the cluster kernel resident at once
+    if (ld <= 16 * 1024) {  // one CTA per row, the row in registers (faster than a cluster even for few rows)
         const cudaError_t e = launch_pdl(topk_reg_kernel<1024, 16>, dim3(nq), dim3(1024), 0, st, scores, ld, n_valid,
                                          k, idx_out, dev_status);
         return e == cudaSuccess ? launch_status() : DSA_ERR_CUDA;
     }
-    const int csz = ld <= kPartMax ? 1 : (ld <= 2 * kPartMax ? 2 : kTopkClusterMax);
+    // clusters: as many CTAs per row as the row's length needs, more while the rows leave SMs idle
+    int csz = ld <= kPartMax ? 1 : (ld <= 2 * kPartMax ? 2 : kTopkClusterMax);
+    while (csz < kTopkClusterMax && (long long)nq * csz * 2 <= slots) csz *= 2;
     const int chunk = ((ld + csz - 1) / csz + 3) & ~3;
     if (chunk > kPartMax) return DSA_ERR_UNSUPPORTED;
     const size_t smem = (size_t)(2 * kBins + 2 * kRankMax + kMarkWords) * sizeof(uint32_t) +
