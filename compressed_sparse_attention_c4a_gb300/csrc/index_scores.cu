@@ -16,6 +16,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 
 #include "common.cuh"
 
@@ -168,6 +169,22 @@ template <bool B>
 struct BoolTag {
     static constexpr bool value = B;
 };
+
+// Two fp32 lanes in one 64-bit register, and their fused multiply-add (fma.rn.f32x2: each lane rounds as
+// a scalar fmaf would).
+__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void fma_f32x2(unsigned long long& acc, unsigned long long a, unsigned long long b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ float sum_f32x2(unsigned long long v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo + hi;
+}
 
 __host__ __device__ constexpr int gbuf_nvis_offset(int n_cols, int dim) { return n_cols * dim + 2 * n_cols * 4; }
 
@@ -440,6 +457,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
         const int ch_lo = sl * nch / NSL, ch_hi = (sl + 1) * nch / NSL;  // this warp's 16-column chunks
         float* fold = s_fold + (warp - 2) * kSlice;
         bool q_neg = false;
+        int g_vis = 0;  // fewest visible entries over the group's queries
         int prev_gb = -1, euse[2] = {0, 0};
         int s = 0, sph = 0, b = 0, bph = 0;  // stage / accumulator index and phase parity
         for (int n = 0;; ++n) {
@@ -471,8 +489,15 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                     neg |= live && ssq[c] < 0.f;
                 }
                 q_neg = __any_sync(0xffffffffu, neg);
+                int vmin = INT_MAX;
+                for (int j = lane; j < nqg; j += 32) vmin = min(vmin, gnv[j]);
+                g_vis = __reduce_min_sync(0xffffffffu, vmin);
                 __syncwarp();
             }
+            // every entry of the item present and visible to every query of the group: unmasked stores
+            bool clean = meta->e0 + kItem <= min(g_vis, a.ld);
+#pragma unroll
+            for (int p = 0; p < kPages; ++p) clean = clean && meta->blk[p] >= 0;
             const float* sscale = reinterpret_cast<const float*>(smem + (size_t)s * a.stage_bytes + tiles_bytes +
                                                                  meta_bytes());
 #pragma unroll
@@ -498,8 +523,9 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                     // holds a negative query scale and takes the literal formula.  Each query's head sum runs
                     // as two independent chains and no branch separates the queries of a chunk; only the
                     // stores are predicated.
-                    auto emit = [&](auto neg_tag, auto lit_tag) {
+                    auto emit = [&](auto neg_tag, auto lit_tag, auto clean_tag) {
                         constexpr bool kNeg = decltype(neg_tag)::value, kLit = decltype(lit_tag)::value;
+                        constexpr bool kClean = decltype(clean_tag)::value;
 #pragma unroll
                         for (int k = 0; k < kBatch; ++k) {
                             if (cb + k >= ch_hi) break;  // warp-uniform
@@ -509,18 +535,18 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                                 const float* x = v[k] + jj * HEADS;
                                 const int c0 = (cb + k) * 16 + jj * HEADS;  // first column of query jj
                                 float a0 = 0.f, a1 = 0.f;
-                                if constexpr (!kLit) {
+                                if constexpr (!kLit) {  // even and odd heads in the two lanes of one register
                                     const float4* u4 = reinterpret_cast<const float4*>(fold + c0 - ch_lo * 16);
+                                    unsigned long long a2 = 0ull;
 #pragma unroll
                                     for (int h4 = 0; h4 < HEADS / 4; ++h4) {
                                         const float4 u = u4[h4];
                                         const float* xh = x + 4 * h4;
-                                        a0 = fmaf(u.x, kNeg ? fminf(xh[0], 0.f) : fmaxf(xh[0], 0.f), a0);
-                                        a1 = fmaf(u.y, kNeg ? fminf(xh[1], 0.f) : fmaxf(xh[1], 0.f), a1);
-                                        a0 = fmaf(u.z, kNeg ? fminf(xh[2], 0.f) : fmaxf(xh[2], 0.f), a0);
-                                        a1 = fmaf(u.w, kNeg ? fminf(xh[3], 0.f) : fmaxf(xh[3], 0.f), a1);
+                                        auto relu = [&](float t) { return kNeg ? fminf(t, 0.f) : fmaxf(t, 0.f); };
+                                        fma_f32x2(a2, pack_f32x2(u.x, u.y), pack_f32x2(relu(xh[0]), relu(xh[1])));
+                                        fma_f32x2(a2, pack_f32x2(u.z, u.w), pack_f32x2(relu(xh[2]), relu(xh[3])));
                                     }
-                                    acc[jj] = (a0 + a1) * sk;
+                                    acc[jj] = sum_f32x2(a2) * sk;
                                 } else {
 #pragma unroll
                                     for (int h = 0; h < HEADS; h += 2) {
@@ -533,14 +559,23 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
 #pragma unroll
                             for (int jj = 0; jj < 16 / HEADS; ++jj) {
                                 const int j = (cb + k) * (16 / HEADS) + jj;  // query of the group
-                                if (e_ok && j < nqg)
+                                if constexpr (kClean) {
+                                    if (j < nqg) out[(long long)j * a.ld] = acc[jj];
+                                } else if (e_ok && j < nqg) {
                                     out[(long long)j * a.ld] = (page_ok && e < gnv[j]) ? acc[jj] : -INFINITY;
+                                }
                             }
                         }
                     };
-                    if (q_neg) emit(BoolTag<false>{}, BoolTag<true>{});
-                    else if (sk < 0.f) emit(BoolTag<true>{}, BoolTag<false>{});
-                    else emit(BoolTag<false>{}, BoolTag<false>{});
+                    if (q_neg) emit(BoolTag<false>{}, BoolTag<true>{}, BoolTag<false>{});
+                    else if (sk < 0.f) {
+                        if (clean) emit(BoolTag<true>{}, BoolTag<false>{}, BoolTag<true>{});
+                        else emit(BoolTag<true>{}, BoolTag<false>{}, BoolTag<false>{});
+                    } else if (clean) {
+                        emit(BoolTag<false>{}, BoolTag<false>{}, BoolTag<true>{});
+                    } else {
+                        emit(BoolTag<false>{}, BoolTag<false>{}, BoolTag<false>{});
+                    }
                     __syncwarp();  // reconverge before the next collective load
                 }
             }
