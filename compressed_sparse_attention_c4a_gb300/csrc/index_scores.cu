@@ -238,13 +238,17 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    pdl_wait();  // on-chip set-up above; global memory only below
-    pdl_launch_dependents();
-
-    // visible-entry count of every query (grid-strided, independent of the tile loop)
-    if (a.n_visible)
-        for (int q = blockIdx.x * kThreads + tid; q < a.nq; q += gridDim.x * kThreads)
-            a.n_visible[q] = visible_of(a, q);
+    // Programmatic dependent launch: the producer resolves its first items (query positions and requests,
+    // the block table: inputs no preceding kernel of the layer writes) while the preceding kernel (the
+    // compressor, which writes keys) finishes; key copies and every global write come after the wait.
+    if (warp != 0) {
+        pdl_wait();
+        pdl_launch_dependents();
+        // visible-entry count of every query (grid-strided over the non-producer threads)
+        if (a.n_visible)
+            for (int q = blockIdx.x * (kThreads - 32) + tid - 32; q < a.nq; q += gridDim.x * (kThreads - 32))
+                a.n_visible[q] = visible_of(a, q);
+    }
 
     if (warp == 0) {
         // ---- producer warp ---------------------------------------------------------------------------
@@ -253,6 +257,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
         // (the next batch is prefetched while the current one is issued); lane 0 issues the copies.
         int* pre = grp_prefix;
         long long carry = 0;
+        bool bad_group = false;  // reported after the wait
         for (int g0 = 0; g0 < a.n_groups; g0 += 32) {
             const int g = g0 + lane;
             int cnt = 0;
@@ -261,7 +266,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                 group_of(a, g, &r, &mv);
                 grp_r[g] = r;
                 grp_mv[g] = mv;
-                if (r < 0) report(a.status, DSA_ERR_DEVICE_FAULT);
+                if (r < 0) bad_group = true;
                 else cnt = min((mv + kItem - 1) / kItem, a.items);
             }
             int incl = cnt;
@@ -299,6 +304,9 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
         int cur_g = -1, gb = 1, guse[2] = {0, 0};  // group in the current buffer, buffer index, loads per buffer
         bool alive = true;
         ItemInfo cur = resolve(lo);
+        pdl_wait();  // keys may come from the preceding kernel
+        pdl_launch_dependents();
+        if (bad_group) report(a.status, DSA_ERR_DEVICE_FAULT);
         for (long long base = lo; base < hi && alive; base += kChunkItems) {
             const ItemInfo nxt = resolve(base + kChunkItems);
             for (int u = 0; u < kChunkItems; ++u) {

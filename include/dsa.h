@@ -148,6 +148,9 @@ dsa_status_t dsa_compress(int32_t kind, int32_t batch, const int32_t* cu_new, co
  *            the 128-entry tile holding n_vis(m) - 1; the rest of the row is not written
  * ld         host int, >= n_vis of every query, a multiple of 4
  * n_visible  [nq] int32 out (n_vis per query), or NULL
+ * Launched with programmatic dependent launch: q_pos, q_req and bt are read before the kernel waits
+ * for the preceding kernel in the stream (keys, queries and every output only after), so a preceding
+ * kernel that releases its dependents early must have written those three by then.
  */
 dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8, const float* q_scale,
                               const float* w, const int32_t* q_pos, const int32_t* q_req, int32_t q_group,
