@@ -796,11 +796,10 @@ __global__ void __launch_bounds__(kClThreads, 1)
     if (warp == 0) tmem_dealloc(tmem, L::kTmemCols);
 }
 
-// Split plans, shared by the workspace query and the launch.
-//   e4m3 rows (mma.sync kernel): one CTA per (row, head group, split) over 64-key chunks;
-//   bf16 rows (tcgen05 kernel): one cluster of `cl` CTAs per (row, head group, split) over 32-key
-//   sub-tiles: clusters of 4 while four CTAs per row still fit on the GPU at once, then 2, then 1;
-//   a row splits further only when its clusters leave SMs idle, and never below two sub-tiles per CTA.
+// Split plans, shared by the workspace query and the launch (both row formats run on the tcgen05
+// kernel): one cluster of `cl` CTAs per (row, head group, split) over 32-key sub-tiles: clusters of 4
+// while four CTAs per row still fit on the GPU at once, then 2, then 1; a row splits further only when
+// its clusters leave SMs idle, and never below two sub-tiles per CTA.
 struct SplitPlan {
     int hg, hg_count, nsplit, cps, cl;
 };
