@@ -47,6 +47,7 @@ struct IdxArgs {
     const float* w;
     const int32_t* q_pos;
     const int32_t* q_req;
+    const int32_t* fresh_from;  // [batch] first entry the preceding kernel may still write, or NULL
     const float* key_scale;
     int num_blocks;
     dsa_block_table_t bt;
@@ -77,6 +78,7 @@ __device__ __forceinline__ int visible_of(const IdxArgs& a, int q) { return visi
 // and the physical blocks of its 64-entry pages, resolved by one producer lane.
 struct ItemInfo {
     int valid, g, t, r, max_vis, want;  // want: bit p set when page p holds visible entries
+    int fresh;                          // 1: a loaded page holds entries the preceding kernel may write
     int blk[4];
 };
 
@@ -100,12 +102,16 @@ __device__ __forceinline__ void group_of(const IdxArgs& a, int g, int* r, int* m
 template <int TPI>
 __device__ __forceinline__ ItemInfo item_info(const IdxArgs& a, int valid, int g, int t, const int* grp_r,
                                               const int* grp_mv) {
-    ItemInfo x{0, g, t, -1, 0, 0, {-1, -1, -1, -1}};
+    ItemInfo x{0, g, t, -1, 0, 0, 1, {-1, -1, -1, -1}};
     if (!valid) return x;
     x.r = grp_r[g];
     x.max_vis = grp_mv[g];
     if (x.r < 0 || t * TPI * kTileEntries >= x.max_vis) return x;
     x.valid = 1;
+    if (a.fresh_from) {  // the loaded pages end at the page holding the item's last visible entry
+        const int end = (min(x.max_vis, (t + 1) * TPI * kTileEntries) + kPage - 1) / kPage * kPage;
+        x.fresh = end > __ldg(a.fresh_from + x.r) ? 1 : 0;
+    }
     // no branch on the loaded table entries: the loads stay in flight until the item is used
 #pragma unroll
     for (int pi = 0; pi < 2 * TPI; ++pi) {
@@ -126,6 +132,7 @@ __device__ __forceinline__ ItemInfo shfl_item(const ItemInfo& x, int src) {
     y.r = __shfl_sync(0xffffffffu, x.r, src);
     y.max_vis = __shfl_sync(0xffffffffu, x.max_vis, src);
     y.want = __shfl_sync(0xffffffffu, x.want, src);
+    y.fresh = __shfl_sync(0xffffffffu, x.fresh, src);
 #pragma unroll
     for (int p = 0; p < 4; ++p) y.blk[p] = __shfl_sync(0xffffffffu, x.blk[p], src);
     return y;
@@ -240,10 +247,15 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
     const uint32_t tmem = *s_tmem;
     // Programmatic dependent launch: the producer resolves its first items (query positions and requests,
     // the block table: inputs no preceding kernel of the layer writes) while the preceding kernel (the
-    // compressor, which writes keys) finishes; key copies and every global write come after the wait.
+    // compressor, which writes keys) finishes.  Without fresh_from, key copies and every global write come
+    // after the wait; with it, pages wholly below fresh_from[r] are copied and scored before it and the
+    // producer waits before its first fresh page (and before the CTA ends in any case).
+    const bool early = a.fresh_from != nullptr;
     if (warp != 0) {
-        pdl_wait();
-        pdl_launch_dependents();
+        if (!early) {
+            pdl_wait();
+            pdl_launch_dependents();
+        }
         // visible-entry count of every query (grid-strided over the non-producer threads)
         if (a.n_visible)
             for (int q = blockIdx.x * (kThreads - 32) + tid - 32; q < a.nq; q += gridDim.x * (kThreads - 32))
@@ -304,14 +316,22 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
         int cur_g = -1, gb = 1, guse[2] = {0, 0};  // group in the current buffer, buffer index, loads per buffer
         bool alive = true;
         ItemInfo cur = resolve(lo);
-        pdl_wait();  // keys may come from the preceding kernel
-        pdl_launch_dependents();
+        bool waited = !early;
+        if (!early) {
+            pdl_wait();  // keys may come from the preceding kernel
+            pdl_launch_dependents();
+        }
         if (bad_group) report(a.status, DSA_ERR_DEVICE_FAULT);
         for (long long base = lo; base < hi && alive; base += kChunkItems) {
             const ItemInfo nxt = resolve(base + kChunkItems);
             for (int u = 0; u < kChunkItems; ++u) {
                 ItemInfo it = shfl_item(cur, u);
                 if (!it.valid) continue;
+                if (it.fresh && !waited) {  // warp-uniform: this item's pages may still be being written
+                    pdl_wait();
+                    pdl_launch_dependents();
+                    waited = true;
+                }
                 // a visible page whose table entry is unmapped or outside the pool: a device fault, not loaded
                 bool bad = false;
 #pragma unroll
@@ -399,6 +419,10 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                 }
             }
             cur = nxt;
+        }
+        if (!waited) {  // the kernel ends after the preceding kernel, whatever it read
+            pdl_wait();
+            pdl_launch_dependents();
         }
         {  // terminal stage: consumers stop here (33 arrivals, no bytes)
             const int s = ps;
@@ -669,7 +693,7 @@ extern "C" dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim,
                                          const float* q_scale, const float* w, const int32_t* q_pos,
                                          const int32_t* q_req, int32_t q_group, const dsa_pool_t* keys,
                                          const dsa_block_table_t* bt, float* scores, int32_t ld, int32_t* n_visible,
-                                         int32_t* dev_status, void* stream) {
+                                         const int32_t* fresh_from, int32_t* dev_status, void* stream) {
     if (nq < 0 || ld < 0 || (ld & 3)) return DSA_ERR_INVALID_ARG;
     if (nq == 0) return DSA_OK;
     if (heads != 4 && heads != 8 && heads != 16) return DSA_ERR_UNSUPPORTED;
@@ -697,6 +721,7 @@ extern "C" dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim,
     a.w = w;
     a.q_pos = q_pos;
     a.q_req = q_req;
+    a.fresh_from = fresh_from;
     a.key_scale = keys->scale;
     a.num_blocks = keys->num_blocks;
     a.bt = *bt;

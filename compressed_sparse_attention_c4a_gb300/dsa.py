@@ -55,7 +55,7 @@ _lib.dsa_attn_plan.restype = ctypes.c_int32
 _lib.dsa_attn_plan.argtypes = [_I, _I, _I, _I, _P]
 for _name, _args in {
     "dsa_compress": [_I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P],
-    "dsa_index_scores": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P],
+    "dsa_index_scores": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P],
     "dsa_topk": [_I, _P, _I, _P, _I, _P, _P, _P],
     "dsa_sparse_attn_decode": [_I, _I, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, ctypes.c_float, _P, _P, _P, _P,
                                ctypes.c_size_t, _P, _P],
@@ -120,11 +120,11 @@ def dsa_compress(kind, cu_new, start_pos, max_new, x_new, logit_new, state_x, st
 
 
 def dsa_index_scores(q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, n_visible=None, dev_status=None,
-                     stream=None):
+                     stream=None, fresh_from=None):
     nq, heads, dim = q8.shape
     code = _lib.dsa_index_scores(nq, heads, dim, _ptr(q8), _ptr(q_scale), _ptr(w), _ptr(q_pos), _ptr(q_req),
                                  int(q_group), ctypes.byref(keys), ctypes.byref(bt), _ptr(scores), scores.shape[1],
-                                 _ptr(n_visible), _ptr(dev_status), _stream(stream))
+                                 _ptr(n_visible), _ptr(fresh_from), _ptr(dev_status), _stream(stream))
     _check("dsa_index_scores", code)
 
 

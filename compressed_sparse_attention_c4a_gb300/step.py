@@ -49,6 +49,14 @@ class LayerStep:
             self.n_visible = torch.empty((nq,), dtype=torch.int32, device=dev)
             self.topk = torch.empty((nq, spec.topk), dtype=torch.int32, device=dev)
             self.q_group = _query_group(spec, spec.idx_heads)
+            # first indexer entry of each request that this step's compressor may write (entry i is complete
+            # at position 4i + 7, so the entries before the first new token are old): older key pages are
+            # scored while the compressor still runs
+            self.fresh_from = None
+            if spec.index_compress:
+                p = case["start_pos"].to(torch.int64) - 1
+                old = torch.where(p >= 7, torch.div(p - 7, 4, rounding_mode="floor") + 1, torch.zeros_like(p))
+                self.fresh_from = old.to(torch.int32).contiguous()
         self.out = torch.empty((nq, spec.heads, spec.dim), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((nq, spec.heads), dtype=torch.float32, device=dev)
         max_keys = (spec.topk if self.has_index else case["bt_main"].shape[1] * epb) + spec.window
@@ -82,7 +90,8 @@ class LayerStep:
     def index(self):
         c = self.case
         dsa.dsa_index_scores(c["q8"], c["q_scale"], c["w"], c["q_pos"], c["q_req"], self.q_group, self.idx,
-                             self.idx_bt, self.scores, self.n_visible, dev_status=self.status)
+                             self.idx_bt, self.scores, self.n_visible, dev_status=self.status,
+                             fresh_from=self.fresh_from)
 
     def select(self):
         dsa.dsa_topk(self.scores, self.n_visible, self.spec.topk, self.topk, dev_status=self.status)

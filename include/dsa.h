@@ -148,14 +148,20 @@ dsa_status_t dsa_compress(int32_t kind, int32_t batch, const int32_t* cu_new, co
  *            the 128-entry tile holding n_vis(m) - 1; the rest of the row is not written
  * ld         host int, >= n_vis of every query, a multiple of 4
  * n_visible  [nq] int32 out (n_vis per query), or NULL
- * Launched with programmatic dependent launch: q_pos, q_req and bt are read before the kernel waits
- * for the preceding kernel in the stream (keys, queries and every output only after), so a preceding
- * kernel that releases its dependents early must have written those three by then.
+ * fresh_from [batch] int32: for request r, the first entry that the preceding kernel in the stream may
+ *            still be writing (after dsa_compress of this step: the entries its new tokens form, i.e.
+ *            n_vis(first new position - 1)); or NULL.
+ * Launched with programmatic dependent launch, so the kernel may start before the preceding kernel in
+ * the stream has finished.  q_pos, q_req and bt are always read before waiting for it.  Without
+ * fresh_from, keys, queries and every output are touched only after the wait.  With fresh_from, key
+ * pages wholly below fresh_from[r], the queries, and the scores / n_visible outputs may be touched before
+ * it: a preceding kernel that releases its dependents early must not write those inputs or read those
+ * outputs after releasing them.  The call ends after the preceding kernel in every case.
  */
 dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8, const float* q_scale,
                               const float* w, const int32_t* q_pos, const int32_t* q_req, int32_t q_group,
                               const dsa_pool_t* keys, const dsa_block_table_t* bt, float* scores, int32_t ld,
-                              int32_t* n_visible, int32_t* dev_status, void* stream);
+                              int32_t* n_visible, const int32_t* fresh_from, int32_t* dev_status, void* stream);
 
 /*
  * dsa_topk - per-query top-k of indexer scores.  [P1] §4.2: S_t = TopK(I_{t,:}, k).

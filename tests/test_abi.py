@@ -51,9 +51,9 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.dsa_topk(0, None, 64, None, 8, None, None, None) == 0          # empty: a no-op
     # indexer: unsupported head count / dim
     lib.dsa_index_scores.argtypes = [ctypes.c_int32] * 3 + [P] * 5 + [ctypes.c_int32, P, P, P, ctypes.c_int32, P, P,
-                                                                       P]
-    assert lib.dsa_index_scores(1, 5, 128, *[P(16)] * 5, 1, P(16), P(16), P(16), 64, None, None, None) == 2
-    assert lib.dsa_index_scores(1, 8, 96, *[P(16)] * 5, 1, P(16), P(16), P(16), 64, None, None, None) == 2
+                                                                       P, P]
+    assert lib.dsa_index_scores(1, 5, 128, *[P(16)] * 5, 1, P(16), P(16), P(16), 64, None, None, None, None) == 2
+    assert lib.dsa_index_scores(1, 8, 96, *[P(16)] * 5, 1, P(16), P(16), P(16), 64, None, None, None, None) == 2
     # compress: bad kind, null pointers
     lib.dsa_compress.restype = ctypes.c_int32
     args = [ctypes.c_int32(7), ctypes.c_int32(1)] + [None] * 18
