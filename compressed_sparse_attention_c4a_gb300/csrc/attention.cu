@@ -53,6 +53,19 @@ __device__ __forceinline__ void cp_async_wait_but_one() { asm volatile("cp.async
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return (uint32_t)float_to_bf16(lo) | ((uint32_t)float_to_bf16(hi) << 16);
 }
+// {lo, hi} -> bf16x2 in one conversion (round to nearest even, as pack_bf16), lo in the low half.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+// 2^x on the special-function unit (PTX ex2.approx.ftz: a few ulp, 2^-inf = 0); for softmax
+// probabilities, which enter the product rounded to bf16.
+__device__ __forceinline__ float ex2_sfu(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // Merge split partials of one (row, head): 128 threads x 4 dims; inverse RoPE; bf16 store.
 __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
@@ -540,11 +553,19 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 tmem_regs_after_wait<16>(*reinterpret_cast<float(*)[16]>(sv + 16));
                 const uint32_t vm = s_mask[st];
                 float mx = -INFINITY;
+                if (!FP8 && vm == 0xFFFFFFFFu) {  // every key of the stage present (the same for all threads)
 #pragma unroll
-                for (int j = 0; j < kClKeys; ++j) {
-                    const float ls = FP8 ? a.scale_log2 * s_ksc[st * kClKeys + j] : a.scale_log2;  // e4m3: times the row scale
-                    sv[j] = ((vm >> j) & 1) ? sv[j] * ls : -INFINITY;
-                    mx = fmaxf(mx, sv[j]);
+                    for (int j = 0; j < kClKeys; ++j) {
+                        sv[j] *= a.scale_log2;
+                        mx = fmaxf(mx, sv[j]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < kClKeys; ++j) {
+                        const float ls = FP8 ? a.scale_log2 * s_ksc[st * kClKeys + j] : a.scale_log2;  // e4m3: times the row scale
+                        sv[j] = ((vm >> j) & 1) ? sv[j] * ls : -INFINITY;
+                        mx = fmaxf(mx, sv[j]);
+                    }
                 }
                 if (mx > m_run + kLazyLog2) {  // also the first finite maximum (m_run = -inf)
                     alpha = exp2f(m_run - mx);
@@ -559,17 +580,14 @@ __global__ void __launch_bounds__(kClThreads, 1)
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
+                        const float p0 = ex2_sfu(sv[8 * c + 2 * e] - mr), p1 = ex2_sfu(sv[8 * c + 2 * e + 1] - mr);
+                        esum += p0 + p1;
                         if constexpr (FP8) {  // the probability that multiplies the codes carries the row scale
-                            const float p0 = exp2f(sv[8 * c + 2 * e] - mr), p1 = exp2f(sv[8 * c + 2 * e + 1] - mr);
                             sum += p0 + p1;
-                            esum += p0 + p1;
-                            w[e] = pack_bf16(p0 * s_ksc[st * kClKeys + 8 * c + 2 * e], p1 * s_ksc[st * kClKeys + 8 * c + 2 * e + 1]);
+                            w[e] = bf16x2_rn(p0 * s_ksc[st * kClKeys + 8 * c + 2 * e], p1 * s_ksc[st * kClKeys + 8 * c + 2 * e + 1]);
                         } else {
-                            const float p0 = exp2f(sv[8 * c + 2 * e] - mr), p1 = exp2f(sv[8 * c + 2 * e + 1] - mr);
-                            const uint16_t b0 = float_to_bf16(p0), b1 = float_to_bf16(p1);
-                            sum += bf16_to_float(b0) + bf16_to_float(b1);
-                            esum += p0 + p1;
-                            w[e] = (uint32_t)b0 | ((uint32_t)b1 << 16);
+                            w[e] = bf16x2_rn(p0, p1);
+                            sum += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xFFFF0000u);
                         }
                     }
                     if (hthread)
