@@ -344,3 +344,51 @@ def test_topk_many_rows_exact():
     got = out.cpu().numpy()
     for i in range(nq):
         assert list(got[i]) == list(OL.topk(scores[i].astype(np.float64), int(nv[i]), k)), i
+
+
+@pytest.mark.parametrize("nq,ld", [(200, 34816), (120, 20004), (16, 65536)])
+def test_topk_long_rows_cluster_sizes_exact(nq, ld):
+    """Rows longer than 16,384 scores at row counts that give clusters of 1 (200 rows), 2 (120 rows) and
+    4 CTAs per row (16 rows) on 152 SMs: random lengths, ReLU-like zeros and heavy ties, index for index."""
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    rng = np.random.default_rng(nq + ld)
+    k = 512
+    scores = np.maximum(rng.standard_normal((nq, ld)), 0.0).astype(np.float32)   # about half exact zeros
+    scores[::3] = np.round(scores[::3] * 4) / 4                                     # heavy ties
+    nv = rng.integers(k - 10, ld + 1, nq).astype(np.int32)
+    nv[::4] = ld
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty((nq, k), dtype=torch.int32, device="cuda")
+    dsa.dsa_topk(torch.from_numpy(scores).cuda(), torch.from_numpy(nv).cuda(), k, out, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = out.cpu().numpy()
+    for i in range(nq):
+        assert list(got[i]) == list(OL.topk(scores[i].astype(np.float64), int(nv[i]), k)), i
+
+
+@pytest.mark.parametrize("name", ["c4a_decode", "c4a_multi_prefill"])
+def test_index_scores_fresh_from_extremes(name):
+    """fresh_from says which key pages the preceding kernel may still write: all of them (zeros: every
+    copy waits) or none (every visible entry old: nothing waits) must give the scores of the call
+    without it, bit for bit."""
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    cpu, gpu, step = _setup(name)
+    step.compress()
+    torch.cuda.synchronize()
+    c = step.case
+    runs = []
+    batch = cpu["spec"].batch
+    for fresh in (None, torch.zeros(batch, dtype=torch.int32, device="cuda"),
+                  torch.full((batch,), 1 << 30, dtype=torch.int32, device="cuda")):
+        scores = torch.full_like(step.scores, float("nan"))
+        dsa.dsa_index_scores(c["q8"], c["q_scale"], c["w"], c["q_pos"], c["q_req"], step.q_group, step.idx,
+                             step.idx_bt, scores, step.n_visible, dev_status=step.status, fresh_from=fresh)
+        torch.cuda.synchronize()
+        assert int(step.status.item()) == 0
+        runs.append(np64(scores))
+    nv = np64(step.n_visible)
+    for q in range(cpu["nq"]):
+        n = int(nv[q])
+        assert np.array_equal(runs[1][q, :n], runs[0][q, :n]), q
+        assert np.array_equal(runs[2][q, :n], runs[0][q, :n]), q
