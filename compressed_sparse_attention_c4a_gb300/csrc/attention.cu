@@ -7,10 +7,10 @@
 // K and V are one stored row; [P2] 深潜 (Inverse RoPE): out = R_m^-1 sum_j p_j k_j; [P2] 融合点 2:
 // the inverse rotation is fused with the output store.
 //
-// Work split: see attn_cl_kernel below (a cluster of CTAs per query row, 64-key sub-tiles, tcgen05 MMAs
+// Work split: see attn_cl_kernel below (a cluster of CTAs per query row, 32-key sub-tiles, tcgen05 MMAs
 // with TMEM accumulators, on-chip merge).  When one cluster per row cannot fill the GPU, a row's keys are
-// split over several clusters; each writes an unnormalised partial (O, max, sum) and attn_combine_kernel
-// merges them and applies the inverse rotation.
+// split over several clusters; each writes an unnormalised partial (O, max, the two sums) and
+// attn_combine_kernel merges them and applies the inverse rotation.
 #include <algorithm>
 #include <mutex>
 
@@ -22,7 +22,7 @@ constexpr int kD = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct AttnArgs {
-    int rows, heads, hg_count, nsplit, cps;   // cps = 64-key sub-tiles per split
+    int rows, heads, hg_count, nsplit, cps;   // cps = 32-key sub-tiles per split
     const uint16_t* q;
     const int32_t* q_pos;
     const int32_t* q_req;                     // NULL: row r belongs to request r
