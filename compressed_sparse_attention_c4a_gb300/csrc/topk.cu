@@ -657,27 +657,54 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (tid == 0 && total != (uint32_t)k) report(status, DSA_ERR_DEVICE_FAULT);
 }
 
+// Which kernel a call runs: rows of up to 16,384 scores one CTA each with the row in registers (faster
+// than a cluster even for few rows); longer rows a cluster of as many CTAs as the row's length needs (a
+// part of at most kPartMax scores each), more while the rows leave SMs idle.  Host arithmetic only.
+static dsa_status_t topk_plan(int32_t nq, int32_t ld, int32_t k, bool* reg, int* csz, int* chunk) {
+    if (nq < 0 || k < 1 || k > 2048 || ld < 0 || (ld & 3)) return DSA_ERR_INVALID_ARG;
+    *reg = ld <= 16 * 1024;
+    *csz = 1;
+    *chunk = ld;
+    if (*reg) return DSA_OK;
+    const long long slots = 2LL * sm_count();  // CTAs of the cluster kernel resident at once
+    int c = ld <= kPartMax ? 1 : (ld <= 2 * kPartMax ? 2 : kTopkClusterMax);
+    while (c < kTopkClusterMax && (long long)nq * c * 2 <= slots) c *= 2;
+    *csz = c;
+    *chunk = ((ld + c - 1) / c + 3) & ~3;
+    return *chunk > kPartMax ? DSA_ERR_UNSUPPORTED : DSA_OK;
+}
+
 }  // namespace dsa
 
 using namespace dsa;
 
+extern "C" dsa_status_t dsa_topk_plan(int32_t nq, int32_t ld, int32_t k, int32_t* plan) {
+    if (!plan) return DSA_ERR_INVALID_ARG;
+    bool reg = false;
+    int csz = 1, chunk = 0;
+    const dsa_status_t st = topk_plan(nq, ld, k, &reg, &csz, &chunk);
+    if (st != DSA_OK) return st;
+    plan[0] = reg ? 0 : 1;
+    plan[1] = csz;
+    plan[2] = reg ? 1024 : kTopkThreads;
+    return DSA_OK;
+}
+
 extern "C" dsa_status_t dsa_topk(int32_t nq, const float* scores, int32_t ld, const int32_t* n_valid, int32_t k,
                                  int32_t* idx_out, int32_t* dev_status, void* stream) {
-    if (nq < 0 || k < 1 || k > 2048 || ld < 0 || (ld & 3)) return DSA_ERR_INVALID_ARG;
+    bool reg = false;
+    int csz = 1, chunk = 0;
+    const dsa_status_t plan_st = topk_plan(nq, ld, k, &reg, &csz, &chunk);
+    if (plan_st == DSA_ERR_INVALID_ARG) return plan_st;
     if (nq == 0) return DSA_OK;
     if (!scores || !n_valid || !idx_out || !aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
+    if (plan_st != DSA_OK) return plan_st;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const long long slots = 2LL * sm_count();  // CTAs of the cluster kernel resident at once
-    if (ld <= 16 * 1024) {  // one CTA per row, the row in registers (faster than a cluster even for few rows)
+    if (reg) {
         const cudaError_t e = launch_pdl(topk_reg_kernel<1024, 16>, dim3(nq), dim3(1024), 0, st, scores, ld, n_valid,
                                          k, idx_out, dev_status);
         return e == cudaSuccess ? launch_status() : DSA_ERR_CUDA;
     }
-    // clusters: as many CTAs per row as the row's length needs, more while the rows leave SMs idle
-    int csz = ld <= kPartMax ? 1 : (ld <= 2 * kPartMax ? 2 : kTopkClusterMax);
-    while (csz < kTopkClusterMax && (long long)nq * csz * 2 <= slots) csz *= 2;
-    const int chunk = ((ld + csz - 1) / csz + 3) & ~3;
-    if (chunk > kPartMax) return DSA_ERR_UNSUPPORTED;
     const size_t smem = (size_t)(2 * kBins + 2 * kRankMax + kMarkWords) * sizeof(uint32_t) +
                         ((size_t)chunk * sizeof(uint16_t) + 15) / 16 * 16;
     if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)

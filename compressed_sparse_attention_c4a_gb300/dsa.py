@@ -19,7 +19,7 @@ DSA_BF16, DSA_FP8_E4M3 = 0, 1
 DSA_C4A, DSA_C128A = 0, 1
 KIND = {"c4a": DSA_C4A, "c128a": DSA_C128A}
 
-EXPORTS = ["dsa_status_string", "dsa_compress", "dsa_index_scores", "dsa_topk", "dsa_attn_workspace_size",
+EXPORTS = ["dsa_status_string", "dsa_compress", "dsa_index_scores", "dsa_topk", "dsa_topk_plan", "dsa_attn_workspace_size",
            "dsa_sparse_attn_decode", "dsa_sparse_attn_prefill", "dsa_gather_rows", "dsa_sparse_attn_decode_static",
            "dsa_attn_static_scratch_bytes", "dsa_attn_plan"]
 
@@ -53,6 +53,8 @@ _lib.dsa_attn_static_scratch_bytes.restype = ctypes.c_size_t
 _lib.dsa_attn_static_scratch_bytes.argtypes = []
 _lib.dsa_attn_plan.restype = ctypes.c_int32
 _lib.dsa_attn_plan.argtypes = [_I, _I, _I, _I, _P]
+_lib.dsa_topk_plan.restype = ctypes.c_int32
+_lib.dsa_topk_plan.argtypes = [_I, _I, _I, _P]
 for _name, _args in {
     "dsa_compress": [_I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P],
     "dsa_index_scores": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P],
@@ -136,6 +138,13 @@ def dsa_topk(scores, n_valid, k, idx_out, dev_status=None, stream=None):
 
 def dsa_attn_workspace_size(nq, heads, max_keys):
     return int(_lib.dsa_attn_workspace_size(int(nq), int(heads), int(max_keys)))
+
+
+def dsa_topk_plan(nq, ld, k):
+    """(kernel: 0 registers / 1 cluster, CTAs per row, threads per CTA) of the top-k call."""
+    plan = (ctypes.c_int32 * 3)()
+    _check("dsa_topk_plan", _lib.dsa_topk_plan(int(nq), int(ld), int(k), plan))
+    return tuple(int(x) for x in plan)
 
 
 def dsa_attn_plan(nq, heads, max_keys, dtype="bf16"):

@@ -178,6 +178,14 @@ dsa_status_t dsa_topk(int32_t nq, const float* scores, int32_t ld, const int32_t
                       int32_t* idx_out, int32_t* dev_status, void* stream);
 
 /*
+ * dsa_topk_plan - how dsa_topk runs for these sizes on the current device; host only, launches nothing.
+ * plan[0] = kernel (0: one CTA per row with the row in registers, for ld <= 16,384; 1: a cluster of
+ * CTAs per row, each holding one part of the row), plan[1] = CTAs per row, plan[2] = threads per CTA.
+ * Returns DSA_ERR_INVALID_ARG / DSA_ERR_UNSUPPORTED as dsa_topk would for these sizes.
+ */
+dsa_status_t dsa_topk_plan(int32_t nq, int32_t ld, int32_t k, int32_t* plan);
+
+/*
  * Workspace (bytes) that dsa_sparse_attn_decode / _prefill need for nq query rows of
  * `heads` heads and at most `max_keys` keys per row (compressed + window) on the current
  * device, for either pool format: the fp32 partial outputs and (max, sums) of rows whose keys

@@ -82,3 +82,22 @@ def test_attention_plan_host_only(lib):
     assert lib.dsa_attn_plan(0, 64, 640, 0, plan) == 1
     assert lib.dsa_attn_plan(4, 48, 640, 0, plan) == 2
     assert lib.dsa_attn_plan(4, 64, 640, 7, plan) == 1
+
+
+def test_topk_plan_host_only(lib):
+    """The top-k dispatch is host arithmetic: valid without a GPU (the SM count falls back to a default of
+    148, so 296 cluster CTAs are resident at once)."""
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    assert dsa.dsa_topk_plan(32, 16384, 512) == (0, 1, 1024)      # decode rows: registers, one CTA each
+    assert dsa.dsa_topk_plan(200, 34816, 512) == (1, 1, 512)      # many long rows: one CTA per row
+    assert dsa.dsa_topk_plan(120, 34816, 512) == (1, 2, 512)      # fewer rows: spread over two SMs
+    assert dsa.dsa_topk_plan(16, 65536, 512) == (1, 4, 512)       # a row past 40,960 needs two parts at least
+    assert dsa.dsa_topk_plan(1000, 65536, 512) == (1, 2, 512)
+    assert dsa.dsa_topk_plan(1, 163840, 512) == (1, 4, 512)       # the longest row four parts hold
+    P = ctypes.c_void_p
+    lib.dsa_topk_plan.argtypes = [ctypes.c_int32] * 3 + [P]
+    plan = (ctypes.c_int32 * 3)()
+    assert lib.dsa_topk_plan(1, 163844, 512, plan) == 2            # DSA_ERR_UNSUPPORTED
+    assert lib.dsa_topk_plan(1, 1026, 512, plan) == 1              # ld not a multiple of 4
+    assert lib.dsa_topk_plan(1, 1024, 0, plan) == 1                # k < 1
+    assert lib.dsa_topk_plan(1, 1024, 512, None) == 1
