@@ -10,9 +10,12 @@ layer (one query per request per step).
 
 Timing: CUDA graphs of the step replayed over 4 resident cache copies (distinct layers), so that
 each step's working set was evicted from L2 by the three steps before it; CUDA events on the
-launching stream; max over ranks.  Multi-GPU: independent replicas (weak scaling), no collective
-on the data path.  ``--impl reference`` times the CPU oracle on a bounded sample of the same
-workload and prints the same JSON line with "impl": "reference".
+launching stream, one pair per graph replay inside the timed region (the median and spread of
+those repetitions are reported beside the whole region's mean); max over ranks.  Multi-GPU:
+independent replicas (weak scaling), no collective on the data path; ``--gpus N`` without a
+launcher starts the N ranks itself under torch.distributed.run.  ``--impl reference`` times the
+CPU oracle on a bounded sample of the same workload and prints the same JSON line with
+"impl": "reference".
 """
 import argparse
 import hashlib
@@ -52,6 +55,22 @@ def parse():
 
 def rank_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def relaunch_ranks(args):
+    """``--gpus N`` (N > 1) outside a launcher: start N ranks of this script under torch.distributed.run on
+    127.0.0.1 and return its exit status.  The GPU arm needs N visible GPUs and fails loudly otherwise."""
+    if args.impl == "gb300":
+        have = torch.cuda.device_count()
+        if have < args.gpus:
+            raise SystemExit(f"bench.py --gpus {args.gpus}: only {have} CUDA device(s) visible")
+    import socket
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        port = so.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+           "--master-addr", "127.0.0.1", f"--master-port={port}", os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
 
 
 # ---------------------------------------------------------------------------------------------
@@ -223,7 +242,7 @@ def run_gpu(args, rank, world, local_rank):
         for i in range(max(3, min(args.warmup, 50))):
             copies[i % COPIES].run()
     torch.cuda.synchronize()
-    per_graph = COPIES * max(1, min(25, args.steps // (COPIES * 4) or 1))
+    per_graph = COPIES * max(1, min(25, args.steps // (COPIES * 20)))  # >= 20 repetitions when steps allow
     g_plain = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_plain, stream=stream):
         for i in range(per_graph):
@@ -261,25 +280,37 @@ def run_gpu(args, rank, world, local_rank):
         for _ in range(warm_reps):
             g_plain.replay()
     barrier()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one event per replay boundary inside the timed region: `reps` repetitions of `per_graph` steps each
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
     with ClockSampler(local_rank) as clk, torch.cuda.stream(stream):
-        t0.record(stream)
-        for _ in range(reps):
+        marks[0].record(stream)
+        for i in range(reps):
             g_plain.replay()
-        t1.record(stream)
+            marks[i + 1].record(stream)
         barrier()
-    ms_total = t0.elapsed_time(t1)
+    ms_total = marks[0].elapsed_time(marks[-1])
+    rep_ms = sorted(marks[i].elapsed_time(marks[i + 1]) / per_graph for i in range(reps))
+    rep_stats = {"reps": reps, "steps_per_rep": per_graph, "median_ms_per_step": round(statistics.median(rep_ms), 6),
+                 "min_ms_per_step": round(rep_ms[0], 6), "max_ms_per_step": round(rep_ms[-1], 6)}
     # kernel durations: event nodes around each launch inside the step graph (its own timed region);
     # where event nodes are unavailable, a graph of back-to-back launches of that stage alone
     stages = ["index", "topk", "attend"] if copies[0].has_index else ["attend"]
     k_ms, timing = {}, "event nodes around each launch in the step graph"
+    k_launches = 0
     try:
         if g_timed is None:
             raise RuntimeError("no external events")
-        with torch.cuda.stream(stream):
-            g_timed.replay()
-        torch.cuda.synchronize()
-        k_ms = {n: statistics.mean(a.elapsed_time(b) for a, b in ev[n]) for n in stages}
+        samples = {n: [] for n in stages}
+        for _ in range(max(1, math.ceil(100 / per_graph))):   # >= 100 launches of each timed kernel
+            with torch.cuda.stream(stream):
+                g_timed.replay()
+            torch.cuda.synchronize()
+            for n in stages:
+                samples[n] += [a.elapsed_time(b) for a, b in ev[n]]
+        k_ms = {n: statistics.median(samples[n]) for n in stages}
+        k_launches = len(samples[stages[0]])
+        timing = (f"median over {k_launches} launches; event nodes around each launch in a step graph (which "
+                  f"also removes that launch's programmatic-launch overlap with its neighbours)")
     except RuntimeError:
         timing = "graph of back-to-back launches of the stage alone"
         for n in stages:
@@ -297,6 +328,7 @@ def run_gpu(args, rank, world, local_rank):
                 b.record(stream)
             torch.cuda.synchronize()
             k_ms[n] = a.elapsed_time(b) / (4 * per_graph)
+            k_launches = 4 * per_graph
     status = max(int(c.status.item()) for c in copies)
 
     # e2e: host (pinned) inputs -> device, step, output -> host, all inside the timed region
@@ -329,6 +361,13 @@ def run_gpu(args, rank, world, local_rank):
         roof = {"kernel": dominant, "bound": "tensor", "achieved": round(kern[dominant]["tflops"], 1), "peak": tfl,
                 "unit": "TFLOP/s", "frac": round(kern[dominant]["tflops"] / tfl, 4),
                 "traffic": ncu_traffic(dominant, args.workload), "peak_source": f"{src} bf16_tflops (burst)"}
+    # the attention's other bound beside the headline one: dense c128a decode streams 128 flop per byte, so
+    # both its HBM fraction and its bf16 tensor fraction are reported
+    a = kern["attn_kernel"]
+    roof_other = {"kernel": "attn_kernel",
+                  "hbm": {"achieved": round(a["gbs"], 1), "peak": hbm, "unit": "GB/s", "frac": round(a["gbs"] / hbm, 4)},
+                  "tensor": {"achieved": round(a["tflops"], 1), "peak": tfl, "unit": "TFLOP/s",
+                             "frac": round(a["tflops"] / tfl, 4), "peak_source": f"{src} bf16_tflops (burst)"}}
     launches_per_step = copies[0].launches_per_step()
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": steps,
@@ -340,7 +379,8 @@ def run_gpu(args, rank, world, local_rank):
         "config": workload_config(args.workload, spec, world),
         "step_bytes": idx_bytes + att_bytes, "step_gbs": round((idx_bytes + att_bytes) / (ms_step * 1e6), 1),
         "kernels": {n: {k: round(v, 6) for k, v in d.items()} for n, d in kern.items()}, "kernel_timing": timing,
-        "roofline": roof, "gpu_launches": launches_per_step * steps, "device_status": status,
+        "roofline": roof, "attention_roofline": roof_other, "timing": rep_stats, "kernel_launches_timed": k_launches,
+        "gpu_launches": launches_per_step * steps, "device_status": status,
         "e2e": {"value": round(q_step * world / (e2e_ms / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e_ms, 6)},
         "clocks": clk.summary(),
@@ -487,8 +527,43 @@ def cpu_cores():
         return os.cpu_count()
 
 
-def cpu_baseline(spec, case, seconds):
-    """Time the oracle on a bounded sample (about `seconds` of CPU work) of the workload."""
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
+def one_thread_baseline(workload, n_requests):
+    """The oracle sample of the first n requests in a child process whose BLAS / OpenMP pools have one thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; from compressed_sparse_attention_c4a_gb300 import synth; "
+            "spec = synth.case_specs()[%r]; case = synth.make_case(spec, 'cpu'); "
+            "rows = None if spec.queries == 'last' else 2; t, q, _ = bench.oracle_sample(spec, case, %d, rows); "
+            "print(json.dumps({'t': t, 'q': q}))") % (ROOT, workload, n_requests)
+    try:
+        res = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+        r = json.loads(res.stdout.strip().splitlines()[-1])
+        return {"value": round(r["q"] / r["t"], 3), "unit": UNIT, "cores": 1, "seconds": round(r["t"], 2),
+                "sample": f"the same oracle step for {r['q']} query tokens, one thread"}
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError, KeyError):
+        return None
+
+
+def cpu_baseline(spec, case, seconds, workload=None):
+    """Time the oracle on a bounded sample (about `seconds` of CPU work) of the workload, on every host core
+    the process may use and (in a child process) on one thread."""
     per_req_rows = None if spec.queries == "last" else 2
     t1, q1, _ = oracle_sample(spec, case, 1, per_req_rows)
     n = max(1, min(spec.batch, int(seconds / max(t1, 1e-3))))
@@ -498,8 +573,11 @@ def cpu_baseline(spec, case, seconds):
         t, q = t1, q1
     what = (f"oracle step (compress, index, top-k, attention) for {n} of {spec.batch} requests"
             if spec.queries == "last" else f"oracle step for {q} of {queries_per_step(spec)} query tokens")
-    return {"value": round(q / t, 3), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": what,
-            "seconds": round(t, 2)}
+    out = {"value": round(q / t, 3), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": what,
+           "seconds": round(t, 2), "cpu_model": cpu_model()}
+    if workload is not None:
+        out["one_thread"] = one_thread_baseline(workload, max(1, min(n, 4)))
+    return out
 
 
 def run_reference(args, rank, world):
@@ -526,13 +604,17 @@ def run_reference(args, rank, world):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "config": workload_config(args.workload, spec, world),
             "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def main():
     args = parse()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(relaunch_ranks(args))
     rank, world, local_rank = rank_env()
+    if world != args.gpus:
+        raise SystemExit(f"bench.py --gpus {args.gpus} under a launcher of {world} rank(s)")
     if args.impl == "reference":
         line = run_reference(args, rank, world)
         if line is not None:
@@ -541,7 +623,7 @@ def main():
     line, copies = run_gpu(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(copies[0].spec, copies[0].case, args.cpu_seconds)
+            line["cpu_baseline"] = cpu_baseline(copies[0].spec, copies[0].case, args.cpu_seconds, args.workload)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

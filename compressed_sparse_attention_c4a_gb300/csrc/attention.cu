@@ -78,7 +78,10 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
         M = fmaxf(M, a.ws_ml[(((long long)row * a.nsplit + sp) * a.heads + head) * 4]);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float Ls = 0.f, Es = 0.f;
-    for (int sp = 0; sp < a.nsplit; ++sp) {
+    bool fault = false;
+    for (int sp = 0; sp < a.nsplit; ++sp)
+        fault |= a.ws_ml[(((long long)row * a.nsplit + sp) * a.heads + head) * 4 + 3] != 0.f;
+    for (int sp = 0; sp < a.nsplit && !fault; ++sp) {
         const long long b = ((long long)row * a.nsplit + sp) * a.heads + head;
         const float ms = a.ws_ml[b * 4], ls = a.ws_ml[b * 4 + 1], es = a.ws_ml[b * 4 + 2];
         if (ms == -INFINITY) continue;
@@ -175,8 +178,9 @@ struct ClSmem {
     static constexpr int kOffFac = kOffStat + 4 * NH * 16;          // float f[NH], L[NH], M[NH], 1/L[NH], E[NH]
     static constexpr int kOffBt = kOffFac + 5 * NH * 4;             // int [kBtCache]: the request's main block table
     static constexpr int kOffSwb = kOffBt + kBtCache * 4;           // int [8]: window-pool blocks from that of wlo
+    static constexpr int kOffFault = kOffSwb + 32;                  // int: a key of this CTA hit a device fault
     static constexpr int kBars = 2 * kClStages + 6;
-    static constexpr int kOffBar = kOffSwb + 32;                    // kBars mbarriers, TMEM address
+    static constexpr int kOffBar = kOffFault + 16;                  // kBars mbarriers, TMEM address
     static constexpr int kBytes = kOffBar + kBars * 8 + 16;
     static constexpr int kAlloc = kBytes + 1024;                    // + alignment slack
     static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
@@ -225,6 +229,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     uint64_t* qfull = pvdone + kClStages;                               // query rows loaded
     uint64_t* xfull = qfull + 1;                                        // exchanged tiles loaded
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(xfull + 1);
+    volatile int* s_fault = reinterpret_cast<volatile int*>(smem + L::kOffFault);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int crank = (int)cluster_ctarank(), csize = (int)cluster_nctarank();
@@ -243,6 +248,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         }
         mbar_init(qfull, 1);
         mbar_init(xfull, 1);
+        *s_fault = 0;
         fence_barrier_init();
     }
     if constexpr (NH < 64)  // the S product reads 64 query rows: rows NH.. are zero
@@ -264,7 +270,10 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const int r = a.q_req ? a.q_req[row] : row;
     const int m = a.q_pos[row];
     const bool row_ok = r >= 0 && r < a.main_bt.batch && r < a.swa_bt.batch && m >= 0;
-    if (!row_ok && tid == 0 && crank == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
+    if (!row_ok && tid == 0) {
+        *s_fault = 1;
+        if (crank == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
+    }
     const int n_vis = row_ok ? entries_formed((long long)m + 1, a.kind_w, a.kind_s) : 0;
     const int n_comp = a.topk ? a.k : n_vis;
     const int ncp = (n_comp + 3) & ~3;
@@ -303,14 +312,19 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 if (j < n_comp && id >= 0) {
                     if (id >= n_vis) {
                         report(a.status, DSA_ERR_DEVICE_FAULT);
+                        *s_fault = 1;
                     } else {
                         const int epb = a.main.rows_per_block;
                         const int lb = id / epb;
                         const int pb = lb < a.main_bt.max_blocks
                                            ? (bt_cached ? s_bt[lb] : __ldg(a.main_bt.table + (long long)r * a.main_bt.max_blocks + lb))
                                            : -1;
-                        if (pb < 0 || pb >= a.main.num_blocks) report(a.status, DSA_ERR_DEVICE_FAULT);
-                        else v = pb * epb + (id - lb * epb);
+                        if (pb < 0 || pb >= a.main.num_blocks) {
+                            report(a.status, DSA_ERR_DEVICE_FAULT);
+                            *s_fault = 1;
+                        } else {
+                            v = pb * epb + (id - lb * epb);
+                        }
                     }
                 }
             } else if (j < n_keys) {
@@ -318,8 +332,12 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 const int pos = wlo + (j - ncp);
                 const int lb = pos / kBlockPositions;
                 const int pb = s_swb[lb - wlo / kBlockPositions];  // the window (<= 1024 positions) spans <= 5 blocks
-                if (pb < 0 || pb >= a.swa.num_blocks) report(a.status, DSA_ERR_DEVICE_FAULT);
-                else v = pb * kBlockPositions + (pos - lb * kBlockPositions);
+                if (pb < 0 || pb >= a.swa.num_blocks) {
+                    report(a.status, DSA_ERR_DEVICE_FAULT);
+                    *s_fault = 1;
+                } else {
+                    v = pb * kBlockPositions + (pos - lb * kBlockPositions);
+                }
             }
             if (v >= 0 && R > 0) {  // rows of later rounds start moving into L2 (the first round is gathered at once)
                 constexpr int kRowBytes = FP8 ? kD : 2 * kD;
@@ -662,12 +680,13 @@ __global__ void __launch_bounds__(kClThreads, 1)
     cluster_wait();  // phase 0: every CTA of the cluster has started
     if (csize > 1 && tid == 0)  // before any peer can push (pushes follow phase 1)
         mbar_arrive_expect_tx(xfull, (uint32_t)((csize - 1) * tiles_per * L::kTile));
+    const float fo = *s_fault ? 1.f : 0.f;  // this CTA met a device fault: the whole row is written as zeros
     for (int h = tid; h < NH; h += kClThreads) {
         const uint32_t dst = smem_u32(s_stat + (crank * NH + h) * 4);
         const float mo = have ? s_own[h] : -INFINITY, lo = have ? s_own[NH + h] : 0.f,
                     eo = have ? s_own[2 * NH + h] : 0.f;
         for (int q = 0; q < csize; ++q)
-            st_cluster_v4(mapa_shared(dst, (uint32_t)q), mo, lo, eo, 0.f);
+            st_cluster_v4(mapa_shared(dst, (uint32_t)q), mo, lo, eo, fo);
     }
     cluster_arrive();  // phase 1: statistics delivered; every CTA's products are complete
     cluster_wait();
@@ -675,20 +694,24 @@ __global__ void __launch_bounds__(kClThreads, 1)
         float M = -INFINITY;
         for (int q = 0; q < csize; ++q) M = fmaxf(M, s_stat[(q * NH + h) * 4]);
         float Ls = 0.f, Es = 0.f;
+        bool fault = false;
         for (int q = 0; q < csize; ++q) {
             const float mq = s_stat[(q * NH + h) * 4];
+            fault |= s_stat[(q * NH + h) * 4 + 3] != 0.f;
             if (mq != -INFINITY) {
                 const float fq = exp2f(mq - M);
                 Ls += s_stat[(q * NH + h) * 4 + 1] * fq;
                 Es += s_stat[(q * NH + h) * 4 + 2] * fq;
             }
         }
+        if (fault) Ls = Es = 0.f;  // every CTA of the cluster sees the same flags: zero factors, zero output
         const float mo = s_stat[(crank * NH + h) * 4];
-        s_fac[h] = mo == -INFINITY ? 0.f : exp2f(mo - M);
+        s_fac[h] = (mo == -INFINITY || fault) ? 0.f : exp2f(mo - M);
         s_L[h] = Ls;
-        s_M[h] = M;
+        s_M[h] = fault ? -INFINITY : M;
         s_inv[h] = Ls > 0.f ? 1.f / Ls : 0.f;
         s_E[h] = Es;
+        if (h == 0) s_vote[0] = fault ? 1 : 0;  // (softmax votes are done) the row's fault flag for the partials
     }
     __syncthreads();
     float f[G], inv[G];
@@ -803,7 +826,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 a.ws_ml[b * 4 + 0] = Ls > 0.f ? M : -INFINITY;
                 a.ws_ml[b * 4 + 1] = Ls;
                 a.ws_ml[b * 4 + 2] = Es;
-                a.ws_ml[b * 4 + 3] = 0.f;
+                a.ws_ml[b * 4 + 3] = s_vote[0] ? 1.f : 0.f;  // a faulted split zeroes the row in the combine
             }
         }
     }
@@ -1026,24 +1049,44 @@ static __device__ __align__(256) uint8_t g_attn_scratch[kStaticScratchBytes];
 constexpr int kMaxDevices = 64;
 static std::mutex g_scratch_mutex;
 static void* g_scratch_addr[kMaxDevices];
+static CUcontext g_scratch_ctx[kMaxDevices];
 
-// Device address of the array on the current device.  In host code `g_attn_scratch` names a
-// host-side stand-in, not device memory, so the address is looked up once per device (with that
-// device current) and cached.
+// The calling thread's current driver context (the one the array's device copy belongs to), through the
+// runtime's driver entry point (no libcuda link dependency); NULL if it cannot be queried.
+static CUcontext current_context() {
+    static PFN_cuCtxGetCurrent_v4000 fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    }();
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+
+// Device address of the array in the current device's current context.  In host code `g_attn_scratch`
+// names a host-side stand-in, not device memory, so the address is looked up (with that device current)
+// and cached per device together with the context it belongs to; a different context on the same device
+// (after cudaDeviceReset, or a caller-created context) looks it up again.
 static void* static_scratch(int* status) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         *status = DSA_ERR_CUDA;
         return nullptr;
     }
+    const CUcontext ctx = current_context();
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev] || !ctx || g_scratch_ctx[dev] != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || !p) {
             *status = DSA_ERR_CUDA;
             return nullptr;
         }
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = current_context();  // the runtime makes a primary context current if none was
     }
     *status = DSA_OK;
     return g_scratch_addr[dev];

@@ -54,6 +54,8 @@ struct IdxArgs {
     float* scores;
     int32_t* n_visible;
     int32_t* status;
+    unsigned long long wait_ns;  // limit of every bounded wait
+    int withhold;                // test hook: the producer issues no copy and posts no stage
 };
 
 // Shared-memory matrix descriptor of a K-major operand whose rows are `row_bytes` (64 or 128) long,
@@ -140,13 +142,13 @@ __device__ __forceinline__ ItemInfo shfl_item(const ItemInfo& x, int src) {
 
 // Bounded wait that also gives up once another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                              int32_t* status) {
+                                              int32_t* status, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             *abort_flag = 1;
             report(status, DSA_ERR_TIMEOUT);
             return false;
@@ -322,7 +324,8 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
             pdl_launch_dependents();
         }
         if (bad_group) report(a.status, DSA_ERR_DEVICE_FAULT);
-        for (long long base = lo; base < hi && alive; base += kChunkItems) {
+        // (test hook) withhold: no copy is issued and no stage posted, so every consumer wait runs out
+        for (long long base = lo; base < hi && alive && !a.withhold; base += kChunkItems) {
             const ItemInfo nxt = resolve(base + kChunkItems);
             for (int u = 0; u < kChunkItems; ++u) {
                 ItemInfo it = shfl_item(cur, u);
@@ -349,7 +352,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                     // the other buffer, once the epilogue has let go of that buffer's previous group
                     gb ^= 1;
                     bool ok = true;
-                    if (lane == 0 && guse[gb] > 0) ok = wait_or_abort(&gempty[gb], (guse[gb] - 1) & 1, abort_flag, a.status);
+                    if (lane == 0 && guse[gb] > 0) ok = wait_or_abort(&gempty[gb], (guse[gb] - 1) & 1, abort_flag, a.status, a.wait_ns);
                     if (!__shfl_sync(0xffffffffu, ok, 0)) {
                         alive = false;
                     } else {
@@ -371,7 +374,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                 const int s = ps;
                 bool go = false;
                 if (lane == 0 && alive) {
-                    go = wait_or_abort(&empty[s], pphase ^ 1, abort_flag, a.status);
+                    go = wait_or_abort(&empty[s], pphase ^ 1, abort_flag, a.status, a.wait_ns);
                     alive = go;
                 }
                 go = __shfl_sync(0xffffffffu, go, 0);
@@ -424,11 +427,11 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
             pdl_wait();
             pdl_launch_dependents();
         }
-        {  // terminal stage: consumers stop here (33 arrivals, no bytes)
+        if (!a.withhold) {  // terminal stage: consumers stop here (33 arrivals, no bytes)
             const int s = ps;
             bool go = false;
             if (lane == 0 && alive) {
-                go = wait_or_abort(&empty[s], pphase ^ 1, abort_flag, a.status);
+                go = wait_or_abort(&empty[s], pphase ^ 1, abort_flag, a.status, a.wait_ns);
                 if (go) stage_meta(s)->terminal = 1;
             }
             go = __shfl_sync(0xffffffffu, go, 0);
@@ -444,8 +447,8 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
         int prev_gb = -1, muse[2] = {0, 0};
         int s = 0, sph = 0, b = 0, bph = 0;  // stage / accumulator index and phase parity
         for (int n = 0;; ++n) {
-            bool ok = wait_or_abort(&full[s], sph, abort_flag, a.status);
-            ok = ok && wait_or_abort(&tempty[b], bph ^ 1, abort_flag, a.status);
+            bool ok = wait_or_abort(&full[s], sph, abort_flag, a.status, a.wait_ns);
+            ok = ok && wait_or_abort(&tempty[b], bph ^ 1, abort_flag, a.status, a.wait_ns);
             if (!__all_sync(0xffffffffu, ok)) break;
             if (stage_meta(s)->terminal) {
                 if (lane == 0) mbar_arrive(&tfull[b]);
@@ -455,7 +458,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
             if (gbi != prev_gb) {  // the first item of a group: its buffer's load
                 prev_gb = gbi;
                 ++muse[gbi];
-                ok = wait_or_abort(&gfull[gbi], (muse[gbi] - 1) & 1, abort_flag, a.status);
+                ok = wait_or_abort(&gfull[gbi], (muse[gbi] - 1) & 1, abort_flag, a.status, a.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) break;
             }
             tc_fence_after();
@@ -493,7 +496,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
         int prev_gb = -1, euse[2] = {0, 0};
         int s = 0, sph = 0, b = 0, bph = 0;  // stage / accumulator index and phase parity
         for (int n = 0;; ++n) {
-            bool ok = wait_or_abort(&full[s], sph, abort_flag, a.status);  // completed: orders the meta
+            bool ok = wait_or_abort(&full[s], sph, abort_flag, a.status, a.wait_ns);  // completed: orders the meta
             if (!__all_sync(0xffffffffu, ok)) break;
             const StageMeta* meta = stage_meta(s);
             if (meta->terminal) break;
@@ -504,9 +507,9 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                 if (prev_gb >= 0 && lane == 0) mbar_arrive(&gempty[prev_gb]);
                 prev_gb = gbi;
                 ++euse[gbi];
-                ok = wait_or_abort(&gfull[gbi], (euse[gbi] - 1) & 1, abort_flag, a.status);
+                ok = wait_or_abort(&gfull[gbi], (euse[gbi] - 1) & 1, abort_flag, a.status, a.wait_ns);
             }
-            ok = ok && wait_or_abort(&tfull[b], bph, abort_flag, a.status);
+            ok = ok && wait_or_abort(&tfull[b], bph, abort_flag, a.status, a.wait_ns);
             if (!__all_sync(0xffffffffu, ok)) break;  // warp-uniform: tcgen05.ld is warp-collective
             tc_fence_after();
             const uint8_t* gp = gbase + (size_t)gbi * a.gbuf_bytes;
@@ -689,11 +692,11 @@ static dsa_status_t launch_index_heads(const CUtensorMap& kmap, const CUtensorMa
 
 using namespace dsa;
 
-extern "C" dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8,
-                                         const float* q_scale, const float* w, const int32_t* q_pos,
-                                         const int32_t* q_req, int32_t q_group, const dsa_pool_t* keys,
-                                         const dsa_block_table_t* bt, float* scores, int32_t ld, int32_t* n_visible,
-                                         const int32_t* fresh_from, int32_t* dev_status, void* stream) {
+static dsa_status_t index_scores(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8, const float* q_scale,
+                                 const float* w, const int32_t* q_pos, const int32_t* q_req, int32_t q_group,
+                                 const dsa_pool_t* keys, const dsa_block_table_t* bt, float* scores, int32_t ld,
+                                 int32_t* n_visible, const int32_t* fresh_from, int32_t* dev_status, void* stream,
+                                 uint64_t wait_ns, int withhold) {
     if (nq < 0 || ld < 0 || (ld & 3)) return DSA_ERR_INVALID_ARG;
     if (nq == 0) return DSA_OK;
     if (heads != 4 && heads != 8 && heads != 16) return DSA_ERR_UNSUPPORTED;
@@ -728,6 +731,8 @@ extern "C" dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim,
     a.scores = scores;
     a.n_visible = n_visible;
     a.status = dev_status;
+    a.wait_ns = wait_ns;
+    a.withhold = withhold;
     CUtensorMap kmap, qmap;
     if (!make_map(&kmap, keys->data, (uint64_t)keys->num_blocks * kPage, dim, kPage)) return DSA_ERR_CUDA;
     if (!make_map(&qmap, q8, (uint64_t)nq * heads, dim, n_cols)) return DSA_ERR_CUDA;
@@ -735,4 +740,26 @@ extern "C" dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim,
     a.n_groups = (nq + q_group - 1) / q_group;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return dim == 128 ? launch_index_heads<128>(kmap, qmap, a, st) : launch_index_heads<64>(kmap, qmap, a, st);
+}
+
+extern "C" dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8,
+                                         const float* q_scale, const float* w, const int32_t* q_pos,
+                                         const int32_t* q_req, int32_t q_group, const dsa_pool_t* keys,
+                                         const dsa_block_table_t* bt, float* scores, int32_t ld, int32_t* n_visible,
+                                         const int32_t* fresh_from, int32_t* dev_status, void* stream) {
+    return index_scores(nq, heads, dim, q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, ld, n_visible,
+                        fresh_from, dev_status, stream, kWaitLimitNs, 0);
+}
+
+// Test hook of the bounded waits: the same launch with a caller-chosen wait limit and the copy-issuing warp
+// withholding every copy, so that the consumers' waits run out while nothing is in flight.
+extern "C" dsa_status_t dsa_debug_index_scores_stalled(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8,
+                                                       const float* q_scale, const float* w, const int32_t* q_pos,
+                                                       const int32_t* q_req, int32_t q_group, const dsa_pool_t* keys,
+                                                       const dsa_block_table_t* bt, float* scores, int32_t ld,
+                                                       int32_t* n_visible, uint64_t wait_limit_ns, int32_t* dev_status,
+                                                       void* stream) {
+    if (wait_limit_ns == 0 || wait_limit_ns > kWaitLimitNs) return DSA_ERR_INVALID_ARG;
+    return index_scores(nq, heads, dim, q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, ld, n_visible,
+                        nullptr, dev_status, stream, wait_limit_ns, 1);
 }

@@ -21,7 +21,7 @@ KIND = {"c4a": DSA_C4A, "c128a": DSA_C128A}
 
 EXPORTS = ["dsa_status_string", "dsa_compress", "dsa_index_scores", "dsa_topk", "dsa_topk_plan", "dsa_attn_workspace_size",
            "dsa_sparse_attn_decode", "dsa_sparse_attn_prefill", "dsa_gather_rows", "dsa_sparse_attn_decode_static",
-           "dsa_attn_static_scratch_bytes", "dsa_attn_plan"]
+           "dsa_attn_static_scratch_bytes", "dsa_attn_plan", "dsa_debug_index_scores_stalled"]
 
 
 class DsaPool(ctypes.Structure):
@@ -58,6 +58,8 @@ _lib.dsa_topk_plan.argtypes = [_I, _I, _I, _P]
 for _name, _args in {
     "dsa_compress": [_I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P],
     "dsa_index_scores": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P],
+    "dsa_debug_index_scores_stalled": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, ctypes.c_uint64, _P,
+                                       _P],
     "dsa_topk": [_I, _P, _I, _P, _I, _P, _P, _P],
     "dsa_sparse_attn_decode": [_I, _I, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, ctypes.c_float, _P, _P, _P, _P,
                                ctypes.c_size_t, _P, _P],
@@ -128,6 +130,18 @@ def dsa_index_scores(q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, n_
                                  int(q_group), ctypes.byref(keys), ctypes.byref(bt), _ptr(scores), scores.shape[1],
                                  _ptr(n_visible), _ptr(fresh_from), _ptr(dev_status), _stream(stream))
     _check("dsa_index_scores", code)
+
+
+def dsa_debug_index_scores_stalled(q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, wait_limit_ns,
+                                   n_visible=None, dev_status=None, stream=None):
+    """Test hook: the indexer launch with every copy withheld, so its bounded waits run out after
+    ``wait_limit_ns`` (see include/dsa.h)."""
+    nq, heads, dim = q8.shape
+    code = _lib.dsa_debug_index_scores_stalled(nq, heads, dim, _ptr(q8), _ptr(q_scale), _ptr(w), _ptr(q_pos),
+                                               _ptr(q_req), int(q_group), ctypes.byref(keys), ctypes.byref(bt),
+                                               _ptr(scores), scores.shape[1], _ptr(n_visible), int(wait_limit_ns),
+                                               _ptr(dev_status), _stream(stream))
+    _check("dsa_debug_index_scores_stalled", code)
 
 
 def dsa_topk(scores, n_valid, k, idx_out, dev_status=None, stream=None):

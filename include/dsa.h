@@ -164,6 +164,21 @@ dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim, const uint
                               int32_t* n_visible, const int32_t* fresh_from, int32_t* dev_status, void* stream);
 
 /*
+ * dsa_debug_index_scores_stalled - test hook of the bounded waits in dsa_index_scores; the pages have no
+ * counterpart.  Launches the indexer as dsa_index_scores would (fresh_from = NULL), except that the warp that
+ * issues the key and query copies issues none and posts no work, so the tensor-core and epilogue warps wait
+ * for tiles that never arrive.  Each of their waits gives up after wait_limit_ns nanoseconds (of
+ * %globaltimer): the kernel records DSA_ERR_TIMEOUT in dev_status, every warp leaves its loop, the tensor
+ * memory is freed and the kernel returns, with nothing in flight.  The scores are not written; n_visible is.
+ * wait_limit_ns: 1 .. 2e9 (else DSA_ERR_INVALID_ARG).  Other arguments and checks as dsa_index_scores.
+ */
+dsa_status_t dsa_debug_index_scores_stalled(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8,
+                                            const float* q_scale, const float* w, const int32_t* q_pos,
+                                            const int32_t* q_req, int32_t q_group, const dsa_pool_t* keys,
+                                            const dsa_block_table_t* bt, float* scores, int32_t ld, int32_t* n_visible,
+                                            uint64_t wait_limit_ns, int32_t* dev_status, void* stream);
+
+/*
  * dsa_topk - per-query top-k of indexer scores.  [P1] §4.2: S_t = TopK(I_{t,:}, k).
  * Row q selects the k largest of scores[q][0 .. n_valid[q]), ties broken toward the
  * lower index, so the selected set is unique; idx_out[q] lists it in increasing index

@@ -66,13 +66,15 @@ class Pool:
 
 
 def compress(kind, start_pos, x_new, z_new, states, rope_dim, out_pool, out_bt,
-             swa_pool=None, swa_bt=None, gamma=None, eps=1e-6, theta=ROPE_THETA):
+             swa_pool=None, swa_bt=None, gamma=None, eps=1e-6, theta=ROPE_THETA, record=None):
     """Append new raw tokens per request, emitting every entry they close.
 
     start_pos [B]; x_new[r] [n_r][d] and z_new[r] [n_r] hold request r's new tokens at
     positions start_pos[r] .. start_pos[r] + n_r - 1; states[r] is its RollingState,
     updated in place.  Entry i goes to ``out_pool`` logical row i; with an SWA pool,
     token p goes to its logical row p as R_p x_p.  Returns the emitted entry ids per request.
+    With a dict ``record``, the float64 rows before storage rounding are also kept there:
+    record[("entry", r, i)] and record[("swa", r, p)].
     """
     emitted = []
     for r in range(len(start_pos)):
@@ -84,8 +86,13 @@ def compress(kind, start_pos, x_new, z_new, states, rope_dim, out_pool, out_bt,
                 i, entry = res
                 out_pool.write(out_bt[r], [i], entry)
                 got.append(i)
+                if record is not None:
+                    record[("entry", r, i)] = entry
             if swa_pool is not None:
-                swa_pool.write(swa_bt[r], [p], swa_rows(np.asarray(x_new[r][j])[None], [p], rope_dim, theta))
+                row = swa_rows(np.asarray(x_new[r][j])[None], [p], rope_dim, theta)
+                swa_pool.write(swa_bt[r], [p], row)
+                if record is not None:
+                    record[("swa", r, p)] = row[0]
         emitted.append(got)
     return emitted
 

@@ -6,13 +6,17 @@ Tolerances (fixed in the tests that use them):
   * top-k sets: identical except elements whose oracle score lies within 1e-3 relative of the
     oracle's k-th score;
   * attention outputs: max abs <= 2e-2 and rel-L2 <= 1e-2 (bf16 / fp8 data);
-  * compressor rows and indexer scores: rel-L2 <= 1e-2.
+  * compressor rows and indexer scores: rel-L2 <= 1e-2, for every row (entry, or query's score row);
+  * e4m3 rows (fp8 pools): an e4m3 code decides an integer from a float, so each code is checked as a
+    correct round-to-nearest of the oracle's float64 value divided by the row scale (up to a relative
+    slack of 1e-4 of that value: the GPU's fp32 value may sit on the other side of a rounding midpoint),
+    and the row scale as amax/448 within 1e-5 relative.
 """
 import numpy as np
 import torch
 
 from oracle import layer as OL, compress as OC
-from oracle.codecs import fp8_dequantize_rows
+from oracle.codecs import fp8_dequantize_rows, fp8_row_scale, e4m3_decode
 
 ATTN_MAX_ABS = 2e-2
 ATTN_REL_L2 = 1e-2
@@ -81,3 +85,60 @@ def topk_sets_match(gpu_idx, oracle_scores, n_valid, k):
     diff = got ^ want
     ok = all(abs(s[i] - kth) <= tol for i in diff if 0 <= i < n_valid) and len(got) == len(want)
     return ok, len(diff)
+
+
+FP8_VALUE_SLACK = 1e-4
+FP8_SCALE_REL = 1e-5
+
+
+def e4m3_half_spacing(a):
+    """Half the e4m3 grid spacing at magnitude a: subnormals 2^-10, normals 2^(floor(log2 a) - 4)."""
+    a = np.asarray(a, np.float64)
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -6)))
+    return np.where(a < 2.0 ** -6, 2.0 ** -10, 2.0 ** (e - 4))
+
+
+def fp8_row_violations(codes, scale, values):
+    """Elements of e4m3 rows (codes uint8 [n][d], fp32 scale [n]) that are not a correct rounding of the
+    float64 values [n][d] / scale; and rows whose scale is not amax/448.  Returns (bad_elements, bad_rows)."""
+    codes = np.asarray(codes, np.uint8)
+    scale = np.asarray(scale, np.float64)
+    values = np.asarray(values, np.float64)
+    want_scale = fp8_row_scale(values)
+    bad_rows = np.nonzero(np.abs(scale - want_scale) > FP8_SCALE_REL * want_scale)[0]
+    u = values / scale[:, None]
+    dec = e4m3_decode(codes)
+    a = np.abs(u)
+    sat = a >= 448.0
+    err = np.abs(dec - u)
+    ok = err <= e4m3_half_spacing(np.minimum(a, 448.0)) + FP8_VALUE_SLACK * a + 1e-12
+    ok = np.where(sat, np.abs(dec) == 448.0, ok) & ((dec == 0) | (np.sign(dec) == np.sign(u)) | (a < 2.0 ** -10))
+    return np.argwhere(~ok), bad_rows
+
+
+def check_rows(got, want, tol=ROW_REL_L2, what="row"):
+    """Per-row rel-L2 of float64 rows [n][d]; returns the worst (rel-L2, max abs)."""
+    got, want = np.asarray(got, np.float64), np.asarray(want, np.float64)
+    worst, mabs = 0.0, 0.0
+    for j in range(len(got)):
+        e = rel_l2(got[j], want[j])
+        assert e <= tol, (what, j, e)
+        worst = max(worst, e)
+        if got[j].size:
+            mabs = max(mabs, float(np.max(np.abs(got[j] - want[j]))))
+    return worst, mabs
+
+
+def check_pool_rows(gdata, gscale, prows, values, stored):
+    """GPU pool rows (physical ids) against the oracle: bf16 rows per-row rel-L2 against the oracle's stored
+    (rounded) rows; e4m3 rows code by code against the oracle's float64 values before rounding."""
+    if gdata.dtype == torch.bfloat16:
+        return check_rows(pool_rows(gdata, gscale, prows), stored)
+    d = gdata.detach().cpu()
+    codes = d[prows].numpy()
+    scale = np64(gscale.detach().cpu()[prows])
+    bad_el, bad_rows = fp8_row_violations(codes, scale, values)
+    assert len(bad_rows) == 0, ("e4m3 row scale", bad_rows[:8])
+    assert len(bad_el) == 0, ("e4m3 code", bad_el[:8])
+    deq = fp8_dequantize_rows(codes, scale)
+    return check_rows(deq, np.asarray(values), tol=2.0 ** -4, what="e4m3 row within the format's bound")

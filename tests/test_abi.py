@@ -101,3 +101,29 @@ def test_topk_plan_host_only(lib):
     assert lib.dsa_topk_plan(1, 1026, 512, plan) == 1              # ld not a multiple of 4
     assert lib.dsa_topk_plan(1, 1024, 0, plan) == 1                # k < 1
     assert lib.dsa_topk_plan(1, 1024, 512, None) == 1
+
+
+def test_static_attention_scratch_covers_every_plan_host_only(lib):
+    """The allocation-free decode call needs dsa_attn_workspace_size() bytes of its fixed array.  A row's keys
+    split over several clusters only while its clusters leave SMs idle, so the partials stay far below the
+    array for any shape (rows x splits x clusters never exceed the SM count); the size check runs before any
+    device call, and a shape that needs partials passes it (its next failure here is the missing device,
+    or the NULL query, never DSA_ERR_UNSUPPORTED)."""
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    cap = dsa.dsa_attn_static_scratch_bytes()
+    worst = 0
+    for rows in list(range(1, 65)) + [100, 151, 152, 200, 4096]:
+        for heads in (16, 32, 64, 128):
+            for keys in (640, 2048 + 1024, 8192 + 128, 65536 + 128, 262144 + 128):
+                worst = max(worst, dsa.dsa_attn_workspace_size(rows, heads, keys))
+    assert 0 < worst <= cap
+    main = dsa.DsaPool(16, None, 8, 64, 512, dsa.DSA_BF16)
+    bt = dsa.DsaBlockTable(16, 4, 8)
+    swa = dsa.DsaPool(16, None, 8, 256, 512, dsa.DSA_BF16)
+    rope = dsa.rope(64)
+    assert dsa.dsa_attn_workspace_size(4, 64, 512 + 128) > 0
+    code = dsa._lib.dsa_sparse_attn_decode_static(4, 64, None, ctypes.c_void_p(16), 0, ctypes.c_void_p(16), 512,
+                                                  ctypes.byref(main), ctypes.byref(bt), ctypes.byref(swa),
+                                                  ctypes.byref(bt), 128, 0.0441941738, ctypes.byref(rope),
+                                                  ctypes.c_void_p(16), None, None, None)
+    assert code in (dsa.DSA_ERR_CUDA, dsa.DSA_ERR_INVALID_ARG)

@@ -56,3 +56,30 @@ def test_weak_scaling_aggregate_and_config():
     assert bench.algorithmic_bytes(spec) == (69201792, 20971520)
     cfg = bench.workload_config("c4a_decode_batch", spec, 4)
     assert cfg["parallelism"] == "replicas x4" and cfg["batch"] == 32
+
+
+def test_gpus_flag_starts_that_many_ranks():
+    """``bench.py --gpus 2`` outside a launcher starts two ranks itself (torch.distributed.run on 127.0.0.1);
+    rank 0 prints the one JSON line with n_gpus = 2, the other rank exits without work (the oracle arm, so
+    this runs on CPU)."""
+    import json
+    import subprocess
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--impl", "reference",
+                          "--workload", "c4a_tiny_decode", "--steps", "1", "--warmup", "0", "--cpu-seconds", "0.5"],
+                         capture_output=True, text=True, timeout=600, env=env)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+    assert line["config"]["parallelism"] == "replicas x2"
+
+
+def test_gpus_flag_inside_a_launcher_must_match_world_size():
+    import subprocess
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--impl", "reference",
+                          "--workload", "c4a_tiny_decode", "--steps", "1"], capture_output=True, text=True, timeout=300,
+                         env=env)
+    assert res.returncode != 0 and "launcher of 1 rank" in res.stderr

@@ -12,7 +12,7 @@ from compressed_sparse_attention_c4a_gb300 import synth
 from compressed_sparse_attention_c4a_gb300.step import LayerStep, SM_SCALE
 from oracle import layer as OL, attention as OA
 from _parity import (ATTN_MAX_ABS, ATTN_REL_L2, ROW_REL_L2, np64, rel_l2, to_device, oracle_pool, rolling_states,
-                     new_tokens, pool_rows, topk_sets_match)
+                     new_tokens, pool_rows, topk_sets_match, check_rows, check_pool_rows)
 
 pytestmark = pytest.mark.gpu
 S = synth.CaseSpec
@@ -33,6 +33,12 @@ CASES = {
                    main_dtype="fp8", swa_dtype="fp8", seed=16),
     "c128a_chunk": S("c128a_chunk", kind="c128a", cached=[300], new=[200], queries="all", idx_heads=0, topk=0,
                      seed=17),
+    # the method's first positions ([P2] 机制四): queries m = 0 .. 299 of a fresh request, so m < 7 sees no c4a
+    # entry (an empty score row, a top-k row of -1) and m < 127 a window shorter than 128 tokens
+    "c4a_early": S("c4a_early", cached=[0], new=[300], queries="all", seed=20),
+    # c128a from position 0: no entry before m = 127, the first one at m = 127, the second at m = 255
+    "c128a_early": S("c128a_early", kind="c128a", cached=[0], new=[300], queries="all", idx_heads=0, topk=0,
+                     seed=21),
 }
 INDEXED = [n for n, s in CASES.items() if s.idx_heads]
 
@@ -43,7 +49,7 @@ def _setup(name):
     return cpu, gpu, LayerStep(gpu)
 
 
-def _oracle_compress(cpu, which):
+def _oracle_compress(cpu, which, record=None):
     spec = cpu["spec"]
     epb = cpu["epb"]
     if which == "main":
@@ -57,39 +63,47 @@ def _oracle_compress(cpu, which):
         rope_dim = min(spec.rope_dim, spec.idx_dim)
     states = rolling_states(cpu, which)
     xs, zs = new_tokens(cpu, which)
-    emitted = OL.compress(spec.kind, np64(cpu["start_pos"]), xs, zs, states, rope_dim, pool, bt, swa, swa_bt)
+    emitted = OL.compress(spec.kind, np64(cpu["start_pos"]), xs, zs, states, rope_dim, pool, bt, swa, swa_bt,
+                          record=record)
     return pool, swa, states, emitted
 
 
 @pytest.mark.parametrize("name", list(CASES))
 def test_compress_main_and_swa(name):
+    """Every emitted entry and every new token's window row, row by row; the rolling state bit for bit."""
     cpu, gpu, step = _setup(name)
     step.compress()
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0
-    pool, swa, states, emitted = _oracle_compress(cpu, "main")
+    rec = {}
+    pool, swa, states, emitted = _oracle_compress(cpu, "main", rec)
     spec, epb = cpu["spec"], cpu["epb"]
     bt = np64(cpu["bt_main"])
-    got, want = [], []
+    prows, vals, stored = [], [], []
     for r, ids in enumerate(emitted):
         for i in ids:
-            prow = int(bt[r][i // epb]) * epb + i % epb
-            got.append(pool_rows(gpu["main_data"], gpu["main_scale"], [prow])[0])
-            want.append(pool.read(bt[r], [i])[0])
-    assert sum(len(e) for e in emitted) == len(got)
-    if got:
-        assert rel_l2(got, want) <= ROW_REL_L2
+            prows.append(int(bt[r][i // epb]) * epb + i % epb)
+            vals.append(rec[("entry", r, i)])
+            stored.append(pool.read(bt[r], [i])[0])
+    if prows:
+        check_pool_rows(gpu["main_data"], gpu["main_scale"], prows, vals, stored)
+    # the first entry a chunk closes spans tokens of the rolling state and of the chunk (when there is one)
+    start = np64(cpu["start_pos"])
+    w, st_ = synth.WINDOW[spec.kind]
+    for r, ids in enumerate(emitted):
+        if ids and start[r] > 0 and st_ * ids[0] < start[r]:
+            assert st_ * ids[0] + w - 1 >= start[r]          # the straddling entry was among those checked
     # SWA rows of every new token
     sbt = np64(cpu["bt_swa"])
-    start, cu = np64(cpu["start_pos"]), np64(cpu["cu_new"])
-    g2, w2 = [], []
+    cu = np64(cpu["cu_new"])
+    prows, vals, stored = [], [], []
     for r in range(spec.batch):
         for j in range(cu[r + 1] - cu[r]):
             p = int(start[r]) + j
-            prow = int(sbt[r][p // 256]) * 256 + p % 256
-            g2.append(pool_rows(gpu["swa_data"], gpu["swa_scale"], [prow])[0])
-            w2.append(swa.read(sbt[r], [p])[0])
-    assert rel_l2(g2, w2) <= ROW_REL_L2
+            prows.append(int(sbt[r][p // 256]) * 256 + p % 256)
+            vals.append(rec[("swa", r, p)])
+            stored.append(swa.read(sbt[r], [p])[0])
+    check_pool_rows(gpu["swa_data"], gpu["swa_scale"], prows, vals, stored)
     # rolling state: a bit-exact copy of the last w raw tokens
     gx, gz = np64(gpu["state_x"]), np64(gpu["state_z"])
     for r in range(spec.batch):
@@ -99,19 +113,22 @@ def test_compress_main_and_swa(name):
 
 @pytest.mark.parametrize("name", [n for n in INDEXED if CASES[n].index_compress])
 def test_compress_indexer_fp8(name):
+    """Indexer entries (e4m3 + amax/448 scale) code by code, row by row."""
     cpu, gpu, step = _setup(name)
     step.compress()
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0
-    pool, _, states, emitted = _oracle_compress(cpu, "index")
+    rec = {}
+    pool, _, states, emitted = _oracle_compress(cpu, "index", rec)
     bt = np64(cpu["bt_idx"])
-    got, want = [], []
+    prows, vals, stored = [], [], []
     for r, ids in enumerate(emitted):
         for i in ids:
-            prow = int(bt[r][i // 64]) * 64 + i % 64
-            got.append(pool_rows(gpu["idx_data"], gpu["idx_scale"], [prow])[0])
-            want.append(pool.read(bt[r], [i])[0])
-    assert got and rel_l2(got, want) <= ROW_REL_L2
+            prows.append(int(bt[r][i // 64]) * 64 + i % 64)
+            vals.append(rec[("entry", r, i)])
+            stored.append(pool.read(bt[r], [i])[0])
+    assert prows
+    check_pool_rows(gpu["idx_data"], gpu["idx_scale"], prows, vals, stored)
     gx = np64(gpu["state_xi"])
     for r in range(cpu["spec"].batch):
         assert np.array_equal(gx[int(np64(cpu["state_slot"])[r])], states[r].x)
@@ -123,6 +140,23 @@ def _oracle_scores_on_gpu_pool(cpu, gpu):
                            np64(cpu["q_req"]), pool, np64(cpu["bt_idx"]))
 
 
+def _check_score_rows(got, want, nvis, gn=None, ld=None):
+    """Each query's score row: rel-L2 <= 1e-2 over its visible entries, -inf to the end of their tile."""
+    rows_g, rows_w = [], []
+    for q, n in nvis.items():
+        if gn is not None:
+            assert gn[q] == n
+        if ld is not None:
+            tile_end = min(ld, ((n + 127) // 128) * 128) if n else 0
+            assert np.all(np.isneginf(got[q, n:tile_end])), q
+        if n:
+            rows_g.append(got[q, :n])
+            rows_w.append(want[q][:n])
+    for j, (g, w) in enumerate(zip(rows_g, rows_w)):
+        e = rel_l2(g, w)
+        assert e <= ROW_REL_L2, (j, e)
+
+
 @pytest.mark.parametrize("name", INDEXED)
 def test_index_scores(name):
     cpu, gpu, step = _setup(name)
@@ -131,16 +165,7 @@ def test_index_scores(name):
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0
     want, nvis = _oracle_scores_on_gpu_pool(cpu, gpu)
-    got = np64(step.scores)
-    gn = np64(step.n_visible)
-    g_all, w_all = [], []
-    for q, n in nvis.items():
-        assert gn[q] == n
-        g_all.append(got[q, :n])
-        w_all.append(want[q][:n])
-        tile_end = min(step.ld, ((n + 127) // 128) * 128) if n else 0
-        assert np.all(np.isneginf(got[q, n:tile_end]))
-    assert rel_l2(np.concatenate(g_all), np.concatenate(w_all)) <= ROW_REL_L2
+    _check_score_rows(np64(step.scores), want, nvis, np64(step.n_visible), step.ld)
 
 
 @pytest.mark.parametrize("name", ["c4a_decode", "c4a_chunk", "c4a_multi_prefill"])
@@ -166,11 +191,8 @@ def test_index_scores_signed_scales(name):
     pool = oracle_pool(gpu["idx_data"], gpu["idx_scale"], 64)
     want, nvis = OL.index_scores(np64(cpu["q8"]), np64(qs), np64(cpu["w"]), np64(cpu["q_pos"]),
                                  np64(cpu["q_req"]), pool, np64(cpu["bt_idx"]))
-    got = np64(step.scores)
-    g_all = np.concatenate([got[q, :n] for q, n in nvis.items()])
-    w_all = np.concatenate([want[q][:n] for q, n in nvis.items()])
-    assert rel_l2(g_all, w_all) <= ROW_REL_L2
-    assert np.any(w_all > 0)
+    _check_score_rows(np64(step.scores), want, nvis)
+    assert any(np.any(want[q][:n] > 0) for q, n in nvis.items())
 
 
 @pytest.mark.parametrize("name", INDEXED)
@@ -392,3 +414,119 @@ def test_index_scores_fresh_from_extremes(name):
         n = int(nv[q])
         assert np.array_equal(runs[1][q, :n], runs[0][q, :n]), q
         assert np.array_equal(runs[2][q, :n], runs[0][q, :n]), q
+
+
+# ---- device-detected faults: a needed block unmapped (-1) in one request's table ---------------------
+# Every kernel resolves its paged reads and writes through the checked block-table translation; an unmapped
+# block raises DSA_ERR_DEVICE_FAULT and affects only the rows that needed it.
+
+def test_compress_unmapped_block_faults_only_that_entry():
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    cpu, gpu, step = _setup("c4a_decode")          # new tokens 1000, 2999, 777, 4095: 2999 and 4095 close entries
+    r, i = 1, (2999 - 7) // 4                        # request 1's new entry 748, block 11 of its main table
+    prow = int(gpu["bt_main"][r, i // 64]) * 64 + i % 64
+    before = gpu["main_data"][prow].clone()
+    gpu["bt_main"][r, i // 64] = -1
+    step.compress()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == dsa.DSA_ERR_DEVICE_FAULT
+    assert torch.equal(gpu["main_data"][prow], before)           # the unmapped entry is not written anywhere
+    rec = {}
+    pool, swa, states, emitted = _oracle_compress(cpu, "main", rec)
+    assert emitted[1] == [i] and emitted[3] == [(4095 - 7) // 4]
+    bt = np64(cpu["bt_main"])
+    j = emitted[3][0]
+    check_pool_rows(gpu["main_data"], gpu["main_scale"], [int(bt[3][j // 64]) * 64 + j % 64], [rec[("entry", 3, j)]],
+                    [pool.read(bt[3], [j])[0]])
+    sbt = np64(cpu["bt_swa"])
+    start = np64(cpu["start_pos"])
+    prows = [int(sbt[q][int(start[q]) // 256]) * 256 + int(start[q]) % 256 for q in range(4)]
+    check_pool_rows(gpu["swa_data"], gpu["swa_scale"], prows, [rec[("swa", q, int(start[q]))] for q in range(4)],
+                    [swa.read(sbt[q], [int(start[q])])[0] for q in range(4)])
+
+
+def test_index_unmapped_block_scores_minus_inf():
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    cpu, gpu, step = _setup("c4a_decode")
+    step.compress()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    want, nvis = _oracle_scores_on_gpu_pool(cpu, gpu)     # with the intact table
+    r, lb = 2, 1                                         # request 2 (193 visible entries): entries 64 .. 127
+    gpu["bt_idx"][r, lb] = -1
+    step.index()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == dsa.DSA_ERR_DEVICE_FAULT
+    got = np64(step.scores)
+    assert nvis[r] == 193
+    assert np.all(np.isneginf(got[r, 64:128]))
+    keep = np.r_[0:64, 128:193]
+    assert rel_l2(got[r, keep], want[r][keep]) <= ROW_REL_L2
+    _check_score_rows(got, want, {q: n for q, n in nvis.items() if q != r})
+
+
+@pytest.mark.parametrize("wait_ms,name", [(20, "c4a_decode"), (20, "c4a_multi_prefill")])
+def test_index_bounded_wait_expires_then_next_call_is_correct(wait_ms, name):
+    """The indexer with its copies withheld: every consumer wait runs out after the given limit, the kernel
+    records DSA_ERR_TIMEOUT, frees its tensor memory and returns; the next normal call is correct."""
+    import time
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    cpu, gpu, step = _setup(name)
+    step.compress()
+    torch.cuda.synchronize()
+    c = step.case
+    scores = torch.full_like(step.scores, float("nan"))
+    t0 = time.time()
+    dsa.dsa_debug_index_scores_stalled(c["q8"], c["q_scale"], c["w"], c["q_pos"], c["q_req"], step.q_group, step.idx,
+                                       step.idx_bt, scores, wait_ms * 1_000_000, n_visible=step.n_visible,
+                                       dev_status=step.status)
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 10.0
+    assert int(step.status.item()) == dsa.DSA_ERR_TIMEOUT
+    assert bool(torch.isnan(scores).all())                       # nothing was scored
+    step.status.zero_()
+    step.index()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    want, nvis = _oracle_scores_on_gpu_pool(cpu, gpu)
+    _check_score_rows(np64(step.scores), want, nvis, np64(step.n_visible), step.ld)
+
+
+@pytest.mark.parametrize("name", ["c4a_decode", "c4a_decode_48"])
+def test_attention_unmapped_block_zeroes_the_row(name):
+    """A selected entry in an unmapped main block (one row) and an unmapped window block (another row): both
+    rows are written as zeros with lse = -inf, the others still match the oracle.  Four rows split their keys
+    over two clusters (the partials' merge kernel zeroes the row); 48 rows merge inside one cluster."""
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    spec = CASES.get(name) or SHARP[name]
+    cpu = synth.make_case(spec, "cpu")
+    gpu = to_device(cpu)
+    step = LayerStep(gpu)
+    step.compress()
+    step.index()
+    step.select()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    tk = np64(step.topk)
+    bt_main0, bt_swa0 = np64(cpu["bt_main"]), np64(cpu["bt_swa"])
+    ra, rb = 0, 3
+    ida = int(tk[ra][tk[ra] >= 0][len(tk[ra][tk[ra] >= 0]) // 2])
+    gpu["bt_main"][ra, ida // 64] = -1
+    mb = int(np64(cpu["q_pos"])[rb])
+    gpu["bt_swa"][rb, mb // 256] = -1                     # the block of row rb's own position
+    step.attend()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == dsa.DSA_ERR_DEVICE_FAULT
+    out, lse = np64(step.out), np64(step.lse)
+    for r in (ra, rb):
+        assert np.all(out[r] == 0.0), r
+        assert np.all(np.isneginf(lse[r])), r
+    main = oracle_pool(gpu["main_data"], gpu["main_scale"], cpu["epb"])
+    swa = oracle_pool(gpu["swa_data"], gpu["swa_scale"], 256)
+    rows = [q for q in range(cpu["nq"]) if q not in (ra, rb)]
+    want, wl = OL.sparse_attn(np64(cpu["q"]), np64(cpu["q_pos"]), np64(cpu["q_req"]), spec.kind, tk, main, bt_main0,
+                              swa, bt_swa0, spec.window, SM_SCALE, spec.rope_dim, rows=rows)
+    W = np.stack([want[q] for q in rows])
+    assert np.max(np.abs(out[rows] - W)) <= ATTN_MAX_ABS
+    assert rel_l2(out[rows], W) <= ATTN_REL_L2
+    assert np.max(np.abs(lse[rows] - np.stack([wl[q] for q in rows]))) <= 1e-3
