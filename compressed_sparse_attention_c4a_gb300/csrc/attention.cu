@@ -20,6 +20,7 @@ namespace dsa {
 
 constexpr int kD = 512;
 constexpr float kLog2e = 1.4426950408889634f;
+DSA_TIMELINE_BUFFER
 
 struct AttnArgs {
     int rows, heads, hg_count, nsplit, cps;   // cps = 32-key sub-tiles per split
@@ -128,35 +129,43 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
 //
 // Inside a CTA (512 threads), warp-specialised and pipelined over four 32 KB key stages (a stage is
 // gathered again as soon as its sub-tile's P V is done, so up to three gathers run ahead of the math):
-//   warps 5-15 gather: resolve keys a round (11 sub-tiles) ahead (top-k index -> block table ->
+//   warps 6-15 gather: resolve keys a round (10 sub-tiles) ahead (top-k index -> block table ->
 //              physical row, tables cached in shared memory), prefetch later rounds into L2, and copy
 //              the rows into a stage with cp.async, 128B-swizzled, laid out [64-dim chunk][32 keys]
 //              [128 B]; e4m3 rows are converted to bf16 on the way, their scales kept beside the stage;
-//   warp 4     loads the query rows (TMA, one 64-dim box per lane) and issues the MMAs (one elected lane):
-//              S   = Q K^T   : M = 64 (heads), N = 32 keys, K = 512; TMEM lanes = heads, columns = keys;
+//   warps 4-5  issue the MMAs, one elected lane each (an MMA's issue costs the issuing warp about 49
+//              cycles at these shapes, so two warps issue twice as fast); warp 4 also loads the query rows
+//              (TMA, one 64-dim box per lane):
+//              S   = Q K^T   : M = 64 (heads), N = 32 keys, K = 512 split in halves, warp 4 summing dims
+//                              0-255 and warp 5 dims 256-511 into two accumulators (TMEM lanes = heads,
+//                              columns = keys) that the softmax adds;
 //              O^T += V^T P^T: M = 128 dims per MMA (the stage read MN-major, K = V), N = NH heads,
-//                              K = 32 keys; four 128-dim accumulators, lanes = dims, columns = heads;
+//                              K = 32 keys; four 128-dim accumulators, tiles 0-1 from warp 4, 2-3 from 5;
 //              S of sub-tile i + 1 is issued before O^T of sub-tile i, so it overlaps the softmax;
 //   warps 0-3  softmax, one thread per head (lanes 0-15 of each quadrant hold the M = 64 rows): the
 //              32 logits of a sub-tile are a row of TMEM, so max and sum are thread-local; P is
 //              written as the head's row of the P^T operand (two buffers).  The running maximum is
 //              lazy: it moves (and O^T is rescaled in TMEM) only when a sub-tile's maximum exceeds it
 //              by more than 2^8, so exp2(s - m) <= 2^8 stays exact in fp32 and rescales are rare.
-// Merge: each CTA sends (m, l) per head to every CTA of the cluster, then scales its O^T by
-// 2^(m - M) (M the cluster maximum) and sends each 128-dim tile to the CTA that owns it (tile t
-// belongs to CTA t mod CL), into that CTA's now idle key stages.  The owner sums the CL tiles,
-// divides by L and applies R_m^-1 (pairs of dims sit in neighbouring lanes) before the bf16 store,
-// or writes an fp32 partial with (M, L) when the row has several splits.
+// Merge (tile t of the 4 128-dim tiles of O^T belongs to CTA t mod CL): as soon as its own products are
+// done, each CTA writes the tiles other CTAs own, unscaled, as bf16 into its idle query rows, and sends
+// (m, l, e) per head to every CTA of the cluster; after one cluster barrier it pushes those tiles into
+// the owners' idle key stages (bulk copies).  The owner weighs each CTA's partial by 2^(m_c - M) (M the
+// cluster maximum), divides by L and applies R_m^-1 (pairs of dims sit in neighbouring lanes) before the
+// bf16 store, or writes an fp32 partial with (M, L) when the row has several splits.
 // ---------------------------------------------------------------------------------------------
 constexpr int kClKeys = 32;                 // keys per sub-tile
 constexpr int kClStages = 4;                // key stages in flight (a stage is free again after its P V)
-constexpr int kClGatherWarps = 11;          // warps 5 .. 15
-constexpr int kClThreads = 32 * (5 + kClGatherWarps);
+constexpr int kClMmaWarps = 2;              // warps 4 and 5
+constexpr int kClFirstGather = 4 + kClMmaWarps;
+constexpr int kClGatherWarps = 10;          // warps 6 .. 15
+constexpr int kClThreads = 32 * (kClFirstGather + kClGatherWarps);
 constexpr int kClGatherThreads = 32 * kClGatherWarps;
-constexpr int kClRound = kClGatherThreads / kClKeys;   // sub-tiles resolved per round (11)
-constexpr int kClRing = 2 * kClRound;                  // resolved sub-tiles kept (a ring of 22)
+constexpr int kClRound = kClGatherThreads / kClKeys;   // sub-tiles resolved per round (10)
+constexpr int kClRing = 2 * kClRound;                  // resolved sub-tiles kept (a ring of 20)
 constexpr int kClStage = kClKeys * kD * 2;
 static_assert(kClKeys == 32, "one 32-bit key mask and 32 S columns per sub-tile");
+static_assert(kClThreads == 512, "16 warps");
 constexpr float kLazyLog2 = 8.f;            // the running maximum moves when exceeded by more than this
 constexpr int kBtCache = 1024;              // main block tables up to this many blocks are cached in shared memory
 
@@ -165,7 +174,7 @@ struct ClSmem {
     static constexpr int kQ = 64 * kD * 2;                          // [8][64 rows][128 B]
     static constexpr int kP = NH * 64 * 2;                          // [NH rows][128 B]: keys 0 .. 31 of 64 used
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kQ;                        // key stages; exchanged tiles at the end
+    static constexpr int kOffK = kOffQ + kQ;                        // key stages; received tiles
     static constexpr int kOffP = kOffK + kClStages * kClStage;      // two P^T buffers; output staging at the end
     static constexpr int kOffRow = kOffP + 2 * kP;                  // int [ring][32]: physical rows (-1 masked)
     static constexpr int kOffPool = kOffRow + kClRing * kClKeys * 4;  // uint8 [ring][32]: 1 main, 2 window
@@ -174,9 +183,9 @@ struct ClSmem {
     static constexpr int kOffAlpha = kOffMask + kClStages * 4;      // float [2][NH]
     static constexpr int kOffVote = kOffAlpha + 2 * NH * 4;         // int [2][4]
     static constexpr int kOffOwn = kOffVote + 32;                   // float m[NH], l[NH], e[NH] of this CTA
-    static constexpr int kOffStat = kOffOwn + 3 * NH * 4;           // float [4 ranks][NH][4]: (m, l, e, 0) of each CTA
-    static constexpr int kOffFac = kOffStat + 4 * NH * 16;          // float f[NH], L[NH], M[NH], 1/L[NH], E[NH]
-    static constexpr int kOffBt = kOffFac + 5 * NH * 4;             // int [kBtCache]: the request's main block table
+    static constexpr int kOffStat = kOffOwn + 3 * NH * 4;           // float [4 ranks][NH][4]: (m, l, e, fault)
+    static constexpr int kOffFac = kOffStat + 4 * NH * 16;          // float f[4 ranks][NH], 1/L, M, L, E [NH]
+    static constexpr int kOffBt = kOffFac + 8 * NH * 4;             // int [kBtCache]: the request's main block table
     static constexpr int kOffSwb = kOffBt + kBtCache * 4;           // int [8]: window-pool blocks from that of wlo
     static constexpr int kOffFault = kOffSwb + 32;                  // int: a key of this CTA hit a device fault
     static constexpr int kBars = 2 * kClStages + 6;
@@ -185,7 +194,8 @@ struct ClSmem {
     static constexpr int kAlloc = kBytes + 1024;                    // + alignment slack
     static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
     static constexpr int kTile = 128 * NH * 2;                      // one exchanged 128-dim O tile: [NH / 4][128] x 4 bf16
-    static_assert(6 * kTile <= kQ + kClStages * kClStage, "sent and received tiles must fit in the query rows and stages");
+    static_assert(3 * kTile <= kQ, "the sent tiles fit in the query rows");
+    static_assert(6 * kTile <= kQ + kClStages * kClStage, "the received tiles fit after them");
     static_assert(NH * 128 * 2 <= 2 * kP, "an output tile must fit in the P^T buffers");
     static constexpr int kTmemCols = 128 + 4 * NH <= 256 ? 256 : 512;
 };
@@ -216,16 +226,16 @@ __global__ void __launch_bounds__(kClThreads, 1)
     int* s_vote = reinterpret_cast<int*>(smem + L::kOffVote);
     float* s_own = reinterpret_cast<float*>(smem + L::kOffOwn);
     float* s_stat = reinterpret_cast<float*>(smem + L::kOffStat);
-    float* s_fac = reinterpret_cast<float*>(smem + L::kOffFac);
-    float* s_L = s_fac + NH;
-    float* s_M = s_L + NH;
-    float* s_inv = s_M + NH;
-    float* s_E = s_inv + NH;
+    float* s_fac = reinterpret_cast<float*>(smem + L::kOffFac);  // [4][NH]: weight of each CTA's partial
+    float* s_inv = s_fac + 4 * NH;
+    float* s_M = s_inv + NH;
+    float* s_L = s_M + NH;
+    float* s_E = s_L + NH;
     // sub-tile i: key stage i % kClStages; S columns, P^T buffer and softmax scratch i & 1
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // [stages] stage gathered (gather threads)
-    uint64_t* sfull = full + kClStages;                                 // [2] S in TMEM (MMA commit)
+    uint64_t* sfull = full + kClStages;                                 // [2] S in TMEM (both MMA warps' commits)
     uint64_t* pfull = sfull + 2;                                        // [2] P^T written (4 warps)
-    uint64_t* pvdone = pfull + 2;                                       // [stages] O^T += V^T P^T done (commit)
+    uint64_t* pvdone = pfull + 2;                                       // [stages] O^T += V^T P^T done (2 commits)
     uint64_t* qfull = pvdone + kClStages;                               // query rows loaded
     uint64_t* xfull = qfull + 1;                                        // exchanged tiles loaded
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(xfull + 1);
@@ -238,12 +248,14 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const int hg = (cid / a.nsplit) % a.hg_count;
     const int row = cid / (a.nsplit * a.hg_count);
     if (tid == 0) {
+        DSA_STAMP_NS(31);
+        DSA_STAMP(0);
         for (int b = 0; b < kClStages; ++b) {
             mbar_init(&full[b], kClGatherThreads);
-            mbar_init(&pvdone[b], 1);
+            mbar_init(&pvdone[b], kClMmaWarps);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&sfull[b], 1);
+            mbar_init(&sfull[b], kClMmaWarps);
             mbar_init(&pfull[b], 4);
         }
         mbar_init(qfull, 1);
@@ -262,18 +274,17 @@ __global__ void __launch_bounds__(kClThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t tS = tmem, tO = tmem + 128;
+    const uint32_t tS = tmem, tO = tmem + 128;  // S: [2 buffers][2 halves][32 columns]; O^T: [4 tiles][NH]
+    if (tid == 0) DSA_STAMP(1);
     cluster_arrive_relaxed();  // phase 0: this CTA has started (waited on before distributed shared memory use)
-    pdl_wait();                // on-chip set-up above; global memory only below
-    pdl_launch_dependents();
 
+    // The row's position, request and block tables, and the query rows: inputs that no kernel of the layer
+    // step writes, read while the preceding kernel (the top-k) finishes.  Top-k indices, cache rows and
+    // every output come after the programmatic-dependent-launch wait.
     const int r = a.q_req ? a.q_req[row] : row;
     const int m = a.q_pos[row];
     const bool row_ok = r >= 0 && r < a.main_bt.batch && r < a.swa_bt.batch && m >= 0;
-    if (!row_ok && tid == 0) {
-        *s_fault = 1;
-        if (crank == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
-    }
+    if (!row_ok && tid == 0) *s_fault = 1;
     const int n_vis = row_ok ? entries_formed((long long)m + 1, a.kind_w, a.kind_s) : 0;
     const int n_comp = a.topk ? a.k : n_vis;
     const int ncp = (n_comp + 3) & ~3;
@@ -282,17 +293,39 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const int n_sub = (n_keys + kClKeys - 1) / kClKeys;
     const int g_lo = split * a.cps, g_hi = min(n_sub, g_lo + a.cps);
     const int n_mine = g_hi > g_lo + crank ? (g_hi - g_lo - crank + csize - 1) / csize : 0;
+    const bool bt_cached = a.main_bt.max_blocks <= kBtCache;
+    int* s_bt = reinterpret_cast<int*>(smem + L::kOffBt);
+    int* s_swb = reinterpret_cast<int*>(smem + L::kOffSwb);
+    if (warp == 4 && n_mine > 0) {  // the query rows, one 64-dim box per lane
+        if (lane == 0) mbar_expect_tx(qfull, NH * kD * 2);
+        __syncwarp();
+        if (lane < kD / 64) tma_load_2d(smem + L::kOffQ + lane * 8192, &qmap, lane * 64, row * a.heads + hg * NH, qfull);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qfull);
+    }
+    const int gt = tid - 32 * kClFirstGather, gw = warp - kClFirstGather;
+    if (warp >= kClFirstGather && n_mine > 0) {
+        // the request's main block table (when it has at most kBtCache blocks) and the window pool's blocks
+        // of positions wlo .. m; a key then resolves with one global load (its top-k index) at most
+        if (bt_cached)
+            for (int b = gt; b < a.main_bt.max_blocks; b += kClGatherThreads)
+                s_bt[b] = __ldg(a.main_bt.table + (long long)r * a.main_bt.max_blocks + b);
+        if (gt < 8) {
+            const int lb = wlo / kBlockPositions + gt;
+            s_swb[gt] = (row_ok && lb <= m / kBlockPositions && lb < a.swa_bt.max_blocks)
+                            ? __ldg(a.swa_bt.table + (long long)r * a.swa_bt.max_blocks + lb)
+                            : -1;
+        }
+        named_bar_sync(1, kClGatherThreads);  // cached tables visible to every gather thread
+    }
+    pdl_wait();  // global memory the preceding kernel writes, and every output, only below
+    pdl_launch_dependents();
+    if (tid == 0) DSA_STAMP(2);
+    if (!row_ok && tid == 0 && crank == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
     bool ok = true;
 
-    if (warp >= 5) {
+    if (warp >= kClFirstGather) {
         // ---- gather warps: resolve keys a round ahead, prefetch rows into L2, copy with cp.async -----
-        const int gt = tid - 160, gw = warp - 5;
-        // The request's main block table (when it has at most kBtCache blocks) and the window pool's blocks
-        // of positions wlo .. m are cached in shared memory, loaded in the same round trip as the first
-        // round's top-k indices; a key then resolves with one global load (its top-k index) at most.
-        const bool bt_cached = a.main_bt.max_blocks <= kBtCache;
-        int* s_bt = reinterpret_cast<int*>(smem + L::kOffBt);
-        int* s_swb = reinterpret_cast<int*>(smem + L::kOffSwb);
         // sub-tiles [R * kClRound, (R + 1) * kClRound): thread -> sub-tile R * kClRound + gt / 32, key gt % 32.
         // Step 1: the key's top-k index (or entry / window position), no dependent load.
         auto key_id = [&](int R, int* id) -> int {  // returns j (the key's index in the row), -1 if none
@@ -353,21 +386,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             const int j = key_id(R, &id);
             finish_key(R, j, id);
         };
-        if (n_mine > 0) {
-            int id0 = -1;
-            const int j0 = key_id(0, &id0);
-            if (bt_cached)
-                for (int b = gt; b < a.main_bt.max_blocks; b += kClGatherThreads)
-                    s_bt[b] = __ldg(a.main_bt.table + (long long)r * a.main_bt.max_blocks + b);
-            if (gt < 8) {
-                const int lb = wlo / kBlockPositions + gt;
-                s_swb[gt] = (row_ok && lb <= m / kBlockPositions && lb < a.swa_bt.max_blocks)
-                                ? __ldg(a.swa_bt.table + (long long)r * a.swa_bt.max_blocks + lb)
-                                : -1;
-            }
-            named_bar_sync(1, kClGatherThreads);  // cached tables visible
-            finish_key(0, j0, id0);
-        }
+        if (n_mine > 0) resolve_round(0);
         for (int i = 0; i < n_mine; ++i) {
             const int s = i % kClStages;
             if (i >= kClStages)  // the stage's previous sub-tile has been multiplied into O^T
@@ -375,7 +394,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             named_bar_sync(1, kClGatherThreads);  // sub-tile i's rows are visible; earlier gathers are done
             const int* rows = s_row + (i % kClRing) * kClKeys;
             const uint8_t* pools = s_pool + (i % kClRing) * kClKeys;
-            if (gt < kClKeys) {  // warp 5: the stage's key mask for the softmax
+            if (gt < kClKeys) {  // the first gather warp: the stage's key mask for the softmax
                 const uint32_t bits = __ballot_sync(0xffffffffu, rows[gt] >= 0);
                 if (lane == 0) s_mask[s] = bits;
             }
@@ -443,6 +462,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 }
             }
             cp_async_commit();
+            if (i == 0 && gt == 0) DSA_STAMP(3);
             if (i == 0) {  // the first round's later sub-tiles start moving into L2 once sub-tile 0 is under way
                 constexpr int kRowBytes = FP8 ? kD : 2 * kD;
                 for (int t = kClKeys + gt; t < kClRound * kClKeys; t += kClGatherThreads) {
@@ -477,42 +497,34 @@ __global__ void __launch_bounds__(kClThreads, 1)
             mbar_arrive(&full[(n_mine - 1) % kClStages]);
         }
         if (!ok) report(a.status, DSA_ERR_TIMEOUT);
-    } else if (warp == 4) {
-        // ---- MMA issue: the whole warp waits, one elected lane issues ----------------------------
+    } else if (warp >= 4) {
+        // ---- MMA issue: two warps, each waiting whole and issuing from one elected lane --------------
         // S of sub-tile i + 1 goes first when its keys are in (it overlaps the softmax of sub-tile i), but
         // the product of sub-tile i never waits behind a gather that has not arrived.
+        const int half = warp - 4;
         const uint32_t idesc_s = idesc_bf16(kClKeys, 0, 64), idesc_o = idesc_bf16(NH, 1, 128);
         const uint64_t dq = sw128_desc(sQ, 16, 1024);
-        if (n_mine > 0) {
-            // the query rows, one 64-dim box per lane (off the gather warps: a single thread issues one box
-            // per several hundred cycles)
-            if (lane == 0) mbar_expect_tx(qfull, NH * kD * 2);
-            __syncwarp();
-            if (lane < kD / 64)
-                tma_load_2d(smem + L::kOffQ + lane * 8192, &qmap, lane * 64, row * a.heads + hg * NH, qfull);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(qfull);
-            ok = mbar_wait_bounded(qfull, 0, kWaitLimitNs);
-        }
-        auto issue_s = [&](int i) {
+        if (n_mine > 0) ok = mbar_wait_bounded(qfull, 0, kWaitLimitNs);
+        auto issue_s = [&](int i) {  // this warp's half of the 512 dims into its own accumulator
             const int s = i % kClStages;
             tc_fence_after();
             const uint64_t dk = sw128_desc(sK + s * kClStage, 16, 1024);
 #pragma unroll
-            for (int ks = 0; ks < kD / 16; ++ks) {  // 64-dim chunks are 64 query rows / 32 key rows apart
+            for (int k = 0; k < kD / 32; ++k) {  // 64-dim chunks are 64 query rows / 32 key rows apart
+                const int ks = half * (kD / 32) + k;
                 const uint64_t oq = (uint64_t)((((ks >> 2) * (64 * 128)) + (ks & 3) * 32) >> 4);
                 const uint64_t ok_ = (uint64_t)((((ks >> 2) * (kClKeys * 128)) + (ks & 3) * 32) >> 4);
-                mma_bf16_ss_elect(tS + (i & 1) * kClKeys, dq + oq, dk + ok_, idesc_s, ks > 0 ? 1u : 0u);
+                mma_bf16_ss_elect(tS + ((i & 1) * 2 + half) * kClKeys, dq + oq, dk + ok_, idesc_s, k > 0 ? 1u : 0u);
             }
             mma_commit_elect(&sfull[i & 1]);
         };
-        auto issue_pv = [&](int i) {
+        auto issue_pv = [&](int i) {  // this warp's two 128-dim tiles
             const int s = i % kClStages;
             tc_fence_after();
             const uint64_t dv = sw128_desc(sK + s * kClStage, kClKeys * 128, 1024);
             const uint64_t dp = sw128_desc(sP + (i & 1) * L::kP, 16, 1024);
 #pragma unroll
-            for (int mt = 0; mt < 4; ++mt)
+            for (int mt = 2 * half; mt < 2 * half + 2; ++mt)
 #pragma unroll
                 for (int ks = 0; ks < kClKeys / 16; ++ks)
                     mma_bf16_ss_elect(tO + mt * NH,
@@ -531,11 +543,13 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 if (next_s < n_mine && next_s <= i + 1 &&
                     __all_sync(0xffffffffu, mbar_try_wait(&full[next_s % kClStages], (next_s / kClStages) & 1))) {
                     issue_s(next_s);
+                    if (next_s == 0 && tid == 128) DSA_STAMP(4);
                     ++next_s;
                     continue;
                 }
                 if (next_s > i && __all_sync(0xffffffffu, mbar_try_wait(&pfull[i & 1], (i >> 1) & 1))) {
                     issue_pv(i);
+                    if (i == n_mine - 1 && tid == 128) DSA_STAMP(6);
                     pv_done = true;
                     continue;
                 }
@@ -564,11 +578,18 @@ __global__ void __launch_bounds__(kClThreads, 1)
             bool resc = false;
             if (ok) {
                 tc_fence_after();
-                tmem_ld_nowait<16>(tS + s * kClKeys + lane_off, *reinterpret_cast<float(*)[16]>(sv));
-                tmem_ld_nowait<16>(tS + s * kClKeys + lane_off + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
+                float sh[kClKeys];  // the second half-sum of the logits
+                tmem_ld_nowait<16>(tS + (s * 2) * kClKeys + lane_off, *reinterpret_cast<float(*)[16]>(sv));
+                tmem_ld_nowait<16>(tS + (s * 2) * kClKeys + lane_off + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
+                tmem_ld_nowait<16>(tS + (s * 2 + 1) * kClKeys + lane_off, *reinterpret_cast<float(*)[16]>(sh));
+                tmem_ld_nowait<16>(tS + (s * 2 + 1) * kClKeys + lane_off + 16, *reinterpret_cast<float(*)[16]>(sh + 16));
                 tmem_wait_ld();
                 tmem_regs_after_wait<16>(*reinterpret_cast<float(*)[16]>(sv));
                 tmem_regs_after_wait<16>(*reinterpret_cast<float(*)[16]>(sv + 16));
+                tmem_regs_after_wait<16>(*reinterpret_cast<float(*)[16]>(sh));
+                tmem_regs_after_wait<16>(*reinterpret_cast<float(*)[16]>(sh + 16));
+#pragma unroll
+                for (int j = 0; j < kClKeys; ++j) sv[j] += sh[j];
                 const uint32_t vm = s_mask[st];
                 float mx = -INFINITY;
                 if (!FP8 && vm == 0xFFFFFFFFu) {  // every key of the stage present (the same for all threads)
@@ -644,11 +665,13 @@ __global__ void __launch_bounds__(kClThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&pfull[s]);
+            if (i == 0 && tid == 0) DSA_STAMP(5);
         }
         if (n_mine > 0) {  // the last product must be complete before O^T is read
             ok = ok && mbar_wait_bounded(&pvdone[(n_mine - 1) % kClStages], ((n_mine - 1) / kClStages) & 1, kWaitLimitNs);
             tc_fence_after();
         }
+        if (tid == 0) DSA_STAMP(7);
         if (hthread) {
             s_own[h] = m_run;
             s_own[NH + h] = l_run;
@@ -658,13 +681,10 @@ __global__ void __launch_bounds__(kClThreads, 1)
     }
 
     // ---- merge across the cluster ---------------------------------------------------------------
-    // Every CTA sends (m, l) per head to every CTA of the cluster (distributed shared memory), so all of
-    // them know the cluster maximum M and denominator L; each scales its O^T by 2^(m - M) and pushes
-    // the tiles that other CTAs own straight into their shared memory (bulk copies); each owner adds its
-    // own tile from TMEM, applies 1 / L and R_m^-1 and stores bf16 (or an fp32 split partial).
     tc_fence_before();
     const bool all_ok = __syncthreads_and(ok);  // O^T complete (the softmax warps waited for it); s_own set
     tc_fence_after();
+    if (tid == 0) DSA_STAMP(8);
     const bool have = n_mine > 0 && all_ok;
     constexpr int G = NH / 4;                    // heads per finishing thread (a TMEM load of G columns)
     const int quad = warp & 3, quarter = warp >> 2;
@@ -677,61 +697,18 @@ __global__ void __launch_bounds__(kClThreads, 1)
         else tmem_ld4(tO + t * NH + lane_off + h0, v);
     };
     auto tmem_cols_nowait = [&](int t, float (&v)[G]) { tmem_ld_nowait<G>(tO + t * NH + lane_off + h0, v); };
-    cluster_wait();  // phase 0: every CTA of the cluster has started
-    if (csize > 1 && tid == 0)  // before any peer can push (pushes follow phase 1)
-        mbar_arrive_expect_tx(xfull, (uint32_t)((csize - 1) * tiles_per * L::kTile));
-    const float fo = *s_fault ? 1.f : 0.f;  // this CTA met a device fault: the whole row is written as zeros
-    for (int h = tid; h < NH; h += kClThreads) {
-        const uint32_t dst = smem_u32(s_stat + (crank * NH + h) * 4);
-        const float mo = have ? s_own[h] : -INFINITY, lo = have ? s_own[NH + h] : 0.f,
-                    eo = have ? s_own[2 * NH + h] : 0.f;
-        for (int q = 0; q < csize; ++q)
-            st_cluster_v4(mapa_shared(dst, (uint32_t)q), mo, lo, eo, fo);
-    }
-    cluster_arrive();  // phase 1: statistics delivered; every CTA's products are complete
-    cluster_wait();
-    for (int h = tid; h < NH; h += kClThreads) {
-        float M = -INFINITY;
-        for (int q = 0; q < csize; ++q) M = fmaxf(M, s_stat[(q * NH + h) * 4]);
-        float Ls = 0.f, Es = 0.f;
-        bool fault = false;
-        for (int q = 0; q < csize; ++q) {
-            const float mq = s_stat[(q * NH + h) * 4];
-            fault |= s_stat[(q * NH + h) * 4 + 3] != 0.f;
-            if (mq != -INFINITY) {
-                const float fq = exp2f(mq - M);
-                Ls += s_stat[(q * NH + h) * 4 + 1] * fq;
-                Es += s_stat[(q * NH + h) * 4 + 2] * fq;
-            }
-        }
-        if (fault) Ls = Es = 0.f;  // every CTA of the cluster sees the same flags: zero factors, zero output
-        const float mo = s_stat[(crank * NH + h) * 4];
-        s_fac[h] = (mo == -INFINITY || fault) ? 0.f : exp2f(mo - M);
-        s_L[h] = Ls;
-        s_M[h] = fault ? -INFINITY : M;
-        s_inv[h] = Ls > 0.f ? 1.f / Ls : 0.f;
-        s_E[h] = Es;
-        if (h == 0) s_vote[0] = fault ? 1 : 0;  // (softmax votes are done) the row's fault flag for the partials
-    }
-    __syncthreads();
-    float f[G], inv[G];
-#pragma unroll
-    for (int e = 0; e < G; e += 4) {
-        const float4 a4 = *reinterpret_cast<const float4*>(s_fac + h0 + e);
-        const float4 b4 = *reinterpret_cast<const float4*>(s_inv + h0 + e);
-        f[e] = a4.x, f[e + 1] = a4.y, f[e + 2] = a4.z, f[e + 3] = a4.w;
-        inv[e] = b4.x, inv[e + 1] = b4.y, inv[e + 2] = b4.z, inv[e + 3] = b4.w;
-    }
-    // tiles this CTA sends sit at [0, 3 tiles) of shared memory, the tiles it receives at [3, 6 tiles)
-    // (query rows and key stages, idle now); each as [NH / 4 head quads][128 dims] x 4 bf16, already scaled
-    // to the cluster maximum (the owner's own tile stays fp32 in TMEM)
+    // Tiles this CTA sends sit at [0, 3 tiles) of shared memory (the query rows, idle now), the tiles it
+    // receives at [3, 6 tiles) (query rows and key stages); each as [NH / 4 head quads][128 dims] x 4 bf16.
     uint8_t* xout = smem + L::kOffQ;
     uint8_t* xin = smem + L::kOffQ + 3 * L::kTile;
     if (csize > 1) {
-        float v[4][G];  // all four tiles' columns in flight together, then the three (or two) sent ones staged
+        // 1. the tiles other CTAs own, unscaled (the owner applies this CTA's factor), staged as bf16; only
+        // this CTA's own accumulators are needed, so no CTA waits for another here
+        float v[4][G];  // static register indices; the sent tiles' columns in flight together
         if (have) {
 #pragma unroll
-            for (int t = 0; t < 4; ++t) tmem_cols_nowait(t, v[t]);
+            for (int t = 0; t < 4; ++t)
+                if (t % csize != crank) tmem_cols_nowait(t, v[t]);
             tmem_wait_ld();
 #pragma unroll
             for (int t = 0; t < 4; ++t) tmem_regs_after_wait<G>(v[t]);
@@ -743,30 +720,81 @@ __global__ void __launch_bounds__(kClThreads, 1)
 #pragma unroll
             for (int q4 = 0; q4 < G / 4; ++q4)
                 *reinterpret_cast<uint2*>(xout + sl * L::kTile + ((h0 / 4 + q4) * 128 + d) * 8) =
-                    have ? make_uint2(pack_bf16(v[t][4 * q4] * f[4 * q4], v[t][4 * q4 + 1] * f[4 * q4 + 1]),
-                                      pack_bf16(v[t][4 * q4 + 2] * f[4 * q4 + 2], v[t][4 * q4 + 3] * f[4 * q4 + 3]))
+                    have ? make_uint2(pack_bf16(v[t][4 * q4], v[t][4 * q4 + 1]), pack_bf16(v[t][4 * q4 + 2], v[t][4 * q4 + 3]))
                          : make_uint2(0u, 0u);
             ++sl;
         }
-        fence_proxy_async_smem();  // staged tiles -> async proxy (the bulk copies)
-        __syncthreads();
-        // one push per sent tile, each from lane 0 of a different warp (one thread issues a bulk copy only
-        // every several hundred cycles)
-        if (lane == 0 && warp < 4 - tiles_per) {
-            int t = 0, seen = -1;
-            for (; t < 4; ++t)
-                if (t % csize != crank && ++seen == warp) break;
-            const int o = t % csize;
-            const int slot = (crank - (crank > o ? 1 : 0)) * tiles_per + t / csize;  // in the owner's xin
-            bulk_s2cluster(mapa_shared(smem_u32(xin + slot * L::kTile), (uint32_t)o),
-                           smem_u32(xout + warp * L::kTile), L::kTile, mapa_shared(smem_u32(xfull), (uint32_t)o));
+        fence_proxy_async_smem();  // staged tiles -> async proxy (the bulk copies after the cluster barrier)
+    }
+    if (tid == 0) DSA_STAMP(9);
+    // 2. (m, l, e, fault) per head to every CTA of the cluster
+    cluster_wait();  // phase 0: every CTA of the cluster has started
+    if (csize > 1 && tid == 0)  // before any peer can push (pushes follow phase 1)
+        mbar_arrive_expect_tx(xfull, (uint32_t)((csize - 1) * tiles_per * L::kTile));
+    const float fo = *s_fault ? 1.f : 0.f;  // this CTA met a device fault: the whole row is written as zeros
+    for (int h = tid; h < NH; h += kClThreads) {
+        const uint32_t dst = smem_u32(s_stat + (crank * NH + h) * 4);
+        const float mo = have ? s_own[h] : -INFINITY, lo = have ? s_own[NH + h] : 0.f,
+                    eo = have ? s_own[2 * NH + h] : 0.f;
+        for (int q = 0; q < csize; ++q)
+            st_cluster_v4(mapa_shared(dst, (uint32_t)q), mo, lo, eo, fo);
+    }
+    cluster_arrive();  // phase 1: statistics delivered, sent tiles staged, every CTA's products complete
+    cluster_wait();
+    if (tid == 0) DSA_STAMP(10);
+    // 3. push: one bulk copy per sent tile, each from lane 0 of a different warp
+    const bool pusher = csize > 1 && lane == 0 && warp < 4 - tiles_per;
+    if (pusher) {
+        int t = 0, seen = -1;
+        for (; t < 4; ++t)
+            if (t % csize != crank && ++seen == warp) break;
+        const int o = t % csize;
+        const int slot = ((crank - o - 1 + csize) % csize) * tiles_per + t / csize;  // in the owner's xin
+        bulk_s2cluster(mapa_shared(smem_u32(xin + slot * L::kTile), (uint32_t)o), smem_u32(xout + warp * L::kTile),
+                       L::kTile, mapa_shared(smem_u32(xfull), (uint32_t)o));
+        bulk_commit();
+    }
+    // 4. per head: the cluster maximum M, each CTA's weight 2^(m_c - M), 1 / L
+    for (int h = tid; h < NH; h += kClThreads) {
+        float M = -INFINITY;
+        bool fault = false;
+        for (int q = 0; q < csize; ++q) {
+            M = fmaxf(M, s_stat[(q * NH + h) * 4]);
+            fault |= s_stat[(q * NH + h) * 4 + 3] != 0.f;
         }
+        float Ls = 0.f, Es = 0.f;
+        for (int q = 0; q < csize; ++q) {
+            const float mq = s_stat[(q * NH + h) * 4];
+            const float fq = (mq == -INFINITY || fault) ? 0.f : exp2f(mq - M);
+            s_fac[q * NH + h] = fq;
+            if (fq != 0.f) {
+                Ls += s_stat[(q * NH + h) * 4 + 1] * fq;
+                Es += s_stat[(q * NH + h) * 4 + 2] * fq;
+            }
+        }
+        s_inv[h] = Ls > 0.f ? 1.f / Ls : 0.f;
+        s_M[h] = fault ? -INFINITY : M;
+        s_L[h] = Ls;
+        s_E[h] = Es;
+        if (h == 0) s_vote[0] = fault ? 1 : 0;  // (the softmax votes are done) the row's fault flag for the partials
+    }
+    __syncthreads();
+    if (tid == 0) DSA_STAMP(11);
+    if (csize > 1) {
         ok = mbar_wait_bounded(xfull, 0, kWaitLimitNs);
         if (!ok && tid == 0) report(a.status, DSA_ERR_TIMEOUT);
-        cluster_arrive_relaxed();  // phase 2: this CTA's incoming tiles are complete (waited on before exit)
     }
+    if (tid == 0) DSA_STAMP(12);
     // ---- owner: finish each owned tile; bf16 output staged as [NH][128] in the P^T buffers and stored
     // with 16-byte writes, or fp32 split partials ------------------------------------------------------
+    float inv[G], fown[G];
+#pragma unroll
+    for (int e = 0; e < G; e += 4) {
+        const float4 b4 = *reinterpret_cast<const float4*>(s_inv + h0 + e);
+        const float4 a4 = *reinterpret_cast<const float4*>(s_fac + crank * NH + h0 + e);
+        inv[e] = b4.x, inv[e + 1] = b4.y, inv[e + 2] = b4.z, inv[e + 3] = b4.w;
+        fown[e] = a4.x, fown[e + 1] = a4.y, fown[e + 2] = a4.z, fown[e + 3] = a4.w;
+    }
     uint8_t* ostage = smem + L::kOffP;
     const int rd = a.rope.rope_dim, firstd = kD - rd;
 #pragma unroll 1
@@ -778,18 +806,21 @@ __global__ void __launch_bounds__(kClThreads, 1)
         float v[G];
         if (have) tmem_cols(t, v);
 #pragma unroll
-        for (int e = 0; e < G; ++e) v[e] = have ? v[e] * f[e] : 0.f;
+        for (int e = 0; e < G; ++e) v[e] = have ? v[e] * fown[e] : 0.f;
 #pragma unroll
         for (int si = 0; si < 3; ++si) {
             if (si < csize - 1) {
-                const uint8_t* src = xin + (si * tiles_per + j) * L::kTile;
+                const int src = (crank + 1 + si) % csize;
+                const float* fsrc = s_fac + src * NH + h0;
+                const uint8_t* p = xin + (si * tiles_per + j) * L::kTile;
 #pragma unroll
                 for (int q4 = 0; q4 < G / 4; ++q4) {
-                    const uint2 w = *reinterpret_cast<const uint2*>(src + ((h0 / 4 + q4) * 128 + d) * 8);
-                    v[4 * q4] += bf16_to_float((uint16_t)(w.x & 0xFFFFu));
-                    v[4 * q4 + 1] += bf16_to_float((uint16_t)(w.x >> 16));
-                    v[4 * q4 + 2] += bf16_to_float((uint16_t)(w.y & 0xFFFFu));
-                    v[4 * q4 + 3] += bf16_to_float((uint16_t)(w.y >> 16));
+                    const uint2 w = *reinterpret_cast<const uint2*>(p + ((h0 / 4 + q4) * 128 + d) * 8);
+                    const float4 f4 = *reinterpret_cast<const float4*>(fsrc + 4 * q4);
+                    v[4 * q4] = fmaf(f4.x, bf16_to_float((uint16_t)(w.x & 0xFFFFu)), v[4 * q4]);
+                    v[4 * q4 + 1] = fmaf(f4.y, bf16_to_float((uint16_t)(w.x >> 16)), v[4 * q4 + 1]);
+                    v[4 * q4 + 2] = fmaf(f4.z, bf16_to_float((uint16_t)(w.y & 0xFFFFu)), v[4 * q4 + 2]);
+                    v[4 * q4 + 3] = fmaf(f4.w, bf16_to_float((uint16_t)(w.y >> 16)), v[4 * q4 + 3]);
                 }
             }
         }
@@ -830,10 +861,15 @@ __global__ void __launch_bounds__(kClThreads, 1)
             }
         }
     }
-    if (csize > 1) cluster_wait();  // phase 2: no copy out of this CTA's shared memory is still running
+    if (tid == 0) DSA_STAMP(13);
+    if (pusher) bulk_wait_all();  // this CTA's shared memory is no longer read by its copies
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (tid == 0) {
+        DSA_STAMP(14);
+        DSA_STAMP_NS(30);
+    }
     if (warp == 0) tmem_dealloc(tmem, L::kTmemCols);
 }
 
@@ -987,6 +1023,8 @@ static dsa_status_t sparse_attn(int32_t rows, int32_t heads, const void* q, cons
 }  // namespace dsa
 
 using namespace dsa;
+
+DSA_TIMELINE_SETTER(dsa_timeline_attention)
 
 extern "C" size_t dsa_attn_workspace_size(int32_t nq, int32_t heads, int32_t max_keys) {
     if (nq <= 0 || heads <= 0 || max_keys <= 0) return 0;

@@ -108,6 +108,35 @@ inline bool table_ok(const dsa_block_table_t* t, int batch) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Timeline instrumentation, compiled only into builds with -DDSA_TIMELINE (never the library itself):
+// DSA_STAMP(k) writes the SM clock to slot k of the CTA's 32-slot record in a buffer that an exported
+// setter of the translation unit installs; slots 30 and 31 hold %globaltimer at the CTA's end and start.
+#ifdef DSA_TIMELINE
+#define DSA_TIMELINE_BUFFER static __device__ unsigned long long* g_timeline;
+#define DSA_STAMP(k)                                                                              \
+    do {                                                                                          \
+        if (g_timeline) {                                                                         \
+            unsigned long long c_;                                                                \
+            asm volatile("mov.u64 %0, %%clock64;" : "=l"(c_));                                    \
+            g_timeline[(unsigned long long)blockIdx.x * 32 + (k)] = c_;                           \
+        }                                                                                         \
+    } while (0)
+#define DSA_STAMP_NS(k)                                                                           \
+    do {                                                                                          \
+        if (g_timeline) g_timeline[(unsigned long long)blockIdx.x * 32 + (k)] = global_ns();      \
+    } while (0)
+#define DSA_TIMELINE_SETTER(name)                                                                 \
+    extern "C" int name(void* p) {                                                                \
+        unsigned long long* q = static_cast<unsigned long long*>(p);                              \
+        return cudaMemcpyToSymbol(dsa::g_timeline, &q, sizeof(q)) == cudaSuccess ? 0 : 1;         \
+    }
+#else
+#define DSA_TIMELINE_BUFFER
+#define DSA_STAMP(k) ((void)0)
+#define DSA_STAMP_NS(k) ((void)0)
+#define DSA_TIMELINE_SETTER(name)
+#endif
+
 // First error wins; later errors leave the recorded code in place.
 __device__ __forceinline__ void report(int32_t* status, int32_t code) {
     if (status) atomicCAS(status, 0, code);

@@ -37,6 +37,7 @@ __host__ __device__ constexpr int slice_cols() { return TPI == 2 ? 128 : 96; }
 constexpr int kTileEntries = 128;
 constexpr int kPage = 64;         // c4a entries per 256-position block
 constexpr int kChunkItems = 32;   // items resolved together (one per producer lane)
+DSA_TIMELINE_BUFFER
 
 struct IdxArgs {
     int nq, heads, q_group, n_cols, tmem_cols, ld;
@@ -227,6 +228,8 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
     auto stage_meta = [&](int s) { return reinterpret_cast<StageMeta*>(smem + (size_t)s * a.stage_bytes + tiles_bytes); };
 
     if (tid == 0) {
+        DSA_STAMP_NS(31);
+        DSA_STAMP(0);
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1 + 32);  // the producer's lane 0 (with the TMA bytes) + 32 scale copies
             mbar_init(&empty[i], EW * 32);
@@ -247,6 +250,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
+    if (tid == 0) DSA_STAMP(1);
     // Programmatic dependent launch: the producer resolves its first items (query positions and requests,
     // the block table: inputs no preceding kernel of the layer writes) while the preceding kernel (the
     // compressor, which writes keys) finishes.  Without fresh_from, key copies and every global write come
@@ -317,6 +321,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
         int n = 0, ps = 0, pphase = 0;  // items issued; stage index and its phase parity
         int cur_g = -1, gb = 1, guse[2] = {0, 0};  // group in the current buffer, buffer index, loads per buffer
         bool alive = true;
+        if (lane == 0) DSA_STAMP(2);
         ItemInfo cur = resolve(lo);
         bool waited = !early;
         if (!early) {
@@ -406,6 +411,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                     mbar_arrive_expect_tx(&full[s], bytes);  // release: the meta writes above are visible
                 }
                 __syncwarp();
+                if (n == 0 && lane == 0) DSA_STAMP(3);
                 if (go && lane < kPages) {  // one page per lane
                     int bp = it.blk[0];
 #pragma unroll
@@ -423,6 +429,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
             }
             cur = nxt;
         }
+        if (lane == 0) DSA_STAMP(4);
         if (!waited) {  // the kernel ends after the preceding kernel, whatever it read
             pdl_wait();
             pdl_launch_dependents();
@@ -471,6 +478,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                     mma_f8_elect(tmem + (b * TPI + tt) * a.n_cols, smem_desc(a_addr + tt * kTileEntries * DIM + ks * 32, DIM),
                                  smem_desc(b_addr + ks * 32, DIM), idesc, ks > 0 ? 1u : 0u);
             mma_commit_elect(&tfull[b]);
+            if (n == 0 && lane == 0) DSA_STAMP(5);
             if (++s == S) {
                 s = 0;
                 sph ^= 1;
@@ -617,6 +625,10 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
             tc_fence_before();
             mbar_arrive(&tempty[b]);
             mbar_arrive(&empty[s]);
+            if (tid == 64) {
+                if (n == 0) DSA_STAMP(6);
+                DSA_STAMP(7);
+            }
             if (++s == S) {
                 s = 0;
                 sph ^= 1;
@@ -630,8 +642,16 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (tid == 0) {
+        DSA_STAMP(8);
+        DSA_STAMP_NS(30);
+    }
     if (warp == 0) tmem_dealloc(tmem, a.tmem_cols);
 }
+
+}  // namespace dsa
+DSA_TIMELINE_SETTER(dsa_timeline_index)
+namespace dsa {
 
 static bool make_map(CUtensorMap* map, const void* base, uint64_t rows, int dim, int box_rows) {
     auto fn = tensor_map_encoder();

@@ -38,6 +38,7 @@ constexpr int kBins = 2048;
 constexpr int kPartMax = 40960;  // scores per CTA (rows up to 163,840 with C = 4)
 constexpr int kRankMax = 256;    // bucket sizes (cluster-wide) resolved by direct ranking
 constexpr int kMarkWords = (kPartMax / 32 + 1 + 3) & ~3;  // winner bitmap, padded to 16 bytes
+DSA_TIMELINE_BUFFER
 
 // Monotone 32-bit key of a score; -0 and +0 compare equal as floats, so they share one key.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -480,8 +481,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     __shared__ uint32_t sel[2];
     __shared__ uint32_t n_cand;
     __shared__ float red[2][32];
+    if (threadIdx.x == 0) {
+        DSA_STAMP_NS(31);
+        DSA_STAMP(0);
+    }
     pdl_wait();
     pdl_launch_dependents();
+    if (threadIdx.x == 0) DSA_STAMP(1);
     const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     int32_t* out = idx_out + (long long)row * k;
     const int n = n_valid[row];
@@ -512,6 +518,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int b = tid; b < kBins; b += THREADS) hist[b] = 0;
     for (int w = tid; w < THREADS * VPT / 32; w += THREADS) marks[w] = 0;
     if (tid == 0) n_cand = 0;
+    if (tid == 0) DSA_STAMP(2);
     float mx = -INFINITY, mn = INFINITY;
 #pragma unroll
     for (int u = 0; u < VPT; ++u)
@@ -554,9 +561,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int u = 0; u < VPT; ++u)
         if (u < nv) atomicAdd(&hist[bin_at(u)], 1u);
     __syncthreads();
+    if (tid == 0) DSA_STAMP(3);
     uint32_t need = (uint32_t)k;
     const uint32_t bstar = SC::select(hist, need, wt, sel);
     const uint32_t in_bucket = hist[bstar];
+    if (tid == 0) DSA_STAMP(4);
     const bool take_all = in_bucket == need;
     const bool rank_mode = !take_all && in_bucket <= (uint32_t)kRankMax;
     // this thread's scores above b* (always taken) and in b*
@@ -625,6 +634,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         T = prefix;
     }
     // 4. ordered compaction: definite members and (lowest-index first) entries equal to T
+    if (tid == 0) DSA_STAMP(5);
     uint32_t dmask = above, tmask = 0u;
     if (take_all) dmask |= inb;
     else if (rank_mode) {
@@ -655,6 +665,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t total = tot_d + min(tot_t, need_T);
     for (int i = (int)total + tid; i < k; i += THREADS) out[i] = -1;
     if (tid == 0 && total != (uint32_t)k) report(status, DSA_ERR_DEVICE_FAULT);
+    if (tid == 0) {
+        DSA_STAMP(6);
+        DSA_STAMP_NS(30);
+    }
 }
 
 // Which kernel a call runs: rows of up to 16,384 scores one CTA each with the row in registers (faster
@@ -677,6 +691,8 @@ static dsa_status_t topk_plan(int32_t nq, int32_t ld, int32_t k, bool* reg, int*
 }  // namespace dsa
 
 using namespace dsa;
+
+DSA_TIMELINE_SETTER(dsa_timeline_topk)
 
 extern "C" dsa_status_t dsa_topk_plan(int32_t nq, int32_t ld, int32_t k, int32_t* plan) {
     if (!plan) return DSA_ERR_INVALID_ARG;

@@ -242,6 +242,10 @@ dsa_status_t dsa_attn_plan(int32_t nq, int32_t heads, int32_t max_keys, int32_t 
  *            NULL when that size is 0; max_keys = (topk ? k : main_bt->max_blocks *
  *            main->rows_per_block) + window
  * Supported: dim 512, rope_dim <= 64.
+ * Launched with programmatic dependent launch: q, q_pos (q_req) and both block tables are read before
+ * waiting for the preceding kernel in the stream, so a preceding kernel that releases its dependents
+ * early must not write them after releasing; top-k indices, cache rows and every output come after the
+ * wait.  A row with a device fault (an unmapped block or an index >= n_vis) is written as zeros, lse -inf.
  */
 dsa_status_t dsa_sparse_attn_decode(int32_t batch, int32_t heads, const void* q, const int32_t* q_pos,
                                     int32_t kind, const int32_t* topk, int32_t k, const dsa_pool_t* main,
