@@ -342,7 +342,7 @@ def run_gpu(args, rank, world, local_rank):
     if "index" in k_ms:
         kern["index_kernel"] = {"ms": k_ms["index"], "bytes": idx_bytes, "gbs": idx_bytes / (k_ms["index"] * 1e6),
                                 "tflops": index_flops(spec) / (k_ms["index"] * 1e9)}
-        kern["topk_kernel"] = {"ms": k_ms["topk"]}
+        kern["topk_kernel"] = {"ms": k_ms["topk"], "counted": bool(copies[0].fused_topk)}
     kern["attn_kernel"] = {"ms": k_ms["attend"], "bytes": att_bytes, "gbs": att_bytes / (k_ms["attend"] * 1e6),
                            "tflops": attention_flops(spec) / (k_ms["attend"] * 1e9)}
     dominant = max((n for n in kern if "bytes" in kern[n]), key=lambda n: kern[n]["ms"])

@@ -50,7 +50,8 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_but_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return (uint32_t)float_to_bf16(lo) | ((uint32_t)float_to_bf16(hi) << 16);
 }
@@ -188,8 +189,9 @@ struct ClSmem {
     static constexpr int kOffBt = kOffFac + 8 * NH * 4;             // int [kBtCache]: the request's main block table
     static constexpr int kOffSwb = kOffBt + kBtCache * 4;           // int [8]: window-pool blocks from that of wlo
     static constexpr int kOffFault = kOffSwb + 32;                  // int: a key of this CTA hit a device fault
+    static constexpr int kOffRope = kOffFault + 16;                 // float [32][2]: cos, sin of each pair's angle at m
     static constexpr int kBars = 2 * kClStages + 6;
-    static constexpr int kOffBar = kOffFault + 16;                  // kBars mbarriers, TMEM address
+    static constexpr int kOffBar = kOffRope + 256;                  // kBars mbarriers, TMEM address
     static constexpr int kBytes = kOffBar + kBars * 8 + 16;
     static constexpr int kAlloc = kBytes + 1024;                    // + alignment slack
     static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
@@ -213,7 +215,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int e, int chunk_stride)
 
 template <int NH, bool FP8>
 __global__ void __launch_bounds__(kClThreads, 1)
-    attn_cl_kernel(const __grid_constant__ CUtensorMap qmap, AttnArgs a) {
+    attn_cl_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap, AttnArgs a) {
     using L = ClSmem<NH>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -240,6 +242,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     uint64_t* xfull = qfull + 1;                                        // exchanged tiles loaded
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(xfull + 1);
     volatile int* s_fault = reinterpret_cast<volatile int*>(smem + L::kOffFault);
+    float* s_rc = reinterpret_cast<float*>(smem + L::kOffRope);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int crank = (int)cluster_ctarank(), csize = (int)cluster_nctarank();
@@ -296,6 +299,12 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const bool bt_cached = a.main_bt.max_blocks <= kBtCache;
     int* s_bt = reinterpret_cast<int*>(smem + L::kOffBt);
     int* s_swb = reinterpret_cast<int*>(smem + L::kOffSwb);
+    if (warp == 0 && lane < a.rope.rope_dim / 2) {  // R_m^-1 of the output: cos and sin of each pair's angle at m
+        float c = 1.f, sn = 0.f;
+        if (row_ok) rope_cos_sin(m, a.rope.inv_freq[lane], &c, &sn);
+        s_rc[2 * lane] = c;
+        s_rc[2 * lane + 1] = sn;
+    }
     if (warp == 4 && n_mine > 0) {  // the query rows, one 64-dim box per lane
         if (lane == 0) mbar_expect_tx(qfull, NH * kD * 2);
         __syncwarp();
@@ -387,10 +396,19 @@ __global__ void __launch_bounds__(kClThreads, 1)
             finish_key(R, j, id);
         };
         if (n_mine > 0) resolve_round(0);
+        int sig = 0;  // first sub-tile whose stage this thread has not yet reported full
         for (int i = 0; i < n_mine; ++i) {
             const int s = i % kClStages;
-            if (i >= kClStages)  // the stage's previous sub-tile has been multiplied into O^T
+            if (i >= kClStages) {
+                // before waiting for a stage, report every sub-tile issued so far (never hold landed rows back)
+                if (!FP8 && sig < i) {
+                    cp_async_wait_all();
+                    fence_proxy_async_smem();  // cp.async writes -> visible to the tensor core (async proxy)
+                    for (; sig < i; ++sig) mbar_arrive(&full[sig % kClStages]);
+                }
+                // the stage's previous sub-tile has been multiplied into O^T
                 ok = ok && mbar_wait_bounded(&pvdone[s], ((i - kClStages) / kClStages) & 1, kWaitLimitNs);
+            }
             named_bar_sync(1, kClGatherThreads);  // sub-tile i's rows are visible; earlier gathers are done
             const int* rows = s_row + (i % kClRing) * kClKeys;
             const uint8_t* pools = s_pool + (i % kClRing) * kClKeys;
@@ -480,21 +498,23 @@ __global__ void __launch_bounds__(kClThreads, 1)
             // the next round of keys once this one's second sub-tile is under way: its rows reach L2 while
             // the sub-tiles in between are processed (ring slots of sub-tiles < i are free by now)
             if (i % kClRound == 2) resolve_round(i / kClRound + 1);
-            // a thread keeps two sub-tiles of copies in flight: sub-tile i - 1 is reported once its group
-            // (the one before sub-tile i's) has landed.  Its stage's consumers never wait on sub-tile i.
+            // a thread keeps up to three sub-tiles of copies in flight: with three outstanding, the oldest is
+            // reported once its group has landed
             if constexpr (FP8) {  // this thread's converted rows are in the stage
                 fence_proxy_async_smem();
                 mbar_arrive(&full[s]);
-            } else if (i > 0) {
-                cp_async_wait_but_one();
-                fence_proxy_async_smem();  // cp.async writes -> visible to the tensor core (async proxy)
-                mbar_arrive(&full[(i - 1) % kClStages]);
+                sig = i + 1;
+            } else if (i - sig >= 2) {
+                cp_async_wait_group<2>();
+                fence_proxy_async_smem();
+                mbar_arrive(&full[sig % kClStages]);
+                ++sig;
             }
         }
-        if (!FP8 && n_mine > 0) {  // the last sub-tile
+        if (!FP8 && sig < n_mine) {  // the sub-tiles not yet reported
             cp_async_wait_all();
             fence_proxy_async_smem();
-            mbar_arrive(&full[(n_mine - 1) % kClStages]);
+            for (; sig < n_mine; ++sig) mbar_arrive(&full[sig % kClStages]);
         }
         if (!ok) report(a.status, DSA_ERR_TIMEOUT);
     } else if (warp >= 4) {
@@ -713,6 +733,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
 #pragma unroll
             for (int t = 0; t < 4; ++t) tmem_regs_after_wait<G>(v[t]);
         }
+        if (tid == 0) DSA_STAMP(15);
         int sl = 0;
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
@@ -720,15 +741,17 @@ __global__ void __launch_bounds__(kClThreads, 1)
 #pragma unroll
             for (int q4 = 0; q4 < G / 4; ++q4)
                 *reinterpret_cast<uint2*>(xout + sl * L::kTile + ((h0 / 4 + q4) * 128 + d) * 8) =
-                    have ? make_uint2(pack_bf16(v[t][4 * q4], v[t][4 * q4 + 1]), pack_bf16(v[t][4 * q4 + 2], v[t][4 * q4 + 3]))
+                    have ? make_uint2(bf16x2_rn(v[t][4 * q4], v[t][4 * q4 + 1]), bf16x2_rn(v[t][4 * q4 + 2], v[t][4 * q4 + 3]))
                          : make_uint2(0u, 0u);
             ++sl;
         }
+        if (tid == 0) DSA_STAMP(16);
         fence_proxy_async_smem();  // staged tiles -> async proxy (the bulk copies after the cluster barrier)
     }
     if (tid == 0) DSA_STAMP(9);
     // 2. (m, l, e, fault) per head to every CTA of the cluster
     cluster_wait();  // phase 0: every CTA of the cluster has started
+    if (tid == 0) DSA_STAMP(17);
     if (csize > 1 && tid == 0)  // before any peer can push (pushes follow phase 1)
         mbar_arrive_expect_tx(xfull, (uint32_t)((csize - 1) * tiles_per * L::kTile));
     const float fo = *s_fault ? 1.f : 0.f;  // this CTA met a device fault: the whole row is written as zeros
@@ -739,45 +762,52 @@ __global__ void __launch_bounds__(kClThreads, 1)
         for (int q = 0; q < csize; ++q)
             st_cluster_v4(mapa_shared(dst, (uint32_t)q), mo, lo, eo, fo);
     }
+    if (tid == 0) DSA_STAMP(18);
     cluster_arrive();  // phase 1: statistics delivered, sent tiles staged, every CTA's products complete
     cluster_wait();
     if (tid == 0) DSA_STAMP(10);
-    // 3. push: one bulk copy per sent tile, each from lane 0 of a different warp
-    const bool pusher = csize > 1 && lane == 0 && warp < 4 - tiles_per;
+    // 3. push: one bulk copy per sent tile, each from lane 0 of one of the last warps (the first warps compute
+    // the factors meanwhile)
+    const int pw = 15 - warp;  // sent tile of this warp
+    const bool pusher = csize > 1 && lane == 0 && pw >= 0 && pw < 4 - tiles_per;
     if (pusher) {
         int t = 0, seen = -1;
         for (; t < 4; ++t)
-            if (t % csize != crank && ++seen == warp) break;
+            if (t % csize != crank && ++seen == pw) break;
         const int o = t % csize;
         const int slot = ((crank - o - 1 + csize) % csize) * tiles_per + t / csize;  // in the owner's xin
-        bulk_s2cluster(mapa_shared(smem_u32(xin + slot * L::kTile), (uint32_t)o), smem_u32(xout + warp * L::kTile),
+        bulk_s2cluster(mapa_shared(smem_u32(xin + slot * L::kTile), (uint32_t)o), smem_u32(xout + pw * L::kTile),
                        L::kTile, mapa_shared(smem_u32(xfull), (uint32_t)o));
         bulk_commit();
     }
-    // 4. per head: the cluster maximum M, each CTA's weight 2^(m_c - M), 1 / L
-    for (int h = tid; h < NH; h += kClThreads) {
-        float M = -INFINITY;
-        bool fault = false;
-        for (int q = 0; q < csize; ++q) {
-            M = fmaxf(M, s_stat[(q * NH + h) * 4]);
-            fault |= s_stat[(q * NH + h) * 4 + 3] != 0.f;
+    // 4. per head: the cluster maximum M, each CTA's weight 2^(m_c - M), 1 / L; one thread per (head, CTA),
+    // the four of a head in neighbouring lanes
+    if (tid < NH * 4) {
+        const int h = tid >> 2, qq = tid & 3;
+        const bool in = qq < csize;
+        const float4 st = in ? *reinterpret_cast<const float4*>(s_stat + (qq * NH + h) * 4)
+                             : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        float M = fmaxf(st.x, __shfl_xor_sync(0xffffffffu, st.x, 1));
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+        int fault = st.w != 0.f;
+        fault |= __shfl_xor_sync(0xffffffffu, fault, 1);
+        fault |= __shfl_xor_sync(0xffffffffu, fault, 2);
+        const float fq = (st.x == -INFINITY || fault) ? 0.f : exp2f(st.x - M);
+        float Ls = fq != 0.f ? st.y * fq : 0.f, Es = fq != 0.f ? st.z * fq : 0.f;
+        Ls += __shfl_xor_sync(0xffffffffu, Ls, 1);
+        Es += __shfl_xor_sync(0xffffffffu, Es, 1);
+        Ls += __shfl_xor_sync(0xffffffffu, Ls, 2);
+        Es += __shfl_xor_sync(0xffffffffu, Es, 2);
+        if (in) s_fac[qq * NH + h] = fq;
+        if (qq == 0) {
+            s_inv[h] = Ls > 0.f ? 1.f / Ls : 0.f;
+            s_M[h] = fault ? -INFINITY : M;
+            s_L[h] = Ls;
+            s_E[h] = Es;
+            if (h == 0) s_vote[0] = fault;  // (the softmax votes are done) the row's fault flag for the partials
         }
-        float Ls = 0.f, Es = 0.f;
-        for (int q = 0; q < csize; ++q) {
-            const float mq = s_stat[(q * NH + h) * 4];
-            const float fq = (mq == -INFINITY || fault) ? 0.f : exp2f(mq - M);
-            s_fac[q * NH + h] = fq;
-            if (fq != 0.f) {
-                Ls += s_stat[(q * NH + h) * 4 + 1] * fq;
-                Es += s_stat[(q * NH + h) * 4 + 2] * fq;
-            }
-        }
-        s_inv[h] = Ls > 0.f ? 1.f / Ls : 0.f;
-        s_M[h] = fault ? -INFINITY : M;
-        s_L[h] = Ls;
-        s_E[h] = Es;
-        if (h == 0) s_vote[0] = fault ? 1 : 0;  // (the softmax votes are done) the row's fault flag for the partials
     }
+    if (tid == 0) DSA_STAMP(19);
     __syncthreads();
     if (tid == 0) DSA_STAMP(11);
     if (csize > 1) {
@@ -795,16 +825,19 @@ __global__ void __launch_bounds__(kClThreads, 1)
         inv[e] = b4.x, inv[e + 1] = b4.y, inv[e + 2] = b4.z, inv[e + 3] = b4.w;
         fown[e] = a4.x, fown[e + 1] = a4.y, fown[e + 2] = a4.z, fown[e + 3] = a4.w;
     }
-    uint8_t* ostage = smem + L::kOffP;
-    const int rd = a.rope.rope_dim, firstd = kD - rd;
+    // output staging: two buffers of [NH][128] bf16 (the P^T buffers, and key stages 2-3, idle by now), each
+    // stored by one TMA box
+    uint8_t* const ob0 = smem + L::kOffP;
+    uint8_t* const ob1 = smem + L::kOffK + 2 * kClStage;
+    const int firstd = kD - a.rope.rope_dim;
+    const bool odd = lane & 1;
 #pragma unroll 1
     for (int j = 0; j < tiles_per; ++j) {
         const int t = crank + csize * j;
         const int D = t * 128 + d;
-        float cs = 1.f, sn = 0.f;
-        if (a.nsplit == 1 && D >= firstd) rope_cos_sin(m, a.rope.inv_freq[(D - firstd) >> 1], &cs, &sn);
         float v[G];
         if (have) tmem_cols(t, v);
+        if (tid == 0 && j == 0) DSA_STAMP(20);
 #pragma unroll
         for (int e = 0; e < G; ++e) v[e] = have ? v[e] * fown[e] : 0.f;
 #pragma unroll
@@ -817,30 +850,45 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 for (int q4 = 0; q4 < G / 4; ++q4) {
                     const uint2 w = *reinterpret_cast<const uint2*>(p + ((h0 / 4 + q4) * 128 + d) * 8);
                     const float4 f4 = *reinterpret_cast<const float4*>(fsrc + 4 * q4);
-                    v[4 * q4] = fmaf(f4.x, bf16_to_float((uint16_t)(w.x & 0xFFFFu)), v[4 * q4]);
-                    v[4 * q4 + 1] = fmaf(f4.y, bf16_to_float((uint16_t)(w.x >> 16)), v[4 * q4 + 1]);
-                    v[4 * q4 + 2] = fmaf(f4.z, bf16_to_float((uint16_t)(w.y & 0xFFFFu)), v[4 * q4 + 2]);
-                    v[4 * q4 + 3] = fmaf(f4.w, bf16_to_float((uint16_t)(w.y >> 16)), v[4 * q4 + 3]);
+                    v[4 * q4] = fmaf(f4.x, __uint_as_float(w.x << 16), v[4 * q4]);
+                    v[4 * q4 + 1] = fmaf(f4.y, __uint_as_float(w.x & 0xFFFF0000u), v[4 * q4 + 1]);
+                    v[4 * q4 + 2] = fmaf(f4.z, __uint_as_float(w.y << 16), v[4 * q4 + 2]);
+                    v[4 * q4 + 3] = fmaf(f4.w, __uint_as_float(w.y & 0xFFFF0000u), v[4 * q4 + 3]);
                 }
             }
         }
         if (a.nsplit == 1) {
+            if (j >= 2) {  // this buffer's previous box has been read out
+                if (tid == 0) bulk_wait_read<1>();
+                __syncthreads();
+            }
+            uint8_t* const obuf = (j & 1) ? ob1 : ob0;
+            uint32_t* o32 = reinterpret_cast<uint32_t*>(obuf);
+            const int De = D & ~1;  // the pair's even dim
+            float rc = 1.f, rs = 0.f;
+            if (De >= firstd) {
+                rc = s_rc[De - firstd];
+                rs = s_rc[De - firstd + 1];
+            }
+            // neighbouring lanes swap one value per pair of heads: the even lane then holds dims (De, De + 1) of
+            // head 2p, the odd lane those of head 2p + 1; each rotates its pair by R_m^-1 and stores it packed
 #pragma unroll
-            for (int e = 0; e < G; ++e) {
-                const float x = v[e] * inv[e];
-                const float y = __shfl_xor_sync(0xffffffffu, x, 1);  // the pair partner's value
-                float o = x;
-                if (D >= firstd) o = (D & 1) ? (-y * sn + x * cs) : (x * cs + y * sn);  // R_m^-1
-                reinterpret_cast<uint16_t*>(ostage)[(h0 + e) * 128 + d] = float_to_bf16(o);
+            for (int pp = 0; pp < G / 2; ++pp) {
+                const float x0 = v[2 * pp] * inv[2 * pp], x1 = v[2 * pp + 1] * inv[2 * pp + 1];
+                const float recv = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
+                const float lo = odd ? recv : x0, hi = odd ? x1 : recv;
+                const float r0 = lo * rc + hi * rs, r1 = hi * rc - lo * rs;
+                const int hh = h0 + 2 * pp + (odd ? 1 : 0);
+                o32[hh * 64 + (d >> 1)] = bf16x2_rn(r0, r1);
             }
+            if (tid == 0 && j == 0) DSA_STAMP(21);
+            fence_proxy_async_smem();  // staged output -> async proxy (the TMA store)
             __syncthreads();
-            // NH rows of 256 bytes -> out[row][hg * NH + h][t * 128 .. + 128]
-            for (int i = tid; i < NH * 16; i += kClThreads) {
-                const int h = i >> 4, u = i & 15;
-                *reinterpret_cast<uint4*>(a.out + ((long long)row * a.heads + hg * NH + h) * kD + t * 128 + u * 8) =
-                    *reinterpret_cast<const uint4*>(ostage + h * 256 + u * 16);
+            if (tid == 0 && j == 0) DSA_STAMP(22);
+            if (tid == 0) {  // NH rows of 128 dims -> out[row][hg * NH .. + NH][t * 128 .. + 128]
+                tma_store_2d(&omap, t * 128, row * a.heads + hg * NH, obuf);
+                bulk_commit();
             }
-            __syncthreads();
         } else {
             const long long base0 = ((long long)row * a.nsplit + split) * a.heads + hg * NH + h0;
 #pragma unroll
@@ -862,7 +910,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         }
     }
     if (tid == 0) DSA_STAMP(13);
-    if (pusher) bulk_wait_all();  // this CTA's shared memory is no longer read by its copies
+    if (pusher || tid == 0) bulk_wait_all();  // this CTA's shared memory is no longer read by its copies / stores
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -929,17 +977,31 @@ static bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t rows, int
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map of the [rows][512] bf16 output for boxes of 128 columns x box_rows rows, unswizzled (the staging
+// layout [box_rows][128]).
+static bool make_out_map(CUtensorMap* map, void* base, uint64_t rows, int box_rows) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    cuuint64_t gdim[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)kD * 2};
+    cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    cuuint32_t estride[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int NH, bool FP8>
 static dsa_status_t launch_attn_cl(const AttnArgs& a, int cl, cudaStream_t st) {
     using L = ClSmem<NH>;
-    CUtensorMap qmap;
+    CUtensorMap qmap, omap;
     if (!make_bf16_map(&qmap, a.q, (uint64_t)a.rows * a.heads, NH)) return DSA_ERR_CUDA;
+    if (!make_out_map(&omap, a.out, (uint64_t)a.rows * a.heads, NH)) return DSA_ERR_CUDA;
     if (cudaFuncSetAttribute(attn_cl_kernel<NH, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
         cudaSuccess)
         return DSA_ERR_CUDA;
     const long long grid = (long long)a.rows * a.hg_count * a.nsplit * cl;
     cudaError_t e = launch_pdl_cluster(attn_cl_kernel<NH, FP8>, dim3((unsigned)grid), dim3(kClThreads), L::kAlloc, st, cl,
-                                       qmap, a);
+                                       qmap, omap, a);
     if (e == cudaSuccess && a.nsplit > 1)
         e = launch_pdl(attn_combine_kernel, dim3(a.rows * a.heads), dim3(128), 0, st, a);
     if (e != cudaSuccess) return DSA_ERR_CUDA;

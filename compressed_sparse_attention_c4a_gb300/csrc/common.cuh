@@ -137,6 +137,14 @@ __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepc
 #define DSA_TIMELINE_SETTER(name)
 #endif
 
+// Monotone 32-bit key of a score (the top-k's radix digits): a larger float has a larger key; -0 and +0 share
+// one key.  Shared by the indexer (which counts each row's top 11 bits while scoring) and the top-k.
+__device__ __forceinline__ uint32_t dsa_score_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // First error wins; later errors leave the recorded code in place.
 __device__ __forceinline__ void report(int32_t* status, int32_t code) {
     if (status) atomicCAS(status, 0, code);
@@ -338,6 +346,16 @@ __device__ __forceinline__ void bulk_s2cluster(uint32_t dst_cluster, uint32_t sr
                  "r"(src_smem), "r"(bytes), "r"(bar_cluster)
                  : "memory");
 }
+// 2-D tiled tensor copy shared -> global (a box of the tensor map at {x, y}), tracked by the issuing thread's
+// bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, const void* src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x), "r"(y),
+                 "r"(smem_u32(src))
+                 : "memory");
+}
+// Wait until at most N of this thread's bulk groups still read their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_global() {

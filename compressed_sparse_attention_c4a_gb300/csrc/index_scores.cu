@@ -57,6 +57,7 @@ struct IdxArgs {
     int32_t* status;
     unsigned long long wait_ns;  // limit of every bounded wait
     int withhold;                // test hook: the producer issues no copy and posts no stage
+    unsigned* hist;              // fused top-k: [nq][2048] counts of the top 11 bits of each row's score keys, or NULL
 };
 
 // Shared-memory matrix descriptor of a K-major operand whose rows are `row_bytes` (64 or 128) long,
@@ -197,6 +198,10 @@ __device__ __forceinline__ float sum_f32x2(unsigned long long v) {
 }
 
 __host__ __device__ constexpr int gbuf_nvis_offset(int n_cols, int dim) { return n_cols * dim + 2 * n_cols * 4; }
+
+// Level-1 histogram of the fused top-k ([P1] §4.2: S_t = TopK(I_t, k)): each visible entry's score is counted
+// by the top 11 bits of its order key (dsa_score_key), the first digit of the top-k's radix select.
+constexpr int kSelBins = 2048;
 
 template <int DIM, int HEADS, int TPI>
 __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -602,10 +607,17 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
 #pragma unroll
                             for (int jj = 0; jj < 16 / HEADS; ++jj) {
                                 const int j = (cb + k) * (16 / HEADS) + jj;  // query of the group
+                                // fused top-k: each visible entry's score also counted in its row's level-1 histogram
                                 if constexpr (kClean) {
-                                    if (j < nqg) out[(long long)j * a.ld] = acc[jj];
+                                    if (j < nqg) {
+                                        out[(long long)j * a.ld] = acc[jj];
+                                        if (a.hist) atomicAdd(a.hist + (long long)(q0 + j) * kSelBins + (dsa_score_key(acc[jj]) >> 21), 1u);
+                                    }
                                 } else if (e_ok && j < nqg) {
-                                    out[(long long)j * a.ld] = (page_ok && e < gnv[j]) ? acc[jj] : -INFINITY;
+                                    const float sv = (page_ok && e < gnv[j]) ? acc[jj] : -INFINITY;
+                                    out[(long long)j * a.ld] = sv;
+                                    if (a.hist && e < gnv[j])
+                                        atomicAdd(a.hist + (long long)(q0 + j) * kSelBins + (dsa_score_key(sv) >> 21), 1u);
                                 }
                             }
                         }
@@ -716,7 +728,7 @@ static dsa_status_t index_scores(int32_t nq, int32_t heads, int32_t dim, const u
                                  const float* w, const int32_t* q_pos, const int32_t* q_req, int32_t q_group,
                                  const dsa_pool_t* keys, const dsa_block_table_t* bt, float* scores, int32_t ld,
                                  int32_t* n_visible, const int32_t* fresh_from, int32_t* dev_status, void* stream,
-                                 uint64_t wait_ns, int withhold) {
+                                 uint64_t wait_ns, int withhold, unsigned* hist = nullptr) {
     if (nq < 0 || ld < 0 || (ld & 3)) return DSA_ERR_INVALID_ARG;
     if (nq == 0) return DSA_OK;
     if (heads != 4 && heads != 8 && heads != 16) return DSA_ERR_UNSUPPORTED;
@@ -753,6 +765,7 @@ static dsa_status_t index_scores(int32_t nq, int32_t heads, int32_t dim, const u
     a.status = dev_status;
     a.wait_ns = wait_ns;
     a.withhold = withhold;
+    a.hist = hist;
     CUtensorMap kmap, qmap;
     if (!make_map(&kmap, keys->data, (uint64_t)keys->num_blocks * kPage, dim, kPage)) return DSA_ERR_CUDA;
     if (!make_map(&qmap, q8, (uint64_t)nq * heads, dim, n_cols)) return DSA_ERR_CUDA;
@@ -782,4 +795,45 @@ extern "C" dsa_status_t dsa_debug_index_scores_stalled(int32_t nq, int32_t heads
     if (wait_limit_ns == 0 || wait_limit_ns > kWaitLimitNs) return DSA_ERR_INVALID_ARG;
     return index_scores(nq, heads, dim, q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, ld, n_visible,
                         nullptr, dev_status, stream, wait_limit_ns, 1);
+}
+
+// Fused indexer + top-k: the indexer counts each row's level-1 histogram while scoring (rows of up to 16,384
+// entries), then the top-k of every row starts its radix select from it (dsa_topk_counted, topk.cu).  The
+// counts are zero-filled by the caller before the first call and cleared again by the top-k of every call that
+// completes.
+extern "C" size_t dsa_index_topk_workspace_size(int32_t nq) {
+    return nq > 0 ? ((size_t)nq * kSelBins * 4 + 255) / 256 * 256 : 0;
+}
+
+extern "C" dsa_status_t dsa_index_scores_counted(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8,
+                                                 const float* q_scale, const float* w, const int32_t* q_pos,
+                                                 const int32_t* q_req, int32_t q_group, const dsa_pool_t* keys,
+                                                 const dsa_block_table_t* bt, float* scores, int32_t ld,
+                                                 int32_t* n_visible, const int32_t* fresh_from, unsigned* counts,
+                                                 int32_t* dev_status, void* stream) {
+    if (nq < 0) return DSA_ERR_INVALID_ARG;
+    if (nq == 0) return DSA_OK;
+    if (!counts || !aligned(counts, 16) || ld > 16384) return DSA_ERR_INVALID_ARG;
+    return index_scores(nq, heads, dim, q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, ld, n_visible,
+                        fresh_from, dev_status, stream, kWaitLimitNs, 0, counts);
+}
+
+extern "C" dsa_status_t dsa_index_topk(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8, const float* q_scale,
+                                       const float* w, const int32_t* q_pos, const int32_t* q_req, int32_t q_group,
+                                       const dsa_pool_t* keys, const dsa_block_table_t* bt, float* scores, int32_t ld,
+                                       int32_t* n_visible, const int32_t* fresh_from, int32_t k, int32_t* idx_out,
+                                       void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    if (nq < 0) return DSA_ERR_INVALID_ARG;
+    if (nq == 0) return DSA_OK;
+    if (k < 1 || k > 2048 || !idx_out || !n_visible || !aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
+    if (ld > 16384) {  // rows the counted top-k does not hold: the plain indexer and top-k
+        const dsa_status_t r = dsa_index_scores(nq, heads, dim, q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores,
+                                                ld, n_visible, fresh_from, dev_status, stream);
+        return r != DSA_OK ? r : dsa_topk(nq, scores, ld, n_visible, k, idx_out, dev_status, stream);
+    }
+    if (!workspace || workspace_bytes < dsa_index_topk_workspace_size(nq)) return DSA_ERR_INVALID_ARG;
+    unsigned* counts = static_cast<unsigned*>(workspace);
+    const dsa_status_t r = dsa_index_scores_counted(nq, heads, dim, q8, q_scale, w, q_pos, q_req, q_group, keys, bt,
+                                                    scores, ld, n_visible, fresh_from, counts, dev_status, stream);
+    return r != DSA_OK ? r : dsa_topk_counted(nq, scores, ld, n_visible, k, idx_out, counts, dev_status, stream);
 }

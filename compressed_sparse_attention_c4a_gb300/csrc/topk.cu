@@ -41,11 +41,7 @@ constexpr int kMarkWords = (kPartMax / 32 + 1 + 3) & ~3;  // winner bitmap, padd
 DSA_TIMELINE_BUFFER
 
 // Monotone 32-bit key of a score; -0 and +0 compare equal as floats, so they share one key.
-__device__ __forceinline__ uint32_t order_key(float f) {
-    uint32_t u = __float_as_uint(f);
-    if (u == 0x80000000u) u = 0u;
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
+__device__ __forceinline__ uint32_t order_key(float f) { return dsa_score_key(f); }
 
 // Block-wide scan and bin selection for a block of THREADS threads (kBins / THREADS bins each).
 template <int THREADS>
@@ -671,6 +667,162 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Rows of up to 16,384 scores whose level-1 histogram -- the count of each value of the top 11 bits of the
+// scores' keys -- the indexer counted while scoring them (dsa_index_topk).  The same selection as
+// topk_reg_kernel, with the key's top 11 bits as the buckets: the max / min reduction and the histogram pass
+// drop out, the bucket b* of the k-th largest key comes from the stored counts, and a crowded b* is resolved
+// by a radix select over the remaining 21 bits.  The stored counts are cleared for the next call.
+// ---------------------------------------------------------------------------------------------
+template <int THREADS, int VPT>
+__global__ void __launch_bounds__(THREADS, 1)
+    topk_hist_kernel(const float* __restrict__ scores, int ld, const int32_t* __restrict__ n_valid, int k,
+                     int32_t* __restrict__ idx_out, unsigned* __restrict__ hist, int32_t* status) {
+    static_assert(VPT % 4 == 0 && VPT <= 32, "a thread's run is a multiple of 4 and fits one 32-bit mask");
+    using SC = RegScan<THREADS>;
+    __shared__ uint32_t h[kBins];
+    __shared__ uint32_t cand_key[kRankMax], cand_idx[kRankMax];
+    __shared__ uint32_t marks[THREADS * VPT / 32];  // ranked winners of a small bucket, by row index
+    __shared__ uint32_t wt[32][2];
+    __shared__ uint32_t sel[2];
+    __shared__ uint32_t n_cand;
+    pdl_wait();
+    pdl_launch_dependents();
+    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+    int32_t* out = idx_out + (long long)row * k;
+    unsigned* gh = hist + (long long)row * kBins;
+    for (int b = tid; b < kBins; b += THREADS) {
+        h[b] = __ldcg(gh + b);
+        gh[b] = 0u;
+    }
+    const int n = n_valid[row];
+    if (n < 0 || n > ld) {
+        if (tid == 0) report(status, DSA_ERR_DEVICE_FAULT);
+        for (int i = tid; i < k; i += THREADS) out[i] = -1;
+        return;
+    }
+    if (n <= k) {
+        for (int i = tid; i < k; i += THREADS) out[i] = i < n ? i : -1;
+        return;
+    }
+    // 1. this thread's run of keys
+    const float* s = scores + (long long)row * ld;
+    const int i0 = tid * VPT;
+    const int nv = max(0, min(VPT, n - i0));  // valid scores in the run
+    uint32_t key[VPT];
+#pragma unroll
+    for (int u = 0; u < VPT; u += 4) {
+        if (u + 4 <= nv) {
+            const float4 q = *reinterpret_cast<const float4*>(s + i0 + u);
+            key[u] = order_key(q.x), key[u + 1] = order_key(q.y), key[u + 2] = order_key(q.z), key[u + 3] = order_key(q.w);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) key[u + e] = u + e < nv ? order_key(s[i0 + u + e]) : 0u;
+        }
+    }
+    for (int w = tid; w < THREADS * VPT / 32; w += THREADS) marks[w] = 0;
+    if (tid == 0) n_cand = 0;
+    __syncthreads();
+    // 2. the bucket (top 11 bits) of the k-th largest key, from the stored counts
+    uint32_t need = (uint32_t)k;
+    const uint32_t bstar = SC::select(h, need, wt, sel);
+    const uint32_t in_bucket = h[bstar];
+    const bool take_all = in_bucket == need;
+    const bool rank_mode = !take_all && in_bucket <= (uint32_t)kRankMax;
+    uint32_t above = 0u, inb = 0u;  // this thread's keys above b* (always taken) and in b*
+#pragma unroll
+    for (int u = 0; u < VPT; ++u) {
+        const uint32_t b = key[u] >> 21;
+        if (u < nv && b > bstar) above |= 1u << u;
+        if (u < nv && b == bstar) inb |= 1u << u;
+    }
+    // 3a. small bucket: its members ranked directly (larger key, or equal key and lower index)
+    if (rank_mode) {
+        const uint32_t cnt = (uint32_t)__popc(inb);
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        uint32_t wbase = 0;
+        if (lane == 31 && incl) wbase = atomicAdd(&n_cand, incl);
+        wbase = __shfl_sync(0xffffffffu, wbase, 31);
+        uint32_t slot = wbase + incl - cnt;
+#pragma unroll
+        for (int u = 0; u < VPT; ++u)
+            if ((inb >> u) & 1u) {
+                cand_key[slot] = key[u];
+                cand_idx[slot] = (uint32_t)(i0 + u);
+                ++slot;
+            }
+        __syncthreads();
+        const int nc = (int)n_cand;
+        for (int c = tid; c < nc; c += THREADS) {
+            const uint32_t my_k = cand_key[c], my_i = cand_idx[c];
+            uint32_t better = 0;
+            for (int j = 0; j < nc; ++j) {
+                const uint32_t kj = cand_key[j];
+                better += (kj > my_k) || (kj == my_k && cand_idx[j] < my_i);
+            }
+            if (better < need) atomicOr(&marks[my_i >> 5], 1u << (my_i & 31));
+        }
+        __syncthreads();
+    }
+    // 3b. crowded bucket: radix select on the key's remaining bits (11, then 10) inside b* for the threshold key
+    // T and the number of keys equal to T still needed
+    uint32_t T = 0u, need_T = 0u;
+    if (!take_all && !rank_mode) {
+        need_T = need;
+        uint32_t prefix = bstar << 21, mask = 0xFFE00000u;
+#pragma unroll 1
+        for (int pass = 1; pass < 3; ++pass) {
+            const int sh = pass == 1 ? 10 : 0;
+            const uint32_t dm = pass == 1 ? 0x7FFu : 0x3FFu;
+            for (int b = tid; b < kBins; b += THREADS) h[b] = 0;
+            __syncthreads();
+#pragma unroll
+            for (int u = 0; u < VPT; ++u)
+                if (((inb >> u) & 1u) && (key[u] & mask) == prefix) atomicAdd(&h[(key[u] >> sh) & dm], 1u);
+            __syncthreads();
+            const uint32_t dg = SC::select(h, need_T, wt, sel);
+            prefix |= dg << sh;
+            mask |= dm << sh;
+        }
+        T = prefix;
+    }
+    // 4. ordered compaction: definite members and (lowest-index first) keys equal to T
+    uint32_t dmask = above, tmask = 0u;
+    if (take_all) dmask |= inb;
+    else if (rank_mode) {
+        for (uint32_t m = inb; m; m &= m - 1) {
+            const int u = __ffs(m) - 1;
+            if ((marks[(i0 + u) >> 5] >> ((i0 + u) & 31)) & 1u) dmask |= 1u << u;
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < VPT; ++u) {
+            if (((inb >> u) & 1u) && key[u] > T) dmask |= 1u << u;
+            if (((inb >> u) & 1u) && key[u] == T) tmask |= 1u << u;
+        }
+    }
+    uint32_t ex_d, ex_t, tot_d, tot_t;
+    SC::scan2((uint32_t)__popc(dmask), (uint32_t)__popc(tmask), &ex_d, &ex_t, &tot_d, &tot_t, wt);
+    uint32_t tie_rank = ex_t;
+    uint32_t pos = ex_d + min(tie_rank, need_T);
+    for (uint32_t m = dmask | tmask; m; m &= m - 1) {
+        const int u = __ffs(m) - 1;
+        if ((dmask >> u) & 1u) out[pos++] = i0 + u;
+        else {
+            if (tie_rank < need_T) out[pos++] = i0 + u;
+            ++tie_rank;
+        }
+    }
+    const uint32_t total = tot_d + min(tot_t, need_T);
+    for (int i = (int)total + tid; i < k; i += THREADS) out[i] = -1;
+    if (tid == 0 && total != (uint32_t)k) report(status, DSA_ERR_DEVICE_FAULT);
+}
+
 // Which kernel a call runs: rows of up to 16,384 scores one CTA each with the row in registers (faster
 // than a cluster even for few rows); longer rows a cluster of as many CTAs as the row's length needs (a
 // part of at most kPartMax scores each), more while the rows leave SMs idle.  Host arithmetic only.
@@ -730,4 +882,16 @@ extern "C" dsa_status_t dsa_topk(int32_t nq, const float* scores, int32_t ld, co
                            idx_out, dev_status, nq, ahead) != cudaSuccess)
         return DSA_ERR_CUDA;
     return launch_status();
+}
+
+extern "C" dsa_status_t dsa_topk_counted(int32_t nq, const float* scores, int32_t ld, const int32_t* n_valid, int32_t k,
+                                         int32_t* idx_out, unsigned* counts, int32_t* dev_status, void* stream) {
+    if (nq < 0 || k < 1 || k > 2048 || ld < 0 || (ld & 3)) return DSA_ERR_INVALID_ARG;
+    if (ld > 16384) return DSA_ERR_UNSUPPORTED;
+    if (nq == 0) return DSA_OK;
+    if (!scores || !n_valid || !idx_out || !counts || !aligned(scores, 16) || !aligned(counts, 16))
+        return DSA_ERR_INVALID_ARG;
+    const cudaError_t e = launch_pdl(topk_hist_kernel<1024, 16>, dim3(nq), dim3(1024), 0, static_cast<cudaStream_t>(stream),
+                                     scores, ld, n_valid, k, idx_out, counts, dev_status);
+    return e == cudaSuccess ? launch_status() : DSA_ERR_CUDA;
 }

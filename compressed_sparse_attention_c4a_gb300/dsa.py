@@ -21,7 +21,8 @@ KIND = {"c4a": DSA_C4A, "c128a": DSA_C128A}
 
 EXPORTS = ["dsa_status_string", "dsa_compress", "dsa_index_scores", "dsa_topk", "dsa_topk_plan", "dsa_attn_workspace_size",
            "dsa_sparse_attn_decode", "dsa_sparse_attn_prefill", "dsa_gather_rows", "dsa_sparse_attn_decode_static",
-           "dsa_attn_static_scratch_bytes", "dsa_attn_plan", "dsa_debug_index_scores_stalled"]
+           "dsa_attn_static_scratch_bytes", "dsa_attn_plan", "dsa_debug_index_scores_stalled", "dsa_index_topk",
+           "dsa_index_topk_workspace_size", "dsa_index_scores_counted", "dsa_topk_counted"]
 
 
 class DsaPool(ctypes.Structure):
@@ -53,6 +54,8 @@ _lib.dsa_attn_static_scratch_bytes.restype = ctypes.c_size_t
 _lib.dsa_attn_static_scratch_bytes.argtypes = []
 _lib.dsa_attn_plan.restype = ctypes.c_int32
 _lib.dsa_attn_plan.argtypes = [_I, _I, _I, _I, _P]
+_lib.dsa_index_topk_workspace_size.restype = ctypes.c_size_t
+_lib.dsa_index_topk_workspace_size.argtypes = [_I]
 _lib.dsa_topk_plan.restype = ctypes.c_int32
 _lib.dsa_topk_plan.argtypes = [_I, _I, _I, _P]
 for _name, _args in {
@@ -61,6 +64,10 @@ for _name, _args in {
     "dsa_debug_index_scores_stalled": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, ctypes.c_uint64, _P,
                                        _P],
     "dsa_topk": [_I, _P, _I, _P, _I, _P, _P, _P],
+    "dsa_index_topk": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _I, _P, _P, ctypes.c_size_t, _P,
+                       _P],
+    "dsa_index_scores_counted": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P],
+    "dsa_topk_counted": [_I, _P, _I, _P, _I, _P, _P, _P, _P],
     "dsa_sparse_attn_decode": [_I, _I, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, ctypes.c_float, _P, _P, _P, _P,
                                ctypes.c_size_t, _P, _P],
     "dsa_sparse_attn_prefill": [_I, _I, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, ctypes.c_float, _P, _P, _P,
@@ -142,6 +149,40 @@ def dsa_debug_index_scores_stalled(q8, q_scale, w, q_pos, q_req, q_group, keys, 
                                                _ptr(scores), scores.shape[1], _ptr(n_visible), int(wait_limit_ns),
                                                _ptr(dev_status), _stream(stream))
     _check("dsa_debug_index_scores_stalled", code)
+
+
+def dsa_index_topk_workspace_size(nq):
+    return int(_lib.dsa_index_topk_workspace_size(int(nq)))
+
+
+def dsa_index_topk(q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, k, idx_out, workspace, n_visible=None,
+                   dev_status=None, stream=None, fresh_from=None):
+    """Indexer scores with the per-query top-k fused in (see include/dsa.h); ``workspace`` a zero-filled
+    device buffer of at least dsa_index_topk_workspace_size(nq) bytes."""
+    nq, heads, dim = q8.shape
+    code = _lib.dsa_index_topk(nq, heads, dim, _ptr(q8), _ptr(q_scale), _ptr(w), _ptr(q_pos), _ptr(q_req),
+                               int(q_group), ctypes.byref(keys), ctypes.byref(bt), _ptr(scores), scores.shape[1],
+                               _ptr(n_visible), _ptr(fresh_from), int(k), _ptr(idx_out), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream))
+    _check("dsa_index_topk", code)
+
+
+def dsa_index_scores_counted(q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, counts, n_visible=None,
+                             dev_status=None, stream=None, fresh_from=None):
+    """dsa_index_scores that also counts each row's level-1 top-k histogram into ``counts`` (zero-filled)."""
+    nq, heads, dim = q8.shape
+    code = _lib.dsa_index_scores_counted(nq, heads, dim, _ptr(q8), _ptr(q_scale), _ptr(w), _ptr(q_pos), _ptr(q_req),
+                                         int(q_group), ctypes.byref(keys), ctypes.byref(bt), _ptr(scores),
+                                         scores.shape[1], _ptr(n_visible), _ptr(fresh_from), _ptr(counts),
+                                         _ptr(dev_status), _stream(stream))
+    _check("dsa_index_scores_counted", code)
+
+
+def dsa_topk_counted(scores, n_valid, k, idx_out, counts, dev_status=None, stream=None):
+    """dsa_topk starting from the counts dsa_index_scores_counted made (and clearing them)."""
+    code = _lib.dsa_topk_counted(scores.shape[0], _ptr(scores), scores.shape[1], _ptr(n_valid), int(k), _ptr(idx_out),
+                                 _ptr(counts), _ptr(dev_status), _stream(stream))
+    _check("dsa_topk_counted", code)
 
 
 def dsa_topk(scores, n_valid, k, idx_out, dev_status=None, stream=None):

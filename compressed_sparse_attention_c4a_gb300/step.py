@@ -27,7 +27,7 @@ def _query_group(spec, idx_heads):
 class LayerStep:
     """Device-resident state and buffers of one case (a dict from ``synth.make_case`` on cuda)."""
 
-    def __init__(self, case):
+    def __init__(self, case, counted_topk=False):
         spec = case["spec"]
         self.case, self.spec = case, spec
         dev = case["q"].device
@@ -39,6 +39,7 @@ class LayerStep:
         self.swa_bt = dsa.block_table(case["bt_swa"])
         self.rope_main = dsa.rope(spec.rope_dim, ROPE_THETA)
         self.has_index = spec.idx_heads > 0
+        self.fused_topk = False
         nq = case["nq"]
         if self.has_index:
             self.idx = dsa.pool(case["idx_data"], 64, case["idx_scale"])
@@ -49,6 +50,14 @@ class LayerStep:
             self.n_visible = torch.empty((nq,), dtype=torch.int32, device=dev)
             self.topk = torch.empty((nq, spec.topk), dtype=torch.int32, device=dev)
             self.q_group = _query_group(spec, spec.idx_heads)
+            # counted_topk: the indexer counts the top-k's first radix digit while scoring and the top-k starts
+            # from those counts (rows of up to 16,384 entries); off by default: on the decode batch the plain
+            # indexer and top-k measure faster (the counts' key-prefix buckets are coarser than the plain top-k's
+            # value buckets)
+            self.fused_topk = counted_topk and self.ld <= 16384
+            self.topk_ws = None
+            if self.fused_topk:
+                self.topk_ws = torch.zeros((dsa.dsa_index_topk_workspace_size(nq) // 4,), dtype=torch.int32, device=dev)
             # first indexer entry of each request that this step's compressor may write (entry i is complete
             # at position 4i + 7, so the entries before the first new token are old): older key pages are
             # scored while the compressor still runs
@@ -88,13 +97,24 @@ class LayerStep:
         self.compress_index()
 
     def index(self):
+        """Indexer scores (counting each row's first top-k digit when the counted top-k follows)."""
         c = self.case
-        dsa.dsa_index_scores(c["q8"], c["q_scale"], c["w"], c["q_pos"], c["q_req"], self.q_group, self.idx,
-                             self.idx_bt, self.scores, self.n_visible, dev_status=self.status,
-                             fresh_from=self.fresh_from)
+        if self.fused_topk:
+            dsa.dsa_index_scores_counted(c["q8"], c["q_scale"], c["w"], c["q_pos"], c["q_req"], self.q_group,
+                                         self.idx, self.idx_bt, self.scores, self.topk_ws, self.n_visible,
+                                         dev_status=self.status, fresh_from=self.fresh_from)
+        else:
+            dsa.dsa_index_scores(c["q8"], c["q_scale"], c["w"], c["q_pos"], c["q_req"], self.q_group, self.idx,
+                                 self.idx_bt, self.scores, self.n_visible, dev_status=self.status,
+                                 fresh_from=self.fresh_from)
 
     def select(self):
-        dsa.dsa_topk(self.scores, self.n_visible, self.spec.topk, self.topk, dev_status=self.status)
+        """Top-k of every query row (from the indexer's counts when it made them)."""
+        if self.fused_topk:
+            dsa.dsa_topk_counted(self.scores, self.n_visible, self.spec.topk, self.topk, self.topk_ws,
+                                 dev_status=self.status)
+        else:
+            dsa.dsa_topk(self.scores, self.n_visible, self.spec.topk, self.topk, dev_status=self.status)
 
     def attend(self, topk=None):
         c, s = self.case, self.spec

@@ -164,6 +164,39 @@ dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim, const uint
                               int32_t* n_visible, const int32_t* fresh_from, int32_t* dev_status, void* stream);
 
 /*
+ * dsa_index_scores_counted / dsa_topk_counted / dsa_index_topk - the indexer and the per-query top-k with the
+ * top-k's first pass fused into the indexer.  [P1] §4.1-4.2 (I_t, then S_t = TopK(I_t, k)), [P2] 第四层 (fuse
+ * work so that intermediate data is not read back).
+ *
+ * dsa_index_scores_counted is dsa_index_scores (same arguments, results and launch rules) that, while scoring,
+ * also counts each query row's visible scores by the top 11 bits of a monotone 32-bit key of the score:
+ * counts [nq][2048] uint32, zero-filled before the call (16-byte aligned).  Rows of at most ld = 16,384 scores.
+ * dsa_topk_counted is dsa_topk for such rows (ld <= 16,384, else DSA_ERR_UNSUPPORTED) that starts from those
+ * counts: the bucket of the k-th largest score comes from them, so the top-k reads its row once; it selects
+ * the same set, in the same order, as dsa_topk and leaves the counts zero-filled again.
+ * dsa_index_topk issues the two (for ld > 16,384: dsa_index_scores then dsa_topk), with the counts in
+ * `workspace` (>= dsa_index_topk_workspace_size(nq) bytes): zero-filled by the caller before the first call;
+ * every call that completes leaves it zero-filled (one that records DSA_ERR_TIMEOUT may not: clear it then).
+ * Calls that overlap on the GPU race on it.
+ *
+ * k          host int, 1 .. 2048;  idx_out [nq][k] int32 out;  n_visible required (the top-k's row lengths)
+ * scores     16-byte aligned
+ */
+size_t dsa_index_topk_workspace_size(int32_t nq);
+dsa_status_t dsa_index_scores_counted(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8, const float* q_scale,
+                                      const float* w, const int32_t* q_pos, const int32_t* q_req, int32_t q_group,
+                                      const dsa_pool_t* keys, const dsa_block_table_t* bt, float* scores, int32_t ld,
+                                      int32_t* n_visible, const int32_t* fresh_from, unsigned* counts,
+                                      int32_t* dev_status, void* stream);
+dsa_status_t dsa_topk_counted(int32_t nq, const float* scores, int32_t ld, const int32_t* n_valid, int32_t k,
+                              int32_t* idx_out, unsigned* counts, int32_t* dev_status, void* stream);
+dsa_status_t dsa_index_topk(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8, const float* q_scale,
+                            const float* w, const int32_t* q_pos, const int32_t* q_req, int32_t q_group,
+                            const dsa_pool_t* keys, const dsa_block_table_t* bt, float* scores, int32_t ld,
+                            int32_t* n_visible, const int32_t* fresh_from, int32_t k, int32_t* idx_out,
+                            void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
  * dsa_debug_index_scores_stalled - test hook of the bounded waits in dsa_index_scores; the pages have no
  * counterpart.  Launches the indexer as dsa_index_scores would (fresh_from = NULL), except that the warp that
  * issues the key and query copies issues none and posts no work, so the tensor-core and epilogue warps wait

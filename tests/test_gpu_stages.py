@@ -445,9 +445,14 @@ def test_compress_unmapped_block_faults_only_that_entry():
                     [swa.read(sbt[q], [int(start[q])])[0] for q in range(4)])
 
 
-def test_index_unmapped_block_scores_minus_inf():
+@pytest.mark.parametrize("counted", [False, True])
+def test_index_unmapped_block_scores_minus_inf(counted):
+    """Plain indexer + top-k, and the indexer that counts the top-k's first digit + the top-k from the counts."""
     from compressed_sparse_attention_c4a_gb300 import dsa
-    cpu, gpu, step = _setup("c4a_decode")
+    cpu = synth.make_case(CASES["c4a_decode"], "cpu")
+    gpu = to_device(cpu)
+    step = LayerStep(gpu, counted_topk=counted)
+    assert step.fused_topk == counted
     step.compress()
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0
@@ -455,6 +460,7 @@ def test_index_unmapped_block_scores_minus_inf():
     r, lb = 2, 1                                         # request 2 (193 visible entries): entries 64 .. 127
     gpu["bt_idx"][r, lb] = -1
     step.index()
+    step.select()
     torch.cuda.synchronize()
     assert int(step.status.item()) == dsa.DSA_ERR_DEVICE_FAULT
     got = np64(step.scores)
@@ -463,6 +469,11 @@ def test_index_unmapped_block_scores_minus_inf():
     keep = np.r_[0:64, 128:193]
     assert rel_l2(got[r, keep], want[r][keep]) <= ROW_REL_L2
     _check_score_rows(got, want, {q: n for q, n in nvis.items() if q != r})
+    tk, nv = np64(step.topk), np64(step.n_visible)        # the counted top-k sees the -inf entries as scores
+    for q in range(cpu["nq"]):
+        assert list(tk[q]) == list(OL.topk(got[q], int(nv[q]), cpu["spec"].topk)), q
+    if counted:
+        assert int(step.topk_ws.count_nonzero().item()) == 0
 
 
 @pytest.mark.parametrize("wait_ms,name", [(20, "c4a_decode"), (20, "c4a_multi_prefill")])
@@ -530,3 +541,79 @@ def test_attention_unmapped_block_zeroes_the_row(name):
     assert np.max(np.abs(out[rows] - W)) <= ATTN_MAX_ABS
     assert rel_l2(out[rows], W) <= ATTN_REL_L2
     assert np.max(np.abs(lse[rows] - np.stack([wl[q] for q in rows]))) <= 1e-3
+
+
+
+# ---- indexer with the top-k's first digit counted while scoring, and the top-k that starts from it ---------
+FUSED = {
+    "c4a_decode": CASES["c4a_decode"],                 # four rows, one of them below k
+    "c4a_decode_48": SHARP["c4a_decode_48"],           # 48 rows, each spread over several CTAs
+    "c4a_multi_prefill": CASES["c4a_multi_prefill"],   # groups of 32 queries selected by the CTA finishing them
+    "c4a_early": CASES["c4a_early"],                   # groups of 4; rows without a visible entry
+}
+
+
+def _fused_call(step, ws, idx):
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    c = step.case
+    dsa.dsa_index_topk(c["q8"], c["q_scale"], c["w"], c["q_pos"], c["q_req"], step.q_group, step.idx, step.idx_bt,
+                       step.scores, step.spec.topk, idx, ws, step.n_visible, dev_status=step.status,
+                       fresh_from=step.fresh_from)
+
+
+@pytest.mark.parametrize("name", list(FUSED))
+def test_index_topk_fused_exact(name):
+    """dsa_index_topk (the indexer counting each row's first radix digit, then the top-k starting from those
+    counts) lists, for the very scores it wrote, exactly the indices the oracle's top-k takes (ties to the lower
+    index, increasing order, -1 padding); twice in a row, the counts back to zero each time."""
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    spec = FUSED[name]
+    cpu = synth.make_case(spec, "cpu")
+    gpu = to_device(cpu)
+    step = LayerStep(gpu)
+    step.compress()
+    torch.cuda.synchronize()
+    nq, k = cpu["nq"], spec.topk
+    ws = torch.zeros((dsa.dsa_index_topk_workspace_size(nq),), dtype=torch.uint8, device="cuda")
+    want, nvis = _oracle_scores_on_gpu_pool(cpu, gpu)
+    for _ in range(2):
+        idx = torch.full((nq, k), -7, dtype=torch.int32, device="cuda")
+        step.scores.fill_(float("nan"))
+        _fused_call(step, ws, idx)
+        torch.cuda.synchronize()
+        assert int(step.status.item()) == 0
+        assert int(ws.count_nonzero().item()) == 0
+        got, gi, nv = np64(step.scores), np64(idx), np64(step.n_visible)
+        _check_score_rows(got, want, nvis, nv, step.ld)
+        for q in range(nq):
+            assert list(gi[q]) == list(OL.topk(got[q], int(nv[q]), k)), q
+            ok, nd = topk_sets_match(gi[q], want[q], int(nv[q]), k)
+            assert ok, (q, nd)
+
+
+def test_index_topk_fused_heavy_ties():
+    """Rows whose scores are all equal (one request's key rows all the same; another request's head weights
+    all zero, so every score is 0): the selection descends to the exact tied key and takes the lowest indices."""
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    cpu, gpu, step = _setup("c4a_decode")
+    step.compress()
+    torch.cuda.synchronize()
+    bt = gpu["bt_idx"]
+    r = 3                                                  # m = 4095: 1023 visible entries in blocks 0 .. 15
+    src = int(bt[r, 0]) * 64
+    for lb in range(16):
+        pb = int(bt[r, lb])
+        gpu["idx_data"][pb * 64:(pb + 1) * 64] = gpu["idx_data"][src]
+        gpu["idx_scale"][pb * 64:(pb + 1) * 64] = gpu["idx_scale"][src]
+    gpu["w"][1].zero_()                                     # request 1 (749 visible entries): every score 0
+    ws = torch.zeros((dsa.dsa_index_topk_workspace_size(cpu["nq"]),), dtype=torch.uint8, device="cuda")
+    idx = torch.full((cpu["nq"], 512), -7, dtype=torch.int32, device="cuda")
+    _fused_call(step, ws, idx)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    gi, got, nv = np64(idx), np64(step.scores), np64(step.n_visible)
+    assert np.all(got[3, :1023] == got[3, 0]) and np.all(got[1, :749] == 0.0)
+    assert list(gi[3]) == list(range(512)) and list(gi[1]) == list(range(512))
+    for q in range(cpu["nq"]):
+        assert list(gi[q]) == list(OL.topk(got[q], int(nv[q]), 512)), q
+    assert int(ws.count_nonzero().item()) == 0
