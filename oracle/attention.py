@@ -17,9 +17,11 @@ Readings:
 """
 import numpy as np
 
+from .codecs import e4m3_encode, fp8_row_scale
 from .rope import rope, ROPE_THETA
 
 SWA_WINDOW = 128
+OUT_Q8_BLOCK = 128   # dims per fp8 output scale
 
 
 def window_positions(m, window=SWA_WINDOW):
@@ -45,3 +47,20 @@ def sparse_attention(q, keys, m, rope_dim, sm_scale, theta=ROPE_THETA, inverse_r
     if inverse_rope:
         o = rope(o, m, rope_dim, theta, inverse=True)
     return o, lse
+
+
+def quantize_output(o, block=OUT_Q8_BLOCK):
+    """The fp8 form of an attention output ([P2] 融合点 2: the inverse-rotated output is quantised to fp8 for
+    the o_lora projection that follows).  o [..., d] float64 (after R_m^-1); every `block` consecutive dims of a
+    row share one fp32 scale = amax / 448 (1 for an all-zero block) and code = e4m3(value / scale).
+
+    Reading (the pages name no granularity): one scale per (token, head, 128-dim block).
+    Returns (codes uint8 [..., d], scales float64 [..., d / block]).
+    """
+    o = np.asarray(o, dtype=np.float64)
+    d = o.shape[-1]
+    assert d % block == 0
+    blocks = o.reshape(o.shape[:-1] + (d // block, block))
+    scale = fp8_row_scale(blocks)                             # [..., d/block], fp32 values
+    codes = e4m3_encode(blocks / scale[..., None])
+    return codes.reshape(o.shape), scale

@@ -12,7 +12,7 @@ to the storage format with this package's codecs, exactly as a stored row reads 
 import numpy as np
 
 from . import codecs, paging
-from .attention import sparse_attention, window_positions
+from .attention import sparse_attention, window_positions, quantize_output
 from .compress import RollingState, WINDOW, C4A, swa_rows
 from .indexer import index_scores as _index_scores, visible_entries
 from .rope import ROPE_THETA
@@ -141,10 +141,19 @@ def sparse_attn(q, q_pos, q_req, kind, topk_ids, main_pool, main_bt, swa_pool, s
     return out, lse
 
 
+def sparse_attn_q8(q, q_pos, q_req, kind, topk_ids, main_pool, main_bt, swa_pool, swa_bt, window, sm_scale,
+                   rope_dim, theta=ROPE_THETA, rows=None):
+    """sparse_attn with the output in fp8 (quantize_output): ({row: (codes [H][d], scales [H][d/128])},
+    {row: lse [H]}, {row: out [H][d] float64 before quantisation})."""
+    out, lse = sparse_attn(q, q_pos, q_req, kind, topk_ids, main_pool, main_bt, swa_pool, swa_bt, window, sm_scale,
+                           rope_dim, theta, rows)
+    return {r: quantize_output(o) for r, o in out.items()}, lse, out
+
+
 def ring_contents(states):
     """(x [B][w][d], z [B][w]) of a list of RollingStates, slot = position mod w."""
     return np.stack([s.x for s in states]), np.stack([s.z for s in states])
 
 
-__all__ = ["Pool", "BF16", "FP8", "compress", "index_scores", "topk", "sparse_attn",
+__all__ = ["Pool", "BF16", "FP8", "compress", "index_scores", "topk", "sparse_attn", "sparse_attn_q8",
            "ring_contents", "WINDOW"]

@@ -178,3 +178,57 @@ def test_single_key_output_is_key_unrotated():
     k = rng.standard_normal(16)
     o, _ = sparse_attention(rng.standard_normal((2, 16)), R.rope(k, 900, 8)[None], 900, 8, 0.5)
     assert np.allclose(o, np.broadcast_to(k, (2, 16)), atol=1e-12)
+
+
+# ---- fp8 output (inverse RoPE + fp8 quantisation, [P2] 融合点 2) -----------------------------------------
+def test_quantize_output_blocks_are_independent_and_saturate_at_448():
+    from oracle.attention import quantize_output
+    from oracle.codecs import e4m3_decode
+    rng = np.random.default_rng(9)
+    o = rng.standard_normal((3, 512))
+    o[0, 5] = 1000.0                                   # a large value in block 0 of head 0 only
+    codes, scale = quantize_output(o)
+    assert codes.shape == (3, 512) and scale.shape == (3, 4)
+    # each block's scale is its own amax / 448 (fp32): the outlier does not touch blocks 1-3
+    for h in range(3):
+        for b in range(4):
+            blk = o[h, 128 * b:128 * (b + 1)]
+            assert scale[h, b] == np.float32(np.max(np.abs(blk)) / 448.0)
+    # the block's largest magnitude maps to the largest code, +-448
+    assert e4m3_decode(codes[0, 5:6])[0] == 448.0
+    assert np.max(np.abs(e4m3_decode(codes[1, :128]))) == 448.0
+    # dequantised within half an e4m3 step: relative 2^-4 for normals (absolute 2^-10 * scale below 2^-6)
+    deq = e4m3_decode(codes).reshape(3, 4, 128) * scale[..., None]
+    err = np.abs(deq.reshape(3, 512) - o)
+    bound = np.maximum(np.abs(o) * 2.0 ** -4, np.repeat(scale, 128, axis=1) * 2.0 ** -10)
+    assert np.all(err <= bound * (1 + 1e-9))
+
+
+def test_quantize_output_zero_block_and_negative_zero():
+    from oracle.attention import quantize_output
+    o = np.zeros((1, 512))
+    o[0, 128:] = 1.0
+    o[0, 200] = -0.0
+    o[0, 300] = -1e-30                                 # rounds to zero, keeps its sign
+    codes, scale = quantize_output(o)
+    assert scale[0, 0] == 1.0 and np.all(codes[0, :128] == 0)   # all-zero block: scale 1, codes +0
+    assert codes[0, 300] == 0x80                                  # -0 code
+    assert np.all(scale[0, 1:] == np.float32(1.0 / 448.0))
+
+
+def test_sparse_attn_q8_is_the_quantised_sparse_attn():
+    """The layer call's fp8 output equals quantize_output of the float64 output it returns beside it."""
+    from oracle import layer as OL
+    from oracle.attention import quantize_output
+    rng = np.random.default_rng(3)
+    epb = 64
+    main = OL.Pool(epb, OL.BF16, rng.standard_normal((4 * epb, 512)))
+    swa = OL.Pool(256, OL.BF16, rng.standard_normal((2 * 256, 512)))
+    bt = np.array([[2, 0, 3, 1]])
+    sbt = np.array([[1, 0]])
+    q = rng.standard_normal((1, 8, 512))
+    topk = np.array([[3, 7, 11, -1]])
+    q8, lse, out = OL.sparse_attn_q8(q, [300], [0], "c4a", topk, main, bt, swa, sbt, 128, 512 ** -0.5, 64)
+    codes, scales = q8[0]
+    want_c, want_s = quantize_output(out[0])
+    assert np.array_equal(codes, want_c) and np.array_equal(scales, want_s)
