@@ -9,6 +9,11 @@ S.1111.111 is NaN).
 
 All rounding is round-to-nearest, ties-to-even, written as ``np.rint`` on the
 significand (numpy's rint rounds half to even).
+
+[P2] 第三层 also names an fp4 indexer cache ("indexer 用 fp4") without its encoding; it follows
+the OCP Microscaling (MX) FP4 E2M1 element (bias 1, values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their
+negatives, no infinities or NaN), two codes per byte with the even element in the low nibble, one
+fp32 scale per row (amax / 6) as for the e4m3 rows.
 """
 import numpy as np
 
@@ -111,3 +116,78 @@ def fp8_quantize_rows(v):
 def fp8_dequantize_rows(codes, scale):
     """Row value = scale * decode(code), the token-wise fp8 reading of a cache row."""
     return e4m3_decode(codes) * np.asarray(scale, dtype=np.float64)[..., None]
+
+
+# ---- fp4 e2m1 ------------------------------------------------------------------------------------
+E2M1_MAX = 6.0
+
+
+def e2m1_decode(codes):
+    """Decode e2m1 codes (0..15) to float64: S EE M, bias 1; E == 0 is subnormal, 0.5 * M."""
+    c = np.asarray(codes, dtype=np.int64) & 0xF
+    s = (c >> 3) & 1
+    E = (c >> 1) & 0x3
+    M = c & 1
+    mag = np.where(E == 0, 0.5 * M, np.ldexp(1.0 + M / 2.0, E - 1))
+    return np.where(s == 1, -mag, mag)
+
+
+def e2m1_round(x):
+    """Round float64 values onto the e2m1 grid, RNE, saturating to +-6.
+
+    Normal range (|x| >= 1): 2 significant bits, so the significand m * 2^2 of frexp is rounded.
+    Subnormal range: multiples of 0.5.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    m, e = np.frexp(a)
+    normal = np.ldexp(np.rint(m * 4.0), e - 2)
+    sub = np.rint(a / 0.5) * 0.5
+    r = np.where(a < 1.0, sub, normal)
+    r = np.minimum(r, E2M1_MAX)
+    return np.where(np.signbit(x), -r, r)
+
+
+_E2M1_POSITIVE = e2m1_decode(np.arange(8))   # codes 0..7, increasing
+
+
+def e2m1_encode(x):
+    """Encode float64 values to e2m1 codes (uint8 0..15; RNE, saturating; the sign kept for -0)."""
+    r = e2m1_round(x)
+    code = np.searchsorted(_E2M1_POSITIVE, np.abs(r)).astype(np.uint8)
+    return np.where(np.signbit(r), code | 0x8, code).astype(np.uint8)
+
+
+def fp4_pack(codes):
+    """[..., d] e2m1 codes -> [..., d / 2] bytes: element 2j in the low nibble, 2j + 1 in the high one."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] & 0xF) | ((c[..., 1::2] & 0xF) << 4)
+
+
+def fp4_unpack(packed):
+    """[..., d / 2] bytes -> [..., d] e2m1 codes."""
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def fp4_row_scale(v):
+    """Per-row scale of fp4 rows: amax / 6 stored as fp32 (1 if amax == 0)."""
+    v = np.asarray(v, dtype=np.float64)
+    amax = np.max(np.abs(v), axis=-1)
+    scale = np.where(amax > 0, amax / E2M1_MAX, 1.0)
+    return scale.astype(np.float32).astype(np.float64)
+
+
+def fp4_quantize_rows(v):
+    """Quantise rows to (packed e2m1 bytes [..., d / 2], fp32 scale) with code = e2m1(v / scale)."""
+    v = np.asarray(v, dtype=np.float64)
+    scale = fp4_row_scale(v)
+    return fp4_pack(e2m1_encode(v / scale[..., None])), scale
+
+
+def fp4_dequantize_rows(packed, scale):
+    """Row value = scale * e2m1(code)."""
+    return e2m1_decode(fp4_unpack(packed)) * np.asarray(scale, dtype=np.float64)[..., None]

@@ -14,7 +14,7 @@ entries score -inf.
 """
 import numpy as np
 
-from .codecs import e4m3_decode
+from .codecs import e4m3_decode, e2m1_decode
 from .compress import n_entries
 
 
@@ -23,14 +23,16 @@ def visible_entries(m, kind):
     return n_entries(m + 1, kind)
 
 
-def index_scores(q_codes, q_scale, w, k_codes, k_scale, n_visible):
+def index_scores(q_codes, q_scale, w, k_codes, k_scale, n_visible, key_format="e4m3"):
     """Scores of one query against entries 0 .. len(k_codes) - 1.
 
-    q_codes [H][d] uint8, q_scale [H], w [H], k_codes [n][d] uint8, k_scale [n].
+    q_codes [H][d] uint8 (e4m3), q_scale [H], w [H], k_codes [n][d] uint8 (e4m3, or e2m1 codes 0..15 with
+    key_format "e2m1": the fp4 indexer cache of [P2] 第三层), k_scale [n].
     Returns float64 [n]; entries at or beyond ``n_visible`` are -inf.
     """
     q = e4m3_decode(q_codes) * np.asarray(q_scale, dtype=np.float64)[:, None]   # [H][d]
-    k = e4m3_decode(k_codes) * np.asarray(k_scale, dtype=np.float64)[:, None]   # [n][d]
+    kdec = e2m1_decode if key_format == "e2m1" else e4m3_decode
+    k = kdec(k_codes) * np.asarray(k_scale, dtype=np.float64)[:, None]          # [n][d]
     per_head = np.maximum(k @ q.T, 0.0)                                          # [n][H]
     scores = per_head @ np.asarray(w, dtype=np.float64)                          # [n]
     scores[n_visible:] = -np.inf

@@ -20,12 +20,14 @@ from .topk import topk as _topk
 
 BF16 = "bf16"
 FP8 = "fp8_e4m3"
+FP4 = "fp4_e2m1"
 
 
 class Pool:
     """A paged cache pool: ``data`` [num_blocks * epb, dim], ``scale`` [num_blocks * epb] for fp8.
 
-    bf16 pools hold either float64 values or the raw uint16 bit patterns (decoded on read).
+    bf16 pools hold either float64 values or the raw uint16 bit patterns (decoded on read); fp4 pools hold
+    packed e2m1 bytes [num_blocks * epb, dim / 2] and a scale per row.
     """
 
     def __init__(self, epb, dtype, data, scale=None):
@@ -46,6 +48,8 @@ class Pool:
             if self.bits:
                 return codecs.bf16_decode(self.data[rows])
             return np.asarray(self.data[rows], dtype=np.float64)
+        if self.dtype == FP4:
+            return codecs.fp4_dequantize_rows(self.data[rows], self.scale[rows])
         return codecs.fp8_dequantize_rows(self.data[rows], self.scale[rows])
 
     def read_codes(self, table_row, ids):
@@ -59,6 +63,10 @@ class Pool:
         values = np.atleast_2d(np.asarray(values, dtype=np.float64))
         if self.dtype == BF16:
             self.data[rows] = codecs.bf16_encode(values) if self.bits else codecs.bf16_round(values)
+        elif self.dtype == FP4:
+            codes, scale = codecs.fp4_quantize_rows(values)
+            self.data[rows] = codes
+            self.scale[rows] = scale
         else:
             codes, scale = codecs.fp8_quantize_rows(values)
             self.data[rows] = codes
@@ -108,7 +116,10 @@ def index_scores(q_codes, q_scale, w, q_pos, q_req, key_pool, bt, kind=C4A, rows
         m, r = int(q_pos[q]), int(q_req[q])
         n = visible_entries(m, kind)
         codes, scale = key_pool.read_codes(bt[r], np.arange(n))
-        out[q] = _index_scores(q_codes[q], q_scale[q], w[q], codes, scale, n)
+        if key_pool.dtype == FP4:
+            codes = codecs.fp4_unpack(codes)
+        out[q] = _index_scores(q_codes[q], q_scale[q], w[q], codes, scale, n,
+                               key_format="e2m1" if key_pool.dtype == FP4 else "e4m3")
         nvis[q] = n
     return out, nvis
 
@@ -155,5 +166,5 @@ def ring_contents(states):
     return np.stack([s.x for s in states]), np.stack([s.z for s in states])
 
 
-__all__ = ["Pool", "BF16", "FP8", "compress", "index_scores", "topk", "sparse_attn", "sparse_attn_q8",
+__all__ = ["Pool", "BF16", "FP8", "FP4", "compress", "index_scores", "topk", "sparse_attn", "sparse_attn_q8",
            "ring_contents", "WINDOW"]

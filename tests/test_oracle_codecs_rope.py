@@ -125,3 +125,76 @@ def test_rope_group_identities():
     s1 = R.rope(q, 500, 64) @ R.rope(k, 300, 64)
     s2 = R.rope(q, 500 + 777, 64) @ R.rope(k, 300 + 777, 64)
     assert abs(s1 - s2) < 1e-10
+
+
+# ---- fp4 e2m1 (the fp4 indexer cache) --------------------------------------------------------------------
+def _e2m1_golden():
+    rows = []
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "e2m1_ocp.txt")):
+        if line.strip() and not line.startswith("#"):
+            c, v = line.split()
+            rows.append((int(c), float(v)))
+    return rows
+
+
+def test_e2m1_decode_matches_the_ocp_table():
+    from oracle.codecs import e2m1_decode
+    g = _e2m1_golden()
+    assert len(g) == 16
+    for c, v in g:
+        got = e2m1_decode(np.array([c]))[0]
+        assert got == v and np.signbit(got) == np.signbit(v), (c, got, v)
+
+
+def test_e2m1_round_trip_midpoints_and_saturation():
+    from oracle.codecs import e2m1_decode, e2m1_encode, e2m1_round
+    codes = np.arange(16, dtype=np.uint8)
+    assert np.array_equal(e2m1_encode(e2m1_decode(codes)), codes)                 # every code (with -0)
+    # ties to even: 0.25 -> 0, 0.75 -> 1, 1.25 -> 1, 1.75 -> 2, 2.5 -> 2, 3.5 -> 4, 5 -> 4
+    x = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -5.0, -0.25])
+    assert list(e2m1_round(x)) == [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, -4.0, -0.0]
+    # just off the midpoints: nearest
+    eps = 1e-9
+    assert list(e2m1_round(np.array([0.25 + eps, 2.5 + eps, 5.0 - eps]))) == [0.5, 3.0, 4.0]
+    # saturation to +-6 and the sign of a negative zero
+    assert list(e2m1_round(np.array([6.9, 1e9, -7.0]))) == [6.0, 6.0, -6.0]
+    assert e2m1_encode(np.array([-1e-9]))[0] == 0x8
+
+
+def test_fp4_pack_order_and_row_quantisation():
+    from oracle.codecs import fp4_pack, fp4_unpack, fp4_quantize_rows, fp4_dequantize_rows, e2m1_decode
+    c = np.array([[1, 2, 3, 15]], dtype=np.uint8)
+    p = fp4_pack(c)
+    assert list(p[0]) == [0x21, 0xF3]                       # element 2j in the low nibble
+    assert np.array_equal(fp4_unpack(p), c)
+    rng = np.random.default_rng(4)
+    v = rng.standard_normal((20, 128)) * np.exp(rng.uniform(-2, 2, (20, 1)))
+    packed, scale = fp4_quantize_rows(v)
+    assert packed.shape == (20, 64)
+    assert np.all(scale == (np.max(np.abs(v), axis=1) / 6.0).astype(np.float32))
+    deq = fp4_dequantize_rows(packed, scale)
+    # the largest magnitude of each row maps to +-6; every element within half a step of the e2m1 grid
+    assert np.all(np.max(np.abs(e2m1_decode(fp4_unpack(packed))), axis=1) == 6.0)
+    u = np.abs(v / scale[:, None])
+    half = np.where(u < 2, 0.25, np.where(u < 4, 0.5, 1.0))
+    assert np.all(np.abs(deq / scale[:, None] - v / scale[:, None]) <= half + 1e-12)
+
+
+def test_index_scores_with_fp4_keys_brute_force():
+    """The indexer score with e2m1 keys: a brute-force loop over heads and dims of the decoded values."""
+    from oracle.indexer import index_scores
+    from oracle.codecs import e2m1_decode, e4m3_decode
+    rng = np.random.default_rng(6)
+    H, d, n = 4, 32, 9
+    qc = rng.integers(0, 0x7F, (H, d)).astype(np.uint8)
+    kc = rng.integers(0, 16, (n, d)).astype(np.uint8)
+    qs, ks, w = rng.uniform(0.1, 1, H), rng.uniform(0.1, 1, n), rng.uniform(0, 1, H)
+    got = index_scores(qc, qs, w, kc, ks, 7, key_format="e2m1")
+    for i in range(n):
+        want = -np.inf
+        if i < 7:
+            want = 0.0
+            for h in range(H):
+                dot = sum(e4m3_decode(qc[h, c]) * e2m1_decode(kc[i, c]) for c in range(d))
+                want += w[h] * max(0.0, qs[h] * ks[i] * dot)
+        assert (got[i] == want) if i >= 7 else abs(got[i] - want) <= 1e-12 * max(1.0, abs(want)), i
