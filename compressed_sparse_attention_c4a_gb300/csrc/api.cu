@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(dsa_pool_t pool, dsa_b
     }
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(pool.data) + prow * row_bytes);
     for (int c = lane; c < pieces; c += 32) dst[c] = src[c];
-    if (lane == 0 && out_scale && pool.dtype == DSA_FP8_E4M3) out_scale[j] = pool.scale[prow];
+    if (lane == 0 && out_scale && pool.dtype != DSA_BF16) out_scale[j] = pool.scale[prow];
 }
 
 }  // namespace dsa
@@ -58,7 +58,7 @@ extern "C" dsa_status_t dsa_gather_rows(const dsa_pool_t* pool, const dsa_block_
     if (n == 0) return DSA_OK;
     if (!pool_ok(pool) || !bt || !bt->table || bt->max_blocks <= 0 || bt->batch <= 0 || !req || !ids || !out)
         return DSA_ERR_INVALID_ARG;
-    const int row_bytes = pool->dim * (pool->dtype == DSA_BF16 ? 2 : 1);
+    const int row_bytes = (int)row_bytes_of(pool);
     if (row_bytes % 16 || !aligned(out, 16)) return DSA_ERR_INVALID_ARG;
     if (launch_pdl(gather_rows_kernel, dim3((n + 7) / 8), dim3(256), 0, static_cast<cudaStream_t>(stream), *pool, *bt,
                    n, req, ids, static_cast<uint8_t*>(out), out_scale, row_bytes, dev_status) != cudaSuccess)

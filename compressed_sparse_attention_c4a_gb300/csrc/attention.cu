@@ -37,7 +37,9 @@ struct AttnArgs {
     int window;
     float scale_log2;                         // sm_scale * log2(e)
     RopeTable rope;
-    uint16_t* out;
+    uint16_t* out;                            // bf16 output, or NULL with out8
+    uint8_t* out8;                            // e4m3 output [rows][heads][512] (with out_scale), or NULL
+    float* out_scale;                         // [rows][heads][4]: amax / 448 of each 128-dim block
     float* lse;
     float* ws_o;                              // [rows][nsplit][heads][512]
     float* ws_ml;                             // [rows][nsplit][heads][4]: M, L (bf16 P), E (fp32 P), 0
@@ -112,8 +114,19 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
             acc[e + 1] = -x0 * sn + x1 * cs;
         }
     }
-    uint16_t* dst = a.out + ((long long)row * a.heads + head) * kD + tid * 4;
-    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
+    if (a.out8) {  // e4m3 with one scale per 128-dim block: a warp holds one block
+        float am = fmaxf(fmaxf(fabsf(acc[0]), fabsf(acc[1])), fmaxf(fabsf(acc[2]), fabsf(acc[3])));
+        am = warp_max(am);
+        const float sc = am > 0.f ? am / 448.f : 1.f;
+        uint32_t c = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c |= (uint32_t)float_to_e4m3(acc[e] / sc) << (8 * e);
+        *reinterpret_cast<uint32_t*>(a.out8 + ((long long)row * a.heads + head) * kD + tid * 4) = c;
+        if ((tid & 31) == 0) a.out_scale[((long long)row * a.heads + head) * 4 + tid / 32] = sc;
+    } else {
+        uint16_t* dst = a.out + ((long long)row * a.heads + head) * kD + tid * 4;
+        *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
+    }
     if (a.lse && tid == 0)
         a.lse[(long long)row * a.heads + head] = Es > 0.f ? (M + log2f(Es)) / kLog2e : -INFINITY;
 }
@@ -872,21 +885,54 @@ __global__ void __launch_bounds__(kClThreads, 1)
             }
             // neighbouring lanes swap one value per pair of heads: the even lane then holds dims (De, De + 1) of
             // head 2p, the odd lane those of head 2p + 1; each rotates its pair by R_m^-1 and stores it packed
+            float rr[G];
 #pragma unroll
             for (int pp = 0; pp < G / 2; ++pp) {
                 const float x0 = v[2 * pp] * inv[2 * pp], x1 = v[2 * pp + 1] * inv[2 * pp + 1];
                 const float recv = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
                 const float lo = odd ? recv : x0, hi = odd ? x1 : recv;
-                const float r0 = lo * rc + hi * rs, r1 = hi * rc - lo * rs;
-                const int hh = h0 + 2 * pp + (odd ? 1 : 0);
-                o32[hh * 64 + (d >> 1)] = bf16x2_rn(r0, r1);
+                rr[2 * pp] = lo * rc + hi * rs;
+                rr[2 * pp + 1] = hi * rc - lo * rs;
+            }
+            if (!a.out8) {
+#pragma unroll
+                for (int pp = 0; pp < G / 2; ++pp)
+                    o32[(h0 + 2 * pp + (odd ? 1 : 0)) * 64 + (d >> 1)] = bf16x2_rn(rr[2 * pp], rr[2 * pp + 1]);
+            } else {
+                // e4m3 ([P2] 融合点 2: the inverse rotation and the fp8 quantisation in one pass): each head's 128
+                // dims of this tile share a scale amax / 448; the amax of a head is reduced over the lanes of its
+                // parity, then over the quarter's four warps in shared memory (the statistics slots, free now)
+                unsigned* s_amax = reinterpret_cast<unsigned*>(s_own);
+                if (tid < NH) s_amax[tid] = 0u;
+                __syncthreads();
+#pragma unroll
+                for (int pp = 0; pp < G / 2; ++pp) {
+                    float am = fmaxf(fabsf(rr[2 * pp]), fabsf(rr[2 * pp + 1]));
+#pragma unroll
+                    for (int o = 2; o < 32; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+                    if (lane < 2) atomicMax(&s_amax[h0 + 2 * pp + lane], __float_as_uint(am));
+                }
+                __syncthreads();
+                uint16_t* o16 = reinterpret_cast<uint16_t*>(obuf);  // [NH][128] e4m3 codes
+#pragma unroll
+                for (int pp = 0; pp < G / 2; ++pp) {
+                    const int hh = h0 + 2 * pp + (odd ? 1 : 0);
+                    const float am = __uint_as_float(s_amax[hh]);
+                    const float sc = am > 0.f ? am / 448.f : 1.f;
+                    o16[hh * 64 + (d >> 1)] =
+                        (uint16_t)(float_to_e4m3(rr[2 * pp] / sc) | ((uint32_t)float_to_e4m3(rr[2 * pp + 1] / sc) << 8));
+                }
+                if (tid < NH) {
+                    const float am = __uint_as_float(s_amax[tid]);
+                    a.out_scale[((long long)row * a.heads + hg * NH + tid) * 4 + t] = am > 0.f ? am / 448.f : 1.f;
+                }
             }
             if (tid == 0 && j == 0) DSA_STAMP(21);
             fence_proxy_async_smem();  // staged output -> async proxy (the TMA store)
             __syncthreads();
             if (tid == 0 && j == 0) DSA_STAMP(22);
             if (tid == 0) {  // NH rows of 128 dims -> out[row][hg * NH .. + NH][t * 128 .. + 128]
-                tma_store_2d(&omap, t * 128, row * a.heads + hg * NH, obuf);
+                tma_store_2d(&omap, a.out8 ? t * 128 : t * 128, row * a.heads + hg * NH, obuf);
                 bulk_commit();
             }
         } else {
@@ -979,15 +1025,17 @@ static bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t rows, int
 
 // Tensor map of the [rows][512] bf16 output for boxes of 128 columns x box_rows rows, unswizzled (the staging
 // layout [box_rows][128]).
-static bool make_out_map(CUtensorMap* map, void* base, uint64_t rows, int box_rows) {
+static bool make_out_map(CUtensorMap* map, void* base, uint64_t rows, int box_rows, bool e4m3) {
     auto fn = tensor_map_encoder();
     if (!fn) return false;
+    const int es = e4m3 ? 1 : 2;
     cuuint64_t gdim[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-    cuuint64_t gstride[1] = {(cuuint64_t)kD * 2};
+    cuuint64_t gstride[1] = {(cuuint64_t)kD * es};
     cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
     cuuint32_t estride[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return fn(map, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, gdim, gstride, box,
+              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int NH, bool FP8>
@@ -995,7 +1043,9 @@ static dsa_status_t launch_attn_cl(const AttnArgs& a, int cl, cudaStream_t st) {
     using L = ClSmem<NH>;
     CUtensorMap qmap, omap;
     if (!make_bf16_map(&qmap, a.q, (uint64_t)a.rows * a.heads, NH)) return DSA_ERR_CUDA;
-    if (!make_out_map(&omap, a.out, (uint64_t)a.rows * a.heads, NH)) return DSA_ERR_CUDA;
+    if (!make_out_map(&omap, a.out8 ? static_cast<void*>(a.out8) : static_cast<void*>(a.out), (uint64_t)a.rows * a.heads,
+                      NH, a.out8 != nullptr))
+        return DSA_ERR_CUDA;
     if (cudaFuncSetAttribute(attn_cl_kernel<NH, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
         cudaSuccess)
         return DSA_ERR_CUDA;
@@ -1013,18 +1063,21 @@ static dsa_status_t sparse_attn(int32_t rows, int32_t heads, const void* q, cons
                                 const dsa_pool_t* main, const dsa_block_table_t* main_bt, const dsa_pool_t* swa,
                                 const dsa_block_table_t* swa_bt, int32_t window, float sm_scale,
                                 const dsa_rope_t* rope, void* out, float* lse, void* workspace,
-                                size_t workspace_bytes, int32_t* dev_status, void* stream) {
+                                size_t workspace_bytes, int32_t* dev_status, void* stream, uint8_t* out8 = nullptr,
+                                float* out_scale = nullptr) {
     if (rows < 0) return DSA_ERR_INVALID_ARG;
     if (rows == 0) return DSA_OK;
     if (kind != DSA_C4A && kind != DSA_C128A) return DSA_ERR_INVALID_ARG;
     if (heads != 16 && heads != 32 && heads != 64 && heads != 128) return DSA_ERR_UNSUPPORTED;
-    if (!q || !q_pos || !out || !rope || !aligned(q, 16) || !aligned(out, 16)) return DSA_ERR_INVALID_ARG;
+    void* const dst = out8 ? static_cast<void*>(out8) : out;
+    if (!q || !q_pos || !dst || !rope || !aligned(q, 16) || !aligned(dst, 16)) return DSA_ERR_INVALID_ARG;
+    if (out8 && (!out_scale || !aligned(out_scale, 16))) return DSA_ERR_INVALID_ARG;
     if (topk && (k < 1 || k > 2048)) return DSA_ERR_INVALID_ARG;
     if (window < 1 || window > 1024 || !(sm_scale > 0.f)) return DSA_ERR_INVALID_ARG;
     if (!pool_ok(main) || !pool_ok(swa) || !main_bt || !main_bt->table || !swa_bt || !swa_bt->table)
         return DSA_ERR_INVALID_ARG;
     if (main->dim != kD || swa->dim != kD) return DSA_ERR_UNSUPPORTED;
-    if (main->dtype != swa->dtype) return DSA_ERR_UNSUPPORTED;
+    if (main->dtype != swa->dtype || main->dtype == DSA_FP4_E2M1) return DSA_ERR_UNSUPPORTED;
     if ((long long)main->num_blocks * main->rows_per_block > 0x7fffffffll ||
         (long long)swa->num_blocks * swa->rows_per_block > 0x7fffffffll)
         return DSA_ERR_UNSUPPORTED;  // rows are addressed with 32-bit indices
@@ -1058,7 +1111,9 @@ static dsa_status_t sparse_attn(int32_t rows, int32_t heads, const void* q, cons
     a.window = window;
     a.scale_log2 = sm_scale * kLog2e;
     a.rope = make_rope_table(rope->rope_dim, rope->theta);
-    a.out = static_cast<uint16_t*>(out);
+    a.out = out8 ? nullptr : static_cast<uint16_t*>(out);
+    a.out8 = out8;
+    a.out_scale = out_scale;
     a.lse = lse;
     if (p.nsplit > 1) {
         a.ws_o = static_cast<float*>(workspace);
@@ -1114,6 +1169,17 @@ extern "C" dsa_status_t dsa_sparse_attn_decode(int32_t batch, int32_t heads, con
                                                size_t workspace_bytes, int32_t* dev_status, void* stream) {
     return sparse_attn(batch, heads, q, q_pos, nullptr, kind, topk, k, main, main_bt, swa, swa_bt, window, sm_scale,
                        rope, out, lse, workspace, workspace_bytes, dev_status, stream);
+}
+
+extern "C" dsa_status_t dsa_sparse_attn_q8(int32_t nq, int32_t heads, const void* q, const int32_t* q_pos,
+                                           const int32_t* q_req, int32_t kind, const int32_t* topk, int32_t k,
+                                           const dsa_pool_t* main, const dsa_block_table_t* main_bt,
+                                           const dsa_pool_t* swa, const dsa_block_table_t* swa_bt, int32_t window,
+                                           float sm_scale, const dsa_rope_t* rope, uint8_t* out, float* out_scale,
+                                           float* lse, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                           void* stream) {
+    return sparse_attn(nq, heads, q, q_pos, q_req, kind, topk, k, main, main_bt, swa, swa_bt, window, sm_scale, rope,
+                       nullptr, lse, workspace, workspace_bytes, dev_status, stream, out, out_scale);
 }
 
 extern "C" dsa_status_t dsa_sparse_attn_prefill(int32_t nq, int32_t heads, const void* q, const int32_t* q_pos,

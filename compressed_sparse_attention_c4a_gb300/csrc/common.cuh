@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -87,9 +88,15 @@ inline int sm_count() {
 
 inline bool pool_ok(const dsa_pool_t* p) {
     if (!p || !p->data || p->num_blocks <= 0 || p->rows_per_block <= 0 || p->dim <= 0) return false;
-    if (p->dtype != DSA_BF16 && p->dtype != DSA_FP8_E4M3) return false;
-    if (p->dtype == DSA_FP8_E4M3 && (!p->scale || !aligned(p->scale, 16))) return false;
+    if (p->dtype != DSA_BF16 && p->dtype != DSA_FP8_E4M3 && p->dtype != DSA_FP4_E2M1) return false;
+    if (p->dtype != DSA_BF16 && (!p->scale || !aligned(p->scale, 16))) return false;
+    if (p->dtype == DSA_FP4_E2M1 && (p->dim % 64 || !aligned(p->data, 32))) return false;
     return aligned(p->data, 16);
+}
+
+// Bytes of one pool row.
+inline long long row_bytes_of(const dsa_pool_t* p) {
+    return p->dtype == DSA_BF16 ? 2ll * p->dim : (p->dtype == DSA_FP8_E4M3 ? p->dim : p->dim / 2);
 }
 
 inline bool table_ok(const dsa_block_table_t* t, int batch) {
@@ -200,6 +207,11 @@ __device__ __forceinline__ uint16_t float_to_bf16(float f) {
 // e4m3 encode (round to nearest even, saturate to +-448) and decode via CUDA's conversions.
 __device__ __forceinline__ uint8_t float_to_e4m3(float f) {
     return (uint8_t)__nv_cvt_float_to_fp8(f, __NV_SATFINITE, __NV_E4M3);
+}
+
+// Two values -> one byte of e2m1 codes (x in the low nibble), round to nearest even, saturating (CUDA's conversion).
+__device__ __forceinline__ uint8_t float2_to_e2m1x2(float x, float y) {
+    return (uint8_t)__nv_cvt_float2_to_fp4x2(make_float2(x, y), __NV_E2M1, cudaRoundNearest);
 }
 
 __device__ __forceinline__ float e4m3_to_float(uint8_t c) {

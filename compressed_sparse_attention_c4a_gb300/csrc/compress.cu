@@ -76,7 +76,7 @@ __device__ __forceinline__ void copy_bf16(uint16_t* dst, const uint16_t* src, in
     }
 }
 
-// Store one row (the warp's E values per lane) into a pool row: bf16, or e4m3 + amax/448 scale.
+// Store one row (the warp's E values per lane) into a pool row: bf16, e4m3 + amax/448 scale, or e2m1 + amax/6.
 template <int E>
 __device__ __forceinline__ void store_row(const dsa_pool_t& pool, long long prow, int lane, const float (&v)[E]) {
     if (pool.dtype == DSA_BF16) {
@@ -93,6 +93,24 @@ __device__ __forceinline__ void store_row(const dsa_pool_t& pool, long long prow
         } else {
             *reinterpret_cast<uint32_t*>(dst) = u[0];
         }
+    } else if (pool.dtype == DSA_FP4_E2M1) {  // e2m1 codes, two per byte, scale amax / 6
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < E; ++k) amax = fmaxf(amax, fabsf(v[k]));
+        amax = warp_max(amax);
+        const float scale = amax > 0.f ? amax / 6.f : 1.f;
+        uint8_t* dst = reinterpret_cast<uint8_t*>(pool.data) + prow * (E * 16) + lane * (E / 2);
+        uint8_t c[E / 2];
+#pragma unroll
+        for (int k = 0; k < E / 2; ++k) c[k] = float2_to_e2m1x2(v[2 * k] / scale, v[2 * k + 1] / scale);
+        if constexpr (E == 16) {
+            *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(c);
+        } else if constexpr (E == 4) {
+            *reinterpret_cast<uint16_t*>(dst) = *reinterpret_cast<const uint16_t*>(c);
+        } else {
+            *dst = c[0];
+        }
+        if (lane == 0) pool.scale[prow] = scale;
     } else {
         float amax = 0.f;
 #pragma unroll
@@ -303,6 +321,7 @@ extern "C" dsa_status_t dsa_compress(int32_t kind, int32_t batch, const int32_t*
     if (swa) {
         if (!pool_ok(swa) || !table_ok(swa_bt, batch)) return DSA_ERR_INVALID_ARG;
         if (swa->rows_per_block != kBlockPositions || swa->dim != dim) return DSA_ERR_INVALID_ARG;
+        if (swa->dtype == DSA_FP4_E2M1) return DSA_ERR_UNSUPPORTED;
     }
     if (!aligned(x_new, 16) || !aligned(state_x, 16)) return DSA_ERR_INVALID_ARG;
 

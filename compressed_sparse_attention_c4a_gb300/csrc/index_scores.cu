@@ -58,6 +58,7 @@ struct IdxArgs {
     unsigned long long wait_ns;  // limit of every bounded wait
     int withhold;                // test hook: the producer issues no copy and posts no stage
     unsigned* hist;              // fused top-k: [nq][2048] counts of the top 11 bits of each row's score keys, or NULL
+    int key_e2m1;                // keys are fp4 e2m1 codes (else e4m3)
 };
 
 // Shared-memory matrix descriptor of a K-major operand whose rows are `row_bytes` (64 or 128) long,
@@ -68,9 +69,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, int row_bytes) {
     return (uint64_t)((addr >> 4) & 0x3FFF) | (1ull << 16) | (sbo << 32) | (1ull << 46) | (layout << 61);
 }
 
-// Instruction descriptor: D fp32, A and B e4m3, both K-major, M = 128, N = n.
-__device__ __forceinline__ uint32_t idesc_f8(int n) {
-    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTileEntries >> 4) << 24);
+// Instruction descriptor of kind::f8f6f4: D fp32, A (keys) e4m3 or e2m1 (A type field 0 or 5), B (queries)
+// e4m3, both K-major, M = 128, N = n.  e2m1 keys sit in shared memory one code per byte (the TMA's unpacking
+// format), so the operand layout and descriptors are those of e4m3 keys.
+__device__ __forceinline__ uint32_t idesc_f8(int n, bool a_e2m1) {
+    return (1u << 4) | ((a_e2m1 ? 5u : 0u) << 7) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTileEntries >> 4) << 24);
 }
 
 // c4a entries visible to the query at position m: those whose last raw token 4i + 7 <= m.
@@ -455,7 +458,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
     } else if (warp == 1) {
         // ---- MMA issuer: D[entry][q*heads + h] = <k8_entry, q8_(q,h)>, accumulated over dim; the warp
         // waits, one elected lane issues --------------------------------------------------------------
-        const uint32_t idesc = idesc_f8(a.n_cols);
+        const uint32_t idesc = idesc_f8(a.n_cols, a.key_e2m1 != 0);
         int prev_gb = -1, muse[2] = {0, 0};
         int s = 0, sph = 0, b = 0, bph = 0;  // stage / accumulator index and phase parity
         for (int n = 0;; ++n) {
@@ -665,14 +668,17 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
 DSA_TIMELINE_SETTER(dsa_timeline_index)
 namespace dsa {
 
-static bool make_map(CUtensorMap* map, const void* base, uint64_t rows, int dim, int box_rows) {
+// Tensor map of [rows][dim] 8-bit codes (or, e2m1, packed 4-bit codes unpacked to one per byte in shared
+// memory: 16 codes of 8 bytes into 16 bytes) in boxes of box_rows rows, swizzled as the MMA operand wants.
+static bool make_map(CUtensorMap* map, const void* base, uint64_t rows, int dim, int box_rows, bool e2m1 = false) {
     auto fn = tensor_map_encoder();
     if (!fn) return false;
     cuuint64_t gdim[2] = {(cuuint64_t)dim, (cuuint64_t)rows};
-    cuuint64_t gstride[1] = {(cuuint64_t)dim};
+    cuuint64_t gstride[1] = {(cuuint64_t)(e2m1 ? dim / 2 : dim)};
     cuuint32_t box[2] = {(cuuint32_t)dim, (cuuint32_t)box_rows};
     cuuint32_t estride[2] = {1, 1};
-    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, estride,
+    CUresult res = fn(map, e2m1 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                      const_cast<void*>(base), gdim, gstride, box, estride,
                       CU_TENSOR_MAP_INTERLEAVE_NONE,
                       dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -736,8 +742,8 @@ static dsa_status_t index_scores(int32_t nq, int32_t heads, int32_t dim, const u
     if (q_group < 1 || q_group * heads > 256) return DSA_ERR_INVALID_ARG;
     if (!q8 || !q_scale || !w || !q_pos || !q_req || !scores || !keys || !bt || !bt->table || bt->max_blocks <= 0)
         return DSA_ERR_INVALID_ARG;
-    if (!pool_ok(keys) || keys->dtype != DSA_FP8_E4M3 || keys->dim != dim || keys->rows_per_block != kPage)
-        return DSA_ERR_INVALID_ARG;
+    if (!pool_ok(keys) || keys->dim != dim || keys->rows_per_block != kPage) return DSA_ERR_INVALID_ARG;
+    if (keys->dtype == DSA_BF16 || (keys->dtype == DSA_FP4_E2M1 && dim != 128)) return DSA_ERR_UNSUPPORTED;
     if (!aligned(q8, 16) || !aligned(q_scale, 16) || !aligned(w, 16)) return DSA_ERR_INVALID_ARG;
     if (q_group > 64) return DSA_ERR_INVALID_ARG;
     if ((nq + q_group - 1) / q_group > 4096) return DSA_ERR_UNSUPPORTED;  // per-group tables live in smem
@@ -766,8 +772,10 @@ static dsa_status_t index_scores(int32_t nq, int32_t heads, int32_t dim, const u
     a.wait_ns = wait_ns;
     a.withhold = withhold;
     a.hist = hist;
+    a.key_e2m1 = keys->dtype == DSA_FP4_E2M1;
     CUtensorMap kmap, qmap;
-    if (!make_map(&kmap, keys->data, (uint64_t)keys->num_blocks * kPage, dim, kPage)) return DSA_ERR_CUDA;
+    if (!make_map(&kmap, keys->data, (uint64_t)keys->num_blocks * kPage, dim, kPage, a.key_e2m1 != 0))
+        return DSA_ERR_CUDA;
     if (!make_map(&qmap, q8, (uint64_t)nq * heads, dim, n_cols)) return DSA_ERR_CUDA;
     a.items = (ld + kTileEntries - 1) / kTileEntries;  // tiles per group; items once the launch picks TPI
     a.n_groups = (nq + q_group - 1) / q_group;

@@ -22,7 +22,7 @@ KIND = {"c4a": DSA_C4A, "c128a": DSA_C128A}
 EXPORTS = ["dsa_status_string", "dsa_compress", "dsa_index_scores", "dsa_topk", "dsa_topk_plan", "dsa_attn_workspace_size",
            "dsa_sparse_attn_decode", "dsa_sparse_attn_prefill", "dsa_gather_rows", "dsa_sparse_attn_decode_static",
            "dsa_attn_static_scratch_bytes", "dsa_attn_plan", "dsa_debug_index_scores_stalled", "dsa_index_topk",
-           "dsa_index_topk_workspace_size", "dsa_index_scores_counted", "dsa_topk_counted"]
+           "dsa_index_topk_workspace_size", "dsa_index_scores_counted", "dsa_topk_counted", "dsa_sparse_attn_q8"]
 
 
 class DsaPool(ctypes.Structure):
@@ -73,6 +73,8 @@ for _name, _args in {
     "dsa_sparse_attn_prefill": [_I, _I, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, ctypes.c_float, _P, _P, _P,
                                 _P, ctypes.c_size_t, _P, _P],
     "dsa_gather_rows": [_P, _P, _I, _P, _P, _P, _P, _P, _P],
+    "dsa_sparse_attn_q8": [_I, _I, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, ctypes.c_float, _P, _P, _P, _P, _P,
+                           ctypes.c_size_t, _P, _P],
     "dsa_sparse_attn_decode_static": [_I, _I, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, ctypes.c_float, _P, _P, _P,
                                       _P, _P],
 }.items():
@@ -233,6 +235,19 @@ def dsa_sparse_attn_prefill(q, q_pos, q_req, kind, topk, k, main, main_bt, swa, 
                                         _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(dev_status),
                                         _stream(stream))
     _check("dsa_sparse_attn_prefill", code)
+
+
+def dsa_sparse_attn_q8(q, q_pos, q_req, kind, topk, k, main, main_bt, swa, swa_bt, window, sm_scale, rope_cfg, out,
+                       out_scale, lse=None, workspace=None, dev_status=None, stream=None):
+    """Attention with the output in e4m3 and an amax/448 scale per 128-dim block (see include/dsa.h); q_req None
+    for decode rows."""
+    nq, H, _ = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    code = _lib.dsa_sparse_attn_q8(nq, H, _ptr(q), _ptr(q_pos), _ptr(q_req), KIND.get(kind, kind), _ptr(topk), int(k),
+                                   ctypes.byref(main), ctypes.byref(main_bt), ctypes.byref(swa), ctypes.byref(swa_bt),
+                                   int(window), float(sm_scale), ctypes.byref(rope_cfg), _ptr(out), _ptr(out_scale),
+                                   _ptr(lse), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
+    _check("dsa_sparse_attn_q8", code)
 
 
 def dsa_gather_rows(pool_, bt, req, ids, out, out_scale=None, dev_status=None, stream=None):

@@ -58,14 +58,16 @@ typedef int32_t dsa_status_t;
 /* storage formats of a pool row */
 #define DSA_BF16 0
 #define DSA_FP8_E4M3 1 /* e4m3 bytes + one fp32 scale per row: value = scale * e4m3(code) */
+#define DSA_FP4_E2M1 2 /* e2m1 codes packed two per byte (element 2j in the low nibble) + one fp32 scale per
+                          row: value = scale * e2m1(code); [P2] 第三层 (the fp4 indexer cache); indexer keys only */
 
 /* compressor kinds ([P1] §5.2, [P2] 机制二) */
 #define DSA_C4A 0   /* window 8 raw tokens, stride 4: 64 entries per block */
 #define DSA_C128A 1 /* window 128, stride 128: 2 entries per block */
 
-/* A paged pool.  data: [num_blocks][rows_per_block][dim] elements (bf16 or e4m3 bytes),
- * row-major and contiguous, 16-byte aligned.  scale: [num_blocks][rows_per_block] fp32,
- * required for DSA_FP8_E4M3 and ignored for DSA_BF16. */
+/* A paged pool.  data: [num_blocks][rows_per_block][dim] elements (bf16 or e4m3 bytes; e2m1: dim / 2 bytes
+ * per row), row-major and contiguous, 16-byte aligned (e2m1: 32-byte).  scale: [num_blocks][rows_per_block]
+ * fp32, required for DSA_FP8_E4M3 and DSA_FP4_E2M1, ignored for DSA_BF16. */
 typedef struct dsa_pool {
     void* data;
     float* scale;
@@ -117,7 +119,8 @@ const char* dsa_status_string(dsa_status_t status);
  * x_new      [cu_new[batch]][dim] bf16;  logit_new [cu_new[batch]] fp32
  * state_*    rolling state; num_slots host int = number of slots; state_slot [batch]
  * rms_gamma  [dim] fp32 or NULL (= all ones);  rms_eps > 0
- * out        bf16 or fp8 pool, rows_per_block = 256/s;  swa: rows_per_block = 256, or NULL
+ * out        bf16, e4m3 or e2m1 pool (e2m1: scale = amax/6), rows_per_block = 256/s;  swa: rows_per_block = 256
+ *            (bf16 or e4m3), or NULL
  * Supported: dim in {64, 128, 512} (multiple of 64), rope_dim even and <= dim.
  */
 dsa_status_t dsa_compress(int32_t kind, int32_t batch, const int32_t* cu_new, const int32_t* start_pos,
@@ -137,13 +140,14 @@ dsa_status_t dsa_compress(int32_t kind, int32_t batch, const int32_t* cu_new, co
  * stages in shared memory.
  *
  * nq         queries (host);  heads in {4, 8, 16};  dim in {64, 128}
+ * keys       e4m3 (DSA_FP8_E4M3) or, with dim 128, e2m1 (DSA_FP4_E2M1: the tensor cores take the fp4 codes as
+ *            they are, A = e2m1, B = e4m3) pool, rows_per_block 64, dim = dim; bt: its block table
  * q8         [nq][heads][dim] e4m3 bytes;  q_scale, w: [nq][heads] fp32
  * q_pos      [nq] int32 position m of each query;  q_req [nq] int32 request of each query
  * q_group    host int in 1 .. 256/heads: queries g*q_group .. g*q_group + q_group - 1 must
  *            belong to one request (decode: 1; chunked prefill: up to 256/heads, at most 64); a
  *            group that mixes requests raises DSA_ERR_DEVICE_FAULT; at most 4096 groups
  *            (ceil(nq / q_group)), else DSA_ERR_UNSUPPORTED
- * keys       fp8 pool, rows_per_block 64, dim = dim; bt: its block table
  * scores     [nq][ld] fp32 out: I(m, i) for i < n_vis(m); -inf for n_vis(m) <= i < the end of
  *            the 128-entry tile holding n_vis(m) - 1; the rest of the row is not written
  * ld         host int, >= n_vis of every query, a multiple of 4
@@ -300,6 +304,25 @@ dsa_status_t dsa_sparse_attn_prefill(int32_t nq, int32_t heads, const void* q, c
                                      float sm_scale, const dsa_rope_t* rope, void* out, float* lse,
                                      void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                      void* stream);
+
+/*
+ * dsa_sparse_attn_q8 - the same attention (decode rows when q_req is NULL, else prefill rows as
+ * dsa_sparse_attn_prefill) with the output in e4m3 for an fp8 projection that follows: [P2] 融合点 2 (the
+ * inverse rotation and the fp8 quantisation fused into one pass over the output, no bf16 round trip).
+ * Each 128-dim block of each (row, head) output is scaled by its own amax / 448 (1 for an all-zero block):
+ *     out_scale[row][h][b] = max_{d in block b} |o_hd| / 448,   out[row][h][d] = e4m3(o_hd / out_scale[row][h][b])
+ * where o is the output dsa_sparse_attn_decode would store in bf16 (R_m^-1 already applied), rounded to nearest
+ * even with saturation.
+ * out        [nq][heads][512] e4m3 bytes, 16-byte aligned;  out_scale [nq][heads][4] fp32, 16-byte aligned
+ * Other arguments, results, workspace and errors as dsa_sparse_attn_decode / _prefill (a faulted row: zero codes,
+ * scales 1, lse -inf).
+ */
+dsa_status_t dsa_sparse_attn_q8(int32_t nq, int32_t heads, const void* q, const int32_t* q_pos, const int32_t* q_req,
+                                int32_t kind, const int32_t* topk, int32_t k, const dsa_pool_t* main,
+                                const dsa_block_table_t* main_bt, const dsa_pool_t* swa,
+                                const dsa_block_table_t* swa_bt, int32_t window, float sm_scale,
+                                const dsa_rope_t* rope, uint8_t* out, float* out_scale, float* lse, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
  * dsa_sparse_attn_decode_static - dsa_sparse_attn_decode without a caller workspace, for callers that

@@ -98,20 +98,22 @@ def e4m3_half_spacing(a):
     return np.where(a < 2.0 ** -6, 2.0 ** -10, 2.0 ** (e - 4))
 
 
-def fp8_row_violations(codes, scale, values):
+def fp8_row_violations(codes, scale, values, value_slack=FP8_VALUE_SLACK, scale_rel=FP8_SCALE_REL):
     """Elements of e4m3 rows (codes uint8 [n][d], fp32 scale [n]) that are not a correct rounding of the
-    float64 values [n][d] / scale; and rows whose scale is not amax/448.  Returns (bad_elements, bad_rows)."""
+    float64 values [n][d] / scale (up to a relative slack of the value); and rows whose scale is not amax/448
+    within scale_rel.  Returns (bad_elements, bad_rows)."""
+    FP8_VALUE_SLACK_ = value_slack
     codes = np.asarray(codes, np.uint8)
     scale = np.asarray(scale, np.float64)
     values = np.asarray(values, np.float64)
     want_scale = fp8_row_scale(values)
-    bad_rows = np.nonzero(np.abs(scale - want_scale) > FP8_SCALE_REL * want_scale)[0]
+    bad_rows = np.nonzero(np.abs(scale - want_scale) > scale_rel * want_scale)[0]
     u = values / scale[:, None]
     dec = e4m3_decode(codes)
     a = np.abs(u)
     sat = a >= 448.0
     err = np.abs(dec - u)
-    ok = err <= e4m3_half_spacing(np.minimum(a, 448.0)) + FP8_VALUE_SLACK * a + 1e-12
+    ok = err <= e4m3_half_spacing(np.minimum(a, 448.0)) + FP8_VALUE_SLACK_ * a + 1e-12
     ok = np.where(sat, np.abs(dec) == 448.0, ok) & ((dec == 0) | (np.sign(dec) == np.sign(u)) | (a < 2.0 ** -10))
     return np.argwhere(~ok), bad_rows
 

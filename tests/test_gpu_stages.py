@@ -617,3 +617,61 @@ def test_index_topk_fused_heavy_ties():
     for q in range(cpu["nq"]):
         assert list(gi[q]) == list(OL.topk(got[q], int(nv[q]), 512)), q
     assert int(ws.count_nonzero().item()) == 0
+
+
+# ---- fp8 attention output (inverse RoPE + fp8 quantisation in one pass) ------------------------------------
+Q8_CASES = {
+    "c4a_decode": CASES["c4a_decode"],          # keys split over two clusters: the partials' merge kernel quantises
+    "c4a_decode_48": SHARP["c4a_decode_48"],    # clusters of two CTAs: the owners quantise their tiles
+    "c4a_chunk": CASES["c4a_chunk"],            # one CTA per row: four tiles in turn
+    "c128a_decode": CASES["c128a_decode"],
+}
+
+
+@pytest.mark.parametrize("name", list(Q8_CASES))
+def test_attention_fp8_output(name):
+    """dsa_sparse_attn_q8 against (a) the oracle's float64 output, within the attention tolerance plus half an
+    e4m3 step, and (b) the same kernel's bf16 output: each block's scale is the amax / 448 of those values, each
+    code a correct rounding of value / scale (a code decides an integer from a float: the slack covers only the
+    bf16 rounding of the reference values); lse as the bf16 call's."""
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    from _parity import fp8_row_violations
+    from oracle.codecs import e4m3_decode
+    spec = Q8_CASES[name]
+    cpu = synth.make_case(spec, "cpu")
+    gpu = to_device(cpu)
+    step = LayerStep(gpu)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    nq, H = cpu["nq"], spec.heads
+    codes = torch.full((nq, H, 512), 0x7F, dtype=torch.uint8, device="cuda")
+    scale = torch.full((nq, H, 4), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.empty((nq, H), dtype=torch.float32, device="cuda")
+    tk = step.topk if step.has_index else None
+    c = step.case
+    dsa.dsa_sparse_attn_q8(c["q"], c["q_pos"], c["q_req"] if spec.queries == "all" else None, step.kind, tk,
+                           spec.topk if step.has_index else 0, step.main, step.main_bt, step.swa, step.swa_bt,
+                           spec.window, SM_SCALE, step.rope_main, codes, scale, lse, step.workspace,
+                           dev_status=step.status)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    cg, sg = codes.cpu().numpy(), np64(scale)
+    deq = (e4m3_decode(cg).reshape(nq, H, 4, 128) * sg[..., None]).reshape(nq, H, 512)
+    main = oracle_pool(gpu["main_data"], gpu["main_scale"], cpu["epb"])
+    swa = oracle_pool(gpu["swa_data"], gpu["swa_scale"], 256)
+    want, wl = OL.sparse_attn(np64(cpu["q"]), np64(cpu["q_pos"]), np64(cpu["q_req"]), spec.kind,
+                              np64(step.topk) if step.has_index else None, main, np64(cpu["bt_main"]), swa,
+                              np64(cpu["bt_swa"]), spec.window, SM_SCALE, spec.rope_dim)
+    W = np.stack([want[q] for q in range(nq)])
+    bound = np.abs(W) * 2.0 ** -4 + np.repeat(sg, 128, axis=-1) * 2.0 ** -10 + ATTN_MAX_ABS
+    assert np.all(np.abs(deq - W) <= bound)
+    for q in range(nq):
+        assert rel_l2(deq[q], W[q]) <= 2.0 ** -4 + ATTN_REL_L2, q
+    # the same kernel's bf16 values decide the codes
+    ref = np64(step.out).reshape(-1, 128)
+    bad_el, bad_rows = fp8_row_violations(cg.reshape(-1, 128), sg.reshape(-1), ref, value_slack=2.0 ** -8,
+                                          scale_rel=2.0 ** -8)
+    assert len(bad_rows) == 0, bad_rows[:8]
+    assert len(bad_el) == 0, bad_el[:8]
+    assert np.allclose(np64(lse), np64(step.lse), rtol=0, atol=1e-6)
