@@ -82,11 +82,12 @@ def n_entries(T, kind):
 
 
 def algorithmic_bytes(spec):
-    """Bytes a step must move at minimum: indexer keys (+scale) of every visible entry, the gathered
-    top-k (or all visible) rows and the window rows of every query (bf16: 1024 B, fp8: 516 B)."""
+    """Bytes a step must move at minimum: indexer keys (+scale) of every visible entry (e4m3: d + 4 B, e2m1:
+    d/2 + 4 B), the gathered top-k (or all visible) rows and the window rows of every query (bf16: 1024 B,
+    fp8: 516 B)."""
     row_main = 1024 if spec.main_dtype == "bf16" else 516
     row_swa = 1024 if spec.swa_dtype == "bf16" else 516
-    idx_row = spec.idx_dim + 4
+    idx_row = (spec.idx_dim // 2 if spec.idx_dtype == "fp4" else spec.idx_dim) + 4
     idx = att = 0
     for r in range(spec.batch):
         T = spec.cached[r] + spec.new[r]
@@ -393,7 +394,8 @@ def workload_config(name, spec, world):
     return {"workload": name, "kind": spec.kind, "batch": spec.batch,
             "context": sorted(set(c + n for c, n in zip(spec.cached, spec.new)))[:4],
             "new_tokens_per_request": max(spec.new), "heads": spec.heads, "dim": spec.dim,
-            "indexer": f"{spec.idx_heads}x{spec.idx_dim} e4m3" if spec.idx_heads else None,
+            "indexer": (f"{spec.idx_heads}x{spec.idx_dim} " + ("e2m1" if spec.idx_dtype == "fp4" else "e4m3"))
+                       if spec.idx_heads else None,
             "topk": spec.topk or None, "window": spec.window, "kv": spec.main_dtype,
             "l2": f"inputs larger than L2: {COPIES} resident cache copies rotate, each step's working set is "
                   f"evicted by the other copies", "parallelism": f"replicas x{world}"}
@@ -474,8 +476,10 @@ def oracle_sample(spec, case, n_requests, rows_per_request=None):
     epb = case["epb"]
     t0 = time.perf_counter()
 
-    def pool(data, scale, rows_per_block):
+    def pool(data, scale, rows_per_block, fmt=None):
         d = data.detach().cpu()
+        if fmt == "fp4":
+            return OL.Pool(rows_per_block, OL.FP4, d.numpy().copy(), np64(scale))
         if d.dtype == torch.bfloat16:
             return OL.Pool(rows_per_block, OL.BF16, d.view(torch.int16).numpy().view(np.uint16).copy())
         return OL.Pool(rows_per_block, OL.FP8, d.numpy().copy(), np64(scale))
@@ -502,7 +506,7 @@ def oracle_sample(spec, case, n_requests, rows_per_request=None):
                 [zs[cu[r]:cu[r + 1]] for r in range(n_requests)], states, spec.rope_dim, main, bt_main, swa, bt_swa)
     topk = None
     if spec.idx_heads:
-        idx = pool(case["idx_data"], case["idx_scale"], 64)
+        idx = pool(case["idx_data"], case["idx_scale"], 64, spec.idx_dtype)
         if spec.index_compress:
             xi, zi = np64(case["xi_new"]), np64(case["zi_new"])
             sxi, szi = np64(case["state_xi"]), np64(case["state_zi"])

@@ -1151,6 +1151,7 @@ extern "C" size_t dsa_attn_workspace_size(int32_t nq, int32_t heads, int32_t max
 
 extern "C" dsa_status_t dsa_attn_plan(int32_t nq, int32_t heads, int32_t max_keys, int32_t dtype, int32_t* plan) {
     if (!plan || nq <= 0 || max_keys <= 0) return DSA_ERR_INVALID_ARG;
+    if (dtype == DSA_FP4_E2M1) return DSA_ERR_UNSUPPORTED;  // e2m1 holds indexer keys only
     if (dtype != DSA_BF16 && dtype != DSA_FP8_E4M3) return DSA_ERR_INVALID_ARG;
     if (heads != 16 && heads != 32 && heads != 64 && heads != 128) return DSA_ERR_UNSUPPORTED;
     const SplitPlan p = plan_for(nq, heads, max_keys, dtype);

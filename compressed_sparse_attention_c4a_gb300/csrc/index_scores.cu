@@ -48,7 +48,7 @@ struct IdxArgs {
     const float* w;
     const int32_t* q_pos;
     const int32_t* q_req;
-    const int32_t* fresh_from;  // [batch] first entry the preceding kernel may still write, or NULL
+    const int32_t* fresh_pos;   // [batch] first raw position the preceding kernel may still compress, or NULL
     const float* key_scale;
     int num_blocks;
     dsa_block_table_t bt;
@@ -80,6 +80,8 @@ __device__ __forceinline__ uint32_t idesc_f8(int n, bool a_e2m1) {
 __device__ __forceinline__ int visible_at(int m) { return m < 7 ? 0 : ((m - 7) >> 2) + 1; }
 
 __device__ __forceinline__ int visible_of(const IdxArgs& a, int q) { return visible_at(a.q_pos[q]); }
+// Entries complete before raw position p, which a compressor that starts at position p cannot write: n_vis(p - 1).
+__device__ __forceinline__ int entries_complete_before(int p) { return p < 1 ? 0 : visible_at(p - 1); }
 
 // Item = `tpi` consecutive 128-entry tiles of one query group (tpi = 1 or 2).  Its request, visibility
 // and the physical blocks of its 64-entry pages, resolved by one producer lane.
@@ -115,9 +117,9 @@ __device__ __forceinline__ ItemInfo item_info(const IdxArgs& a, int valid, int g
     x.max_vis = grp_mv[g];
     if (x.r < 0 || t * TPI * kTileEntries >= x.max_vis) return x;
     x.valid = 1;
-    if (a.fresh_from) {  // the loaded pages end at the page holding the item's last visible entry
+    if (a.fresh_pos) {  // the loaded pages end at the page holding the item's last visible entry
         const int end = (min(x.max_vis, (t + 1) * TPI * kTileEntries) + kPage - 1) / kPage * kPage;
-        x.fresh = end > __ldg(a.fresh_from + x.r) ? 1 : 0;
+        x.fresh = end > entries_complete_before(__ldg(a.fresh_pos + x.r)) ? 1 : 0;
     }
     // no branch on the loaded table entries: the loads stay in flight until the item is used
 #pragma unroll
@@ -261,10 +263,10 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
     if (tid == 0) DSA_STAMP(1);
     // Programmatic dependent launch: the producer resolves its first items (query positions and requests,
     // the block table: inputs no preceding kernel of the layer writes) while the preceding kernel (the
-    // compressor, which writes keys) finishes.  Without fresh_from, key copies and every global write come
-    // after the wait; with it, pages wholly below fresh_from[r] are copied and scored before it and the
-    // producer waits before its first fresh page (and before the CTA ends in any case).
-    const bool early = a.fresh_from != nullptr;
+    // compressor, which writes keys) finishes.  Without fresh_pos, key copies and every global write come
+    // after the wait; with it, pages wholly below entry n_vis(fresh_pos[r] - 1) are copied and scored before
+    // it and the producer waits before its first fresh page (and before the CTA ends in any case).
+    const bool early = a.fresh_pos != nullptr;
     if (warp != 0) {
         if (!early) {
             pdl_wait();
@@ -407,11 +409,14 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                     StageMeta* meta = stage_meta(s);
                     meta->terminal = 0;
                     meta->gb = gb;
+                    // a page's copy completes its global bytes on the barrier: 64 rows of DIM e4m3 codes, or of
+                    // DIM / 2 bytes of packed e2m1 codes (which land unpacked, one code per byte, in shared memory)
+                    const uint32_t page_bytes = a.key_e2m1 ? kPage * DIM / 2 : kPage * DIM;
                     uint32_t bytes = 0;
 #pragma unroll
                     for (int p = 0; p < 4; ++p) {
                         meta->blk[p] = p < kPages ? it.blk[p] : -1;
-                        if (p < kPages && it.blk[p] >= 0) bytes += kPage * DIM;
+                        if (p < kPages && it.blk[p] >= 0) bytes += page_bytes;
                     }
                     meta->nq = nqg;
                     meta->q0 = q0;
@@ -733,7 +738,7 @@ using namespace dsa;
 static dsa_status_t index_scores(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8, const float* q_scale,
                                  const float* w, const int32_t* q_pos, const int32_t* q_req, int32_t q_group,
                                  const dsa_pool_t* keys, const dsa_block_table_t* bt, float* scores, int32_t ld,
-                                 int32_t* n_visible, const int32_t* fresh_from, int32_t* dev_status, void* stream,
+                                 int32_t* n_visible, const int32_t* fresh_pos, int32_t* dev_status, void* stream,
                                  uint64_t wait_ns, int withhold, unsigned* hist = nullptr) {
     if (nq < 0 || ld < 0 || (ld & 3)) return DSA_ERR_INVALID_ARG;
     if (nq == 0) return DSA_OK;
@@ -762,7 +767,7 @@ static dsa_status_t index_scores(int32_t nq, int32_t heads, int32_t dim, const u
     a.w = w;
     a.q_pos = q_pos;
     a.q_req = q_req;
-    a.fresh_from = fresh_from;
+    a.fresh_pos = fresh_pos;
     a.key_scale = keys->scale;
     a.num_blocks = keys->num_blocks;
     a.bt = *bt;
@@ -787,9 +792,9 @@ extern "C" dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim,
                                          const float* q_scale, const float* w, const int32_t* q_pos,
                                          const int32_t* q_req, int32_t q_group, const dsa_pool_t* keys,
                                          const dsa_block_table_t* bt, float* scores, int32_t ld, int32_t* n_visible,
-                                         const int32_t* fresh_from, int32_t* dev_status, void* stream) {
+                                         const int32_t* fresh_pos, int32_t* dev_status, void* stream) {
     return index_scores(nq, heads, dim, q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, ld, n_visible,
-                        fresh_from, dev_status, stream, kWaitLimitNs, 0);
+                        fresh_pos, dev_status, stream, kWaitLimitNs, 0);
 }
 
 // Test hook of the bounded waits: the same launch with a caller-chosen wait limit and the copy-issuing warp
@@ -817,31 +822,31 @@ extern "C" dsa_status_t dsa_index_scores_counted(int32_t nq, int32_t heads, int3
                                                  const float* q_scale, const float* w, const int32_t* q_pos,
                                                  const int32_t* q_req, int32_t q_group, const dsa_pool_t* keys,
                                                  const dsa_block_table_t* bt, float* scores, int32_t ld,
-                                                 int32_t* n_visible, const int32_t* fresh_from, unsigned* counts,
+                                                 int32_t* n_visible, const int32_t* fresh_pos, unsigned* counts,
                                                  int32_t* dev_status, void* stream) {
     if (nq < 0) return DSA_ERR_INVALID_ARG;
     if (nq == 0) return DSA_OK;
     if (!counts || !aligned(counts, 16) || ld > 16384) return DSA_ERR_INVALID_ARG;
     return index_scores(nq, heads, dim, q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, ld, n_visible,
-                        fresh_from, dev_status, stream, kWaitLimitNs, 0, counts);
+                        fresh_pos, dev_status, stream, kWaitLimitNs, 0, counts);
 }
 
 extern "C" dsa_status_t dsa_index_topk(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8, const float* q_scale,
                                        const float* w, const int32_t* q_pos, const int32_t* q_req, int32_t q_group,
                                        const dsa_pool_t* keys, const dsa_block_table_t* bt, float* scores, int32_t ld,
-                                       int32_t* n_visible, const int32_t* fresh_from, int32_t k, int32_t* idx_out,
+                                       int32_t* n_visible, const int32_t* fresh_pos, int32_t k, int32_t* idx_out,
                                        void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
     if (nq < 0) return DSA_ERR_INVALID_ARG;
     if (nq == 0) return DSA_OK;
     if (k < 1 || k > 2048 || !idx_out || !n_visible || !aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
     if (ld > 16384) {  // rows the counted top-k does not hold: the plain indexer and top-k
         const dsa_status_t r = dsa_index_scores(nq, heads, dim, q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores,
-                                                ld, n_visible, fresh_from, dev_status, stream);
+                                                ld, n_visible, fresh_pos, dev_status, stream);
         return r != DSA_OK ? r : dsa_topk(nq, scores, ld, n_visible, k, idx_out, dev_status, stream);
     }
     if (!workspace || workspace_bytes < dsa_index_topk_workspace_size(nq)) return DSA_ERR_INVALID_ARG;
     unsigned* counts = static_cast<unsigned*>(workspace);
     const dsa_status_t r = dsa_index_scores_counted(nq, heads, dim, q8, q_scale, w, q_pos, q_req, q_group, keys, bt,
-                                                    scores, ld, n_visible, fresh_from, counts, dev_status, stream);
+                                                    scores, ld, n_visible, fresh_pos, counts, dev_status, stream);
     return r != DSA_OK ? r : dsa_topk_counted(nq, scores, ld, n_visible, k, idx_out, counts, dev_status, stream);
 }

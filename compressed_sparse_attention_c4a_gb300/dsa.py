@@ -15,7 +15,7 @@ if not os.path.exists(_PATH):
 _lib = ctypes.CDLL(_PATH)
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_DEVICE_FAULT, DSA_ERR_TIMEOUT = range(6)
-DSA_BF16, DSA_FP8_E4M3 = 0, 1
+DSA_BF16, DSA_FP8_E4M3, DSA_FP4_E2M1 = 0, 1, 2
 DSA_C4A, DSA_C128A = 0, 1
 KIND = {"c4a": DSA_C4A, "c128a": DSA_C128A}
 
@@ -101,12 +101,17 @@ def dsa_status_string(code):
     return _lib.dsa_status_string(code).decode()
 
 
-def pool(data, rows_per_block, scale=None):
-    """A DsaPool over a tensor viewed as [num_blocks * rows_per_block, dim] (bf16 or uint8 e4m3)."""
-    dim = data.shape[-1]
-    rows = data.numel() // dim
+def pool(data, rows_per_block, scale=None, fmt=None):
+    """A DsaPool over a tensor viewed as [num_blocks * rows_per_block, row] (bf16, uint8 e4m3, or with
+    fmt="fp4" uint8 bytes of two e2m1 codes each, so that dim = 2 * row)."""
+    rows = data.numel() // data.shape[-1]
     assert rows % rows_per_block == 0
-    dtype = DSA_BF16 if data.dtype == torch.bfloat16 else DSA_FP8_E4M3
+    if fmt == "fp4":
+        assert data.dtype == torch.uint8
+        dtype, dim = DSA_FP4_E2M1, 2 * data.shape[-1]
+    else:
+        dtype = DSA_BF16 if data.dtype == torch.bfloat16 else DSA_FP8_E4M3
+        dim = data.shape[-1]
     return DsaPool(data.data_ptr(), None if scale is None else scale.data_ptr(), rows // rows_per_block,
                    rows_per_block, dim, dtype)
 
@@ -133,11 +138,11 @@ def dsa_compress(kind, cu_new, start_pos, max_new, x_new, logit_new, state_x, st
 
 
 def dsa_index_scores(q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, n_visible=None, dev_status=None,
-                     stream=None, fresh_from=None):
+                     stream=None, fresh_pos=None):
     nq, heads, dim = q8.shape
     code = _lib.dsa_index_scores(nq, heads, dim, _ptr(q8), _ptr(q_scale), _ptr(w), _ptr(q_pos), _ptr(q_req),
                                  int(q_group), ctypes.byref(keys), ctypes.byref(bt), _ptr(scores), scores.shape[1],
-                                 _ptr(n_visible), _ptr(fresh_from), _ptr(dev_status), _stream(stream))
+                                 _ptr(n_visible), _ptr(fresh_pos), _ptr(dev_status), _stream(stream))
     _check("dsa_index_scores", code)
 
 
@@ -158,24 +163,24 @@ def dsa_index_topk_workspace_size(nq):
 
 
 def dsa_index_topk(q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, k, idx_out, workspace, n_visible=None,
-                   dev_status=None, stream=None, fresh_from=None):
+                   dev_status=None, stream=None, fresh_pos=None):
     """Indexer scores with the per-query top-k fused in (see include/dsa.h); ``workspace`` a zero-filled
     device buffer of at least dsa_index_topk_workspace_size(nq) bytes."""
     nq, heads, dim = q8.shape
     code = _lib.dsa_index_topk(nq, heads, dim, _ptr(q8), _ptr(q_scale), _ptr(w), _ptr(q_pos), _ptr(q_req),
                                int(q_group), ctypes.byref(keys), ctypes.byref(bt), _ptr(scores), scores.shape[1],
-                               _ptr(n_visible), _ptr(fresh_from), int(k), _ptr(idx_out), _ptr(workspace),
+                               _ptr(n_visible), _ptr(fresh_pos), int(k), _ptr(idx_out), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream))
     _check("dsa_index_topk", code)
 
 
 def dsa_index_scores_counted(q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, counts, n_visible=None,
-                             dev_status=None, stream=None, fresh_from=None):
+                             dev_status=None, stream=None, fresh_pos=None):
     """dsa_index_scores that also counts each row's level-1 top-k histogram into ``counts`` (zero-filled)."""
     nq, heads, dim = q8.shape
     code = _lib.dsa_index_scores_counted(nq, heads, dim, _ptr(q8), _ptr(q_scale), _ptr(w), _ptr(q_pos), _ptr(q_req),
                                          int(q_group), ctypes.byref(keys), ctypes.byref(bt), _ptr(scores),
-                                         scores.shape[1], _ptr(n_visible), _ptr(fresh_from), _ptr(counts),
+                                         scores.shape[1], _ptr(n_visible), _ptr(fresh_pos), _ptr(counts),
                                          _ptr(dev_status), _stream(stream))
     _check("dsa_index_scores_counted", code)
 

@@ -42,7 +42,7 @@ class LayerStep:
         self.fused_topk = False
         nq = case["nq"]
         if self.has_index:
-            self.idx = dsa.pool(case["idx_data"], 64, case["idx_scale"])
+            self.idx = dsa.pool(case["idx_data"], 64, case["idx_scale"], fmt=spec.idx_dtype)
             self.idx_bt = dsa.block_table(case["bt_idx"])
             self.rope_idx = dsa.rope(min(spec.rope_dim, spec.idx_dim), ROPE_THETA)
             self.ld = case["ld"]
@@ -58,14 +58,9 @@ class LayerStep:
             self.topk_ws = None
             if self.fused_topk:
                 self.topk_ws = torch.zeros((dsa.dsa_index_topk_workspace_size(nq) // 4,), dtype=torch.int32, device=dev)
-            # first indexer entry of each request that this step's compressor may write (entry i is complete
-            # at position 4i + 7, so the entries before the first new token are old): older key pages are
-            # scored while the compressor still runs
-            self.fresh_from = None
-            if spec.index_compress:
-                p = case["start_pos"].to(torch.int64) - 1
-                old = torch.where(p >= 7, torch.div(p - 7, 4, rounding_mode="floor") + 1, torch.zeros_like(p))
-                self.fresh_from = old.to(torch.int32).contiguous()
+            # this step's compressor starts each request at start_pos: the indexer scores the key pages of
+            # entries complete before it while the compressor still runs
+            self.fresh_pos = case["start_pos"] if spec.index_compress else None
         self.out = torch.empty((nq, spec.heads, spec.dim), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((nq, spec.heads), dtype=torch.float32, device=dev)
         max_keys = (spec.topk if self.has_index else case["bt_main"].shape[1] * epb) + spec.window
@@ -85,7 +80,7 @@ class LayerStep:
                          self.swa_bt, dev_status=self.status)
 
     def compress_index(self):
-        """Indexer-cache compressor (fp8 keys + scale)."""
+        """Indexer-cache compressor (e4m3 or e2m1 keys + scale)."""
         c = self.case
         if self.has_index and self.spec.index_compress:
             dsa.dsa_compress(self.kind, c["cu_new"], c["start_pos"], self.max_new, c["xi_new"], c["zi_new"],
@@ -102,11 +97,11 @@ class LayerStep:
         if self.fused_topk:
             dsa.dsa_index_scores_counted(c["q8"], c["q_scale"], c["w"], c["q_pos"], c["q_req"], self.q_group,
                                          self.idx, self.idx_bt, self.scores, self.topk_ws, self.n_visible,
-                                         dev_status=self.status, fresh_from=self.fresh_from)
+                                         dev_status=self.status, fresh_pos=self.fresh_pos)
         else:
             dsa.dsa_index_scores(c["q8"], c["q_scale"], c["w"], c["q_pos"], c["q_req"], self.q_group, self.idx,
                                  self.idx_bt, self.scores, self.n_visible, dev_status=self.status,
-                                 fresh_from=self.fresh_from)
+                                 fresh_pos=self.fresh_pos)
 
     def select(self):
         """Top-k of every query row (from the indexer's counts when it made them)."""

@@ -10,7 +10,8 @@ tokens; the queries are either the last new token of each request (decode) or ev
 new token (chunked prefill).  All value draws are N(0, 1) (indexer head weights
 U(0, 1)); bf16 values are torch's round-to-nearest of fp32 draws; fp8 codes are
 torch's e4m3 conversion of 64 * N(0, 1) draws with a per-row scale drawn
-U(0.5, 1.5) / 64.  Physical blocks are a seeded permutation of a pool that is about
+U(0.5, 1.5) / 64; fp4 indexer keys are uniformly random bytes (two e2m1 codes each, every code
+equally likely) with a per-row scale drawn U(0.5, 1.5) / 6.  Physical blocks are a seeded permutation of a pool that is about
 12% larger than what the requests need, so tables are shuffled and fragmented.
 """
 from dataclasses import dataclass, field
@@ -38,6 +39,7 @@ class CaseSpec:
     topk: int = 512
     window: int = 128
     main_dtype: str = "bf16"                            # "bf16" or "fp8"
+    idx_dtype: str = "fp8"                              # indexer keys: "fp8" (e4m3) or "fp4" (e2m1, packed)
     swa_dtype: str = "bf16"
     index_compress: bool = True                         # run the indexer compressor on the new tokens
     seed: int = 0
@@ -66,6 +68,12 @@ def _fp8_codes_and_scale(rows, dim, gen, device):
     codes = x.to(torch.float8_e4m3fn).view(torch.uint8)
     scale = (torch.rand((rows,), generator=gen, device=device) + 0.5) / 64.0
     return codes, scale
+
+
+def _fp4_codes_and_scale(rows, dim, gen, device):
+    packed = torch.randint(0, 256, (rows, dim // 2), generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
+    scale = (torch.rand((rows,), generator=gen, device=device) + 0.5) / 6.0
+    return packed, scale
 
 
 def _tables(blocks_needed, cpu_gen, spare=0.125):
@@ -109,7 +117,8 @@ def make_case(spec: CaseSpec, device="cpu"):
     if spec.idx_heads:
         bt_idx, nb_idx = _tables(main_blocks, cpu)
         out["bt_idx"], out["nb_idx"] = bt_idx.to(dev), nb_idx
-        out["idx_data"], out["idx_scale"] = _fp8_codes_and_scale(nb_idx * epb, spec.idx_dim, gen, dev)
+        draw = _fp4_codes_and_scale if spec.idx_dtype == "fp4" else _fp8_codes_and_scale
+        out["idx_data"], out["idx_scale"] = draw(nb_idx * epb, spec.idx_dim, gen, dev)
 
     # sliding-window pool: only blocks that some query's window or a new token touches
     if spec.queries == "last":
@@ -181,12 +190,14 @@ def log_uniform_lengths(n, lo, hi, seed):
 
 
 def case_specs():
-    """The five workloads at full size, keyed by name."""
+    """The five workloads at full size, keyed by name, plus the decode batch with fp4 (e2m1) indexer keys."""
     mixed = log_uniform_lengths(64, 2048, 262144, seed=1004)
     return {
         "c4a_tiny_decode": CaseSpec("c4a_tiny_decode", cached=[0], new=[4096], heads=16,
                                     idx_heads=4, idx_dim=64, index_compress=False, seed=1001),
         "c4a_decode_batch": CaseSpec("c4a_decode_batch", cached=[65535] * 32, new=[1] * 32, seed=1002),
+        "c4a_decode_batch_fp4": CaseSpec("c4a_decode_batch_fp4", cached=[65535] * 32, new=[1] * 32, idx_dtype="fp4",
+                                         seed=1002),
         "c128a_decode": CaseSpec("c128a_decode", kind="c128a", cached=[1048575] * 16, new=[1] * 16,
                                  idx_heads=0, topk=0, seed=1003),
         "c128a_decode_fp8": CaseSpec("c128a_decode_fp8", kind="c128a", cached=[1048575] * 16,

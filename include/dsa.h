@@ -152,20 +152,21 @@ dsa_status_t dsa_compress(int32_t kind, int32_t batch, const int32_t* cu_new, co
  *            the 128-entry tile holding n_vis(m) - 1; the rest of the row is not written
  * ld         host int, >= n_vis of every query, a multiple of 4
  * n_visible  [nq] int32 out (n_vis per query), or NULL
- * fresh_from [batch] int32: for request r, the first entry that the preceding kernel in the stream may
- *            still be writing (after dsa_compress of this step: the entries its new tokens form, i.e.
- *            n_vis(first new position - 1)); or NULL.
+ * fresh_pos  [batch] int32: for request r, the first raw position whose tokens the preceding kernel in the
+ *            stream may still be compressing into the key pool (after dsa_compress of this step: its
+ *            start_pos[r]); or NULL.  The entries those tokens can complete, i >= n_vis(fresh_pos[r] - 1)
+ *            (c4a: 4i + 7 >= fresh_pos[r]), may still be written; older entries may not.
  * Launched with programmatic dependent launch, so the kernel may start before the preceding kernel in
  * the stream has finished.  q_pos, q_req and bt are always read before waiting for it.  Without
- * fresh_from, keys, queries and every output are touched only after the wait.  With fresh_from, key
- * pages wholly below fresh_from[r], the queries, and the scores / n_visible outputs may be touched before
+ * fresh_pos, keys, queries and every output are touched only after the wait.  With fresh_pos, key pages
+ * wholly below entry n_vis(fresh_pos[r] - 1), the queries, and the scores / n_visible outputs may be touched before
  * it: a preceding kernel that releases its dependents early must not write those inputs or read those
  * outputs after releasing them.  The call ends after the preceding kernel in every case.
  */
 dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8, const float* q_scale,
                               const float* w, const int32_t* q_pos, const int32_t* q_req, int32_t q_group,
                               const dsa_pool_t* keys, const dsa_block_table_t* bt, float* scores, int32_t ld,
-                              int32_t* n_visible, const int32_t* fresh_from, int32_t* dev_status, void* stream);
+                              int32_t* n_visible, const int32_t* fresh_pos, int32_t* dev_status, void* stream);
 
 /*
  * dsa_index_scores_counted / dsa_topk_counted / dsa_index_topk - the indexer and the per-query top-k with the
@@ -190,19 +191,19 @@ size_t dsa_index_topk_workspace_size(int32_t nq);
 dsa_status_t dsa_index_scores_counted(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8, const float* q_scale,
                                       const float* w, const int32_t* q_pos, const int32_t* q_req, int32_t q_group,
                                       const dsa_pool_t* keys, const dsa_block_table_t* bt, float* scores, int32_t ld,
-                                      int32_t* n_visible, const int32_t* fresh_from, unsigned* counts,
+                                      int32_t* n_visible, const int32_t* fresh_pos, unsigned* counts,
                                       int32_t* dev_status, void* stream);
 dsa_status_t dsa_topk_counted(int32_t nq, const float* scores, int32_t ld, const int32_t* n_valid, int32_t k,
                               int32_t* idx_out, unsigned* counts, int32_t* dev_status, void* stream);
 dsa_status_t dsa_index_topk(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8, const float* q_scale,
                             const float* w, const int32_t* q_pos, const int32_t* q_req, int32_t q_group,
                             const dsa_pool_t* keys, const dsa_block_table_t* bt, float* scores, int32_t ld,
-                            int32_t* n_visible, const int32_t* fresh_from, int32_t k, int32_t* idx_out,
+                            int32_t* n_visible, const int32_t* fresh_pos, int32_t k, int32_t* idx_out,
                             void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
  * dsa_debug_index_scores_stalled - test hook of the bounded waits in dsa_index_scores; the pages have no
- * counterpart.  Launches the indexer as dsa_index_scores would (fresh_from = NULL), except that the warp that
+ * counterpart.  Launches the indexer as dsa_index_scores would (fresh_pos = NULL), except that the warp that
  * issues the key and query copies issues none and posts no work, so the tensor-core and epilogue warps wait
  * for tiles that never arrive.  Each of their waits gives up after wait_limit_ns nanoseconds (of
  * %globaltimer): the kernel records DSA_ERR_TIMEOUT in dev_status, every warp leaves its loop, the tensor

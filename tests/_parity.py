@@ -10,13 +10,15 @@ Tolerances (fixed in the tests that use them):
   * e4m3 rows (fp8 pools): an e4m3 code decides an integer from a float, so each code is checked as a
     correct round-to-nearest of the oracle's float64 value divided by the row scale (up to a relative
     slack of 1e-4 of that value: the GPU's fp32 value may sit on the other side of a rounding midpoint),
-    and the row scale as amax/448 within 1e-5 relative.
+    and the row scale as amax/448 within 1e-5 relative;
+  * e2m1 rows (fp4 indexer pools): the same, on the e2m1 grid, with the row scale amax/6.
 """
 import numpy as np
 import torch
 
 from oracle import layer as OL, compress as OC
-from oracle.codecs import fp8_dequantize_rows, fp8_row_scale, e4m3_decode
+from oracle.codecs import (fp8_dequantize_rows, fp8_row_scale, e4m3_decode, fp4_dequantize_rows, fp4_row_scale,
+                           fp4_unpack, e2m1_decode)
 
 ATTN_MAX_ABS = 2e-2
 ATTN_REL_L2 = 1e-2
@@ -42,11 +44,18 @@ def to_device(case, device="cuda"):
     return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in case.items()}
 
 
-def oracle_pool(data, scale, epb):
-    """An oracle Pool over (copies of) a case's pool tensors."""
+def oracle_pool(data, scale, epb, fmt=None):
+    """An oracle Pool over (copies of) a case's pool tensors (fmt "fp4": packed e2m1 bytes)."""
+    if fmt == "fp4":
+        return OL.Pool(epb, OL.FP4, data.detach().cpu().numpy().copy(), np64(scale).copy())
     if data.dtype == torch.bfloat16:
         return OL.Pool(epb, OL.BF16, data.detach().cpu().view(torch.int16).numpy().view(np.uint16).copy())
     return OL.Pool(epb, OL.FP8, data.detach().cpu().numpy().copy(), np64(scale).copy())
+
+
+def idx_pool(case):
+    """The oracle Pool over a case's indexer key pool."""
+    return oracle_pool(case["idx_data"], case["idx_scale"], 64, case["spec"].idx_dtype)
 
 
 def rolling_states(case, which="main"):
@@ -65,11 +74,13 @@ def new_tokens(case, which="main"):
     return [x[cu[r]:cu[r + 1]] for r in range(len(cu) - 1)], [z[cu[r]:cu[r + 1]] for r in range(len(cu) - 1)]
 
 
-def pool_rows(data, scale, rows):
+def pool_rows(data, scale, rows, fmt=None):
     """Decoded float64 rows of a (device) pool at physical row ids."""
     d = data.detach().cpu()
     if d.dtype == torch.bfloat16:
         return np64(d[rows])
+    if fmt == "fp4":
+        return fp4_dequantize_rows(d[rows].numpy(), np64(scale.detach().cpu()[rows]))
     return fp8_dequantize_rows(d[rows].numpy(), np64(scale.detach().cpu()[rows]))
 
 
@@ -118,6 +129,34 @@ def fp8_row_violations(codes, scale, values, value_slack=FP8_VALUE_SLACK, scale_
     return np.argwhere(~ok), bad_rows
 
 
+FP4_VALUE_SLACK = 1e-4
+FP4_SCALE_REL = 1e-5
+
+
+def e2m1_half_spacing(a):
+    """Half the e2m1 grid spacing of the cell holding magnitude a: 0.25 below 2, 0.5 in [2, 4), 1 from 4."""
+    a = np.asarray(a, np.float64)
+    return np.where(a < 2.0, 0.25, np.where(a < 4.0, 0.5, 1.0))
+
+
+def fp4_row_violations(packed, scale, values, value_slack=FP4_VALUE_SLACK, scale_rel=FP4_SCALE_REL):
+    """Elements of packed e2m1 rows (uint8 [n][d / 2], fp32 scale [n]) that are not a correct rounding of
+    the float64 values [n][d] / scale (up to a relative slack of the value); and rows whose scale is not
+    amax/6 within scale_rel.  Returns (bad_elements, bad_rows), element indices in unpacked order."""
+    codes = fp4_unpack(np.asarray(packed, np.uint8))
+    scale = np.asarray(scale, np.float64)
+    values = np.asarray(values, np.float64)
+    want_scale = fp4_row_scale(values)
+    bad_rows = np.nonzero(np.abs(scale - want_scale) > scale_rel * want_scale)[0]
+    u = values / scale[:, None]
+    dec = e2m1_decode(codes)
+    a = np.abs(u)
+    err = np.abs(dec - u)
+    ok = err <= e2m1_half_spacing(np.minimum(a, 6.0)) + value_slack * a + 1e-12
+    ok = np.where(a >= 6.0, np.abs(dec) == 6.0, ok) & ((dec == 0) | (np.sign(dec) == np.sign(u)))
+    return np.argwhere(~ok), bad_rows
+
+
 def check_rows(got, want, tol=ROW_REL_L2, what="row"):
     """Per-row rel-L2 of float64 rows [n][d]; returns the worst (rel-L2, max abs)."""
     got, want = np.asarray(got, np.float64), np.asarray(want, np.float64)
@@ -131,14 +170,20 @@ def check_rows(got, want, tol=ROW_REL_L2, what="row"):
     return worst, mabs
 
 
-def check_pool_rows(gdata, gscale, prows, values, stored):
+def check_pool_rows(gdata, gscale, prows, values, stored, fmt=None):
     """GPU pool rows (physical ids) against the oracle: bf16 rows per-row rel-L2 against the oracle's stored
-    (rounded) rows; e4m3 rows code by code against the oracle's float64 values before rounding."""
+    (rounded) rows; e4m3 and e2m1 rows code by code against the oracle's float64 values before rounding."""
     if gdata.dtype == torch.bfloat16:
         return check_rows(pool_rows(gdata, gscale, prows), stored)
     d = gdata.detach().cpu()
     codes = d[prows].numpy()
     scale = np64(gscale.detach().cpu()[prows])
+    if fmt == "fp4":
+        bad_el, bad_rows = fp4_row_violations(codes, scale, values)
+        assert len(bad_rows) == 0, ("e2m1 row scale", bad_rows[:8])
+        assert len(bad_el) == 0, ("e2m1 code", bad_el[:8])
+        # each element is already bounded by half its grid cell; the row error is reported, not re-bounded
+        return check_rows(fp4_dequantize_rows(codes, scale), np.asarray(values), tol=np.inf, what="e2m1 row")
     bad_el, bad_rows = fp8_row_violations(codes, scale, values)
     assert len(bad_rows) == 0, ("e4m3 row scale", bad_rows[:8])
     assert len(bad_el) == 0, ("e4m3 code", bad_el[:8])

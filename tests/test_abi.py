@@ -127,3 +127,25 @@ def test_static_attention_scratch_covers_every_plan_host_only(lib):
                                                   ctypes.byref(bt), 128, 0.0441941738, ctypes.byref(rope),
                                                   ctypes.c_void_p(16), None, None, None)
     assert code in (dsa.DSA_ERR_CUDA, dsa.DSA_ERR_INVALID_ARG)
+
+
+def test_fp4_pool_checks_host_only(lib):
+    """e2m1 pools: indexer keys at dim 128 only, a 32-byte aligned base, and no e2m1 window or attention pools."""
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    P = ctypes.c_void_p
+    bt = dsa.DsaBlockTable(64, 1, 4)
+    scale = 256
+    fn = lib.dsa_index_scores
+    fn.argtypes = [ctypes.c_int32] * 3 + [P] * 5 + [ctypes.c_int32, P, P, P, ctypes.c_int32, P, P, P, P]
+
+    def index(dim, base, dtype=dsa.DSA_FP4_E2M1):
+        keys = dsa.DsaPool(base, scale, 4, 64, dim, dtype)
+        return fn(1, 8, dim, *[P(16)] * 5, 1, ctypes.cast(ctypes.pointer(keys), P), ctypes.cast(ctypes.pointer(bt), P),
+                  P(16), 64, None, None, None, None)
+
+    assert index(64, 32) == dsa.DSA_ERR_UNSUPPORTED                  # fp4 keys: dim 128 only
+    assert index(128, 48) == dsa.DSA_ERR_INVALID_ARG                 # 16- but not 32-byte aligned
+    assert index(128, 32, dsa.DSA_BF16) == dsa.DSA_ERR_UNSUPPORTED   # bf16 keys
+    lib.dsa_attn_plan.argtypes = [ctypes.c_int32] * 4 + [P]
+    plan = (ctypes.c_int32 * 4)()
+    assert lib.dsa_attn_plan(4, 64, 640, dsa.DSA_FP4_E2M1, plan) == dsa.DSA_ERR_UNSUPPORTED

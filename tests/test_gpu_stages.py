@@ -11,7 +11,8 @@ import torch
 from compressed_sparse_attention_c4a_gb300 import synth
 from compressed_sparse_attention_c4a_gb300.step import LayerStep, SM_SCALE
 from oracle import layer as OL, attention as OA
-from _parity import (ATTN_MAX_ABS, ATTN_REL_L2, ROW_REL_L2, np64, rel_l2, to_device, oracle_pool, rolling_states,
+from _parity import (ATTN_MAX_ABS, ATTN_REL_L2, ROW_REL_L2, np64, rel_l2, to_device, oracle_pool, idx_pool,
+                     rolling_states,
                      new_tokens, pool_rows, topk_sets_match, check_rows, check_pool_rows)
 
 pytestmark = pytest.mark.gpu
@@ -39,6 +40,10 @@ CASES = {
     # c128a from position 0: no entry before m = 127, the first one at m = 127, the second at m = 255
     "c128a_early": S("c128a_early", kind="c128a", cached=[0], new=[300], queries="all", idx_heads=0, topk=0,
                      seed=21),
+    # fp4 (e2m1) indexer keys ([P2] 第三层): the compressor writes packed codes, the indexer's tensor cores read them
+    "c4a_decode_fp4": S("c4a_decode_fp4", cached=[1000, 2999, 777, 4095, 130], new=[1] * 5, idx_dtype="fp4",
+                        seed=22),
+    "c4a_chunk_fp4": S("c4a_chunk_fp4", cached=[1037, 64], new=[300, 75], queries="all", idx_dtype="fp4", seed=23),
 }
 INDEXED = [n for n, s in CASES.items() if s.idx_heads]
 
@@ -58,7 +63,7 @@ def _oracle_compress(cpu, which, record=None):
         bt, swa_bt = np64(cpu["bt_main"]), np64(cpu["bt_swa"])
         rope_dim = spec.rope_dim
     else:
-        pool = oracle_pool(cpu["idx_data"], cpu["idx_scale"], 64)
+        pool = idx_pool(cpu)
         swa, bt, swa_bt = None, np64(cpu["bt_idx"]), None
         rope_dim = min(spec.rope_dim, spec.idx_dim)
     states = rolling_states(cpu, which)
@@ -112,8 +117,8 @@ def test_compress_main_and_swa(name):
 
 
 @pytest.mark.parametrize("name", [n for n in INDEXED if CASES[n].index_compress])
-def test_compress_indexer_fp8(name):
-    """Indexer entries (e4m3 + amax/448 scale) code by code, row by row."""
+def test_compress_indexer(name):
+    """Indexer entries (e4m3 + amax/448 scale, or e2m1 + amax/6) code by code, row by row."""
     cpu, gpu, step = _setup(name)
     step.compress()
     torch.cuda.synchronize()
@@ -128,14 +133,14 @@ def test_compress_indexer_fp8(name):
             vals.append(rec[("entry", r, i)])
             stored.append(pool.read(bt[r], [i])[0])
     assert prows
-    check_pool_rows(gpu["idx_data"], gpu["idx_scale"], prows, vals, stored)
+    check_pool_rows(gpu["idx_data"], gpu["idx_scale"], prows, vals, stored, fmt=cpu["spec"].idx_dtype)
     gx = np64(gpu["state_xi"])
     for r in range(cpu["spec"].batch):
         assert np.array_equal(gx[int(np64(cpu["state_slot"])[r])], states[r].x)
 
 
 def _oracle_scores_on_gpu_pool(cpu, gpu):
-    pool = oracle_pool(gpu["idx_data"], gpu["idx_scale"], 64)
+    pool = idx_pool(gpu)
     return OL.index_scores(np64(cpu["q8"]), np64(cpu["q_scale"]), np64(cpu["w"]), np64(cpu["q_pos"]),
                            np64(cpu["q_req"]), pool, np64(cpu["bt_idx"]))
 
@@ -168,7 +173,7 @@ def test_index_scores(name):
     _check_score_rows(np64(step.scores), want, nvis, np64(step.n_visible), step.ld)
 
 
-@pytest.mark.parametrize("name", ["c4a_decode", "c4a_chunk", "c4a_multi_prefill"])
+@pytest.mark.parametrize("name", ["c4a_decode", "c4a_chunk", "c4a_multi_prefill", "c4a_chunk_fp4"])
 def test_index_scores_signed_scales(name):
     """Negative query scales in some query groups and negative key scales on some entries: the ReLU
     then keeps the other sign of <q8, k8>, so both the folded-weight path (with its sign branch per
@@ -188,7 +193,7 @@ def test_index_scores_signed_scales(name):
     step.index()
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0
-    pool = oracle_pool(gpu["idx_data"], gpu["idx_scale"], 64)
+    pool = idx_pool(gpu)
     want, nvis = OL.index_scores(np64(cpu["q8"]), np64(qs), np64(cpu["w"]), np64(cpu["q_pos"]),
                                  np64(cpu["q_req"]), pool, np64(cpu["bt_idx"]))
     _check_score_rows(np64(step.scores), want, nvis)
@@ -390,10 +395,11 @@ def test_topk_long_rows_cluster_sizes_exact(nq, ld):
 
 
 @pytest.mark.parametrize("name", ["c4a_decode", "c4a_multi_prefill"])
-def test_index_scores_fresh_from_extremes(name):
-    """fresh_from says which key pages the preceding kernel may still write: all of them (zeros: every
-    copy waits) or none (every visible entry old: nothing waits) must give the scores of the call
-    without it, bit for bit."""
+def test_index_scores_fresh_pos(name):
+    """fresh_pos says from which raw position the preceding kernel may still be compressing keys: the
+    compressor's own start (the entries before it are scored before the wait), position 0 (every copy
+    waits) or past every query (nothing waits) must give the scores of the call without it, bit for bit.
+    The entries complete before position p are n_vis(p - 1) = entries i with 4i + 7 < p."""
     from compressed_sparse_attention_c4a_gb300 import dsa
     cpu, gpu, step = _setup(name)
     step.compress()
@@ -402,10 +408,10 @@ def test_index_scores_fresh_from_extremes(name):
     runs = []
     batch = cpu["spec"].batch
     for fresh in (None, torch.zeros(batch, dtype=torch.int32, device="cuda"),
-                  torch.full((batch,), 1 << 30, dtype=torch.int32, device="cuda")):
+                  torch.full((batch,), 1 << 30, dtype=torch.int32, device="cuda"), c["start_pos"]):
         scores = torch.full_like(step.scores, float("nan"))
         dsa.dsa_index_scores(c["q8"], c["q_scale"], c["w"], c["q_pos"], c["q_req"], step.q_group, step.idx,
-                             step.idx_bt, scores, step.n_visible, dev_status=step.status, fresh_from=fresh)
+                             step.idx_bt, scores, step.n_visible, dev_status=step.status, fresh_pos=fresh)
         torch.cuda.synchronize()
         assert int(step.status.item()) == 0
         runs.append(np64(scores))
@@ -414,6 +420,7 @@ def test_index_scores_fresh_from_extremes(name):
         n = int(nv[q])
         assert np.array_equal(runs[1][q, :n], runs[0][q, :n]), q
         assert np.array_equal(runs[2][q, :n], runs[0][q, :n]), q
+        assert np.array_equal(runs[3][q, :n], runs[0][q, :n]), q
 
 
 # ---- device-detected faults: a needed block unmapped (-1) in one request's table ---------------------
@@ -445,11 +452,12 @@ def test_compress_unmapped_block_faults_only_that_entry():
                     [swa.read(sbt[q], [int(start[q])])[0] for q in range(4)])
 
 
-@pytest.mark.parametrize("counted", [False, True])
-def test_index_unmapped_block_scores_minus_inf(counted):
-    """Plain indexer + top-k, and the indexer that counts the top-k's first digit + the top-k from the counts."""
+@pytest.mark.parametrize("counted,name", [(False, "c4a_decode"), (True, "c4a_decode"), (False, "c4a_decode_fp4")])
+def test_index_unmapped_block_scores_minus_inf(counted, name):
+    """Plain indexer + top-k, and the indexer that counts the top-k's first digit + the top-k from the counts;
+    e4m3 and e2m1 keys."""
     from compressed_sparse_attention_c4a_gb300 import dsa
-    cpu = synth.make_case(CASES["c4a_decode"], "cpu")
+    cpu = synth.make_case(CASES[name], "cpu")
     gpu = to_device(cpu)
     step = LayerStep(gpu, counted_topk=counted)
     assert step.fused_topk == counted
@@ -558,7 +566,7 @@ def _fused_call(step, ws, idx):
     c = step.case
     dsa.dsa_index_topk(c["q8"], c["q_scale"], c["w"], c["q_pos"], c["q_req"], step.q_group, step.idx, step.idx_bt,
                        step.scores, step.spec.topk, idx, ws, step.n_visible, dev_status=step.status,
-                       fresh_from=step.fresh_from)
+                       fresh_pos=step.fresh_pos)
 
 
 @pytest.mark.parametrize("name", list(FUSED))

@@ -13,7 +13,8 @@ import torch
 from compressed_sparse_attention_c4a_gb300 import synth
 from compressed_sparse_attention_c4a_gb300.step import LayerStep, SM_SCALE
 from oracle import layer as OL
-from _parity import (ATTN_MAX_ABS, ATTN_REL_L2, ROW_REL_L2, np64, rel_l2, to_device, oracle_pool, rolling_states,
+from _parity import (ATTN_MAX_ABS, ATTN_REL_L2, ROW_REL_L2, np64, rel_l2, to_device, oracle_pool, idx_pool,
+                     rolling_states,
                      new_tokens, topk_sets_match, check_pool_rows)
 
 pytestmark = pytest.mark.gpu
@@ -39,7 +40,7 @@ def _compare_compress(cpu, gpu, which):
         bt, sbt, rope_dim, rpb = np64(cpu["bt_main"]), np64(cpu["bt_swa"]), spec.rope_dim, epb
         gdata, gscale = gpu["main_data"], gpu["main_scale"]
     else:
-        pool = oracle_pool(cpu["idx_data"], cpu["idx_scale"], 64)
+        pool = idx_pool(cpu)
         swa, sbt, bt, rope_dim, rpb = None, None, np64(cpu["bt_idx"]), min(spec.rope_dim, spec.idx_dim), 64
         gdata, gscale = gpu["idx_data"], gpu["idx_scale"]
     states = rolling_states(cpu, which)
@@ -53,7 +54,7 @@ def _compare_compress(cpu, gpu, which):
             vals.append(rec[("entry", r, i)])
             stored.append(pool.read(bt[r], [i])[0])
     assert prows, "the step emits entries"
-    check_pool_rows(gdata, gscale, prows, vals, stored)
+    check_pool_rows(gdata, gscale, prows, vals, stored, fmt=None if which == "main" else spec.idx_dtype)
     key = "state_x" if which == "main" else "state_xi"
     gx = np64(gpu[key])
     slots = np64(cpu["state_slot"])
@@ -74,7 +75,7 @@ def _compare_compress(cpu, gpu, which):
 
 
 @pytest.mark.parametrize("name", ["c4a_tiny_decode", "c4a_decode_batch", "c128a_decode", "c128a_decode_fp8",
-                                  "c4a_mixed_decode", "c4a_chunked_prefill"])
+                                  "c4a_mixed_decode", "c4a_chunked_prefill", "c4a_decode_batch_fp4"])
 def test_workload_parity(name):
     spec = SPECS[name]
     cpu = synth.make_case(spec, "cpu")
@@ -101,9 +102,9 @@ def test_workload_parity(name):
 
     topk = None
     if spec.idx_heads:
-        idx_pool = oracle_pool(gpu["idx_data"], gpu["idx_scale"], 64)
+        ipool = idx_pool(gpu)
         want, nvis = OL.index_scores(np64(cpu["q8"]), np64(cpu["q_scale"]), np64(cpu["w"]), np64(cpu["q_pos"]),
-                                     np64(cpu["q_req"]), idx_pool, np64(cpu["bt_idx"]), rows=rows)
+                                     np64(cpu["q_req"]), ipool, np64(cpu["bt_idx"]), rows=rows)
         got = np64(step.scores[rows_t])
         gn = np64(step.n_visible)
         gidx = np64(step.topk[rows_t])
