@@ -216,6 +216,7 @@ def ncu_traffic(kernel, workload):
 def run_gpu(args, rank, world, local_rank):
     from compressed_sparse_attention_c4a_gb300 import build as _build
     _build.build()
+    from compressed_sparse_attention_c4a_gb300 import dsa
     from compressed_sparse_attention_c4a_gb300.step import LayerStep
 
     torch.cuda.set_device(local_rank)
@@ -243,6 +244,11 @@ def run_gpu(args, rank, world, local_rank):
         for i in range(max(3, min(args.warmup, 50))):
             copies[i % COPIES].run()
     torch.cuda.synchronize()
+    # a step that reports a device error (an expired bounded wait costs up to 2 s per launch) is not timed
+    warm_status = max(int(c.status.item()) for c in copies)
+    if warm_status:
+        raise SystemExit(f"device status {warm_status} ({dsa.dsa_status_string(warm_status)}) after the warm-up "
+                         f"steps: not timing a failing step")
     per_graph = COPIES * max(1, min(25, args.steps // (COPIES * 20)))  # >= 20 repetitions when steps allow
     g_plain = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_plain, stream=stream):
@@ -262,8 +268,7 @@ def run_gpu(args, rank, world, local_rank):
         with torch.cuda.graph(g_timed, stream=stream):
             for i in range(per_graph):
                 st = copies[i % COPIES]
-                st.compress_main()
-                st.compress_index()
+                st.compress()
                 if st.has_index:
                     ev["index"][i][0].record(stream)
                     st.index()

@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
                     } else {
                         const int epb = a.main.rows_per_block;
                         const int lb = id / epb;
-                        const int pb = lb < a.main_bt.max_blocks
+                        const int pb = lb < a.main_bt.max_blocks && (!bt_cached || DSA_IDX_OK(lb, kBtCache, a.status))
                                            ? (bt_cached ? s_bt[lb] : __ldg(a.main_bt.table + (long long)r * a.main_bt.max_blocks + lb))
                                            : -1;
                         if (pb < 0 || pb >= a.main.num_blocks) {
@@ -386,7 +386,8 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 pool = 2;
                 const int pos = wlo + (j - ncp);
                 const int lb = pos / kBlockPositions;
-                const int pb = s_swb[lb - wlo / kBlockPositions];  // the window (<= 1024 positions) spans <= 5 blocks
+                const int sb = lb - wlo / kBlockPositions;  // the window (<= 1024 positions) spans <= 5 blocks
+                const int pb = DSA_IDX_OK(sb, 8, a.status) ? s_swb[sb] : -1;
                 if (pb < 0 || pb >= a.swa.num_blocks) {
                     report(a.status, DSA_ERR_DEVICE_FAULT);
                     *s_fault = 1;

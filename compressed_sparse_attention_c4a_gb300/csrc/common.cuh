@@ -132,6 +132,15 @@ __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepc
     do {                                                                                          \
         if (g_timeline) g_timeline[(unsigned long long)blockIdx.x * 32 + (k)] = global_ns();      \
     } while (0)
+// DSA_TRACE(n, k): the SM clock of event k of work item n of CTAs 0-7 (items below 64), in records 8192 + .
+#define DSA_TRACE(n, k)                                                                           \
+    do {                                                                                          \
+        if (g_timeline && blockIdx.x < 8 && (n) < 64) {                                           \
+            unsigned long long c_;                                                                \
+            asm volatile("mov.u64 %0, %%clock64;" : "=l"(c_));                                    \
+            g_timeline[(8192ull + blockIdx.x * 64 + (n)) * 32 + (k)] = c_;                        \
+        }                                                                                         \
+    } while (0)
 #define DSA_TIMELINE_SETTER(name)                                                                 \
     extern "C" int name(void* p) {                                                                \
         unsigned long long* q = static_cast<unsigned long long*>(p);                              \
@@ -141,6 +150,7 @@ __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepc
 #define DSA_TIMELINE_BUFFER
 #define DSA_STAMP(k) ((void)0)
 #define DSA_STAMP_NS(k) ((void)0)
+#define DSA_TRACE(n, k) ((void)0)
 #define DSA_TIMELINE_SETTER(name)
 #endif
 
@@ -156,6 +166,20 @@ __device__ __forceinline__ uint32_t dsa_score_key(float f) {
 __device__ __forceinline__ void report(int32_t* status, int32_t code) {
     if (status) atomicCAS(status, 0, code);
 }
+
+// Bounds checks of computed shared-memory and table indexes, compiled into DSA_CHECKED builds only: an index
+// outside [0, n) records DSA_ERR_DEVICE_FAULT in the status word and the guarded access is skipped (never a
+// trap).  In other builds the check is the constant true and costs nothing.
+#ifdef DSA_CHECKED
+__device__ __forceinline__ bool dsa_index_ok(long long i, long long n, int32_t* status) {
+    if (i >= 0 && i < n) return true;
+    report(status, DSA_ERR_DEVICE_FAULT);
+    return false;
+}
+#define DSA_IDX_OK(i, n, status) dsa_index_ok((long long)(i), (long long)(n), (status))
+#else
+#define DSA_IDX_OK(i, n, status) true
+#endif
 
 // Number of entries of a kind (window w, stride s) that T raw tokens form.
 __device__ __forceinline__ int entries_formed(long long T, int w, int s) {

@@ -100,15 +100,16 @@ __device__ __forceinline__ void store_row(const dsa_pool_t& pool, long long prow
         amax = warp_max(amax);
         const float scale = amax > 0.f ? amax / 6.f : 1.f;
         uint8_t* dst = reinterpret_cast<uint8_t*>(pool.data) + prow * (E * 16) + lane * (E / 2);
-        uint8_t c[E / 2];
+        uint32_t c[(E / 2 + 3) / 4] = {};  // the lane's E/2 code bytes, little-endian in words
 #pragma unroll
-        for (int k = 0; k < E / 2; ++k) c[k] = float2_to_e2m1x2(v[2 * k] / scale, v[2 * k + 1] / scale);
+        for (int k = 0; k < E / 2; ++k)
+            c[k / 4] |= (uint32_t)float2_to_e2m1x2(v[2 * k] / scale, v[2 * k + 1] / scale) << (8 * (k % 4));
         if constexpr (E == 16) {
-            *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(c);
+            *reinterpret_cast<uint2*>(dst) = make_uint2(c[0], c[1]);
         } else if constexpr (E == 4) {
-            *reinterpret_cast<uint16_t*>(dst) = *reinterpret_cast<const uint16_t*>(c);
+            *reinterpret_cast<uint16_t*>(dst) = (uint16_t)c[0];
         } else {
-            *dst = c[0];
+            *dst = (uint8_t)c[0];
         }
         if (lane == 0) pool.scale[prow] = scale;
     } else {
@@ -118,15 +119,15 @@ __device__ __forceinline__ void store_row(const dsa_pool_t& pool, long long prow
         amax = warp_max(amax);
         const float scale = amax > 0.f ? amax / 448.f : 1.f;
         uint8_t* dst = reinterpret_cast<uint8_t*>(pool.data) + prow * (E * 32) + lane * E;
-        uint8_t c[E];
+        uint32_t c[(E + 3) / 4] = {};  // the lane's E codes, little-endian in words
 #pragma unroll
-        for (int k = 0; k < E; ++k) c[k] = float_to_e4m3(v[k] / scale);
+        for (int k = 0; k < E; ++k) c[k / 4] |= (uint32_t)float_to_e4m3(v[k] / scale) << (8 * (k % 4));
         if constexpr (E == 16) {
-            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(c);
+            *reinterpret_cast<uint4*>(dst) = make_uint4(c[0], c[1], c[2], c[3]);
         } else if constexpr (E == 4) {
-            *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(c);
+            *reinterpret_cast<uint32_t*>(dst) = c[0];
         } else {
-            *reinterpret_cast<uint16_t*>(dst) = *reinterpret_cast<const uint16_t*>(c);
+            *reinterpret_cast<uint16_t*>(dst) = (uint16_t)c[0];
         }
         if (lane == 0) pool.scale[prow] = scale;
     }
@@ -149,36 +150,51 @@ __device__ __forceinline__ void rope_row(float (&v)[E], int lane, int dim, const
     }
 }
 
+// One warp's item of one job: an entry (item < entry_items) or a new token.  The request's schedule
+// (cu_new, start_pos, state_slot), the destination rows' block-table entries and the norm weights are read
+// before waiting for the preceding kernel in the stream; raw tokens, logits and the rolling state after it.
+// Every thread reaches the wait exactly once.
 template <int DIM, int W>
-__global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
-    pdl_wait();
-    pdl_launch_dependents();
+__device__ __forceinline__ void compress_item(const CompressArgs& a, int item, int r, int lane) {
     constexpr int E = DIM / 32;
-    const int lane = threadIdx.x & 31;
-    const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int r = blockIdx.y;
-    const int cu0 = a.cu_new[r];
-    const int n = a.cu_new[r + 1] - cu0;
-    const long long start = a.start_pos[r];
-    const long long end = start + n;
-    const int slot = a.state_slot[r];
-    if (n < 0 || start < 0 || slot < 0 || slot >= a.num_slots) {
-        if (item == 0 && lane == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
-        return;
-    }
     constexpr int w = W;
     const int s = a.s;
-
-    if (item < a.entry_items) {
+    const int cu0 = __ldg(a.cu_new + r);
+    const int n = __ldg(a.cu_new + r + 1) - cu0;
+    const long long start = __ldg(a.start_pos + r);
+    const long long end = start + n;
+    const int slot = __ldg(a.state_slot + r);
+    const bool bad_req = n < 0 || start < 0 || slot < 0 || slot >= a.num_slots;
+    // this warp's work: entry i (is_entry) or new token j
+    const bool is_entry = item < a.entry_items;
+    long long i = -1, prow = -1;
+    int j = -1;
+    float gam[E];
+    if (!bad_req && is_entry) {
         // entries whose last raw token s*i + w - 1 lies in [start, end)
         const long long lo_num = start - w + 1;
         const long long i_lo = lo_num <= 0 ? 0 : (lo_num + s - 1) / s;
         const long long i_hi = end >= w ? (end - w) / s : -1;
-        const long long i = i_lo + item;
-        if (i > i_hi) return;
+        i = i_lo + item;
+        if (i > i_hi) i = -1;
+        else prow = physical_row(a.out_bt, r, i, a.out.rows_per_block, a.out.num_blocks);
+#pragma unroll
+        for (int k = 0; k < E; ++k) gam[k] = a.gamma ? __ldg(a.gamma + lane * E + k) : 1.f;
+    } else if (!bad_req) {
+        j = item - a.entry_items;
+        if (j >= n || j >= a.token_items) j = -1;
+        else if (a.has_swa) prow = physical_row(a.swa_bt, r, start + j, kBlockPositions, a.swa.num_blocks);
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    if (bad_req) {
+        if (item == 0 && lane == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
+        return;
+    }
+
+    if (is_entry) {
+        if (i < 0) return;
         const long long base = (long long)s * i;
-        // the destination row first: its block-table load is in flight with the logits and rows below
-        const long long prow = physical_row(a.out_bt, r, i, a.out.rows_per_block, a.out.num_blocks);
         auto logit_at = [&](long long p) -> float {
             return p < start ? a.state_logit[(long long)slot * w + (p % w)] : a.logit_new[cu0 + (p - start)];
         };
@@ -188,12 +204,16 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
         };
         // gate g_j = softmax_j(z_{s i + j}): lane l holds the logits of window tokens l, l + 32, ...
         constexpr int LPL = (W + 31) / 32;  // logits per lane
+        constexpr int RB = W < 8 ? W : 8;   // window rows in flight at a time
         float z[LPL];
+        float x[RB][E];
+#pragma unroll
+        for (int u = 0; u < RB; ++u) load_bf16<E>(row_at(base + u), lane, x[u]);  // with the logits
         float mx = -INFINITY;
 #pragma unroll
         for (int u = 0; u < LPL; ++u) {
-            const int j = lane + 32 * u;
-            z[u] = j < W ? logit_at(base + j) : -INFINITY;
+            const int jj = lane + 32 * u;
+            z[u] = jj < W ? logit_at(base + jj) : -INFINITY;
             mx = fmaxf(mx, z[u]);
         }
         mx = warp_max(mx);
@@ -208,17 +228,16 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
         float acc[E];
 #pragma unroll
         for (int k = 0; k < E; ++k) acc[k] = 0.f;
-        // weighted sum, 8 window rows in flight at a time
-        constexpr int RB = W < 8 ? W : 8;
 #pragma unroll 1
         for (int j0 = 0; j0 < W; j0 += RB) {
-            float x[RB][E];
+            if (j0 > 0) {
 #pragma unroll
-            for (int u = 0; u < RB; ++u) load_bf16<E>(row_at(base + j0 + u), lane, x[u]);
+                for (int u = 0; u < RB; ++u) load_bf16<E>(row_at(base + j0 + u), lane, x[u]);
+            }
 #pragma unroll
             for (int u = 0; u < RB; ++u) {
-                const int j = j0 + u;
-                const float g = __shfl_sync(0xffffffffu, z[j / 32 < LPL ? j / 32 : 0], j & 31) * inv_den;
+                const int jj = j0 + u;
+                const float g = __shfl_sync(0xffffffffu, z[jj / 32 < LPL ? jj / 32 : 0], jj & 31) * inv_den;
 #pragma unroll
                 for (int k = 0; k < E; ++k) acc[k] = fmaf(g, x[u][k], acc[k]);
             }
@@ -230,7 +249,7 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
         ss = warp_sum(ss);
         const float rs = rsqrtf(ss / (float)DIM + a.eps);
 #pragma unroll
-        for (int k = 0; k < E; ++k) acc[k] *= rs * (a.gamma ? a.gamma[lane * E + k] : 1.f);
+        for (int k = 0; k < E; ++k) acc[k] *= rs * gam[k];
         // RoPE at the last covered position
         rope_row<E>(acc, lane, DIM, a.rope, base + w - 1);
         if (prow < 0) {
@@ -241,12 +260,10 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
         return;
     }
 
-    const int j = item - a.entry_items;
-    if (j >= n || j >= a.token_items) return;
+    if (j < 0) return;
     const long long p = start + j;
     const uint16_t* xrow = a.x_new + (long long)(cu0 + j) * DIM;
     if (a.has_swa) {
-        const long long prow = physical_row(a.swa_bt, r, p, kBlockPositions, a.swa.num_blocks);  // with the row load
         float v[E];
         load_bf16<E>(xrow, lane, v);
         rope_row<E>(v, lane, DIM, a.rope, p);
@@ -263,15 +280,42 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
     }
 }
 
+constexpr int kMaxJobs = 4;
+
+// The jobs of one launch: the caches of one layer that compress the same tokens of the same requests
+// (main cache with its window insert, indexer cache), each its own rows, norm, RoPE and pool.
+struct CompressJobs {
+    CompressArgs job[kMaxJobs];
+    int n_jobs;
+};
+
+// Grid (warp blocks, 1, job): blockIdx.z picks the job, so the caches of a layer compress side by side in
+// one launch ([P2] 融合点 3: independent per-token work of one layer dispatched by warp index in one kernel).
+// The (request, item) pairs of a job are dealt to consecutive warps, so a decode batch (two items per
+// request) fills few CTAs and leaves the other SMs to the kernel that follows.
+template <int W>
+__global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ CompressJobs js) {
+    const CompressArgs& a = js.job[blockIdx.z];
+    const int lane = threadIdx.x & 31;
+    const int per_req = a.entry_items + a.token_items;
+    const int wi = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int r = wi / per_req, item = wi - r * per_req;
+    if (r >= a.batch) {  // no work; the grid still ends after the preceding kernel
+        pdl_wait();
+        pdl_launch_dependents();
+        return;
+    }
+    switch (a.dim) {
+        case 64: compress_item<64, W>(a, item, r, lane); break;
+        case 128: compress_item<128, W>(a, item, r, lane); break;
+        default: compress_item<512, W>(a, item, r, lane); break;
+    }
+}
+
 // Rolling-state update after a multi-token append: slot p % w <- token p for the last w new tokens.
 template <int DIM>
-__global__ void __launch_bounds__(256) ring_update_kernel(CompressArgs a) {
-    pdl_wait();
-    pdl_launch_dependents();
+__device__ __forceinline__ void ring_update_item(const CompressArgs& a, int item, int r, int lane) {
     constexpr int E = DIM / 32;
-    const int lane = threadIdx.x & 31;
-    const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int r = blockIdx.y;
     const int cu0 = a.cu_new[r];
     const int n = a.cu_new[r + 1] - cu0;
     const int slot = a.state_slot[r];
@@ -284,14 +328,29 @@ __global__ void __launch_bounds__(256) ring_update_kernel(CompressArgs a) {
     if (lane == 0) a.state_logit[ring] = a.logit_new[cu0 + j];
 }
 
-template <int DIM>
-static dsa_status_t launch_compress(const CompressArgs& a, int max_new, cudaStream_t st) {
-    const int items = a.entry_items + a.token_items;
-    dim3 grid((items + 7) / 8, a.batch);
-    cudaError_t e = a.w == 8 ? launch_pdl(compress_kernel<DIM, 8>, grid, dim3(256), 0, st, a)
-                             : launch_pdl(compress_kernel<DIM, 128>, grid, dim3(256), 0, st, a);
-    if (e == cudaSuccess && !a.fuse_ring && max_new > 0)
-        e = launch_pdl(ring_update_kernel<DIM>, dim3((a.w + 7) / 8, a.batch), dim3(256), 0, st, a);
+__global__ void __launch_bounds__(256) ring_update_kernel(const __grid_constant__ CompressJobs js) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const CompressArgs& a = js.job[blockIdx.z];
+    const int lane = threadIdx.x & 31;
+    const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
+    switch (a.dim) {
+        case 64: ring_update_item<64>(a, item, blockIdx.y, lane); break;
+        case 128: ring_update_item<128>(a, item, blockIdx.y, lane); break;
+        default: ring_update_item<512>(a, item, blockIdx.y, lane); break;
+    }
+}
+
+static dsa_status_t launch_compress(const CompressJobs& js, int w, int batch, int max_new, cudaStream_t st) {
+    long long warps = 0;
+    for (int k = 0; k < js.n_jobs; ++k)
+        warps = std::max(warps, (long long)batch * (js.job[k].entry_items + js.job[k].token_items));
+    if ((warps + 7) / 8 > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
+    dim3 grid((unsigned)((warps + 7) / 8), 1, js.n_jobs);
+    cudaError_t e = w == 8 ? launch_pdl(compress_kernel<8>, grid, dim3(256), 0, st, js)
+                           : launch_pdl(compress_kernel<128>, grid, dim3(256), 0, st, js);
+    if (e == cudaSuccess && !js.job[0].fuse_ring && max_new > 0)
+        e = launch_pdl(ring_update_kernel, dim3((w + 7) / 8, batch, js.n_jobs), dim3(256), 0, st, js);
     if (e != cudaSuccess) return DSA_ERR_CUDA;
     return launch_status();
 }
@@ -299,6 +358,76 @@ static dsa_status_t launch_compress(const CompressArgs& a, int max_new, cudaStre
 }  // namespace dsa
 
 using namespace dsa;
+
+// Checks one job's arguments and fills its kernel arguments (the request schedule is set by the caller).
+static dsa_status_t make_job(int batch, int max_new, int w, int s, const void* x_new, const float* logit_new,
+                             void* state_x, float* state_logit, const float* rms_gamma, float rms_eps,
+                             const dsa_rope_t* rope, const dsa_pool_t* out, const dsa_block_table_t* out_bt,
+                             const dsa_pool_t* swa, const dsa_block_table_t* swa_bt, CompressArgs* a) {
+    if (!(rms_eps > 0.f)) return DSA_ERR_INVALID_ARG;
+    if (!x_new || !logit_new || !state_x || !state_logit || !rope) return DSA_ERR_INVALID_ARG;
+    if (!pool_ok(out) || !table_ok(out_bt, batch)) return DSA_ERR_INVALID_ARG;
+    if (out->rows_per_block != kBlockPositions / s) return DSA_ERR_INVALID_ARG;
+    const int dim = out->dim;
+    if (dim != 64 && dim != 128 && dim != 512) return DSA_ERR_UNSUPPORTED;
+    if (rope->rope_dim < 0 || rope->rope_dim > dim || (rope->rope_dim & 1) || !(rope->theta > 0.0))
+        return DSA_ERR_INVALID_ARG;
+    if (rope->rope_dim > 64) return DSA_ERR_UNSUPPORTED;  // the frequency table holds 32 pairs
+    if (swa) {
+        if (!pool_ok(swa) || !table_ok(swa_bt, batch)) return DSA_ERR_INVALID_ARG;
+        if (swa->rows_per_block != kBlockPositions || swa->dim != dim) return DSA_ERR_INVALID_ARG;
+        if (swa->dtype == DSA_FP4_E2M1) return DSA_ERR_UNSUPPORTED;
+    }
+    if (!aligned(x_new, 16) || !aligned(state_x, 16)) return DSA_ERR_INVALID_ARG;
+    a->w = w;
+    a->s = s;
+    a->batch = batch;
+    a->dim = dim;
+    a->x_new = static_cast<const uint16_t*>(x_new);
+    a->logit_new = logit_new;
+    a->state_x = static_cast<uint16_t*>(state_x);
+    a->state_logit = state_logit;
+    a->gamma = rms_gamma;
+    a->eps = rms_eps;
+    a->rope = make_rope_table(rope->rope_dim, rope->theta);
+    a->out = *out;
+    a->out_bt = *out_bt;
+    a->has_swa = swa != nullptr;
+    if (swa) {
+        a->swa = *swa;
+        a->swa_bt = *swa_bt;
+    }
+    a->entry_items = max_new / s + 1;
+    a->token_items = max_new;
+    a->fuse_ring = max_new <= 1;
+    return DSA_OK;
+}
+
+static dsa_status_t compress_jobs(int32_t kind, int32_t batch, const int32_t* cu_new, const int32_t* start_pos,
+                                  int32_t max_new, const int32_t* state_slot, int32_t num_slots, int32_t n_jobs,
+                                  const dsa_compress_job_t* jobs, int32_t* dev_status, void* stream) {
+    if (kind != DSA_C4A && kind != DSA_C128A) return DSA_ERR_INVALID_ARG;
+    if (batch < 0 || max_new < 0 || num_slots <= 0) return DSA_ERR_INVALID_ARG;
+    if (n_jobs < 1 || n_jobs > kMaxJobs || !jobs) return DSA_ERR_INVALID_ARG;
+    if (batch == 0 || max_new == 0) return DSA_OK;
+    if (!cu_new || !start_pos || !state_slot) return DSA_ERR_INVALID_ARG;
+    const int w = window_of(kind), s = stride_of(kind);
+    CompressJobs js{};
+    js.n_jobs = n_jobs;
+    for (int k = 0; k < n_jobs; ++k) {
+        const dsa_compress_job_t& j = jobs[k];
+        const dsa_status_t e = make_job(batch, max_new, w, s, j.x_new, j.logit_new, j.state_x, j.state_logit,
+                                        j.rms_gamma, j.rms_eps, j.rope, j.out, j.out_bt, j.swa, j.swa_bt, &js.job[k]);
+        if (e != DSA_OK) return e;
+        CompressArgs& a = js.job[k];
+        a.cu_new = cu_new;
+        a.start_pos = start_pos;
+        a.state_slot = state_slot;
+        a.num_slots = num_slots;
+        a.status = dev_status;
+    }
+    return launch_compress(js, w, batch, max_new, static_cast<cudaStream_t>(stream));
+}
 
 extern "C" dsa_status_t dsa_compress(int32_t kind, int32_t batch, const int32_t* cu_new, const int32_t* start_pos,
                                      int32_t max_new, const void* x_new, const float* logit_new, void* state_x,
@@ -309,53 +438,15 @@ extern "C" dsa_status_t dsa_compress(int32_t kind, int32_t batch, const int32_t*
     if (kind != DSA_C4A && kind != DSA_C128A) return DSA_ERR_INVALID_ARG;
     if (batch < 0 || max_new < 0 || num_slots <= 0 || !(rms_eps > 0.f)) return DSA_ERR_INVALID_ARG;
     if (batch == 0 || max_new == 0) return DSA_OK;
-    if (!cu_new || !start_pos || !x_new || !logit_new || !state_x || !state_logit || !state_slot || !rope)
-        return DSA_ERR_INVALID_ARG;
-    if (!pool_ok(out) || !table_ok(out_bt, batch)) return DSA_ERR_INVALID_ARG;
-    const int w = window_of(kind), s = stride_of(kind);
-    if (out->rows_per_block != kBlockPositions / s) return DSA_ERR_INVALID_ARG;
-    const int dim = out->dim;
-    if (dim != 64 && dim != 128 && dim != 512) return DSA_ERR_UNSUPPORTED;
-    if (rope->rope_dim < 0 || rope->rope_dim > dim || (rope->rope_dim & 1) || !(rope->theta > 0.0))
-        return DSA_ERR_INVALID_ARG;
-    if (swa) {
-        if (!pool_ok(swa) || !table_ok(swa_bt, batch)) return DSA_ERR_INVALID_ARG;
-        if (swa->rows_per_block != kBlockPositions || swa->dim != dim) return DSA_ERR_INVALID_ARG;
-        if (swa->dtype == DSA_FP4_E2M1) return DSA_ERR_UNSUPPORTED;
-    }
-    if (!aligned(x_new, 16) || !aligned(state_x, 16)) return DSA_ERR_INVALID_ARG;
+    const dsa_compress_job_t job{x_new, logit_new, state_x, state_logit, rms_gamma, rms_eps, rope, out, out_bt, swa,
+                                 swa_bt};
+    return compress_jobs(kind, batch, cu_new, start_pos, max_new, state_slot, num_slots, 1, &job, dev_status, stream);
+}
 
-    CompressArgs a{};
-    a.w = w;
-    a.s = s;
-    a.batch = batch;
-    a.dim = dim;
-    a.cu_new = cu_new;
-    a.start_pos = start_pos;
-    a.x_new = static_cast<const uint16_t*>(x_new);
-    a.logit_new = logit_new;
-    a.state_x = static_cast<uint16_t*>(state_x);
-    a.state_logit = state_logit;
-    a.state_slot = state_slot;
-    a.num_slots = num_slots;
-    a.gamma = rms_gamma;
-    a.eps = rms_eps;
-    a.rope = make_rope_table(rope->rope_dim, rope->theta);
-    a.out = *out;
-    a.out_bt = *out_bt;
-    a.has_swa = swa != nullptr;
-    if (swa) {
-        a.swa = *swa;
-        a.swa_bt = *swa_bt;
-    }
-    a.entry_items = max_new / s + 1;
-    a.token_items = max_new;
-    a.fuse_ring = max_new <= 1;
-    a.status = dev_status;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    switch (dim) {
-        case 64: return launch_compress<64>(a, max_new, st);
-        case 128: return launch_compress<128>(a, max_new, st);
-        default: return launch_compress<512>(a, max_new, st);
-    }
+extern "C" dsa_status_t dsa_compress_jobs(int32_t kind, int32_t batch, const int32_t* cu_new,
+                                          const int32_t* start_pos, int32_t max_new, const int32_t* state_slot,
+                                          int32_t num_slots, int32_t n_jobs, const dsa_compress_job_t* jobs,
+                                          int32_t* dev_status, void* stream) {
+    return compress_jobs(kind, batch, cu_new, start_pos, max_new, state_slot, num_slots, n_jobs, jobs, dev_status,
+                         stream);
 }

@@ -112,7 +112,7 @@ template <int TPI>
 __device__ __forceinline__ ItemInfo item_info(const IdxArgs& a, int valid, int g, int t, const int* grp_r,
                                               const int* grp_mv) {
     ItemInfo x{0, g, t, -1, 0, 0, 1, {-1, -1, -1, -1}};
-    if (!valid) return x;
+    if (!valid || !DSA_IDX_OK(g, a.n_groups, a.status)) return x;
     x.r = grp_r[g];
     x.max_vis = grp_mv[g];
     if (x.r < 0 || t * TPI * kTileEntries >= x.max_vis) return x;
@@ -163,23 +163,32 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
     }
 }
 
-// Per-stage layout (bytes from the stage start): key tiles [TPI][128][DIM] (swizzled), StageMeta, fp32
-// entry scales [TPI * 128] (cp.async, 16 bytes per producer lane and tile, completing on the stage's
-// barrier).  Group buffer: query tile [n_cols][DIM] (swizzled), head weights [n_cols], query scales
-// [n_cols], visible entries of each query of the group [64] (written by the producer lanes before the
-// buffer's barrier is armed).  Only the producer walks the work list; it describes each item in its
-// stage (or posts a terminal stage), so the MMA and epilogue roles never touch global metadata.  The
-// epilogue releases the stage, so everything it reads stays in shared memory until it is done.
+// Shared memory: S stages of key tiles [TPI][128][DIM] (swizzled; TMA, completing on full[s]), released by
+// the tensor cores' completion (tcgen05.commit on empty[s]) as soon as the MMAs that read them are done;
+// item slots (4 for two-tile items, 8 for one-tile items) of StageMeta and fp32 entry scales [TPI * 128]
+// (cp.async, 16 bytes per producer lane and tile, completing on ifull[k]), released by the epilogue
+// (sempty[k]); NA TMEM accumulators (tfull[b] / tempty[b]).  So the epilogue may trail the copies by a few
+// items without holding key tiles.
+// Group buffer: query tile [n_cols][DIM] (swizzled), head weights [n_cols], query scales [n_cols], visible
+// entries of each query of the group [64] (written by the producer lanes before the buffer's barrier is
+// armed).  Only the producer walks the work list; it describes each item in its slot (or posts a terminal
+// item), so the MMA and epilogue roles never touch global metadata.
 struct StageMeta {
     int terminal;  // 1: no more items for this CTA
     int gb;        // group buffer holding the item's query codes, weights and query scales
-    int blk[4];    // physical block of each 64-entry page, -1 if not loaded
+    int blk[4];    // physical block of each 64-entry page, -1 if not loaded (key tiles in stage n mod S)
     int nq;        // queries in the group
     int q0;        // first query of the group
     int e0;        // first entry of the tile
 };
 
 __host__ __device__ constexpr int meta_bytes() { return ((int)sizeof(StageMeta) + 15) / 16 * 16; }
+
+// Bytes of one item slot: StageMeta + the item's fp32 entry scales.
+template <int TPI>
+__host__ __device__ constexpr int item_slot_bytes() { return meta_bytes() + TPI * kTileEntries * 4; }
+template <int TPI>
+__host__ __device__ constexpr int item_slots() { return TPI == 2 ? 4 : 8; }
 
 template <bool B>
 struct BoolTag {
@@ -208,7 +217,7 @@ __host__ __device__ constexpr int gbuf_nvis_offset(int n_cols, int dim) { return
 // by the top 11 bits of its order key (dsa_score_key), the first digit of the top-k's radix select.
 constexpr int kSelBins = 2048;
 
-template <int DIM, int HEADS, int TPI>
+template <int DIM, int HEADS, int TPI, bool N16>
 __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_constant__ CUtensorMap kmap,
                                                             const __grid_constant__ CUtensorMap qmap, IdxArgs a) {
     constexpr int kItem = TPI * kTileEntries;  // entries per item
@@ -219,13 +228,16 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = a.stages, NA = a.n_acc;
-    const int tiles_bytes = kItem * DIM;
     uint8_t* gbase = smem + (size_t)S * a.stage_bytes;  // two group buffers
-    float* s_fold = reinterpret_cast<float*>(gbase + 2 * a.gbuf_bytes);  // [EW][kSlice]: each epilogue warp's w_h * sq_h
+    constexpr int NK = item_slots<TPI>();
+    uint8_t* slots = gbase + 2 * a.gbuf_bytes;          // [NK] item slots: StageMeta + entry scales
+    float* s_fold = reinterpret_cast<float*>(slots + NK * item_slot_bytes<TPI>());  // [EW][kSlice]: w_h * sq_h per epilogue warp
     uint64_t* full = reinterpret_cast<uint64_t*>(s_fold + EW * kSlice);
     uint64_t* empty = full + S;
-    uint64_t* tfull = empty + S;   // [NA]
-    uint64_t* tempty = tfull + 4;  // [NA]
+    uint64_t* ifull = empty + S;    // [NK] item slot written (meta + scales)
+    uint64_t* sempty = ifull + 8;   // [NK] item slot released by the epilogue
+    uint64_t* tfull = sempty + 8;   // [NA]
+    uint64_t* tempty = tfull + 4;   // [NA] accumulator released by the epilogue
     uint64_t* gfull = tempty + 4;  // [2] group buffer loaded
     uint64_t* gempty = gfull + 2;  // [2] group buffer released by the epilogue warps
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(gempty + 2);
@@ -235,14 +247,19 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
     int* grp_mv = grp_r + a.n_groups;                    // [n_groups] visible-entry bound of each group
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    auto stage_meta = [&](int s) { return reinterpret_cast<StageMeta*>(smem + (size_t)s * a.stage_bytes + tiles_bytes); };
+    auto slot_meta = [&](int b) { return reinterpret_cast<StageMeta*>(slots + (size_t)b * item_slot_bytes<TPI>()); };
+    auto slot_scale = [&](int b) { return reinterpret_cast<float*>(slots + (size_t)b * item_slot_bytes<TPI>() + meta_bytes()); };
 
     if (tid == 0) {
         DSA_STAMP_NS(31);
         DSA_STAMP(0);
         for (int i = 0; i < S; ++i) {
-            mbar_init(&full[i], 1 + 32);  // the producer's lane 0 (with the TMA bytes) + 32 scale copies
-            mbar_init(&empty[i], EW * 32);
+            mbar_init(&full[i], 1);   // the producer's lane 0, with the TMA bytes
+            mbar_init(&empty[i], 1);  // the MMAs that read the stage are complete (tcgen05.commit)
+        }
+        for (int k = 0; k < NK; ++k) {
+            mbar_init(&ifull[k], 1 + 32);  // the producer's lane 0 (meta written) + 32 scale copies
+            mbar_init(&sempty[k], EW * 32);
         }
         for (int b = 0; b < NA; ++b) {
             mbar_init(&tfull[b], 1);
@@ -329,6 +346,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
             return item_info<TPI>(a, valid, g, t, grp_r, grp_mv);
         };
         int n = 0, ps = 0, pphase = 0;  // items issued; stage index and its phase parity
+        int pb = 0, pbph = 0;           // item slot index and its phase parity
         int cur_g = -1, gb = 1, guse[2] = {0, 0};  // group in the current buffer, buffer index, loads per buffer
         bool alive = true;
         if (lane == 0) DSA_STAMP(2);
@@ -386,27 +404,29 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                         cur_g = it.g;
                     }
                 }
-                const int s = ps;
+                const int s = ps, b = pb;
                 bool go = false;
-                if (lane == 0 && alive) {
-                    go = wait_or_abort(&empty[s], pphase ^ 1, abort_flag, a.status, a.wait_ns);
+                if (lane == 0 && alive) {  // the stage's previous MMAs done, the slot's previous item scored
+                    go = wait_or_abort(&empty[s], pphase ^ 1, abort_flag, a.status, a.wait_ns) &&
+                         wait_or_abort(&sempty[b], pbph ^ 1, abort_flag, a.status, a.wait_ns);
                     alive = go;
                 }
                 go = __shfl_sync(0xffffffffu, go, 0);
+                if (lane == 0) DSA_TRACE(n, 0);
                 uint8_t* st = smem + (size_t)s * a.stage_bytes;
                 if (go) {  // the entry scales: 16 lanes per page, zero-filled where a page is absent
+                    float* sc = slot_scale(b);
 #pragma unroll
                     for (int i = 0; i < TPI; ++i) {
                         const int pg = 2 * i + (lane >> 4);
                         const int bp = (lane >> 4) ? it.blk[2 * i + 1] : it.blk[2 * i];
                         const float* src = bp >= 0 ? a.key_scale + (long long)bp * kPage + (lane & 15) * 4 : a.key_scale;
-                        cp_async16_nc(smem_u32(st + tiles_bytes + meta_bytes() + (pg * kPage + (lane & 15) * 4) * 4), src,
-                                      bp >= 0 ? 16u : 0u);
+                        cp_async16_nc(smem_u32(sc + pg * kPage + (lane & 15) * 4), src, bp >= 0 ? 16u : 0u);
                     }
-                    cp_async_arrive_noinc(&full[s]);
+                    cp_async_arrive_noinc(&ifull[b]);
                 }
                 if (lane == 0 && go) {
-                    StageMeta* meta = stage_meta(s);
+                    StageMeta* meta = slot_meta(b);
                     meta->terminal = 0;
                     meta->gb = gb;
                     // a page's copy completes its global bytes on the barrier: 64 rows of DIM e4m3 codes, or of
@@ -421,7 +441,8 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                     meta->nq = nqg;
                     meta->q0 = q0;
                     meta->e0 = it.t * kItem;
-                    mbar_arrive_expect_tx(&full[s], bytes);  // release: the meta writes above are visible
+                    mbar_arrive(&ifull[b]);                  // release: the meta writes above are visible
+                    mbar_arrive_expect_tx(&full[s], bytes);
                 }
                 __syncwarp();
                 if (n == 0 && lane == 0) DSA_STAMP(3);
@@ -439,6 +460,10 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                     ps = 0;
                     pphase ^= 1;
                 }
+                if (++pb == NK) {
+                    pb = 0;
+                    pbph ^= 1;
+                }
             }
             cur = nxt;
         }
@@ -447,17 +472,21 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
             pdl_wait();
             pdl_launch_dependents();
         }
-        if (!a.withhold) {  // terminal stage: consumers stop here (33 arrivals, no bytes)
-            const int s = ps;
+        if (!a.withhold) {  // terminal item: consumers stop here (no bytes; 33 slot arrivals, 1 stage arrival)
+            const int s = ps, b = pb;
             bool go = false;
             if (lane == 0 && alive) {
-                go = wait_or_abort(&empty[s], pphase ^ 1, abort_flag, a.status, a.wait_ns);
-                if (go) stage_meta(s)->terminal = 1;
+                go = wait_or_abort(&empty[s], pphase ^ 1, abort_flag, a.status, a.wait_ns) &&
+                     wait_or_abort(&sempty[b], pbph ^ 1, abort_flag, a.status, a.wait_ns);
+                if (go) slot_meta(b)->terminal = 1;
             }
             go = __shfl_sync(0xffffffffu, go, 0);
             if (go) {
-                mbar_arrive(&full[s]);
-                if (lane == 0) mbar_arrive(&full[s]);
+                mbar_arrive(&ifull[b]);
+                if (lane == 0) {
+                    mbar_arrive(&ifull[b]);
+                    mbar_arrive(&full[s]);
+                }
             }
         }
     } else if (warp == 1) {
@@ -466,20 +495,24 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
         const uint32_t idesc = idesc_f8(a.n_cols, a.key_e2m1 != 0);
         int prev_gb = -1, muse[2] = {0, 0};
         int s = 0, sph = 0, b = 0, bph = 0;  // stage / accumulator index and phase parity
+        int k = 0, kph = 0;                  // item slot index and phase parity
         for (int n = 0;; ++n) {
             bool ok = wait_or_abort(&full[s], sph, abort_flag, a.status, a.wait_ns);
+            ok = ok && wait_or_abort(&ifull[k], kph, abort_flag, a.status, a.wait_ns);
             ok = ok && wait_or_abort(&tempty[b], bph ^ 1, abort_flag, a.status, a.wait_ns);
             if (!__all_sync(0xffffffffu, ok)) break;
-            if (stage_meta(s)->terminal) {
+            if (lane == 0) DSA_TRACE(n, 1);
+            if (slot_meta(k)->terminal) {
                 if (lane == 0) mbar_arrive(&tfull[b]);
                 break;
             }
-            const int gbi = stage_meta(s)->gb;
+            const int gbi = slot_meta(k)->gb;
             if (gbi != prev_gb) {  // the first item of a group: its buffer's load
                 prev_gb = gbi;
                 ++muse[gbi];
                 ok = wait_or_abort(&gfull[gbi], (muse[gbi] - 1) & 1, abort_flag, a.status, a.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) break;
+                if (lane == 0) DSA_TRACE(n, 6);
             }
             tc_fence_after();
             const uint32_t a_addr = smem_u32(smem + (size_t)s * a.stage_bytes);
@@ -491,6 +524,8 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                     mma_f8_elect(tmem + (b * TPI + tt) * a.n_cols, smem_desc(a_addr + tt * kTileEntries * DIM + ks * 32, DIM),
                                  smem_desc(b_addr + ks * 32, DIM), idesc, ks > 0 ? 1u : 0u);
             mma_commit_elect(&tfull[b]);
+            mma_commit_elect(&empty[s]);  // the key tiles are free once these MMAs are done
+            if (lane == 0) DSA_TRACE(n, 2);
             if (n == 0 && lane == 0) DSA_STAMP(5);
             if (++s == S) {
                 s = 0;
@@ -499,6 +534,125 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
             if (++b == NA) {
                 b = 0;
                 bph ^= 1;
+            }
+            if (++k == NK) {
+                k = 0;
+                kph ^= 1;
+            }
+        }
+    } else if constexpr (N16) {
+        // ---- epilogue of decode-shaped groups (q_group * heads <= 16: one 16-column chunk): both tiles of an
+        // item come out of TMEM under one wait, the group's folded weights stay in registers, and each entry's
+        // score is a short sum over its query's heads ------------------------------------------------------
+        constexpr int QPC = 16 / HEADS;  // queries per 16-column chunk
+        const int quad = warp & 3;       // TMEM lanes this warp may access (EW == 4)
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        float u[16];  // w_c * sq_c of the group's columns (0 past its queries)
+        int nv[QPC];  // visible entries of each query of the group
+        bool q_neg = false;
+        int nqg = 0, q0 = 0;
+        int prev_gb = -1, euse[2] = {0, 0};
+        int b = 0, bph = 0;  // accumulator index and phase parity
+        int k = 0, kph = 0;  // item slot index and phase parity
+        for (int n = 0;; ++n) {
+            bool ok = wait_or_abort(&ifull[k], kph, abort_flag, a.status, a.wait_ns);  // completed: orders the meta
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const StageMeta* meta = slot_meta(k);
+            if (meta->terminal) break;
+            const int gbi = meta->gb;
+            const bool new_group = gbi != prev_gb;
+            if (new_group) {  // this warp is done with the previous group's buffer
+                if (prev_gb >= 0 && lane == 0) mbar_arrive(&gempty[prev_gb]);
+                prev_gb = gbi;
+                ++euse[gbi];
+                ok = wait_or_abort(&gfull[gbi], (euse[gbi] - 1) & 1, abort_flag, a.status, a.wait_ns);
+            }
+            if (tid == 64) DSA_TRACE(n, 5);
+            ok = ok && wait_or_abort(&tfull[b], bph, abort_flag, a.status, a.wait_ns);
+            if (!__all_sync(0xffffffffu, ok)) break;  // warp-uniform: tcgen05.ld is warp-collective
+            if (tid == 64) DSA_TRACE(n, 3);
+            tc_fence_after();
+            float v0[16], v1[16];
+            tmem_ld_nowait<16>(lane_base + (b * 2) * 16, v0);
+            tmem_ld_nowait<16>(lane_base + (b * 2 + 1) * 16, v1);
+            // while the loads are in flight: the group's weights, the entries' scales and pages
+            if (new_group) {
+                const uint8_t* gp = gbase + (size_t)gbi * a.gbuf_bytes;
+                const float* sw = reinterpret_cast<const float*>(gp + 16 * DIM);
+                const float* ssq = sw + 16;
+                const int* gnv = reinterpret_cast<const int*>(gp + gbuf_nvis_offset(16, DIM));
+                nqg = meta->nq;
+                q0 = meta->q0;
+                bool neg = false;
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const bool live = c < nqg * HEADS;  // columns past the group's queries hold stale values
+                    u[c] = live ? sw[c] * ssq[c] : 0.f;
+                    neg |= live && ssq[c] < 0.f;
+                }
+                q_neg = neg;
+#pragma unroll
+                for (int j = 0; j < QPC; ++j) nv[j] = j < nqg ? gnv[j] : 0;
+                if (tid == 64) DSA_TRACE(n, 7);
+            }
+            const float* sc = slot_scale(k);
+            const int e0 = meta->e0;
+            const bool ok0 = meta->blk[row / kPage] >= 0, ok1 = meta->blk[(kTileEntries + row) / kPage] >= 0;
+            const float sk0 = ok0 ? sc[row] : 0.f, sk1 = ok1 ? sc[kTileEntries + row] : 0.f;
+            const float* gsw = reinterpret_cast<const float*>(gbase + (size_t)gbi * a.gbuf_bytes + 16 * DIM);
+            tmem_wait_ld();
+            tmem_regs_after_wait<16>(v0);
+            tmem_regs_after_wait<16>(v1);
+            auto emit = [&](const float (&x)[16], float sk, bool page_ok, int e) {
+#pragma unroll
+                for (int j = 0; j < QPC; ++j) {
+                    if (j >= nqg) break;
+                    float a0 = 0.f, a1 = 0.f;
+                    if (!q_neg) {  // sk * sum_h u_h * (sk >= 0 ? max(x, 0) : min(x, 0)), two chains
+#pragma unroll
+                        for (int h = 0; h < HEADS; h += 2) {
+                            const float x0 = x[j * HEADS + h], x1 = x[j * HEADS + h + 1];
+                            a0 = fmaf(u[j * HEADS + h], sk >= 0.f ? fmaxf(x0, 0.f) : fminf(x0, 0.f), a0);
+                            a1 = fmaf(u[j * HEADS + h + 1], sk >= 0.f ? fmaxf(x1, 0.f) : fminf(x1, 0.f), a1);
+                        }
+                        a0 = (a0 + a1) * sk;
+                    } else {  // a negative query scale: the literal w_h * max(0, sq_h * sk * x_h)
+                        const float* gsq = gsw + 16;
+#pragma unroll
+                        for (int h = 0; h < HEADS; ++h) {
+                            const int c = j * HEADS + h;
+                            a0 = fmaf(gsw[c], fmaxf(0.f, gsq[c] * sk * x[c]), a0);
+                        }
+                    }
+                    if (e < a.ld) {
+                        const bool vis = e < nv[j];
+                        const float sv = (page_ok && vis) ? a0 : -INFINITY;
+                        a.scores[(long long)(q0 + j) * a.ld + e] = sv;
+                        // fused top-k: each visible entry's score also counted in its row's level-1 histogram
+                        if (a.hist && vis)
+                            atomicAdd(a.hist + (long long)(q0 + j) * kSelBins + (dsa_score_key(sv) >> 21), 1u);
+                    }
+                }
+            };
+            emit(v0, sk0, ok0, e0 + row);
+            if (tid == 64) DSA_TRACE(n, 8);
+            emit(v1, sk1, ok1, e0 + kTileEntries + row);
+            tc_fence_before();
+            if (tid == 64) DSA_TRACE(n, 4);
+            mbar_arrive(&tempty[b]);
+            mbar_arrive(&sempty[k]);
+            if (tid == 64) {
+                if (n == 0) DSA_STAMP(6);
+                DSA_STAMP(7);
+            }
+            if (++b == NA) {
+                b = 0;
+                bph ^= 1;
+            }
+            if (++k == NK) {
+                k = 0;
+                kph ^= 1;
             }
         }
     } else {
@@ -515,11 +669,12 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
         bool q_neg = false;
         int g_vis = 0;  // fewest visible entries over the group's queries
         int prev_gb = -1, euse[2] = {0, 0};
-        int s = 0, sph = 0, b = 0, bph = 0;  // stage / accumulator index and phase parity
+        int b = 0, bph = 0;  // accumulator index and phase parity
+        int k = 0, kph = 0;  // item slot index and phase parity
         for (int n = 0;; ++n) {
-            bool ok = wait_or_abort(&full[s], sph, abort_flag, a.status, a.wait_ns);  // completed: orders the meta
+            bool ok = wait_or_abort(&ifull[k], kph, abort_flag, a.status, a.wait_ns);  // completed: orders the meta
             if (!__all_sync(0xffffffffu, ok)) break;
-            const StageMeta* meta = stage_meta(s);
+            const StageMeta* meta = slot_meta(k);
             if (meta->terminal) break;
 
             const int gbi = meta->gb, nqg = meta->nq, q0 = meta->q0;
@@ -530,8 +685,10 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                 ++euse[gbi];
                 ok = wait_or_abort(&gfull[gbi], (euse[gbi] - 1) & 1, abort_flag, a.status, a.wait_ns);
             }
+            if (tid == 64) DSA_TRACE(n, 5);
             ok = ok && wait_or_abort(&tfull[b], bph, abort_flag, a.status, a.wait_ns);
             if (!__all_sync(0xffffffffu, ok)) break;  // warp-uniform: tcgen05.ld is warp-collective
+            if (tid == 64) DSA_TRACE(n, 3);
             tc_fence_after();
             const uint8_t* gp = gbase + (size_t)gbi * a.gbuf_bytes;
             const float* sw = reinterpret_cast<const float*>(gp + a.n_cols * DIM);
@@ -549,13 +706,13 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                 for (int j = lane; j < nqg; j += 32) vmin = min(vmin, gnv[j]);
                 g_vis = __reduce_min_sync(0xffffffffu, vmin);
                 __syncwarp();
+                if (tid == 64) DSA_TRACE(n, 7);
             }
             // every entry of the item present and visible to every query of the group: unmasked stores
             bool clean = meta->e0 + kItem <= min(g_vis, a.ld);
 #pragma unroll
             for (int p = 0; p < kPages; ++p) clean = clean && meta->blk[p] >= 0;
-            const float* sscale = reinterpret_cast<const float*>(smem + (size_t)s * a.stage_bytes + tiles_bytes +
-                                                                 meta_bytes());
+            const float* sscale = slot_scale(k);
 #pragma unroll
             for (int tt = 0; tt < TPI; ++tt) {
                 const int er = tt * kTileEntries + row;  // entry of the item
@@ -641,21 +798,23 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                     }
                     __syncwarp();  // reconverge before the next collective load
                 }
+                if (tid == 64 && tt == 0) DSA_TRACE(n, 8);
             }
             tc_fence_before();
+            if (tid == 64) DSA_TRACE(n, 4);
             mbar_arrive(&tempty[b]);
-            mbar_arrive(&empty[s]);
+            mbar_arrive(&sempty[k]);
             if (tid == 64) {
                 if (n == 0) DSA_STAMP(6);
                 DSA_STAMP(7);
             }
-            if (++s == S) {
-                s = 0;
-                sph ^= 1;
-            }
             if (++b == NA) {
                 b = 0;
                 bph ^= 1;
+            }
+            if (++k == NK) {
+                k = 0;
+                kph ^= 1;
             }
         }
     }
@@ -690,26 +849,30 @@ static bool make_map(CUtensorMap* map, const void* base, uint64_t rows, int dim,
     return res == CUDA_SUCCESS;
 }
 
-template <int DIM, int HEADS, int TPI>
+template <int DIM, int HEADS, int TPI, bool N16>
 static dsa_status_t launch_index(const CUtensorMap& kmap, const CUtensorMap& qmap, IdxArgs a, cudaStream_t st) {
-    // stage = TPI key tiles + metadata + entry scales; two group buffers of query codes + weights + query
-    // scales + per-query visible entries
-    a.stage_bytes = (TPI * kTileEntries * DIM + meta_bytes() + TPI * kTileEntries * 4 + 1023) / 1024 * 1024;
+    // stage = TPI key tiles; two group buffers of query codes + weights + query scales + per-query visible
+    // entries; the item slots of metadata + entry scales
+    a.stage_bytes = TPI * kTileEntries * DIM;  // a multiple of 1024 (the swizzle atom's alignment)
     a.gbuf_bytes = (gbuf_nvis_offset(a.n_cols, DIM) + 64 * 4 + 1023) / 1024 * 1024;
     a.items = (a.items + TPI - 1) / TPI;  // tiles -> items per group
-    // alignment slack + group buffers + the epilogue warps' folded weights + barriers and flags + the
-    // per-group prefix of valid items, requests and visible-entry bounds
-    const int extra = 1024 + 2 * a.gbuf_bytes + epi_warps<TPI>() * slice_cols<TPI>() * 4 + 256 +
-                      ((3 * a.n_groups + 1) * 4 + 15) / 16 * 16;
-    const int ctas_per_sm = 2 * (extra + 3 * a.stage_bytes) <= 227 * 1024 && 2 * a.tmem_cols <= 512 ? 2 : 1;
-    a.stages = max(2, min(8, (227 * 1024 / ctas_per_sm - extra) / a.stage_bytes));
+    // alignment slack + group buffers + item slots + the epilogue warps' folded weights + barriers and flags
+    // + the per-group prefix of valid items, requests and visible-entry bounds
+    const int extra = 1024 + 2 * a.gbuf_bytes + item_slots<TPI>() * item_slot_bytes<TPI>() +
+                      epi_warps<TPI>() * slice_cols<TPI>() * 4 + 448 + ((3 * a.n_groups + 1) * 4 + 15) / 16 * 16;
+    // an SM holds 228 KB of shared memory, 1 KB of it reserved per resident CTA
+    constexpr int kSmemPerSm = 228 * 1024, kReservedPerCta = 1024;
+    const int two_cta_budget = kSmemPerSm / 2 - kReservedPerCta;
+    const int ctas_per_sm = extra + 3 * a.stage_bytes <= two_cta_budget && 2 * a.tmem_cols <= 512 ? 2 : 1;
+    const int budget = ctas_per_sm == 2 ? two_cta_budget : 227 * 1024;
+    a.stages = max(2, min(8, (budget - extra) / a.stage_bytes));
     const int smem = extra + a.stages * a.stage_bytes;
-    if (cudaFuncSetAttribute(index_kernel<DIM, HEADS, TPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    if (cudaFuncSetAttribute(index_kernel<DIM, HEADS, TPI, N16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
         return DSA_ERR_CUDA;
     a.total_items = (long long)a.items * a.n_groups;
     const long long grid = std::min<long long>(a.total_items, (long long)sm_count() * ctas_per_sm);
-    if (launch_pdl(index_kernel<DIM, HEADS, TPI>, dim3((unsigned)std::max<long long>(grid, 1)), dim3(idx_threads<TPI>()), smem,
+    if (launch_pdl(index_kernel<DIM, HEADS, TPI, N16>, dim3((unsigned)std::max<long long>(grid, 1)), dim3(idx_threads<TPI>()), smem,
                    st, kmap, qmap, a) != cudaSuccess)
         return DSA_ERR_CUDA;
     return launch_status();
@@ -718,7 +881,9 @@ static dsa_status_t launch_index(const CUtensorMap& kmap, const CUtensorMap& qma
 template <int DIM, int HEADS>
 static dsa_status_t launch_index_tpi(const CUtensorMap& kmap, const CUtensorMap& qmap, const IdxArgs& a,
                                      cudaStream_t st) {
-    return a.n_cols <= 128 ? launch_index<DIM, HEADS, 2>(kmap, qmap, a, st) : launch_index<DIM, HEADS, 1>(kmap, qmap, a, st);
+    if (a.n_cols == 16) return launch_index<DIM, HEADS, 2, true>(kmap, qmap, a, st);  // decode-shaped groups
+    return a.n_cols <= 128 ? launch_index<DIM, HEADS, 2, false>(kmap, qmap, a, st)
+                           : launch_index<DIM, HEADS, 1, false>(kmap, qmap, a, st);
 }
 
 template <int DIM>

@@ -280,6 +280,9 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
             const int i = i0 + u * kTopkThreads * 4;
             if (i >= mq) break;
             uint32_t b0 = bin_of(q[u].x), b1 = bin_of(q[u].y), b2 = bin_of(q[u].z), b3 = bin_of(q[u].w);
+            if (!(DSA_IDX_OK(b0, kBins, status) && DSA_IDX_OK(b1, kBins, status) && DSA_IDX_OK(b2, kBins, status) &&
+                  DSA_IDX_OK(b3, kBins, status)))
+                continue;
             if (i + 4 <= mq) {
                 atomicAdd(&hist[b0], 1u);
                 atomicAdd(&hist[b1], 1u);
@@ -342,8 +345,10 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
                 ++cnt_d;
             } else if (rank_mode) {
                 const uint32_t slot = atomicAdd(&n_cand, 1u);  // at most kRankMax over the cluster
-                cand_key[slot] = order_key(s[i]);
-                cand_idx[slot] = (uint32_t)(base + i);
+                if (DSA_IDX_OK(slot, kRankMax, status)) {
+                    cand_key[slot] = order_key(s[i]);
+                    cand_idx[slot] = (uint32_t)(base + i);
+                }
             } else {
                 const uint32_t key = order_key(s[i]);
                 cnt_d += key > T;
@@ -376,8 +381,10 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
             }
             if (better < need) {
                 const uint32_t li = my_i - (uint32_t)base;
-                atomicOr(&marks[li >> 5], 1u << (li & 31));
-                atomicAdd(&wcnt[li / seg][0], 1u);
+                if (DSA_IDX_OK(li >> 5, kMarkWords, status) && DSA_IDX_OK(li / seg, kTopkWarps, status)) {
+                    atomicOr(&marks[li >> 5], 1u << (li & 31));
+                    atomicAdd(&wcnt[li / seg][0], 1u);
+                }
             }
         }
     }
@@ -555,7 +562,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto bin_at = [&](int u) -> uint32_t { return (bins[u / 2] >> (16 * (u & 1))) & 0xFFFFu; };
 #pragma unroll
     for (int u = 0; u < VPT; ++u)
-        if (u < nv) atomicAdd(&hist[bin_at(u)], 1u);
+        if (u < nv && DSA_IDX_OK(bin_at(u), kBins, status)) atomicAdd(&hist[bin_at(u)], 1u);
     __syncthreads();
     if (tid == 0) DSA_STAMP(3);
     uint32_t need = (uint32_t)k;
@@ -588,8 +595,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int u = 0; u < VPT; ++u)  // static indices keep v[] in registers
             if ((inb >> u) & 1u) {
-                cand_key[slot] = order_key(v[u]);
-                cand_idx[slot] = (uint32_t)(i0 + u);
+                if (DSA_IDX_OK(slot, kRankMax, status)) {
+                    cand_key[slot] = order_key(v[u]);
+                    cand_idx[slot] = (uint32_t)(i0 + u);
+                }
                 ++slot;
             }
         __syncthreads();
@@ -601,7 +610,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t kj = cand_key[j];
                 better += (kj > my_k) || (kj == my_k && cand_idx[j] < my_i);
             }
-            if (better < need) atomicOr(&marks[my_i >> 5], 1u << (my_i & 31));
+            if (better < need && DSA_IDX_OK(my_i >> 5, THREADS * VPT / 32, status))
+                atomicOr(&marks[my_i >> 5], 1u << (my_i & 31));
         }
         __syncthreads();
     }
@@ -752,8 +762,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int u = 0; u < VPT; ++u)
             if ((inb >> u) & 1u) {
-                cand_key[slot] = key[u];
-                cand_idx[slot] = (uint32_t)(i0 + u);
+                if (DSA_IDX_OK(slot, kRankMax, status)) {
+                    cand_key[slot] = key[u];
+                    cand_idx[slot] = (uint32_t)(i0 + u);
+                }
                 ++slot;
             }
         __syncthreads();
@@ -765,7 +777,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t kj = cand_key[j];
                 better += (kj > my_k) || (kj == my_k && cand_idx[j] < my_i);
             }
-            if (better < need) atomicOr(&marks[my_i >> 5], 1u << (my_i & 31));
+            if (better < need && DSA_IDX_OK(my_i >> 5, THREADS * VPT / 32, status))
+                atomicOr(&marks[my_i >> 5], 1u << (my_i & 31));
         }
         __syncthreads();
     }

@@ -9,9 +9,12 @@ import os
 
 import torch
 
-_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdsa.so")
+# DSA_CHECKED=1 selects the bounds-checked build of the same kernels (libdsa_checked.so)
+_CHECKED = os.environ.get("DSA_CHECKED") == "1"
+_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdsa_checked.so" if _CHECKED else "libdsa.so")
 if not os.path.exists(_PATH):
-    raise ImportError(f"{_PATH} is not built; run `python -m compressed_sparse_attention_c4a_gb300.build`")
+    raise ImportError(f"{_PATH} is not built; run `python -m compressed_sparse_attention_c4a_gb300.build"
+                      f"{' --checked' if _CHECKED else ''}`")
 _lib = ctypes.CDLL(_PATH)
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_DEVICE_FAULT, DSA_ERR_TIMEOUT = range(6)
@@ -22,7 +25,8 @@ KIND = {"c4a": DSA_C4A, "c128a": DSA_C128A}
 EXPORTS = ["dsa_status_string", "dsa_compress", "dsa_index_scores", "dsa_topk", "dsa_topk_plan", "dsa_attn_workspace_size",
            "dsa_sparse_attn_decode", "dsa_sparse_attn_prefill", "dsa_gather_rows", "dsa_sparse_attn_decode_static",
            "dsa_attn_static_scratch_bytes", "dsa_attn_plan", "dsa_debug_index_scores_stalled", "dsa_index_topk",
-           "dsa_index_topk_workspace_size", "dsa_index_scores_counted", "dsa_topk_counted", "dsa_sparse_attn_q8"]
+           "dsa_index_topk_workspace_size", "dsa_index_scores_counted", "dsa_topk_counted", "dsa_sparse_attn_q8",
+           "dsa_compress_jobs"]
 
 
 class DsaPool(ctypes.Structure):
@@ -36,6 +40,14 @@ class DsaBlockTable(ctypes.Structure):
 
 class DsaRope(ctypes.Structure):
     _fields_ = [("rope_dim", ctypes.c_int32), ("theta", ctypes.c_double)]
+
+
+class DsaCompressJob(ctypes.Structure):
+    _fields_ = [("x_new", ctypes.c_void_p), ("logit_new", ctypes.c_void_p), ("state_x", ctypes.c_void_p),
+                ("state_logit", ctypes.c_void_p), ("rms_gamma", ctypes.c_void_p), ("rms_eps", ctypes.c_float),
+                ("rope", ctypes.POINTER(DsaRope)), ("out", ctypes.POINTER(DsaPool)),
+                ("out_bt", ctypes.POINTER(DsaBlockTable)), ("swa", ctypes.POINTER(DsaPool)),
+                ("swa_bt", ctypes.POINTER(DsaBlockTable))]
 
 
 class DsaError(RuntimeError):
@@ -60,6 +72,7 @@ _lib.dsa_topk_plan.restype = ctypes.c_int32
 _lib.dsa_topk_plan.argtypes = [_I, _I, _I, _P]
 for _name, _args in {
     "dsa_compress": [_I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P],
+    "dsa_compress_jobs": [_I, _I, _P, _P, _I, _P, _I, _I, _P, _P, _P],
     "dsa_index_scores": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P],
     "dsa_debug_index_scores_stalled": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, ctypes.c_uint64, _P,
                                        _P],
@@ -135,6 +148,22 @@ def dsa_compress(kind, cu_new, start_pos, max_new, x_new, logit_new, state_x, st
                              None if swa is None else ctypes.byref(swa),
                              None if swa_bt is None else ctypes.byref(swa_bt), _ptr(dev_status), _stream(stream))
     _check("dsa_compress", code)
+
+
+def compress_job(x_new, logit_new, state_x, state_logit, rope_cfg, out, out_bt, swa=None, swa_bt=None,
+                 rms_gamma=None, rms_eps=1e-6):
+    """One cache's arguments of dsa_compress_jobs (the struct keeps the rope, pool and table objects alive)."""
+    return DsaCompressJob(x_new.data_ptr(), logit_new.data_ptr(), state_x.data_ptr(), state_logit.data_ptr(),
+                          None if rms_gamma is None else rms_gamma.data_ptr(), float(rms_eps), ctypes.pointer(rope_cfg),
+                          ctypes.pointer(out), ctypes.pointer(out_bt), None if swa is None else ctypes.pointer(swa),
+                          None if swa_bt is None else ctypes.pointer(swa_bt))
+
+
+def dsa_compress_jobs(kind, cu_new, start_pos, max_new, state_slot, num_slots, jobs, dev_status=None, stream=None):
+    arr = (DsaCompressJob * len(jobs))(*jobs)
+    code = _lib.dsa_compress_jobs(KIND.get(kind, kind), start_pos.numel(), _ptr(cu_new), _ptr(start_pos), int(max_new),
+                                  _ptr(state_slot), int(num_slots), len(jobs), arr, _ptr(dev_status), _stream(stream))
+    _check("dsa_compress_jobs", code)
 
 
 def dsa_index_scores(q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, n_visible=None, dev_status=None,

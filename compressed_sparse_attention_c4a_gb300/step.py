@@ -27,7 +27,7 @@ def _query_group(spec, idx_heads):
 class LayerStep:
     """Device-resident state and buffers of one case (a dict from ``synth.make_case`` on cuda)."""
 
-    def __init__(self, case, counted_topk=False):
+    def __init__(self, case, counted_topk=False, two_streams=False):
         spec = case["spec"]
         self.case, self.spec = case, spec
         dev = case["q"].device
@@ -69,6 +69,8 @@ class LayerStep:
         self.workspace = torch.empty((max(ws, 256),), dtype=torch.uint8, device=dev) if ws else None
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
         self.max_new = max(spec.new) if spec.new else 0
+        self.jobs = None
+        self.two_streams = two_streams
         self.side = None
 
     # ---- stages ------------------------------------------------------------------------
@@ -88,8 +90,18 @@ class LayerStep:
                              dev_status=self.status)
 
     def compress(self):
-        self.compress_main()
-        self.compress_index()
+        """Both compressors of the layer in one launch (main cache + SWA insert, and the indexer cache)."""
+        c = self.case
+        if not (self.has_index and self.spec.index_compress):
+            self.compress_main()
+            return
+        if self.jobs is None:
+            self.jobs = [dsa.compress_job(c["x_new"], c["z_new"], c["state_x"], c["state_z"], self.rope_main,
+                                          self.main, self.main_bt, self.swa, self.swa_bt),
+                         dsa.compress_job(c["xi_new"], c["zi_new"], c["state_xi"], c["state_zi"], self.rope_idx,
+                                          self.idx, self.idx_bt)]
+        dsa.dsa_compress_jobs(self.kind, c["cu_new"], c["start_pos"], self.max_new, c["state_slot"],
+                              c["state_x"].shape[0], self.jobs, dev_status=self.status)
 
     def index(self):
         """Indexer scores (counting each row's first top-k digit when the counted top-k follows)."""
@@ -130,19 +142,26 @@ class LayerStep:
         per_compress = 1 + (1 if self.max_new > 1 else 0)
         n = per_compress
         if self.has_index:
-            n += (per_compress if self.spec.index_compress else 0) + 2
+            n += (per_compress if self.spec.index_compress and self.two_streams else 0) + 2
         n += self.attn_plan[3]
         return n
 
     def run(self):
         """The whole step: compress (+SWA insert), index, top-k, attention with inverse RoPE.
 
-        Two streams, as in the pages' multi-stream layout: the main-cache compressor and SWA insert
-        run on a side stream while the indexer chain (indexer compressor -> scores -> top-k) runs on
-        the current one; attention waits for both.  Captured into a CUDA graph this is a fork/join.
+        One stream: both compressors in one launch, then the indexer, the top-k and the attention, each
+        launched programmatically so that its set-up overlaps the tail of the kernel before it.  With
+        ``two_streams`` the main-cache compressor and SWA insert run on a side stream beside the indexer chain
+        (indexer compressor -> scores -> top-k) and the attention waits for both (a fork/join in a graph).
         """
         if not self.has_index:
             self.compress_main()
+            self.attend()
+            return self.out
+        if not self.two_streams:
+            self.compress()
+            self.index()
+            self.select()
             self.attend()
             return self.out
         cur = torch.cuda.current_stream()

@@ -121,7 +121,10 @@ const char* dsa_status_string(dsa_status_t status);
  * rms_gamma  [dim] fp32 or NULL (= all ones);  rms_eps > 0
  * out        bf16, e4m3 or e2m1 pool (e2m1: scale = amax/6), rows_per_block = 256/s;  swa: rows_per_block = 256
  *            (bf16 or e4m3), or NULL
- * Supported: dim in {64, 128, 512} (multiple of 64), rope_dim even and <= dim.
+ * Supported: dim in {64, 128, 512}, rope_dim even and <= min(dim, 64).
+ * Launched with programmatic dependent launch: cu_new, start_pos, state_slot, the block tables and rms_gamma
+ * are read before waiting for the preceding kernel in the stream; the raw tokens, logits and rolling state
+ * are read, and the pools and state written, only after it.
  */
 dsa_status_t dsa_compress(int32_t kind, int32_t batch, const int32_t* cu_new, const int32_t* start_pos,
                           int32_t max_new, const void* x_new, const float* logit_new, void* state_x,
@@ -129,6 +132,33 @@ dsa_status_t dsa_compress(int32_t kind, int32_t batch, const int32_t* cu_new, co
                           const float* rms_gamma, float rms_eps, const dsa_rope_t* rope,
                           const dsa_pool_t* out, const dsa_block_table_t* out_bt, const dsa_pool_t* swa,
                           const dsa_block_table_t* swa_bt, int32_t* dev_status, void* stream);
+
+/*
+ * dsa_compress_jobs - dsa_compress of up to 4 caches of one layer in one launch.  [P2] 融合点 3 (per-token work
+ * of one layer that touches different caches runs side by side in one kernel, picked by warp and block index).
+ * The jobs share the requests and their new tokens' positions (kind, batch, cu_new, start_pos, max_new,
+ * state_slot, num_slots: as dsa_compress); each job has its own raw rows, logits, rolling state, norm weights,
+ * RoPE, pool and optional window pool, with the meaning, layout and checks of dsa_compress (a layer's main
+ * cache with its window insert, and its indexer cache).  Each job's results equal those of its own
+ * dsa_compress call.  The jobs must not share an output row or a rolling state.  n_jobs: 1 .. 4.
+ */
+typedef struct dsa_compress_job {
+    const void* x_new;          /* [cu_new[batch]][dim] bf16 */
+    const float* logit_new;     /* [cu_new[batch]] */
+    void* state_x;              /* [num_slots][w][dim] bf16 */
+    float* state_logit;         /* [num_slots][w] */
+    const float* rms_gamma;     /* [dim] or NULL */
+    float rms_eps;
+    const dsa_rope_t* rope;
+    const dsa_pool_t* out;
+    const dsa_block_table_t* out_bt;
+    const dsa_pool_t* swa;      /* or NULL */
+    const dsa_block_table_t* swa_bt;
+} dsa_compress_job_t;
+
+dsa_status_t dsa_compress_jobs(int32_t kind, int32_t batch, const int32_t* cu_new, const int32_t* start_pos,
+                               int32_t max_new, const int32_t* state_slot, int32_t num_slots, int32_t n_jobs,
+                               const dsa_compress_job_t* jobs, int32_t* dev_status, void* stream);
 
 /*
  * dsa_index_scores - lightning-indexer scores of each query against every visible

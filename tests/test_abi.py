@@ -149,3 +149,23 @@ def test_fp4_pool_checks_host_only(lib):
     lib.dsa_attn_plan.argtypes = [ctypes.c_int32] * 4 + [P]
     plan = (ctypes.c_int32 * 4)()
     assert lib.dsa_attn_plan(4, 64, 640, dsa.DSA_FP4_E2M1, plan) == dsa.DSA_ERR_UNSUPPORTED
+
+
+def test_compress_rejects_rope_beyond_its_table_host_only(lib):
+    """RoPE frequencies are a 32-pair table: rope_dim > 64 is DSA_ERR_UNSUPPORTED before any launch, for the one-cache
+    call and for a job of the several-cache call; n_jobs outside 1 .. 4 is DSA_ERR_INVALID_ARG."""
+    import torch
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    P = ctypes.c_void_p
+    rope = dsa.DsaRope(128, 10000.0)
+    out = dsa.DsaPool(1 << 20, None, 4, 64, 128, dsa.DSA_BF16)
+    bt = dsa.DsaBlockTable(64, 1, 4)
+    args = [0, 1, P(16), P(16), 1, P(16), P(16), P(16), P(16), P(16), 4, None, ctypes.c_float(1e-6), ctypes.byref(rope),
+            ctypes.byref(out), ctypes.byref(bt), None, None, None, None]
+    assert dsa._lib.dsa_compress(*args) == dsa.DSA_ERR_UNSUPPORTED
+    t = torch.zeros(16)
+    job = dsa.compress_job(t, t, t, t, rope, out, bt)
+    arr = (dsa.DsaCompressJob * 1)(job)
+    assert dsa._lib.dsa_compress_jobs(0, 1, P(16), P(16), 1, P(16), 4, 1, arr, None, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert dsa._lib.dsa_compress_jobs(0, 1, P(16), P(16), 1, P(16), 4, 5, arr, None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert dsa._lib.dsa_compress_jobs(0, 1, P(16), P(16), 1, P(16), 4, 0, arr, None, None) == dsa.DSA_ERR_INVALID_ARG

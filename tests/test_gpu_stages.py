@@ -139,6 +139,28 @@ def test_compress_indexer(name):
         assert np.array_equal(gx[int(np64(cpu["state_slot"])[r])], states[r].x)
 
 
+@pytest.mark.parametrize("name", ["c4a_decode", "c4a_chunk", "c4a_early", "c4a_decode_fp4", "c4a_multi_prefill"])
+def test_compress_jobs_equal_separate_calls(name):
+    """dsa_compress_jobs (main cache + window insert and the indexer cache in one launch) writes the same bytes
+    to every pool, window row and rolling state as one dsa_compress call per cache."""
+    cpu = synth.make_case(CASES[name], "cpu")
+    outs = []
+    for fused in (True, False):
+        gpu = to_device(cpu)
+        step = LayerStep(gpu)
+        if fused:
+            step.compress()
+        else:
+            step.compress_main()
+            step.compress_index()
+        torch.cuda.synchronize()
+        assert int(step.status.item()) == 0
+        outs.append({k: gpu[k].cpu() for k in ("main_data", "swa_data", "idx_data", "idx_scale", "state_x", "state_z",
+                                               "state_xi", "state_zi")})
+    for k in outs[0]:
+        assert torch.equal(outs[0][k], outs[1][k]), k
+
+
 def _oracle_scores_on_gpu_pool(cpu, gpu):
     pool = idx_pool(gpu)
     return OL.index_scores(np64(cpu["q8"]), np64(cpu["q_scale"]), np64(cpu["w"]), np64(cpu["q_pos"]),
