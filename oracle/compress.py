@@ -10,6 +10,9 @@ coff * ratio raw tokens (8 for c4a, 128 for c128a) between steps.
 Readings where the pages are open (each also listed in the design notes):
   * gate: g_j = softmax_j(z) over the window, one scalar logit z per raw token, the
     same logit in both windows that contain a token;
+  * per-channel gate (a variant; the pages say only "weighted sum"): one logit per raw token and
+    channel, z [T][d], and a separate softmax over the window for every channel c,
+    u_c = sum_j softmax_j(z_{., c})_j x_{j, c};
   * RMSNorm: v = gamma * u / sqrt(mean(u^2) + eps), gamma = 1, eps = 1e-6 unless given;
   * entry i covers raw positions s*i .. s*i + w - 1 and is rotated at the last one,
     pos_i = s*i + w - 1;
@@ -44,10 +47,11 @@ def entry_position(i, kind):
 
 
 def gate(z):
-    """Softmax of the window's logits, float64."""
+    """Softmax over the window (axis 0) of the window's logits, float64: z [w] (one weight per token) or
+    z [w][d] (per channel: a softmax down every column)."""
     z = np.asarray(z, dtype=np.float64)
-    e = np.exp(z - np.max(z))
-    return e / np.sum(e)
+    e = np.exp(z - np.max(z, axis=0))
+    return e / np.sum(e, axis=0)
 
 
 def rms_norm(u, gamma=None, eps=RMS_EPS):
@@ -58,14 +62,17 @@ def rms_norm(u, gamma=None, eps=RMS_EPS):
 
 
 def compress_entry(x_win, z_win, pos, rope_dim, gamma=None, eps=RMS_EPS, theta=ROPE_THETA):
-    """One compressed entry: R_pos(RMSNorm(sum_j g_j x_j)) with g = softmax(z_win)."""
+    """One compressed entry: R_pos(RMSNorm(sum_j g_j x_j)) with g = softmax(z_win); z_win [w] (scalar gate) or
+    [w][d] (per-channel gate, g_j a vector multiplying x_j element by element)."""
     g = gate(z_win)
-    u = np.sum(g[:, None] * np.asarray(x_win, dtype=np.float64), axis=0)
+    if g.ndim == 1:
+        g = g[:, None]
+    u = np.sum(g * np.asarray(x_win, dtype=np.float64), axis=0)
     return rope(rms_norm(u, gamma, eps), pos, rope_dim, theta)
 
 
 def compress_tokens(x, z, kind, rope_dim, gamma=None, eps=RMS_EPS, theta=ROPE_THETA):
-    """All entries formed from raw tokens x [T][d] with logits z [T] (bulk path)."""
+    """All entries formed from raw tokens x [T][d] with logits z [T] or [T][d] (bulk path)."""
     w, s = WINDOW[kind]
     x = np.asarray(x, dtype=np.float64)
     n = n_entries(x.shape[0], kind)
@@ -77,13 +84,15 @@ def compress_tokens(x, z, kind, rope_dim, gamma=None, eps=RMS_EPS, theta=ROPE_TH
 
 
 class RollingState:
-    """Per-request residual: the last w raw tokens and logits, slot = position mod w."""
+    """Per-request residual: the last w raw tokens and logits, slot = position mod w (logits [w], or [w][d]
+    for the per-channel gate)."""
 
-    def __init__(self, kind, dim, ring_x=None, ring_z=None):
+    def __init__(self, kind, dim, ring_x=None, ring_z=None, per_channel=False):
         self.kind = kind
         w, _ = WINDOW[kind]
         self.x = np.zeros((w, dim)) if ring_x is None else np.array(ring_x, dtype=np.float64)
-        self.z = np.zeros(w) if ring_z is None else np.array(ring_z, dtype=np.float64)
+        zshape = (w, dim) if per_channel else (w,)
+        self.z = np.zeros(zshape) if ring_z is None else np.array(ring_z, dtype=np.float64)
 
     def step(self, x_p, z_p, p, rope_dim, gamma=None, eps=RMS_EPS, theta=ROPE_THETA):
         """Append token p; return (i, entry) when p closes entry i, else None."""

@@ -77,7 +77,7 @@ def compress(kind, start_pos, x_new, z_new, states, rope_dim, out_pool, out_bt,
              swa_pool=None, swa_bt=None, gamma=None, eps=1e-6, theta=ROPE_THETA, record=None):
     """Append new raw tokens per request, emitting every entry they close.
 
-    start_pos [B]; x_new[r] [n_r][d] and z_new[r] [n_r] hold request r's new tokens at
+    start_pos [B]; x_new[r] [n_r][d] and z_new[r] [n_r] (or [n_r][d], per-channel gate) hold request r's new tokens at
     positions start_pos[r] .. start_pos[r] + n_r - 1; states[r] is its RollingState,
     updated in place.  Entry i goes to ``out_pool`` logical row i; with an SWA pool,
     token p goes to its logical row p as R_p x_p.  Returns the emitted entry ids per request.
@@ -162,7 +162,7 @@ def sparse_attn_q8(q, q_pos, q_req, kind, topk_ids, main_pool, main_bt, swa_pool
 
 
 def ring_contents(states):
-    """(x [B][w][d], z [B][w]) of a list of RollingStates, slot = position mod w."""
+    """(x [B][w][d], z [B][w] or [B][w][d]) of a list of RollingStates, slot = position mod w."""
     return np.stack([s.x for s in states]), np.stack([s.z for s in states])
 
 

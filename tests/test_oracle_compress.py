@@ -155,3 +155,62 @@ def test_layer_compress_fp8_pool_and_swa_rows():
     codes, scale = codecs.fp8_quantize_rows(e1[None])
     assert np.array_equal(pool.data[1], codes[0]) and pool.scale[1] == scale[0]
     assert np.array_equal(swa.data[9], codecs.bf16_round(R.rope(x[9], 9, 8)))
+
+
+# ---- per-channel gate (a variant: one logit per raw token and channel, a softmax down every channel) ----
+
+def test_per_channel_gate_brute_force():
+    """u_c = sum_j exp(z_jc) / sum_k exp(z_kc) * x_jc, written out with scalar loops on a tiny window."""
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((8, 5))
+    z = rng.standard_normal((8, 5)) * 2.0
+    u = np.zeros(5)
+    for c in range(5):
+        den = sum(math.exp(z[k, c]) for k in range(8))
+        u[c] = sum(math.exp(z[j, c]) / den * x[j, c] for j in range(8))
+    want = R.rope(u / math.sqrt(float(np.dot(u, u)) / 5 + 1e-6), 7, 0)
+    got = C.compress_entry(x, z, pos=7, rope_dim=0)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-13)
+    g = C.gate(z)
+    assert g.shape == (8, 5) and np.allclose(g.sum(axis=0), 1.0, rtol=1e-14)
+
+
+def test_per_channel_gate_with_equal_columns_is_the_scalar_gate():
+    """Logits that are the same in every channel of a token give the scalar gate's entry (up to the order in
+    which numpy sums a window: a one-dimensional sum and a column sum round differently in the last bit)."""
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((8, 64))
+    zs = rng.standard_normal(8)
+    scalar = C.compress_entry(x, zs, pos=15, rope_dim=16)
+    per_channel = C.compress_entry(x, np.repeat(zs[:, None], 64, axis=1), pos=15, rope_dim=16)
+    assert np.allclose(scalar, per_channel, rtol=1e-13, atol=1e-14)
+
+
+def test_per_channel_gate_picks_a_token_per_channel():
+    """A dominant logit in channel c selects token j_c for that channel only: different channels take their
+    values from different tokens."""
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((8, 16))
+    z = np.zeros((8, 16))
+    pick = np.arange(16) % 8
+    z[pick, np.arange(16)] = 800.0
+    t = x[pick, np.arange(16)]
+    want = t / math.sqrt(float(np.dot(t, t)) / 16 + 1e-6)
+    assert np.allclose(C.compress_entry(x, z, pos=3, rope_dim=0), want, atol=1e-12)
+
+
+@pytest.mark.parametrize("kind,T", [(C.C4A, 203), (C.C128A, 300)])
+def test_per_channel_incremental_equals_bulk_bitwise(kind, T):
+    rng = np.random.default_rng(14)
+    x = rng.standard_normal((T, 32))
+    z = rng.standard_normal((T, 32))
+    bulk = C.compress_tokens(x, z, kind, rope_dim=8)
+    st = C.RollingState(kind, 32, per_channel=True)
+    got = {}
+    for p in range(T):
+        res = st.step(x[p], z[p], p, rope_dim=8)
+        if res is not None:
+            got[res[0]] = res[1]
+    assert sorted(got) == list(range(len(bulk)))
+    for i, e in got.items():
+        assert np.array_equal(e, bulk[i])
