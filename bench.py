@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU work of the oracle sample")
+    ap.add_argument("--copies", type=int, default=COPIES,
+                    help="resident cache copies the steps rotate over (fewer for small profiling captures)")
     return ap.parse_args()
 
 
@@ -226,7 +228,7 @@ def run_gpu(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
     spec = synth.case_specs()[args.workload]
     copies = []
-    for c in range(COPIES):
+    for c in range(args.copies):
         s = synth.CaseSpec(**{**spec.__dict__, "seed": spec.seed + 100 * c + 10000 * rank})
         copies.append(LayerStep(synth.make_case(s, dev)))
     torch.cuda.synchronize()
@@ -242,18 +244,18 @@ def run_gpu(args, rank, world, local_rank):
     # warm-up (eager; also loads the kernels) then graphs: S steps rotate over the copies
     with torch.cuda.stream(stream):
         for i in range(max(3, min(args.warmup, 50))):
-            copies[i % COPIES].run()
+            copies[i % args.copies].run()
     torch.cuda.synchronize()
     # a step that reports a device error (an expired bounded wait costs up to 2 s per launch) is not timed
     warm_status = max(int(c.status.item()) for c in copies)
     if warm_status:
         raise SystemExit(f"device status {warm_status} ({dsa.dsa_status_string(warm_status)}) after the warm-up "
                          f"steps: not timing a failing step")
-    per_graph = COPIES * max(1, min(25, args.steps // (COPIES * 20)))  # >= 20 repetitions when steps allow
+    per_graph = args.copies * max(1, min(25, args.steps // (args.copies * 20)))  # >= 20 repetitions when steps allow
     g_plain = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_plain, stream=stream):
         for i in range(per_graph):
-            copies[i % COPIES].run()
+            copies[i % args.copies].run()
     # same steps with events around the indexer, top-k and attention launches (kernel durations)
     def timing_event():
         try:
@@ -267,7 +269,7 @@ def run_gpu(args, rank, world, local_rank):
         g_timed = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_timed, stream=stream):
             for i in range(per_graph):
-                st = copies[i % COPIES]
+                st = copies[i % args.copies]
                 st.compress()
                 if st.has_index:
                     ev["index"][i][0].record(stream)
@@ -323,7 +325,7 @@ def run_gpu(args, rank, world, local_rank):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for i in range(per_graph):
-                    st = copies[i % COPIES]
+                    st = copies[i % args.copies]
                     {"index": st.index, "topk": st.select, "attend": st.attend}[n]()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             with torch.cuda.stream(stream):
@@ -380,9 +382,10 @@ def run_gpu(args, rank, world, local_rank):
         "warmup": warm_reps * per_graph, "ms_per_step": round(ms_step, 6), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": ("bf16" if spec.main_dtype == "bf16" else "e4m3 (token-wise scale, codes to bf16 on the tensor cores)")
-        + " attention" + (" + e4m3 indexer" if spec.idx_heads else "") + " (fp32 accumulate)",
+        + " attention" + ((" + e2m1 indexer keys, e4m3 queries" if spec.idx_dtype == "fp4" else " + e4m3 indexer")
+                          if spec.idx_heads else "") + " (fp32 accumulate)",
         "data": "synthetic (seeded N(0,1) caches, queries and tokens; no weights)",
-        "config": workload_config(args.workload, spec, world),
+        "config": workload_config(args.workload, spec, world, args.copies),
         "step_bytes": idx_bytes + att_bytes, "step_gbs": round((idx_bytes + att_bytes) / (ms_step * 1e6), 1),
         "kernels": {n: {k: round(v, 6) for k, v in d.items()} for n, d in kern.items()}, "kernel_timing": timing,
         "roofline": roof, "attention_roofline": roof_other, "timing": rep_stats, "kernel_launches_timed": k_launches,
@@ -394,7 +397,7 @@ def run_gpu(args, rank, world, local_rank):
     return line, copies
 
 
-def workload_config(name, spec, world):
+def workload_config(name, spec, world, copies=COPIES):
     """The `config` object of both arms' JSON lines."""
     return {"workload": name, "kind": spec.kind, "batch": spec.batch,
             "context": sorted(set(c + n for c, n in zip(spec.cached, spec.new)))[:4],
@@ -402,7 +405,7 @@ def workload_config(name, spec, world):
             "indexer": (f"{spec.idx_heads}x{spec.idx_dim} " + ("e2m1" if spec.idx_dtype == "fp4" else "e4m3"))
                        if spec.idx_heads else None,
             "topk": spec.topk or None, "window": spec.window, "kv": spec.main_dtype,
-            "l2": f"inputs larger than L2: {COPIES} resident cache copies rotate, each step's working set is "
+            "l2": f"inputs larger than L2: {copies} resident cache copies rotate, each step's working set is "
                   f"evicted by the other copies", "parallelism": f"replicas x{world}"}
 
 

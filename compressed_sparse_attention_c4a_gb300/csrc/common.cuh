@@ -130,7 +130,12 @@ __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepc
     } while (0)
 #define DSA_STAMP_NS(k)                                                                           \
     do {                                                                                          \
-        if (g_timeline) g_timeline[(unsigned long long)blockIdx.x * 32 + (k)] = global_ns();      \
+        if (g_timeline) {                                                                         \
+            unsigned smid_;                                                                       \
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid_));                                    \
+            g_timeline[(unsigned long long)blockIdx.x * 32 + 29] = smid_;                         \
+            g_timeline[(unsigned long long)blockIdx.x * 32 + (k)] = global_ns();                  \
+        }                                                                                         \
     } while (0)
 // DSA_TRACE(n, k): the SM clock of event k of work item n of CTAs 0-7 (items below 64), in records 8192 + .
 #define DSA_TRACE(n, k)                                                                           \

@@ -35,6 +35,7 @@ struct CompressArgs {
     int entry_items;  // warps per request reserved for entries
     int token_items;  // warps per request reserved for new tokens
     int fuse_ring;    // token warps also update the rolling state (at most one new token per request)
+    int gate_pc;      // per-channel gate: logits [n][dim] and rolling logits [slots][w][dim]
     int32_t* status;
 };
 
@@ -73,6 +74,35 @@ __device__ __forceinline__ void copy_bf16(uint16_t* dst, const uint16_t* src, in
         *reinterpret_cast<uint2*>(dst + lane * E) = *reinterpret_cast<const uint2*>(src + lane * E);
     } else {
         *reinterpret_cast<uint32_t*>(dst + lane * E) = *reinterpret_cast<const uint32_t*>(src + lane * E);
+    }
+}
+
+template <int E>
+__device__ __forceinline__ void load_f32(const float* row, int lane, float (&v)[E]) {
+    const float* p = row + lane * E;
+    if constexpr (E % 4 == 0) {
+#pragma unroll
+        for (int k = 0; k < E; k += 4) {
+            const float4 t = *reinterpret_cast<const float4*>(p + k);
+            v[k] = t.x, v[k + 1] = t.y, v[k + 2] = t.z, v[k + 3] = t.w;
+        }
+    } else {
+        static_assert(E == 2, "row width");
+        const float2 t = *reinterpret_cast<const float2*>(p);
+        v[0] = t.x, v[1] = t.y;
+    }
+}
+
+template <int E>
+__device__ __forceinline__ void copy_f32(float* dst, const float* src, int lane) {
+    float v[E];
+    load_f32<E>(src, lane, v);
+    if constexpr (E % 4 == 0) {
+#pragma unroll
+        for (int k = 0; k < E; k += 4)
+            *reinterpret_cast<float4*>(dst + lane * E + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+    } else {
+        *reinterpret_cast<float2*>(dst + lane * E) = make_float2(v[0], v[1]);
     }
 }
 
@@ -202,6 +232,40 @@ __device__ __forceinline__ void compress_item(const CompressArgs& a, int item, i
             return p < start ? a.state_x + ((long long)slot * w + (p % w)) * DIM
                              : a.x_new + (long long)(cu0 + (p - start)) * DIM;
         };
+        float acc[E];
+        if (a.gate_pc) {
+            // per-channel gate: for each of the lane's channels an online softmax over the window (running
+            // maximum, denominator and weighted sum), RC window rows of values and logits in flight at a time
+            auto zrow_at = [&](long long p) -> const float* {
+                return p < start ? a.state_logit + ((long long)slot * w + (p % w)) * DIM
+                                 : a.logit_new + (long long)(cu0 + (p - start)) * DIM;
+            };
+            constexpr int RC = E >= 16 ? 2 : (W < 8 ? W : 8);
+            float m[E], den[E];
+#pragma unroll
+            for (int k = 0; k < E; ++k) m[k] = -INFINITY, den[k] = 0.f, acc[k] = 0.f;
+#pragma unroll 1
+            for (int j0 = 0; j0 < W; j0 += RC) {
+                float xv[RC][E], zv[RC][E];
+#pragma unroll
+                for (int u = 0; u < RC; ++u) {
+                    load_bf16<E>(row_at(base + j0 + u), lane, xv[u]);
+                    load_f32<E>(zrow_at(base + j0 + u), lane, zv[u]);
+                }
+#pragma unroll
+                for (int u = 0; u < RC; ++u)
+#pragma unroll
+                    for (int k = 0; k < E; ++k) {
+                        const float mn = fmaxf(m[k], zv[u][k]);
+                        const float sc = expf(m[k] - mn), e = expf(zv[u][k] - mn);
+                        den[k] = fmaf(den[k], sc, e);
+                        acc[k] = fmaf(acc[k], sc, e * xv[u][k]);
+                        m[k] = mn;
+                    }
+            }
+#pragma unroll
+            for (int k = 0; k < E; ++k) acc[k] /= den[k];
+        } else {
         // gate g_j = softmax_j(z_{s i + j}): lane l holds the logits of window tokens l, l + 32, ...
         constexpr int LPL = (W + 31) / 32;  // logits per lane
         constexpr int RB = W < 8 ? W : 8;   // window rows in flight at a time
@@ -225,7 +289,6 @@ __device__ __forceinline__ void compress_item(const CompressArgs& a, int item, i
         }
         den = warp_sum(den);
         const float inv_den = 1.f / den;
-        float acc[E];
 #pragma unroll
         for (int k = 0; k < E; ++k) acc[k] = 0.f;
 #pragma unroll 1
@@ -241,6 +304,7 @@ __device__ __forceinline__ void compress_item(const CompressArgs& a, int item, i
 #pragma unroll
                 for (int k = 0; k < E; ++k) acc[k] = fmaf(g, x[u][k], acc[k]);
             }
+        }
         }
         // RMSNorm
         float ss = 0.f;
@@ -276,7 +340,8 @@ __device__ __forceinline__ void compress_item(const CompressArgs& a, int item, i
     if (a.fuse_ring && j >= n - w) {
         const long long ring = (long long)slot * w + (p % w);
         copy_bf16<E>(a.state_x + ring * DIM, xrow, lane);
-        if (lane == 0) a.state_logit[ring] = a.logit_new[cu0 + j];
+        if (a.gate_pc) copy_f32<E>(a.state_logit + ring * DIM, a.logit_new + (long long)(cu0 + j) * DIM, lane);
+        else if (lane == 0) a.state_logit[ring] = a.logit_new[cu0 + j];
     }
 }
 
@@ -298,7 +363,7 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
     const CompressArgs& a = js.job[blockIdx.z];
     const int lane = threadIdx.x & 31;
     const int per_req = a.entry_items + a.token_items;
-    const int wi = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int wi = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int r = wi / per_req, item = wi - r * per_req;
     if (r >= a.batch) {  // no work; the grid still ends after the preceding kernel
         pdl_wait();
@@ -325,7 +390,8 @@ __device__ __forceinline__ void ring_update_item(const CompressArgs& a, int item
     const long long p = (long long)a.start_pos[r] + j;
     const long long ring = (long long)slot * a.w + (p % a.w);
     copy_bf16<E>(a.state_x + ring * DIM, a.x_new + (long long)(cu0 + j) * DIM, lane);
-    if (lane == 0) a.state_logit[ring] = a.logit_new[cu0 + j];
+    if (a.gate_pc) copy_f32<E>(a.state_logit + ring * DIM, a.logit_new + (long long)(cu0 + j) * DIM, lane);
+    else if (lane == 0) a.state_logit[ring] = a.logit_new[cu0 + j];
 }
 
 __global__ void __launch_bounds__(256) ring_update_kernel(const __grid_constant__ CompressJobs js) {
@@ -345,10 +411,13 @@ static dsa_status_t launch_compress(const CompressJobs& js, int w, int batch, in
     long long warps = 0;
     for (int k = 0; k < js.n_jobs; ++k)
         warps = std::max(warps, (long long)batch * (js.job[k].entry_items + js.job[k].token_items));
-    if ((warps + 7) / 8 > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
-    dim3 grid((unsigned)((warps + 7) / 8), 1, js.n_jobs);
-    cudaError_t e = w == 8 ? launch_pdl(compress_kernel<8>, grid, dim3(256), 0, st, js)
-                           : launch_pdl(compress_kernel<128>, grid, dim3(256), 0, st, js);
+    // small grids (decode) in CTAs of 2 warps: they fit beside two CTAs of the indexer that follows on an SM,
+    // which 8-warp CTAs do not (each SM quarter has its own registers)
+    const int wpc = warps * js.n_jobs <= 4LL * sm_count() ? 2 : 8;
+    if ((warps + wpc - 1) / wpc > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
+    dim3 grid((unsigned)((warps + wpc - 1) / wpc), 1, js.n_jobs);
+    cudaError_t e = w == 8 ? launch_pdl(compress_kernel<8>, grid, dim3(32 * wpc), 0, st, js)
+                           : launch_pdl(compress_kernel<128>, grid, dim3(32 * wpc), 0, st, js);
     if (e == cudaSuccess && !js.job[0].fuse_ring && max_new > 0)
         e = launch_pdl(ring_update_kernel, dim3((w + 7) / 8, batch, js.n_jobs), dim3(256), 0, st, js);
     if (e != cudaSuccess) return DSA_ERR_CUDA;
@@ -363,7 +432,7 @@ using namespace dsa;
 static dsa_status_t make_job(int batch, int max_new, int w, int s, const void* x_new, const float* logit_new,
                              void* state_x, float* state_logit, const float* rms_gamma, float rms_eps,
                              const dsa_rope_t* rope, const dsa_pool_t* out, const dsa_block_table_t* out_bt,
-                             const dsa_pool_t* swa, const dsa_block_table_t* swa_bt, CompressArgs* a) {
+                             const dsa_pool_t* swa, const dsa_block_table_t* swa_bt, int gate_pc, CompressArgs* a) {
     if (!(rms_eps > 0.f)) return DSA_ERR_INVALID_ARG;
     if (!x_new || !logit_new || !state_x || !state_logit || !rope) return DSA_ERR_INVALID_ARG;
     if (!pool_ok(out) || !table_ok(out_bt, batch)) return DSA_ERR_INVALID_ARG;
@@ -379,7 +448,10 @@ static dsa_status_t make_job(int batch, int max_new, int w, int s, const void* x
         if (swa->dtype == DSA_FP4_E2M1) return DSA_ERR_UNSUPPORTED;
     }
     if (!aligned(x_new, 16) || !aligned(state_x, 16)) return DSA_ERR_INVALID_ARG;
+    if (gate_pc != 0 && gate_pc != 1) return DSA_ERR_INVALID_ARG;
+    if (gate_pc && (!aligned(logit_new, 16) || !aligned(state_logit, 16))) return DSA_ERR_INVALID_ARG;
     a->w = w;
+    a->gate_pc = gate_pc;
     a->s = s;
     a->batch = batch;
     a->dim = dim;
@@ -417,7 +489,8 @@ static dsa_status_t compress_jobs(int32_t kind, int32_t batch, const int32_t* cu
     for (int k = 0; k < n_jobs; ++k) {
         const dsa_compress_job_t& j = jobs[k];
         const dsa_status_t e = make_job(batch, max_new, w, s, j.x_new, j.logit_new, j.state_x, j.state_logit,
-                                        j.rms_gamma, j.rms_eps, j.rope, j.out, j.out_bt, j.swa, j.swa_bt, &js.job[k]);
+                                        j.rms_gamma, j.rms_eps, j.rope, j.out, j.out_bt, j.swa, j.swa_bt,
+                                        j.gate_per_channel, &js.job[k]);
         if (e != DSA_OK) return e;
         CompressArgs& a = js.job[k];
         a.cu_new = cu_new;
@@ -439,7 +512,7 @@ extern "C" dsa_status_t dsa_compress(int32_t kind, int32_t batch, const int32_t*
     if (batch < 0 || max_new < 0 || num_slots <= 0 || !(rms_eps > 0.f)) return DSA_ERR_INVALID_ARG;
     if (batch == 0 || max_new == 0) return DSA_OK;
     const dsa_compress_job_t job{x_new, logit_new, state_x, state_logit, rms_gamma, rms_eps, rope, out, out_bt, swa,
-                                 swa_bt};
+                                 swa_bt, 0};
     return compress_jobs(kind, batch, cu_new, start_pos, max_new, state_slot, num_slots, 1, &job, dev_status, stream);
 }
 

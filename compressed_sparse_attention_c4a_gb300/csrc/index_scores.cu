@@ -49,6 +49,7 @@ struct IdxArgs {
     const int32_t* q_pos;
     const int32_t* q_req;
     const int32_t* fresh_pos;   // [batch] first raw position the preceding kernel may still compress, or NULL
+    unsigned* work;             // [2] item counter and finished-CTA counter (dynamic split), or NULL (static)
     const float* key_scale;
     int num_blocks;
     dsa_block_table_t bt;
@@ -267,7 +268,9 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&gfull[b], 1);
-            mbar_init(&gempty[b], EW);
+            // released by the epilogue warps (and, for decode-shaped groups, whose epilogue keeps the group's
+            // values in registers and lets go at once, by the tensor cores' completion of the group's last MMA)
+            mbar_init(&gempty[b], N16 ? EW + 1 : EW);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -326,7 +329,20 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
         if (lane == 0) pre[a.n_groups] = (int)carry;
         __syncwarp();
         const long long V = carry;
-        const long long lo = V * blockIdx.x / gridDim.x, hi = V * (blockIdx.x + 1) / gridDim.x;
+        // static split: an equal contiguous share [lo, hi).  With a work counter (a.work): a contiguous run of
+        // half a fair share first, then runs of consecutive items taken from the counter (two requests in
+        // flight from the start, read when the static run ends), so that a CTA that starts late takes less
+        const bool dyn = a.work != nullptr;
+        const long long R = dyn ? V / (2 * gridDim.x) : 0;         // static run per CTA (dynamic split)
+        const long long base_dyn = R * gridDim.x;                   // first item of the shared remainder
+        const int G = dyn ? (int)max(1ll, min((long long)kChunkItems, (V - base_dyn) / gridDim.x)) : kChunkItems;
+        const long long lo = dyn ? R * blockIdx.x : V * blockIdx.x / gridDim.x;
+        const long long hi = dyn ? R * (blockIdx.x + 1) : V * (blockIdx.x + 1) / gridDim.x;
+        auto grab = [&]() -> long long {  // lane 0 issues the atomic; the value is read (shuffled) later
+            long long v = 0;
+            if (lane == 0) v = (long long)atomicAdd(a.work, (unsigned)G);
+            return v;
+        };
         // item index -> (group, tile) by binary search over the prefix
         auto locate = [&](long long idx, int* g, int* t) {
             int l = 0, h = a.n_groups - 1;
@@ -338,10 +354,10 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
             *g = l;
             *t = (int)(idx - pre[l]);
         };
-        auto resolve = [&](long long base) {
+        auto resolve = [&](long long base, long long end) {  // items [base, end), at most 32
             const long long idx = base + lane;
             int g = 0, t = 0;
-            const int valid = lane < kChunkItems && idx < hi;
+            const int valid = lane < kChunkItems && idx < end;
             if (valid) locate(idx, &g, &t);
             return item_info<TPI>(a, valid, g, t, grp_r, grp_mv);
         };
@@ -350,7 +366,16 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
         int cur_g = -1, gb = 1, guse[2] = {0, 0};  // group in the current buffer, buffer index, loads per buffer
         bool alive = true;
         if (lane == 0) DSA_STAMP(2);
-        ItemInfo cur = resolve(lo);
+        long long ahead1 = dyn ? grab() : 0, ahead2 = dyn ? grab() : 0;  // lane 0: the next two runs, in flight
+        long long base = lo, run_end = hi;  // the current run: [base, run_end)
+        auto next_run = [&](long long* b, long long* e) {  // a run from the counter (empty past the last item)
+            *b = base_dyn + __shfl_sync(0xffffffffu, ahead1, 0);
+            *e = min(*b + G, V);
+            ahead1 = ahead2;
+            ahead2 = grab();
+        };
+        if (dyn && base >= run_end) next_run(&base, &run_end);
+        ItemInfo cur = resolve(base, run_end);
         bool waited = !early;
         if (!early) {
             pdl_wait();  // keys may come from the preceding kernel
@@ -358,8 +383,13 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
         }
         if (bad_group) report(a.status, DSA_ERR_DEVICE_FAULT);
         // (test hook) withhold: no copy is issued and no stage posted, so every consumer wait runs out
-        for (long long base = lo; base < hi && alive && !a.withhold; base += kChunkItems) {
-            const ItemInfo nxt = resolve(base + kChunkItems);
+        while (base < run_end && alive && !a.withhold) {
+            long long nb = base + kChunkItems, ne = run_end;  // the next chunk of this run, or the next run
+            if (nb >= run_end) {
+                if (dyn) next_run(&nb, &ne);
+                else ne = nb;
+            }
+            const ItemInfo nxt = resolve(nb, ne);
             for (int u = 0; u < kChunkItems; ++u) {
                 ItemInfo it = shfl_item(cur, u);
                 if (!it.valid) continue;
@@ -466,6 +496,8 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                 }
             }
             cur = nxt;
+            base = nb;
+            run_end = ne;
         }
         if (lane == 0) DSA_STAMP(4);
         if (!waited) {  // the kernel ends after the preceding kernel, whatever it read
@@ -508,6 +540,9 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
             }
             const int gbi = slot_meta(k)->gb;
             if (gbi != prev_gb) {  // the first item of a group: its buffer's load
+                // decode-shaped groups: the previous group's buffer is free once its MMAs are complete
+                if constexpr (N16)
+                    if (prev_gb >= 0) mma_commit_elect(&gempty[prev_gb]);
                 prev_gb = gbi;
                 ++muse[gbi];
                 ok = wait_or_abort(&gfull[gbi], (muse[gbi] - 1) & 1, abort_flag, a.status, a.wait_ns);
@@ -548,7 +583,8 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
         const int quad = warp & 3;       // TMEM lanes this warp may access (EW == 4)
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        float u[16];  // w_c * sq_c of the group's columns (0 past its queries)
+        float u[16];              // w_c * sq_c of the group's columns (0 past its queries)
+        float wr[16], sqr[16];    // w_c and sq_c (the literal formula of a group with a negative query scale)
         int nv[QPC];  // visible entries of each query of the group
         bool q_neg = false;
         int nqg = 0, q0 = 0;
@@ -562,8 +598,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
             if (meta->terminal) break;
             const int gbi = meta->gb;
             const bool new_group = gbi != prev_gb;
-            if (new_group) {  // this warp is done with the previous group's buffer
-                if (prev_gb >= 0 && lane == 0) mbar_arrive(&gempty[prev_gb]);
+            if (new_group) {  // the group's values come into registers below, and the buffer is let go there
                 prev_gb = gbi;
                 ++euse[gbi];
                 ok = wait_or_abort(&gfull[gbi], (euse[gbi] - 1) & 1, abort_flag, a.status, a.wait_ns);
@@ -588,19 +623,22 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const bool live = c < nqg * HEADS;  // columns past the group's queries hold stale values
-                    u[c] = live ? sw[c] * ssq[c] : 0.f;
+                    wr[c] = live ? sw[c] : 0.f;
+                    sqr[c] = live ? ssq[c] : 0.f;
+                    u[c] = wr[c] * sqr[c];
                     neg |= live && ssq[c] < 0.f;
                 }
                 q_neg = neg;
 #pragma unroll
                 for (int j = 0; j < QPC; ++j) nv[j] = j < nqg ? gnv[j] : 0;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&gempty[gbi]);  // this warp no longer reads the buffer
                 if (tid == 64) DSA_TRACE(n, 7);
             }
             const float* sc = slot_scale(k);
             const int e0 = meta->e0;
             const bool ok0 = meta->blk[row / kPage] >= 0, ok1 = meta->blk[(kTileEntries + row) / kPage] >= 0;
             const float sk0 = ok0 ? sc[row] : 0.f, sk1 = ok1 ? sc[kTileEntries + row] : 0.f;
-            const float* gsw = reinterpret_cast<const float*>(gbase + (size_t)gbi * a.gbuf_bytes + 16 * DIM);
             tmem_wait_ld();
             tmem_regs_after_wait<16>(v0);
             tmem_regs_after_wait<16>(v1);
@@ -618,11 +656,10 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
                         }
                         a0 = (a0 + a1) * sk;
                     } else {  // a negative query scale: the literal w_h * max(0, sq_h * sk * x_h)
-                        const float* gsq = gsw + 16;
 #pragma unroll
                         for (int h = 0; h < HEADS; ++h) {
                             const int c = j * HEADS + h;
-                            a0 = fmaf(gsw[c], fmaxf(0.f, gsq[c] * sk * x[c]), a0);
+                            a0 = fmaf(wr[c], fmaxf(0.f, sqr[c] * sk * x[c]), a0);
                         }
                     }
                     if (e < a.ld) {
@@ -824,6 +861,13 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
     if (tid == 0) {
         DSA_STAMP(8);
         DSA_STAMP_NS(30);
+        if (a.work) {  // every CTA has taken its last run: the last to finish leaves the counters zero
+            __threadfence();
+            if (atomicAdd(a.work + 1, 1u) == gridDim.x - 1) {
+                atomicExch(a.work, 0u);
+                atomicExch(a.work + 1, 0u);
+            }
+        }
     }
     if (warp == 0) tmem_dealloc(tmem, a.tmem_cols);
 }
@@ -903,8 +947,8 @@ using namespace dsa;
 static dsa_status_t index_scores(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8, const float* q_scale,
                                  const float* w, const int32_t* q_pos, const int32_t* q_req, int32_t q_group,
                                  const dsa_pool_t* keys, const dsa_block_table_t* bt, float* scores, int32_t ld,
-                                 int32_t* n_visible, const int32_t* fresh_pos, int32_t* dev_status, void* stream,
-                                 uint64_t wait_ns, int withhold, unsigned* hist = nullptr) {
+                                 int32_t* n_visible, const int32_t* fresh_pos, uint32_t* work, int32_t* dev_status,
+                                 void* stream, uint64_t wait_ns, int withhold, unsigned* hist = nullptr) {
     if (nq < 0 || ld < 0 || (ld & 3)) return DSA_ERR_INVALID_ARG;
     if (nq == 0) return DSA_OK;
     if (heads != 4 && heads != 8 && heads != 16) return DSA_ERR_UNSUPPORTED;
@@ -914,7 +958,7 @@ static dsa_status_t index_scores(int32_t nq, int32_t heads, int32_t dim, const u
         return DSA_ERR_INVALID_ARG;
     if (!pool_ok(keys) || keys->dim != dim || keys->rows_per_block != kPage) return DSA_ERR_INVALID_ARG;
     if (keys->dtype == DSA_BF16 || (keys->dtype == DSA_FP4_E2M1 && dim != 128)) return DSA_ERR_UNSUPPORTED;
-    if (!aligned(q8, 16) || !aligned(q_scale, 16) || !aligned(w, 16)) return DSA_ERR_INVALID_ARG;
+    if (!aligned(q8, 16) || !aligned(q_scale, 16) || !aligned(w, 16) || !aligned(work, 8)) return DSA_ERR_INVALID_ARG;
     if (q_group > 64) return DSA_ERR_INVALID_ARG;
     if ((nq + q_group - 1) / q_group > 4096) return DSA_ERR_UNSUPPORTED;  // per-group tables live in smem
     const int n_cols = ((q_group * heads + 15) / 16) * 16;  // M = 128 needs N % 16 == 0
@@ -933,6 +977,7 @@ static dsa_status_t index_scores(int32_t nq, int32_t heads, int32_t dim, const u
     a.q_pos = q_pos;
     a.q_req = q_req;
     a.fresh_pos = fresh_pos;
+    a.work = work;
     a.key_scale = keys->scale;
     a.num_blocks = keys->num_blocks;
     a.bt = *bt;
@@ -957,9 +1002,9 @@ extern "C" dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim,
                                          const float* q_scale, const float* w, const int32_t* q_pos,
                                          const int32_t* q_req, int32_t q_group, const dsa_pool_t* keys,
                                          const dsa_block_table_t* bt, float* scores, int32_t ld, int32_t* n_visible,
-                                         const int32_t* fresh_pos, int32_t* dev_status, void* stream) {
+                                         const int32_t* fresh_pos, uint32_t* work, int32_t* dev_status, void* stream) {
     return index_scores(nq, heads, dim, q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, ld, n_visible,
-                        fresh_pos, dev_status, stream, kWaitLimitNs, 0);
+                        fresh_pos, work, dev_status, stream, kWaitLimitNs, 0);
 }
 
 // Test hook of the bounded waits: the same launch with a caller-chosen wait limit and the copy-issuing warp
@@ -972,28 +1017,28 @@ extern "C" dsa_status_t dsa_debug_index_scores_stalled(int32_t nq, int32_t heads
                                                        void* stream) {
     if (wait_limit_ns == 0 || wait_limit_ns > kWaitLimitNs) return DSA_ERR_INVALID_ARG;
     return index_scores(nq, heads, dim, q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, ld, n_visible,
-                        nullptr, dev_status, stream, wait_limit_ns, 1);
+                        nullptr, nullptr, dev_status, stream, wait_limit_ns, 1);
 }
 
 // Fused indexer + top-k: the indexer counts each row's level-1 histogram while scoring (rows of up to 16,384
 // entries), then the top-k of every row starts its radix select from it (dsa_topk_counted, topk.cu).  The
 // counts are zero-filled by the caller before the first call and cleared again by the top-k of every call that
 // completes.
-extern "C" size_t dsa_index_topk_workspace_size(int32_t nq) {
-    return nq > 0 ? ((size_t)nq * kSelBins * 4 + 255) / 256 * 256 : 0;
-}
+// Workspace of dsa_index_topk: the level-1 counts [nq][2048], then the indexer's work counters [2].
+static size_t counts_bytes(int32_t nq) { return ((size_t)nq * kSelBins * 4 + 255) / 256 * 256; }
+extern "C" size_t dsa_index_topk_workspace_size(int32_t nq) { return nq > 0 ? counts_bytes(nq) + 256 : 0; }
 
 extern "C" dsa_status_t dsa_index_scores_counted(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8,
                                                  const float* q_scale, const float* w, const int32_t* q_pos,
                                                  const int32_t* q_req, int32_t q_group, const dsa_pool_t* keys,
                                                  const dsa_block_table_t* bt, float* scores, int32_t ld,
-                                                 int32_t* n_visible, const int32_t* fresh_pos, unsigned* counts,
-                                                 int32_t* dev_status, void* stream) {
+                                                 int32_t* n_visible, const int32_t* fresh_pos, uint32_t* work,
+                                                 unsigned* counts, int32_t* dev_status, void* stream) {
     if (nq < 0) return DSA_ERR_INVALID_ARG;
     if (nq == 0) return DSA_OK;
     if (!counts || !aligned(counts, 16) || ld > 16384) return DSA_ERR_INVALID_ARG;
     return index_scores(nq, heads, dim, q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, ld, n_visible,
-                        fresh_pos, dev_status, stream, kWaitLimitNs, 0, counts);
+                        fresh_pos, work, dev_status, stream, kWaitLimitNs, 0, counts);
 }
 
 extern "C" dsa_status_t dsa_index_topk(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8, const float* q_scale,
@@ -1004,14 +1049,15 @@ extern "C" dsa_status_t dsa_index_topk(int32_t nq, int32_t heads, int32_t dim, c
     if (nq < 0) return DSA_ERR_INVALID_ARG;
     if (nq == 0) return DSA_OK;
     if (k < 1 || k > 2048 || !idx_out || !n_visible || !aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
-    if (ld > 16384) {  // rows the counted top-k does not hold: the plain indexer and top-k
-        const dsa_status_t r = dsa_index_scores(nq, heads, dim, q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores,
-                                                ld, n_visible, fresh_pos, dev_status, stream);
-        return r != DSA_OK ? r : dsa_topk(nq, scores, ld, n_visible, k, idx_out, dev_status, stream);
-    }
     if (!workspace || workspace_bytes < dsa_index_topk_workspace_size(nq)) return DSA_ERR_INVALID_ARG;
     unsigned* counts = static_cast<unsigned*>(workspace);
+    uint32_t* work = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + counts_bytes(nq));
+    if (ld > 16384) {  // rows the counted top-k does not hold: the plain indexer and top-k
+        const dsa_status_t r = dsa_index_scores(nq, heads, dim, q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores,
+                                                ld, n_visible, fresh_pos, work, dev_status, stream);
+        return r != DSA_OK ? r : dsa_topk(nq, scores, ld, n_visible, k, idx_out, dev_status, stream);
+    }
     const dsa_status_t r = dsa_index_scores_counted(nq, heads, dim, q8, q_scale, w, q_pos, q_req, q_group, keys, bt,
-                                                    scores, ld, n_visible, fresh_pos, counts, dev_status, stream);
+                                                    scores, ld, n_visible, fresh_pos, work, counts, dev_status, stream);
     return r != DSA_OK ? r : dsa_topk_counted(nq, scores, ld, n_visible, k, idx_out, counts, dev_status, stream);
 }

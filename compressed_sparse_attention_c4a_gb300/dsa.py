@@ -47,7 +47,7 @@ class DsaCompressJob(ctypes.Structure):
                 ("state_logit", ctypes.c_void_p), ("rms_gamma", ctypes.c_void_p), ("rms_eps", ctypes.c_float),
                 ("rope", ctypes.POINTER(DsaRope)), ("out", ctypes.POINTER(DsaPool)),
                 ("out_bt", ctypes.POINTER(DsaBlockTable)), ("swa", ctypes.POINTER(DsaPool)),
-                ("swa_bt", ctypes.POINTER(DsaBlockTable))]
+                ("swa_bt", ctypes.POINTER(DsaBlockTable)), ("gate_per_channel", ctypes.c_int32)]
 
 
 class DsaError(RuntimeError):
@@ -73,13 +73,13 @@ _lib.dsa_topk_plan.argtypes = [_I, _I, _I, _P]
 for _name, _args in {
     "dsa_compress": [_I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P],
     "dsa_compress_jobs": [_I, _I, _P, _P, _I, _P, _I, _I, _P, _P, _P],
-    "dsa_index_scores": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P],
+    "dsa_index_scores": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P],
     "dsa_debug_index_scores_stalled": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, ctypes.c_uint64, _P,
                                        _P],
     "dsa_topk": [_I, _P, _I, _P, _I, _P, _P, _P],
     "dsa_index_topk": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _I, _P, _P, ctypes.c_size_t, _P,
                        _P],
-    "dsa_index_scores_counted": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P],
+    "dsa_index_scores_counted": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P],
     "dsa_topk_counted": [_I, _P, _I, _P, _I, _P, _P, _P, _P],
     "dsa_sparse_attn_decode": [_I, _I, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, ctypes.c_float, _P, _P, _P, _P,
                                ctypes.c_size_t, _P, _P],
@@ -151,12 +151,13 @@ def dsa_compress(kind, cu_new, start_pos, max_new, x_new, logit_new, state_x, st
 
 
 def compress_job(x_new, logit_new, state_x, state_logit, rope_cfg, out, out_bt, swa=None, swa_bt=None,
-                 rms_gamma=None, rms_eps=1e-6):
-    """One cache's arguments of dsa_compress_jobs (the struct keeps the rope, pool and table objects alive)."""
+                 rms_gamma=None, rms_eps=1e-6, per_channel=False):
+    """One cache's arguments of dsa_compress_jobs (the struct keeps the rope, pool and table objects alive).
+    per_channel: logits per raw token and channel (logit_new [n][dim], state_logit [slots][w][dim])."""
     return DsaCompressJob(x_new.data_ptr(), logit_new.data_ptr(), state_x.data_ptr(), state_logit.data_ptr(),
                           None if rms_gamma is None else rms_gamma.data_ptr(), float(rms_eps), ctypes.pointer(rope_cfg),
                           ctypes.pointer(out), ctypes.pointer(out_bt), None if swa is None else ctypes.pointer(swa),
-                          None if swa_bt is None else ctypes.pointer(swa_bt))
+                          None if swa_bt is None else ctypes.pointer(swa_bt), 1 if per_channel else 0)
 
 
 def dsa_compress_jobs(kind, cu_new, start_pos, max_new, state_slot, num_slots, jobs, dev_status=None, stream=None):
@@ -167,11 +168,11 @@ def dsa_compress_jobs(kind, cu_new, start_pos, max_new, state_slot, num_slots, j
 
 
 def dsa_index_scores(q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, n_visible=None, dev_status=None,
-                     stream=None, fresh_pos=None):
+                     stream=None, fresh_pos=None, work=None):
     nq, heads, dim = q8.shape
     code = _lib.dsa_index_scores(nq, heads, dim, _ptr(q8), _ptr(q_scale), _ptr(w), _ptr(q_pos), _ptr(q_req),
                                  int(q_group), ctypes.byref(keys), ctypes.byref(bt), _ptr(scores), scores.shape[1],
-                                 _ptr(n_visible), _ptr(fresh_pos), _ptr(dev_status), _stream(stream))
+                                 _ptr(n_visible), _ptr(fresh_pos), _ptr(work), _ptr(dev_status), _stream(stream))
     _check("dsa_index_scores", code)
 
 
@@ -204,12 +205,12 @@ def dsa_index_topk(q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, k, i
 
 
 def dsa_index_scores_counted(q8, q_scale, w, q_pos, q_req, q_group, keys, bt, scores, counts, n_visible=None,
-                             dev_status=None, stream=None, fresh_pos=None):
+                             dev_status=None, stream=None, fresh_pos=None, work=None):
     """dsa_index_scores that also counts each row's level-1 top-k histogram into ``counts`` (zero-filled)."""
     nq, heads, dim = q8.shape
     code = _lib.dsa_index_scores_counted(nq, heads, dim, _ptr(q8), _ptr(q_scale), _ptr(w), _ptr(q_pos), _ptr(q_req),
                                          int(q_group), ctypes.byref(keys), ctypes.byref(bt), _ptr(scores),
-                                         scores.shape[1], _ptr(n_visible), _ptr(fresh_pos), _ptr(counts),
+                                         scores.shape[1], _ptr(n_visible), _ptr(fresh_pos), _ptr(work), _ptr(counts),
                                          _ptr(dev_status), _stream(stream))
     _check("dsa_index_scores_counted", code)
 

@@ -27,7 +27,7 @@ def _query_group(spec, idx_heads):
 class LayerStep:
     """Device-resident state and buffers of one case (a dict from ``synth.make_case`` on cuda)."""
 
-    def __init__(self, case, counted_topk=False, two_streams=False):
+    def __init__(self, case, counted_topk=False, two_streams=False, dynamic_split=False):
         spec = case["spec"]
         self.case, self.spec = case, spec
         dev = case["q"].device
@@ -61,6 +61,8 @@ class LayerStep:
             # this step's compressor starts each request at start_pos: the indexer scores the key pages of
             # entries complete before it while the compressor still runs
             self.fresh_pos = case["start_pos"] if spec.index_compress else None
+            # the indexer's work counter (CTAs take runs of items from it; it is left zero after each call)
+            self.idx_work = torch.zeros((4,), dtype=torch.int32, device=dev)
         self.out = torch.empty((nq, spec.heads, spec.dim), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((nq, spec.heads), dtype=torch.float32, device=dev)
         max_keys = (spec.topk if self.has_index else case["bt_main"].shape[1] * epb) + spec.window
@@ -71,12 +73,29 @@ class LayerStep:
         self.max_new = max(spec.new) if spec.new else 0
         self.jobs = None
         self.two_streams = two_streams
+        # dynamic_split: the indexer's CTAs take part of their work from a counter (idx_work) instead of an equal
+        # static share; off by default (measured slower on the decode batch: more query-group switches)
+        self.dynamic_split = dynamic_split
         self.side = None
 
     # ---- stages ------------------------------------------------------------------------
+    def _jobs(self):
+        if self.jobs is None:
+            c, pc = self.case, self.spec.gate == "channel"
+            self.jobs = [dsa.compress_job(c["x_new"], c["z_new"], c["state_x"], c["state_z"], self.rope_main,
+                                          self.main, self.main_bt, self.swa, self.swa_bt, per_channel=pc)]
+            if self.has_index:
+                self.jobs.append(dsa.compress_job(c["xi_new"], c["zi_new"], c["state_xi"], c["state_zi"],
+                                                  self.rope_idx, self.idx, self.idx_bt, per_channel=pc))
+        return self.jobs
+
     def compress_main(self):
         """Main-cache compressor + SWA insert."""
         c = self.case
+        if self.spec.gate == "channel":  # the one-cache call takes a scalar gate only
+            dsa.dsa_compress_jobs(self.kind, c["cu_new"], c["start_pos"], self.max_new, c["state_slot"],
+                                  c["state_x"].shape[0], self._jobs()[:1], dev_status=self.status)
+            return
         dsa.dsa_compress(self.kind, c["cu_new"], c["start_pos"], self.max_new, c["x_new"], c["z_new"], c["state_x"],
                          c["state_z"], c["state_slot"], self.rope_main, self.main, self.main_bt, self.swa,
                          self.swa_bt, dev_status=self.status)
@@ -84,7 +103,10 @@ class LayerStep:
     def compress_index(self):
         """Indexer-cache compressor (e4m3 or e2m1 keys + scale)."""
         c = self.case
-        if self.has_index and self.spec.index_compress:
+        if self.has_index and self.spec.index_compress and self.spec.gate == "channel":
+            dsa.dsa_compress_jobs(self.kind, c["cu_new"], c["start_pos"], self.max_new, c["state_slot"],
+                                  c["state_x"].shape[0], self._jobs()[1:], dev_status=self.status)
+        elif self.has_index and self.spec.index_compress:
             dsa.dsa_compress(self.kind, c["cu_new"], c["start_pos"], self.max_new, c["xi_new"], c["zi_new"],
                              c["state_xi"], c["state_zi"], c["state_slot"], self.rope_idx, self.idx, self.idx_bt,
                              dev_status=self.status)
@@ -95,13 +117,8 @@ class LayerStep:
         if not (self.has_index and self.spec.index_compress):
             self.compress_main()
             return
-        if self.jobs is None:
-            self.jobs = [dsa.compress_job(c["x_new"], c["z_new"], c["state_x"], c["state_z"], self.rope_main,
-                                          self.main, self.main_bt, self.swa, self.swa_bt),
-                         dsa.compress_job(c["xi_new"], c["zi_new"], c["state_xi"], c["state_zi"], self.rope_idx,
-                                          self.idx, self.idx_bt)]
         dsa.dsa_compress_jobs(self.kind, c["cu_new"], c["start_pos"], self.max_new, c["state_slot"],
-                              c["state_x"].shape[0], self.jobs, dev_status=self.status)
+                              c["state_x"].shape[0], self._jobs(), dev_status=self.status)
 
     def index(self):
         """Indexer scores (counting each row's first top-k digit when the counted top-k follows)."""
@@ -109,11 +126,12 @@ class LayerStep:
         if self.fused_topk:
             dsa.dsa_index_scores_counted(c["q8"], c["q_scale"], c["w"], c["q_pos"], c["q_req"], self.q_group,
                                          self.idx, self.idx_bt, self.scores, self.topk_ws, self.n_visible,
-                                         dev_status=self.status, fresh_pos=self.fresh_pos)
+                                         dev_status=self.status, fresh_pos=self.fresh_pos,
+                                         work=self.idx_work if self.dynamic_split else None)
         else:
             dsa.dsa_index_scores(c["q8"], c["q_scale"], c["w"], c["q_pos"], c["q_req"], self.q_group, self.idx,
                                  self.idx_bt, self.scores, self.n_visible, dev_status=self.status,
-                                 fresh_pos=self.fresh_pos)
+                                 fresh_pos=self.fresh_pos, work=self.idx_work if self.dynamic_split else None)
 
     def select(self):
         """Top-k of every query row (from the indexer's counts when it made them)."""

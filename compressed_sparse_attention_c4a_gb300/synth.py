@@ -12,7 +12,8 @@ U(0, 1)); bf16 values are torch's round-to-nearest of fp32 draws; fp8 codes are
 torch's e4m3 conversion of 64 * N(0, 1) draws with a per-row scale drawn
 U(0.5, 1.5) / 64; fp4 indexer keys are uniformly random bytes (two e2m1 codes each, every code
 equally likely) with a per-row scale drawn U(0.5, 1.5) / 6.  Physical blocks are a seeded permutation of a pool that is about
-12% larger than what the requests need, so tables are shuffled and fragmented.
+12% larger than what the requests need, so tables are shuffled and fragmented.  With the per-channel gate
+the logits are N(0, 1) per raw token and channel.
 """
 from dataclasses import dataclass, field
 import math
@@ -40,6 +41,7 @@ class CaseSpec:
     window: int = 128
     main_dtype: str = "bf16"                            # "bf16" or "fp8"
     idx_dtype: str = "fp8"                              # indexer keys: "fp8" (e4m3) or "fp4" (e2m1, packed)
+    gate: str = "scalar"                                # compressor logits: "scalar" (per raw token) or "channel"
     swa_dtype: str = "bf16"
     index_compress: bool = True                         # run the indexer compressor on the new tokens
     seed: int = 0
@@ -140,11 +142,12 @@ def make_case(spec: CaseSpec, device="cpu"):
 
     # compressor rolling state: slot r holds request r's last w raw tokens (slot = pos mod w)
     out["state_slot"] = torch.arange(B, dtype=torch.int32, device=dev)
+    pc = spec.gate == "channel"
     out["state_x"] = _randn((B, w, D), gen, dev).to(torch.bfloat16)
-    out["state_z"] = _randn((B, w), gen, dev)
+    out["state_z"] = _randn((B, w, D) if pc else (B, w), gen, dev)
     if spec.idx_heads:
         out["state_xi"] = _randn((B, w, spec.idx_dim), gen, dev).to(torch.bfloat16)
-        out["state_zi"] = _randn((B, w), gen, dev)
+        out["state_zi"] = _randn((B, w, spec.idx_dim) if pc else (B, w), gen, dev)
 
     # new raw tokens (un-rotated shared-KV vectors and indexer vectors) with gate logits
     n_new = sum(spec.new)
@@ -154,10 +157,10 @@ def make_case(spec: CaseSpec, device="cpu"):
     out["cu_new"] = torch.tensor(cu, dtype=torch.int32, device=dev)
     out["start_pos"] = torch.tensor(spec.cached, dtype=torch.int32, device=dev)
     out["x_new"] = _randn((n_new, D), gen, dev).to(torch.bfloat16)
-    out["z_new"] = _randn((n_new,), gen, dev)
+    out["z_new"] = _randn((n_new, D) if pc else (n_new,), gen, dev)
     if spec.idx_heads:
         out["xi_new"] = _randn((n_new, spec.idx_dim), gen, dev).to(torch.bfloat16)
-        out["zi_new"] = _randn((n_new,), gen, dev)
+        out["zi_new"] = _randn((n_new, spec.idx_dim) if pc else (n_new,), gen, dev)
 
     # queries
     q_pos, q_req = [], []

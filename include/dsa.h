@@ -154,6 +154,11 @@ typedef struct dsa_compress_job {
     const dsa_block_table_t* out_bt;
     const dsa_pool_t* swa;      /* or NULL */
     const dsa_block_table_t* swa_bt;
+    int32_t gate_per_channel;   /* 0: one logit per raw token (logit_new [n], state_logit [slots][w]);
+                                   1: one per raw token and channel (logit_new [n][dim], state_logit
+                                   [slots][w][dim], both 16-byte aligned), a softmax over the window for every
+                                   channel c: u_c = sum_j softmax_j(z_{., c}) x_{j, c} (a variant: the pages
+                                   say only "weighted sum") */
 } dsa_compress_job_t;
 
 dsa_status_t dsa_compress_jobs(int32_t kind, int32_t batch, const int32_t* cu_new, const int32_t* start_pos,
@@ -186,6 +191,10 @@ dsa_status_t dsa_compress_jobs(int32_t kind, int32_t batch, const int32_t* cu_ne
  *            stream may still be compressing into the key pool (after dsa_compress of this step: its
  *            start_pos[r]); or NULL.  The entries those tokens can complete, i >= n_vis(fresh_pos[r] - 1)
  *            (c4a: 4i + 7 >= fresh_pos[r]), may still be written; older entries may not.
+ * work       NULL (each CTA scores an equal share of the entries), or [2] uint32, 8-byte aligned, zero before the
+ *            first call: the CTAs take runs of consecutive (query group, 128-entry tile) items from this counter,
+ *            so a CTA that starts late (its SM still busy with another kernel) takes less; the last CTA leaves
+ *            it zero again.  Calls that may overlap on the GPU must not share it.
  * Launched with programmatic dependent launch, so the kernel may start before the preceding kernel in
  * the stream has finished.  q_pos, q_req and bt are always read before waiting for it.  Without
  * fresh_pos, keys, queries and every output are touched only after the wait.  With fresh_pos, key pages
@@ -196,7 +205,8 @@ dsa_status_t dsa_compress_jobs(int32_t kind, int32_t batch, const int32_t* cu_ne
 dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8, const float* q_scale,
                               const float* w, const int32_t* q_pos, const int32_t* q_req, int32_t q_group,
                               const dsa_pool_t* keys, const dsa_block_table_t* bt, float* scores, int32_t ld,
-                              int32_t* n_visible, const int32_t* fresh_pos, int32_t* dev_status, void* stream);
+                              int32_t* n_visible, const int32_t* fresh_pos, uint32_t* work, int32_t* dev_status,
+                              void* stream);
 
 /*
  * dsa_index_scores_counted / dsa_topk_counted / dsa_index_topk - the indexer and the per-query top-k with the
@@ -209,8 +219,9 @@ dsa_status_t dsa_index_scores(int32_t nq, int32_t heads, int32_t dim, const uint
  * dsa_topk_counted is dsa_topk for such rows (ld <= 16,384, else DSA_ERR_UNSUPPORTED) that starts from those
  * counts: the bucket of the k-th largest score comes from them, so the top-k reads its row once; it selects
  * the same set, in the same order, as dsa_topk and leaves the counts zero-filled again.
- * dsa_index_topk issues the two (for ld > 16,384: dsa_index_scores then dsa_topk), with the counts in
- * `workspace` (>= dsa_index_topk_workspace_size(nq) bytes): zero-filled by the caller before the first call;
+ * dsa_index_topk issues the two (for ld > 16,384: dsa_index_scores then dsa_topk), with the counts and the
+ * indexer's work counter in `workspace` (>= dsa_index_topk_workspace_size(nq) bytes): zero-filled by the caller
+ * before the first call;
  * every call that completes leaves it zero-filled (one that records DSA_ERR_TIMEOUT may not: clear it then).
  * Calls that overlap on the GPU race on it.
  *
@@ -221,7 +232,7 @@ size_t dsa_index_topk_workspace_size(int32_t nq);
 dsa_status_t dsa_index_scores_counted(int32_t nq, int32_t heads, int32_t dim, const uint8_t* q8, const float* q_scale,
                                       const float* w, const int32_t* q_pos, const int32_t* q_req, int32_t q_group,
                                       const dsa_pool_t* keys, const dsa_block_table_t* bt, float* scores, int32_t ld,
-                                      int32_t* n_visible, const int32_t* fresh_pos, unsigned* counts,
+                                      int32_t* n_visible, const int32_t* fresh_pos, uint32_t* work, unsigned* counts,
                                       int32_t* dev_status, void* stream);
 dsa_status_t dsa_topk_counted(int32_t nq, const float* scores, int32_t ld, const int32_t* n_valid, int32_t k,
                               int32_t* idx_out, unsigned* counts, int32_t* dev_status, void* stream);

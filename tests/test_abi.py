@@ -51,9 +51,9 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.dsa_topk(0, None, 64, None, 8, None, None, None) == 0          # empty: a no-op
     # indexer: unsupported head count / dim
     lib.dsa_index_scores.argtypes = [ctypes.c_int32] * 3 + [P] * 5 + [ctypes.c_int32, P, P, P, ctypes.c_int32, P, P,
-                                                                       P, P]
-    assert lib.dsa_index_scores(1, 5, 128, *[P(16)] * 5, 1, P(16), P(16), P(16), 64, None, None, None, None) == 2
-    assert lib.dsa_index_scores(1, 8, 96, *[P(16)] * 5, 1, P(16), P(16), P(16), 64, None, None, None, None) == 2
+                                                                       P, P, P]
+    assert lib.dsa_index_scores(1, 5, 128, *[P(16)] * 5, 1, P(16), P(16), P(16), 64, None, None, None, None, None) == 2
+    assert lib.dsa_index_scores(1, 8, 96, *[P(16)] * 5, 1, P(16), P(16), P(16), 64, None, None, None, None, None) == 2
     # compress: bad kind, null pointers
     lib.dsa_compress.restype = ctypes.c_int32
     args = [ctypes.c_int32(7), ctypes.c_int32(1)] + [None] * 18
@@ -136,12 +136,12 @@ def test_fp4_pool_checks_host_only(lib):
     bt = dsa.DsaBlockTable(64, 1, 4)
     scale = 256
     fn = lib.dsa_index_scores
-    fn.argtypes = [ctypes.c_int32] * 3 + [P] * 5 + [ctypes.c_int32, P, P, P, ctypes.c_int32, P, P, P, P]
+    fn.argtypes = [ctypes.c_int32] * 3 + [P] * 5 + [ctypes.c_int32, P, P, P, ctypes.c_int32, P, P, P, P, P]
 
     def index(dim, base, dtype=dsa.DSA_FP4_E2M1):
         keys = dsa.DsaPool(base, scale, 4, 64, dim, dtype)
         return fn(1, 8, dim, *[P(16)] * 5, 1, ctypes.cast(ctypes.pointer(keys), P), ctypes.cast(ctypes.pointer(bt), P),
-                  P(16), 64, None, None, None, None)
+                  P(16), 64, None, None, None, None, None)
 
     assert index(64, 32) == dsa.DSA_ERR_UNSUPPORTED                  # fp4 keys: dim 128 only
     assert index(128, 48) == dsa.DSA_ERR_INVALID_ARG                 # 16- but not 32-byte aligned

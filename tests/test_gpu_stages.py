@@ -44,6 +44,11 @@ CASES = {
     "c4a_decode_fp4": S("c4a_decode_fp4", cached=[1000, 2999, 777, 4095, 130], new=[1] * 5, idx_dtype="fp4",
                         seed=22),
     "c4a_chunk_fp4": S("c4a_chunk_fp4", cached=[1037, 64], new=[300, 75], queries="all", idx_dtype="fp4", seed=23),
+    # per-channel compressor gate (one logit per raw token and channel), decode, chunk (ring + chunk) and c128a
+    "c4a_decode_pc": S("c4a_decode_pc", cached=[1000, 2999, 777, 6], new=[1] * 4, gate="channel", seed=24),
+    "c4a_chunk_pc": S("c4a_chunk_pc", cached=[1037, 3], new=[300, 40], queries="all", gate="channel", seed=25),
+    "c128a_chunk_pc": S("c128a_chunk_pc", kind="c128a", cached=[300, 64], new=[200, 130], queries="all", idx_heads=0,
+                        topk=0, gate="channel", seed=26),
 }
 INDEXED = [n for n, s in CASES.items() if s.idx_heads]
 
@@ -139,7 +144,8 @@ def test_compress_indexer(name):
         assert np.array_equal(gx[int(np64(cpu["state_slot"])[r])], states[r].x)
 
 
-@pytest.mark.parametrize("name", ["c4a_decode", "c4a_chunk", "c4a_early", "c4a_decode_fp4", "c4a_multi_prefill"])
+@pytest.mark.parametrize("name", ["c4a_decode", "c4a_chunk", "c4a_early", "c4a_decode_fp4", "c4a_multi_prefill",
+                                  "c4a_chunk_pc"])
 def test_compress_jobs_equal_separate_calls(name):
     """dsa_compress_jobs (main cache + window insert and the indexer cache in one launch) writes the same bytes
     to every pool, window row and rolling state as one dsa_compress call per cache."""
@@ -443,6 +449,33 @@ def test_index_scores_fresh_pos(name):
         assert np.array_equal(runs[1][q, :n], runs[0][q, :n]), q
         assert np.array_equal(runs[2][q, :n], runs[0][q, :n]), q
         assert np.array_equal(runs[3][q, :n], runs[0][q, :n]), q
+
+
+@pytest.mark.parametrize("name", ["c4a_decode", "c4a_multi_prefill", "c4a_decode_fp4", "c4a_chunk"])
+def test_index_work_counter_same_scores_and_left_zero(name):
+    """With a work counter the CTAs take runs of items dynamically: the scores equal those of the static
+    split bit for bit, and each call leaves the counter zero (three calls in a row)."""
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    cpu, gpu, step = _setup(name)
+    step.compress()
+    torch.cuda.synchronize()
+    c = step.case
+    work = torch.zeros((4,), dtype=torch.int32, device="cuda")
+    runs = []
+    for wk in (None, work, work, work):
+        scores = torch.full_like(step.scores, float("nan"))
+        dsa.dsa_index_scores(c["q8"], c["q_scale"], c["w"], c["q_pos"], c["q_req"], step.q_group, step.idx,
+                             step.idx_bt, scores, step.n_visible, dev_status=step.status, fresh_pos=step.fresh_pos,
+                             work=wk)
+        torch.cuda.synchronize()
+        assert int(step.status.item()) == 0
+        assert int(work.count_nonzero().item()) == 0
+        runs.append(np64(scores))
+    nv = np64(step.n_visible)
+    for q in range(cpu["nq"]):
+        n = int(nv[q])
+        for r in runs[1:]:
+            assert np.array_equal(r[q, :n], runs[0][q, :n]), q
 
 
 # ---- device-detected faults: a needed block unmapped (-1) in one request's table ---------------------
