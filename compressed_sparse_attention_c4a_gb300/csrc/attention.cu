@@ -824,6 +824,9 @@ __global__ void __launch_bounds__(kClThreads, 1)
     if (tid == 0) DSA_STAMP(19);
     __syncthreads();
     if (tid == 0) DSA_STAMP(11);
+    // this CTA's first owned tile leaves TMEM while the other CTAs' tiles are still arriving
+    float v_first[G];
+    if (have) tmem_cols(crank, v_first);
     if (csize > 1) {
         ok = mbar_wait_bounded(xfull, 0, kWaitLimitNs);
         if (!ok && tid == 0) report(a.status, DSA_ERR_TIMEOUT);
@@ -850,7 +853,14 @@ __global__ void __launch_bounds__(kClThreads, 1)
         const int t = crank + csize * j;
         const int D = t * 128 + d;
         float v[G];
-        if (have) tmem_cols(t, v);
+        if (have) {
+            if (j == 0) {
+#pragma unroll
+                for (int e = 0; e < G; ++e) v[e] = v_first[e];
+            } else {
+                tmem_cols(t, v);
+            }
+        }
         if (tid == 0 && j == 0) DSA_STAMP(20);
 #pragma unroll
         for (int e = 0; e < G; ++e) v[e] = have ? v[e] * fown[e] : 0.f;

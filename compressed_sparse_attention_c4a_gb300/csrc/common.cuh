@@ -32,6 +32,15 @@ inline dsa_status_t launch_status() {
     return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
+// Every kernel asks for the largest shared-memory carveout: an SM changes its shared-memory / L1 split only
+// when it is idle, so a kernel launched with a small carveout (little shared memory) would leave SMs on which
+// the next kernel's large CTAs fit once at a time, the second starting only when the first ends.
+template <typename... Exp>
+inline void prefer_max_shared(void (*kernel)(Exp...)) {
+    cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel), cudaFuncAttributePreferredSharedMemoryCarveout,
+                         (int)cudaSharedmemCarveoutMaxShared);
+}
+
 // As launch_pdl, in clusters of `cluster` CTAs along x (grid.x a multiple of it).
 template <typename... Exp, typename... Act>
 inline cudaError_t launch_pdl_cluster(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
@@ -50,6 +59,7 @@ inline cudaError_t launch_pdl_cluster(void (*kernel)(Exp...), dim3 grid, dim3 bl
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
+    prefer_max_shared(kernel);
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...);
 }
 
@@ -66,6 +76,7 @@ inline cudaError_t launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, siz
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    prefer_max_shared(kernel);
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...);
 }
 

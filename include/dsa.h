@@ -273,8 +273,10 @@ dsa_status_t dsa_topk(int32_t nq, const float* scores, int32_t ld, const int32_t
 
 /*
  * dsa_topk_plan - how dsa_topk runs for these sizes on the current device; host only, launches nothing.
- * plan[0] = kernel (0: one CTA per row with the row in registers, for ld <= 16,384; 1: a cluster of
- * CTAs per row, each holding one part of the row), plan[1] = CTAs per row, plan[2] = threads per CTA.
+ * plan[0] = kernel (0: the row in registers, for ld <= 16,384: one CTA of 1024 threads per row, or, while
+ * four CTAs per row fit on the GPU at once, a cluster of four 512-thread CTAs holding a quarter each; 1: a
+ * cluster of CTAs per row, each holding one part of the row in shared memory), plan[1] = CTAs per row,
+ * plan[2] = threads per CTA.
  * Returns DSA_ERR_INVALID_ARG / DSA_ERR_UNSUPPORTED as dsa_topk would for these sizes.
  */
 dsa_status_t dsa_topk_plan(int32_t nq, int32_t ld, int32_t k, int32_t* plan);

@@ -88,7 +88,8 @@ def test_topk_plan_host_only(lib):
     """The top-k dispatch is host arithmetic: valid without a GPU (the SM count falls back to a default of
     148, so 296 cluster CTAs are resident at once)."""
     from compressed_sparse_attention_c4a_gb300 import dsa
-    assert dsa.dsa_topk_plan(32, 16384, 512) == (0, 1, 1024)      # decode rows: registers, one CTA each
+    assert dsa.dsa_topk_plan(32, 16384, 512) == (0, 4, 512)       # few short rows: a 4-CTA cluster each
+    assert dsa.dsa_topk_plan(100, 16384, 512) == (0, 1, 1024)     # many short rows: one CTA each
     assert dsa.dsa_topk_plan(200, 34816, 512) == (1, 1, 512)      # many long rows: one CTA per row
     assert dsa.dsa_topk_plan(120, 34816, 512) == (1, 2, 512)      # fewer rows: spread over two SMs
     assert dsa.dsa_topk_plan(16, 65536, 512) == (1, 4, 512)       # a row past 40,960 needs two parts at least

@@ -401,6 +401,31 @@ def test_topk_many_rows_exact():
         assert list(got[i]) == list(OL.topk(scores[i].astype(np.float64), int(nv[i]), k)), i
 
 
+@pytest.mark.parametrize("ld", [1004, 6004, 12292, 16384])
+def test_topk_short_rows_on_a_cluster_exact(ld):
+    """Few short rows run on a cluster of four CTAs, a quarter of the row each (parts that hold no visible
+    score included): random rows, heavy ties across the quarters, rows of one repeated value, and random
+    lengths, against the oracle's top-k index for index."""
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    assert dsa.dsa_topk_plan(40, ld, 512) == (0, 4, 512)
+    rng = np.random.default_rng(ld + 1)
+    nq, k = 40, 512
+    scores = rng.standard_normal((nq, ld)).astype(np.float32)
+    scores[1::4] = np.round(scores[1::4] * 3)                    # heavy ties (radix select)
+    scores[2::8] = 0.25                                          # one value (take the lowest indices)
+    scores[3::8, ld // 2:] = -np.inf
+    nv = rng.integers(0, ld + 1, nq).astype(np.int32)
+    nv[::3] = ld
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty((nq, k), dtype=torch.int32, device="cuda")
+    dsa.dsa_topk(torch.from_numpy(scores).cuda(), torch.from_numpy(nv).cuda(), k, out, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = out.cpu().numpy()
+    for i in range(nq):
+        assert list(got[i]) == list(OL.topk(scores[i].astype(np.float64), int(nv[i]), k)), i
+
+
 @pytest.mark.parametrize("nq,ld", [(200, 34816), (120, 20004), (16, 65536)])
 def test_topk_long_rows_cluster_sizes_exact(nq, ld):
     """Rows longer than 16,384 scores at row counts that give clusters of 1 (200 rows), 2 (120 rows) and
