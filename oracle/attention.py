@@ -49,6 +49,22 @@ def sparse_attention(q, keys, m, rope_dim, sm_scale, theta=ROPE_THETA, inverse_r
     return o, lse
 
 
+def query_prep(q_raw, m, rope_dim, gamma=None, eps=1e-6, theta=ROPE_THETA):
+    """The query of the attention from its raw projection ([P2] 融合点 3: Q-norm, done beside the key RoPE and
+    insert): q_raw [..., H, d] at position m; every head's row is RMS-normalised,
+    v_h = gamma * q_h / sqrt(mean(q_h^2) + eps), then rotated by R_m on the last rope_dim dims (the attention
+    takes its queries rotated at their position, reading 4 of the attention above).
+
+    Reading (the pages name the Q-norm only): the compressor's RMSNorm (gamma = 1, eps = 1e-6 unless given)
+    and the rotation at the query's own position.
+    """
+    q = np.asarray(q_raw, dtype=np.float64)
+    v = q / np.sqrt(np.mean(q * q, axis=-1, keepdims=True) + eps)
+    if gamma is not None:
+        v = v * np.asarray(gamma, dtype=np.float64)
+    return rope(v, m, rope_dim, theta)
+
+
 def quantize_output(o, block=OUT_Q8_BLOCK):
     """The fp8 form of an attention output ([P2] 融合点 2: the inverse-rotated output is quantised to fp8 for
     the o_lora projection that follows).  o [..., d] float64 (after R_m^-1); every `block` consecutive dims of a

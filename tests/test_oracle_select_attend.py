@@ -232,3 +232,52 @@ def test_sparse_attn_q8_is_the_quantised_sparse_attn():
     codes, scales = q8[0]
     want_c, want_s = quantize_output(out[0])
     assert np.array_equal(codes, want_c) and np.array_equal(scales, want_s)
+
+
+# ---- query prep ([P2] 融合点 3: the Q-norm beside the key RoPE and insert) ----------------------------------
+
+def test_query_prep_brute_force():
+    """Per head: divide by sqrt(mean(q^2) + eps), then rotate each pair of the last rope_dim dims by m * f_j,
+    written with scalar loops on a tiny case."""
+    import math
+    from oracle.attention import query_prep
+    from oracle.rope import inv_freq
+    rng = np.random.default_rng(31)
+    q = rng.standard_normal((2, 8))
+    m, rd, eps = 37, 4, 1e-6
+    f = inv_freq(rd)
+    want = np.zeros_like(q)
+    for h in range(2):
+        ms = sum(float(x) * float(x) for x in q[h]) / 8
+        v = [float(x) / math.sqrt(ms + eps) for x in q[h]]
+        for j in range(rd // 2):
+            a = m * f[j]
+            i0 = 8 - rd + 2 * j
+            x0, x1 = v[i0], v[i0 + 1]
+            v[i0], v[i0 + 1] = x0 * math.cos(a) - x1 * math.sin(a), x0 * math.sin(a) + x1 * math.cos(a)
+        want[h] = v
+    assert np.allclose(query_prep(q, m, rd), want, rtol=1e-12, atol=1e-13)
+
+
+def test_query_prep_norm_scale_invariance_and_gamma():
+    from oracle.attention import query_prep
+    rng = np.random.default_rng(32)
+    q = rng.standard_normal((64, 512)) * 3.0
+    out = query_prep(q, 1000, 64, eps=0.0)
+    assert np.allclose(np.sqrt(np.mean(out * out, axis=-1)), 1.0, atol=1e-12)     # the rotation keeps the RMS
+    assert np.allclose(query_prep(7.5 * q, 1000, 64, eps=0.0), out, atol=1e-12)   # a scale drops out
+    assert np.allclose(query_prep(q, 1000, 64, gamma=np.full(512, 2.0), eps=0.0), 2.0 * out, atol=1e-12)
+
+
+def test_query_prep_scores_depend_on_relative_position():
+    """<query_prep(q, m), R_n k> depends on m - n only (the query is rotated at its own position)."""
+    from oracle.attention import query_prep
+    from oracle.rope import rope
+    rng = np.random.default_rng(33)
+    q = rng.standard_normal((4, 64))
+    k = rng.standard_normal(64)
+    s1 = query_prep(q, 500, 32) @ rope(k, 480, 32)
+    s2 = query_prep(q, 90500, 32) @ rope(k, 90480, 32)
+    s3 = query_prep(q, 500, 32) @ rope(k, 470, 32)
+    assert np.allclose(s1, s2, atol=1e-9)
+    assert not np.allclose(s1, s3, atol=1e-3)                                     # negative control
