@@ -347,24 +347,92 @@ __device__ __forceinline__ void compress_item(const CompressArgs& a, int item, i
 
 constexpr int kMaxJobs = 4;
 
-// The jobs of one launch: the caches of one layer that compress the same tokens of the same requests
-// (main cache with its window insert, indexer cache), each its own rows, norm, RoPE and pool.
-struct CompressJobs {
-    CompressArgs job[kMaxJobs];
-    int n_jobs;
+// The query job of a launch: each (query, head) row of the raw queries RMS-normalised and rotated at the
+// query's position ([P2] 融合点 3: the Q-norm beside the key RoPE and insert).
+struct QueryArgs {
+    int nq, heads, dim;
+    const uint16_t* q_raw;
+    uint16_t* q_out;
+    const int32_t* q_pos;
+    const float* gamma;
+    float eps;
+    RopeTable rope;
+    int32_t* status;
 };
 
-// Grid (warp blocks, 1, job): blockIdx.z picks the job, so the caches of a layer compress side by side in
-// one launch ([P2] 融合点 3: independent per-token work of one layer dispatched by warp index in one kernel).
-// The (request, item) pairs of a job are dealt to consecutive warps, so a decode batch (two items per
-// request) fills few CTAs and leaves the other SMs to the kernel that follows.
+// The jobs of one launch: the caches of one layer that compress the same tokens of the same requests
+// (main cache with its window insert, indexer cache), each its own rows, norm, RoPE and pool, and optionally
+// the layer's queries.  Job k takes CTAs [cta_off[k], cta_off[k + 1]); the query job is job n_jobs.
+struct CompressJobs {
+    CompressArgs job[kMaxJobs];
+    QueryArgs query;
+    int n_jobs, has_query;
+    int cta_off[kMaxJobs + 2];
+};
+
+// One warp's (query, head) row: q / sqrt(mean(q^2) + eps) * gamma, then R_m on the last rope_dim dims, as
+// bf16.  The position is read before waiting for the preceding kernel, the raw row after it.
+template <int DIM>
+__device__ __forceinline__ void query_item(const QueryArgs& a, long long wi, int lane) {
+    constexpr int E = DIM / 32;
+    const long long q = wi / a.heads;
+    const bool live = q < a.nq;
+    const int m = live ? __ldg(a.q_pos + q) : 0;
+    float gam[E];
+#pragma unroll
+    for (int k = 0; k < E; ++k) gam[k] = a.gamma ? __ldg(a.gamma + lane * E + k) : 1.f;
+    pdl_wait();
+    pdl_launch_dependents();
+    if (!live) return;
+    if (m < 0) {
+        if (lane == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
+        return;
+    }
+    float v[E];
+    load_bf16<E>(a.q_raw + wi * DIM, lane, v);
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < E; ++k) ss = fmaf(v[k], v[k], ss);
+    ss = warp_sum(ss);
+    const float rs = rsqrtf(ss / (float)DIM + a.eps);
+#pragma unroll
+    for (int k = 0; k < E; ++k) v[k] *= rs * gam[k];
+    rope_row<E>(v, lane, DIM, a.rope, m);
+    uint16_t* dst = a.q_out + wi * DIM + lane * E;
+#pragma unroll
+    for (int k = 0; k < E; k += 8) {
+        uint4 u;
+        u.x = (uint32_t)float_to_bf16(v[k]) | ((uint32_t)float_to_bf16(v[k + 1]) << 16);
+        u.y = E > k + 2 ? ((uint32_t)float_to_bf16(v[k + 2]) | ((uint32_t)float_to_bf16(v[k + 3]) << 16)) : 0u;
+        u.z = E > k + 4 ? ((uint32_t)float_to_bf16(v[k + 4]) | ((uint32_t)float_to_bf16(v[k + 5]) << 16)) : 0u;
+        u.w = E > k + 6 ? ((uint32_t)float_to_bf16(v[k + 6]) | ((uint32_t)float_to_bf16(v[k + 7]) << 16)) : 0u;
+        if constexpr (E >= 8) *reinterpret_cast<uint4*>(dst + k) = u;
+        else if constexpr (E == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(u.x, u.y);
+        else *reinterpret_cast<uint32_t*>(dst) = u.x;
+    }
+}
+
+// Grid: the CTAs of every job side by side along x (job k from cta_off[k]), so the caches of a layer (and its
+// queries) are processed in one launch ([P2] 融合点 3: independent per-token work of one layer dispatched by
+// warp and block index in one kernel).  The (request, item) pairs of a job are dealt to consecutive warps, so
+// a decode batch (two items per request) fills few CTAs and leaves the other SMs to the kernel that follows.
 template <int W>
 __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ CompressJobs js) {
-    const CompressArgs& a = js.job[blockIdx.z];
+    int k = 0;
+    while (k < js.n_jobs + js.has_query - 1 && (int)blockIdx.x >= js.cta_off[k + 1]) ++k;
     const int lane = threadIdx.x & 31;
+    const long long wi = (long long)(blockIdx.x - js.cta_off[k]) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (k == js.n_jobs) {  // the query job
+        switch (js.query.dim) {
+            case 64: query_item<64>(js.query, wi, lane); break;
+            case 128: query_item<128>(js.query, wi, lane); break;
+            default: query_item<512>(js.query, wi, lane); break;
+        }
+        return;
+    }
+    const CompressArgs& a = js.job[k];
     const int per_req = a.entry_items + a.token_items;
-    const int wi = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int r = wi / per_req, item = wi - r * per_req;
+    const int r = (int)(wi / per_req), item = (int)(wi - (long long)r * per_req);
     if (r >= a.batch) {  // no work; the grid still ends after the preceding kernel
         pdl_wait();
         pdl_launch_dependents();
@@ -407,15 +475,25 @@ __global__ void __launch_bounds__(256) ring_update_kernel(const __grid_constant_
     }
 }
 
-static dsa_status_t launch_compress(const CompressJobs& js, int w, int batch, int max_new, cudaStream_t st) {
-    long long warps = 0;
-    for (int k = 0; k < js.n_jobs; ++k)
-        warps = std::max(warps, (long long)batch * (js.job[k].entry_items + js.job[k].token_items));
-    // small grids (decode) in CTAs of 2 warps: they fit beside two CTAs of the indexer that follows on an SM,
-    // which 8-warp CTAs do not (each SM quarter has its own registers)
-    const int wpc = warps * js.n_jobs <= 4LL * sm_count() ? 2 : 8;
-    if ((warps + wpc - 1) / wpc > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
-    dim3 grid((unsigned)((warps + wpc - 1) / wpc), 1, js.n_jobs);
+static dsa_status_t launch_compress(CompressJobs js, int w, int batch, int max_new, cudaStream_t st) {
+    long long warps[kMaxJobs + 1], comp = 0;
+    for (int k = 0; k < js.n_jobs; ++k) {
+        warps[k] = (long long)batch * (js.job[k].entry_items + js.job[k].token_items);
+        comp += warps[k];
+    }
+    if (js.has_query) warps[js.n_jobs] = (long long)js.query.nq * js.query.heads;
+    // small compressor grids (decode) in CTAs of 2 warps: they fit beside two CTAs of the indexer that follows
+    // on an SM, which 8-warp CTAs do not (each SM quarter has its own registers)
+    const int wpc = comp <= 4LL * sm_count() ? 2 : 8;
+    long long off = 0;
+    for (int k = 0; k < js.n_jobs + js.has_query; ++k) {
+        js.cta_off[k] = (int)off;
+        off += (warps[k] + wpc - 1) / wpc;
+        if (off > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
+    }
+    js.cta_off[js.n_jobs + js.has_query] = (int)off;
+    if (off == 0) return DSA_OK;
+    dim3 grid((unsigned)off);
     cudaError_t e = w == 8 ? launch_pdl(compress_kernel<8>, grid, dim3(32 * wpc), 0, st, js)
                            : launch_pdl(compress_kernel<128>, grid, dim3(32 * wpc), 0, st, js);
     if (e == cudaSuccess && !js.job[0].fuse_ring && max_new > 0)
@@ -475,17 +553,49 @@ static dsa_status_t make_job(int batch, int max_new, int w, int s, const void* x
     return DSA_OK;
 }
 
+static dsa_status_t make_query(const dsa_query_job_t* q, QueryArgs* a) {
+    if (q->nq < 0 || q->heads < 1) return DSA_ERR_INVALID_ARG;
+    if (q->dim != 64 && q->dim != 128 && q->dim != 512) return DSA_ERR_UNSUPPORTED;
+    if (q->nq > 0 && (!q->q_raw || !q->q_out || !q->q_pos || !q->rope)) return DSA_ERR_INVALID_ARG;
+    if (!aligned(q->q_raw, 16) || !aligned(q->q_out, 16) || !(q->rms_eps > 0.f)) return DSA_ERR_INVALID_ARG;
+    if (q->rope && (q->rope->rope_dim < 0 || q->rope->rope_dim > q->dim || (q->rope->rope_dim & 1) ||
+                    !(q->rope->theta > 0.0)))
+        return DSA_ERR_INVALID_ARG;
+    if (q->rope && q->rope->rope_dim > 64) return DSA_ERR_UNSUPPORTED;
+    a->nq = q->nq;
+    a->heads = q->heads;
+    a->dim = q->dim;
+    a->q_raw = static_cast<const uint16_t*>(q->q_raw);
+    a->q_out = static_cast<uint16_t*>(q->q_out);
+    a->q_pos = q->q_pos;
+    a->gamma = q->rms_gamma;
+    a->eps = q->rms_eps;
+    if (q->rope) a->rope = make_rope_table(q->rope->rope_dim, q->rope->theta);
+    return DSA_OK;
+}
+
 static dsa_status_t compress_jobs(int32_t kind, int32_t batch, const int32_t* cu_new, const int32_t* start_pos,
                                   int32_t max_new, const int32_t* state_slot, int32_t num_slots, int32_t n_jobs,
-                                  const dsa_compress_job_t* jobs, int32_t* dev_status, void* stream) {
+                                  const dsa_compress_job_t* jobs, const dsa_query_job_t* query, int32_t* dev_status,
+                                  void* stream) {
     if (kind != DSA_C4A && kind != DSA_C128A) return DSA_ERR_INVALID_ARG;
     if (batch < 0 || max_new < 0 || num_slots <= 0) return DSA_ERR_INVALID_ARG;
     if (n_jobs < 1 || n_jobs > kMaxJobs || !jobs) return DSA_ERR_INVALID_ARG;
-    if (batch == 0 || max_new == 0) return DSA_OK;
-    if (!cu_new || !start_pos || !state_slot) return DSA_ERR_INVALID_ARG;
     const int w = window_of(kind), s = stride_of(kind);
     CompressJobs js{};
     js.n_jobs = n_jobs;
+    if (query) {
+        const dsa_status_t e = make_query(query, &js.query);
+        if (e != DSA_OK) return e;
+        js.query.status = dev_status;
+        js.has_query = query->nq > 0;
+    }
+    if ((batch == 0 || max_new == 0) && !js.has_query) return DSA_OK;
+    if (batch > 0 && max_new > 0 && (!cu_new || !start_pos || !state_slot)) return DSA_ERR_INVALID_ARG;
+    if (batch == 0 || max_new == 0) {  // only the queries: no compressor work
+        js.n_jobs = 0;
+        return launch_compress(js, w, 0, 0, static_cast<cudaStream_t>(stream));
+    }
     for (int k = 0; k < n_jobs; ++k) {
         const dsa_compress_job_t& j = jobs[k];
         const dsa_status_t e = make_job(batch, max_new, w, s, j.x_new, j.logit_new, j.state_x, j.state_logit,
@@ -513,13 +623,14 @@ extern "C" dsa_status_t dsa_compress(int32_t kind, int32_t batch, const int32_t*
     if (batch == 0 || max_new == 0) return DSA_OK;
     const dsa_compress_job_t job{x_new, logit_new, state_x, state_logit, rms_gamma, rms_eps, rope, out, out_bt, swa,
                                  swa_bt, 0};
-    return compress_jobs(kind, batch, cu_new, start_pos, max_new, state_slot, num_slots, 1, &job, dev_status, stream);
+    return compress_jobs(kind, batch, cu_new, start_pos, max_new, state_slot, num_slots, 1, &job, nullptr, dev_status,
+                         stream);
 }
 
 extern "C" dsa_status_t dsa_compress_jobs(int32_t kind, int32_t batch, const int32_t* cu_new,
                                           const int32_t* start_pos, int32_t max_new, const int32_t* state_slot,
                                           int32_t num_slots, int32_t n_jobs, const dsa_compress_job_t* jobs,
-                                          int32_t* dev_status, void* stream) {
-    return compress_jobs(kind, batch, cu_new, start_pos, max_new, state_slot, num_slots, n_jobs, jobs, dev_status,
-                         stream);
+                                          const dsa_query_job_t* query, int32_t* dev_status, void* stream) {
+    return compress_jobs(kind, batch, cu_new, start_pos, max_new, state_slot, num_slots, n_jobs, jobs, query,
+                         dev_status, stream);
 }

@@ -50,6 +50,12 @@ class DsaCompressJob(ctypes.Structure):
                 ("swa_bt", ctypes.POINTER(DsaBlockTable)), ("gate_per_channel", ctypes.c_int32)]
 
 
+class DsaQueryJob(ctypes.Structure):
+    _fields_ = [("nq", ctypes.c_int32), ("heads", ctypes.c_int32), ("dim", ctypes.c_int32), ("q_raw", ctypes.c_void_p),
+                ("q_out", ctypes.c_void_p), ("q_pos", ctypes.c_void_p), ("rms_gamma", ctypes.c_void_p),
+                ("rms_eps", ctypes.c_float), ("rope", ctypes.POINTER(DsaRope))]
+
+
 class DsaError(RuntimeError):
     def __init__(self, fn, code):
         super().__init__(f"{fn}: {dsa_status_string(code)} ({code})")
@@ -72,7 +78,7 @@ _lib.dsa_topk_plan.restype = ctypes.c_int32
 _lib.dsa_topk_plan.argtypes = [_I, _I, _I, _P]
 for _name, _args in {
     "dsa_compress": [_I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P],
-    "dsa_compress_jobs": [_I, _I, _P, _P, _I, _P, _I, _I, _P, _P, _P],
+    "dsa_compress_jobs": [_I, _I, _P, _P, _I, _P, _I, _I, _P, _P, _P, _P],
     "dsa_index_scores": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P],
     "dsa_debug_index_scores_stalled": [_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, ctypes.c_uint64, _P,
                                        _P],
@@ -160,10 +166,19 @@ def compress_job(x_new, logit_new, state_x, state_logit, rope_cfg, out, out_bt, 
                           None if swa_bt is None else ctypes.pointer(swa_bt), 1 if per_channel else 0)
 
 
-def dsa_compress_jobs(kind, cu_new, start_pos, max_new, state_slot, num_slots, jobs, dev_status=None, stream=None):
-    arr = (DsaCompressJob * len(jobs))(*jobs)
+def query_job(q_raw, q_out, q_pos, rope_cfg, rms_gamma=None, rms_eps=1e-6):
+    """The query job of dsa_compress_jobs: q_raw, q_out [nq][heads][dim] bf16 (q_out may be q_raw)."""
+    nq, heads, dim = q_raw.shape
+    return DsaQueryJob(nq, heads, dim, q_raw.data_ptr(), q_out.data_ptr(), q_pos.data_ptr(),
+                       None if rms_gamma is None else rms_gamma.data_ptr(), float(rms_eps), ctypes.pointer(rope_cfg))
+
+
+def dsa_compress_jobs(kind, cu_new, start_pos, max_new, state_slot, num_slots, jobs, dev_status=None, stream=None,
+                      query=None):
+    arr = (DsaCompressJob * len(jobs))(*jobs) if jobs else None
     code = _lib.dsa_compress_jobs(KIND.get(kind, kind), start_pos.numel(), _ptr(cu_new), _ptr(start_pos), int(max_new),
-                                  _ptr(state_slot), int(num_slots), len(jobs), arr, _ptr(dev_status), _stream(stream))
+                                  _ptr(state_slot), int(num_slots), len(jobs), arr,
+                                  None if query is None else ctypes.byref(query), _ptr(dev_status), _stream(stream))
     _check("dsa_compress_jobs", code)
 
 

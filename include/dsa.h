@@ -161,9 +161,33 @@ typedef struct dsa_compress_job {
                                    say only "weighted sum") */
 } dsa_compress_job_t;
 
+/*
+ * The query job of dsa_compress_jobs ([P2] 融合点 3: the Q-norm beside the key RoPE and insert): every
+ * (query, head) row of q_raw becomes q_out = R_m(gamma * q / sqrt(mean(q^2) + eps)), m = q_pos[query], the
+ * rotation on the last rope_dim dims, as bf16 (the queries dsa_sparse_attn_* take, rotated at their
+ * position).  q_raw, q_out: [nq][heads][dim] bf16, 16-byte aligned (q_out may be q_raw); q_pos [nq] int32
+ * (read before waiting for the preceding kernel; a negative position raises DSA_ERR_DEVICE_FAULT and leaves
+ * that row); rms_gamma [dim] fp32 or NULL (ones); rms_eps > 0; dim in {64, 128, 512}; rope_dim even,
+ * <= min(dim, 64).  nq = 0 is no work.
+ */
+typedef struct dsa_query_job {
+    int32_t nq;
+    int32_t heads;
+    int32_t dim;
+    const void* q_raw;
+    void* q_out;
+    const int32_t* q_pos;
+    const float* rms_gamma;
+    float rms_eps;
+    const dsa_rope_t* rope;
+} dsa_query_job_t;
+
+/* query: NULL, or the layer's queries, prepared in the same launch by warps of their own (batch or max_new may
+ * then be 0: the queries alone). */
 dsa_status_t dsa_compress_jobs(int32_t kind, int32_t batch, const int32_t* cu_new, const int32_t* start_pos,
                                int32_t max_new, const int32_t* state_slot, int32_t num_slots, int32_t n_jobs,
-                               const dsa_compress_job_t* jobs, int32_t* dev_status, void* stream);
+                               const dsa_compress_job_t* jobs, const dsa_query_job_t* query, int32_t* dev_status,
+                               void* stream);
 
 /*
  * dsa_index_scores - lightning-indexer scores of each query against every visible

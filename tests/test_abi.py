@@ -167,6 +167,17 @@ def test_compress_rejects_rope_beyond_its_table_host_only(lib):
     t = torch.zeros(16)
     job = dsa.compress_job(t, t, t, t, rope, out, bt)
     arr = (dsa.DsaCompressJob * 1)(job)
-    assert dsa._lib.dsa_compress_jobs(0, 1, P(16), P(16), 1, P(16), 4, 1, arr, None, None) == dsa.DSA_ERR_UNSUPPORTED
-    assert dsa._lib.dsa_compress_jobs(0, 1, P(16), P(16), 1, P(16), 4, 5, arr, None, None) == dsa.DSA_ERR_INVALID_ARG
-    assert dsa._lib.dsa_compress_jobs(0, 1, P(16), P(16), 1, P(16), 4, 0, arr, None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert dsa._lib.dsa_compress_jobs(0, 1, P(16), P(16), 1, P(16), 4, 1, arr, None, None, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert dsa._lib.dsa_compress_jobs(0, 1, P(16), P(16), 1, P(16), 4, 5, arr, None, None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert dsa._lib.dsa_compress_jobs(0, 1, P(16), P(16), 1, P(16), 4, 0, arr, None, None, None) == dsa.DSA_ERR_INVALID_ARG
+    # a query job: rope_dim beyond the table, a dim the kernels do not take
+    tq = torch.zeros((2, 4, 128), dtype=torch.bfloat16)
+    pos = torch.zeros(2, dtype=torch.int32)
+    qj = dsa.query_job(tq, tq, pos, rope)
+    ok_job = (dsa.DsaCompressJob * 1)(dsa.compress_job(t, t, t, t, dsa.DsaRope(64, 1e4), out, bt))
+    assert dsa._lib.dsa_compress_jobs(0, 1, P(16), P(16), 1, P(16), 4, 1, ok_job, ctypes.byref(qj), None,
+                                      None) == dsa.DSA_ERR_UNSUPPORTED
+    qj.dim = 96
+    qj.rope = ctypes.pointer(dsa.DsaRope(64, 1e4))
+    assert dsa._lib.dsa_compress_jobs(0, 1, P(16), P(16), 1, P(16), 4, 1, ok_job, ctypes.byref(qj), None,
+                                      None) == dsa.DSA_ERR_UNSUPPORTED

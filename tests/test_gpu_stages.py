@@ -167,6 +167,48 @@ def test_compress_jobs_equal_separate_calls(name):
         assert torch.equal(outs[0][k], outs[1][k]), k
 
 
+@pytest.mark.parametrize("name", ["c4a_decode", "c4a_multi_prefill", "c128a_early"])
+def test_query_job_matches_oracle(name):
+    """The query job of the compressor launch ([P2] 融合点 3): every (query, head) row is the oracle's
+    query_prep (RMSNorm, then R_m) within bf16 rounding, in place or not; the compressor's outputs are those of
+    the launch without it, bit for bit; and the queries alone (no compressor work) are accepted."""
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    cpu = synth.make_case(CASES[name], "cpu")
+    spec = cpu["spec"]
+    g = torch.Generator().manual_seed(99)
+    q_raw = (torch.randn(cpu["q"].shape, generator=g) * 3.0).to(torch.bfloat16)
+    want = OA.query_prep(np64(q_raw), np64(cpu["q_pos"])[:, None], spec.rope_dim)
+    outs = []
+    for mode in ("without", "with", "in_place"):
+        gpu = to_device(cpu)
+        step = LayerStep(gpu)
+        jobs = step._jobs()
+        qr = q_raw.cuda()
+        qo = qr if mode == "in_place" else torch.empty_like(qr)
+        qj = dsa.query_job(qr, qo, gpu["q_pos"], step.rope_main) if mode != "without" else None
+        dsa.dsa_compress_jobs(step.kind, gpu["cu_new"], gpu["start_pos"], step.max_new, gpu["state_slot"],
+                              gpu["state_x"].shape[0], jobs, dev_status=step.status, query=qj)
+        torch.cuda.synchronize()
+        assert int(step.status.item()) == 0
+        outs.append(({k: gpu[k].cpu() for k in ("main_data", "swa_data", "state_x", "state_z")}, qo.cpu()))
+    for k in outs[0][0]:
+        assert torch.equal(outs[0][0][k], outs[1][0][k]) and torch.equal(outs[0][0][k], outs[2][0][k]), k
+    assert torch.equal(outs[1][1], outs[2][1])
+    got = np64(outs[1][1]).reshape(-1, spec.dim)
+    check_rows(got, want.reshape(-1, spec.dim))
+    assert np.max(np.abs(got - want.reshape(-1, spec.dim))) <= 2e-2
+    # the queries alone
+    gpu = to_device(cpu)
+    step = LayerStep(gpu)
+    qo = torch.empty_like(q_raw).cuda()
+    dsa.dsa_compress_jobs(step.kind, gpu["cu_new"], gpu["start_pos"], 0, gpu["state_slot"], gpu["state_x"].shape[0],
+                          step._jobs(), dev_status=step.status, query=dsa.query_job(q_raw.cuda(), qo, gpu["q_pos"],
+                                                                                     step.rope_main))
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    assert torch.equal(qo.cpu(), outs[1][1])
+
+
 def _oracle_scores_on_gpu_pool(cpu, gpu):
     pool = idx_pool(gpu)
     return OL.index_scores(np64(cpu["q8"]), np64(cpu["q_scale"]), np64(cpu["w"]), np64(cpu["q_pos"]),
