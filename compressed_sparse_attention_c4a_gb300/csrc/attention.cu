@@ -50,6 +50,9 @@ struct AttnArgs {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 template <int N>
@@ -208,6 +211,7 @@ struct ClSmem {
     static constexpr int kBytes = kOffBar + kBars * 8 + 16;
     static constexpr int kAlloc = kBytes + 1024;                    // + alignment slack
     static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
+    static_assert(kOffKsc % 16 == 0, "the row scales are read as float4");
     static constexpr int kTile = 128 * NH * 2;                      // one exchanged 128-dim O tile: [NH / 4][128] x 4 bf16
     static_assert(3 * kTile <= kQ, "the sent tiles fit in the query rows");
     static_assert(6 * kTile <= kQ + kClStages * kClStage, "the received tiles fit after them");
@@ -409,16 +413,60 @@ __global__ void __launch_bounds__(kClThreads, 1)
             const int j = key_id(R, &id);
             finish_key(R, j, id);
         };
+        // e4m3 codes of a landed sub-tile -> bf16 in the same stage, exactly (e4m3 -> fp16 -> fp32 -> bf16 loses
+        // nothing); every gather thread reads its rows' codes before any writes, since the bf16 rows overwrite
+        // the codes' half of the stage.  Called by all gather threads alike.
+        auto widen_fp8 = [&](int st) {
+            constexpr int kRowsPerWarp = (kClKeys + kClGatherWarps - 1) / kClGatherWarps;
+            const uint32_t stage = sK + st * kClStage;
+            const uint8_t* raw = smem + L::kOffK + st * kClStage + kClStage / 2;
+            named_bar_sync(1, kClGatherThreads);  // every thread's copies of the sub-tile have landed
+            uint4 code[kRowsPerWarp];
+#pragma unroll
+            for (int u = 0; u < kRowsPerWarp; ++u) {
+                const int kk = gw + u * kClGatherWarps;
+                code[u] = kk < kClKeys ? *reinterpret_cast<const uint4*>(raw + kk * kD + lane * 16) : make_uint4(0, 0, 0, 0);
+            }
+            named_bar_sync(1, kClGatherThreads);  // all codes read: the bf16 rows may overwrite them
+#pragma unroll
+            for (int u = 0; u < kRowsPerWarp; ++u) {
+                const int kk = gw + u * kClGatherWarps;
+                if (kk < kClKeys) {
+                    const uint32_t w4[4] = {code[u].x, code[u].y, code[u].z, code[u].w};
+                    uint32_t bf[8];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                        for (int hlf = 0; hlf < 2; ++hlf) {
+                            const __half2_raw h2 =
+                                __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[q] >> (16 * hlf)), __NV_E4M3);
+                            const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+                            bf[2 * q + hlf] = pack_bf16(f2.x, f2.y);
+                        }
+                    }
+                    const int d0 = 16 * lane;
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + sw128_offset(kk, d0, kClKeys * 128)),
+                                 "r"(bf[0]), "r"(bf[1]), "r"(bf[2]), "r"(bf[3])
+                                 : "memory");
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + sw128_offset(kk, d0 + 8, kClKeys * 128)),
+                                 "r"(bf[4]), "r"(bf[5]), "r"(bf[6]), "r"(bf[7])
+                                 : "memory");
+                }
+            }
+        };
         if (n_mine > 0) resolve_round(0);
         int sig = 0;  // first sub-tile whose stage this thread has not yet reported full
         for (int i = 0; i < n_mine; ++i) {
             const int s = i % kClStages;
             if (i >= kClStages) {
                 // before waiting for a stage, report every sub-tile issued so far (never hold landed rows back)
-                if (!FP8 && sig < i) {
+                if (sig < i) {
                     cp_async_wait_all();
-                    fence_proxy_async_smem();  // cp.async writes -> visible to the tensor core (async proxy)
-                    for (; sig < i; ++sig) mbar_arrive(&full[sig % kClStages]);
+                    for (; sig < i; ++sig) {
+                        if constexpr (FP8) widen_fp8(sig % kClStages);
+                        fence_proxy_async_smem();  // cp.async writes -> visible to the tensor core (async proxy)
+                        mbar_arrive(&full[sig % kClStages]);
+                    }
                 }
                 // the stage's previous sub-tile has been multiplied into O^T
                 ok = ok && mbar_wait_bounded(&pvdone[s], ((i - kClStages) / kClStages) & 1, kWaitLimitNs);
@@ -445,51 +493,22 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 }
             }
             if (ok && FP8) {
-                // e4m3 rows: lane l holds codes of dims 16 l .. 16 l + 15 (one 16-byte load per row); every
-                // row of this warp is loaded first, then the codes become bf16 (exactly: e4m3 -> fp16 -> fp32 ->
-                // bf16 loses nothing) in the swizzled stage; the row scale goes beside the stage
+                // e4m3 rows: copied as they are into the upper half of the stage (row kk at 16 KB + 512 kk, lane
+                // l the codes of dims 16 l .. 16 l + 15), the row scale beside the stage; they become bf16 in
+                // place once they have landed (widen_fp8 below), so copies of three sub-tiles stay in flight
                 constexpr int kRowsPerWarp = (kClKeys + kClGatherWarps - 1) / kClGatherWarps;
-                const uint32_t stage = sK + s * kClStage;
-                uint4 code[kRowsPerWarp];
-                float ksc = 0.f;
+                const uint32_t raw = sK + s * kClStage + kClStage / 2;
 #pragma unroll
                 for (int u = 0; u < kRowsPerWarp; ++u) {
                     const int kk = gw + u * kClGatherWarps;
-                    code[u] = make_uint4(0, 0, 0, 0);
                     if (kk < kClKeys) {
                         const int rr = rows[kk];
                         const dsa_pool_t& pl = pools[kk] == 2 ? a.swa : a.main;
-                        if (rr >= 0) {
-                            code[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(pl.data) +
-                                                                           (long long)rr * kD) + lane);
-                            if (lane == u) ksc = __ldg(pl.scale + rr);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kRowsPerWarp; ++u) {
-                    const int kk = gw + u * kClGatherWarps;
-                    if (kk < kClKeys) {
-                        const uint32_t w4[4] = {code[u].x, code[u].y, code[u].z, code[u].w};
-                        uint32_t bf[8];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-#pragma unroll
-                            for (int hlf = 0; hlf < 2; ++hlf) {
-                                const __half2_raw h2 =
-                                    __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[q] >> (16 * hlf)), __NV_E4M3);
-                                const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-                                bf[2 * q + hlf] = pack_bf16(f2.x, f2.y);
-                            }
-                        }
-                        const int d0 = 16 * lane;
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + sw128_offset(kk, d0, kClKeys * 128)),
-                                     "r"(bf[0]), "r"(bf[1]), "r"(bf[2]), "r"(bf[3])
-                                     : "memory");
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + sw128_offset(kk, d0 + 8, kClKeys * 128)),
-                                     "r"(bf[4]), "r"(bf[5]), "r"(bf[6]), "r"(bf[7])
-                                     : "memory");
-                        if (lane == u) s_ksc[s * kClKeys + kk] = rows[kk] >= 0 ? ksc : 0.f;
+                        const uint8_t* src = static_cast<const uint8_t*>(pl.data) + (rr >= 0 ? (long long)rr * kD : 0);
+                        cp_async16(raw + kk * kD + lane * 16, src + lane * 16, rr >= 0 ? 16u : 0u);
+                        if (lane == 0)
+                            cp_async4(smem_u32(s_ksc + s * kClKeys + kk), rr >= 0 ? pl.scale + rr : pl.scale,
+                                      rr >= 0 ? 4u : 0u);
                     }
                 }
             }
@@ -514,21 +533,21 @@ __global__ void __launch_bounds__(kClThreads, 1)
             if (i % kClRound == 2) resolve_round(i / kClRound + 1);
             // a thread keeps up to three sub-tiles of copies in flight: with three outstanding, the oldest is
             // reported once its group has landed
-            if constexpr (FP8) {  // this thread's converted rows are in the stage
-                fence_proxy_async_smem();
-                mbar_arrive(&full[s]);
-                sig = i + 1;
-            } else if (i - sig >= 2) {
+            if (i - sig >= 2) {
                 cp_async_wait_group<2>();
+                if constexpr (FP8) widen_fp8(sig % kClStages);
                 fence_proxy_async_smem();
                 mbar_arrive(&full[sig % kClStages]);
                 ++sig;
             }
         }
-        if (!FP8 && sig < n_mine) {  // the sub-tiles not yet reported
+        if (sig < n_mine) {  // the sub-tiles not yet reported
             cp_async_wait_all();
-            fence_proxy_async_smem();
-            for (; sig < n_mine; ++sig) mbar_arrive(&full[sig % kClStages]);
+            for (; sig < n_mine; ++sig) {
+                if constexpr (FP8) widen_fp8(sig % kClStages);
+                fence_proxy_async_smem();
+                mbar_arrive(&full[sig % kClStages]);
+            }
         }
         if (!ok) report(a.status, DSA_ERR_TIMEOUT);
     } else if (warp >= 4) {
@@ -633,11 +652,19 @@ __global__ void __launch_bounds__(kClThreads, 1)
                         mx = fmaxf(mx, sv[j]);
                     }
                 } else {
+                    const float4* k4 = reinterpret_cast<const float4*>(s_ksc + st * kClKeys);  // e4m3 row scales
 #pragma unroll
-                    for (int j = 0; j < kClKeys; ++j) {
-                        const float ls = FP8 ? a.scale_log2 * s_ksc[st * kClKeys + j] : a.scale_log2;  // e4m3: times the row scale
-                        sv[j] = ((vm >> j) & 1) ? sv[j] * ls : -INFINITY;
-                        mx = fmaxf(mx, sv[j]);
+                    for (int j4 = 0; j4 < kClKeys; j4 += 4) {
+                        float4 ks = make_float4(1.f, 1.f, 1.f, 1.f);
+                        if constexpr (FP8) ks = k4[j4 / 4];
+                        const float kv[4] = {ks.x, ks.y, ks.z, ks.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = j4 + e;
+                            const float ls = FP8 ? a.scale_log2 * kv[e] : a.scale_log2;  // e4m3: times the row scale
+                            sv[j] = ((vm >> j) & 1) ? sv[j] * ls : -INFINITY;
+                            mx = fmaxf(mx, sv[j]);
+                        }
                     }
                 }
                 if (mx > m_run + kLazyLog2) {  // also the first finite maximum (m_run = -inf)
@@ -651,13 +678,20 @@ __global__ void __launch_bounds__(kClThreads, 1)
 #pragma unroll
                 for (int c = 0; c < kClKeys / 8; ++c) {
                     uint32_t w[4];
+                    float kc[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+                    if constexpr (FP8) {  // the eight row scales of this chunk
+                        const float4* k4 = reinterpret_cast<const float4*>(s_ksc + st * kClKeys + 8 * c);
+                        const float4 ka = k4[0], kb = k4[1];
+                        kc[0] = ka.x, kc[1] = ka.y, kc[2] = ka.z, kc[3] = ka.w, kc[4] = kb.x, kc[5] = kb.y, kc[6] = kb.z,
+                        kc[7] = kb.w;
+                    }
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float p0 = ex2_sfu(sv[8 * c + 2 * e] - mr), p1 = ex2_sfu(sv[8 * c + 2 * e + 1] - mr);
                         esum += p0 + p1;
                         if constexpr (FP8) {  // the probability that multiplies the codes carries the row scale
                             sum += p0 + p1;
-                            w[e] = bf16x2_rn(p0 * s_ksc[st * kClKeys + 8 * c + 2 * e], p1 * s_ksc[st * kClKeys + 8 * c + 2 * e + 1]);
+                            w[e] = bf16x2_rn(p0 * kc[2 * e], p1 * kc[2 * e + 1]);
                         } else {
                             w[e] = bf16x2_rn(p0, p1);
                             sum += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xFFFF0000u);

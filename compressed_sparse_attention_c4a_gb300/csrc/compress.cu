@@ -36,6 +36,8 @@ struct CompressArgs {
     int token_items;  // warps per request reserved for new tokens
     int fuse_ring;    // token warps also update the rolling state (at most one new token per request)
     int gate_pc;      // per-channel gate: logits [n][dim] and rolling logits [slots][w][dim]
+    int nsub;         // warps per entry (kSplit for the c128a window with a scalar gate, else 1)
+    int req_items;    // warps per request: entry_items * nsub + token_items, rounded up to whole CTAs
     int32_t* status;
 };
 
@@ -184,8 +186,13 @@ __device__ __forceinline__ void rope_row(float (&v)[E], int lane, int dim, const
 // (cu_new, start_pos, state_slot), the destination rows' block-table entries and the norm weights are read
 // before waiting for the preceding kernel in the stream; raw tokens, logits and the rolling state after it.
 // Every thread reaches the wait exactly once.
+// Warps per entry of a 128-token window (c128a, scalar gate): eight warps of one CTA each sum 16 of the rows,
+// warp 0 adds the partial sums in shared memory.
+constexpr int kSplit = 8;
+
 template <int DIM, int W>
-__device__ __forceinline__ void compress_item(const CompressArgs& a, int item, int r, int lane) {
+__device__ __forceinline__ void compress_item(const CompressArgs& a, int item, int r, int lane, int sub = 0,
+                                              float* part = nullptr) {
     constexpr int E = DIM / 32;
     constexpr int w = W;
     const int s = a.s;
@@ -291,9 +298,15 @@ __device__ __forceinline__ void compress_item(const CompressArgs& a, int item, i
         const float inv_den = 1.f / den;
 #pragma unroll
         for (int k = 0; k < E; ++k) acc[k] = 0.f;
+        // this warp's window rows (a 128-token window may be split over kSplit warps)
+        const int j_lo = W == 128 ? sub * (W / a.nsub) : 0, j_hi = W == 128 ? j_lo + W / a.nsub : W;
+        if (j_lo > 0) {
+#pragma unroll
+            for (int u = 0; u < RB; ++u) load_bf16<E>(row_at(base + j_lo + u), lane, x[u]);
+        }
 #pragma unroll 1
-        for (int j0 = 0; j0 < W; j0 += RB) {
-            if (j0 > 0) {
+        for (int j0 = j_lo; j0 < j_hi; j0 += RB) {
+            if (j0 > j_lo) {
 #pragma unroll
                 for (int u = 0; u < RB; ++u) load_bf16<E>(row_at(base + j0 + u), lane, x[u]);
             }
@@ -303,6 +316,18 @@ __device__ __forceinline__ void compress_item(const CompressArgs& a, int item, i
                 const float g = __shfl_sync(0xffffffffu, z[jj / 32 < LPL ? jj / 32 : 0], jj & 31) * inv_den;
 #pragma unroll
                 for (int k = 0; k < E; ++k) acc[k] = fmaf(g, x[u][k], acc[k]);
+            }
+        }
+        if (W == 128 && a.nsub > 1) {  // the CTA's warps are this entry's: warp 0 adds their partial sums
+#pragma unroll
+            for (int k = 0; k < E; ++k) part[sub * DIM + lane * E + k] = acc[k];
+            __syncthreads();
+            if (sub != 0) return;
+#pragma unroll
+            for (int k = 0; k < E; ++k) {
+                float t = 0.f;
+                for (int q = 0; q < a.nsub; ++q) t += part[q * DIM + lane * E + k];
+                acc[k] = t;
             }
         }
         }
@@ -431,17 +456,26 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
         return;
     }
     const CompressArgs& a = js.job[k];
-    const int per_req = a.entry_items + a.token_items;
-    const int r = (int)(wi / per_req), item = (int)(wi - (long long)r * per_req);
-    if (r >= a.batch) {  // no work; the grid still ends after the preceding kernel
+    const int per_req = a.req_items;
+    const int r = (int)(wi / per_req), it = (int)(wi - (long long)r * per_req);
+    // items [0, entry_items * nsub) are entries (nsub consecutive warps each, one CTA when nsub > 1), then tokens
+    const int split_items = a.entry_items * a.nsub;
+    const int item = it < split_items ? it / a.nsub : a.entry_items + (it - split_items);
+    const int sub = it < split_items ? it % a.nsub : 0;
+    if (r >= a.batch || (it >= split_items && it - split_items >= a.token_items)) {  // no work
         pdl_wait();
         pdl_launch_dependents();
         return;
     }
+    float* part = nullptr;
+    if constexpr (W == 128) {
+        __shared__ float s_part[kSplit * 512];  // the partial window sums of a split entry
+        part = s_part;
+    }
     switch (a.dim) {
-        case 64: compress_item<64, W>(a, item, r, lane); break;
-        case 128: compress_item<128, W>(a, item, r, lane); break;
-        default: compress_item<512, W>(a, item, r, lane); break;
+        case 64: compress_item<64, W>(a, item, r, lane, sub, part); break;
+        case 128: compress_item<128, W>(a, item, r, lane, sub, part); break;
+        default: compress_item<512, W>(a, item, r, lane, sub, part); break;
     }
 }
 
@@ -477,14 +511,20 @@ __global__ void __launch_bounds__(256) ring_update_kernel(const __grid_constant_
 
 static dsa_status_t launch_compress(CompressJobs js, int w, int batch, int max_new, cudaStream_t st) {
     long long warps[kMaxJobs + 1], comp = 0;
+    bool split = false;
     for (int k = 0; k < js.n_jobs; ++k) {
-        warps[k] = (long long)batch * (js.job[k].entry_items + js.job[k].token_items);
-        comp += warps[k];
+        split |= js.job[k].nsub > 1;
+        comp += (long long)batch * (js.job[k].entry_items * js.job[k].nsub + js.job[k].token_items);
+    }
+    // small compressor grids (decode) in CTAs of 2 warps: they fit beside two CTAs of the indexer that follows
+    // on an SM, which 8-warp CTAs do not (each SM quarter has its own registers); split entries take whole CTAs
+    const int wpc = split ? kSplit : (comp <= 4LL * sm_count() ? 2 : 8);
+    for (int k = 0; k < js.n_jobs; ++k) {
+        CompressArgs& a = js.job[k];
+        a.req_items = (a.entry_items * a.nsub + a.token_items + wpc - 1) / wpc * wpc;
+        warps[k] = (long long)batch * a.req_items;
     }
     if (js.has_query) warps[js.n_jobs] = (long long)js.query.nq * js.query.heads;
-    // small compressor grids (decode) in CTAs of 2 warps: they fit beside two CTAs of the indexer that follows
-    // on an SM, which 8-warp CTAs do not (each SM quarter has its own registers)
-    const int wpc = comp <= 4LL * sm_count() ? 2 : 8;
     long long off = 0;
     for (int k = 0; k < js.n_jobs + js.has_query; ++k) {
         js.cta_off[k] = (int)off;
@@ -549,6 +589,7 @@ static dsa_status_t make_job(int batch, int max_new, int w, int s, const void* x
     }
     a->entry_items = max_new / s + 1;
     a->token_items = max_new;
+    a->nsub = (w == 128 && !gate_pc) ? kSplit : 1;
     a->fuse_ring = max_new <= 1;
     return DSA_OK;
 }
