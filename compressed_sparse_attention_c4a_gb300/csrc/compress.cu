@@ -14,6 +14,8 @@
 
 namespace dsa {
 
+DSA_TIMELINE_BUFFER
+
 struct CompressArgs {
     int w, s, batch, dim;
     const int32_t* cu_new;
@@ -224,6 +226,7 @@ __device__ __forceinline__ void compress_item(const CompressArgs& a, int item, i
     }
     pdl_wait();
     pdl_launch_dependents();
+    if (threadIdx.x == 0) DSA_STAMP(1);
     if (bad_req) {
         if (item == 0 && lane == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
         return;
@@ -443,6 +446,10 @@ __device__ __forceinline__ void query_item(const QueryArgs& a, long long wi, int
 // a decode batch (two items per request) fills few CTAs and leaves the other SMs to the kernel that follows.
 template <int W>
 __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ CompressJobs js) {
+    if (threadIdx.x == 0) {
+        DSA_STAMP_NS(31);
+        DSA_STAMP(0);
+    }
     int k = 0;
     while (k < js.n_jobs + js.has_query - 1 && (int)blockIdx.x >= js.cta_off[k + 1]) ++k;
     const int lane = threadIdx.x & 31;
@@ -465,6 +472,7 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
     if (r >= a.batch || (it >= split_items && it - split_items >= a.token_items)) {  // no work
         pdl_wait();
         pdl_launch_dependents();
+        if (lane == 0) DSA_STAMP_NS(30);
         return;
     }
     float* part = nullptr;
@@ -477,6 +485,7 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
         case 128: compress_item<128, W>(a, item, r, lane, sub, part); break;
         default: compress_item<512, W>(a, item, r, lane, sub, part); break;
     }
+    if (lane == 0) DSA_STAMP_NS(30);  // (timeline builds) the last warp to finish sets the CTA's end
 }
 
 // Rolling-state update after a multi-token append: slot p % w <- token p for the last w new tokens.
@@ -545,6 +554,8 @@ static dsa_status_t launch_compress(CompressJobs js, int w, int batch, int max_n
 }  // namespace dsa
 
 using namespace dsa;
+
+DSA_TIMELINE_SETTER(dsa_timeline_compress)
 
 // Checks one job's arguments and fills its kernel arguments (the request schedule is set by the caller).
 static dsa_status_t make_job(int batch, int max_new, int w, int s, const void* x_new, const float* logit_new,

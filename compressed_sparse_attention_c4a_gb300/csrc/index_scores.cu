@@ -361,6 +361,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
             if (valid) locate(idx, &g, &t);
             return item_info<TPI>(a, valid, g, t, grp_r, grp_mv);
         };
+        const uint64_t key_policy = l2_evict_first();  // every key page is read once
         int n = 0, ps = 0, pphase = 0;  // items issued; stage index and its phase parity
         int pb = 0, pbph = 0;           // item slot index and its phase parity
         int cur_g = -1, gb = 1, guse[2] = {0, 0};  // group in the current buffer, buffer index, loads per buffer
@@ -481,7 +482,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
 #pragma unroll
                     for (int p = 1; p < kPages; ++p)
                         if (lane == p) bp = it.blk[p];
-                    if (bp >= 0) tma_load_2d(st + lane * kPage * DIM, &kmap, 0, bp * kPage, &full[s]);
+                    if (bp >= 0) tma_load_2d_hint(st + lane * kPage * DIM, &kmap, 0, bp * kPage, &full[s], key_policy);
                 }
                 alive = __shfl_sync(0xffffffffu, alive, 0);
                 if (!alive) break;
@@ -503,6 +504,7 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
         if (!waited) {  // the kernel ends after the preceding kernel, whatever it read
             pdl_wait();
             pdl_launch_dependents();
+            if (lane == 0) DSA_STAMP(17);
         }
         if (!a.withhold) {  // terminal item: consumers stop here (no bytes; 33 slot arrivals, 1 stage arrival)
             const int s = ps, b = pb;

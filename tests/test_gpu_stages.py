@@ -11,7 +11,7 @@ import torch
 from compressed_sparse_attention_c4a_gb300 import synth
 from compressed_sparse_attention_c4a_gb300.step import LayerStep, SM_SCALE
 from oracle import layer as OL, attention as OA
-from _parity import (ATTN_MAX_ABS, ATTN_REL_L2, ROW_REL_L2, np64, rel_l2, to_device, oracle_pool, idx_pool,
+from _parity import (ATTN_REL_L2, assert_attn_close, attn_bound, pool_absmax, ROW_REL_L2, np64, rel_l2, to_device, oracle_pool, idx_pool,
                      rolling_states,
                      new_tokens, pool_rows, topk_sets_match, check_rows, check_pool_rows)
 
@@ -303,8 +303,7 @@ def test_attention(name):
                                np64(cpu["bt_main"]), swa, np64(cpu["bt_swa"]), spec.window, SM_SCALE, spec.rope_dim)
     got, glse = np64(step.out), np64(step.lse)
     W = np.stack([want[q] for q in range(cpu["nq"])])
-    assert np.max(np.abs(got - W)) <= ATTN_MAX_ABS
-    assert rel_l2(got, W) <= ATTN_REL_L2
+    assert_attn_close(got, W, pool_absmax((gpu["main_data"], gpu["main_scale"]), (gpu["swa_data"], gpu["swa_scale"])))
     assert np.max(np.abs(glse - np.stack([lse[q] for q in range(cpu["nq"])]))) <= 1e-3
 
 
@@ -340,8 +339,7 @@ def test_attention_sharp_scores(name):
                                np64(cpu["bt_main"]), swa, np64(cpu["bt_swa"]), spec.window, SM_SCALE, spec.rope_dim)
     got, glse = np64(step.out), np64(step.lse)
     W = np.stack([want[q] for q in range(cpu["nq"])])
-    assert np.max(np.abs(got - W)) <= ATTN_MAX_ABS
-    assert rel_l2(got, W) <= ATTN_REL_L2
+    assert_attn_close(got, W, pool_absmax((gpu["main_data"], gpu["main_scale"]), (gpu["swa_data"], gpu["swa_scale"])))
     L = np.stack([lse[q] for q in range(cpu["nq"])])
     assert np.max(np.abs(glse - L) / np.maximum(1.0, np.abs(L))) <= 1e-4
 
@@ -668,8 +666,7 @@ def test_attention_unmapped_block_zeroes_the_row(name):
     want, wl = OL.sparse_attn(np64(cpu["q"]), np64(cpu["q_pos"]), np64(cpu["q_req"]), spec.kind, tk, main, bt_main0,
                               swa, bt_swa0, spec.window, SM_SCALE, spec.rope_dim, rows=rows)
     W = np.stack([want[q] for q in rows])
-    assert np.max(np.abs(out[rows] - W)) <= ATTN_MAX_ABS
-    assert rel_l2(out[rows], W) <= ATTN_REL_L2
+    assert_attn_close(out[rows], W, pool_absmax((gpu["main_data"], gpu["main_scale"]), (gpu["swa_data"], gpu["swa_scale"])))
     assert np.max(np.abs(lse[rows] - np.stack([wl[q] for q in rows]))) <= 1e-3
 
 
@@ -794,7 +791,8 @@ def test_attention_fp8_output(name):
                               np64(step.topk) if step.has_index else None, main, np64(cpu["bt_main"]), swa,
                               np64(cpu["bt_swa"]), spec.window, SM_SCALE, spec.rope_dim)
     W = np.stack([want[q] for q in range(nq)])
-    bound = np.abs(W) * 2.0 ** -4 + np.repeat(sg, 128, axis=-1) * 2.0 ** -10 + ATTN_MAX_ABS
+    vmax = pool_absmax((gpu["main_data"], gpu["main_scale"]), (gpu["swa_data"], gpu["swa_scale"]))
+    bound = np.abs(W) * 2.0 ** -4 + np.repeat(sg, 128, axis=-1) * 2.0 ** -10 + attn_bound(W, vmax)
     assert np.all(np.abs(deq - W) <= bound)
     for q in range(nq):
         assert rel_l2(deq[q], W[q]) <= 2.0 ** -4 + ATTN_REL_L2, q

@@ -3,7 +3,9 @@ fails, and a value on a rounding midpoint accepts either neighbour (the only lat
 import numpy as np
 
 from oracle.codecs import fp8_quantize_rows, e4m3_decode, e4m3_encode
-from _parity import fp8_row_violations, e4m3_half_spacing, check_rows
+import torch
+
+from _parity import fp8_row_violations, e4m3_half_spacing, check_rows, pool_absmax, attn_bound, assert_attn_close
 
 
 def test_half_spacing_matches_the_grid():
@@ -68,3 +70,41 @@ def test_check_rows_is_per_row():
         assert e.args[0][1] == 17
     else:
         raise AssertionError("a 5% row error passed the per-row check")
+
+
+def test_pool_absmax_equals_the_decoded_maximum():
+    """e4m3 magnitudes grow with a code's low 7 bits, so the largest low-7-bit code of a row decodes to the
+    row's largest magnitude; checked against decoding every code."""
+    mags = np.abs(e4m3_decode(np.arange(0x7F, dtype=np.uint8)))
+    assert np.all(np.diff(mags) > 0)
+    rng = np.random.default_rng(5)
+    codes = rng.integers(0, 256, (50, 64), dtype=np.uint8)
+    codes[codes & 0x7F == 0x7F] = 0x10                      # no NaN codes in a pool
+    scale = rng.uniform(0.5, 1.5, 50)
+    want = float(np.max(np.abs(e4m3_decode(codes) * scale[:, None])))
+    assert pool_absmax((torch.from_numpy(codes), torch.from_numpy(scale))) == want
+    bf = torch.from_numpy(rng.standard_normal((30, 8))).to(torch.bfloat16)
+    assert pool_absmax((bf, None), (torch.from_numpy(codes), torch.from_numpy(scale))) == max(
+        want, float(bf.float().abs().max()))
+
+
+def test_attention_bound_catches_a_wrong_weight():
+    """An output off by one key's weight error of a few percent fails the element bound; rounding-sized
+    perturbations of the weights pass."""
+    rng = np.random.default_rng(6)
+    v = rng.standard_normal((640, 512))
+    p = rng.uniform(0, 1, 640)
+    w = p / p.sum()
+    o = w @ v
+    vmax = np.abs(v).max()
+    wr = p * (1 + rng.uniform(-2.0 ** -9, 2.0 ** -9, 640))
+    assert_attn_close(wr / wr.sum() @ v, o, vmax)            # bf16-sized weight errors pass
+    bad = p.copy()
+    bad[int(np.argmax(p))] *= 1.5                            # one key's weight wrong by half
+    try:
+        assert_attn_close(bad / bad.sum() @ v, o, vmax)
+    except AssertionError:
+        pass
+    else:
+        raise AssertionError("a wrong weight passed the attention bound")
+    assert np.all(attn_bound(o, vmax) > 0)
