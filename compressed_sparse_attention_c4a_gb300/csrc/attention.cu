@@ -152,10 +152,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
 //              physical row, tables cached in shared memory), prefetch later rounds into L2, and copy
 //              the rows into a stage with cp.async, 128B-swizzled, laid out [64-dim chunk][32 keys]
 //              [128 B]; e4m3 rows are converted to bf16 on the way, their scales kept beside the stage.
-//              A row's window keys come first: they are located and prefetched into L2 before the
-//              programmatic-launch wait, so a CTA's first sub-tile (window rows) is copied and reported
-//              while the top-k indices of the next ones are still being read.  Gathered rows are read
-//              with an evict-first L2 policy (each serves one query row);
+//              Gathered rows are read with an evict-first L2 policy (each serves one query row);
 //   warps 4-5  issue the MMAs, one elected lane each (an MMA's issue costs the issuing warp about 49
 //              cycles at these shapes, so two warps issue twice as fast); warp 4 also loads the query rows
 //              (TMA, one 64-dim box per lane):
@@ -225,15 +222,6 @@ struct ClSmem {
     static constexpr int kTmemCols = 128 + 4 * NH <= 256 ? 256 : 512;
 };
 
-// Physical row of window position pos in the window pool, through the pool blocks of positions wlo .. cached in
-// s_swb; -1 when that block is unmapped or outside the pool.
-__device__ __forceinline__ int window_row(const dsa_pool_t& swa, const int* s_swb, int wlo, int pos) {
-    const int lb = pos / kBlockPositions;
-    const int sb = lb - wlo / kBlockPositions;  // the window (<= 1024 positions) spans <= 5 blocks
-    const int pb = sb >= 0 && sb < 8 ? s_swb[sb] : -1;
-    return pb < 0 || pb >= swa.num_blocks ? -1 : pb * kBlockPositions + (pos - lb * kBlockPositions);
-}
-
 // Byte offset of element (row r, element e) in a tile of 128B-swizzled atoms whose rows are 128 bytes
 // (64 bf16) long: atoms of 8 rows are 1024 bytes apart, 64-element chunks `chunk_stride` apart.
 __device__ __forceinline__ uint32_t sw128_offset(int r, int e, int chunk_stride) {
@@ -242,9 +230,8 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int e, int chunk_stride)
                       ((in & 7) << 1));
 }
 
-// Keys of a row for the tensor-core kernel: [0, nw) the window positions wlo .. m, then [nw, nw + n_comp) the
-// compressed slots.  The window comes first because its rows depend on no kernel of the step that may still be
-// running when the attention starts: they are located and brought into L2 before the programmatic-launch wait.
+// Keys of a row for the tensor-core kernel: [0, n_comp) compressed slots, [n_comp, ncp) padding up to a
+// multiple of 4, [ncp, ncp + window count) window positions.
 
 template <int NH, bool FP8>
 __global__ void __launch_bounds__(kClThreads, 1)
@@ -323,13 +310,12 @@ __global__ void __launch_bounds__(kClThreads, 1)
     if (!row_ok && tid == 0) *s_fault = 1;
     const int n_vis = row_ok ? entries_formed((long long)m + 1, a.kind_w, a.kind_s) : 0;
     const int n_comp = a.topk ? a.k : n_vis;
+    const int ncp = (n_comp + 3) & ~3;
     const int wlo = max(0, m - a.window + 1);
-    const int nw = row_ok ? m - wlo + 1 : 0;  // window keys [0, nw), compressed keys [nw, n_keys)
-    const int n_keys = row_ok ? nw + n_comp : 0;
+    const int n_keys = row_ok ? ncp + (m - wlo + 1) : 0;
     const int n_sub = (n_keys + kClKeys - 1) / kClKeys;
     const int g_lo = split * a.cps, g_hi = min(n_sub, g_lo + a.cps);
     const int n_mine = g_hi > g_lo + crank ? (g_hi - g_lo - crank + csize - 1) / csize : 0;
-    const bool pre0 = n_mine > 0 && (g_lo + crank + 1) * kClKeys <= nw;  // first sub-tile: window keys only
     const bool bt_cached = a.main_bt.max_blocks <= kBtCache;
     int* s_bt = reinterpret_cast<int*>(smem + L::kOffBt);
     int* s_swb = reinterpret_cast<int*>(smem + L::kOffSwb);
@@ -360,20 +346,6 @@ __global__ void __launch_bounds__(kClThreads, 1)
                             : -1;
         }
         named_bar_sync(1, kClGatherThreads);  // cached tables visible to every gather thread
-        // the first round's window keys: rows located and moved into L2 now; when the CTA's first sub-tile
-        // holds window keys only, its rows are kept for copying right after the wait
-        const int i = gt / kClKeys;
-        const int j = (g_lo + crank + csize * i) * kClKeys + gt % kClKeys;
-        if (gt < kClRound * kClKeys && i < n_mine && j < nw) {
-            constexpr int kRowBytes = FP8 ? kD : 2 * kD;
-            const int v = window_row(a.swa, s_swb, wlo, wlo + j);
-            if (v >= 0) prefetch_l2(static_cast<const uint8_t*>(a.swa.data) + (long long)v * kRowBytes, kRowBytes);
-            if (pre0 && i == 0) {
-                s_row[gt] = v;
-                s_pool[gt] = 2;
-            }
-        }
-        named_bar_sync(1, kClGatherThreads);  // the first sub-tile's rows visible
     }
     pdl_wait();  // global memory the preceding kernel writes, and every output, only below
     pdl_launch_dependents();
@@ -390,7 +362,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             if (gt >= kClRound * kClKeys || i >= n_mine) return -1;
             const int j = (g_lo + crank + csize * i) * kClKeys + gt % kClKeys;
             *id = -1;
-            if (j >= nw && j < n_keys) *id = a.topk ? __ldg(a.topk + (long long)row * a.k + (j - nw)) : j - nw;
+            if (j < n_keys && j < n_comp) *id = a.topk ? __ldg(a.topk + (long long)row * a.k + j) : j;
             return j;
         };
         // Step 2: index -> physical row through the cached tables (or global memory), L2 prefetch, ring slot.
@@ -398,8 +370,8 @@ __global__ void __launch_bounds__(kClThreads, 1)
             const int i = R * kClRound + gt / kClKeys;
             if (j < 0) return;
             int v = -1, pool = 1;
-            if (j >= nw) {
-                if (j < n_keys && id >= 0) {
+            if (j < ncp) {
+                if (j < n_comp && id >= 0) {
                     if (id >= n_vis) {
                         report(a.status, DSA_ERR_DEVICE_FAULT);
                         *s_fault = 1;
@@ -417,15 +389,19 @@ __global__ void __launch_bounds__(kClThreads, 1)
                         }
                     }
                 }
-            } else {
+            } else if (j < n_keys) {
                 pool = 2;
-                v = window_row(a.swa, s_swb, wlo, wlo + j);
-                if (v < 0) {
+                const int pos = wlo + (j - ncp);
+                const int lb = pos / kBlockPositions;
+                const int sb = lb - wlo / kBlockPositions;  // the window (<= 1024 positions) spans <= 5 blocks
+                const int pb = DSA_IDX_OK(sb, 8, a.status) ? s_swb[sb] : -1;
+                if (pb < 0 || pb >= a.swa.num_blocks) {
                     report(a.status, DSA_ERR_DEVICE_FAULT);
                     *s_fault = 1;
+                } else {
+                    v = pb * kBlockPositions + (pos - lb * kBlockPositions);
                 }
             }
-            if (pre0 && R == 0 && i == 0) return;  // located before the wait; its copies may be under way
             if (v >= 0 && R > 0) {  // rows of later rounds start moving into L2 (the first round is gathered at once)
                 constexpr int kRowBytes = FP8 ? kD : 2 * kD;
                 const uint8_t* base = pool == 2 ? static_cast<const uint8_t*>(a.swa.data)
@@ -482,9 +458,24 @@ __global__ void __launch_bounds__(kClThreads, 1)
             }
         };
         const uint64_t row_policy = l2_evict_first();  // a gathered row serves this query row only
-        // copies of sub-tile i into its stage (every gather thread), and the stage's key mask for the softmax
-        auto issue = [&](int i) {
+        if (n_mine > 0) resolve_round(0);
+        int sig = 0;  // first sub-tile whose stage this thread has not yet reported full
+        for (int i = 0; i < n_mine; ++i) {
             const int s = i % kClStages;
+            if (i >= kClStages) {
+                // before waiting for a stage, report every sub-tile issued so far (never hold landed rows back)
+                if (sig < i) {
+                    cp_async_wait_all();
+                    for (; sig < i; ++sig) {
+                        if constexpr (FP8) widen_fp8(sig % kClStages);
+                        fence_proxy_async_smem();  // cp.async writes -> visible to the tensor core (async proxy)
+                        mbar_arrive(&full[sig % kClStages]);
+                    }
+                }
+                // the stage's previous sub-tile has been multiplied into O^T
+                ok = ok && mbar_wait_bounded(&pvdone[s], ((i - kClStages) / kClStages) & 1, kWaitLimitNs);
+            }
+            named_bar_sync(1, kClGatherThreads);  // sub-tile i's rows are visible; earlier gathers are done
             const int* rows = s_row + (i % kClRing) * kClKeys;
             const uint8_t* pools = s_pool + (i % kClRing) * kClKeys;
             if (gt < kClKeys) {  // the first gather warp: the stage's key mask for the softmax
@@ -526,34 +517,6 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 }
             }
             cp_async_commit();
-        };
-        if (pre0) issue(0);  // window rows located before the wait: no top-k index to wait for
-        if (n_mine > 0) resolve_round(0);
-        int sig = 0;  // first sub-tile whose stage this thread has not yet reported full
-        if (pre0) {  // the window rows (in L2 by now) are reported before the round's top-k rows are issued
-            cp_async_wait_all();
-            if constexpr (FP8) widen_fp8(0);
-            fence_proxy_async_smem();
-            mbar_arrive(&full[0]);
-            sig = 1;
-        }
-        for (int i = 0; i < n_mine; ++i) {
-            const int s = i % kClStages;
-            if (i >= kClStages) {
-                // before waiting for a stage, report every sub-tile issued so far (never hold landed rows back)
-                if (sig < i) {
-                    cp_async_wait_all();
-                    for (; sig < i; ++sig) {
-                        if constexpr (FP8) widen_fp8(sig % kClStages);
-                        fence_proxy_async_smem();  // cp.async writes -> visible to the tensor core (async proxy)
-                        mbar_arrive(&full[sig % kClStages]);
-                    }
-                }
-                // the stage's previous sub-tile has been multiplied into O^T
-                ok = ok && mbar_wait_bounded(&pvdone[s], ((i - kClStages) / kClStages) & 1, kWaitLimitNs);
-            }
-            named_bar_sync(1, kClGatherThreads);  // sub-tile i's rows are visible; earlier gathers are done
-            if (i > 0 || !pre0) issue(i);
             if (i == 0 && gt == 0) DSA_STAMP(3);
             if (i == 0) {  // the first round's later sub-tiles start moving into L2 once sub-tile 0 is under way
                 constexpr int kRowBytes = FP8 ? kD : 2 * kD;
