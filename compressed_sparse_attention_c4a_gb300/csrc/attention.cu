@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
         const int col = tid * 4 + e;
         if (col >= first) {
             float cs, sn;
-            rope_cos_sin(m, a.rope.inv_freq[(col - first) >> 1], &cs, &sn);
+            rope_cos_sin(m, a.rope, (col - first) >> 1, &cs, &sn);
             const float x0 = acc[e], x1 = acc[e + 1];
             acc[e] = x0 * cs + x1 * sn;
             acc[e + 1] = -x0 * sn + x1 * cs;
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     int* s_swb = reinterpret_cast<int*>(smem + L::kOffSwb);
     if (warp == 0 && lane < a.rope.rope_dim / 2) {  // R_m^-1 of the output: cos and sin of each pair's angle at m
         float c = 1.f, sn = 0.f;
-        if (row_ok) rope_cos_sin(m, a.rope.inv_freq[lane], &c, &sn);
+        if (row_ok) rope_cos_sin(m, a.rope, lane, &c, &sn);
         s_rc[2 * lane] = c;
         s_rc[2 * lane + 1] = sn;
     }
@@ -355,6 +355,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
 
     if (warp >= kClFirstGather) {
         // ---- gather warps: resolve keys a round ahead, prefetch rows into L2, copy with cp.async -----
+        const uint64_t row_policy = l2_evict_first();  // a gathered row serves this query row only
         // sub-tiles [R * kClRound, (R + 1) * kClRound): thread -> sub-tile R * kClRound + gt / 32, key gt % 32.
         // Step 1: the key's top-k index (or entry / window position), no dependent load.
         auto key_id = [&](int R, int* id) -> int {  // returns j (the key's index in the row), -1 if none
@@ -457,7 +458,6 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 }
             }
         };
-        const uint64_t row_policy = l2_evict_first();  // a gathered row serves this query row only
         if (n_mine > 0) resolve_round(0);
         int sig = 0;  // first sub-tile whose stage this thread has not yet reported full
         for (int i = 0; i < n_mine; ++i) {

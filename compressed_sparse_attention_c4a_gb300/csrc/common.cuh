@@ -216,23 +216,50 @@ __device__ __forceinline__ long long physical_row(const dsa_block_table_t& bt, i
 // RoPE frequencies theta^(-2j / rope_dim), j < rope_dim / 2, computed on the host in double precision and
 // passed by value in the kernel arguments (no device memory, no device-side pow).
 struct RopeTable {
-    double inv_freq[32];
+    float f_hi[32], f_lo[32];  // inv_freq of each pair as a float pair: hi + lo carries 48 of its bits
     int rope_dim;
 };
 
 inline RopeTable make_rope_table(int rope_dim, double theta) {
     RopeTable t{};
     t.rope_dim = rope_dim;
-    for (int j = 0; j < rope_dim / 2 && j < 32; ++j) t.inv_freq[j] = pow(theta, -2.0 * j / (double)rope_dim);
+    for (int j = 0; j < rope_dim / 2 && j < 32; ++j) {
+        const double f = pow(theta, -2.0 * j / (double)rope_dim);
+        t.f_hi[j] = (float)f;
+        t.f_lo[j] = (float)(f - (double)t.f_hi[j]);
+    }
     return t;
 }
 
-// cos / sin of pos * inv_freq: the angle is formed and reduced modulo 2 pi in double precision (at
-// positions near 2^20 a float angle has no fraction bits left), then evaluated in float.
-__device__ __forceinline__ void rope_cos_sin(long long pos, double inv_freq, float* c, float* s) {
-    const double a = (double)pos * inv_freq;
-    const double r = fma(-kTwoPi, rint(a * (1.0 / kTwoPi)), a);
-    sincosf((float)r, s, c);
+// 2 pi as three floats (Cody-Waite): A + B + C equals 2 pi to within 5e-23; 1 / (2 pi) rounded to float.
+constexpr float kTwoPiA = 0x1.921fb6p+2f, kTwoPiB = -0x1.777a5cp-23f, kTwoPiC = -0x1.ee59dap-48f;
+constexpr float kInvTwoPiF = 0x1.45f306p-3f;
+
+// cos / sin of pos * inv_freq_j.  A float angle at positions near 2^20 has no fraction bits left, and the
+// GPU's fp64 rate is a small fraction of its fp32 rate, so the angle is kept as a float pair instead: the
+// product of the position (exact as a float below 2^24) with hi + lo is p + e, e = the product's rounding
+// error (one fma, exact) + pos * lo; p is reduced modulo 2 pi with k = rint(p / 2 pi) by one fma per part of
+// 2 pi, each rounding a result of magnitude <= 4 once, and e is added last.  The reduced angle is within
+// about 3e-7 rad of the exact one below 2^24; larger (or negative) positions take an fp64 reduction.  The
+// reduced angle lies in [-pi - 1, pi + 1], where the hardware sine and cosine (__sincosf) are accurate to
+// about 5e-7 absolute and take a few instructions (sincosf also carries a long path for huge arguments,
+// code that a kernel rotating 8 pairs per lane would repeat 8 times).
+__device__ __forceinline__ void rope_cos_sin(long long pos, const RopeTable& t, int j, float* c, float* s) {
+    const float hi = t.f_hi[j], lo = t.f_lo[j];
+    float r;
+    if (pos < 0 || pos >= (1ll << 24)) {
+        const double a = (double)pos * ((double)hi + (double)lo);
+        r = (float)fma(-kTwoPi, rint(a * (1.0 / kTwoPi)), a);
+    } else {
+        const float x = (float)pos;
+        const float p = x * hi;
+        const float e = fmaf(x, hi, -p) + x * lo;
+        const float k = rintf(p * kInvTwoPiF);
+        r = fmaf(-k, kTwoPiA, p);
+        r = fmaf(-k, kTwoPiB, r);
+        r = fmaf(-k, kTwoPiC, r) + e;
+    }
+    __sincosf(r, s, c);
 }
 
 __device__ __forceinline__ float bf16_to_float(uint16_t b) {
@@ -572,6 +599,15 @@ __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
 // Prefetch `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+// prefetch_l2 with an L2 cache policy.
+__device__ __forceinline__ void prefetch_l2_hint(const void* p, uint32_t bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p), "r"(bytes), "l"(policy)
+                 : "memory");
+}
+// The 128-byte line holding p into L2 (no alignment or size rule).
+__device__ __forceinline__ void prefetch_line_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {

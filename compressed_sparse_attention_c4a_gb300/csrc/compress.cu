@@ -176,7 +176,7 @@ __device__ __forceinline__ void rope_row(float (&v)[E], int lane, int dim, const
         const int d = lane * E + k;
         if (d >= first) {
             float c, s;
-            rope_cos_sin(pos, rt.inv_freq[(d - first) >> 1], &c, &s);
+            rope_cos_sin(pos, rt, (d - first) >> 1, &c, &s);
             const float x0 = v[k], x1 = v[k + 1];
             v[k] = x0 * c - x1 * s;
             v[k + 1] = x0 * s + x1 * c;
@@ -223,6 +223,23 @@ __device__ __forceinline__ void compress_item(const CompressArgs& a, int item, i
         j = item - a.entry_items;
         if (j >= n || j >= a.token_items) j = -1;
         else if (a.has_swa) prow = physical_row(a.swa_bt, r, start + j, kBlockPositions, a.swa.num_blocks);
+    }
+    // The rows this warp will read start moving into L2: the window's rows of the rolling state (written only
+    // by earlier calls) and the new tokens' rows.  A prefetch returns nothing, so every read still comes after
+    // the wait below; it only spares the reads a trip to DRAM.
+    if (!bad_req && is_entry && i >= 0) {
+        const long long base = (long long)s * i;
+        const int u_lo = W == 128 ? sub * (W / a.nsub) : 0, u_hi = W == 128 ? u_lo + W / a.nsub : W;
+        for (int u = u_lo + lane; u < u_hi; u += 32) {
+            const long long p = base + u;
+            const long long row = p < start ? (long long)slot * w + (p % w) : (long long)cu0 + (p - start);
+            prefetch_l2((p < start ? a.state_x : a.x_new) + row * DIM, DIM * 2);
+            if (a.gate_pc) prefetch_l2((p < start ? a.state_logit : a.logit_new) + row * DIM, DIM * 4);
+        }
+        if (!a.gate_pc)
+            for (int u = lane; u * 32 < w; u += 32) prefetch_line_l2(a.state_logit + (long long)slot * w + u * 32);
+    } else if (!bad_req && j >= 0 && lane == 0) {
+        prefetch_l2(a.x_new + (long long)(cu0 + j) * DIM, DIM * 2);
     }
     pdl_wait();
     pdl_launch_dependents();
@@ -291,6 +308,7 @@ __device__ __forceinline__ void compress_item(const CompressArgs& a, int item, i
             mx = fmaxf(mx, z[u]);
         }
         mx = warp_max(mx);
+        if (lane == 0 && threadIdx.x < 64) DSA_STAMP(2 + 4 * (threadIdx.x >> 5));
         float den = 0.f;
 #pragma unroll
         for (int u = 0; u < LPL; ++u) {
@@ -334,6 +352,7 @@ __device__ __forceinline__ void compress_item(const CompressArgs& a, int item, i
             }
         }
         }
+        if (lane == 0 && threadIdx.x < 64) DSA_STAMP(3 + 4 * (threadIdx.x >> 5));
         // RMSNorm
         float ss = 0.f;
 #pragma unroll
@@ -349,6 +368,7 @@ __device__ __forceinline__ void compress_item(const CompressArgs& a, int item, i
             return;
         }
         store_row<E>(a.out, prow, lane, acc);
+        if (lane == 0 && threadIdx.x < 64) DSA_STAMP(4 + 4 * (threadIdx.x >> 5));
         return;
     }
 
@@ -359,6 +379,7 @@ __device__ __forceinline__ void compress_item(const CompressArgs& a, int item, i
         float v[E];
         load_bf16<E>(xrow, lane, v);
         rope_row<E>(v, lane, DIM, a.rope, p);
+        if (lane == 0 && threadIdx.x < 64) DSA_STAMP(3 + 4 * (threadIdx.x >> 5));
         if (prow < 0) {
             if (lane == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
         } else {
@@ -371,6 +392,7 @@ __device__ __forceinline__ void compress_item(const CompressArgs& a, int item, i
         if (a.gate_pc) copy_f32<E>(a.state_logit + ring * DIM, a.logit_new + (long long)(cu0 + j) * DIM, lane);
         else if (lane == 0) a.state_logit[ring] = a.logit_new[cu0 + j];
     }
+    if (lane == 0 && threadIdx.x < 64) DSA_STAMP(4 + 4 * (threadIdx.x >> 5));
 }
 
 constexpr int kMaxJobs = 4;
