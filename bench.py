@@ -275,11 +275,12 @@ def run_gpu(args, rank, world, local_rank):
                     ev["index"][i][0].record(stream)
                     st.index()
                     ev["index"][i][1].record(stream)
-                    ev["topk"][i][0].record(stream)
-                    st.select()
-                    ev["topk"][i][1].record(stream)
+                    if not st.fused_select:
+                        ev["topk"][i][0].record(stream)
+                        st.select()
+                        ev["topk"][i][1].record(stream)
                 ev["attend"][i][0].record(stream)
-                st.attend()
+                st.select_attend() if st.fused_select else st.attend()
                 ev["attend"][i][1].record(stream)
     reps = max(1, math.ceil(args.steps / per_graph))
     steps = reps * per_graph
@@ -302,7 +303,8 @@ def run_gpu(args, rank, world, local_rank):
                  "min_ms_per_step": round(rep_ms[0], 6), "max_ms_per_step": round(rep_ms[-1], 6)}
     # kernel durations: event nodes around each launch inside the step graph (its own timed region);
     # where event nodes are unavailable, a graph of back-to-back launches of that stage alone
-    stages = ["index", "topk", "attend"] if copies[0].has_index else ["attend"]
+    fused = copies[0].fused_select  # the top-k runs inside the attention call (one kernel when the plan allows)
+    stages = (["index", "attend"] if fused else ["index", "topk", "attend"]) if copies[0].has_index else ["attend"]
     k_ms, timing = {}, "event nodes around each launch in the step graph"
     k_launches = 0
     try:
@@ -326,7 +328,8 @@ def run_gpu(args, rank, world, local_rank):
             with torch.cuda.graph(g, stream=stream):
                 for i in range(per_graph):
                     st = copies[i % args.copies]
-                    {"index": st.index, "topk": st.select, "attend": st.attend}[n]()
+                    {"index": st.index, "topk": st.select,
+                     "attend": st.select_attend if fused else st.attend}[n]()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             with torch.cuda.stream(stream):
                 g.replay()
@@ -350,9 +353,15 @@ def run_gpu(args, rank, world, local_rank):
     if "index" in k_ms:
         kern["index_kernel"] = {"ms": k_ms["index"], "bytes": idx_bytes, "gbs": idx_bytes / (k_ms["index"] * 1e6),
                                 "tflops": index_flops(spec) / (k_ms["index"] * 1e9)}
-        kern["topk_kernel"] = {"ms": k_ms["topk"], "counted": bool(copies[0].fused_topk)}
-    kern["attn_kernel"] = {"ms": k_ms["attend"], "bytes": att_bytes, "gbs": att_bytes / (k_ms["attend"] * 1e6),
+        if not fused:
+            kern["topk_kernel"] = {"ms": k_ms["topk"], "counted": bool(copies[0].fused_topk)}
+    # fused: the attention kernel also reads every query row's scores (4 B each) for its top-k phase
+    a_bytes = att_bytes + (4 * sum(int(n) for n in copies[0].n_visible.tolist()) if fused else 0)
+    kern["attn_kernel"] = {"ms": k_ms["attend"], "bytes": a_bytes, "gbs": a_bytes / (k_ms["attend"] * 1e6),
                            "tflops": attention_flops(spec) / (k_ms["attend"] * 1e9)}
+    if fused:
+        kern["attn_kernel"]["fused_topk"] = True
+        kern["attn_kernel"]["kernels_per_call"] = copies[0].select_attend_kernels
     dominant = max((n for n in kern if "bytes" in kern[n]), key=lambda n: kern[n]["ms"])
     if spec.queries == "last":  # decode: every stage streams keys once
         roof = {"kernel": dominant, "bound": "hbm", "achieved": round(kern[dominant]["gbs"], 1),

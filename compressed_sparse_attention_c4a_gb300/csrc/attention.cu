@@ -15,12 +15,12 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "topk_cluster.cuh"
 
 namespace dsa {
 
 constexpr int kD = 512;
 constexpr float kLog2e = 1.4426950408889634f;
-DSA_TIMELINE_BUFFER
 
 struct AttnArgs {
     int rows, heads, hg_count, nsplit, cps;   // cps = 32-key sub-tiles per split
@@ -43,6 +43,10 @@ struct AttnArgs {
     float* lse;
     float* ws_o;                              // [rows][nsplit][heads][512]
     float* ws_ml;                             // [rows][nsplit][heads][4]: M, L (bf16 P), E (fp32 P), 0
+    const float* scores;                      // fused top-k: indexer scores [rows][score_ld]
+    int score_ld;
+    const int32_t* n_valid;                   // fused top-k: [rows] valid scores of a row
+    int32_t* topk_out;                        // fused top-k: the selected entries [rows][k]
     int32_t* status;
 };
 
@@ -188,6 +192,8 @@ static_assert(kClKeys == 32, "one 32-bit key mask and 32 S columns per sub-tile"
 static_assert(kClThreads == 512, "16 warps");
 constexpr float kLazyLog2 = 8.f;            // the running maximum moves when exceeded by more than this
 constexpr int kBtCache = 1024;              // main block tables up to this many blocks are cached in shared memory
+constexpr int kFusedK = 512;                // the fused top-k + attention kernel: k up to this
+constexpr int kFusedVpt = 8;                // ... scores per thread: rows up to 4 * 512 * 8 = 16,384 entries
 
 template <int NH>
 struct ClSmem {
@@ -211,7 +217,8 @@ struct ClSmem {
     static constexpr int kOffRope = kOffFault + 16;                 // float [32][2]: cos, sin of each pair's angle at m
     static constexpr int kBars = 2 * kClStages + 6;
     static constexpr int kOffBar = kOffRope + 256;                  // kBars mbarriers, TMEM address
-    static constexpr int kBytes = kOffBar + kBars * 8 + 16;
+    static constexpr int kOffTopk = kOffBar + kBars * 8 + 16;       // int [kFusedK]: the row's top-k (fused)
+    static constexpr int kBytes = kOffTopk + kFusedK * 4;
     static constexpr int kAlloc = kBytes + 1024;                    // + alignment slack
     static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
     static_assert(kOffKsc % 16 == 0, "the row scales are read as float4");
@@ -233,7 +240,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int e, int chunk_stride)
 // Keys of a row for the tensor-core kernel: [0, n_comp) compressed slots, [n_comp, ncp) padding up to a
 // multiple of 4, [ncp, ncp + window count) window positions.
 
-template <int NH, bool FP8>
+template <int NH, bool FP8, bool FUSED>
 __global__ void __launch_bounds__(kClThreads, 1)
     attn_cl_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap, AttnArgs a) {
     using L = ClSmem<NH>;
@@ -309,7 +316,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const bool row_ok = r >= 0 && r < a.main_bt.batch && r < a.swa_bt.batch && m >= 0;
     if (!row_ok && tid == 0) *s_fault = 1;
     const int n_vis = row_ok ? entries_formed((long long)m + 1, a.kind_w, a.kind_s) : 0;
-    const int n_comp = a.topk ? a.k : n_vis;
+    const int n_comp = (FUSED || a.topk) ? a.k : n_vis;
     const int ncp = (n_comp + 3) & ~3;
     const int wlo = max(0, m - a.window + 1);
     const int n_keys = row_ok ? ncp + (m - wlo + 1) : 0;
@@ -351,6 +358,30 @@ __global__ void __launch_bounds__(kClThreads, 1)
     pdl_launch_dependents();
     if (tid == 0) DSA_STAMP(2);
     if (!row_ok && tid == 0 && crank == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
+    int* s_topk = reinterpret_cast<int*>(smem + L::kOffTopk);
+    if constexpr (FUSED) {
+        // The row's top-k of the indexer scores on this cluster (one cluster of four CTAs per row), every
+        // selected entry written into each CTA's s_topk (and topk_out); its scratch is the key stages, idle
+        // until the gather below.  Its first cluster barrier completes phase 0 (every CTA has started).
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster_wait();
+        auto& ts = *reinterpret_cast<TopkRowScratch<kClThreads, kFusedVpt, 4>*>(smem + L::kOffK);
+        int32_t* tout = a.topk_out + (long long)row * a.k;
+        auto emit = [&](int pos, int idx) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) *cluster.map_shared_rank(s_topk + pos, c) = idx;
+            tout[pos] = idx;
+        };
+        const int nv_row = a.n_valid[row];  // the same in every CTA of the cluster
+        if (nv_row < 0 || nv_row > a.score_ld) {
+            if (tid == 0 && crank == 0) report(a.status, DSA_ERR_DEVICE_FAULT);
+            for (int i = crank * kClThreads + tid; i < a.k; i += 4 * kClThreads) emit(i, -1);
+        } else {
+            topk_row_cluster<kClThreads, kFusedVpt, 4>(cluster, ts, a.scores + (long long)row * a.score_ld, nv_row,
+                                                       a.k, emit, a.status, 23);
+        }
+        cluster.sync();  // every CTA's s_topk complete; the scratch (key stages) no longer read by a peer
+    }
     bool ok = true;
 
     if (warp >= kClFirstGather) {
@@ -363,7 +394,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             if (gt >= kClRound * kClKeys || i >= n_mine) return -1;
             const int j = (g_lo + crank + csize * i) * kClKeys + gt % kClKeys;
             *id = -1;
-            if (j < n_keys && j < n_comp) *id = a.topk ? __ldg(a.topk + (long long)row * a.k + j) : j;
+            if (j < n_keys && j < n_comp) *id = FUSED ? s_topk[j] : (a.topk ? __ldg(a.topk + (long long)row * a.k + j) : j);
             return j;
         };
         // Step 2: index -> physical row through the cached tables (or global memory), L2 prefetch, ring slot.
@@ -802,7 +833,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     }
     if (tid == 0) DSA_STAMP(9);
     // 2. (m, l, e, fault) per head to every CTA of the cluster
-    cluster_wait();  // phase 0: every CTA of the cluster has started
+    if constexpr (!FUSED) cluster_wait();  // phase 0: every CTA of the cluster has started (fused: waited above)
     if (tid == 0) DSA_STAMP(17);
     if (csize > 1 && tid == 0)  // before any peer can push (pushes follow phase 1)
         mbar_arrive_expect_tx(xfull, (uint32_t)((csize - 1) * tiles_per * L::kTile));
@@ -1087,7 +1118,7 @@ static bool make_out_map(CUtensorMap* map, void* base, uint64_t rows, int box_ro
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NH, bool FP8>
+template <int NH, bool FP8, bool FUSED = false>
 static dsa_status_t launch_attn_cl(const AttnArgs& a, int cl, cudaStream_t st) {
     using L = ClSmem<NH>;
     CUtensorMap qmap, omap;
@@ -1095,16 +1126,29 @@ static dsa_status_t launch_attn_cl(const AttnArgs& a, int cl, cudaStream_t st) {
     if (!make_out_map(&omap, a.out8 ? static_cast<void*>(a.out8) : static_cast<void*>(a.out), (uint64_t)a.rows * a.heads,
                       NH, a.out8 != nullptr))
         return DSA_ERR_CUDA;
-    if (cudaFuncSetAttribute(attn_cl_kernel<NH, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
+    if (cudaFuncSetAttribute(attn_cl_kernel<NH, FP8, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
         cudaSuccess)
         return DSA_ERR_CUDA;
     const long long grid = (long long)a.rows * a.hg_count * a.nsplit * cl;
-    cudaError_t e = launch_pdl_cluster(attn_cl_kernel<NH, FP8>, dim3((unsigned)grid), dim3(kClThreads), L::kAlloc, st, cl,
+    cudaError_t e = launch_pdl_cluster(attn_cl_kernel<NH, FP8, FUSED>, dim3((unsigned)grid), dim3(kClThreads), L::kAlloc, st, cl,
                                        qmap, omap, a);
     if (e == cudaSuccess && a.nsplit > 1)
         e = launch_pdl(attn_combine_kernel, dim3(a.rows * a.heads), dim3(128), 0, st, a);
     if (e != cudaSuccess) return DSA_ERR_CUDA;
     return launch_status();
+}
+
+// The indexer scores a fused call selects from (the kernel's top-k phase), and whether a plan allows it: one
+// cluster of four CTAs per row holding all 64 heads, no key split, rows of at most 16,384 scores, k <= 512.
+struct FusedTopk {
+    const float* scores;
+    int32_t ld;
+    const int32_t* n_valid;
+};
+
+static bool fusable(const SplitPlan& p, int heads, int ld, int k) {
+    return heads == 64 && p.hg_count == 1 && p.cl == 4 && p.nsplit == 1 && ld <= 4 * kClThreads * kFusedVpt &&
+           k <= kFusedK;
 }
 
 static dsa_status_t sparse_attn(int32_t rows, int32_t heads, const void* q, const int32_t* q_pos,
@@ -1113,7 +1157,7 @@ static dsa_status_t sparse_attn(int32_t rows, int32_t heads, const void* q, cons
                                 const dsa_block_table_t* swa_bt, int32_t window, float sm_scale,
                                 const dsa_rope_t* rope, void* out, float* lse, void* workspace,
                                 size_t workspace_bytes, int32_t* dev_status, void* stream, uint8_t* out8 = nullptr,
-                                float* out_scale = nullptr) {
+                                float* out_scale = nullptr, const FusedTopk* fz = nullptr) {
     if (rows < 0) return DSA_ERR_INVALID_ARG;
     if (rows == 0) return DSA_OK;
     if (kind != DSA_C4A && kind != DSA_C128A) return DSA_ERR_INVALID_ARG;
@@ -1172,6 +1216,15 @@ static dsa_status_t sparse_attn(int32_t rows, int32_t heads, const void* q, cons
     a.status = dev_status;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool fp8 = main->dtype == DSA_FP8_E4M3;
+    if (fz) {  // topk is the output of the kernel's own top-k phase
+        if (!fusable(p, heads, fz->ld, k)) return DSA_ERR_UNSUPPORTED;
+        a.topk = nullptr;
+        a.topk_out = const_cast<int32_t*>(topk);
+        a.scores = fz->scores;
+        a.score_ld = fz->ld;
+        a.n_valid = fz->n_valid;
+        return fp8 ? launch_attn_cl<64, true, true>(a, p.cl, st) : launch_attn_cl<64, false, true>(a, p.cl, st);
+    }
     if (!fp8) {
         switch (p.hg) {
             case 16: return launch_attn_cl<16, false>(a, p.cl, st);
@@ -1219,6 +1272,30 @@ extern "C" dsa_status_t dsa_sparse_attn_decode(int32_t batch, int32_t heads, con
                                                size_t workspace_bytes, int32_t* dev_status, void* stream) {
     return sparse_attn(batch, heads, q, q_pos, nullptr, kind, topk, k, main, main_bt, swa, swa_bt, window, sm_scale,
                        rope, out, lse, workspace, workspace_bytes, dev_status, stream);
+}
+
+extern "C" dsa_status_t dsa_topk_sparse_attn_decode(
+    int32_t batch, int32_t heads, const void* q, const int32_t* q_pos, int32_t kind, const float* scores, int32_t ld,
+    const int32_t* n_visible, int32_t k, int32_t* topk_out, const dsa_pool_t* main, const dsa_block_table_t* main_bt,
+    const dsa_pool_t* swa, const dsa_block_table_t* swa_bt, int32_t window, float sm_scale, const dsa_rope_t* rope,
+    void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    if (batch < 0) return DSA_ERR_INVALID_ARG;
+    if (batch == 0) return DSA_OK;
+    if (!scores || !n_visible || !topk_out || k < 1 || k > 2048 || ld < 0 || (ld & 3) || !aligned(scores, 16) ||
+        !main)
+        return DSA_ERR_INVALID_ARG;
+    if (heads != 16 && heads != 32 && heads != 64 && heads != 128) return DSA_ERR_UNSUPPORTED;
+    if (window < 1 || window > 1024) return DSA_ERR_INVALID_ARG;
+    const SplitPlan p = plan_for(batch, heads, k + window, main->dtype);
+    if (!fusable(p, heads, ld, k)) {  // two launches: the top-k, then the attention over its output
+        const dsa_status_t e = dsa_topk(batch, scores, ld, n_visible, k, topk_out, dev_status, stream);
+        if (e != DSA_OK) return e;
+        return sparse_attn(batch, heads, q, q_pos, nullptr, kind, topk_out, k, main, main_bt, swa, swa_bt, window,
+                           sm_scale, rope, out, lse, workspace, workspace_bytes, dev_status, stream);
+    }
+    const FusedTopk fz{scores, ld, n_visible};
+    return sparse_attn(batch, heads, q, q_pos, nullptr, kind, topk_out, k, main, main_bt, swa, swa_bt, window, sm_scale,
+                       rope, out, lse, workspace, workspace_bytes, dev_status, stream, nullptr, nullptr, &fz);
 }
 
 extern "C" dsa_status_t dsa_sparse_attn_q8(int32_t nq, int32_t heads, const void* q, const int32_t* q_pos,

@@ -169,6 +169,7 @@ __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepc
 #define DSA_TRACE(n, k) ((void)0)
 #define DSA_TIMELINE_SETTER(name)
 #endif
+DSA_TIMELINE_BUFFER  // one buffer pointer per translation unit
 
 // Monotone 32-bit key of a score (the top-k's radix digits): a larger float has a larger key; -0 and +0 share
 // one key.  Shared by the indexer (which counts each row's top 11 bits while scoring) and the top-k.

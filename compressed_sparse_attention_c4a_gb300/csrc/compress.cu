@@ -14,7 +14,6 @@
 
 namespace dsa {
 
-DSA_TIMELINE_BUFFER
 
 struct CompressArgs {
     int w, s, batch, dim;

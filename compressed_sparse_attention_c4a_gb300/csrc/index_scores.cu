@@ -37,7 +37,6 @@ __host__ __device__ constexpr int slice_cols() { return TPI == 2 ? 128 : 96; }
 constexpr int kTileEntries = 128;
 constexpr int kPage = 64;         // c4a entries per 256-position block
 constexpr int kChunkItems = 32;   // items resolved together (one per producer lane)
-DSA_TIMELINE_BUFFER
 
 struct IdxArgs {
     int nq, heads, q_group, n_cols, tmem_cols, ld;

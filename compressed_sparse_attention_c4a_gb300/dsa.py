@@ -26,7 +26,7 @@ EXPORTS = ["dsa_status_string", "dsa_compress", "dsa_index_scores", "dsa_topk", 
            "dsa_sparse_attn_decode", "dsa_sparse_attn_prefill", "dsa_gather_rows", "dsa_sparse_attn_decode_static",
            "dsa_attn_static_scratch_bytes", "dsa_attn_plan", "dsa_debug_index_scores_stalled", "dsa_index_topk",
            "dsa_index_topk_workspace_size", "dsa_index_scores_counted", "dsa_topk_counted", "dsa_sparse_attn_q8",
-           "dsa_compress_jobs"]
+           "dsa_compress_jobs", "dsa_topk_sparse_attn_decode"]
 
 
 class DsaPool(ctypes.Structure):
@@ -91,6 +91,8 @@ for _name, _args in {
                                ctypes.c_size_t, _P, _P],
     "dsa_sparse_attn_prefill": [_I, _I, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, ctypes.c_float, _P, _P, _P,
                                 _P, ctypes.c_size_t, _P, _P],
+    "dsa_topk_sparse_attn_decode": [_I, _I, _P, _P, _I, _P, _I, _P, _I, _P, _P, _P, _P, _P, _I, ctypes.c_float, _P,
+                                    _P, _P, _P, ctypes.c_size_t, _P, _P],
     "dsa_gather_rows": [_P, _P, _I, _P, _P, _P, _P, _P, _P],
     "dsa_sparse_attn_q8": [_I, _I, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, ctypes.c_float, _P, _P, _P, _P, _P,
                            ctypes.c_size_t, _P, _P],
@@ -273,6 +275,21 @@ def dsa_sparse_attn_decode(q, q_pos, kind, topk, k, main, main_bt, swa, swa_bt, 
                                        _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(dev_status),
                                        _stream(stream))
     _check("dsa_sparse_attn_decode", code)
+
+
+def dsa_topk_sparse_attn_decode(q, q_pos, kind, scores, n_visible, k, topk_out, main, main_bt, swa, swa_bt, window,
+                                sm_scale, rope_cfg, out, lse=None, workspace=None, dev_status=None, stream=None):
+    """dsa_topk of (scores, n_visible, k) into topk_out, then dsa_sparse_attn_decode over it (one kernel when the
+    work split allows)."""
+    B, H, _ = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    code = _lib.dsa_topk_sparse_attn_decode(B, H, _ptr(q), _ptr(q_pos), KIND.get(kind, kind), _ptr(scores),
+                                            scores.shape[1], _ptr(n_visible), int(k), _ptr(topk_out),
+                                            ctypes.byref(main), ctypes.byref(main_bt), ctypes.byref(swa),
+                                            ctypes.byref(swa_bt), int(window), float(sm_scale), ctypes.byref(rope_cfg),
+                                            _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                                            _stream(stream))
+    _check("dsa_topk_sparse_attn_decode", code)
 
 
 def dsa_sparse_attn_prefill(q, q_pos, q_req, kind, topk, k, main, main_bt, swa, swa_bt, window, sm_scale, rope_cfg,

@@ -27,7 +27,7 @@ def _query_group(spec, idx_heads):
 class LayerStep:
     """Device-resident state and buffers of one case (a dict from ``synth.make_case`` on cuda)."""
 
-    def __init__(self, case, counted_topk=False, two_streams=False, dynamic_split=False):
+    def __init__(self, case, counted_topk=False, two_streams=False, dynamic_split=False, fused_select=False):
         spec = case["spec"]
         self.case, self.spec = case, spec
         dev = case["q"].device
@@ -77,6 +77,16 @@ class LayerStep:
         # static share; off by default (measured slower on the decode batch: more query-group switches)
         self.dynamic_split = dynamic_split
         self.side = None
+        # fused_select: decode rows take the top-k and the attention in one call (one kernel when one cluster of
+        # four CTAs per row holds all 64 heads, rows of at most 16,384 scores and k <= 512); off by default: on
+        # the decode batch it measured level with the two launches (44.6 against 44.4 us a step), its top-k
+        # phase running about 3 us slower inside the attention kernel than the top-k kernel alone
+        self.fused_select = fused_select and self.has_index and spec.queries == "last" and not self.fused_topk
+        self.select_attend_kernels = 2
+        if self.fused_select:
+            one = (tuple(self.attn_plan) == (64, 4, 1, 1) and spec.heads == 64 and self.ld <= 16384
+                   and spec.topk <= 512)
+            self.select_attend_kernels = 1 if one else 1 + self.attn_plan[3]
 
     # ---- stages ------------------------------------------------------------------------
     def _jobs(self):
@@ -154,13 +164,23 @@ class LayerStep:
                                         self.swa, self.swa_bt, s.window, SM_SCALE, self.rope_main, self.out,
                                         self.lse, self.workspace, dev_status=self.status)
 
+    def select_attend(self):
+        """Top-k and attention in one call (decode rows): the top-k indices land in self.topk as well."""
+        c, s = self.case, self.spec
+        dsa.dsa_topk_sparse_attn_decode(c["q"], c["q_pos"], self.kind, self.scores, self.n_visible, s.topk, self.topk,
+                                        self.main, self.main_bt, self.swa, self.swa_bt, s.window, SM_SCALE,
+                                        self.rope_main, self.out, self.lse, self.workspace, dev_status=self.status)
+
     def launches_per_step(self):
         """Kernels one ``run()`` launches (compress: +1 ring kernel when a request appends > 1 token;
         attention: +1 merge kernel when a row's keys are split over several clusters)."""
         per_compress = 1 + (1 if self.max_new > 1 else 0)
         n = per_compress
         if self.has_index:
-            n += (per_compress if self.spec.index_compress and self.two_streams else 0) + 2
+            n += (per_compress if self.spec.index_compress and self.two_streams else 0) + 1
+            if self.fused_select and not self.two_streams:
+                return n + self.select_attend_kernels
+            n += 1
         n += self.attn_plan[3]
         return n
 
@@ -179,8 +199,11 @@ class LayerStep:
         if not self.two_streams:
             self.compress()
             self.index()
-            self.select()
-            self.attend()
+            if self.fused_select:
+                self.select_attend()
+            else:
+                self.select()
+                self.attend()
             return self.out
         cur = torch.cuda.current_stream()
         if self.side is None:

@@ -374,6 +374,29 @@ dsa_status_t dsa_sparse_attn_prefill(int32_t nq, int32_t heads, const void* q, c
                                      void* stream);
 
 /*
+ * dsa_topk_sparse_attn_decode - dsa_topk followed by dsa_sparse_attn_decode over its output, in one kernel
+ * where the work split allows it.  [P1] §4.2 (S_t = TopK(I_t), then attention over S_t), [P2] 第四层 (kernel
+ * fusion: adjacent steps of the path share one launch so that the intermediate never leaves the chip): the
+ * cluster of CTAs that attends to a query row first selects the row's top-k from its scores, keeps the
+ * selected entry ids in shared memory and gathers those rows.
+ *     topk_out[b] = dsa_topk's row b of (scores, n_visible, k);  out, lse = dsa_sparse_attn_decode(topk_out)
+ * scores     [batch][ld] fp32, 16-byte aligned, ld a multiple of 4;  n_visible [batch] int32
+ * topk_out   [batch][k] int32 (required): the selected entry ids, exactly as dsa_topk writes them
+ * Other arguments as dsa_sparse_attn_decode with topk = topk_out (workspace sized for max_keys = k + window).
+ * One kernel when one cluster of four CTAs per row holds all heads without a key split (64 heads, at most
+ * 38 rows on a 152-SM GPU), ld <= 16,384 and k <= 512 (dsa_attn_plan(batch, heads, k + window) gives
+ * (64, 4, 1, 1)); else the two calls in sequence.  Programmatic dependent launch as dsa_sparse_attn_decode:
+ * scores and n_visible are read after the wait.  Errors: those of both calls.
+ */
+dsa_status_t dsa_topk_sparse_attn_decode(int32_t batch, int32_t heads, const void* q, const int32_t* q_pos,
+                                         int32_t kind, const float* scores, int32_t ld, const int32_t* n_visible,
+                                         int32_t k, int32_t* topk_out, const dsa_pool_t* main,
+                                         const dsa_block_table_t* main_bt, const dsa_pool_t* swa,
+                                         const dsa_block_table_t* swa_bt, int32_t window, float sm_scale,
+                                         const dsa_rope_t* rope, void* out, float* lse, void* workspace,
+                                         size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
  * dsa_sparse_attn_q8 - the same attention (decode rows when q_req is NULL, else prefill rows as
  * dsa_sparse_attn_prefill) with the output in e4m3 for an fp8 projection that follows: [P2] 融合点 2 (the
  * inverse rotation and the fp8 quantisation fused into one pass over the output, no bf16 round trip).

@@ -62,6 +62,27 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.dsa_compress(*args) == 1
 
 
+def test_fused_topk_attention_host_validation(lib):
+    """dsa_topk_sparse_attn_decode: the top-k output buffer is required, ld a multiple of 4, k in 1..2048, an
+    empty batch a no-op; all decided on the host."""
+    from compressed_sparse_attention_c4a_gb300 import dsa
+    P = ctypes.c_void_p
+    bt = dsa.DsaBlockTable(64, 4, 4)
+    main = dsa.DsaPool(256, None, 16, 64, 512, dsa.DSA_BF16)
+    rope = dsa.DsaRope(64, 10000.0)
+    f = dsa._lib.dsa_topk_sparse_attn_decode
+
+    def call(batch=4, ld=64, k=8, topk_out=P(16), scores=P(16)):
+        return f(batch, 64, P(16), P(16), 0, scores, ld, P(16), k, topk_out, ctypes.byref(main), ctypes.byref(bt),
+                 ctypes.byref(main), ctypes.byref(bt), 128, 0.044, ctypes.byref(rope), P(16), None, None, 0, None,
+                 None)
+    assert call(topk_out=None) == dsa.DSA_ERR_INVALID_ARG
+    assert call(ld=66) == dsa.DSA_ERR_INVALID_ARG
+    assert call(k=0) == dsa.DSA_ERR_INVALID_ARG
+    assert call(scores=P(20)) == dsa.DSA_ERR_INVALID_ARG        # scores not 16-byte aligned
+    assert call(batch=0) == dsa.DSA_OK
+
+
 def test_workspace_size_is_zero_for_unsupported_heads(lib):
     lib.dsa_attn_workspace_size.restype = ctypes.c_size_t
     assert lib.dsa_attn_workspace_size(32, 48, 640) == 0

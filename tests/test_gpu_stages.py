@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from compressed_sparse_attention_c4a_gb300 import synth
+from compressed_sparse_attention_c4a_gb300 import dsa, synth
 from compressed_sparse_attention_c4a_gb300.step import LayerStep, SM_SCALE
 from oracle import layer as OL, attention as OA
 from _parity import (ATTN_REL_L2, assert_attn_close, attn_bound, pool_absmax, ROW_REL_L2, np64, rel_l2, to_device, oracle_pool, idx_pool,
@@ -305,6 +305,78 @@ def test_attention(name):
     W = np.stack([want[q] for q in range(cpu["nq"])])
     assert_attn_close(got, W, pool_absmax((gpu["main_data"], gpu["main_scale"]), (gpu["swa_data"], gpu["swa_scale"])))
     assert np.max(np.abs(glse - np.stack([lse[q] for q in range(cpu["nq"])]))) <= 1e-3
+
+
+SELECT_ATTEND = {
+    # 32 decode rows of 64 heads: one cluster of four CTAs per row, so the top-k runs inside the attention kernel;
+    # ragged contexts, rows below k visible entries (the identity top-k) and rows near the 16,384-score limit
+    "c4a_decode_32": S("c4a_decode_32", cached=[int(x) for x in np.random.default_rng(30).integers(100, 65500, 30)]
+                       + [1500, 65535], new=[1] * 32, seed=30),
+    "c4a_decode_32_fp8": S("c4a_decode_32_fp8", cached=[int(x) for x in np.random.default_rng(31).integers(100, 40000, 32)],
+                           new=[1] * 32, main_dtype="fp8", swa_dtype="fp8", seed=31),
+}
+
+
+def _fused_pair(name):
+    cpu = synth.make_case(SELECT_ATTEND[name], "cpu")
+    gpu = to_device(cpu)
+    fused, separate = LayerStep(gpu, fused_select=True), LayerStep(gpu)
+    assert fused.fused_select and fused.select_attend_kernels == 1, "the case must run the one-kernel path"
+    return cpu, gpu, fused, separate
+
+
+@pytest.mark.parametrize("name", list(SELECT_ATTEND))
+def test_fused_topk_attention_equals_separate_calls(name):
+    """The fused call selects exactly the top-k dsa_topk selects and attends exactly as dsa_sparse_attn_decode
+    does over it (the same kernel code after the selection): indices, output and lse bit-identical; the output
+    also matches the oracle."""
+    cpu, gpu, fused, separate = _fused_pair(name)
+    separate.run()
+    torch.cuda.synchronize()
+    t_sep, o_sep, l_sep = separate.topk.clone(), separate.out.clone(), separate.lse.clone()
+    fused.run()
+    torch.cuda.synchronize()
+    assert int(fused.status.item()) == 0 and int(separate.status.item()) == 0
+    assert torch.equal(fused.topk, t_sep)
+    assert torch.equal(fused.out, o_sep)
+    assert torch.equal(fused.lse, l_sep)
+    spec, epb = cpu["spec"], cpu["epb"]
+    main = oracle_pool(gpu["main_data"], gpu["main_scale"], epb)
+    swa = oracle_pool(gpu["swa_data"], gpu["swa_scale"], 256)
+    want, lse = OL.sparse_attn(np64(cpu["q"]), np64(cpu["q_pos"]), np64(cpu["q_req"]), spec.kind, np64(fused.topk),
+                               main, np64(cpu["bt_main"]), swa, np64(cpu["bt_swa"]), spec.window, SM_SCALE,
+                               spec.rope_dim)
+    W = np.stack([want[q] for q in range(cpu["nq"])])
+    assert_attn_close(np64(fused.out), W, pool_absmax((gpu["main_data"], gpu["main_scale"]),
+                                                      (gpu["swa_data"], gpu["swa_scale"])))
+    assert np.max(np.abs(np64(fused.lse) - np.stack([lse[q] for q in range(cpu["nq"])]))) <= 1e-3
+    # the indices against the oracle's top-k of the same scores
+    scores, nv = np64(fused.scores), np64(fused.n_visible)
+    for q in range(cpu["nq"]):
+        assert list(np64(fused.topk)[q]) == list(OL.topk(scores[q], int(nv[q]), spec.topk)), q
+
+
+def test_fused_topk_attention_bad_visible_count():
+    """A row whose visible count exceeds its score row is a device fault in both forms: its top-k row is all -1,
+    its attention sees the window only, and every other row is unchanged."""
+    cpu, gpu, fused, separate = _fused_pair("c4a_decode_32")
+    bad = 5
+    outs = []
+    for st in (separate, fused):
+        st.compress()
+        st.index()
+        st.n_visible[bad] = st.ld + 4
+        if st is fused:
+            st.select_attend()
+        else:
+            st.select()
+            st.attend()
+        torch.cuda.synchronize()
+        assert int(st.status.item()) == dsa.DSA_ERR_DEVICE_FAULT
+        assert bool((st.topk[bad] == -1).all())
+        outs.append((st.topk.clone(), st.out.clone(), st.lse.clone()))
+    for x, y in zip(*outs):
+        assert torch.equal(x, y)
 
 
 SHARP = {
