@@ -916,7 +916,14 @@ static dsa_status_t launch_index(const CUtensorMap& kmap, const CUtensorMap& qma
         cudaSuccess)
         return DSA_ERR_CUDA;
     a.total_items = (long long)a.items * a.n_groups;
-    const long long grid = std::min<long long>(a.total_items, (long long)sm_count() * ctas_per_sm);
+    // Two CTAs per SM fill the GPU only if every SM is free: the compressor that the indexer follows (launched
+    // programmatically, so still running on some SMs) leaves room for one indexer CTA there, and the CTAs that
+    // did not fit started a compressor's duration late with a full static share (measured on the decode batch:
+    // 16 of 304).  A fifth of the SMs' second slots is left out: every CTA starts at once, each with a share
+    // a few percent larger (decode step 44.7 -> 43.6 us; leaving out 0, 8, 16, 24, 32 slots measured 44.7, 44.3,
+    // 43.7, 43.9, 43.6 us).
+    const long long slots = ctas_per_sm == 2 ? 2LL * sm_count() - sm_count() / 5 : (long long)sm_count();
+    const long long grid = std::min<long long>(a.total_items, slots);
     if (launch_pdl(index_kernel<DIM, HEADS, TPI, N16>, dim3((unsigned)std::max<long long>(grid, 1)), dim3(idx_threads<TPI>()), smem,
                    st, kmap, qmap, a) != cudaSuccess)
         return DSA_ERR_CUDA;
