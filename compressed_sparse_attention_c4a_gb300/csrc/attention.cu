@@ -152,19 +152,20 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
 //
 // Inside a CTA (512 threads), warp-specialised and pipelined over four 32 KB key stages (a stage is
 // gathered again as soon as its sub-tile's P V is done, so up to three gathers run ahead of the math):
-//   warps 6-15 gather: resolve keys a round (10 sub-tiles) ahead (top-k index -> block table ->
+//   warps 4 + MW .. 15 gather (MW MMA warps below: 2 for bf16 rows, 4 for e4m3 rows): resolve keys a round
+//              (one sub-tile per gather warp) ahead (top-k index -> block table ->
 //              physical row, tables cached in shared memory), prefetch later rounds into L2, and copy
 //              the rows into a stage with cp.async, 128B-swizzled, laid out [64-dim chunk][32 keys]
 //              [128 B]; e4m3 rows are converted to bf16 on the way, their scales kept beside the stage.
 //              Gathered rows are read with an evict-first L2 policy (each serves one query row);
-//   warps 4-5  issue the MMAs, one elected lane each (an MMA's issue costs the issuing warp about 49
-//              cycles at these shapes, so two warps issue twice as fast); warp 4 also loads the query rows
-//              (TMA, one 64-dim box per lane):
-//              S   = Q K^T   : M = 64 (heads), N = 32 keys, K = 512 split in halves, warp 4 summing dims
-//                              0-255 and warp 5 dims 256-511 into two accumulators (TMEM lanes = heads,
-//                              columns = keys) that the softmax adds;
+//   warps 4 .. 3 + MW issue the MMAs, one elected lane each (an MMA's issue costs the issuing warp about
+//              49 cycles at these shapes, so MW warps issue MW times as fast as one, up to the tensor pipe's
+//              own rate at M = 64); warp 4 also loads the query rows (TMA, one 64-dim box per lane):
+//              S   = Q K^T   : M = 64 (heads), N = 32 keys, K = 512 split in MW parts, warp 4 + q summing
+//                              dims (512 / MW) q .. into its own accumulator (TMEM lanes = heads,
+//                              columns = keys); the softmax adds the MW partial sums;
 //              O^T += V^T P^T: M = 128 dims per MMA (the stage read MN-major, K = V), N = NH heads,
-//                              K = 32 keys; four 128-dim accumulators, tiles 0-1 from warp 4, 2-3 from 5;
+//                              K = 32 keys; four 128-dim accumulators, 4 / MW tiles per MMA warp;
 //              S of sub-tile i + 1 is issued before O^T of sub-tile i, so it overlaps the softmax;
 //   warps 0-3  softmax, one thread per head (lanes 0-15 of each quadrant hold the M = 64 rows): the
 //              32 logits of a sub-tile are a row of TMEM, so max and sum are thread-local; P is
@@ -180,13 +181,19 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
 // ---------------------------------------------------------------------------------------------
 constexpr int kClKeys = 32;                 // keys per sub-tile
 constexpr int kClStages = 4;                // key stages in flight (a stage is free again after its P V)
-constexpr int kClMmaWarps = 2;              // warps 4 and 5
-constexpr int kClFirstGather = 4 + kClMmaWarps;
-constexpr int kClGatherWarps = 10;          // warps 6 .. 15
-constexpr int kClThreads = 32 * (kClFirstGather + kClGatherWarps);
-constexpr int kClGatherThreads = 32 * kClGatherWarps;
-constexpr int kClRound = kClGatherThreads / kClKeys;   // sub-tiles resolved per round (10)
-constexpr int kClRing = 2 * kClRound;                  // resolved sub-tiles kept (a ring of 20)
+constexpr int kClThreads = 512;             // 16 warps: 4 softmax, MW issuing MMAs, the rest gathering
+// Warp roles for MW MMA-issuing warps (4 .. 3 + MW); the gather warps follow.  bf16 rows take MW = 2 (the
+// gather, ten warps strong, sets the pace); e4m3 rows, half the bytes, MW = 4 (the MMA issue sets it).
+template <int MW>
+struct ClRoles {
+    static constexpr int kMma = MW;
+    static constexpr int kFirstGather = 4 + MW;
+    static constexpr int kGatherWarps = 16 - kFirstGather;
+    static constexpr int kGatherThreads = 32 * kGatherWarps;
+    static constexpr int kRound = kGatherThreads / kClKeys;  // sub-tiles resolved per round
+    static constexpr int kRing = 2 * kRound;                 // resolved sub-tiles kept
+};
+constexpr int kClRingMax = ClRoles<2>::kRing;
 constexpr int kClStage = kClKeys * kD * 2;
 static_assert(kClKeys == 32, "one 32-bit key mask and 32 S columns per sub-tile");
 static_assert(kClThreads == 512, "16 warps");
@@ -203,8 +210,8 @@ struct ClSmem {
     static constexpr int kOffK = kOffQ + kQ;                        // key stages; received tiles
     static constexpr int kOffP = kOffK + kClStages * kClStage;      // two P^T buffers; output staging at the end
     static constexpr int kOffRow = kOffP + 2 * kP;                  // int [ring][32]: physical rows (-1 masked)
-    static constexpr int kOffPool = kOffRow + kClRing * kClKeys * 4;  // uint8 [ring][32]: 1 main, 2 window
-    static constexpr int kOffKsc = kOffPool + kClRing * kClKeys;    // float [stages][32]: e4m3 row scales
+    static constexpr int kOffPool = kOffRow + kClRingMax * kClKeys * 4;  // uint8 [ring][32]: 1 main, 2 window
+    static constexpr int kOffKsc = kOffPool + kClRingMax * kClKeys;    // float [stages][32]: e4m3 row scales
     static constexpr int kOffMask = kOffKsc + kClStages * kClKeys * 4;  // uint32 [stages]: valid keys of a stage
     static constexpr int kOffAlpha = kOffMask + kClStages * 4;      // float [2][NH]
     static constexpr int kOffVote = kOffAlpha + 2 * NH * 4;         // int [2][4]
@@ -226,7 +233,7 @@ struct ClSmem {
     static_assert(3 * kTile <= kQ, "the sent tiles fit in the query rows");
     static_assert(6 * kTile <= kQ + kClStages * kClStage, "the received tiles fit after them");
     static_assert(NH * 128 * 2 <= 2 * kP, "an output tile must fit in the P^T buffers");
-    static constexpr int kTmemCols = 128 + 4 * NH <= 256 ? 256 : 512;
+    static constexpr int kTmemCols = 512;  // S: [2 buffers][4 parts][32 keys]; O^T: [4 tiles][NH heads]
 };
 
 // Byte offset of element (row r, element e) in a tile of 128B-swizzled atoms whose rows are 128 bytes
@@ -244,6 +251,7 @@ template <int NH, bool FP8, bool FUSED>
 __global__ void __launch_bounds__(kClThreads, 1)
     attn_cl_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap, AttnArgs a) {
     using L = ClSmem<NH>;
+    using Ro = ClRoles<FP8 ? 4 : 2>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sQ = smem_u32(smem + L::kOffQ), sK = smem_u32(smem + L::kOffK), sP = smem_u32(smem + L::kOffP);
@@ -281,11 +289,11 @@ __global__ void __launch_bounds__(kClThreads, 1)
         DSA_STAMP_NS(31);
         DSA_STAMP(0);
         for (int b = 0; b < kClStages; ++b) {
-            mbar_init(&full[b], kClGatherThreads);
-            mbar_init(&pvdone[b], kClMmaWarps);
+            mbar_init(&full[b], Ro::kGatherThreads);
+            mbar_init(&pvdone[b], Ro::kMma);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&sfull[b], kClMmaWarps);
+            mbar_init(&sfull[b], Ro::kMma);
             mbar_init(&pfull[b], 4);
         }
         mbar_init(qfull, 1);
@@ -304,7 +312,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t tS = tmem, tO = tmem + 128;  // S: [2 buffers][2 halves][32 columns]; O^T: [4 tiles][NH]
+    const uint32_t tS = tmem, tO = tmem + 2 * Ro::kMma * kClKeys;  // S: [2 buffers][MW parts][32]; O^T: [4][NH]
     if (tid == 0) DSA_STAMP(1);
     cluster_arrive_relaxed();  // phase 0: this CTA has started (waited on before distributed shared memory use)
 
@@ -339,12 +347,12 @@ __global__ void __launch_bounds__(kClThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(qfull);
     }
-    const int gt = tid - 32 * kClFirstGather, gw = warp - kClFirstGather;
-    if (warp >= kClFirstGather && n_mine > 0) {
+    const int gt = tid - 32 * Ro::kFirstGather, gw = warp - Ro::kFirstGather;
+    if (warp >= Ro::kFirstGather && n_mine > 0) {
         // the request's main block table (when it has at most kBtCache blocks) and the window pool's blocks
         // of positions wlo .. m; a key then resolves with one global load (its top-k index) at most
         if (bt_cached)
-            for (int b = gt; b < a.main_bt.max_blocks; b += kClGatherThreads)
+            for (int b = gt; b < a.main_bt.max_blocks; b += Ro::kGatherThreads)
                 s_bt[b] = __ldg(a.main_bt.table + (long long)r * a.main_bt.max_blocks + b);
         if (gt < 8) {
             const int lb = wlo / kBlockPositions + gt;
@@ -352,7 +360,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
                             ? __ldg(a.swa_bt.table + (long long)r * a.swa_bt.max_blocks + lb)
                             : -1;
         }
-        named_bar_sync(1, kClGatherThreads);  // cached tables visible to every gather thread
+        named_bar_sync(1, Ro::kGatherThreads);  // cached tables visible to every gather thread
     }
     pdl_wait();  // global memory the preceding kernel writes, and every output, only below
     pdl_launch_dependents();
@@ -384,14 +392,14 @@ __global__ void __launch_bounds__(kClThreads, 1)
     }
     bool ok = true;
 
-    if (warp >= kClFirstGather) {
+    if (warp >= Ro::kFirstGather) {
         // ---- gather warps: resolve keys a round ahead, prefetch rows into L2, copy with cp.async -----
         const uint64_t row_policy = l2_evict_first();  // a gathered row serves this query row only
-        // sub-tiles [R * kClRound, (R + 1) * kClRound): thread -> sub-tile R * kClRound + gt / 32, key gt % 32.
+        // sub-tiles [R * Ro::kRound, (R + 1) * Ro::kRound): thread -> sub-tile R * Ro::kRound + gt / 32, key gt % 32.
         // Step 1: the key's top-k index (or entry / window position), no dependent load.
         auto key_id = [&](int R, int* id) -> int {  // returns j (the key's index in the row), -1 if none
-            const int i = R * kClRound + gt / kClKeys;
-            if (gt >= kClRound * kClKeys || i >= n_mine) return -1;
+            const int i = R * Ro::kRound + gt / kClKeys;
+            if (gt >= Ro::kRound * kClKeys || i >= n_mine) return -1;
             const int j = (g_lo + crank + csize * i) * kClKeys + gt % kClKeys;
             *id = -1;
             if (j < n_keys && j < n_comp) *id = FUSED ? s_topk[j] : (a.topk ? __ldg(a.topk + (long long)row * a.k + j) : j);
@@ -399,7 +407,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         };
         // Step 2: index -> physical row through the cached tables (or global memory), L2 prefetch, ring slot.
         auto finish_key = [&](int R, int j, int id) {
-            const int i = R * kClRound + gt / kClKeys;
+            const int i = R * Ro::kRound + gt / kClKeys;
             if (j < 0) return;
             int v = -1, pool = 1;
             if (j < ncp) {
@@ -440,8 +448,8 @@ __global__ void __launch_bounds__(kClThreads, 1)
                                                 : static_cast<const uint8_t*>(a.main.data);
                 prefetch_l2(base + (long long)v * kRowBytes, kRowBytes);
             }
-            s_row[(i % kClRing) * kClKeys + gt % kClKeys] = v;
-            s_pool[(i % kClRing) * kClKeys + gt % kClKeys] = (uint8_t)pool;
+            s_row[(i % Ro::kRing) * kClKeys + gt % kClKeys] = v;
+            s_pool[(i % Ro::kRing) * kClKeys + gt % kClKeys] = (uint8_t)pool;
         };
         auto resolve_round = [&](int R) {
             int id = -1;
@@ -452,20 +460,20 @@ __global__ void __launch_bounds__(kClThreads, 1)
         // nothing); every gather thread reads its rows' codes before any writes, since the bf16 rows overwrite
         // the codes' half of the stage.  Called by all gather threads alike.
         auto widen_fp8 = [&](int st) {
-            constexpr int kRowsPerWarp = (kClKeys + kClGatherWarps - 1) / kClGatherWarps;
+            constexpr int kRowsPerWarp = (kClKeys + Ro::kGatherWarps - 1) / Ro::kGatherWarps;
             const uint32_t stage = sK + st * kClStage;
             const uint8_t* raw = smem + L::kOffK + st * kClStage + kClStage / 2;
-            named_bar_sync(1, kClGatherThreads);  // every thread's copies of the sub-tile have landed
+            named_bar_sync(1, Ro::kGatherThreads);  // every thread's copies of the sub-tile have landed
             uint4 code[kRowsPerWarp];
 #pragma unroll
             for (int u = 0; u < kRowsPerWarp; ++u) {
-                const int kk = gw + u * kClGatherWarps;
+                const int kk = gw + u * Ro::kGatherWarps;
                 code[u] = kk < kClKeys ? *reinterpret_cast<const uint4*>(raw + kk * kD + lane * 16) : make_uint4(0, 0, 0, 0);
             }
-            named_bar_sync(1, kClGatherThreads);  // all codes read: the bf16 rows may overwrite them
+            named_bar_sync(1, Ro::kGatherThreads);  // all codes read: the bf16 rows may overwrite them
 #pragma unroll
             for (int u = 0; u < kRowsPerWarp; ++u) {
-                const int kk = gw + u * kClGatherWarps;
+                const int kk = gw + u * Ro::kGatherWarps;
                 if (kk < kClKeys) {
                     const uint32_t w4[4] = {code[u].x, code[u].y, code[u].z, code[u].w};
                     uint32_t bf[8];
@@ -501,14 +509,15 @@ __global__ void __launch_bounds__(kClThreads, 1)
                         if constexpr (FP8) widen_fp8(sig % kClStages);
                         fence_proxy_async_smem();  // cp.async writes -> visible to the tensor core (async proxy)
                         mbar_arrive(&full[sig % kClStages]);
+                        if (gt == 0) DSA_TRACE(sig, 1);
                     }
                 }
                 // the stage's previous sub-tile has been multiplied into O^T
                 ok = ok && mbar_wait_bounded(&pvdone[s], ((i - kClStages) / kClStages) & 1, kWaitLimitNs);
             }
-            named_bar_sync(1, kClGatherThreads);  // sub-tile i's rows are visible; earlier gathers are done
-            const int* rows = s_row + (i % kClRing) * kClKeys;
-            const uint8_t* pools = s_pool + (i % kClRing) * kClKeys;
+            named_bar_sync(1, Ro::kGatherThreads);  // sub-tile i's rows are visible; earlier gathers are done
+            const int* rows = s_row + (i % Ro::kRing) * kClKeys;
+            const uint8_t* pools = s_pool + (i % Ro::kRing) * kClKeys;
             if (gt < kClKeys) {  // the first gather warp: the stage's key mask for the softmax
                 const uint32_t bits = __ballot_sync(0xffffffffu, rows[gt] >= 0);
                 if (lane == 0) s_mask[s] = bits;
@@ -516,7 +525,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             if (ok && !FP8) {
                 const uint32_t stage = sK + s * kClStage;
 #pragma unroll 1
-                for (int kk = gw; kk < kClKeys; kk += kClGatherWarps) {
+                for (int kk = gw; kk < kClKeys; kk += Ro::kGatherWarps) {
                     const int rr = rows[kk];
                     const uint8_t* base = pools[kk] == 2 ? static_cast<const uint8_t*>(a.swa.data)
                                                          : static_cast<const uint8_t*>(a.main.data);
@@ -531,11 +540,11 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 // e4m3 rows: copied as they are into the upper half of the stage (row kk at 16 KB + 512 kk, lane
                 // l the codes of dims 16 l .. 16 l + 15), the row scale beside the stage; they become bf16 in
                 // place once they have landed (widen_fp8 below), so copies of three sub-tiles stay in flight
-                constexpr int kRowsPerWarp = (kClKeys + kClGatherWarps - 1) / kClGatherWarps;
+                constexpr int kRowsPerWarp = (kClKeys + Ro::kGatherWarps - 1) / Ro::kGatherWarps;
                 const uint32_t raw = sK + s * kClStage + kClStage / 2;
 #pragma unroll
                 for (int u = 0; u < kRowsPerWarp; ++u) {
-                    const int kk = gw + u * kClGatherWarps;
+                    const int kk = gw + u * Ro::kGatherWarps;
                     if (kk < kClKeys) {
                         const int rr = rows[kk];
                         const dsa_pool_t& pl = pools[kk] == 2 ? a.swa : a.main;
@@ -548,15 +557,16 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 }
             }
             cp_async_commit();
+            if (gt == 0) DSA_TRACE(i, 0);
             if (i == 0 && gt == 0) DSA_STAMP(3);
             if (i == 0) {  // the first round's later sub-tiles start moving into L2 once sub-tile 0 is under way
                 constexpr int kRowBytes = FP8 ? kD : 2 * kD;
-                for (int t = kClKeys + gt; t < kClRound * kClKeys; t += kClGatherThreads) {
+                for (int t = kClKeys + gt; t < Ro::kRound * kClKeys; t += Ro::kGatherThreads) {
                     const int ii = t / kClKeys;
                     if (ii >= n_mine) break;
-                    const int rr = s_row[(ii % kClRing) * kClKeys + (t % kClKeys)];
+                    const int rr = s_row[(ii % Ro::kRing) * kClKeys + (t % kClKeys)];
                     if (rr >= 0) {
-                        const uint8_t* base = s_pool[(ii % kClRing) * kClKeys + (t % kClKeys)] == 2
+                        const uint8_t* base = s_pool[(ii % Ro::kRing) * kClKeys + (t % kClKeys)] == 2
                                                   ? static_cast<const uint8_t*>(a.swa.data)
                                                   : static_cast<const uint8_t*>(a.main.data);
                         prefetch_l2(base + (long long)rr * kRowBytes, kRowBytes);
@@ -565,7 +575,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             }
             // the next round of keys once this one's second sub-tile is under way: its rows reach L2 while
             // the sub-tiles in between are processed (ring slots of sub-tiles < i are free by now)
-            if (i % kClRound == 2) resolve_round(i / kClRound + 1);
+            if (i % Ro::kRound == 2) resolve_round(i / Ro::kRound + 1);
             // a thread keeps up to three sub-tiles of copies in flight: with three outstanding, the oldest is
             // reported once its group has landed
             if (i - sig >= 2) {
@@ -573,6 +583,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 if constexpr (FP8) widen_fp8(sig % kClStages);
                 fence_proxy_async_smem();
                 mbar_arrive(&full[sig % kClStages]);
+                if (gt == 0) DSA_TRACE(sig, 1);
                 ++sig;
             }
         }
@@ -582,6 +593,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 if constexpr (FP8) widen_fp8(sig % kClStages);
                 fence_proxy_async_smem();
                 mbar_arrive(&full[sig % kClStages]);
+                if (gt == 0) DSA_TRACE(sig, 1);
             }
         }
         if (!ok) report(a.status, DSA_ERR_TIMEOUT);
@@ -589,30 +601,30 @@ __global__ void __launch_bounds__(kClThreads, 1)
         // ---- MMA issue: two warps, each waiting whole and issuing from one elected lane --------------
         // S of sub-tile i + 1 goes first when its keys are in (it overlaps the softmax of sub-tile i), but
         // the product of sub-tile i never waits behind a gather that has not arrived.
-        const int half = warp - 4;
+        const int part = warp - 4;  // this warp's 512 / MW dims of S and its 4 / MW 128-dim tiles of O^T
         const uint32_t idesc_s = idesc_bf16(kClKeys, 0, 64), idesc_o = idesc_bf16(NH, 1, 128);
         const uint64_t dq = sw128_desc(sQ, 16, 1024);
         if (n_mine > 0) ok = mbar_wait_bounded(qfull, 0, kWaitLimitNs);
-        auto issue_s = [&](int i) {  // this warp's half of the 512 dims into its own accumulator
+        auto issue_s = [&](int i) {  // this warp's 512 / MW dims into its own accumulator
             const int s = i % kClStages;
             tc_fence_after();
             const uint64_t dk = sw128_desc(sK + s * kClStage, 16, 1024);
 #pragma unroll
-            for (int k = 0; k < kD / 32; ++k) {  // 64-dim chunks are 64 query rows / 32 key rows apart
-                const int ks = half * (kD / 32) + k;
+            for (int k = 0; k < kD / (16 * Ro::kMma); ++k) {  // 64-dim chunks: 64 query rows / 32 key rows apart
+                const int ks = part * (kD / (16 * Ro::kMma)) + k;
                 const uint64_t oq = (uint64_t)((((ks >> 2) * (64 * 128)) + (ks & 3) * 32) >> 4);
                 const uint64_t ok_ = (uint64_t)((((ks >> 2) * (kClKeys * 128)) + (ks & 3) * 32) >> 4);
-                mma_bf16_ss_elect(tS + ((i & 1) * 2 + half) * kClKeys, dq + oq, dk + ok_, idesc_s, k > 0 ? 1u : 0u);
+                mma_bf16_ss_elect(tS + ((i & 1) * Ro::kMma + part) * kClKeys, dq + oq, dk + ok_, idesc_s, k > 0 ? 1u : 0u);
             }
             mma_commit_elect(&sfull[i & 1]);
         };
-        auto issue_pv = [&](int i) {  // this warp's two 128-dim tiles
+        auto issue_pv = [&](int i) {  // this warp's 128-dim tiles
             const int s = i % kClStages;
             tc_fence_after();
             const uint64_t dv = sw128_desc(sK + s * kClStage, kClKeys * 128, 1024);
             const uint64_t dp = sw128_desc(sP + (i & 1) * L::kP, 16, 1024);
 #pragma unroll
-            for (int mt = 2 * half; mt < 2 * half + 2; ++mt)
+            for (int mt = part * (4 / Ro::kMma); mt < (part + 1) * (4 / Ro::kMma); ++mt)
 #pragma unroll
                 for (int ks = 0; ks < kClKeys / 16; ++ks)
                     mma_bf16_ss_elect(tO + mt * NH,
@@ -631,12 +643,14 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 if (next_s < n_mine && next_s <= i + 1 &&
                     __all_sync(0xffffffffu, mbar_try_wait(&full[next_s % kClStages], (next_s / kClStages) & 1))) {
                     issue_s(next_s);
+                    if (tid == 128) DSA_TRACE(next_s, 2);
                     if (next_s == 0 && tid == 128) DSA_STAMP(4);
                     ++next_s;
                     continue;
                 }
                 if (next_s > i && __all_sync(0xffffffffu, mbar_try_wait(&pfull[i & 1], (i >> 1) & 1))) {
                     issue_pv(i);
+                    if (tid == 128) DSA_TRACE(i, 5);
                     if (i == n_mine - 1 && tid == 128) DSA_STAMP(6);
                     pv_done = true;
                     continue;
@@ -661,23 +675,29 @@ __global__ void __launch_bounds__(kClThreads, 1)
             if (i >= 2)  // P^T buffer free: the product of sub-tile i - 2 is done
                 ok = ok && mbar_wait_bounded(&pvdone[(i - 2) % kClStages], ((i - 2) / kClStages) & 1, kWaitLimitNs);
             ok = __all_sync(0xffffffffu, ok);
+            if (tid == 0) DSA_TRACE(i, 3);
             float sv[kClKeys];
             float alpha = 1.f;
             bool resc = false;
             if (ok) {
                 tc_fence_after();
-                float sh[kClKeys];  // the second half-sum of the logits
-                tmem_ld_nowait<16>(tS + (s * 2) * kClKeys + lane_off, *reinterpret_cast<float(*)[16]>(sv));
-                tmem_ld_nowait<16>(tS + (s * 2) * kClKeys + lane_off + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
-                tmem_ld_nowait<16>(tS + (s * 2 + 1) * kClKeys + lane_off, *reinterpret_cast<float(*)[16]>(sh));
-                tmem_ld_nowait<16>(tS + (s * 2 + 1) * kClKeys + lane_off + 16, *reinterpret_cast<float(*)[16]>(sh + 16));
-                tmem_wait_ld();
-                tmem_regs_after_wait<16>(*reinterpret_cast<float(*)[16]>(sv));
-                tmem_regs_after_wait<16>(*reinterpret_cast<float(*)[16]>(sv + 16));
-                tmem_regs_after_wait<16>(*reinterpret_cast<float(*)[16]>(sh));
-                tmem_regs_after_wait<16>(*reinterpret_cast<float(*)[16]>(sh + 16));
+                float sh[kClKeys];  // a further partial sum of the logits
+                // the MW partial products summed in order: ((p0 + p1) + p2) + ...
+                tmem_ld_nowait<16>(tS + (s * Ro::kMma) * kClKeys + lane_off, *reinterpret_cast<float(*)[16]>(sv));
+                tmem_ld_nowait<16>(tS + (s * Ro::kMma) * kClKeys + lane_off + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
+#pragma unroll 1
+                for (int pp = 1; pp < Ro::kMma; ++pp) {
+                    tmem_ld_nowait<16>(tS + (s * Ro::kMma + pp) * kClKeys + lane_off, *reinterpret_cast<float(*)[16]>(sh));
+                    tmem_ld_nowait<16>(tS + (s * Ro::kMma + pp) * kClKeys + lane_off + 16,
+                                       *reinterpret_cast<float(*)[16]>(sh + 16));
+                    tmem_wait_ld();
+                    tmem_regs_after_wait<16>(*reinterpret_cast<float(*)[16]>(sv));
+                    tmem_regs_after_wait<16>(*reinterpret_cast<float(*)[16]>(sv + 16));
+                    tmem_regs_after_wait<16>(*reinterpret_cast<float(*)[16]>(sh));
+                    tmem_regs_after_wait<16>(*reinterpret_cast<float(*)[16]>(sh + 16));
 #pragma unroll
-                for (int j = 0; j < kClKeys; ++j) sv[j] += sh[j];
+                    for (int j = 0; j < kClKeys; ++j) sv[j] += sh[j];
+                }
                 const uint32_t vm = s_mask[st];
                 float mx = -INFINITY;
                 if (!FP8 && vm == 0xFFFFFFFFu) {  // every key of the stage present (the same for all threads)
@@ -768,6 +788,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&pfull[s]);
+            if (tid == 0) DSA_TRACE(i, 4);
             if (i == 0 && tid == 0) DSA_STAMP(5);
         }
         if (n_mine > 0) {  // the last product must be complete before O^T is read
