@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
 //              physical row, tables cached in shared memory), prefetch later rounds into L2, and copy
 //              the rows into a stage with cp.async, 128B-swizzled, laid out [64-dim chunk][32 keys]
 //              [128 B]; e4m3 rows are converted to bf16 on the way, their scales kept beside the stage.
-//              Gathered rows are read with an evict-first L2 policy (each serves one query row);
+//              Decode rows are gathered with an evict-first L2 policy (each serves one query row);
 //   warps 4 .. 3 + MW issue the MMAs, one elected lane each (an MMA's issue costs the issuing warp about
 //              49 cycles at these shapes, so MW warps issue MW times as fast as one, up to the tensor pipe's
 //              own rate at M = 64); warp 4 also loads the query rows (TMA, one 64-dim box per lane):
@@ -394,7 +394,9 @@ __global__ void __launch_bounds__(kClThreads, 1)
 
     if (warp >= Ro::kFirstGather) {
         // ---- gather warps: resolve keys a round ahead, prefetch rows into L2, copy with cp.async -----
-        const uint64_t row_policy = l2_evict_first();  // a gathered row serves this query row only
+        // decode rows (one query row per request): a gathered row serves this query row only and leaves L2 first;
+        // prefill rows of one request share their keys, which keep the default policy
+        const uint64_t row_policy = a.q_req ? l2_evict_normal() : l2_evict_first();
         // sub-tiles [R * Ro::kRound, (R + 1) * Ro::kRound): thread -> sub-tile R * Ro::kRound + gt / 32, key gt % 32.
         // Step 1: the key's top-k index (or entry / window position), no dependent load.
         auto key_id = [&](int R, int* id) -> int {  // returns j (the key's index in the row), -1 if none

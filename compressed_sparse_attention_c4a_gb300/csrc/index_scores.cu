@@ -360,7 +360,9 @@ __global__ void __maxnreg__(TPI == 2 ? 168 : 128) index_kernel(const __grid_cons
             if (valid) locate(idx, &g, &t);
             return item_info<TPI>(a, valid, g, t, grp_r, grp_mv);
         };
-        const uint64_t key_policy = l2_evict_first();  // every key page is read once
+        // with at most one query group per request (decode) every key page is read once: it leaves L2 first;
+        // groups that share a request's pages (prefill) keep the default policy, so the pages stay for the next
+        const uint64_t key_policy = a.n_groups <= a.bt.batch ? l2_evict_first() : l2_evict_normal();
         int n = 0, ps = 0, pphase = 0;  // items issued; stage index and its phase parity
         int pb = 0, pbph = 0;           // item slot index and its phase parity
         int cur_g = -1, gb = 1, guse[2] = {0, 0};  // group in the current buffer, buffer index, loads per buffer
