@@ -222,7 +222,7 @@ struct ClSmem {
     static constexpr int kOffSwb = kOffBt + kBtCache * 4;           // int [8]: window-pool blocks from that of wlo
     static constexpr int kOffFault = kOffSwb + 32;                  // int: a key of this CTA hit a device fault
     static constexpr int kOffRope = kOffFault + 16;                 // float [32][2]: cos, sin of each pair's angle at m
-    static constexpr int kBars = 2 * kClStages + 6;
+    static constexpr int kBars = 2 * kClStages + 8;
     static constexpr int kOffBar = kOffRope + 256;                  // kBars mbarriers, TMEM address
     static constexpr int kOffTopk = kOffBar + kBars * 8 + 16;       // int [kFusedK]: the row's top-k (fused)
     static constexpr int kBytes = kOffTopk + kFusedK * 4;
@@ -274,8 +274,8 @@ __global__ void __launch_bounds__(kClThreads, 1)
     uint64_t* pfull = sfull + 2;                                        // [2] P^T written (4 warps)
     uint64_t* pvdone = pfull + 2;                                       // [stages] O^T += V^T P^T done (2 commits)
     uint64_t* qfull = pvdone + kClStages;                               // query rows loaded
-    uint64_t* xfull = qfull + 1;                                        // exchanged tiles loaded
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(xfull + 1);
+    uint64_t* xfull = qfull + 1;                                        // [3] each received tile slot loaded
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(xfull + 3);
     volatile int* s_fault = reinterpret_cast<volatile int*>(smem + L::kOffFault);
     float* s_rc = reinterpret_cast<float*>(smem + L::kOffRope);
 
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             mbar_init(&pfull[b], 4);
         }
         mbar_init(qfull, 1);
-        mbar_init(xfull, 1);
+        for (int b = 0; b < 3; ++b) mbar_init(&xfull[b], 1);
         *s_fault = 0;
         fence_barrier_init();
     }
@@ -859,7 +859,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     if constexpr (!FUSED) cluster_wait();  // phase 0: every CTA of the cluster has started (fused: waited above)
     if (tid == 0) DSA_STAMP(17);
     if (csize > 1 && tid == 0)  // before any peer can push (pushes follow phase 1)
-        mbar_arrive_expect_tx(xfull, (uint32_t)((csize - 1) * tiles_per * L::kTile));
+        for (int b = 0; b < (csize - 1) * tiles_per; ++b) mbar_arrive_expect_tx(&xfull[b], (uint32_t)L::kTile);
     const float fo = *s_fault ? 1.f : 0.f;  // this CTA met a device fault: the whole row is written as zeros
     for (int h = tid; h < NH; h += kClThreads) {
         const uint32_t dst = smem_u32(s_stat + (crank * NH + h) * 4);
@@ -872,18 +872,24 @@ __global__ void __launch_bounds__(kClThreads, 1)
     cluster_arrive();  // phase 1: statistics delivered, sent tiles staged, every CTA's products complete
     cluster_wait();
     if (tid == 0) DSA_STAMP(10);
-    // 3. push: one bulk copy per sent tile, each from lane 0 of one of the last warps (the first warps compute
-    // the factors meanwhile)
-    const int pw = 15 - warp;  // sent tile of this warp
-    const bool pusher = csize > 1 && lane == 0 && pw >= 0 && pw < 4 - tiles_per;
+    // 3. push: one bulk copy per sent tile, all from lane 0 of the last warp (the first warps compute the
+    // factors meanwhile), the next CTA's tiles first, then the one after: every owner receives one CTA's tiles at
+    // a time, each tile signalling its own slot, so the owner adds the first arrivals while the rest stream in
+    const bool pusher = csize > 1 && warp == 15 && lane == 0;
     if (pusher) {
-        int t = 0, seen = -1;
-        for (; t < 4; ++t)
-            if (t % csize != crank && ++seen == pw) break;
-        const int o = t % csize;
-        const int slot = ((crank - o - 1 + csize) % csize) * tiles_per + t / csize;  // in the owner's xin
-        bulk_s2cluster(mapa_shared(smem_u32(xin + slot * L::kTile), (uint32_t)o), smem_u32(xout + pw * L::kTile),
-                       L::kTile, mapa_shared(smem_u32(xfull), (uint32_t)o));
+        for (int k = 1; k < csize; ++k) {
+            const int o = (crank + k) % csize;
+            for (int t = 0, sl = 0; t < 4; ++t) {
+                if (t % csize == crank) continue;
+                if (t % csize == o) {
+                    const int slot = ((crank - o - 1 + csize) % csize) * tiles_per + t / csize;  // in the owner's xin
+                    bulk_s2cluster(mapa_shared(smem_u32(xin + slot * L::kTile), (uint32_t)o),
+                                   smem_u32(xout + sl * L::kTile), L::kTile,
+                                   mapa_shared(smem_u32(&xfull[slot]), (uint32_t)o));
+                }
+                ++sl;
+            }
+        }
         bulk_commit();
     }
     // 4. per head: the cluster maximum M, each CTA's weight 2^(m_c - M), 1 / L; one thread per (head, CTA),
@@ -914,15 +920,24 @@ __global__ void __launch_bounds__(kClThreads, 1)
         }
     }
     if (tid == 0) DSA_STAMP(19);
-    __syncthreads();
+    if (csize > 1) {
+        // the factors reach every thread; the pushing warp (15, still issuing its copies one after another)
+        // joins through a barrier of its own with the factor threads, so that the others need not wait for it
+        static_assert(kClThreads == 512, "warps 0-14 and warp 15");
+        if (tid < NH * 4) named_bar_arrive(4, NH * 4 + 32);
+        if (warp == 15) {
+            __syncwarp();  // lane 0 has issued the pushes
+            named_bar_sync(4, NH * 4 + 32);
+        } else {
+            named_bar_sync(3, kClThreads - 32);
+        }
+    } else {
+        __syncthreads();
+    }
     if (tid == 0) DSA_STAMP(11);
     // this CTA's first owned tile leaves TMEM while the other CTAs' tiles are still arriving
     float v_first[G];
     if (have) tmem_cols(crank, v_first);
-    if (csize > 1) {
-        ok = mbar_wait_bounded(xfull, 0, kWaitLimitNs);
-        if (!ok && tid == 0) report(a.status, DSA_ERR_TIMEOUT);
-    }
     if (tid == 0) DSA_STAMP(12);
     // ---- owner: finish each owned tile; bf16 output staged as [NH][128] in the P^T buffers and stored
     // with 16-byte writes, or fp32 split partials ------------------------------------------------------
@@ -956,12 +971,18 @@ __global__ void __launch_bounds__(kClThreads, 1)
         if (tid == 0 && j == 0) DSA_STAMP(20);
 #pragma unroll
         for (int e = 0; e < G; ++e) v[e] = have ? v[e] * fown[e] : 0.f;
+        // received tiles in the order they arrive: slot si holds CTA crank + 1 + si's, and CTA crank - 1 (the
+        // last si) sends to this CTA first
 #pragma unroll
-        for (int si = 0; si < 3; ++si) {
-            if (si < csize - 1) {
+        for (int sr = 0; sr < 3; ++sr) {
+            const int si = csize - 2 - sr;
+            if (si >= 0) {
                 const int src = (crank + 1 + si) % csize;
                 const float* fsrc = s_fac + src * NH + h0;
                 const uint8_t* p = xin + (si * tiles_per + j) * L::kTile;
+                const bool landed = mbar_wait_bounded(&xfull[si * tiles_per + j], 0, kWaitLimitNs);
+                if (!landed && tid == 0) report(a.status, DSA_ERR_TIMEOUT);
+                ok = ok && landed;
 #pragma unroll
                 for (int q4 = 0; q4 < G / 4; ++q4) {
                     const uint2 w = *reinterpret_cast<const uint2*>(p + ((h0 / 4 + q4) * 128 + d) * 8);

@@ -696,5 +696,9 @@ __device__ __forceinline__ void st_cluster_v2(uint32_t addr, float x, float y) {
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// Arrive at named barrier `id` without waiting (the threads that sync on it see this thread's earlier writes).
+__device__ __forceinline__ void named_bar_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 }  // namespace dsa
