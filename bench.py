@@ -429,10 +429,11 @@ def max_over_ranks(values, device):
 
 
 def run_e2e(copies, stream, spec, args, barrier):
-    """Per step: pinned host inputs -> device, the step, output -> pinned host, for the 4 resident layers in
-    one CUDA graph.  The copies run on their own stream, as a serving loop would pipeline them: every
-    layer's inputs go in up front, each step waits only for its own, and each output comes back while
-    the next step computes.  Every byte still moves inside the timed region."""
+    """Per step: pinned host inputs -> device, the step, output -> pinned host, as a serving loop pipelines
+    them: one CUDA graph of `rounds` passes over the resident layers, the inputs of step s + len(copies) copied
+    in (on an H2D stream) once step s, which used the same device buffers, is done, and each output copied out
+    (on a D2H stream) while the next steps compute; a step starts once its inputs are in and its output buffer's
+    previous contents are out.  Every byte still moves inside the timed region."""
     names = ["x_new", "z_new", "q", "q_pos", "start_pos"]
     if spec.idx_heads:
         names += ["xi_new", "zi_new", "q8", "q_scale", "w"]
@@ -442,28 +443,46 @@ def run_e2e(copies, stream, spec, args, barrier):
     outs = [torch.empty(st.out.shape, dtype=st.out.dtype, pin_memory=True) for st in copies]
     h2d = sum(t.numel() * t.element_size() for t in hosts[0].values())
     d2h = outs[0].numel() * outs[0].element_size()
+    nc = len(copies)
+    rounds = max(1, min(8, args.steps // (4 * nc)))
+    n = nc * rounds  # steps per graph
     graph = torch.cuda.CUDAGraph()
-    copy_stream = torch.cuda.Stream(device=stream.device)
+    h2d_stream = torch.cuda.Stream(device=stream.device)
+    d2h_stream = torch.cuda.Stream(device=stream.device)
+
+    def copy_in(s):
+        i = s % nc
+        with torch.cuda.stream(h2d_stream):
+            for nm in names:
+                copies[i].case[nm].copy_(hosts[i][nm], non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(h2d_stream)
+        return ev
+
     with torch.cuda.graph(graph, stream=stream):
-        copy_stream.wait_stream(stream)  # fork
-        inputs_in = []
-        with torch.cuda.stream(copy_stream):
-            for i, st in enumerate(copies):
-                for n in names:
-                    st.case[n].copy_(hosts[i][n], non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(copy_stream)
-                inputs_in.append(ev)
-        for i, st in enumerate(copies):
-            stream.wait_event(inputs_in[i])
-            st.run()
+        h2d_stream.wait_stream(stream)  # fork
+        d2h_stream.wait_stream(stream)
+        ev_in = {s: copy_in(s) for s in range(min(nc, n))}
+        ev_out = {}
+        for s in range(n):
+            i = s % nc
+            stream.wait_event(ev_in[s])
+            if s >= nc:
+                stream.wait_event(ev_out[s - nc])  # this layer's previous output has left its buffer
+            copies[i].run()
             done = torch.cuda.Event()
             done.record(stream)
-            copy_stream.wait_event(done)
-            with torch.cuda.stream(copy_stream):
-                outs[i].copy_(st.out, non_blocking=True)
-        stream.wait_stream(copy_stream)  # join
-    reps = max(1, min(200, args.steps // (4 * len(copies))))
+            d2h_stream.wait_event(done)
+            with torch.cuda.stream(d2h_stream):
+                outs[i].copy_(copies[i].out, non_blocking=True)
+            ev_out[s] = torch.cuda.Event()
+            ev_out[s].record(d2h_stream)
+            if s + nc < n:
+                h2d_stream.wait_event(done)  # step s has read this layer's inputs
+                ev_in[s + nc] = copy_in(s + nc)
+        stream.wait_stream(h2d_stream)  # join
+        stream.wait_stream(d2h_stream)
+    reps = max(1, min(200, args.steps // n))
     with torch.cuda.stream(stream):
         for _ in range(3):
             graph.replay()
@@ -475,7 +494,7 @@ def run_e2e(copies, stream, spec, args, barrier):
             graph.replay()
         t1.record(stream)
     barrier()
-    return {"ms_step": t0.elapsed_time(t1) / (reps * len(copies)), "h2d": h2d, "d2h": d2h}
+    return {"ms_step": t0.elapsed_time(t1) / (reps * n), "h2d": h2d, "d2h": d2h}
 
 
 # ---------------------------------------------------------------------------------------------
