@@ -198,13 +198,22 @@ def peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+def kernel_source_digest(kernel):
+    """sha256 (16 hex digits) of a kernel's source file followed by the headers every kernel includes, so that a
+    change in shared device code also marks the kernel's ncu summary as stale."""
+    csrc = os.path.join(ROOT, "compressed_sparse_attention_c4a_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in (KERNEL_SOURCES[kernel], "common.cuh", "topk_cluster.cuh"):
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def ncu_traffic(kernel, workload):
     """dram bytes per launch from the committed ncu summary, or None if absent or the kernel changed."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
-    src = os.path.join(ROOT, "compressed_sparse_attention_c4a_gb300", "csrc", KERNEL_SOURCES[kernel])
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    digest = kernel_source_digest(kernel)
     txt = open(path).read()
     got_hash = got_bytes = None
     for line in txt.splitlines():

@@ -135,6 +135,9 @@ struct TopkRowScratch {
     uint32_t wt[32][2];
     uint32_t sel[2];
     uint32_t n_cand;
+    uint32_t n_above;       // this CTA's entries above the bucket b* (small-bucket path)
+    uint32_t pub[C][2];     // each CTA's (entries above b*, members of b*), written into every CTA of the cluster
+    uint32_t sel_cnt[C];    // each CTA's members of b* among the `need` best (small-bucket path)
     float red[2][32];
     float cl_mm[C][2];      // each CTA's (max, min), written into every CTA of the cluster
     uint32_t cl_tot[C][2];  // each CTA's (definite members, entries equal to T)
@@ -173,7 +176,7 @@ __device__ __forceinline__ void topk_row_cluster(cg::cluster_group& cluster, Top
     }
     for (int b = tid; b < kBins; b += THREADS) sm.hist[b] = 0;
     for (int w = tid; w < THREADS * VPT / 32; w += THREADS) sm.marks[w] = 0;
-    if (tid == 0) sm.n_cand = 0;
+    if (tid == 0) sm.n_cand = 0, sm.n_above = 0;
     if (tid == 0) DSA_STAMP(stamp0);
     float mx = -INFINITY, mn = INFINITY;
 #pragma unroll
@@ -233,6 +236,10 @@ __device__ __forceinline__ void topk_row_cluster(cg::cluster_group& cluster, Top
     if (tid == 0) DSA_STAMP(stamp0 + 2);
     const bool take_all = in_bucket == need;
     const bool rank_mode = !take_all && in_bucket <= (uint32_t)kRankMax;
+#ifdef DSA_TIMELINE
+    if (tid == 0 && g_timeline)  // (timeline builds) the bucket's size and which path resolves it
+        g_timeline[(unsigned long long)blockIdx.x * 32 + 27] = in_bucket | (take_all ? 1ull << 40 : 0) | (rank_mode ? 1ull << 41 : 0);
+#endif
     uint32_t above = 0u, inb = 0u;
 #pragma unroll
     for (int u = 0; u < VPT; ++u) {
@@ -263,35 +270,62 @@ __device__ __forceinline__ void topk_row_cluster(cg::cluster_group& cluster, Top
                 }
                 ++slot;
             }
-        cluster.sync();  // every CTA's list is complete
-        // the cluster's lists, copied into this CTA's shared memory (at most kRankMax entries in all), then
-        // each of this CTA's members is ranked against them locally
-        uint32_t nq_c[C], total_c = 0;
-#pragma unroll
-        for (int q = 0; q < C; ++q) nq_c[q] = *cluster.map_shared_rank(&sm.n_cand, q);
+        // this CTA's entries above b* (its definite members), counted now so that the output's offsets need no
+        // further exchange: they travel with the list lengths, pushed into every CTA before one cluster barrier
+        const uint32_t na_w = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(above));
+        if (lane == 0 && na_w) atomicAdd(&sm.n_above, na_w);
+        if (tid < C) sm.sel_cnt[tid] = 0;
+        __syncthreads();
+        if (tid < C) {  // (entries above b*, members of b*) into slot crank of CTA tid
+            uint32_t* dst = cluster.map_shared_rank(&sm.pub[0][0], tid);
+            dst[2 * crank] = sm.n_above;
+            dst[2 * crank + 1] = sm.n_cand;
+        }
+        cluster.sync();  // every CTA's list and counts are complete
+        // the cluster's lists, copied into this CTA's shared memory (at most kRankMax entries in all): a thread's
+        // entries of every list are requested before any is stored, so the copy costs one remote round trip
+        uint32_t nq[C], base[C], total_c = 0, longest = 0;
 #pragma unroll
         for (int q = 0; q < C; ++q) {
-            const uint32_t* rk = cluster.map_shared_rank(sm.cand_key, q);
-            const uint32_t* ri = cluster.map_shared_rank(sm.cand_idx, q);
-            for (uint32_t j = tid; j < nq_c[q]; j += THREADS)
-                if (DSA_IDX_OK(total_c + j, kRankMax, status)) {
-                    sm.all_key[total_c + j] = rk[j];
-                    sm.all_idx[total_c + j] = ri[j];
+            nq[q] = sm.pub[q][1];
+            base[q] = total_c;
+            total_c += nq[q];
+            longest = max(longest, nq[q]);
+        }
+        for (uint32_t j = tid; j < longest; j += THREADS) {
+            uint32_t kq[C], iq[C];
+#pragma unroll
+            for (int q = 0; q < C; ++q)
+                if (j < nq[q]) {
+                    kq[q] = cluster.map_shared_rank(sm.cand_key, q)[j];
+                    iq[q] = cluster.map_shared_rank(sm.cand_idx, q)[j];
                 }
-            total_c += nq_c[q];
+#pragma unroll
+            for (int q = 0; q < C; ++q)
+                if (j < nq[q] && DSA_IDX_OK(base[q] + j, kRankMax, status)) {
+                    sm.all_key[base[q] + j] = kq[q];
+                    sm.all_idx[base[q] + j] = iq[q];
+                }
         }
         __syncthreads();
-        const int nc = (int)sm.n_cand, na = (int)min(total_c, (uint32_t)kRankMax);
-        for (int c = tid; c < nc; c += THREADS) {
-            const uint32_t my_k = sm.cand_key[c], my_i = sm.cand_idx[c];
+        cluster_arrive();  // done reading the other CTAs' lists (waited for before returning)
+        // every member of the cluster's lists ranked (larger score, or equal score and lower index, is better):
+        // this CTA's winners marked, every CTA's winners counted (the same counts in every CTA)
+        const int na = (int)min(total_c, (uint32_t)kRankMax);
+        for (int c = tid; c < na; c += THREADS) {
+            const uint32_t my_k = sm.all_key[c], my_i = sm.all_idx[c];
             uint32_t better = 0;
             for (int j = 0; j < na; ++j) {
                 const uint32_t kj = sm.all_key[j];
                 better += (kj > my_k) || (kj == my_k && sm.all_idx[j] < my_i);
             }
-            const uint32_t li = my_i - (uint32_t)part0;
-            if (better < need && DSA_IDX_OK(li >> 5, THREADS * VPT / 32, status))
-                atomicOr(&sm.marks[li >> 5], 1u << (li & 31));
+            if (better < need) {
+                const int src = (int)(my_i / (uint32_t)(THREADS * VPT));  // the CTA whose part holds it
+                if (DSA_IDX_OK(src, C, status)) atomicAdd(&sm.sel_cnt[src], 1u);
+                const uint32_t li = my_i - (uint32_t)part0;
+                if (src == crank && DSA_IDX_OK(li >> 5, THREADS * VPT / 32, status))
+                    atomicOr(&sm.marks[li >> 5], 1u << (li & 31));
+            }
         }
         __syncthreads();
     }
@@ -340,21 +374,30 @@ __device__ __forceinline__ void topk_row_cluster(cg::cluster_group& cluster, Top
     }
     uint32_t ex_d, ex_t, tot_d, tot_t;
     SC::scan2((uint32_t)__popc(dmask), (uint32_t)__popc(tmask), &ex_d, &ex_t, &tot_d, &tot_t, sm.wt);
-    if (tid < C) {  // this CTA's counts into slot crank of CTA tid
-        uint32_t* dst = cluster.map_shared_rank(&sm.cl_tot[0][0], tid);
-        dst[2 * crank] = tot_d;
-        dst[2 * crank + 1] = tot_t;
-    }
-    cluster.sync();  // also: no CTA reads another's shared memory after this point
     uint32_t off_d = 0, off_t = 0, all_d = 0, all_t = 0;
+    if (rank_mode) {  // every CTA's selected count is already known here: above b* plus its winners in b*
 #pragma unroll
-    for (int c = 0; c < C; ++c) {
-        if (c < crank) {
-            off_d += sm.cl_tot[c][0];
-            off_t += sm.cl_tot[c][1];
+        for (int c = 0; c < C; ++c) {
+            const uint32_t sel = sm.pub[c][0] + sm.sel_cnt[c];
+            if (c < crank) off_d += sel;
+            all_d += sel;
         }
-        all_d += sm.cl_tot[c][0];
-        all_t += sm.cl_tot[c][1];
+    } else {
+        if (tid < C) {  // this CTA's counts into slot crank of CTA tid
+            uint32_t* dst = cluster.map_shared_rank(&sm.cl_tot[0][0], tid);
+            dst[2 * crank] = tot_d;
+            dst[2 * crank + 1] = tot_t;
+        }
+        cluster.sync();  // also: no CTA reads another's shared memory after this point
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            if (c < crank) {
+                off_d += sm.cl_tot[c][0];
+                off_t += sm.cl_tot[c][1];
+            }
+            all_d += sm.cl_tot[c][0];
+            all_t += sm.cl_tot[c][1];
+        }
     }
     uint32_t tie_rank = off_t + ex_t;
     uint32_t pos = off_d + ex_d + min(tie_rank, need_T);
@@ -374,6 +417,7 @@ __device__ __forceinline__ void topk_row_cluster(cg::cluster_group& cluster, Top
     const uint32_t total = all_d + min(all_t, need_T);
     for (int i = (int)total + crank * THREADS + tid; i < k; i += C * THREADS) emit(i, -1);
     if (crank == 0 && tid == 0 && total != (uint32_t)k) report(status, DSA_ERR_DEVICE_FAULT);
+    if (rank_mode) cluster_wait();  // no other CTA reads this CTA's lists after this point
 }
 
 }  // namespace dsa
