@@ -154,10 +154,12 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
 // gathered again as soon as its sub-tile's P V is done, so up to three gathers run ahead of the math):
 //   warps 4 + MW .. 15 gather (MW MMA warps below: 2 for bf16 rows, 4 for e4m3 rows): resolve keys a round
 //              (one sub-tile per gather warp) ahead (top-k index -> block table ->
-//              physical row, tables cached in shared memory), prefetch later rounds into L2, and copy
+//              physical row, tables cached in shared memory) and copy
 //              the rows into a stage with cp.async, 128B-swizzled, laid out [64-dim chunk][32 keys]
 //              [128 B]; e4m3 rows are converted to bf16 on the way, their scales kept beside the stage.
-//              Decode rows are gathered with an evict-first L2 policy (each serves one query row);
+//              Decode rows are gathered with an evict-first L2 policy (each serves one query row).
+//              No L2 prefetch of rows ahead of their copy: measured, it cost more (the prefetches queue
+//              in front of the copies that are needed first) than the early arrival saved;
 //   warps 4 .. 3 + MW issue the MMAs, one elected lane each (an MMA's issue costs the issuing warp about
 //              49 cycles at these shapes, so MW warps issue MW times as fast as one, up to the tensor pipe's
 //              own rate at M = 64); warp 4 also loads the query rows (TMA, one 64-dim box per lane):
@@ -213,7 +215,7 @@ struct ClSmem {
     static constexpr int kOffPool = kOffRow + kClRingMax * kClKeys * 4;  // uint8 [ring][32]: 1 main, 2 window
     static constexpr int kOffKsc = kOffPool + kClRingMax * kClKeys;    // float [stages][32]: e4m3 row scales
     static constexpr int kOffMask = kOffKsc + kClStages * kClKeys * 4;  // uint32 [stages]: valid keys of a stage
-    static constexpr int kOffAlpha = kOffMask + kClStages * 4;      // float [2][NH]
+    static constexpr int kOffAlpha = kOffMask + (kClStages * 4 + 15) / 16 * 16;  // float [2][NH]
     static constexpr int kOffVote = kOffAlpha + 2 * NH * 4;         // int [2][4]
     static constexpr int kOffOwn = kOffVote + 32;                   // float m[NH], l[NH], e[NH] of this CTA
     static constexpr int kOffStat = kOffOwn + 3 * NH * 4;           // float [4 ranks][NH][4]: (m, l, e, fault)
@@ -229,6 +231,11 @@ struct ClSmem {
     static constexpr int kAlloc = kBytes + 1024;                    // + alignment slack
     static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
     static_assert(kOffKsc % 16 == 0, "the row scales are read as float4");
+    // every region starts on a 16-byte boundary (float4 reads, 8-byte mbarriers), whatever the stage count
+    static_assert(kOffAlpha % 16 == 0 && kOffVote % 16 == 0 && kOffOwn % 16 == 0 && kOffStat % 16 == 0 &&
+                      kOffFac % 16 == 0 && kOffBt % 16 == 0 && kOffSwb % 16 == 0 && kOffFault % 16 == 0 &&
+                      kOffRope % 16 == 0 && kOffBar % 16 == 0 && kOffTopk % 16 == 0,
+                  "shared-memory regions 16-byte aligned");
     static constexpr int kTile = 128 * NH * 2;                      // one exchanged 128-dim O tile: [NH / 4][128] x 4 bf16
     static_assert(3 * kTile <= kQ, "the sent tiles fit in the query rows");
     static_assert(6 * kTile <= kQ + kClStages * kClStage, "the received tiles fit after them");
@@ -393,7 +400,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     bool ok = true;
 
     if (warp >= Ro::kFirstGather) {
-        // ---- gather warps: resolve keys a round ahead, prefetch rows into L2, copy with cp.async -----
+        // ---- gather warps: resolve keys a round ahead, copy with cp.async ----------------------------
         // decode rows (one query row per request): a gathered row serves this query row only and leaves L2 first;
         // prefill rows of one request share their keys, which keep the default policy
         const uint64_t row_policy = a.q_req ? l2_evict_normal() : l2_evict_first();
@@ -407,7 +414,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             if (j < n_keys && j < n_comp) *id = FUSED ? s_topk[j] : (a.topk ? __ldg(a.topk + (long long)row * a.k + j) : j);
             return j;
         };
-        // Step 2: index -> physical row through the cached tables (or global memory), L2 prefetch, ring slot.
+        // Step 2: index -> physical row through the cached tables (or global memory), ring slot.
         auto finish_key = [&](int R, int j, int id) {
             const int i = R * Ro::kRound + gt / kClKeys;
             if (j < 0) return;
@@ -443,12 +450,6 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 } else {
                     v = pb * kBlockPositions + (pos - lb * kBlockPositions);
                 }
-            }
-            if (v >= 0 && R > 0) {  // rows of later rounds start moving into L2 (the first round is gathered at once)
-                constexpr int kRowBytes = FP8 ? kD : 2 * kD;
-                const uint8_t* base = pool == 2 ? static_cast<const uint8_t*>(a.swa.data)
-                                                : static_cast<const uint8_t*>(a.main.data);
-                prefetch_l2(base + (long long)v * kRowBytes, kRowBytes);
             }
             s_row[(i % Ro::kRing) * kClKeys + gt % kClKeys] = v;
             s_pool[(i % Ro::kRing) * kClKeys + gt % kClKeys] = (uint8_t)pool;
@@ -541,7 +542,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             if (ok && FP8) {
                 // e4m3 rows: copied as they are into the upper half of the stage (row kk at 16 KB + 512 kk, lane
                 // l the codes of dims 16 l .. 16 l + 15), the row scale beside the stage; they become bf16 in
-                // place once they have landed (widen_fp8 below), so copies of three sub-tiles stay in flight
+                // place once they have landed (widen_fp8 below), so copies of two sub-tiles stay in flight
                 constexpr int kRowsPerWarp = (kClKeys + Ro::kGatherWarps - 1) / Ro::kGatherWarps;
                 const uint32_t raw = sK + s * kClStage + kClStage / 2;
 #pragma unroll
@@ -561,27 +562,14 @@ __global__ void __launch_bounds__(kClThreads, 1)
             cp_async_commit();
             if (gt == 0) DSA_TRACE(i, 0);
             if (i == 0 && gt == 0) DSA_STAMP(3);
-            if (i == 0) {  // the first round's later sub-tiles start moving into L2 once sub-tile 0 is under way
-                constexpr int kRowBytes = FP8 ? kD : 2 * kD;
-                for (int t = kClKeys + gt; t < Ro::kRound * kClKeys; t += Ro::kGatherThreads) {
-                    const int ii = t / kClKeys;
-                    if (ii >= n_mine) break;
-                    const int rr = s_row[(ii % Ro::kRing) * kClKeys + (t % kClKeys)];
-                    if (rr >= 0) {
-                        const uint8_t* base = s_pool[(ii % Ro::kRing) * kClKeys + (t % kClKeys)] == 2
-                                                  ? static_cast<const uint8_t*>(a.swa.data)
-                                                  : static_cast<const uint8_t*>(a.main.data);
-                        prefetch_l2(base + (long long)rr * kRowBytes, kRowBytes);
-                    }
-                }
-            }
-            // the next round of keys once this one's second sub-tile is under way: its rows reach L2 while
-            // the sub-tiles in between are processed (ring slots of sub-tiles < i are free by now)
+            // the next round of keys once this one's second sub-tile is under way, so its rows are known
+            // before they are copied (ring slots of sub-tiles < i are free by now)
             if (i % Ro::kRound == 2) resolve_round(i / Ro::kRound + 1);
-            // a thread keeps up to three sub-tiles of copies in flight: with three outstanding, the oldest is
-            // reported once its group has landed
-            if (i - sig >= 2) {
-                cp_async_wait_group<2>();
+            // a thread keeps up to two sub-tiles of copies in flight: with two outstanding, the older is
+            // reported once its group has landed (a third in flight was measured slower: the copies of
+            // the sub-tile the MMAs wait for share the memory pipe with those of one more)
+            if (i - sig >= 1) {
+                cp_async_wait_group<1>();
                 if constexpr (FP8) widen_fp8(sig % kClStages);
                 fence_proxy_async_smem();
                 mbar_arrive(&full[sig % kClStages]);
