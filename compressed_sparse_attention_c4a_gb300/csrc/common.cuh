@@ -601,15 +601,6 @@ __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
-// prefetch_l2 with an L2 cache policy.
-__device__ __forceinline__ void prefetch_l2_hint(const void* p, uint32_t bytes, uint64_t policy) {
-    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p), "r"(bytes), "l"(policy)
-                 : "memory");
-}
-// The 128-byte line holding p into L2 (no alignment or size rule).
-__device__ __forceinline__ void prefetch_line_l2(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
-}
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
     asm volatile(
