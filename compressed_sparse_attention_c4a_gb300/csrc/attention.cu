@@ -327,6 +327,20 @@ __global__ void __launch_bounds__(kClThreads, 1)
     // step writes, read while the preceding kernel (the top-k) finishes.  Top-k indices, cache rows and
     // every output come after the programmatic-dependent-launch wait.
     const int r = a.q_req ? a.q_req[row] : row;
+    // the gather threads' share of the request's main block table (when it has at most kBtCache blocks): its
+    // loads, which need only the request, are in flight with the position's and are stored in shared memory
+    // later (after the wait, unless the kernel selects its own top-k first)
+    const bool bt_cached = a.main_bt.max_blocks <= kBtCache;
+    constexpr int kBtPer = (kBtCache + Ro::kGatherThreads - 1) / Ro::kGatherThreads;
+    int btv[kBtPer];
+    if (warp >= Ro::kFirstGather) {
+        const bool r_in = bt_cached && r >= 0 && r < a.main_bt.batch;
+#pragma unroll
+        for (int u = 0; u < kBtPer; ++u) {
+            const int b = tid - 32 * Ro::kFirstGather + u * Ro::kGatherThreads;
+            btv[u] = r_in && b < a.main_bt.max_blocks ? __ldg(a.main_bt.table + (long long)r * a.main_bt.max_blocks + b) : -1;
+        }
+    }
     const int m = a.q_pos[row];
     const bool row_ok = r >= 0 && r < a.main_bt.batch && r < a.swa_bt.batch && m >= 0;
     if (!row_ok && tid == 0) *s_fault = 1;
@@ -338,7 +352,6 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const int n_sub = (n_keys + kClKeys - 1) / kClKeys;
     const int g_lo = split * a.cps, g_hi = min(n_sub, g_lo + a.cps);
     const int n_mine = g_hi > g_lo + crank ? (g_hi - g_lo - crank + csize - 1) / csize : 0;
-    const bool bt_cached = a.main_bt.max_blocks <= kBtCache;
     int* s_bt = reinterpret_cast<int*>(smem + L::kOffBt);
     int* s_swb = reinterpret_cast<int*>(smem + L::kOffSwb);
     if (warp == 0 && lane < a.rope.rope_dim / 2) {  // R_m^-1 of the output: cos and sin of each pair's angle at m
@@ -355,19 +368,28 @@ __global__ void __launch_bounds__(kClThreads, 1)
         if (lane == 0) mbar_arrive(qfull);
     }
     const int gt = tid - 32 * Ro::kFirstGather, gw = warp - Ro::kFirstGather;
-    if (warp >= Ro::kFirstGather && n_mine > 0) {
-        // the request's main block table (when it has at most kBtCache blocks) and the window pool's blocks
-        // of positions wlo .. m; a key then resolves with one global load (its top-k index) at most
+    // the cached tables: the main block table (above) and the window pool's blocks of positions wlo .. m; a
+    // key then resolves with one global load (its top-k index) at most.  Published by the caller's barrier.
+    int swbv = -1;
+    if (warp >= Ro::kFirstGather && gt < 8 && n_mine > 0) {
+        const int lb = wlo / kBlockPositions + gt;
+        if (row_ok && lb <= m / kBlockPositions && lb < a.swa_bt.max_blocks)
+            swbv = __ldg(a.swa_bt.table + (long long)r * a.swa_bt.max_blocks + lb);
+    }
+    auto store_tables = [&]() {
         if (bt_cached)
-            for (int b = gt; b < a.main_bt.max_blocks; b += Ro::kGatherThreads)
-                s_bt[b] = __ldg(a.main_bt.table + (long long)r * a.main_bt.max_blocks + b);
-        if (gt < 8) {
-            const int lb = wlo / kBlockPositions + gt;
-            s_swb[gt] = (row_ok && lb <= m / kBlockPositions && lb < a.swa_bt.max_blocks)
-                            ? __ldg(a.swa_bt.table + (long long)r * a.swa_bt.max_blocks + lb)
-                            : -1;
+#pragma unroll
+            for (int u = 0; u < kBtPer; ++u) {
+                const int b = gt + u * Ro::kGatherThreads;
+                if (b < a.main_bt.max_blocks) s_bt[b] = btv[u];
+            }
+        if (gt < 8) s_swb[gt] = swbv;
+    };
+    if constexpr (FUSED) {
+        if (warp >= Ro::kFirstGather && n_mine > 0) {
+            store_tables();
+            named_bar_sync(1, Ro::kGatherThreads);  // cached tables visible to every gather thread
         }
-        named_bar_sync(1, Ro::kGatherThreads);  // cached tables visible to every gather thread
     }
     pdl_wait();  // global memory the preceding kernel writes, and every output, only below
     pdl_launch_dependents();
@@ -500,7 +522,17 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 }
             }
         };
-        if (n_mine > 0) resolve_round(0);
+        if constexpr (FUSED) {
+            if (n_mine > 0) resolve_round(0);
+        } else if (n_mine > 0) {
+            // the first round's top-k indices requested before the cached tables are stored, so that both
+            // loads' latencies overlap (a CTA that starts after the top-k has ended waits for neither alone)
+            int id0 = -1;
+            const int j0 = key_id(0, &id0);
+            store_tables();
+            named_bar_sync(1, Ro::kGatherThreads);  // cached tables visible to every gather thread
+            finish_key(0, j0, id0);
+        }
         int sig = 0;  // first sub-tile whose stage this thread has not yet reported full
         for (int i = 0; i < n_mine; ++i) {
             const int s = i % kClStages;
