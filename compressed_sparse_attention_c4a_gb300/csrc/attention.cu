@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const uint32_t tmem = *s_tmem;
     const uint32_t tS = tmem, tO = tmem + 2 * Ro::kMma * kClKeys;  // S: [2 buffers][MW parts][32]; O^T: [4][NH]
     if (tid == 0) DSA_STAMP(1);
-    cluster_arrive_relaxed();  // phase 0: this CTA has started (waited on before distributed shared memory use)
+    if (csize > 1) cluster_arrive_relaxed();  // phase 0: this CTA has started (waited on before DSMEM use)
 
     // The row's position, request and block tables, and the query rows: inputs that no kernel of the layer
     // step writes, read while the preceding kernel (the top-k) finishes.  Top-k indices, cache rows and
@@ -876,7 +876,8 @@ __global__ void __launch_bounds__(kClThreads, 1)
     }
     if (tid == 0) DSA_STAMP(9);
     // 2. (m, l, e, fault) per head to every CTA of the cluster
-    if constexpr (!FUSED) cluster_wait();  // phase 0: every CTA of the cluster has started (fused: waited above)
+    if constexpr (!FUSED)
+        if (csize > 1) cluster_wait();  // phase 0: every CTA of the cluster has started (fused: waited above)
     if (tid == 0) DSA_STAMP(17);
     if (csize > 1 && tid == 0)  // before any peer can push (pushes follow phase 1)
         for (int b = 0; b < (csize - 1) * tiles_per; ++b) mbar_arrive_expect_tx(&xfull[b], (uint32_t)L::kTile);
@@ -885,12 +886,19 @@ __global__ void __launch_bounds__(kClThreads, 1)
         const uint32_t dst = smem_u32(s_stat + (crank * NH + h) * 4);
         const float mo = have ? s_own[h] : -INFINITY, lo = have ? s_own[NH + h] : 0.f,
                     eo = have ? s_own[2 * NH + h] : 0.f;
-        for (int q = 0; q < csize; ++q)
-            st_cluster_v4(mapa_shared(dst, (uint32_t)q), mo, lo, eo, fo);
+        if (csize == 1)
+            *reinterpret_cast<float4*>(s_stat + h * 4) = make_float4(mo, lo, eo, fo);
+        else
+            for (int q = 0; q < csize; ++q)
+                st_cluster_v4(mapa_shared(dst, (uint32_t)q), mo, lo, eo, fo);
     }
     if (tid == 0) DSA_STAMP(18);
-    cluster_arrive();  // phase 1: statistics delivered, sent tiles staged, every CTA's products complete
-    cluster_wait();
+    if (csize > 1) {
+        cluster_arrive();  // phase 1: statistics delivered, sent tiles staged, every CTA's products complete
+        cluster_wait();
+    } else {
+        __syncthreads();  // one CTA: the statistics in its own shared memory, its products complete
+    }
     if (tid == 0) DSA_STAMP(10);
     // 3. push: one bulk copy per sent tile, all from lane 0 of the last warp (the first warps compute the
     // factors meanwhile), the next CTA's tiles first, then the one after: every owner receives one CTA's tiles at
@@ -975,6 +983,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     uint8_t* const ob1 = smem + L::kOffK + 2 * kClStage;
     const int firstd = kD - a.rope.rope_dim;
     const bool odd = lane & 1;
+    float v_next[G];  // the next owned tile's columns, loaded from TMEM while this one is finished and stored
 #pragma unroll 1
     for (int j = 0; j < tiles_per; ++j) {
         const int t = crank + csize * j;
@@ -985,8 +994,12 @@ __global__ void __launch_bounds__(kClThreads, 1)
 #pragma unroll
                 for (int e = 0; e < G; ++e) v[e] = v_first[e];
             } else {
-                tmem_cols(t, v);
+                tmem_wait_ld();
+                tmem_regs_after_wait<G>(v_next);
+#pragma unroll
+                for (int e = 0; e < G; ++e) v[e] = v_next[e];
             }
+            if (j + 1 < tiles_per) tmem_cols_nowait(t + csize, v_next);
         }
         if (tid == 0 && j == 0) DSA_STAMP(20);
 #pragma unroll
