@@ -79,8 +79,9 @@ class LayerStep:
         self.side = None
         # fused_select: decode rows take the top-k and the attention in one call (one kernel when one cluster of
         # four CTAs per row holds all 64 heads, rows of at most 16,384 scores and k <= 512); off by default: on
-        # the decode batch it measured level with the two launches (44.6 against 44.4 us a step), its top-k
-        # phase running about 3 us slower inside the attention kernel than the top-k kernel alone
+        # the decode batch it measures level with the two launches (41.75 against 41.86 us a step; 38.1 against
+        # 38.8 us with e2m1 indexer keys), its top-k phase running slower inside the attention kernel than the
+        # top-k kernel alone
         self.fused_select = fused_select and self.has_index and spec.queries == "last" and not self.fused_topk
         self.select_attend_kernels = 2
         if self.fused_select:
