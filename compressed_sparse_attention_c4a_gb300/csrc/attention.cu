@@ -213,8 +213,8 @@ struct ClSmem {
     static constexpr int kOffP = kOffK + kClStages * kClStage;      // two P^T buffers; output staging at the end
     static constexpr int kOffRow = kOffP + 2 * kP;                  // int [ring][32]: physical rows (-1 masked)
     static constexpr int kOffPool = kOffRow + kClRingMax * kClKeys * 4;  // uint8 [ring][32]: 1 main, 2 window
-    static constexpr int kOffKsc = kOffPool + kClRingMax * kClKeys;    // float [stages][32]: e4m3 row scales
-    static constexpr int kOffMask = kOffKsc + kClStages * kClKeys * 4;  // uint32 [stages]: valid keys of a stage
+    static constexpr int kOffKsc = kOffPool + kClRingMax * kClKeys;    // float [stages + 2][32]: e4m3 row scales
+    static constexpr int kOffMask = kOffKsc + (kClStages + 2) * kClKeys * 4;  // uint32 [stages]: valid keys of a stage
     static constexpr int kOffAlpha = kOffMask + (kClStages * 4 + 15) / 16 * 16;  // float [2][NH]
     static constexpr int kOffVote = kOffAlpha + 2 * NH * 4;         // int [2][4]
     static constexpr int kOffOwn = kOffVote + 32;                   // float m[NH], l[NH], e[NH] of this CTA
@@ -259,6 +259,9 @@ __global__ void __launch_bounds__(kClThreads, 1)
     attn_cl_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap, AttnArgs a) {
     using L = ClSmem<NH>;
     using Ro = ClRoles<FP8 ? 4 : 2>;
+    // bf16 key stages: four for bf16 rows; three for e4m3 rows, whose codes land in a ring of two raw slots
+    // (16 KB each, the fourth stage's space) and are widened into a stage once its previous product is done
+    constexpr int NS = FP8 ? kClStages - 1 : kClStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sQ = smem_u32(smem + L::kOffQ), sK = smem_u32(smem + L::kOffK), sP = smem_u32(smem + L::kOffP);
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     float* s_M = s_inv + NH;
     float* s_L = s_M + NH;
     float* s_E = s_L + NH;
-    // sub-tile i: key stage i % kClStages; S columns, P^T buffer and softmax scratch i & 1
+    // sub-tile i: key stage i % NS; S columns, P^T buffer and softmax scratch i & 1
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // [stages] stage gathered (gather threads)
     uint64_t* sfull = full + kClStages;                                 // [2] S in TMEM (both MMA warps' commits)
     uint64_t* pfull = sfull + 2;                                        // [2] P^T written (4 warps)
@@ -481,26 +484,28 @@ __global__ void __launch_bounds__(kClThreads, 1)
             const int j = key_id(R, &id);
             finish_key(R, j, id);
         };
-        // e4m3 codes of a landed sub-tile -> bf16 in the same stage, exactly (e4m3 -> fp16 -> fp32 -> bf16 loses
-        // nothing); every gather thread reads its rows' codes before any writes, since the bf16 rows overwrite
-        // the codes' half of the stage.  Called by all gather threads alike.
-        auto widen_fp8 = [&](int st) {
+        // e4m3 rows of sub-tile j (landed in raw slot j & 1) -> bf16 in key stage j % NS, exactly (e4m3 -> fp16 ->
+        // fp32 -> bf16 loses nothing), with the rows' scales and the stage's key mask, once the stage's previous
+        // product (sub-tile j - NS) is done; then the stage is reported full.  Called by all gather threads
+        // alike, after each has waited for its own copies of sub-tile j.
+        auto widen_fp8 = [&](int j) {
             constexpr int kRowsPerWarp = (kClKeys + Ro::kGatherWarps - 1) / Ro::kGatherWarps;
+            const int st = j % NS;
             const uint32_t stage = sK + st * kClStage;
-            const uint8_t* raw = smem + L::kOffK + st * kClStage + kClStage / 2;
+            const uint8_t* raw = smem + L::kOffK + NS * kClStage + (j & 1) * (kClStage / 2);
             named_bar_sync(1, Ro::kGatherThreads);  // every thread's copies of the sub-tile have landed
-            uint4 code[kRowsPerWarp];
-#pragma unroll
-            for (int u = 0; u < kRowsPerWarp; ++u) {
-                const int kk = gw + u * Ro::kGatherWarps;
-                code[u] = kk < kClKeys ? *reinterpret_cast<const uint4*>(raw + kk * kD + lane * 16) : make_uint4(0, 0, 0, 0);
+            if (j >= NS) ok = ok && mbar_wait_bounded(&pvdone[st], ((j - NS) / NS) & 1, kWaitLimitNs);
+            if (gt < kClKeys) {  // the first gather warp (whole): the stage's row scales and key mask
+                if (ok) s_ksc[st * kClKeys + gt] = s_ksc[(kClStages + (j & 1)) * kClKeys + gt];
+                const uint32_t bits = __ballot_sync(0xffffffffu, s_row[(j % Ro::kRing) * kClKeys + gt] >= 0);
+                if (ok && lane == 0) s_mask[st] = bits;
             }
-            named_bar_sync(1, Ro::kGatherThreads);  // all codes read: the bf16 rows may overwrite them
 #pragma unroll
             for (int u = 0; u < kRowsPerWarp; ++u) {
                 const int kk = gw + u * Ro::kGatherWarps;
-                if (kk < kClKeys) {
-                    const uint32_t w4[4] = {code[u].x, code[u].y, code[u].z, code[u].w};
+                if (ok && kk < kClKeys) {
+                    const uint4 code = *reinterpret_cast<const uint4*>(raw + kk * kD + lane * 16);
+                    const uint32_t w4[4] = {code.x, code.y, code.z, code.w};
                     uint32_t bf[8];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -521,6 +526,9 @@ __global__ void __launch_bounds__(kClThreads, 1)
                                  : "memory");
                 }
             }
+            fence_proxy_async_smem();  // the bf16 rows -> visible to the tensor core (async proxy)
+            mbar_arrive(&full[st]);
+            if (gt == 0) DSA_TRACE(j, 1);
         };
         if constexpr (FUSED) {
             if (n_mine > 0) resolve_round(0);
@@ -534,88 +542,110 @@ __global__ void __launch_bounds__(kClThreads, 1)
             finish_key(0, j0, id0);
         }
         int sig = 0;  // first sub-tile whose stage this thread has not yet reported full
-        for (int i = 0; i < n_mine; ++i) {
-            const int s = i % kClStages;
-            if (i >= kClStages) {
-                // before waiting for a stage, report every sub-tile issued so far (never hold landed rows back)
-                if (sig < i) {
-                    cp_async_wait_all();
-                    for (; sig < i; ++sig) {
-                        if constexpr (FP8) widen_fp8(sig % kClStages);
-                        fence_proxy_async_smem();  // cp.async writes -> visible to the tensor core (async proxy)
-                        mbar_arrive(&full[sig % kClStages]);
-                        if (gt == 0) DSA_TRACE(sig, 1);
+        if constexpr (!FP8) {
+            for (int i = 0; i < n_mine; ++i) {
+                const int s = i % NS;
+                if (i >= NS) {
+                    // before waiting for a stage, report every sub-tile issued so far (never hold landed rows back)
+                    if (sig < i) {
+                        cp_async_wait_all();
+                        for (; sig < i; ++sig) {
+                            fence_proxy_async_smem();  // cp.async writes -> visible to the tensor core (async proxy)
+                            mbar_arrive(&full[sig % NS]);
+                            if (gt == 0) DSA_TRACE(sig, 1);
+                        }
                     }
+                    // the stage's previous sub-tile has been multiplied into O^T
+                    ok = ok && mbar_wait_bounded(&pvdone[s], ((i - NS) / NS) & 1, kWaitLimitNs);
                 }
-                // the stage's previous sub-tile has been multiplied into O^T
-                ok = ok && mbar_wait_bounded(&pvdone[s], ((i - kClStages) / kClStages) & 1, kWaitLimitNs);
-            }
-            named_bar_sync(1, Ro::kGatherThreads);  // sub-tile i's rows are visible; earlier gathers are done
-            const int* rows = s_row + (i % Ro::kRing) * kClKeys;
-            const uint8_t* pools = s_pool + (i % Ro::kRing) * kClKeys;
-            if (gt < kClKeys) {  // the first gather warp: the stage's key mask for the softmax
-                const uint32_t bits = __ballot_sync(0xffffffffu, rows[gt] >= 0);
-                if (lane == 0) s_mask[s] = bits;
-            }
-            if (ok && !FP8) {
-                const uint32_t stage = sK + s * kClStage;
+                named_bar_sync(1, Ro::kGatherThreads);  // sub-tile i's rows are visible; earlier gathers are done
+                const int* rows = s_row + (i % Ro::kRing) * kClKeys;
+                const uint8_t* pools = s_pool + (i % Ro::kRing) * kClKeys;
+                if (gt < kClKeys) {  // the first gather warp: the stage's key mask for the softmax
+                    const uint32_t bits = __ballot_sync(0xffffffffu, rows[gt] >= 0);
+                    if (lane == 0) s_mask[s] = bits;
+                }
+                if (ok) {
+                    const uint32_t stage = sK + s * kClStage;
 #pragma unroll 1
-                for (int kk = gw; kk < kClKeys; kk += Ro::kGatherWarps) {
-                    const int rr = rows[kk];
-                    const uint8_t* base = pools[kk] == 2 ? static_cast<const uint8_t*>(a.swa.data)
-                                                         : static_cast<const uint8_t*>(a.main.data);
-                    const uint8_t* src = rr >= 0 ? base + (long long)rr * (2 * kD) : base;
-#pragma unroll
-                    for (int piece = lane; piece < kD / 8; piece += 32)
-                        cp_async16_hint(stage + sw128_offset(kk, piece * 8, kClKeys * 128), src + piece * 16,
-                                        rr >= 0 ? 16u : 0u, row_policy);
-                }
-            }
-            if (ok && FP8) {
-                // e4m3 rows: copied as they are into the upper half of the stage (row kk at 16 KB + 512 kk, lane
-                // l the codes of dims 16 l .. 16 l + 15), the row scale beside the stage; they become bf16 in
-                // place once they have landed (widen_fp8 below), so copies of two sub-tiles stay in flight
-                constexpr int kRowsPerWarp = (kClKeys + Ro::kGatherWarps - 1) / Ro::kGatherWarps;
-                const uint32_t raw = sK + s * kClStage + kClStage / 2;
-#pragma unroll
-                for (int u = 0; u < kRowsPerWarp; ++u) {
-                    const int kk = gw + u * Ro::kGatherWarps;
-                    if (kk < kClKeys) {
+                    for (int kk = gw; kk < kClKeys; kk += Ro::kGatherWarps) {
                         const int rr = rows[kk];
-                        const dsa_pool_t& pl = pools[kk] == 2 ? a.swa : a.main;
-                        const uint8_t* src = static_cast<const uint8_t*>(pl.data) + (rr >= 0 ? (long long)rr * kD : 0);
-                        cp_async16_hint(raw + kk * kD + lane * 16, src + lane * 16, rr >= 0 ? 16u : 0u, row_policy);
-                        if (lane == 0)
-                            cp_async4(smem_u32(s_ksc + s * kClKeys + kk), rr >= 0 ? pl.scale + rr : pl.scale,
-                                      rr >= 0 ? 4u : 0u);
+                        const uint8_t* base = pools[kk] == 2 ? static_cast<const uint8_t*>(a.swa.data)
+                                                             : static_cast<const uint8_t*>(a.main.data);
+                        const uint8_t* src = rr >= 0 ? base + (long long)rr * (2 * kD) : base;
+#pragma unroll
+                        for (int piece = lane; piece < kD / 8; piece += 32)
+                            cp_async16_hint(stage + sw128_offset(kk, piece * 8, kClKeys * 128), src + piece * 16,
+                                            rr >= 0 ? 16u : 0u, row_policy);
                     }
                 }
+                cp_async_commit();
+                if (gt == 0) DSA_TRACE(i, 0);
+                if (i == 0 && gt == 0) DSA_STAMP(3);
+                // the next round of keys once this one's second sub-tile is under way, so its rows are known
+                // before they are copied (ring slots of sub-tiles < i are free by now)
+                if (i % Ro::kRound == 2) resolve_round(i / Ro::kRound + 1);
+                // a thread keeps up to two sub-tiles of copies in flight: with two outstanding, the older is
+                // reported once its group has landed (a third in flight was measured slower: the copies of
+                // the sub-tile the MMAs wait for share the memory pipe with those of one more)
+                if (i - sig >= 1) {
+                    cp_async_wait_group<1>();
+                    fence_proxy_async_smem();
+                    mbar_arrive(&full[sig % NS]);
+                    if (gt == 0) DSA_TRACE(sig, 1);
+                    ++sig;
+                }
             }
-            cp_async_commit();
-            if (gt == 0) DSA_TRACE(i, 0);
-            if (i == 0 && gt == 0) DSA_STAMP(3);
-            // the next round of keys once this one's second sub-tile is under way, so its rows are known
-            // before they are copied (ring slots of sub-tiles < i are free by now)
-            if (i % Ro::kRound == 2) resolve_round(i / Ro::kRound + 1);
-            // a thread keeps up to two sub-tiles of copies in flight: with two outstanding, the older is
-            // reported once its group has landed (a third in flight was measured slower: the copies of
-            // the sub-tile the MMAs wait for share the memory pipe with those of one more)
-            if (i - sig >= 1) {
-                cp_async_wait_group<1>();
-                if constexpr (FP8) widen_fp8(sig % kClStages);
-                fence_proxy_async_smem();
-                mbar_arrive(&full[sig % kClStages]);
-                if (gt == 0) DSA_TRACE(sig, 1);
-                ++sig;
+            if (sig < n_mine) {  // the sub-tiles not yet reported
+                cp_async_wait_all();
+                for (; sig < n_mine; ++sig) {
+                    fence_proxy_async_smem();
+                    mbar_arrive(&full[sig % NS]);
+                    if (gt == 0) DSA_TRACE(sig, 1);
+                }
             }
-        }
-        if (sig < n_mine) {  // the sub-tiles not yet reported
-            cp_async_wait_all();
-            for (; sig < n_mine; ++sig) {
-                if constexpr (FP8) widen_fp8(sig % kClStages);
-                fence_proxy_async_smem();
-                mbar_arrive(&full[sig % kClStages]);
-                if (gt == 0) DSA_TRACE(sig, 1);
+        } else {
+            // e4m3 rows: sub-tile i's codes are copied as they are into raw slot i & 1 (row kk at 512 kk, lane
+            // l the codes of dims 16 l .. 16 l + 15; the row scales into the slot's scale row) as soon as the
+            // slot's previous sub-tile has been widened, without waiting for a key stage; each landed sub-tile
+            // is then widened into its stage (widen_fp8), so two sub-tiles of copies stay in flight
+            constexpr int kRowsPerWarp = (kClKeys + Ro::kGatherWarps - 1) / Ro::kGatherWarps;
+            for (int i = 0; i < n_mine; ++i) {
+                if (i - sig >= 2) {  // raw slot i & 1 still holds sub-tile i - 2: widen it first
+                    cp_async_wait_group<1>();
+                    widen_fp8(sig++);
+                }
+                named_bar_sync(1, Ro::kGatherThreads);  // sub-tile i's rows are visible; raw slot i & 1 is free
+                const int* rows = s_row + (i % Ro::kRing) * kClKeys;
+                const uint8_t* pools = s_pool + (i % Ro::kRing) * kClKeys;
+                if (ok) {
+                    const uint32_t raw = sK + NS * kClStage + (i & 1) * (kClStage / 2);
+                    float* ksc = s_ksc + (kClStages + (i & 1)) * kClKeys;
+#pragma unroll
+                    for (int u = 0; u < kRowsPerWarp; ++u) {
+                        const int kk = gw + u * Ro::kGatherWarps;
+                        if (kk < kClKeys) {
+                            const int rr = rows[kk];
+                            const dsa_pool_t& pl = pools[kk] == 2 ? a.swa : a.main;
+                            const uint8_t* src = static_cast<const uint8_t*>(pl.data) + (rr >= 0 ? (long long)rr * kD : 0);
+                            cp_async16_hint(raw + kk * kD + lane * 16, src + lane * 16, rr >= 0 ? 16u : 0u, row_policy);
+                            if (lane == 0)
+                                cp_async4(smem_u32(ksc + kk), rr >= 0 ? pl.scale + rr : pl.scale, rr >= 0 ? 4u : 0u);
+                        }
+                    }
+                }
+                cp_async_commit();
+                if (gt == 0) DSA_TRACE(i, 0);
+                if (i == 0 && gt == 0) DSA_STAMP(3);
+                if (i % Ro::kRound == 2) resolve_round(i / Ro::kRound + 1);
+                if (i - sig >= 1) {  // the older of the two sub-tiles in flight, once landed
+                    cp_async_wait_group<1>();
+                    widen_fp8(sig++);
+                }
+            }
+            if (sig < n_mine) {
+                cp_async_wait_all();
+                for (; sig < n_mine; ++sig) widen_fp8(sig);
             }
         }
         if (!ok) report(a.status, DSA_ERR_TIMEOUT);
@@ -628,7 +658,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         const uint64_t dq = sw128_desc(sQ, 16, 1024);
         if (n_mine > 0) ok = mbar_wait_bounded(qfull, 0, kWaitLimitNs);
         auto issue_s = [&](int i) {  // this warp's 512 / MW dims into its own accumulator
-            const int s = i % kClStages;
+            const int s = i % NS;
             tc_fence_after();
             const uint64_t dk = sw128_desc(sK + s * kClStage, 16, 1024);
 #pragma unroll
@@ -641,7 +671,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             mma_commit_elect(&sfull[i & 1]);
         };
         auto issue_pv = [&](int i) {  // this warp's 128-dim tiles
-            const int s = i % kClStages;
+            const int s = i % NS;
             tc_fence_after();
             const uint64_t dv = sw128_desc(sK + s * kClStage, kClKeys * 128, 1024);
             const uint64_t dp = sw128_desc(sP + (i & 1) * L::kP, 16, 1024);
@@ -663,7 +693,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             bool pv_done = false;
             while (ok && !pv_done) {
                 if (next_s < n_mine && next_s <= i + 1 &&
-                    __all_sync(0xffffffffu, mbar_try_wait(&full[next_s % kClStages], (next_s / kClStages) & 1))) {
+                    __all_sync(0xffffffffu, mbar_try_wait(&full[next_s % NS], (next_s / NS) & 1))) {
                     issue_s(next_s);
                     if (tid == 128) DSA_TRACE(next_s, 2);
                     if (next_s == 0 && tid == 128) DSA_STAMP(4);
@@ -691,11 +721,11 @@ __global__ void __launch_bounds__(kClThreads, 1)
         // exact); e: sum of the fp32 probabilities (the log-sum-exp)
         float m_run = -INFINITY, l_run = 0.f, e_run = 0.f;
         for (int i = 0; i < n_mine; ++i) {
-            const int st = i % kClStages, s = i & 1;  // key stage; S columns, P^T buffer and scratch
-            ok = ok && mbar_wait_bounded(&full[st], (i / kClStages) & 1, kWaitLimitNs);  // the stage's key mask
+            const int st = i % NS, s = i & 1;  // key stage; S columns, P^T buffer and scratch
+            ok = ok && mbar_wait_bounded(&full[st], (i / NS) & 1, kWaitLimitNs);  // the stage's key mask
             ok = ok && mbar_wait_bounded(&sfull[s], (i >> 1) & 1, kWaitLimitNs);
             if (i >= 2)  // P^T buffer free: the product of sub-tile i - 2 is done
-                ok = ok && mbar_wait_bounded(&pvdone[(i - 2) % kClStages], ((i - 2) / kClStages) & 1, kWaitLimitNs);
+                ok = ok && mbar_wait_bounded(&pvdone[(i - 2) % NS], ((i - 2) / NS) & 1, kWaitLimitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (tid == 0) DSA_TRACE(i, 3);
             float sv[kClKeys];
@@ -788,7 +818,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             named_bar_sync(2, 128);
             if (s_vote[s * 4] | s_vote[s * 4 + 1] | s_vote[s * 4 + 2] | s_vote[s * 4 + 3]) {
                 // a head's maximum moved: O^T (after the previous sub-tile's product) times alpha per head
-                ok = ok && mbar_wait_bounded(&pvdone[(i - 1) % kClStages], ((i - 1) / kClStages) & 1, kWaitLimitNs);
+                ok = ok && mbar_wait_bounded(&pvdone[(i - 1) % NS], ((i - 1) / NS) & 1, kWaitLimitNs);
                 ok = __all_sync(0xffffffffu, ok);
                 if (ok) {
                     tc_fence_after();
@@ -814,7 +844,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             if (i == 0 && tid == 0) DSA_STAMP(5);
         }
         if (n_mine > 0) {  // the last product must be complete before O^T is read
-            ok = ok && mbar_wait_bounded(&pvdone[(n_mine - 1) % kClStages], ((n_mine - 1) / kClStages) & 1, kWaitLimitNs);
+            ok = ok && mbar_wait_bounded(&pvdone[(n_mine - 1) % NS], ((n_mine - 1) / NS) & 1, kWaitLimitNs);
             tc_fence_after();
         }
         if (tid == 0) DSA_STAMP(7);
